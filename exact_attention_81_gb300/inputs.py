@@ -1,0 +1,110 @@
+"""Seeded synthetic inputs for the attention forward path.
+
+This module holds the workload shapes and the random-number recipes only: no
+attention arithmetic.  Both sides of every parity check (the CUDA library and the
+CPU oracle) read the tensors made here.
+
+Recipe: Q, K, V entries are iid N(0, 1) drawn in float32 from a seeded
+``torch.Generator`` and rounded to bf16 (round-to-nearest-even by ``.to``).
+Decode cache lengths are integers uniform in [1024, 32768] from a CPU generator;
+cache rows at or past a sequence's length are filled with NaN so that a read past
+the visible prefix shows up in the output.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    kind: str  # "dense" or "kvcache"
+    B: int
+    Hq: int
+    Hkv: int
+    Nq: int
+    Nk: int  # dense: key length; kvcache: padded cache length Lmax
+    d: int
+    causal: bool
+    seed: int
+
+    @property
+    def scale(self) -> float:
+        # 1/sqrt(d) rounded once to float32: the value handed to the kernels.
+        return float(torch.tensor(1.0 / math.sqrt(self.d), dtype=torch.float32))
+
+
+# The five workloads of the exact-attention forward pass (bf16, iid N(0,1)).
+WORKLOADS = {
+    "tiny": Workload("tiny", "dense", 1, 1, 1, 256, 256, 64, False, 1001),
+    "dense2k": Workload("dense2k", "dense", 4, 16, 16, 2048, 2048, 128, False, 1002),
+    "causal8k": Workload("causal8k", "dense", 2, 32, 32, 8192, 8192, 128, True, 1003),
+    "gqa16k": Workload("gqa16k", "dense", 1, 32, 8, 16384, 16384, 128, True, 1004),
+    "decode": Workload("decode", "kvcache", 64, 32, 8, 1, 32768, 128, False, 1005),
+}
+
+
+def bf16_normal(shape, seed: int, device="cpu") -> torch.Tensor:
+    """iid N(0,1) float32 draws from a seeded generator, rounded to bf16."""
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    return torch.randn(tuple(shape), dtype=torch.float32, generator=g, device=device).to(
+        torch.bfloat16)
+
+
+def dense_inputs(B, Nq, Nk, Hq, Hkv, d, seed, device="cpu"):
+    """Q [B,Nq,Hq,d], K/V [B,Nk,Hkv,d] in the (batch, seqlen, nheads, headdim) layout."""
+    q = bf16_normal((B, Nq, Hq, d), seed, device)
+    k = bf16_normal((B, Nk, Hkv, d), seed + 7919, device)
+    v = bf16_normal((B, Nk, Hkv, d), seed + 15823, device)
+    return q, k, v
+
+
+def workload_inputs(w: Workload, device="cpu", seed=None):
+    s = w.seed if seed is None else seed
+    return dense_inputs(w.B, w.Nq, w.Nk, w.Hq, w.Hkv, w.d, s, device)
+
+
+def varlen_inputs(seqlens_q, seqlens_k, Hq, Hkv, d, seed, device="cpu"):
+    """Packed Q [total_q,Hq,d], K/V [total_k,Hkv,d] and int32 prefix sums [B+1]."""
+    sq = torch.tensor([0] + list(seqlens_q), dtype=torch.int64)
+    sk = torch.tensor([0] + list(seqlens_k), dtype=torch.int64)
+    cu_q = torch.cumsum(sq, 0).to(torch.int32)
+    cu_k = torch.cumsum(sk, 0).to(torch.int32)
+    tq, tk = int(cu_q[-1]), int(cu_k[-1])
+    q = bf16_normal((tq, Hq, d), seed, device)
+    k = bf16_normal((tk, Hkv, d), seed + 7919, device)
+    v = bf16_normal((tk, Hkv, d), seed + 15823, device)
+    return q, k, v, cu_q.to(device), cu_k.to(device)
+
+
+def decode_lengths(B, lo=1024, hi=32768, seed=1005) -> torch.Tensor:
+    """Per-sequence cache lengths, integers uniform in [lo, hi] (CPU generator)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    return torch.randint(lo, hi + 1, (B,), generator=g, dtype=torch.int64).to(torch.int32)
+
+
+def kvcache_inputs(B, Lmax, Hq, Hkv, d, seed, lengths=None, device="cpu", poison=True):
+    """Q [B,1,Hq,d], padded caches [B,Lmax,Hkv,d], lengths int32 [B].
+
+    Rows at or past lengths[b] are NaN when ``poison`` is set.  The cache is drawn
+    one batch entry at a time to bound the float32 temporary.
+    """
+    if lengths is None:
+        lengths = decode_lengths(B, seed=seed)
+    lengths = torch.as_tensor(lengths, dtype=torch.int32).cpu()
+    q = bf16_normal((B, 1, Hq, d), seed, device)
+    kc = torch.empty((B, Lmax, Hkv, d), dtype=torch.bfloat16, device=device)
+    vc = torch.empty((B, Lmax, Hkv, d), dtype=torch.bfloat16, device=device)
+    for b in range(B):
+        kc[b] = bf16_normal((Lmax, Hkv, d), seed * 1000003 + 2 * b + 1, device)
+        vc[b] = bf16_normal((Lmax, Hkv, d), seed * 1000003 + 2 * b + 2, device)
+        if poison:
+            n = int(lengths[b])
+            kc[b, n:] = float("nan")
+            vc[b, n:] = float("nan")
+    return q, kc, vc, lengths.to(device)

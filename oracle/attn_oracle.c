@@ -1,0 +1,364 @@
+/*
+ * attn_oracle.c -- plain fp64 CPU oracle for exact scaled-dot-product attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or call
+ * this file: only the tests, the smoke check and the benchmark's CPU-baseline leg
+ * use it.  It shares no code, header, table or helper with the CUDA library.
+ *
+ * What it computes (the plain definition, no blocking, no fusion):
+ *   "FlashAttention 1-4 详解" (pinghaoyang.com.cn), section 原算法 -- the standard
+ *   attention S = Q K^T, P = softmax(S / sqrt(d)), O = P V, written there as one
+ *   formula and as the three-step S/P/O pipeline.  The scale is an argument
+ *   (default 1/sqrt(d)) and is applied to the scores before the softmax.
+ *   The softmax of one row is the numerically stable two-pass form of the same
+ *   page's "Online Softmax 数学推导" section: m = max_k x_k, then
+ *   e^{x_i - m} / sum_j e^{x_j - m}.
+ *   The per-row log-sum-exp that the fused kernel outputs (the softmax_lse kept
+ *   for the backward pass, "flash-attention" (ai-reference-codex.pages.dev),
+ *   sections 2.1 and 2.3) is LSE = m + ln(sum_j e^{x_j - m}), natural log of the
+ *   sum of exponentials of the scaled scores.
+ *
+ * Readings taken where the pages are silent (each one is listed in the design notes):
+ *   - causal masking is aligned bottom-right: query i of Nq may see key j of Nk when
+ *     j <= i + (Nk - Nq); for Nq == Nk this is j <= i ("FlashAttention 1-4 详解",
+ *     FlashAttention 2 engineering notes, causal lower triangle);
+ *   - a row with no visible key has O = 0 and LSE = -inf;
+ *   - grouped-query attention maps query head h to key/value head h / (Hq / Hkv)
+ *     ("flash-attention", capabilities table, MQA / GQA row: Hkv divides Hq);
+ *   - variable-length batches are packed along the token axis and delimited by the
+ *     prefix sums cu_seqlens ("flash-attention", capabilities table, varlen row);
+ *   - single-query decode attends to the first cache_seqlens[b] rows of the cache
+ *     ("flash-attention", capabilities table, KV cache row; section 1 usage).
+ *
+ * Inputs are bf16 bit patterns (uint16).  Each is widened exactly to double, so the
+ * oracle sees the same numbers the GPU sees; all arithmetic is IEEE double.
+ * Work is spread over threads by query row; the arithmetic of a row does not depend
+ * on the thread count.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* bf16 bits -> exact double (bf16 is the upper half of an IEEE binary32). */
+static double bf16_to_double(uint16_t bits) {
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/*
+ * One query row against keys 0..nkeys-1 (the visible set).
+ * q      : d bf16 values
+ * krow(j): key j at kbase + j * k_stride, d values
+ * vrow(j): value j at vbase + j * v_stride, d values
+ * s      : scratch of nkeys doubles; on return it holds the probabilities P_j
+ * o      : d doubles, o = sum_j P_j v_j
+ * lse    : natural-log sum of exp of the scaled scores
+ */
+static void attend_row(const uint16_t *q, const uint16_t *kbase, int64_t k_stride,
+                       const uint16_t *vbase, int64_t v_stride, int64_t nkeys, int d,
+                       double scale, double *s, double *o, double *lse) {
+    for (int c = 0; c < d; ++c) o[c] = 0.0;
+    if (nkeys <= 0) {
+        *lse = -INFINITY;
+        return;
+    }
+    /* S = scale * q . k_j */
+    for (int64_t j = 0; j < nkeys; ++j) {
+        const uint16_t *kr = kbase + j * k_stride;
+        double acc = 0.0;
+        for (int c = 0; c < d; ++c) acc += bf16_to_double(q[c]) * bf16_to_double(kr[c]);
+        s[j] = scale * acc;
+    }
+    /* stable softmax: m = max_j s_j, l = sum_j e^{s_j - m}, P_j = e^{s_j - m} / l */
+    double m = s[0];
+    for (int64_t j = 1; j < nkeys; ++j)
+        if (s[j] > m) m = s[j];
+    double l = 0.0;
+    for (int64_t j = 0; j < nkeys; ++j) {
+        s[j] = exp(s[j] - m);
+        l += s[j];
+    }
+    for (int64_t j = 0; j < nkeys; ++j) s[j] /= l;
+    /* O = P V */
+    for (int64_t j = 0; j < nkeys; ++j) {
+        const uint16_t *vr = vbase + j * v_stride;
+        for (int c = 0; c < d; ++c) o[c] += s[j] * bf16_to_double(vr[c]);
+    }
+    *lse = m + log(l);
+}
+
+/* Number of keys query i may see: all Nk, or (causal, bottom-right) i + Nk - Nq + 1. */
+static int64_t visible_keys(int64_t i, int64_t Nq, int64_t Nk, int causal) {
+    if (!causal) return Nk;
+    int64_t last = i + (Nk - Nq);
+    if (last < 0) return 0;
+    if (last >= Nk) return Nk;
+    return last + 1;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Work description shared by the threaded drivers.                          */
+
+typedef struct {
+    /* dense layout: element (b, n, h, c) at base + b*s[0] + n*s[1] + h*s[2] + c */
+    const uint16_t *q, *k, *v;
+    int64_t qs[3], ks[3], vs[3];
+    int B, Nq, Nk, Hq, Hkv, d, causal;
+    double scale;
+    /* varlen: prefix sums over the packed token axis (B+1 entries) */
+    const int32_t *cu_q, *cu_k;
+    /* kv cache: visible prefix length per batch entry */
+    const int32_t *cache_len;
+    /* optional list of (b, h, i) triples; when set only those rows are computed */
+    const int32_t *rows;
+    int64_t nrows;
+    /* outputs */
+    double *o, *lse;
+    int64_t os[3];      /* output strides (b, n, h) for the full drivers */
+    int64_t lse_s[3];   /* lse strides (b, h, n) */
+    int mode;           /* 0 dense, 1 varlen, 2 kvcache */
+    int nthreads, tid;
+    int64_t total;      /* number of (b, h, i) work items */
+} job_t;
+
+/* Map a flat work index to (b, h, i) for the full drivers. */
+static void decode_index(const job_t *J, int64_t w, int *b, int *h, int64_t *i) {
+    if (J->rows) {
+        *b = J->rows[3 * w];
+        *h = J->rows[3 * w + 1];
+        *i = J->rows[3 * w + 2];
+        return;
+    }
+    if (J->mode == 1) {
+        /* varlen: w runs over (token t of the packed batch, head h) */
+        int64_t t = w / J->Hq;
+        *h = (int)(w % J->Hq);
+        int bb = 0;
+        while (J->cu_q[bb + 1] <= t) ++bb;
+        *b = bb;
+        *i = t - J->cu_q[bb];
+        return;
+    }
+    int64_t per_b = (int64_t)J->Nq * J->Hq;
+    *b = (int)(w / per_b);
+    int64_t r = w % per_b;
+    *i = r / J->Hq;
+    *h = (int)(r % J->Hq);
+}
+
+static void *worker(void *arg) {
+    job_t *J = (job_t *)arg;
+    int64_t max_keys = J->Nk;
+    double *s = (double *)malloc(sizeof(double) * (size_t)(max_keys > 0 ? max_keys : 1));
+    double *orow = (double *)malloc(sizeof(double) * (size_t)J->d);
+    int group = J->Hq / J->Hkv;
+    for (int64_t w = J->tid; w < J->total; w += J->nthreads) {
+        int b, h;
+        int64_t i;
+        decode_index(J, w, &b, &h, &i);
+        int g = h / group; /* key/value head shared by this query head */
+        const uint16_t *qrow, *kbase, *vbase;
+        int64_t nkeys, k_stride, v_stride;
+        if (J->mode == 0) {
+            qrow = J->q + b * J->qs[0] + i * J->qs[1] + h * J->qs[2];
+            kbase = J->k + b * J->ks[0] + g * J->ks[2];
+            vbase = J->v + b * J->vs[0] + g * J->vs[2];
+            k_stride = J->ks[1];
+            v_stride = J->vs[1];
+            nkeys = visible_keys(i, J->Nq, J->Nk, J->causal);
+        } else if (J->mode == 1) {
+            int64_t nq = J->cu_q[b + 1] - J->cu_q[b];
+            int64_t nk = J->cu_k[b + 1] - J->cu_k[b];
+            qrow = J->q + (J->cu_q[b] + i) * J->qs[1] + h * J->qs[2];
+            kbase = J->k + J->cu_k[b] * J->ks[1] + g * J->ks[2];
+            vbase = J->v + J->cu_k[b] * J->vs[1] + g * J->vs[2];
+            k_stride = J->ks[1];
+            v_stride = J->vs[1];
+            nkeys = visible_keys(i, nq, nk, J->causal);
+        } else {
+            /* decode: one query per batch entry sees the whole cached prefix */
+            qrow = J->q + b * J->qs[0] + h * J->qs[2];
+            kbase = J->k + b * J->ks[0] + g * J->ks[2];
+            vbase = J->v + b * J->vs[0] + g * J->vs[2];
+            k_stride = J->ks[1];
+            v_stride = J->vs[1];
+            nkeys = J->cache_len[b];
+        }
+        double lse;
+        attend_row(qrow, kbase, k_stride, vbase, v_stride, nkeys, J->d, J->scale, s, orow, &lse);
+        double *odst;
+        double *ldst;
+        if (J->rows) {
+            odst = J->o + w * J->d;
+            ldst = J->lse + w;
+        } else if (J->mode == 1) {
+            int64_t t = J->cu_q[b] + i;
+            odst = J->o + t * J->os[1] + h * J->os[2];
+            ldst = J->lse + h * J->lse_s[1] + t * J->lse_s[2];
+        } else {
+            odst = J->o + b * J->os[0] + i * J->os[1] + h * J->os[2];
+            ldst = J->lse + b * J->lse_s[0] + h * J->lse_s[1] + i * J->lse_s[2];
+        }
+        memcpy(odst, orow, sizeof(double) * (size_t)J->d);
+        *ldst = lse;
+    }
+    free(s);
+    free(orow);
+    return NULL;
+}
+
+static int run_threads(job_t *base) {
+    int n = base->nthreads < 1 ? 1 : base->nthreads;
+    if (n > 512) n = 512;
+    pthread_t th[512];
+    job_t jobs[512];
+    for (int t = 0; t < n; ++t) {
+        jobs[t] = *base;
+        jobs[t].nthreads = n;
+        jobs[t].tid = t;
+    }
+    for (int t = 1; t < n; ++t)
+        if (pthread_create(&th[t], NULL, worker, &jobs[t]) != 0) return -1;
+    worker(&jobs[0]);
+    for (int t = 1; t < n; ++t) pthread_join(th[t], NULL);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Exported entry points (called through ctypes by oracle/oracle.py).        */
+
+/*
+ * Dense batched attention.  q: [B, Nq, Hq, d], k/v: [B, Nk, Hkv, d] with element
+ * strides (b, n, h) given, unit stride over d.  o: [B, Nq, Hq, d] contiguous
+ * doubles, lse: [B, Hq, Nq] contiguous doubles.  Returns 0 on success.
+ */
+int oracle_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int Nq, int Nk,
+               int Hq, int Hkv, int d, const int64_t *q_strides, const int64_t *k_strides,
+               const int64_t *v_strides, double scale, int causal, double *o, double *lse,
+               int nthreads) {
+    if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0) return -1;
+    job_t J;
+    memset(&J, 0, sizeof J);
+    J.q = q; J.k = k; J.v = v;
+    for (int a = 0; a < 3; ++a) { J.qs[a] = q_strides[a]; J.ks[a] = k_strides[a]; J.vs[a] = v_strides[a]; }
+    J.B = B; J.Nq = Nq; J.Nk = Nk; J.Hq = Hq; J.Hkv = Hkv; J.d = d; J.causal = causal;
+    J.scale = scale;
+    J.o = o; J.lse = lse;
+    J.os[0] = (int64_t)Nq * Hq * d; J.os[1] = (int64_t)Hq * d; J.os[2] = d;
+    J.lse_s[0] = (int64_t)Hq * Nq; J.lse_s[1] = Nq; J.lse_s[2] = 1;
+    J.mode = 0;
+    J.nthreads = nthreads;
+    J.total = (int64_t)B * Nq * Hq;
+    return run_threads(&J);
+}
+
+/*
+ * Dense attention on a chosen set of rows: rows is n triples (b, h, i).
+ * o: [n, d] doubles, lse: [n] doubles.
+ */
+int oracle_fwd_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int Nq, int Nk,
+                    int Hq, int Hkv, int d, const int64_t *q_strides, const int64_t *k_strides,
+                    const int64_t *v_strides, double scale, int causal, const int32_t *rows,
+                    int64_t n, double *o, double *lse, int nthreads) {
+    if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0) return -1;
+    job_t J;
+    memset(&J, 0, sizeof J);
+    J.q = q; J.k = k; J.v = v;
+    for (int a = 0; a < 3; ++a) { J.qs[a] = q_strides[a]; J.ks[a] = k_strides[a]; J.vs[a] = v_strides[a]; }
+    J.B = B; J.Nq = Nq; J.Nk = Nk; J.Hq = Hq; J.Hkv = Hkv; J.d = d; J.causal = causal;
+    J.scale = scale;
+    J.rows = rows; J.nrows = n;
+    J.o = o; J.lse = lse;
+    J.mode = 0;
+    J.nthreads = nthreads;
+    J.total = n;
+    return run_threads(&J);
+}
+
+/*
+ * Packed variable-length batch.  q: [total_q, Hq, d], k/v: [total_k, Hkv, d] with
+ * token and head strides given ((b) stride unused); cu_q, cu_k: B+1 prefix sums
+ * (host memory).  o: [total_q, Hq, d] doubles, lse: [Hq, total_q] doubles.
+ */
+int oracle_fwd_varlen(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                      const int32_t *cu_q, const int32_t *cu_k, int B, int Hq, int Hkv, int d,
+                      const int64_t *q_strides, const int64_t *k_strides, const int64_t *v_strides,
+                      double scale, int causal, double *o, double *lse, int nthreads) {
+    if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0) return -1;
+    job_t J;
+    memset(&J, 0, sizeof J);
+    J.q = q; J.k = k; J.v = v;
+    for (int a = 0; a < 3; ++a) { J.qs[a] = q_strides[a]; J.ks[a] = k_strides[a]; J.vs[a] = v_strides[a]; }
+    int64_t total_q = cu_q[B];
+    int max_k = 0;
+    for (int b = 0; b < B; ++b) {
+        int nk = cu_k[b + 1] - cu_k[b];
+        if (nk > max_k) max_k = nk;
+    }
+    J.B = B; J.Nq = 0; J.Nk = max_k; J.Hq = Hq; J.Hkv = Hkv; J.d = d; J.causal = causal;
+    J.scale = scale;
+    J.cu_q = cu_q; J.cu_k = cu_k;
+    J.o = o; J.lse = lse;
+    J.os[0] = 0; J.os[1] = (int64_t)Hq * d; J.os[2] = d;
+    J.lse_s[0] = 0; J.lse_s[1] = total_q; J.lse_s[2] = 1;
+    J.mode = 1;
+    J.nthreads = nthreads;
+    J.total = total_q * Hq;
+    return run_threads(&J);
+}
+
+/*
+ * Single-query decode over a padded KV cache.  q: [B, 1, Hq, d] (strides given),
+ * k/v cache: [B, Lmax, Hkv, d] (strides given), cache_len: B visible lengths.
+ * o: [B, Hq, d] doubles, lse: [B, Hq] doubles.
+ */
+int oracle_fwd_kvcache(const uint16_t *q, const uint16_t *kc, const uint16_t *vc,
+                       const int32_t *cache_len, int B, int Lmax, int Hq, int Hkv, int d,
+                       const int64_t *q_strides, const int64_t *k_strides, const int64_t *v_strides,
+                       double scale, double *o, double *lse, int nthreads) {
+    if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0) return -1;
+    for (int b = 0; b < B; ++b)
+        if (cache_len[b] < 0 || cache_len[b] > Lmax) return -1;
+    job_t J;
+    memset(&J, 0, sizeof J);
+    J.q = q; J.k = kc; J.v = vc;
+    for (int a = 0; a < 3; ++a) { J.qs[a] = q_strides[a]; J.ks[a] = k_strides[a]; J.vs[a] = v_strides[a]; }
+    J.B = B; J.Nq = 1; J.Nk = Lmax; J.Hq = Hq; J.Hkv = Hkv; J.d = d; J.causal = 0;
+    J.scale = scale;
+    J.cache_len = cache_len;
+    J.o = o; J.lse = lse;
+    J.os[0] = (int64_t)Hq * d; J.os[1] = 0; J.os[2] = d;
+    J.lse_s[0] = Hq; J.lse_s[1] = 1; J.lse_s[2] = 0;
+    J.mode = 2;
+    J.nthreads = nthreads;
+    J.total = (int64_t)B * Hq;
+    return run_threads(&J);
+}
+
+/*
+ * Probabilities of one dense row (b, h, i): P_j for j < Nk (0 for keys the row may
+ * not see).  Exposed so that tests can check invariants of P itself on tiny cases.
+ */
+int oracle_row_probs(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int Nq, int Nk,
+                     int Hq, int Hkv, int d, const int64_t *q_strides, const int64_t *k_strides,
+                     const int64_t *v_strides, double scale, int causal, int b, int h, int i,
+                     double *p_out) {
+    if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || b >= B || h >= Hq || i >= Nq) return -1;
+    int g = h / (Hq / Hkv);
+    int64_t nkeys = visible_keys(i, Nq, Nk, causal);
+    double *s = (double *)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+    double *orow = (double *)malloc(sizeof(double) * (size_t)d);
+    double lse;
+    attend_row(q + b * q_strides[0] + (int64_t)i * q_strides[1] + h * q_strides[2],
+               k + b * k_strides[0] + g * k_strides[2], k_strides[1],
+               v + b * v_strides[0] + g * v_strides[2], v_strides[1], nkeys, d, scale, s, orow,
+               &lse);
+    for (int64_t j = 0; j < Nk; ++j) p_out[j] = j < nkeys ? s[j] : 0.0;
+    free(s);
+    free(orow);
+    return 0;
+}

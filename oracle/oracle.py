@@ -1,0 +1,192 @@
+"""fp64 CPU oracle for exact attention -- Python side (ctypes over attn_oracle.c).
+
+TEST INFRASTRUCTURE ONLY.  The product path (the CUDA library and its Python
+binding) never imports this module; only the tests, ``__graft_entry__.smoke()``
+and the CPU-baseline leg of ``bench.py`` do.  It shares no code with the CUDA
+path: the C source is compiled here with gcc into ``oracle/_build``.
+
+Every function takes bf16 inputs as their 16-bit patterns (numpy ``uint16``) so
+that the oracle reads exactly the numbers the GPU reads, widens them exactly to
+double and computes the plain definition of attention
+("FlashAttention 1-4 详解", section 原算法: S = Q K^T, P = softmax(scale * S),
+O = P V; plus the natural-log log-sum-exp of each row of scaled scores).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile attn_oracle.c with gcc (plain -O2, IEEE double, no fast-math)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    stale = (not os.path.exists(_LIB_PATH)) or (
+        os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+    if force or stale:
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+               "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = build()
+            lib = ctypes.CDLL(path)
+            p = ctypes.c_void_p
+            i = ctypes.c_int
+            i64 = ctypes.c_int64
+            d = ctypes.c_double
+            lib.oracle_fwd.argtypes = [p, p, p, i, i, i, i, i, i, p, p, p, d, i, p, p, i]
+            lib.oracle_fwd_rows.argtypes = [p, p, p, i, i, i, i, i, i, p, p, p, d, i, p, i64,
+                                            p, p, i]
+            lib.oracle_fwd_varlen.argtypes = [p, p, p, p, p, i, i, i, i, p, p, p, d, i, p, p, i]
+            lib.oracle_fwd_kvcache.argtypes = [p, p, p, p, i, i, i, i, i, p, p, p, d, p, p, i]
+            lib.oracle_row_probs.argtypes = [p, p, p, i, i, i, i, i, i, p, p, p, d, i, i, i, i,
+                                             p]
+            for f in (lib.oracle_fwd, lib.oracle_fwd_rows, lib.oracle_fwd_varlen,
+                      lib.oracle_fwd_kvcache, lib.oracle_row_probs):
+                f.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _threads(n):
+    return int(n) if n else (os.cpu_count() or 1)
+
+
+def _bits(a) -> np.ndarray:
+    """Accept a numpy uint16 array or a torch bf16 tensor; return uint16 bits."""
+    if hasattr(a, "dtype") and str(a.dtype) == "torch.bfloat16":
+        import torch  # local: only the tests hand torch tensors in
+        a = a.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint16:
+        raise TypeError("oracle inputs are bf16 bit patterns (uint16)")
+    return a
+
+
+def _strides4(a: np.ndarray):
+    """(b, n, h) element strides of a contiguous [B, N, H, d] array."""
+    s = [x // a.itemsize for x in a.strides]
+    return (ctypes.c_int64 * 3)(s[0], s[1], s[2])
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def attention(q, k, v, scale: float, causal: bool = False, nthreads: int | None = None):
+    """Dense attention.  q [B,Nq,Hq,d], k/v [B,Nk,Hkv,d] (bf16 bits).
+
+    Returns (O [B,Nq,Hq,d] float64, LSE [B,Hq,Nq] float64).
+    """
+    q, k, v = _bits(q), _bits(k), _bits(v)
+    B, Nq, Hq, d = q.shape
+    _, Nk, Hkv, _ = k.shape
+    o = np.zeros((B, Nq, Hq, d), np.float64)
+    lse = np.zeros((B, Hq, Nq), np.float64)
+    rc = _load().oracle_fwd(_ptr(q), _ptr(k), _ptr(v), B, Nq, Nk, Hq, Hkv, d, _strides4(q),
+                            _strides4(k), _strides4(v), float(scale), int(bool(causal)),
+                            _ptr(o), _ptr(lse), _threads(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_fwd rejected its arguments")
+    return o, lse
+
+
+def attention_rows(q, k, v, rows, scale: float, causal: bool = False,
+                   nthreads: int | None = None):
+    """Dense attention on selected rows; rows is an (n, 3) int array of (b, h, i).
+
+    Returns (O [n, d] float64, LSE [n] float64).
+    """
+    q, k, v = _bits(q), _bits(k), _bits(v)
+    B, Nq, Hq, d = q.shape
+    _, Nk, Hkv, _ = k.shape
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 3))
+    n = rows.shape[0]
+    o = np.zeros((n, d), np.float64)
+    lse = np.zeros((n,), np.float64)
+    rc = _load().oracle_fwd_rows(_ptr(q), _ptr(k), _ptr(v), B, Nq, Nk, Hq, Hkv, d,
+                                 _strides4(q), _strides4(k), _strides4(v), float(scale),
+                                 int(bool(causal)), _ptr(rows), n, _ptr(o), _ptr(lse),
+                                 _threads(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_fwd_rows rejected its arguments")
+    return o, lse
+
+
+def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, causal: bool = False,
+                     nthreads: int | None = None):
+    """Packed varlen attention.  q [total_q,Hq,d], k/v [total_k,Hkv,d].
+
+    Returns (O [total_q,Hq,d] float64, LSE [Hq,total_q] float64).
+    """
+    q, k, v = _bits(q), _bits(k), _bits(v)
+    cu_q = np.ascontiguousarray(np.asarray(cu_seqlens_q, dtype=np.int32))
+    cu_k = np.ascontiguousarray(np.asarray(cu_seqlens_k, dtype=np.int32))
+    B = cu_q.shape[0] - 1
+    total_q, Hq, d = q.shape
+    Hkv = k.shape[1]
+
+    def st3(a):
+        s = [x // a.itemsize for x in a.strides]
+        return (ctypes.c_int64 * 3)(0, s[0], s[1])
+
+    o = np.zeros((total_q, Hq, d), np.float64)
+    lse = np.zeros((Hq, total_q), np.float64)
+    rc = _load().oracle_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_q), _ptr(cu_k), B, Hq,
+                                   Hkv, d, st3(q), st3(k), st3(v), float(scale),
+                                   int(bool(causal)), _ptr(o), _ptr(lse), _threads(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_fwd_varlen rejected its arguments")
+    return o, lse
+
+
+def attention_kvcache(q, k_cache, v_cache, cache_seqlens, scale: float,
+                      nthreads: int | None = None):
+    """Single-query decode.  q [B,1,Hq,d], caches [B,Lmax,Hkv,d], lengths [B].
+
+    Returns (O [B,Hq,d] float64, LSE [B,Hq] float64).
+    """
+    q, kc, vc = _bits(q), _bits(k_cache), _bits(v_cache)
+    lens = np.ascontiguousarray(np.asarray(cache_seqlens, dtype=np.int32))
+    B, _, Hq, d = q.shape
+    _, Lmax, Hkv, _ = kc.shape
+    o = np.zeros((B, Hq, d), np.float64)
+    lse = np.zeros((B, Hq), np.float64)
+    rc = _load().oracle_fwd_kvcache(_ptr(q), _ptr(kc), _ptr(vc), _ptr(lens), B, Lmax, Hq, Hkv,
+                                    d, _strides4(q), _strides4(kc), _strides4(vc),
+                                    float(scale), _ptr(o), _ptr(lse), _threads(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_fwd_kvcache rejected its arguments")
+    return o, lse
+
+
+def row_probs(q, k, v, b: int, h: int, i: int, scale: float, causal: bool = False):
+    """Softmax probabilities P[i, :] of one dense row (zeros on invisible keys)."""
+    q, k, v = _bits(q), _bits(k), _bits(v)
+    B, Nq, Hq, d = q.shape
+    _, Nk, Hkv, _ = k.shape
+    p = np.zeros((Nk,), np.float64)
+    rc = _load().oracle_row_probs(_ptr(q), _ptr(k), _ptr(v), B, Nq, Nk, Hq, Hkv, d,
+                                  _strides4(q), _strides4(k), _strides4(v), float(scale),
+                                  int(bool(causal)), b, h, i, _ptr(p))
+    if rc != 0:
+        raise ValueError("oracle_row_probs rejected its arguments")
+    return p

@@ -1,0 +1,387 @@
+"""Pins for the fp64 oracle: checks against facts fixed outside the oracle itself.
+
+Each ``pin_*`` function takes an oracle module (``oracle.oracle`` or a copy built
+from a mutated source) and raises ``AssertionError`` when the oracle disagrees with
+what the pages and the mathematics fix:
+
+* a library routine it does not call (``torch.nn.functional.scaled_dot_product_attention``
+  and ``torch.logsumexp`` in float64);
+* closed forms (uniform scores, a single visible key, constant V, two keys, rows
+  with no visible key, the hard-max limit);
+* invariants (rows of P sum to one, shift of every key by one vector, joint
+  permutation of keys and values, GQA as MHA with repeated K/V heads, varlen as
+  per-sequence dense, decode as dense with one query, sampled rows as full rows);
+* an independent algorithm: the tiled online-softmax recurrence of
+  "FlashAttention 1-4 详解", section Online Softmax 数学推导 (running max m,
+  running sum l, rescaled accumulator), written here in numpy with the scale and
+  the causal mask added, which must reach the same result as the oracle's direct
+  two-pass softmax.
+
+The same battery runs against deliberately broken copies of the oracle
+(tests/test_oracle.py) to show that a plausible slip in it fails a pin.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+import torch.nn.functional as F
+
+from exact_attention_81_gb300.inputs import bf16_normal, dense_inputs, varlen_inputs
+
+
+def _f64(t: torch.Tensor) -> torch.Tensor:
+    return t.to(torch.float64)
+
+
+def _np(t: torch.Tensor) -> np.ndarray:
+    return t.to(torch.float64).numpy()
+
+
+def _bottom_right_mask(Nq, Nk):
+    i = torch.arange(Nq)[:, None]
+    j = torch.arange(Nk)[None, :]
+    return j <= i + (Nk - Nq)
+
+
+def _library_attention(q, k, v, scale, causal):
+    """float64 torch SDPA + logsumexp; q [B,Nq,Hq,d] -> (O [B,Nq,Hq,d], LSE [B,Hq,Nq])."""
+    Hq, Hkv = q.shape[2], k.shape[2]
+    G = Hq // Hkv
+    qq = _f64(q).permute(0, 2, 1, 3)
+    kk = _f64(k).permute(0, 2, 1, 3).repeat_interleave(G, dim=1)
+    vv = _f64(v).permute(0, 2, 1, 3).repeat_interleave(G, dim=1)
+    mask = _bottom_right_mask(q.shape[1], k.shape[1]) if causal else None
+    o = F.scaled_dot_product_attention(qq, kk, vv, attn_mask=mask, scale=scale)
+    scores = torch.matmul(qq, kk.transpose(-1, -2)) * scale
+    if mask is not None:
+        scores = scores.masked_fill(~mask, float("-inf"))
+    lse = torch.logsumexp(scores, dim=-1)
+    return o.permute(0, 2, 1, 3).numpy(), lse.numpy()
+
+
+def _close(a, b, tol, what):
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    assert a.shape == b.shape, f"{what}: shape {a.shape} vs {b.shape}"
+    fin = np.isfinite(b)
+    assert np.array_equal(np.isfinite(a), fin), f"{what}: finiteness differs"
+    assert np.array_equal(a[~fin], b[~fin]), f"{what}: infinite entries differ"
+    if fin.any():
+        err = np.max(np.abs(a[fin] - b[fin]))
+        assert err <= tol, f"{what}: max abs error {err:.3e} > {tol:.1e}"
+
+
+# --------------------------------------------------------------------------
+# library cross-check
+
+LIB_CASES = [
+    # B, Nq, Nk, Hq, Hkv, d, causal
+    (1, 64, 64, 2, 2, 16, False),
+    (2, 37, 37, 4, 2, 64, True),
+    (1, 50, 80, 4, 1, 32, True),  # Nq < Nk: bottom-right causal alignment
+    (1, 70, 45, 2, 2, 16, False),
+    (1, 130, 130, 2, 2, 128, True),
+]
+
+
+def pin_library(O, cases=LIB_CASES):
+    for n, (B, Nq, Nk, Hq, Hkv, d, causal) in enumerate(cases):
+        q, k, v = dense_inputs(B, Nq, Nk, Hq, Hkv, d, seed=50 + n)
+        scale = 1.0 / math.sqrt(d)
+        o, lse = O.attention(q, k, v, scale, causal)
+        o_ref, lse_ref = _library_attention(q, k, v, scale, causal)
+        _close(o, o_ref, 1e-11, f"O vs torch SDPA case {n}")
+        _close(lse, lse_ref, 1e-11, f"LSE vs torch logsumexp case {n}")
+
+
+# --------------------------------------------------------------------------
+# closed forms
+
+def pin_uniform_scores(O):
+    """Q = 0: every visible key scores 0, so O is the mean of the visible V rows and
+    LSE = ln(#visible)."""
+    B, N, H, d = 1, 40, 2, 16
+    _, k, v = dense_inputs(B, N, N, H, H, d, seed=7)
+    q = torch.zeros((B, N, H, d), dtype=torch.bfloat16)
+    vv = _np(v)
+    for causal in (False, True):
+        o, lse = O.attention(q, k, v, 0.25, causal)
+        for i in range(N):
+            n_vis = i + 1 if causal else N
+            for h in range(H):
+                _close(o[0, i, h], vv[0, :n_vis, h].mean(axis=0), 1e-13, "uniform O")
+                _close(lse[0, h, i], math.log(n_vis), 1e-13, "uniform LSE")
+
+
+def pin_single_key(O):
+    """Causal row 0 sees key 0 only: O = v_0, LSE = scale * q_0 . k_0."""
+    B, N, H, d = 2, 9, 3, 32
+    q, k, v = dense_inputs(B, N, N, H, H, d, seed=8)
+    scale = 0.3
+    o, lse = O.attention(q, k, v, scale, True)
+    qq, kk, vv = _np(q), _np(k), _np(v)
+    for b in range(B):
+        for h in range(H):
+            _close(o[b, 0, h], vv[b, 0, h], 1e-14, "single-key O")
+            s0 = scale * float(np.dot(qq[b, 0, h], kk[b, 0, h]))
+            _close(lse[b, h, 0], s0, 1e-12, "single-key LSE")
+
+
+def pin_constant_v(O):
+    """All value rows equal to c: O = c for every row, whatever the scores."""
+    B, Nq, Nk, H, d = 1, 20, 33, 2, 16
+    q, k, _ = dense_inputs(B, Nq, Nk, H, H, d, seed=9)
+    c = bf16_normal((1, 1, H, d), seed=10)
+    v = c.expand(B, Nk, H, d).contiguous()
+    for causal in (False, True):
+        o, _ = O.attention(q, k, v, 0.2, causal)
+        _close(o, np.broadcast_to(_np(c), o.shape), 1e-14, "constant-V O")
+
+
+def pin_two_keys(O):
+    """Two keys: P = (sigmoid(s0 - s1), sigmoid(s1 - s0)), LSE = logaddexp(s0, s1)."""
+    B, Nq, Nk, H, d = 1, 6, 2, 2, 8
+    q, k, v = dense_inputs(B, Nq, Nk, H, H, d, seed=11)
+    scale = 0.7
+    o, lse = O.attention(q, k, v, scale, False)
+    qq, kk, vv = _np(q), _np(k), _np(v)
+    for i in range(Nq):
+        for h in range(H):
+            s0 = scale * float(np.dot(qq[0, i, h], kk[0, 0, h]))
+            s1 = scale * float(np.dot(qq[0, i, h], kk[0, 1, h]))
+            p0 = 1.0 / (1.0 + math.exp(s1 - s0))
+            p1 = 1.0 / (1.0 + math.exp(s0 - s1))
+            _close(o[0, i, h], p0 * vv[0, 0, h] + p1 * vv[0, 1, h], 1e-13, "two-key O")
+            _close(lse[0, h, i], np.logaddexp(s0, s1), 1e-13, "two-key LSE")
+
+
+def pin_empty_rows(O):
+    """Causal with Nq > Nk (bottom-right): the first Nq - Nk rows see no key and give
+    O = 0, LSE = -inf; the others see i - (Nq - Nk) + 1 keys."""
+    B, Nq, Nk, H, d = 1, 12, 5, 1, 16
+    q, k, v = dense_inputs(B, Nq, Nk, H, H, d, seed=12)
+    o, lse = O.attention(q, k, v, 0.25, True)
+    for i in range(Nq - Nk):
+        assert np.all(o[0, i] == 0.0), "empty row O must be 0"
+        assert lse[0, 0, i] == -np.inf, "empty row LSE must be -inf"
+    # the last row sees every key: equal to the non-causal last row
+    o_nc, lse_nc = O.attention(q, k, v, 0.25, False)
+    _close(o[0, -1], o_nc[0, -1], 1e-14, "last causal row")
+    _close(lse[0, 0, -1], lse_nc[0, 0, -1], 1e-14, "last causal row LSE")
+
+
+def pin_hard_max(O):
+    """A large scale makes the softmax a hard max: O tends to the value row of the
+    best key, within sum_{j != *} exp(-(s* - s_j)) * max|v|."""
+    B, N, H, d = 1, 24, 1, 16
+    q, k, v = dense_inputs(B, N, N, H, H, d, seed=13)
+    scale = 40.0
+    o, lse = O.attention(q, k, v, scale, False)
+    qq, kk, vv = _np(q), _np(k), _np(v)
+    for i in range(N):
+        s = scale * (kk[0, :, 0] @ qq[0, i, 0])
+        j = int(np.argmax(s))
+        gap = np.sort(s)[-1] - s
+        bound = np.sum(np.exp(-gap[gap > 0])) * np.max(np.abs(vv)) * 2 + 1e-12
+        err = np.max(np.abs(o[0, i, 0] - vv[0, j, 0]))
+        assert err <= bound, f"hard-max row {i}: {err:.3e} > {bound:.3e}"
+        assert s[j] <= lse[0, 0, i] <= s[j] + math.log(N) + 1e-12, "hard-max LSE bounds"
+
+
+# --------------------------------------------------------------------------
+# invariants
+
+def pin_probs(O):
+    """Rows of P sum to one, P_j / P_0 = exp(s_j - s_0), invisible keys get 0."""
+    B, N, H, d = 1, 30, 2, 16
+    q, k, v = dense_inputs(B, N, N, H, H, d, seed=14)
+    scale = 0.25
+    qq, kk = _np(q), _np(k)
+    for causal in (False, True):
+        for i in (0, 7, N - 1):
+            p = O.row_probs(q, k, v, 0, 1, i, scale, causal)
+            n_vis = i + 1 if causal else N
+            assert abs(p.sum() - 1.0) <= 1e-14, "P row must sum to 1"
+            assert np.all(p[n_vis:] == 0.0), "invisible keys must have P = 0"
+            s = scale * (kk[0, :n_vis, 1] @ qq[0, i, 1])
+            _close(p[:n_vis] / p[0], np.exp(s - s[0]), 1e-12, "P ratios")
+
+
+def pin_shift(O):
+    """Adding one vector u to every key leaves O unchanged and shifts LSE by
+    scale * q . u (keys and u are small integers, so K + u is exact in bf16)."""
+    B, N, H, d = 1, 25, 2, 16
+    g = torch.Generator().manual_seed(15)
+    q = bf16_normal((B, N, H, d), seed=16)
+    k = torch.randint(-8, 9, (B, N, H, d), generator=g).to(torch.bfloat16)
+    u = torch.randint(-8, 9, (1, 1, H, d), generator=g).to(torch.bfloat16)
+    v = bf16_normal((B, N, H, d), seed=17)
+    k2 = (k.float() + u.float()).to(torch.bfloat16)
+    assert torch.equal(k2.float(), k.float() + u.float())
+    scale = 0.125
+    for causal in (False, True):
+        o1, l1 = O.attention(q, k, v, scale, causal)
+        o2, l2 = O.attention(q, k2, v, scale, causal)
+        _close(o2, o1, 1e-12, "shifted-keys O")
+        qu = scale * np.einsum("bnhd,hd->bhn", _np(q), _np(u)[0, 0])
+        _close(l2, l1 + qu, 1e-11, "shifted-keys LSE")
+
+
+def pin_permutation(O):
+    """Non-causal attention does not depend on the order of the (key, value) pairs."""
+    B, Nq, Nk, H, d = 2, 17, 29, 2, 32
+    q, k, v = dense_inputs(B, Nq, Nk, H, H, d, seed=18)
+    perm = torch.randperm(Nk, generator=torch.Generator().manual_seed(19))
+    o1, l1 = O.attention(q, k, v, 0.2, False)
+    o2, l2 = O.attention(q, k[:, perm].contiguous(), v[:, perm].contiguous(), 0.2, False)
+    _close(o2, o1, 1e-13, "permuted O")
+    _close(l2, l1, 1e-13, "permuted LSE")
+
+
+def pin_gqa(O):
+    """GQA with Hq = G * Hkv equals MHA with each K/V head repeated G times."""
+    B, N, Hq, Hkv, d = 2, 21, 8, 2, 16
+    q, k, v = dense_inputs(B, N, N, Hq, Hkv, d, seed=20)
+    G = Hq // Hkv
+    kr = k.repeat_interleave(G, dim=2).contiguous()
+    vr = v.repeat_interleave(G, dim=2).contiguous()
+    for causal in (False, True):
+        o1, l1 = O.attention(q, k, v, 0.25, causal)
+        o2, l2 = O.attention(q, kr, vr, 0.25, causal)
+        _close(o1, o2, 0.0, "GQA vs repeated-head MHA O")
+        _close(l1, l2, 0.0, "GQA vs repeated-head MHA LSE")
+
+
+def pin_varlen(O):
+    """A packed varlen batch equals each sequence run on its own (dense)."""
+    sq = [5, 0, 19, 33, 1]
+    sk = [7, 3, 19, 20, 1]
+    Hq, Hkv, d = 4, 2, 16
+    q, k, v, cu_q, cu_k = varlen_inputs(sq, sk, Hq, Hkv, d, seed=21)
+    for causal in (False, True):
+        o, lse = O.attention_varlen(q, k, v, cu_q, cu_k, 0.25, causal)
+        for b in range(len(sq)):
+            a, e = int(cu_q[b]), int(cu_q[b + 1])
+            ka, ke = int(cu_k[b]), int(cu_k[b + 1])
+            if e == a:
+                continue
+            qb = q[a:e].unsqueeze(0).contiguous()
+            kb = k[ka:ke].unsqueeze(0).contiguous()
+            vb = v[ka:ke].unsqueeze(0).contiguous()
+            if ke == ka:
+                assert np.all(o[a:e] == 0.0) and np.all(lse[:, a:e] == -np.inf)
+                continue
+            ob, lb = O.attention(qb, kb, vb, 0.25, causal)
+            _close(o[a:e], ob[0], 0.0, f"varlen seq {b} O")
+            _close(lse[:, a:e], lb[0], 0.0, f"varlen seq {b} LSE")
+
+
+def pin_kvcache(O):
+    """Decode over the first L_b cache rows equals dense attention with one query and
+    Nk = L_b; NaN rows past L_b never reach the result."""
+    B, Lmax, Hq, Hkv, d = 3, 40, 4, 2, 16
+    lens = [40, 1, 23]
+    q = bf16_normal((B, 1, Hq, d), seed=22)
+    kc = bf16_normal((B, Lmax, Hkv, d), seed=23)
+    vc = bf16_normal((B, Lmax, Hkv, d), seed=24)
+    for b, n in enumerate(lens):
+        kc[b, n:] = float("nan")
+        vc[b, n:] = float("nan")
+    o, lse = O.attention_kvcache(q, kc, vc, lens, 0.25)
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
+    for b, n in enumerate(lens):
+        ob, lb = O.attention(q[b:b + 1].contiguous(), kc[b:b + 1, :n].contiguous(),
+                             vc[b:b + 1, :n].contiguous(), 0.25, False)
+        _close(o[b], ob[0, 0], 0.0, f"decode batch {b} O")
+        _close(lse[b], lb[0, :, 0], 0.0, f"decode batch {b} LSE")
+
+
+def pin_rows(O):
+    """Row sampling returns exactly the rows of the full computation."""
+    B, N, Hq, Hkv, d = 2, 33, 4, 2, 16
+    q, k, v = dense_inputs(B, N, N, Hq, Hkv, d, seed=25)
+    o, lse = O.attention(q, k, v, 0.25, True)
+    rows = np.array([[0, 0, 0], [1, 3, 32], [0, 2, 17], [1, 1, 5]], np.int32)
+    orow, lrow = O.attention_rows(q, k, v, rows, 0.25, True)
+    for n, (b, h, i) in enumerate(rows):
+        _close(orow[n], o[b, i, h], 0.0, "sampled row O")
+        _close(lrow[n], lse[b, h, i], 0.0, "sampled row LSE")
+
+
+def online_softmax_attention(q, k, v, scale, causal, Br, Bc):
+    """Tiled forward with the online-softmax recurrence (numpy, fp64), following the
+    update rules m_new = max(m, rowmax(S_ij)), P~ = exp(S_ij - m_new),
+    l_new = e^{m - m_new} l + rowsum(P~), O_new = e^{m - m_new} O + P~ V_j and the
+    final O / l, with the scale applied to S and masked entries set to -inf."""
+    qq, kk, vv = _np(q), _np(k), _np(v)
+    B, Nq, Hq, d = qq.shape
+    Nk, Hkv = kk.shape[1], kk.shape[2]
+    G = Hq // Hkv
+    O_out = np.zeros((B, Nq, Hq, d))
+    L_out = np.zeros((B, Hq, Nq))
+    for b in range(B):
+        for h in range(Hq):
+            Q = qq[b, :, h]
+            K = kk[b, :, h // G]
+            V = vv[b, :, h // G]
+            for i0 in range(0, Nq, Br):
+                Qi = Q[i0:i0 + Br]
+                rows = np.arange(i0, i0 + Qi.shape[0])
+                m = np.full(Qi.shape[0], -np.inf)
+                l = np.zeros(Qi.shape[0])
+                Oi = np.zeros((Qi.shape[0], d))
+                for j0 in range(0, Nk, Bc):
+                    Kj, Vj = K[j0:j0 + Bc], V[j0:j0 + Bc]
+                    S = scale * (Qi @ Kj.T)
+                    if causal:
+                        cols = np.arange(j0, j0 + Kj.shape[0])
+                        S = np.where(cols[None, :] <= rows[:, None] + (Nk - Nq), S, -np.inf)
+                    m_new = np.maximum(m, S.max(axis=1))
+                    safe = np.where(np.isfinite(m_new), m_new, 0.0)
+                    P = np.exp(S - safe[:, None])
+                    alpha = np.where(np.isfinite(m), np.exp(m - safe), 0.0)
+                    l = alpha * l + P.sum(axis=1)
+                    Oi = alpha[:, None] * Oi + P @ Vj
+                    m = m_new
+                with np.errstate(invalid="ignore", divide="ignore"):
+                    O_out[b, i0:i0 + Br, h] = np.where(l[:, None] > 0, Oi / np.where(
+                        l > 0, l, 1.0)[:, None], 0.0)
+                    L_out[b, h, i0:i0 + Br] = np.where(l > 0, m + np.log(np.where(
+                        l > 0, l, 1.0)), -np.inf)
+    return O_out, L_out
+
+
+def pin_recurrence(O):
+    """The oracle's direct softmax and the tiled online recurrence agree."""
+    cases = [(1, 70, 70, 2, 1, 16, True, 16, 16), (2, 45, 61, 2, 2, 32, False, 16, 16),
+             (1, 150, 150, 1, 1, 64, True, 128, 128), (1, 30, 50, 2, 2, 16, True, 16, 32)]
+    for n, (B, Nq, Nk, Hq, Hkv, d, causal, Br, Bc) in enumerate(cases):
+        q, k, v = dense_inputs(B, Nq, Nk, Hq, Hkv, d, seed=30 + n)
+        scale = 1.0 / math.sqrt(d)
+        o, lse = O.attention(q, k, v, scale, causal)
+        o2, l2 = online_softmax_attention(q, k, v, scale, causal, Br, Bc)
+        _close(o, o2, 1e-12, f"recurrence case {n} O")
+        _close(lse, l2, 1e-12, f"recurrence case {n} LSE")
+
+
+def pin_lse_recompute(O):
+    """P recomputed from the saved LSE, P = exp(scale * S - LSE), has unit row sums
+    and reproduces O = P V (the relation the backward pass relies on)."""
+    B, N, H, d = 1, 48, 2, 32
+    q, k, v = dense_inputs(B, N, N, H, H, d, seed=40)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = O.attention(q, k, v, scale, True)
+    qq, kk, vv = _np(q), _np(k), _np(v)
+    for h in range(H):
+        S = scale * qq[0, :, h] @ kk[0, :, h].T
+        S = np.where(_bottom_right_mask(N, N).numpy(), S, -np.inf)
+        P = np.exp(S - lse[0, h][:, None])
+        _close(P.sum(axis=1), np.ones(N), 1e-12, "recomputed P row sums")
+        _close(P @ vv[0, :, h], o[0, :, h], 1e-12, "recomputed O")
+
+
+ALL_PINS = [pin_library, pin_uniform_scores, pin_single_key, pin_constant_v, pin_two_keys,
+            pin_empty_rows, pin_hard_max, pin_probs, pin_shift, pin_permutation, pin_gqa,
+            pin_varlen, pin_kvcache, pin_rows, pin_recurrence, pin_lse_recompute]

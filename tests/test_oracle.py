@@ -1,0 +1,79 @@
+"""CPU tests: the fp64 oracle against its pins, and the pins against planted slips."""
+import importlib.util
+import os
+import shutil
+
+import pytest
+
+import oracle.oracle as ORACLE
+from tests import oracle_pins as P
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.mark.parametrize("pin", P.ALL_PINS, ids=lambda f: f.__name__)
+def test_oracle_pin(pin):
+    pin(ORACLE)
+
+
+# Plausible slips in the oracle's C source.  Each one, planted in a copy built in a
+# temporary directory, must make at least one pin fail.
+MUTATIONS = [
+    ("scale dropped", "s[j] = scale * acc;", "s[j] = acc;"),
+    ("exponent sign flipped", "s[j] = exp(s[j] - m);", "s[j] = exp(m - s[j]);"),
+    ("normalisation dropped", "for (int64_t j = 0; j < nkeys; ++j) s[j] /= l;", ""),
+    ("max term dropped from LSE", "*lse = m + log(l);", "*lse = log(l);"),
+    ("keys read from V", "const uint16_t *kr = kbase + j * k_stride;",
+     "const uint16_t *kr = vbase + j * v_stride;"),
+    ("values read from K", "const uint16_t *vr = vbase + j * v_stride;",
+     "const uint16_t *vr = kbase + j * k_stride;"),
+    ("GQA head index wrong", "int g = h / group;", "int g = h % J->Hkv;"),
+    ("causal aligned top-left", "int64_t last = i + (Nk - Nq);", "int64_t last = i;"),
+    ("causal off by one", "return last + 1;", "return last;"),
+    ("varlen query offset from key offsets",
+     "qrow = J->q + (J->cu_q[b] + i) * J->qs[1] + h * J->qs[2];",
+     "qrow = J->q + (J->cu_k[b] + i) * J->qs[1] + h * J->qs[2];"),
+    ("decode ignores cache length", "nkeys = J->cache_len[b];", "nkeys = J->Nk;"),
+]
+
+
+def _mutated_oracle(tmp_path, old, new):
+    src = open(os.path.join(ROOT, "oracle", "attn_oracle.c")).read()
+    assert src.count(old) == 1, f"mutation anchor not unique: {old!r}"
+    d = tmp_path / "mut"
+    d.mkdir()
+    (d / "attn_oracle.c").write_text(src.replace(old, new))
+    shutil.copy(os.path.join(ROOT, "oracle", "oracle.py"), d / "oracle.py")
+    spec = importlib.util.spec_from_file_location("oracle_mutant", str(d / "oracle.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_pins_catch_planted_slip(tmp_path, name, old, new):
+    mod = _mutated_oracle(tmp_path, old, new)
+    caught = []
+    for pin in P.ALL_PINS:
+        try:
+            pin(mod)
+        except (AssertionError, ValueError, FloatingPointError):
+            caught.append(pin.__name__)
+    assert caught, f"no pin fails when the oracle has the slip: {name}"
+
+
+def test_golden_tiny_rows_reproduce():
+    """The stored oracle rows of the tiny workload are reproduced (regression)."""
+    import json
+
+    import numpy as np
+
+    from exact_attention_81_gb300.inputs import WORKLOADS, workload_inputs
+
+    g = json.load(open(os.path.join(ROOT, "tests", "golden", "tiny_rows.json")))
+    w = WORKLOADS["tiny"]
+    q, k, v = workload_inputs(w)
+    rows = np.array([[0, 0, i] for i in g["rows"]], np.int32)
+    o, lse = ORACLE.attention_rows(q, k, v, rows, w.scale, w.causal)
+    assert np.max(np.abs(o - np.array(g["o"]))) <= 1e-12
+    assert np.max(np.abs(lse - np.array(g["lse"]))) <= 1e-12
