@@ -1,0 +1,284 @@
+"""ctypes binding over libfa.so (the C ABI in include/fa.h).
+
+Argument marshalling only: it checks tensor types, reads pointers, shapes and strides,
+allocates outputs with torch when the caller does not pass them, and calls the C entry
+point of the same name on the current CUDA stream.  Every step of the attention itself
+runs in the library's CUDA kernels.  If libfa.so is missing or fails to load, every call
+raises; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfa.so")
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_CUDA = 3
+FA_ERR_WORKSPACE = 4
+FA_ERR_TIMEOUT = 5
+
+
+class FAError(RuntimeError):
+    """A libfa call returned a non-zero fa_status."""
+
+    def __init__(self, status: int, where: str, detail: str = ""):
+        self.status = int(status)
+        msg = f"{where}: {status_string(self.status)}"
+        if detail:
+            msg += f" [{detail}]"
+        super().__init__(msg)
+
+
+class FwdParams(ctypes.Structure):
+    """Mirror of fa_fwd_params."""
+
+    _fields_ = [
+        ("q", ctypes.c_void_p),
+        ("k", ctypes.c_void_p),
+        ("v", ctypes.c_void_p),
+        ("o", ctypes.c_void_p),
+        ("lse", ctypes.c_void_p),
+        ("B", ctypes.c_int),
+        ("Nq", ctypes.c_int),
+        ("Nk", ctypes.c_int),
+        ("Hq", ctypes.c_int),
+        ("Hkv", ctypes.c_int),
+        ("d", ctypes.c_int),
+        ("q_strides", ctypes.c_int64 * 3),
+        ("k_strides", ctypes.c_int64 * 3),
+        ("v_strides", ctypes.c_int64 * 3),
+        ("o_strides", ctypes.c_int64 * 3),
+        ("scale", ctypes.c_float),
+        ("causal", ctypes.c_int),
+    ]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load_library(path: str | None = None):
+    """Load libfa.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(
+                f"{p} not found: build it with `python -m exact_attention_81_gb300.build`")
+        lib = ctypes.CDLL(p)
+        vp, i, i64, f, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
+                             ctypes.c_size_t)
+        lib.fa_fwd.argtypes = [ctypes.POINTER(FwdParams), vp]
+        lib.fa_fwd.restype = i
+        lib.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i,
+                                      vp]
+        lib.fa_fwd_varlen.restype = i
+        lib.fa_fwd_kvcache_workspace_size.argtypes = [i, i, i, i, i]
+        lib.fa_fwd_kvcache_workspace_size.restype = sz
+        lib.fa_fwd_kvcache.argtypes = [vp, vp, vp, vp, i, i, i, i, i, ctypes.POINTER(i64), f, i,
+                                       vp, sz, vp, vp, vp]
+        lib.fa_fwd_kvcache.restype = i
+        lib.fa_get_last_device_error.argtypes = [vp]
+        lib.fa_get_last_device_error.restype = i
+        lib.fa_status_string.argtypes = [i]
+        lib.fa_status_string.restype = ctypes.c_char_p
+        lib.fa_last_cuda_error.argtypes = []
+        lib.fa_last_cuda_error.restype = ctypes.c_char_p
+        lib.fa_set_wait_timeout_ns.argtypes = [ctypes.c_ulonglong]
+        lib.fa_set_wait_timeout_ns.restype = None
+        lib.fa_fwd_params_size.argtypes = []
+        lib.fa_fwd_params_size.restype = sz
+        if lib.fa_fwd_params_size() != ctypes.sizeof(FwdParams):
+            raise RuntimeError("fa_fwd_params layout mismatch between libfa.so and the binding")
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().fa_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str):
+    if status != FA_OK:
+        detail = load_library().fa_last_cuda_error().decode() if status == FA_ERR_CUDA else ""
+        raise FAError(status, where, detail)
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else int(t.data_ptr())
+
+
+def _require_bf16_cuda(name, t, ndim):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != torch.bfloat16 or not t.is_cuda:
+        raise TypeError(f"{name} must be a bf16 CUDA tensor")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions")
+    if t.numel() > 0 and t.stride(-1) != 1:
+        raise ValueError(f"{name} must have unit stride in the head dimension")
+
+
+def default_scale(d: int) -> float:
+    return 1.0 / math.sqrt(d)
+
+
+def fa_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
+           stream=None):
+    """Dense attention.  q [B,Nq,Hq,d], k/v [B,Nk,Hkv,d] (bf16, CUDA).
+
+    Returns (out [B,Nq,Hq,d] bf16, lse [B,Hq,Nq] fp32).
+    """
+    _require_bf16_cuda("q", q, 4)
+    _require_bf16_cuda("k", k, 4)
+    _require_bf16_cuda("v", v, 4)
+    B, Nq, Hq, d = q.shape
+    Nk, Hkv = k.shape[1], k.shape[2]
+    if tuple(k.shape) != (B, Nk, Hkv, d) or tuple(v.shape) != (B, Nk, Hkv, d):
+        raise ValueError("k and v must be [B, Nk, Hkv, d] matching q")
+    if out is None:
+        out = torch.empty((B, Nq, Hq, d), dtype=torch.bfloat16, device=q.device)
+    else:
+        _require_bf16_cuda("out", out, 4)
+        if tuple(out.shape) != (B, Nq, Hq, d):
+            raise ValueError("out must be [B, Nq, Hq, d]")
+    if lse is None:
+        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
+    elif lse.dtype != torch.float32 or tuple(lse.shape) != (B, Hq, Nq) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [B, Hq, Nq] tensor")
+    p = FwdParams()
+    p.q, p.k, p.v, p.o, p.lse = _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse)
+    p.B, p.Nq, p.Nk, p.Hq, p.Hkv, p.d = B, Nq, Nk, Hq, Hkv, d
+    for name, t in (("q_strides", q), ("k_strides", k), ("v_strides", v), ("o_strides", out)):
+        getattr(p, name)[:] = list(t.stride()[:3])
+    p.scale = default_scale(d) if scale is None else float(scale)
+    p.causal = int(bool(causal))
+    _check(load_library().fa_fwd(ctypes.byref(p), _stream_handle(stream)), "fa_fwd")
+    return out, lse
+
+
+def fa_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int,
+                  causal: bool = False, scale: float | None = None, out=None, lse=None,
+                  stream=None):
+    """Packed varlen attention.  q [total_q,Hq,d], k/v [total_k,Hkv,d], cu_seqlens int32 [B+1].
+
+    Returns (out [total_q,Hq,d] bf16, lse [Hq,total_q] fp32).
+    """
+    _require_bf16_cuda("q", q, 3)
+    _require_bf16_cuda("k", k, 3)
+    _require_bf16_cuda("v", v, 3)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous for the varlen call")
+    for name, t in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous int32 CUDA tensor")
+    total_q, Hq, d = q.shape
+    total_k, Hkv = k.shape[0], k.shape[1]
+    B = cu_seqlens_q.numel() - 1
+    if cu_seqlens_k.numel() != B + 1:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must have the same length")
+    if out is None:
+        out = torch.empty((total_q, Hq, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((Hq, total_q), dtype=torch.float32, device=q.device)
+    sc = default_scale(d) if scale is None else float(scale)
+    st = load_library().fa_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                                      _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), B,
+                                      int(max_seqlen_q), int(max_seqlen_k), total_q, total_k, Hq,
+                                      Hkv, d, sc, int(bool(causal)), _stream_handle(stream))
+    _check(st, "fa_fwd_varlen")
+    return out, lse
+
+
+def fa_fwd_kvcache_workspace_size(B: int, Hq: int, Lmax: int, d: int, num_splits: int = 0) -> int:
+    return int(load_library().fa_fwd_kvcache_workspace_size(B, Hq, Lmax, d, num_splits))
+
+
+def fa_fwd_kvcache(q, k_cache, v_cache, cache_seqlens, scale: float | None = None,
+                   num_splits: int = 0, workspace=None, out=None, lse=None, stream=None):
+    """Single-query decode.  q [B,1,Hq,d], caches [B,Lmax,Hkv,d], cache_seqlens int32 [B].
+
+    Returns (out [B,1,Hq,d] bf16, lse [B,Hq] fp32).
+    """
+    _require_bf16_cuda("q", q, 4)
+    _require_bf16_cuda("k_cache", k_cache, 4)
+    _require_bf16_cuda("v_cache", v_cache, 4)
+    if k_cache.stride() != v_cache.stride() or k_cache.shape != v_cache.shape:
+        raise ValueError("k_cache and v_cache must share shape and strides")
+    if cache_seqlens.dtype != torch.int32 or not cache_seqlens.is_cuda:
+        raise TypeError("cache_seqlens must be an int32 CUDA tensor")
+    if not q.is_contiguous():
+        raise ValueError("q must be contiguous")
+    B, _, Hq, d = q.shape
+    Lmax, Hkv = k_cache.shape[1], k_cache.shape[2]
+    if out is None:
+        out = torch.empty((B, 1, Hq, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    need = fa_fwd_kvcache_workspace_size(B, Hq, Lmax, d, num_splits)
+    if workspace is None:
+        workspace = torch.empty((max(need, 256),), dtype=torch.uint8, device=q.device)
+    strides = (ctypes.c_int64 * 3)(*k_cache.stride()[:3])
+    sc = default_scale(d) if scale is None else float(scale)
+    st = load_library().fa_fwd_kvcache(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cache_seqlens),
+                                       B, Lmax, Hq, Hkv, d, strides, sc, int(num_splits),
+                                       _ptr(workspace), workspace.numel(), _ptr(out), _ptr(lse),
+                                       _stream_handle(stream))
+    _check(st, "fa_fwd_kvcache")
+    return out, lse
+
+
+def get_last_device_error(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error status."""
+    return int(load_library().fa_get_last_device_error(_stream_handle(stream)))
+
+
+def set_wait_timeout_ns(ns: int):
+    """Limit on device-side waits for later launches (0 = default)."""
+    load_library().fa_set_wait_timeout_ns(int(ns))
+
+
+# Names of the upstream Python API ("flash-attention", section 1), mapped onto the C calls.
+def flash_attn_func(q, k, v, dropout_p: float = 0.0, softmax_scale=None, causal=False,
+                    return_lse=False):
+    if dropout_p != 0.0:
+        raise NotImplementedError("dropout is not part of this forward path")
+    o, lse = fa_fwd(q, k, v, causal=causal, scale=softmax_scale)
+    return (o, lse) if return_lse else o
+
+
+def flash_attn_varlen_func(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
+                           dropout_p: float = 0.0, softmax_scale=None, causal=False,
+                           return_lse=False):
+    if dropout_p != 0.0:
+        raise NotImplementedError("dropout is not part of this forward path")
+    o, lse = fa_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
+                           causal=causal, scale=softmax_scale)
+    return (o, lse) if return_lse else o
+
+
+def flash_attn_with_kvcache(q, k_cache, v_cache, cache_seqlens, softmax_scale=None,
+                            causal=True, num_splits=0, return_lse=False):
+    # With one query per sequence, bottom-right causal alignment lets it see the whole
+    # visible prefix, so `causal` does not change the result.
+    o, lse = fa_fwd_kvcache(q, k_cache, v_cache, cache_seqlens, scale=softmax_scale,
+                            num_splits=num_splits)
+    return (o, lse) if return_lse else o

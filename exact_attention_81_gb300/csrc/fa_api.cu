@@ -1,0 +1,412 @@
+// fa_api.cu -- the C ABI of libfa.so (declared in include/fa.h): argument validation,
+// TMA tensor-map construction, work decomposition and kernel launches.  No allocation,
+// no synchronisation (except in fa_get_last_device_error), everything on the caller's
+// stream.
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/fa.h"
+#include "fa_internal.h"
+
+namespace {
+
+// Per-device word the kernels OR their fault bits into.
+__device__ unsigned int g_device_error;
+
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kDefaultTimeoutNs = 10ull * 1000 * 1000 * 1000;
+
+struct DeviceInfo {
+  bool ready = false;
+  bool supported = false;
+  int sm_count = 0;
+  unsigned int *err = nullptr;  // device address of g_device_error on this device
+};
+
+std::mutex g_mutex;
+DeviceInfo g_dev[kMaxDevices];
+unsigned long long g_timeout_ns = kDefaultTimeoutNs;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+thread_local char g_cuda_msg[512] = "";
+
+fa_status cuda_fail(const char *what, cudaError_t e) {
+  snprintf(g_cuda_msg, sizeof g_cuda_msg, "%s: %s (%s)", what, cudaGetErrorName(e),
+           cudaGetErrorString(e));
+  return FA_ERR_CUDA;
+}
+
+// Looks up the current device; fills its capabilities and the error-word address once.
+fa_status current_device(DeviceInfo **out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail("cudaGetDevice", e);
+  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceInfo &d = g_dev[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
+      return cuda_fail("cudaDeviceGetAttribute", e);
+    if ((e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+      return cuda_fail("cudaDeviceGetAttribute", e);
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail("cudaDeviceGetAttribute", e);
+    d.supported = (major == 10 && minor == 3);
+    d.sm_count = sms;
+    if (d.supported) {
+      void *p = nullptr;
+      if ((e = cudaGetSymbolAddress(&p, g_device_error)) != cudaSuccess)
+        return cuda_fail("cudaGetSymbolAddress", e);
+      d.err = static_cast<unsigned int *>(p);
+      if (g_encode == nullptr) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
+          return cuda_fail("cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)",
+                           e != cudaSuccess ? e : cudaErrorSymbolNotFound);
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+      }
+    }
+    d.ready = true;
+  }
+  if (!d.supported) return FA_ERR_UNSUPPORTED;
+  *out = &d;
+  return FA_OK;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// 4-D bf16 tensor map over a (batch, seq, head, d) tensor, dimensions ordered
+// {d, head, seq, batch}, box {64, 1, 128, 1} (64 columns x 128 rows of one head), 128-byte
+// swizzle, zero fill past the tensor edges.  sn/sh/sb are element strides.
+fa_status make_map(CUtensorMap *map, const void *base, int d, int64_t n, int64_t h, int64_t b,
+                   int64_t sn, int64_t sh, int64_t sb) {
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(h),
+                        static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(b)};
+  // The stride of a dimension of extent 1 is never used; give it a legal value.
+  const int64_t bh = h > 1 ? sh * 2 : static_cast<int64_t>(d) * 2;
+  const int64_t bn = n > 1 ? sn * 2 : bh * h;
+  const int64_t bb = b > 1 ? sb * 2 : bn * n;
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(bh), static_cast<cuuint64_t>(bn),
+                           static_cast<cuuint64_t>(bb)};
+  for (int i = 0; i < 3; ++i)
+    if (strides[i] == 0 || (strides[i] % 16) != 0 || strides[i] >= (cuuint64_t(1) << 40))
+      return FA_ERR_INVALID_ARG;
+  cuuint32_t box[4] = {64, 1, 128, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(g_cuda_msg, sizeof g_cuda_msg, "cuTensorMapEncodeTiled failed (CUresult %d)",
+             static_cast<int>(r));
+    return FA_ERR_CUDA;
+  }
+  return FA_OK;
+}
+
+bool stride_ok(int64_t s, int64_t extent) {
+  if (extent <= 1) return s >= 0;
+  return s > 0 && (s % 8) == 0 && s < (int64_t(1) << 38);
+}
+
+float scale_log2(float scale) {
+  return static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+}
+
+bool scale_ok(float s) { return std::isfinite(s) && s > 0.f; }
+
+int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
+
+// Keys per split for the decode path (a multiple of the 128-key block).
+int decode_chunk(int Lmax, int num_splits) {
+  int64_t c;
+  if (num_splits > 0) {
+    c = (static_cast<int64_t>(Lmax) + num_splits - 1) / num_splits;
+  } else {
+    c = (static_cast<int64_t>(Lmax) + 31) / 32;  // about 32 splits of a full-length cache
+    if (c < 256) c = 256;
+  }
+  c = ((c + 127) / 128) * 128;
+  if (c < 128) c = 128;
+  return static_cast<int>(c);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: invalid argument";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: unsupported configuration or device";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA: CUDA call failed";
+    case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE: workspace missing or too small";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a device-side wait gave up";
+  }
+  return "unknown fa_status";
+}
+
+const char *fa_last_cuda_error(void) { return g_cuda_msg; }
+
+size_t fa_fwd_params_size(void) { return sizeof(fa_fwd_params); }
+
+void fa_set_wait_timeout_ns(unsigned long long ns) {
+  g_timeout_ns = ns == 0 ? kDefaultTimeoutNs : ns;
+}
+
+fa_status fa_fwd(const fa_fwd_params *p, cudaStream_t stream) {
+  if (p == nullptr) return FA_ERR_INVALID_ARG;
+  const fa_fwd_params &a = *p;
+  if (a.B < 0 || a.Nq < 0 || a.Nk < 0 || a.Hq <= 0 || a.Hkv <= 0 || a.Hq % a.Hkv != 0)
+    return FA_ERR_INVALID_ARG;
+  if (a.d != 64 && a.d != 128) return FA_ERR_UNSUPPORTED;
+  if (!scale_ok(a.scale)) return FA_ERR_INVALID_ARG;
+  if (a.Nq > (1 << 30) || a.Nk > (1 << 30)) return FA_ERR_INVALID_ARG;
+  if (a.B == 0 || a.Nq == 0) return FA_OK;
+  if (a.q == nullptr || a.o == nullptr || a.lse == nullptr) return FA_ERR_INVALID_ARG;
+  if (!aligned(a.q, 16) || !aligned(a.o, 16) || !aligned(a.lse, 4)) return FA_ERR_INVALID_ARG;
+  if (!stride_ok(a.q_strides[0], a.B) || !stride_ok(a.q_strides[1], a.Nq) ||
+      !stride_ok(a.q_strides[2], a.Hq) || !stride_ok(a.o_strides[0], a.B) ||
+      !stride_ok(a.o_strides[1], a.Nq) || !stride_ok(a.o_strides[2], a.Hq))
+    return FA_ERR_INVALID_ARG;
+  if (a.Nk > 0) {
+    if (a.k == nullptr || a.v == nullptr) return FA_ERR_INVALID_ARG;
+    if (!aligned(a.k, 16) || !aligned(a.v, 16)) return FA_ERR_INVALID_ARG;
+    if (!stride_ok(a.k_strides[0], a.B) || !stride_ok(a.k_strides[1], a.Nk) ||
+        !stride_ok(a.k_strides[2], a.Hkv) || !stride_ok(a.v_strides[0], a.B) ||
+        !stride_ok(a.v_strides[1], a.Nk) || !stride_ok(a.v_strides[2], a.Hkv))
+      return FA_ERR_INVALID_ARG;
+  }
+  const int mblocks = ceil_div(a.Nq, 256);
+  const int64_t tiles = static_cast<int64_t>(a.B) * a.Hq * mblocks;
+  if (tiles > INT32_MAX) return FA_ERR_INVALID_ARG;
+
+  DeviceInfo *dev = nullptr;
+  fa_status st = current_device(&dev);
+  if (st != FA_OK) return st;
+  const int64_t lse_sb = static_cast<int64_t>(a.Hq) * a.Nq, lse_sh = a.Nq;
+  if (a.Nk == 0) {
+    cudaError_t e = fa::launch_fill_empty(a.o, a.lse, a.B, a.Nq, a.Hq, a.d, a.o_strides[0],
+                                          a.o_strides[1], a.o_strides[2], lse_sb, lse_sh, stream);
+    return e == cudaSuccess ? FA_OK : cuda_fail("fill kernel launch", e);
+  }
+  CUtensorMap tq, tk, tv;
+  if ((st = make_map(&tq, a.q, a.d, a.Nq, a.Hq, a.B, a.q_strides[1], a.q_strides[2],
+                     a.q_strides[0])) != FA_OK)
+    return st;
+  if ((st = make_map(&tk, a.k, a.d, a.Nk, a.Hkv, a.B, a.k_strides[1], a.k_strides[2],
+                     a.k_strides[0])) != FA_OK)
+    return st;
+  if ((st = make_map(&tv, a.v, a.d, a.Nk, a.Hkv, a.B, a.v_strides[1], a.v_strides[2],
+                     a.v_strides[0])) != FA_OK)
+    return st;
+  fa::PrefillArgs pa{};
+  pa.o = a.o;
+  pa.lse = a.lse;
+  pa.o_sb = a.o_strides[0];
+  pa.o_sn = a.o_strides[1];
+  pa.o_sh = a.o_strides[2];
+  pa.lse_sb = lse_sb;
+  pa.lse_sh = lse_sh;
+  pa.B = a.B;
+  pa.Hq = a.Hq;
+  pa.Hkv = a.Hkv;
+  pa.group = a.Hq / a.Hkv;
+  pa.Nq = a.Nq;
+  pa.Nk = a.Nk;
+  pa.varlen = 0;
+  pa.mblocks = mblocks;
+  pa.num_tiles = static_cast<int>(tiles);
+  pa.scale_log2 = scale_log2(a.scale);
+  pa.err = dev->err;
+  pa.timeout_ns = g_timeout_ns;
+  const int grid = static_cast<int>(tiles < dev->sm_count ? tiles : dev->sm_count);
+  cudaError_t e = fa::launch_prefill(a.d, a.causal != 0, tq, tk, tv, pa, grid, stream);
+  return e == cudaSuccess ? FA_OK : cuda_fail("prefill kernel launch", e);
+}
+
+fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                        const int *cu_seqlens_q, const int *cu_seqlens_k, int B,
+                        int max_seqlen_q, int max_seqlen_k, int total_q, int total_k, int Hq,
+                        int Hkv, int d, float scale, int causal, cudaStream_t stream) {
+  if (B < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || total_q < 0 || total_k < 0 || Hq <= 0 ||
+      Hkv <= 0 || Hq % Hkv != 0)
+    return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (!scale_ok(scale)) return FA_ERR_INVALID_ARG;
+  if (max_seqlen_q > (1 << 30) || total_q > (1 << 30) || total_k > (1 << 30))
+    return FA_ERR_INVALID_ARG;
+  if (B == 0 || total_q == 0 || max_seqlen_q == 0) return FA_OK;
+  if (q == nullptr || o == nullptr || lse == nullptr || cu_seqlens_q == nullptr ||
+      cu_seqlens_k == nullptr)
+    return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(o, 16) || !aligned(lse, 4) || !aligned(cu_seqlens_q, 4) ||
+      !aligned(cu_seqlens_k, 4))
+    return FA_ERR_INVALID_ARG;
+  if (total_k > 0 && (k == nullptr || v == nullptr || !aligned(k, 16) || !aligned(v, 16)))
+    return FA_ERR_INVALID_ARG;
+  const int mblocks = ceil_div(max_seqlen_q, 256);
+  const int64_t tiles = static_cast<int64_t>(B) * Hq * mblocks;
+  if (tiles > INT32_MAX) return FA_ERR_INVALID_ARG;
+
+  DeviceInfo *dev = nullptr;
+  fa_status st = current_device(&dev);
+  if (st != FA_OK) return st;
+  const int64_t o_sn = static_cast<int64_t>(Hq) * d, o_sh = d;
+  if (total_k == 0) {
+    cudaError_t e = fa::launch_fill_empty(o, lse, 1, total_q, Hq, d, 0, o_sn, o_sh, 0, total_q,
+                                          stream);
+    return e == cudaSuccess ? FA_OK : cuda_fail("fill kernel launch", e);
+  }
+  CUtensorMap tq, tk, tv;
+  if ((st = make_map(&tq, q, d, total_q, Hq, 1, static_cast<int64_t>(Hq) * d, d, 0)) != FA_OK)
+    return st;
+  if ((st = make_map(&tk, k, d, total_k, Hkv, 1, static_cast<int64_t>(Hkv) * d, d, 0)) != FA_OK)
+    return st;
+  if ((st = make_map(&tv, v, d, total_k, Hkv, 1, static_cast<int64_t>(Hkv) * d, d, 0)) != FA_OK)
+    return st;
+  fa::PrefillArgs pa{};
+  pa.o = o;
+  pa.lse = lse;
+  pa.o_sb = 0;
+  pa.o_sn = o_sn;
+  pa.o_sh = o_sh;
+  pa.lse_sb = 0;
+  pa.lse_sh = total_q;
+  pa.B = B;
+  pa.Hq = Hq;
+  pa.Hkv = Hkv;
+  pa.group = Hq / Hkv;
+  pa.Nq = max_seqlen_q;
+  pa.Nk = max_seqlen_k;
+  pa.varlen = 1;
+  pa.cu_q = cu_seqlens_q;
+  pa.cu_k = cu_seqlens_k;
+  pa.total_q = total_q;
+  pa.total_k = total_k;
+  pa.mblocks = mblocks;
+  pa.num_tiles = static_cast<int>(tiles);
+  pa.scale_log2 = scale_log2(scale);
+  pa.err = dev->err;
+  pa.timeout_ns = g_timeout_ns;
+  const int grid = static_cast<int>(tiles < dev->sm_count ? tiles : dev->sm_count);
+  cudaError_t e = fa::launch_prefill(d, causal != 0, tq, tk, tv, pa, grid, stream);
+  return e == cudaSuccess ? FA_OK : cuda_fail("prefill kernel launch", e);
+}
+
+size_t fa_fwd_kvcache_workspace_size(int B, int Hq, int Lmax, int d, int num_splits) {
+  if (B <= 0 || Hq <= 0 || Lmax <= 0 || d <= 0 || num_splits < 0) return 0;
+  const int chunk = decode_chunk(Lmax, num_splits);
+  const int64_t maxch = (static_cast<int64_t>(Lmax) + chunk - 1) / chunk;
+  const int64_t bytes = static_cast<int64_t>(B) * Hq * maxch * (d + 1) * 4;
+  return static_cast<size_t>((bytes + 255) / 256 * 256);
+}
+
+fa_status fa_fwd_kvcache(const void *q, const void *k_cache, const void *v_cache,
+                         const int *cache_seqlens, int B, int Lmax, int Hq, int Hkv, int d,
+                         const int64_t cache_strides[3], float scale, int num_splits,
+                         void *workspace, size_t workspace_bytes, void *o, float *lse,
+                         cudaStream_t stream) {
+  if (B < 0 || Lmax < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || num_splits < 0)
+    return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  const int group = Hq / Hkv;
+  if (group != 1 && group != 2 && group != 4 && group != 8) return FA_ERR_UNSUPPORTED;
+  if (!scale_ok(scale)) return FA_ERR_INVALID_ARG;
+  if (Lmax > (1 << 30)) return FA_ERR_INVALID_ARG;
+  if (B == 0) return FA_OK;
+  if (q == nullptr || o == nullptr || lse == nullptr || cache_seqlens == nullptr)
+    return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(o, 16) || !aligned(lse, 4) || !aligned(cache_seqlens, 4))
+    return FA_ERR_INVALID_ARG;
+  int chunk = 128, maxch = 0;
+  float *o_part = nullptr, *lse_part = nullptr;
+  if (Lmax > 0) {
+    if (k_cache == nullptr || v_cache == nullptr || cache_strides == nullptr)
+      return FA_ERR_INVALID_ARG;
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16)) return FA_ERR_INVALID_ARG;
+    if (!stride_ok(cache_strides[0], B) || !stride_ok(cache_strides[1], Lmax) ||
+        !stride_ok(cache_strides[2], Hkv))
+      return FA_ERR_INVALID_ARG;
+    const size_t need = fa_fwd_kvcache_workspace_size(B, Hq, Lmax, d, num_splits);
+    if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256))
+      return FA_ERR_WORKSPACE;
+    chunk = decode_chunk(Lmax, num_splits);
+    maxch = ceil_div(Lmax, chunk);
+    o_part = static_cast<float *>(workspace);
+    lse_part = o_part + static_cast<int64_t>(B) * Hq * maxch * d;
+  }
+  const int64_t units = static_cast<int64_t>(maxch) * B * Hkv;
+  if (units > INT32_MAX) return FA_ERR_INVALID_ARG;
+
+  DeviceInfo *dev = nullptr;
+  fa_status st = current_device(&dev);
+  if (st != FA_OK) return st;
+  if (Lmax > 0) {
+    CUtensorMap tk, tv;
+    if ((st = make_map(&tk, k_cache, d, Lmax, Hkv, B, cache_strides[1], cache_strides[2],
+                       cache_strides[0])) != FA_OK)
+      return st;
+    if ((st = make_map(&tv, v_cache, d, Lmax, Hkv, B, cache_strides[1], cache_strides[2],
+                       cache_strides[0])) != FA_OK)
+      return st;
+    fa::DecodeArgs da{};
+    da.q = q;
+    da.cache_len = cache_seqlens;
+    da.o_part = o_part;
+    da.lse_part = lse_part;
+    da.B = B;
+    da.Hq = Hq;
+    da.Hkv = Hkv;
+    da.Lmax = Lmax;
+    da.chunk = chunk;
+    da.maxch = maxch;
+    da.num_units = static_cast<int>(units);
+    da.scale_log2 = scale_log2(scale);
+    da.err = dev->err;
+    da.timeout_ns = g_timeout_ns;
+    const int grid = static_cast<int>(units < dev->sm_count ? units : dev->sm_count);
+    cudaError_t e = fa::launch_decode(d, group, tk, tv, da, grid, stream);
+    if (e != cudaSuccess) return cuda_fail("decode kernel launch", e);
+  }
+  cudaError_t e = fa::launch_combine(d, o_part, lse_part, cache_seqlens, B, Hq, Lmax, chunk,
+                                     maxch, o, lse, dev->err, stream);
+  return e == cudaSuccess ? FA_OK : cuda_fail("combine kernel launch", e);
+}
+
+fa_status fa_get_last_device_error(cudaStream_t stream) {
+  DeviceInfo *dev = nullptr;
+  fa_status st = current_device(&dev);
+  if (st != FA_OK) return st;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail("cudaStreamSynchronize", e);
+  unsigned int word = 0;
+  e = cudaMemcpyFromSymbol(&word, g_device_error, sizeof word);
+  if (e != cudaSuccess) return cuda_fail("cudaMemcpyFromSymbol", e);
+  const unsigned int zero = 0;
+  e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero);
+  if (e != cudaSuccess) return cuda_fail("cudaMemcpyToSymbol", e);
+  if (word & (fa::DEVERR_PREFILL_TIMEOUT | fa::DEVERR_DECODE_TIMEOUT)) return FA_ERR_TIMEOUT;
+  if (word & (fa::DEVERR_BAD_CU_SEQLENS | fa::DEVERR_BAD_CACHE_LEN)) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,73 @@
+// fa_internal.h -- declarations shared by the host API (fa_api.cu) and the kernel
+// translation units.  Not part of the public C ABI (include/fa.h).
+#pragma once
+
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+// Bits of the per-device error word that kernels set.
+enum : unsigned int {
+  DEVERR_PREFILL_TIMEOUT = 1u,  // a bounded wait in the prefill kernel gave up
+  DEVERR_DECODE_TIMEOUT = 2u,   // a bounded wait in the decode kernel gave up
+  DEVERR_BAD_CU_SEQLENS = 4u,   // varlen prefix sums out of range (sequence skipped)
+  DEVERR_BAD_CACHE_LEN = 8u,    // cache_seqlens outside [0, Lmax] (clamped)
+};
+
+// Arguments of the fused prefill kernel (dense and varlen share it).
+struct PrefillArgs {
+  void *o;              // bf16 output
+  float *lse;           // fp32 output
+  int64_t o_sb, o_sn, o_sh;   // output element strides (batch, token, head)
+  int64_t lse_sb, lse_sh;     // lse offset = b*lse_sb + h*lse_sh + token
+  int B, Hq, Hkv, group;      // group = Hq / Hkv
+  int Nq, Nk;                 // dense: lengths; varlen: max_seqlen_q / max_seqlen_k
+  int varlen;
+  const int *cu_q, *cu_k;     // varlen prefix sums (device)
+  int total_q, total_k;
+  int mblocks;                // 256-row query blocks per (batch, head)
+  int num_tiles;              // B * Hq * mblocks
+  float scale_log2;           // scale * log2(e)
+  unsigned int *err;          // device error word
+  unsigned long long timeout_ns;
+};
+
+cudaError_t launch_prefill(int d, bool causal, const CUtensorMap &tq, const CUtensorMap &tk,
+                           const CUtensorMap &tv, const PrefillArgs &a, int grid,
+                           cudaStream_t stream);
+
+// O = 0 and LSE = -inf for every row (no visible keys anywhere).
+cudaError_t launch_fill_empty(void *o, float *lse, int B, int N, int H, int d, int64_t o_sb,
+                              int64_t o_sn, int64_t o_sh, int64_t lse_sb, int64_t lse_sh,
+                              cudaStream_t stream);
+
+// Arguments of the split-KV decode kernel.
+struct DecodeArgs {
+  const void *q;              // [B, 1, Hq, d] bf16 contiguous
+  const int *cache_len;       // [B] device
+  float *o_part;              // [B*Hq, maxch, d] fp32 partial outputs (normalised per chunk)
+  float *lse_part;            // [B*Hq, maxch] fp32 partial LSE (natural log)
+  int B, Hq, Hkv, Lmax;
+  int chunk;                  // keys per split (multiple of 128)
+  int maxch;                  // ceil(Lmax / chunk)
+  int num_units;              // maxch * B * Hkv
+  float scale_log2;
+  unsigned int *err;
+  unsigned long long timeout_ns;
+};
+
+cudaError_t launch_decode(int d, int group, const CUtensorMap &tk, const CUtensorMap &tv,
+                          const DecodeArgs &a, int grid, cudaStream_t stream);
+
+cudaError_t launch_combine(int d, const float *o_part, const float *lse_part,
+                           const int *cache_len, int B, int Hq, int Lmax, int chunk, int maxch,
+                           void *o, float *lse, unsigned int *err, cudaStream_t stream);
+
+// Shared-memory bytes the kernels request (for host-side checks).
+int prefill_smem_bytes(int d);
+int decode_smem_bytes(int d, int group);
+
+}  // namespace fa

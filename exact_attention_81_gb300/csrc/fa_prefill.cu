@@ -1,0 +1,560 @@
+// fa_prefill.cu -- fused exact-attention forward ("prefill") kernel for sm_103a.
+//
+// One persistent CTA per SM walks a list of work tiles.  A work tile is one (batch, query
+// head, 256-row query block): two 128-row query sub-tiles that share one K/V stream, the
+// larger-tile / two-tile ping-pong of "FlashAttention 1-4 详解", FlashAttention 4 section
+// (tile (Br, Bc) -> (Br', Bc') with Br' ~ 2 Br).  For every 128-key K/V tile j the CTA
+// computes, for each sub-tile t,
+//     S_t = Q_t K_j^T                       (tcgen05.mma, fp32 accumulator in TMEM)
+//     m_new = max(m, rowmax S_t * c),  P = 2^(S_t c - m_new),  l = 2^(m - m_new) l + rowsum P
+//     O_t = 2^(m - m_new) O_t + P V_j       (P stored to TMEM as bf16, tcgen05.mma again)
+// with c = scale * log2(e) folded into one FMA before the exp2 ("flash-attention",
+// section 4, scale_apply_exp2), the O rescale done only for warps whose row maxima grew
+// ("FlashAttention 1-4 详解", FlashAttention 4, conditional rescale when m_new > m), and
+// the division by l deferred to the epilogue ("FlashAttention 1-4 详解", FlashAttention 2,
+// normalise once after the inner loop).  The epilogue writes O (bf16) and the natural-log
+// LSE = ln2 * (m + log2 l).  S and P never leave the SM.
+//
+// Warp roles (320 threads):
+//   warps 0-3  softmax + correction + epilogue for sub-tile 0 (thread = query row)
+//   warps 4-7  the same for sub-tile 1
+//   warp  8    TMA producer: Q tiles and the K/V ring (one elected lane)
+//   warp  9    TMEM allocator and MMA issuer (one elected lane)
+// TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+d), O_1 [384,384+d).
+// P_t overwrites the first 64 columns of S_t as packed bf16 pairs and is the A operand of
+// the PV MMA straight from TMEM.
+//
+// Causal masking ("FlashAttention 1-4 详解", FlashAttention 2 engineering notes: skip the
+// tiles above the diagonal, ~N^2/2 work) limits each sub-tile to the K/V tiles that hold a
+// visible key and masks only the tiles that straddle the diagonal or the sequence end.
+// Tiles are ordered head-major with the largest causal query blocks first, so CTAs that
+// run at the same time share one head's K/V in L2 and long tiles start early.
+#include <cmath>
+
+#include "fa_internal.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int BR = 128;             // query rows per sub-tile (MMA M)
+constexpr int BC = 128;             // keys per K/V tile
+constexpr int NTHREADS = 320;
+constexpr int PRODUCER_WARP = 8;
+constexpr int MMA_WARP = 9;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int BOX_BYTES = 128 * 128;  // one TMA box: 128 rows x 64 bf16 (128 B, swizzled)
+constexpr float LN2 = 0.6931471805599453f;
+
+__host__ __device__ constexpr uint32_t s_col(int t) { return static_cast<uint32_t>(t * 128); }
+__host__ __device__ constexpr uint32_t o_col(int t) {
+  return static_cast<uint32_t>(256 + t * 128);
+}
+
+template <int D>
+struct Cfg {
+  static constexpr int KCH = D / 64;                     // 64-wide boxes per row
+  static constexpr int TILE_BYTES = KCH * BOX_BYTES;     // one [128 x D] bf16 tile
+  static constexpr int NSLOTS = D == 128 ? 4 : 8;        // K/V ring depth
+  static constexpr int Q_OFF = 0;
+  static constexpr int RING_OFF = 2 * TILE_BYTES;
+  static constexpr int BAR_OFF = RING_OFF + NSLOTS * TILE_BYTES;
+  static constexpr int SMEM_BYTES = BAR_OFF + 512 + 1024;  // barriers + alignment slack
+  static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BC, false, false);
+  static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, false, true);
+};
+
+struct Bars {
+  uint64_t q_full, q_empty;
+  uint64_t kv_full[8], kv_empty[8];
+  uint64_t s_full[2], p_ready[2], o_full[2], o_empty[2];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+struct TileInfo {
+  int b, h, hk;
+  int q_row0;       // first query row of the 256-row block, within its sequence
+  int q_tok, k_tok; // packed-token offset of the sequence (varlen), else 0
+  int tma_b;        // batch coordinate of the TMA maps (0 for varlen)
+  int nq, nk;       // sequence lengths
+  int nrows[2];     // valid query rows per sub-tile
+  int nkv[2];       // K/V tiles visited per sub-tile
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ TileInfo tile_info(const PrefillArgs &a, int tile) {
+  TileInfo ti;
+  const int bh = tile / a.mblocks;
+  const int r = tile - bh * a.mblocks;
+  const int mb = CAUSAL ? (a.mblocks - 1 - r) : r;
+  ti.b = bh / a.Hq;
+  ti.h = bh - ti.b * a.Hq;
+  ti.hk = ti.h / a.group;
+  ti.q_row0 = mb * 2 * BR;
+  if (a.varlen) {
+    const int q0 = a.cu_q[ti.b], q1 = a.cu_q[ti.b + 1];
+    const int k0 = a.cu_k[ti.b], k1 = a.cu_k[ti.b + 1];
+    const bool bad = q0 < 0 || q1 < q0 || q1 > a.total_q || k0 < 0 || k1 < k0 ||
+                     k1 > a.total_k || (q1 - q0) > a.Nq;
+    ti.q_tok = bad ? 0 : q0;
+    ti.k_tok = bad ? 0 : k0;
+    ti.nq = bad ? 0 : q1 - q0;
+    ti.nk = bad ? 0 : k1 - k0;
+    ti.tma_b = 0;
+  } else {
+    ti.q_tok = 0;
+    ti.k_tok = 0;
+    ti.nq = a.Nq;
+    ti.nk = a.Nk;
+    ti.tma_b = ti.b;
+  }
+  const int nkv_all = (ti.nk + BC - 1) / BC;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int first = ti.q_row0 + t * BR;
+    const int nr = min(max(ti.nq - first, 0), BR);
+    ti.nrows[t] = nr;
+    if (nr == 0) {
+      ti.nkv[t] = 0;
+    } else if (!CAUSAL) {
+      ti.nkv[t] = nkv_all;
+    } else {
+      const long long last_key = static_cast<long long>(first) + nr - 1 + ti.nk - ti.nq;
+      ti.nkv[t] = last_key < 0 ? 0 : min(static_cast<int>(last_key / BC) + 1, nkv_all);
+    }
+  }
+  return ti;
+}
+
+__device__ __forceinline__ bool varlen_bad(const PrefillArgs &a, int b) {
+  const int q0 = a.cu_q[b], q1 = a.cu_q[b + 1];
+  const int k0 = a.cu_k[b], k1 = a.cu_k[b + 1];
+  return q0 < 0 || q1 < q0 || q1 > a.total_q || k0 < 0 || k1 < k0 || k1 > a.total_k ||
+         (q1 - q0) > a.Nq;
+}
+
+// S_t = Q_t K^T: D/16 MMAs of 128 x 128 x 16.  Both operands K-major, 128B-swizzled:
+// k-step kk lives in box kk/4 at byte offset 32*(kk%4) inside each 128-byte row.
+template <int D>
+__device__ __forceinline__ void issue_s(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = static_cast<uint32_t>((kk >> 2) * BOX_BYTES + (kk & 3) * 32);
+    mma_bf16_ss(d_tmem, sw128_desc(q_smem + off, 16, 1024), sw128_desc(k_smem + off, 16, 1024),
+                Cfg<D>::IDESC_S, kk > 0 ? 1u : 0u);
+  }
+}
+
+// O_t (+)= P_t V: BC/16 MMAs of 128 x D x 16.  P from TMEM (8 columns of bf16 pairs per
+// k-step); V MN-major, 128B-swizzled: 16 keys = 2048 bytes per k-step, d halves one box apart.
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_smem,
+                                         bool accumulate) {
+#pragma unroll
+  for (int kk = 0; kk < BC / 16; ++kk) {
+    mma_bf16_ts(o_tmem, p_tmem + static_cast<uint32_t>(kk * 8),
+                sw128_desc(v_smem + static_cast<uint32_t>(kk * 16 * 128), BOX_BYTES, 1024),
+                Cfg<D>::IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+// ------------------------------------------------------------------------------------
+// Producer: Q tiles and the K/V ring (ring order K_0, V_0, K_1, V_1, ...).
+
+template <int D, bool CAUSAL>
+__device__ void producer_role(const PrefillArgs &a, const CUtensorMap *tmq,
+                              const CUtensorMap *tmk, const CUtensorMap *tmv, uint8_t *smem,
+                              Bars *bars, const WaitCtl &wc) {
+  using C = Cfg<D>;
+  uint32_t kv_iter = 0, q_iter = 0;
+  for (int tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x) {
+    const TileInfo ti = tile_info<CAUSAL>(a, tile);
+    if (a.varlen && (ti.q_row0 == 0) && varlen_bad(a, ti.b)) atomicOr(a.err, DEVERR_BAD_CU_SEQLENS);
+    const int n = max(ti.nkv[0], ti.nkv[1]);
+    if (n == 0) continue;
+    if (q_iter > 0 && !mbar_wait(&bars->q_empty, (q_iter - 1) & 1u, wc)) goto out;
+    mbar_arrive_expect_tx(&bars->q_full, 2 * C::TILE_BYTES);
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+#pragma unroll
+      for (int c = 0; c < C::KCH; ++c)
+        tma_load_4d(smem + C::Q_OFF + t * C::TILE_BYTES + c * BOX_BYTES, tmq, &bars->q_full,
+                    c * 64, ti.h, ti.q_tok + ti.q_row0 + t * BR, ti.tma_b);
+    ++q_iter;
+    for (int j = 0; j < n; ++j) {
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const int slot = static_cast<int>(kv_iter % C::NSLOTS);
+        const uint32_t use = kv_iter / C::NSLOTS;
+        if (!mbar_wait(&bars->kv_empty[slot], (use & 1u) ^ 1u, wc)) goto out;
+        mbar_arrive_expect_tx(&bars->kv_full[slot], C::TILE_BYTES);
+#pragma unroll
+        for (int c = 0; c < C::KCH; ++c)
+          tma_load_4d(smem + C::RING_OFF + slot * C::TILE_BYTES + c * BOX_BYTES,
+                      which ? tmv : tmk, &bars->kv_full[slot], c * 64, ti.hk, ti.k_tok + j * BC,
+                      ti.tma_b);
+        ++kv_iter;
+      }
+    }
+  }
+out:
+  // Teardown: let every bulk copy this thread issued land before the CTA may exit.
+  for (int s = 0; s < C::NSLOTS; ++s) {
+    if (kv_iter > static_cast<uint32_t>(s)) {
+      const uint32_t uses = (kv_iter - 1 - s) / C::NSLOTS + 1;
+      mbar_wait_teardown(&bars->kv_full[s], (uses - 1) & 1u, 1000000000ull);
+    }
+  }
+  if (q_iter > 0) mbar_wait_teardown(&bars->q_full, (q_iter - 1) & 1u, 1000000000ull);
+}
+
+// ------------------------------------------------------------------------------------
+// MMA issuer.  Order per K/V step j (both sub-tiles):
+//   PV_0(j), S_0(j+1), PV_1(j), S_1(j+1)
+// so that each softmax group finds its next S ready while the tensor core works on the
+// other sub-tile.  tcgen05.mma executes in issue order, so S_t(j+1) may overwrite the
+// TMEM columns that PV_t(j) reads P_t(j) from.
+
+template <int D, bool CAUSAL>
+__device__ void mma_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, uint32_t tmem,
+                         const WaitCtl &wc) {
+  using C = Cfg<D>;
+  uint32_t kv_iter = 0, q_iter = 0;
+  uint32_t p_phase[2] = {0u, 0u}, oe_phase[2] = {0u, 0u};
+  bool o_pending[2] = {false, false};
+  const uint32_t q_smem[2] = {smem_u32(smem + C::Q_OFF), smem_u32(smem + C::Q_OFF + C::TILE_BYTES)};
+  const uint32_t ring = smem_u32(smem + C::RING_OFF);
+  for (int tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x) {
+    const TileInfo ti = tile_info<CAUSAL>(a, tile);
+    const int n = max(ti.nkv[0], ti.nkv[1]);
+    if (n == 0) continue;
+    if (!mbar_wait(&bars->q_full, q_iter & 1u, wc)) goto out;
+    ++q_iter;
+    {
+      int slot_k = static_cast<int>(kv_iter % C::NSLOTS);
+      if (!mbar_wait(&bars->kv_full[slot_k], (kv_iter / C::NSLOTS) & 1u, wc)) goto out;
+      ++kv_iter;
+      tc_fence_after();
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        if (ti.nkv[t] > 0) {
+          issue_s<D>(tmem + s_col(t), q_smem[t], ring + slot_k * C::TILE_BYTES);
+          mma_commit(&bars->s_full[t]);
+        }
+      }
+      mma_commit(&bars->kv_empty[slot_k]);
+      for (int j = 0; j < n; ++j) {
+        const int slot_v = static_cast<int>(kv_iter % C::NSLOTS);
+        if (!mbar_wait(&bars->kv_full[slot_v], (kv_iter / C::NSLOTS) & 1u, wc)) goto out;
+        ++kv_iter;
+        slot_k = -1;
+        if (j + 1 < n) {
+          slot_k = static_cast<int>(kv_iter % C::NSLOTS);
+          if (!mbar_wait(&bars->kv_full[slot_k], (kv_iter / C::NSLOTS) & 1u, wc)) goto out;
+          ++kv_iter;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (j < ti.nkv[t]) {
+            if (j == 0 && o_pending[t]) {
+              // O_t still holds the previous tile's result until its epilogue has read it.
+              if (!mbar_wait(&bars->o_empty[t], oe_phase[t], wc)) goto out;
+              oe_phase[t] ^= 1u;
+              o_pending[t] = false;
+            }
+            if (!mbar_wait(&bars->p_ready[t], p_phase[t], wc)) goto out;
+            p_phase[t] ^= 1u;
+            tc_fence_after();
+            issue_pv<D>(tmem + o_col(t), tmem + s_col(t), ring + slot_v * C::TILE_BYTES, j > 0);
+            if (j == ti.nkv[t] - 1) {
+              mma_commit(&bars->o_full[t]);
+              o_pending[t] = true;
+            }
+          }
+          if (t == 1) mma_commit(&bars->kv_empty[slot_v]);
+          if (j + 1 < ti.nkv[t]) {
+            issue_s<D>(tmem + s_col(t), q_smem[t], ring + slot_k * C::TILE_BYTES);
+            mma_commit(&bars->s_full[t]);
+          }
+        }
+        if (slot_k >= 0) mma_commit(&bars->kv_empty[slot_k]);
+      }
+    }
+    mma_commit(&bars->q_empty);
+  }
+out:
+  // Teardown: every MMA issued so far must finish before TMEM is released.
+  mma_commit(&bars->mma_done);
+  mbar_wait_teardown(&bars->mma_done, 0u, 1000000000ull);
+}
+
+// ------------------------------------------------------------------------------------
+// Softmax / correction / epilogue: one thread per query row of its sub-tile.
+
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const WaitCtl &wc) {
+  const bool ok = mbar_wait(bar, parity, wc);
+  return __all_sync(0xffffffffu, ok);
+}
+
+template <int D, bool CAUSAL>
+__device__ void softmax_role(const PrefillArgs &a, Bars *bars, uint32_t tmem, const WaitCtl &wc,
+                             int warp, int lane) {
+  const int t = warp >> 2;
+  const int wq = warp & 3;
+  const int rit = wq * 32 + lane;  // row inside the sub-tile = TMEM lane
+  const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+  const uint32_t tS = tmem + lane_off + s_col(t);
+  const uint32_t tO = tmem + lane_off + o_col(t);
+  const float c = a.scale_log2;
+  uint32_t s_phase = 0, o_phase = 0;
+  __nv_bfloat16 *obase = reinterpret_cast<__nv_bfloat16 *>(a.o);
+
+  for (int tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x) {
+    const TileInfo ti = tile_info<CAUSAL>(a, tile);
+    if (ti.nrows[t] == 0) continue;
+    const int nkv = ti.nkv[t];
+    const int first_row = ti.q_row0 + t * BR;
+    const int row = first_row + rit;
+    const bool row_ok = rit < ti.nrows[t];
+    // Last key index this row may see, and the smallest such index over the sub-tile.
+    const int limit = CAUSAL ? min(row + ti.nk - ti.nq, ti.nk - 1) : ti.nk - 1;
+    const int min_limit = CAUSAL ? min(first_row + ti.nk - ti.nq, ti.nk - 1) : ti.nk - 1;
+
+    float m = -INFINITY, l = 0.f;
+    for (int j = 0; j < nkv; ++j) {
+      if (!warp_wait(&bars->s_full[t], s_phase, wc)) return;
+      s_phase ^= 1u;
+      tc_fence_after();
+      float s[BC];
+      {
+        uint32_t r[64];
+        tmem_ld_x64(tS, r);
+#pragma unroll
+        for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(r[i]);
+        tmem_ld_x64(tS + 64, r);
+#pragma unroll
+        for (int i = 0; i < 64; ++i) s[64 + i] = __uint_as_float(r[i]);
+      }
+      const int kbase = j * BC;
+      if (kbase + BC - 1 > min_limit) {
+        const int lim = limit - kbase;
+#pragma unroll
+        for (int i = 0; i < BC; ++i)
+          if (i > lim) s[i] = -INFINITY;
+      }
+      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+      for (int i = 4; i < BC; i += 4) {
+        mx0 = fmaxf(mx0, s[i]);
+        mx1 = fmaxf(mx1, s[i + 1]);
+        mx2 = fmaxf(mx2, s[i + 2]);
+        mx3 = fmaxf(mx3, s[i + 3]);
+      }
+      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+      const float m_new = fmaxf(m, mx * c);
+      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      float alpha = 1.f;
+      if (j > 0) {
+        const bool grow = m_new > m;
+        if (grow) alpha = ex2_approx(m - m_use);
+        if (__any_sync(0xffffffffu, grow)) {
+          // Conditional rescale of the O accumulator held in TMEM.  PV_t(j-1) has
+          // completed: its commit precedes the one that signalled S_t(j).
+#pragma unroll
+          for (int cc = 0; cc < D; cc += 32) {
+            uint32_t r[32];
+            tmem_ld_x32(tO + cc, r);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+            tmem_st_x32(tO + cc, r);
+          }
+        }
+      }
+      const float neg = -m_use;
+      float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+      uint32_t p[64];
+#pragma unroll
+      for (int i = 0; i < 64; i += 2) {
+        const float p0 = ex2_approx(fmaf(s[2 * i], c, neg));
+        const float p1 = ex2_approx(fmaf(s[2 * i + 1], c, neg));
+        const float p2 = ex2_approx(fmaf(s[2 * i + 2], c, neg));
+        const float p3 = ex2_approx(fmaf(s[2 * i + 3], c, neg));
+        l0 += p0;
+        l1 += p1;
+        l2 += p2;
+        l3 += p3;
+        p[i] = pack_bf16x2(p0, p1);
+        p[i + 1] = pack_bf16x2(p2, p3);
+      }
+      l = l * alpha + ((l0 + l1) + (l2 + l3));
+      {
+        uint32_t (&p0)[32] = *reinterpret_cast<uint32_t (*)[32]>(&p[0]);
+        uint32_t (&p1)[32] = *reinterpret_cast<uint32_t (*)[32]>(&p[32]);
+        tmem_st_x32(tS, p0);
+        tmem_st_x32(tS + 32, p1);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars->p_ready[t]);
+      m = m_new;
+    }
+
+    // Epilogue: O / l -> bf16, LSE = ln2 * (m + log2 l).
+    const int64_t tok = static_cast<int64_t>(ti.q_tok) + row;
+    __nv_bfloat16 *orow = obase + static_cast<int64_t>(ti.b) * a.o_sb + tok * a.o_sn +
+                          static_cast<int64_t>(ti.h) * a.o_sh;
+    if (nkv > 0) {
+      if (!warp_wait(&bars->o_full[t], o_phase, wc)) return;
+      o_phase ^= 1u;
+      tc_fence_after();
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+      for (int cc = 0; cc < D; cc += 32) {
+        uint32_t r[32];
+        tmem_ld_x32(tO + cc, r);
+        if (row_ok) {
+          uint4 *dst = reinterpret_cast<uint4 *>(orow + cc);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv_l, __uint_as_float(r[8 * v + 1]) * inv_l);
+            w.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv_l, __uint_as_float(r[8 * v + 3]) * inv_l);
+            w.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv_l, __uint_as_float(r[8 * v + 5]) * inv_l);
+            w.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv_l, __uint_as_float(r[8 * v + 7]) * inv_l);
+            dst[v] = w;
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->o_empty[t]);
+    } else if (row_ok) {
+      uint4 *dst = reinterpret_cast<uint4 *>(orow);
+#pragma unroll
+      for (int v = 0; v < D / 8; ++v) dst[v] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (row_ok) {
+      const float lse = l > 0.f ? (m + log2f(l)) * LN2 : -INFINITY;
+      a.lse[static_cast<int64_t>(ti.b) * a.lse_sb + static_cast<int64_t>(ti.h) * a.lse_sh + tok] = lse;
+    }
+  }
+}
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                   const __grid_constant__ CUtensorMap tmv, const PrefillArgs a) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  Bars *bars = reinterpret_cast<Bars *>(smem + C::BAR_OFF);
+  const int warp = static_cast<int>(threadIdx.x) >> 5;
+  const int lane = static_cast<int>(threadIdx.x) & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 1);
+    for (int s = 0; s < C::NSLOTS; ++s) {
+      mbar_init(&bars->kv_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->p_ready[t], 128);
+      mbar_init(&bars->o_full[t], 1);
+      mbar_init(&bars->o_empty[t], 128);
+    }
+    mbar_init(&bars->mma_done, 1);
+    bars->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == PRODUCER_WARP && lane == 0) {
+    tma_prefetch_desc(&tmq);
+    tma_prefetch_desc(&tmk);
+    tma_prefetch_desc(&tmv);
+  }
+  if (warp == MMA_WARP) {
+    tmem_alloc(&bars->tmem_base, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const WaitCtl wc{&bars->abort, a.err, a.timeout_ns, DEVERR_PREFILL_TIMEOUT};
+
+  if (warp < PRODUCER_WARP) {
+    softmax_role<D, CAUSAL>(a, bars, tmem, wc, warp, lane);
+  } else if (warp == PRODUCER_WARP) {
+    if (lane == 0) producer_role<D, CAUSAL>(a, &tmq, &tmk, &tmv, smem, bars, wc);
+  } else {
+    if (lane == 0) mma_role<D, CAUSAL>(a, smem, bars, tmem, wc);
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_impl(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                        const PrefillArgs &a, int grid, cudaStream_t stream) {
+  constexpr int smem = Cfg<D>::SMEM_BYTES;
+  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, CAUSAL>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  prefill_kernel<D, CAUSAL><<<grid, NTHREADS, smem, stream>>>(tq, tk, tv, a);
+  return cudaGetLastError();
+}
+
+// O = 0 and LSE = -inf for B x N x H rows.
+__global__ void fill_empty_kernel(__nv_bfloat16 *o, float *lse, int B, int N, int H, int d,
+                                  int64_t o_sb, int64_t o_sn, int64_t o_sh, int64_t lse_sb,
+                                  int64_t lse_sh) {
+  const int64_t rows = static_cast<int64_t>(B) * N * H;
+  for (int64_t r = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; r < rows;
+       r += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int h = static_cast<int>(r % H);
+    const int64_t bn = r / H;
+    const int n = static_cast<int>(bn % N);
+    const int b = static_cast<int>(bn / N);
+    __nv_bfloat16 *orow = o + b * o_sb + n * o_sn + h * o_sh;
+    for (int c = 0; c < d; ++c) orow[c] = __float2bfloat16(0.f);
+    lse[b * lse_sb + h * lse_sh + n] = -INFINITY;
+  }
+}
+
+}  // namespace
+
+int prefill_smem_bytes(int d) { return d == 64 ? Cfg<64>::SMEM_BYTES : Cfg<128>::SMEM_BYTES; }
+
+cudaError_t launch_prefill(int d, bool causal, const CUtensorMap &tq, const CUtensorMap &tk,
+                           const CUtensorMap &tv, const PrefillArgs &a, int grid,
+                           cudaStream_t stream) {
+  if (d == 64) {
+    return causal ? launch_impl<64, true>(tq, tk, tv, a, grid, stream)
+                  : launch_impl<64, false>(tq, tk, tv, a, grid, stream);
+  }
+  return causal ? launch_impl<128, true>(tq, tk, tv, a, grid, stream)
+                : launch_impl<128, false>(tq, tk, tv, a, grid, stream);
+}
+
+cudaError_t launch_fill_empty(void *o, float *lse, int B, int N, int H, int d, int64_t o_sb,
+                              int64_t o_sn, int64_t o_sh, int64_t lse_sb, int64_t lse_sh,
+                              cudaStream_t stream) {
+  const int64_t rows = static_cast<int64_t>(B) * N * H;
+  if (rows == 0) return cudaSuccess;
+  const int threads = 256;
+  const int blocks = static_cast<int>(std::min<int64_t>((rows + threads - 1) / threads, 4096));
+  fill_empty_kernel<<<blocks, threads, 0, stream>>>(reinterpret_cast<__nv_bfloat16 *>(o), lse, B,
+                                                    N, H, d, o_sb, o_sn, o_sh, lse_sb, lse_sh);
+  return cudaGetLastError();
+}
+
+}  // namespace fa

@@ -1,0 +1,164 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) exact-attention forward library, libfa.so.
+ *
+ * The library computes exact scaled-dot-product attention and the per-row
+ * log-sum-exp:
+ *     O   = softmax(scale * Q K^T) V
+ *     LSE = ln( sum_j exp(scale * q . k_j) )       (natural log, one value per query row)
+ * ("FlashAttention 1-4 详解" (pinghaoyang.com.cn), section 原算法 for the definition;
+ *  "flash-attention" (ai-reference-codex.pages.dev), sections 2.1 and 2.3 for the
+ *  out + softmax_lse pair written by the fused forward kernel.)
+ * It never materialises the N x N score or probability matrices: every call runs a
+ * fused kernel that keeps the online-softmax state (running max m, running sum l,
+ * rescaled output accumulator; "FlashAttention 1-4 详解", section Online Softmax
+ * 数学推导) on chip.
+ *
+ * Conventions shared by every call
+ *   - Element type: Q, K, V and O are bf16 (IEEE bfloat16 bit patterns); LSE is fp32.
+ *   - Head dimension d must be 64 or 128 (a subset of the upstream limit "d <= 256 and
+ *     a multiple of 8" -- "flash-attention", section 5).
+ *   - Grouped-query attention: Hkv must divide Hq; query head h reads key/value head
+ *     h / (Hq / Hkv) ("flash-attention", capabilities table, MQA / GQA row).
+ *   - Causal masking is aligned bottom-right: query i of Nq sees key j of Nk when
+ *     j <= i + (Nk - Nq).  Rows that see no key produce O = 0 and LSE = -inf.
+ *   - All pointers are caller-owned DEVICE memory (unless stated otherwise).  The library
+ *     does not allocate, free or synchronise: it validates, then enqueues kernels on the
+ *     caller's stream and returns.  Outputs are valid once that stream reaches them.
+ *   - Alignment (TMA): q, k, v, k_cache and v_cache must be 16-byte aligned and every
+ *     stride a multiple of 8 elements; o must be 16-byte aligned with strides a
+ *     multiple of 8 elements; lse 4-byte aligned.
+ *   - Errors: arguments are validated on the host before any CUDA call; an invalid call
+ *     returns a non-zero fa_status and enqueues nothing.  FA_ERR_CUDA means a CUDA call
+ *     failed; fa_last_cuda_error() gives its text.  Faults detected on the device (a
+ *     bounded wait that ran out, an out-of-range sequence length) are recorded in a
+ *     per-device error word that fa_get_last_device_error() reads.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fa_status {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1, /* null pointer, bad size, Hq % Hkv != 0, misaligned pointer/stride */
+    FA_ERR_UNSUPPORTED = 2, /* d not in {64, 128}, decode group size not in {1,2,4,8},
+                               or the current device is not an sm_103 GPU */
+    FA_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed: see fa_last_cuda_error() */
+    FA_ERR_WORKSPACE = 4,   /* workspace pointer null or smaller than required */
+    FA_ERR_TIMEOUT = 5      /* a device-side wait gave up (reported by fa_get_last_device_error) */
+} fa_status;
+
+/*
+ * Dense batched attention, the flash_attn_func call of "flash-attention" section 1:
+ * q/k/v in the (batch, seqlen, nheads, headdim) layout.
+ *   q   : [B, Nq, Hq,  d] bf16, element (b,n,h,c) at q + b*q_strides[0] + n*q_strides[1]
+ *                                                    + h*q_strides[2] + c
+ *   k, v: [B, Nk, Hkv, d] bf16, same convention with k_strides / v_strides
+ *   o   : [B, Nq, Hq,  d] bf16 output, same convention with o_strides
+ *   lse : [B, Hq, Nq] fp32 output, contiguous
+ * Strides are in elements; the head dimension has unit stride.
+ * scale multiplies the scores before the softmax (usually 1/sqrt(d)); causal != 0
+ * applies the bottom-right causal mask.  Nk = 0 is allowed (O = 0, LSE = -inf);
+ * B = 0 or Nq = 0 is a no-op.
+ */
+typedef struct fa_fwd_params {
+    const void *q;
+    const void *k;
+    const void *v;
+    void *o;
+    float *lse;
+    int B, Nq, Nk, Hq, Hkv, d;
+    int64_t q_strides[3], k_strides[3], v_strides[3], o_strides[3]; /* (b, n, h) */
+    float scale;
+    int causal;
+} fa_fwd_params;
+
+fa_status fa_fwd(const fa_fwd_params *p, cudaStream_t stream);
+
+/*
+ * Packed variable-length batch, the flash_attn_varlen_func call of "flash-attention"
+ * section 1 (capabilities table, varlen row: sequences packed by cu_seqlens).
+ *   q   : [total_q, Hq,  d] bf16, contiguous
+ *   k, v: [total_k, Hkv, d] bf16, contiguous
+ *   cu_seqlens_q, cu_seqlens_k: DEVICE int32 [B+1] prefix sums; sequence b owns query
+ *         tokens [cu_seqlens_q[b], cu_seqlens_q[b+1]) and key tokens likewise.  They must
+ *         start at 0, be non-decreasing and end at most at total_q / total_k; sequence
+ *         b's query length must not exceed max_seqlen_q.  A sequence that breaks this is
+ *         skipped and flagged in the device error word (FA_ERR_INVALID_ARG from
+ *         fa_get_last_device_error).
+ *   o   : [total_q, Hq, d] bf16 output, contiguous
+ *   lse : [Hq, total_q] fp32 output, contiguous
+ * Each sequence is attended on its own; causal alignment is per sequence.
+ */
+fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                        const int *cu_seqlens_q, const int *cu_seqlens_k, int B,
+                        int max_seqlen_q, int max_seqlen_k, int total_q, int total_k, int Hq,
+                        int Hkv, int d, float scale, int causal, cudaStream_t stream);
+
+/*
+ * Single-query decode against a padded KV cache, the flash_attn_with_kvcache call of
+ * "flash-attention" section 1, computed with split-KV: the keys of each sequence are cut
+ * into chunks, every (batch, kv head, chunk) writes a partial (O_s, LSE_s) to the
+ * workspace, and a combine kernel merges them with weights exp(LSE_s - LSE)
+ * ("flash-attention", code map: combine_attn_seqk_parallel; section 4 on folding the
+ * query heads of one GQA group into one work unit).
+ *   q            : [B, 1, Hq, d] bf16, contiguous
+ *   k_cache/v_cache: [B, Lmax, Hkv, d] bf16 with element strides cache_strides (b, n, h)
+ *                  (host array of 3), shared by both caches
+ *   cache_seqlens: DEVICE int32 [B]; query b sees cache rows [0, cache_seqlens[b]).
+ *                  Rows at or past that length are never read into the result.  A length
+ *                  outside [0, Lmax] is clamped and flagged in the device error word.
+ *   num_splits   : 0 picks the chunk length automatically; n > 0 uses chunks of
+ *                  ceil(Lmax / n) keys rounded up to a multiple of 128.
+ *   workspace    : DEVICE scratch of at least fa_fwd_kvcache_workspace_size(...) bytes,
+ *                  256-byte aligned; owned by the caller, overwritten by the call.
+ *   o            : [B, 1, Hq, d] bf16 output, contiguous
+ *   lse          : [B, Hq] fp32 output, contiguous
+ * Hq / Hkv must be 1, 2, 4 or 8.
+ */
+size_t fa_fwd_kvcache_workspace_size(int B, int Hq, int Lmax, int d, int num_splits);
+
+fa_status fa_fwd_kvcache(const void *q, const void *k_cache, const void *v_cache,
+                         const int *cache_seqlens, int B, int Lmax, int Hq, int Hkv, int d,
+                         const int64_t cache_strides[3], float scale, int num_splits,
+                         void *workspace, size_t workspace_bytes, void *o, float *lse,
+                         cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's error word.
+ * Returns FA_OK when no kernel recorded a fault since the last read, FA_ERR_TIMEOUT when a
+ * bounded device-side wait gave up (the kernel then stopped early and its outputs are
+ * not valid), FA_ERR_INVALID_ARG when a device-resident argument (cu_seqlens,
+ * cache_seqlens) was out of range, FA_ERR_CUDA if the synchronisation itself failed.
+ */
+fa_status fa_get_last_device_error(cudaStream_t stream);
+
+/* sizeof(fa_fwd_params), so that foreign-language bindings can check their struct layout. */
+size_t fa_fwd_params_size(void);
+
+/* Static text for a status code. */
+const char *fa_status_string(fa_status s);
+
+/* Text of the last CUDA error seen by this thread inside the library ("" if none). */
+const char *fa_last_cuda_error(void);
+
+/*
+ * Limit, in nanoseconds, on every device-side wait of the kernels launched after this
+ * call (process-wide).  0 restores the default (10 s).  Testing aid: a very small value
+ * makes the waits give up and return FA_ERR_TIMEOUT through fa_get_last_device_error
+ * instead of computing, without faulting the GPU.
+ */
+void fa_set_wait_timeout_ns(unsigned long long ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

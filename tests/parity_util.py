@@ -1,0 +1,58 @@
+"""Helpers shared by the GPU parity tests: tolerances and comparisons.
+
+The bar for every call (dense, varlen, decode) is the one the exact-attention forward
+pass is held to: max|O - O_ref| <= 1e-2, mean|O - O_ref| <= 1e-3 and
+max|LSE - LSE_ref| <= 1e-3, with O_ref and LSE_ref from the fp64 oracle on the same
+bf16 inputs.  Rows that see no key must give O = 0 exactly and LSE = -inf.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+O_MAX_TOL = 1e-2
+O_MEAN_TOL = 1e-3
+LSE_TOL = 1e-3
+
+
+def to_np(t: torch.Tensor) -> np.ndarray:
+    return t.detach().to(torch.float64).cpu().numpy()
+
+
+def compare(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
+    """o_* broadcastable [..., d], lse_* [...] with matching row order."""
+    o = to_np(o_gpu) if isinstance(o_gpu, torch.Tensor) else np.asarray(o_gpu, np.float64)
+    lse = to_np(lse_gpu) if isinstance(lse_gpu, torch.Tensor) else np.asarray(lse_gpu, np.float64)
+    o_ref = np.asarray(o_ref, np.float64)
+    lse_ref = np.asarray(lse_ref, np.float64)
+    assert o.shape == o_ref.shape, f"{what}: O shape {o.shape} vs {o_ref.shape}"
+    assert lse.shape == lse_ref.shape, f"{what}: LSE shape {lse.shape} vs {lse_ref.shape}"
+    assert np.all(np.isfinite(o)), f"{what}: non-finite O"
+    empty = ~np.isfinite(lse_ref)
+    assert np.array_equal(~np.isfinite(lse), empty), f"{what}: -inf LSE rows differ"
+    assert np.all(lse[empty] == -np.inf), f"{what}: empty rows must have LSE = -inf"
+    if empty.any():
+        assert np.all(o[empty] == 0.0), f"{what}: empty rows must have O = 0"
+    err = np.abs(o - o_ref)
+    max_o, mean_o = float(err.max(initial=0.0)), float(err.mean()) if err.size else 0.0
+    fin = ~empty
+    max_l = float(np.abs(lse[fin] - lse_ref[fin]).max(initial=0.0))
+    assert max_o <= O_MAX_TOL, f"{what}: max|dO| = {max_o:.3e} > {O_MAX_TOL}"
+    assert mean_o <= O_MEAN_TOL, f"{what}: mean|dO| = {mean_o:.3e} > {O_MEAN_TOL}"
+    assert max_l <= LSE_TOL, f"{what}: max|dLSE| = {max_l:.3e} > {LSE_TOL}"
+    return {"max_abs_o": max_o, "mean_abs_o": mean_o, "max_abs_lse": max_l}
+
+
+def sample_rows(B, H, N, n, seed, must=()):
+    """(b, h, i) triples: tile edges of every (b, h) subset plus random rows."""
+    rng = np.random.default_rng(seed)
+    rows = set(tuple(r) for r in must)
+    edges = [0, 1, 127, 128, 129, 255, 256, N // 2, N - 129, N - 128, N - 2, N - 1]
+    for b in range(B):
+        for h in range(H):
+            for i in rng.choice(edges, size=2, replace=False):
+                if 0 <= i < N:
+                    rows.add((b, h, int(i)))
+    while len(rows) < n + len(must):
+        rows.add((int(rng.integers(B)), int(rng.integers(H)), int(rng.integers(N))))
+    return np.array(sorted(rows), dtype=np.int32)

@@ -1,0 +1,132 @@
+"""CPU tests of the C ABI: libfa.so builds for sm_103a, loads, exports every function that
+include/fa.h declares, and rejects bad arguments on the host before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from exact_attention_81_gb300 import build
+    build.build()
+    import exact_attention_81_gb300 as fa
+    return fa.load_library()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "fa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_symbols_exported(lib):
+    names = _declared_functions()
+    assert "fa_fwd" in names and "fa_fwd_varlen" in names and "fa_fwd_kvcache" in names
+    for n in names:
+        assert hasattr(lib, n), f"libfa.so does not export {n}"
+
+
+def test_struct_layout(lib):
+    from exact_attention_81_gb300._binding import FwdParams
+    assert lib.fa_fwd_params_size() == ctypes.sizeof(FwdParams)
+
+
+def _params(**kw):
+    from exact_attention_81_gb300._binding import FwdParams
+    p = FwdParams()
+    p.q = p.k = p.v = p.o = 4096
+    p.lse = 4096
+    p.B, p.Nq, p.Nk, p.Hq, p.Hkv, p.d = 1, 128, 128, 4, 2, 128
+    for name in ("q_strides", "k_strides", "v_strides", "o_strides"):
+        getattr(p, name)[:] = [128 * 4 * 128, 4 * 128, 128]
+    p.scale = 0.088
+    p.causal = 0
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+@pytest.mark.parametrize("change,status", [
+    ({"d": 96}, 2), ({"d": 256}, 2), ({"Hkv": 3}, 1), ({"Hq": 0}, 1), ({"B": -1}, 1),
+    ({"scale": 0.0}, 1), ({"scale": float("nan")}, 1), ({"scale": -1.0}, 1),
+    ({"q": 4098}, 1), ({"o": 4100}, 1), ({"lse": 4098}, 1), ({"q": None}, 1),
+    ({"k": None}, 1), ({"Nq": -5}, 1),
+])
+def test_fwd_rejects_bad_arguments(lib, change, status):
+    p = _params(**change)
+    assert lib.fa_fwd(ctypes.byref(p), None) == status
+
+
+def test_fwd_rejects_misaligned_stride(lib):
+    p = _params()
+    p.q_strides[1] = 4 * 128 + 4  # not a multiple of 8 elements
+    assert lib.fa_fwd(ctypes.byref(p), None) == 1
+
+
+def test_fwd_empty_batch_is_noop(lib):
+    assert lib.fa_fwd(ctypes.byref(_params(B=0)), None) == 0
+    assert lib.fa_fwd(ctypes.byref(_params(Nq=0)), None) == 0
+    assert lib.fa_fwd(None, None) == 1
+
+
+def test_varlen_rejects_bad_arguments(lib):
+    f = lib.fa_fwd_varlen
+    good = dict(q=4096, k=4096, v=4096, o=4096, lse=4096, cq=4096, ck=4096, B=2, mq=10, mk=10,
+                tq=20, tk=20, Hq=4, Hkv=2, d=64, scale=0.1, causal=1)
+
+    def call(**kw):
+        a = dict(good, **kw)
+        return f(a["q"], a["k"], a["v"], a["o"], a["lse"], a["cq"], a["ck"], a["B"], a["mq"],
+                 a["mk"], a["tq"], a["tk"], a["Hq"], a["Hkv"], a["d"], a["scale"], a["causal"],
+                 None)
+
+    assert call(d=80) == 2
+    assert call(Hkv=3) == 1
+    assert call(cq=None) == 1
+    assert call(q=4097) == 1
+    assert call(tq=-1) == 1
+    assert call(B=0) == 0
+    assert call(tq=0) == 0
+
+
+def test_kvcache_rejects_bad_arguments(lib):
+    strides = (ctypes.c_int64 * 3)(1024 * 8 * 128, 8 * 128, 128)
+
+    def call(**kw):
+        a = dict(q=4096, kc=4096, vc=4096, lens=4096, B=2, L=1024, Hq=32, Hkv=8, d=128,
+                 scale=0.1, ns=0, ws=4096, wsb=1 << 30, o=4096, lse=4096)
+        a.update(kw)
+        return lib.fa_fwd_kvcache(a["q"], a["kc"], a["vc"], a["lens"], a["B"], a["L"], a["Hq"],
+                                  a["Hkv"], a["d"], strides, a["scale"], a["ns"], a["ws"],
+                                  a["wsb"], a["o"], a["lse"], None)
+
+    assert call(Hq=32, Hkv=2) == 2          # group of 16 not supported by decode
+    assert call(d=32) == 2
+    assert call(Hkv=5) == 1
+    assert call(ns=-1) == 1
+    assert call(lens=None) == 1
+    assert call(ws=None) == 4
+    need = lib.fa_fwd_kvcache_workspace_size(2, 32, 1024, 128, 0)
+    assert call(wsb=need - 1) == 4
+    assert call(ws=4096 + 16) == 4          # workspace must be 256-byte aligned
+    assert call(B=0) == 0
+
+
+def test_workspace_size(lib):
+    ws = lib.fa_fwd_kvcache_workspace_size
+    # automatic chunking: ~32 splits of a full-length cache, chunk >= 256, multiple of 128
+    assert ws(64, 32, 32768, 128, 0) == 64 * 32 * 32 * 129 * 4
+    assert ws(1, 1, 100, 64, 0) == ((1 * 1 * 1 * 65 * 4 + 255) // 256) * 256
+    assert ws(2, 4, 1000, 64, 3) == 2 * 4 * 3 * 65 * 4 // 256 * 256 + (256 if (2 * 4 * 3 * 65 * 4) % 256 else 0)
+    assert ws(0, 4, 100, 64, 0) == 0
+    assert ws(2, 4, 100, 64, -1) == 0
+
+
+def test_status_strings(lib):
+    lib.fa_status_string.restype = ctypes.c_char_p
+    for s in range(6):
+        assert lib.fa_status_string(s).decode().startswith("FA_")

@@ -1,0 +1,190 @@
+"""GPU parity of the dense and varlen prefill path (libfa.so through its C ABI) against the
+fp64 oracle, on seeded inputs: small cases compared element by element, the full-size
+workloads on sampled rows plus whole-output properties."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.oracle as ORACLE
+from exact_attention_81_gb300 import (FA_OK, fa_fwd, fa_fwd_varlen, get_last_device_error)
+from exact_attention_81_gb300.inputs import (WORKLOADS, dense_inputs, varlen_inputs,
+                                             workload_inputs)
+from tests.parity_util import compare, sample_rows, to_np
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def _run_dense(q, k, v, causal, scale=None):
+    o, lse = fa_fwd(q, k, v, causal=causal, scale=scale)
+    assert get_last_device_error() == FA_OK
+    return o, lse
+
+
+def _oracle_dense(q, k, v, causal, scale):
+    return ORACLE.attention(q.cpu(), k.cpu(), v.cpu(), scale, causal)
+
+
+# ------------------------------------------------------------------ small, full compare
+
+DENSE_CASES = [
+    # B, Nq, Nk, Hq, Hkv, d, causal
+    (1, 256, 256, 1, 1, 64, False),
+    (1, 256, 256, 1, 1, 64, True),
+    (2, 300, 300, 2, 2, 128, False),   # ragged tail (300 = 2*128 + 44)
+    (2, 300, 300, 2, 2, 128, True),
+    (1, 1, 1, 1, 1, 128, False),       # single row, single key
+    (1, 1, 1, 1, 1, 64, True),
+    (1, 100, 700, 2, 1, 128, True),    # Nq < Nk, bottom-right causal
+    (1, 700, 100, 2, 2, 64, True),     # Nq > Nk: leading rows see no key
+    (1, 129, 383, 3, 3, 128, False),
+    (2, 517, 517, 8, 2, 128, True),    # GQA 4:1, several tiles + tail
+    (1, 384, 384, 8, 1, 64, False),    # MQA 8:1
+    (1, 640, 640, 4, 4, 128, True),
+    (3, 64, 200, 4, 2, 64, False),
+]
+
+
+@pytest.mark.parametrize("case", DENSE_CASES, ids=lambda c: "B{}_q{}_k{}_h{}x{}_d{}_{}".format(
+    c[0], c[1], c[2], c[3], c[4], c[5], "causal" if c[6] else "full"))
+def test_dense_small(case):
+    B, Nq, Nk, Hq, Hkv, d, causal = case
+    q, k, v = dense_inputs(B, Nq, Nk, Hq, Hkv, d, seed=2000 + Nq + Nk + d, device=DEV)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = _run_dense(q, k, v, causal)
+    o_ref, lse_ref = _oracle_dense(q, k, v, causal, float(np.float32(scale)))
+    compare(o, lse, o_ref, lse_ref, f"dense {case}")
+
+
+def test_tiny_workload_and_golden_rows():
+    """The tiny workload (1 x 256 x 1 head, d = 64) in full, plus the stored oracle rows."""
+    import json
+    import os
+    w = WORKLOADS["tiny"]
+    q, k, v = workload_inputs(w, device=DEV)
+    o, lse = _run_dense(q, k, v, w.causal)
+    o_ref, lse_ref = _oracle_dense(q, k, v, w.causal, w.scale)
+    compare(o, lse, o_ref, lse_ref, "tiny")
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "tiny_rows.json")))
+    rows = g["rows"]
+    compare(o[0, rows, 0], lse[0, 0, rows], np.array(g["o"]), np.array(g["lse"]), "golden rows")
+
+
+def test_scale_argument():
+    q, k, v = dense_inputs(1, 200, 200, 2, 2, 128, seed=77, device=DEV)
+    for scale in (0.03, 0.5):
+        o, lse = _run_dense(q, k, v, True, scale=scale)
+        o_ref, lse_ref = _oracle_dense(q, k, v, True, float(np.float32(scale)))
+        compare(o, lse, o_ref, lse_ref, f"scale {scale}")
+
+
+def test_strided_views_and_guard_bands():
+    """Non-contiguous q/k/v/o views (a slice of a larger buffer) are honoured, and nothing
+    outside the output view is written."""
+    B, N, H, d = 2, 260, 3, 128
+    big_q = torch.randn(B, N, H + 2, d, device=DEV).to(torch.bfloat16)
+    big_k = torch.randn(B, N, H + 1, d, device=DEV).to(torch.bfloat16)
+    big_v = torch.randn(B, N, H + 1, d, device=DEV).to(torch.bfloat16)
+    q, k, v = big_q[:, :, 1:H + 1], big_k[:, :, :H], big_v[:, :, 1:]
+    guard = torch.full((B, N + 16, H + 2, d), 7.0, device=DEV, dtype=torch.bfloat16)
+    out = guard[:, 8:N + 8, 1:H + 1]
+    o, lse = fa_fwd(q, k, v, causal=True, out=out)
+    assert get_last_device_error() == FA_OK
+    o_ref, lse_ref = _oracle_dense(q.contiguous(), k.contiguous(), v.contiguous(), True,
+                                   float(np.float32(1 / math.sqrt(d))))
+    compare(o, lse, o_ref, lse_ref, "strided")
+    mask = torch.ones_like(guard, dtype=torch.bool)
+    mask[:, 8:N + 8, 1:H + 1] = False
+    assert torch.all(guard[mask] == 7.0), "write outside the output view"
+
+
+def test_empty_keys():
+    q, _, _ = dense_inputs(2, 50, 1, 2, 2, 64, seed=5, device=DEV)
+    k = torch.empty((2, 0, 2, 64), dtype=torch.bfloat16, device=DEV)
+    o, lse = _run_dense(q, k, k, False)
+    assert torch.all(o == 0) and torch.all(torch.isneginf(lse))
+
+
+def test_deterministic():
+    q, k, v = dense_inputs(2, 777, 777, 4, 2, 128, seed=9, device=DEV)
+    o1, l1 = _run_dense(q, k, v, True)
+    o2, l2 = _run_dense(q, k, v, True)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+# ------------------------------------------------------------------ varlen
+
+VARLEN_CASES = [
+    ([5, 0, 19, 333, 1, 128, 129, 256], [7, 3, 19, 333, 1, 128, 200, 256], 4, 2, 128),
+    ([1000, 17, 600], [1000, 17, 600], 2, 2, 64),
+    ([0, 0], [5, 0], 2, 1, 128),
+]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("case", VARLEN_CASES)
+def test_varlen(case, causal):
+    sq, sk, Hq, Hkv, d = case
+    q, k, v, cu_q, cu_k = varlen_inputs(sq, sk, Hq, Hkv, d, seed=31, device=DEV)
+    total_q = q.shape[0]
+    o_buf = torch.full((total_q + 8, Hq, d), 3.0, dtype=torch.bfloat16, device=DEV)
+    out = o_buf[4:total_q + 4]
+    o, lse = fa_fwd_varlen(q, k, v, cu_q, cu_k, max(sq), max(sk), causal=causal, out=out)
+    assert get_last_device_error() == FA_OK
+    o_ref, lse_ref = ORACLE.attention_varlen(q.cpu(), k.cpu(), v.cpu(), cu_q.cpu(), cu_k.cpu(),
+                                             float(np.float32(1 / math.sqrt(d))), causal)
+    if total_q:
+        compare(o, lse, o_ref, lse_ref, f"varlen {case} causal={causal}")
+    assert torch.all(o_buf[:4] == 3.0) and torch.all(o_buf[total_q + 4:] == 3.0)
+
+
+def test_varlen_matches_dense():
+    """A one-sequence varlen call equals the dense call bit for bit."""
+    q, k, v = dense_inputs(1, 500, 500, 4, 2, 128, seed=41, device=DEV)
+    o_d, l_d = _run_dense(q, k, v, True)
+    cu = torch.tensor([0, 500], dtype=torch.int32, device=DEV)
+    o_v, l_v = fa_fwd_varlen(q[0], k[0], v[0], cu, cu, 500, 500, causal=True)
+    assert torch.equal(o_v, o_d[0]) and torch.equal(l_v, l_d[0])
+
+
+def test_varlen_bad_cu_seqlens_flagged():
+    """Out-of-range prefix sums on the device are reported, not followed."""
+    from exact_attention_81_gb300 import FA_ERR_INVALID_ARG
+    q, k, v, _, _ = varlen_inputs([10, 10], [10, 10], 2, 2, 64, seed=3, device=DEV)
+    bad = torch.tensor([0, 10, 40], dtype=torch.int32, device=DEV)  # ends past total
+    fa_fwd_varlen(q, k, v, bad, bad, 30, 30)
+    assert get_last_device_error() == FA_ERR_INVALID_ARG
+    assert get_last_device_error() == FA_OK
+
+
+# ------------------------------------------------------------------ full-size workloads
+
+@pytest.mark.parametrize("name", ["dense2k", "causal8k", "gqa16k"])
+def test_full_size_workload(name):
+    """The benchmark workloads at full size, in the benchmark's launch configuration:
+    sampled rows against the oracle, plus properties of the whole output (finite, each O
+    a convex combination of V rows, LSE >= the largest visible score)."""
+    w = WORKLOADS[name]
+    q, k, v = workload_inputs(w, device=DEV)
+    o, lse = _run_dense(q, k, v, w.causal)
+    rows = sample_rows(w.B, w.Hq, w.Nq, 160, seed=w.seed)
+    o_ref, lse_ref = ORACLE.attention_rows(q.cpu(), k.cpu(), v.cpu(), rows, w.scale, w.causal)
+    r = torch.as_tensor(rows, dtype=torch.long)
+    o_s = o[r[:, 0], r[:, 2], r[:, 1]]
+    l_s = lse[r[:, 0], r[:, 1], r[:, 2]]
+    compare(o_s, l_s, o_ref, lse_ref, name)
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+    G = w.Hq // w.Hkv
+    vmax = v.float().amax(dim=1).repeat_interleave(G, dim=1)  # [B, Hq, d]
+    vmin = v.float().amin(dim=1).repeat_interleave(G, dim=1)
+    of = o.float()
+    assert (of <= vmax[:, None] + 1e-2).all() and (of >= vmin[:, None] - 1e-2).all()
+    # LSE >= scale * q_i . k_j for the diagonal key (always visible in the causal case)
+    if w.causal:
+        G = w.Hq // w.Hkv
+        kk = k.float().repeat_interleave(G, dim=2)
+        diag = (q.float() * kk).sum(-1) * w.scale  # [B, N, Hq]
+        assert (lse >= diag.transpose(1, 2) - 1e-3).all()
