@@ -1,0 +1,458 @@
+"""Benchmark of the exact-attention forward path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Headline: attention forward TFLOPS on the long causal prefill workload (B = 2, H = 32,
+N = 8192, d = 128, bf16, causal), FLOPs = 4 * Nq * Nk * d per (batch, head), halved for
+causal.  One step = one fa_fwd call over that whole workload with inputs resident in HBM
+(402 MB of Q/K/V, larger than the 129 MB L2).  The same JSON line also carries:
+  roofline      the prefill kernel against the measured dense bf16 peak
+  e2e           the same metric through the public call with pinned host buffers, the
+                host->device copies of Q/K/V and the device->host copy of O/LSE timed
+  cpu_baseline  the fp64 oracle on a bounded sample of rows, on this host's cores
+  extra         the other workloads (dense 2k, GQA 16k causal, split-KV decode) measured
+                the same way, decode against HBM bandwidth
+Under torchrun (N > 1) every rank runs the full workload on its own GPU (weak scaling;
+the (batch, head) units are independent, so there is no collective on the data path);
+the step time is the max over ranks.
+`--impl reference` times the fp64 CPU oracle instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+HEADLINE = "causal8k"
+METRIC = "attention fwd TFLOPS (bf16 causal N=8192 d=128) & % of GB300 BF16 peak"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def flops(w) -> float:
+    f = 4.0 * w.Nq * w.Nk * w.d * w.B * w.Hq
+    return f / 2 if w.causal else f
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return {"bf16": float(p["bf16_tflops"]), "bf16_sustained": float(p["bf16_tflops_sustained"]),
+                "hbm": float(p["hbm_gbs"]), "basis": "measured"}
+    except Exception:
+        return {"bf16": 1900.0, "bf16_sustained": 1700.0, "hbm": 6800.0, "basis": "fallback"}
+
+
+def source_hash(files) -> str:
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:12]
+
+
+PREFILL_SRC = ["exact_attention_81_gb300/csrc/fa_prefill.cu", "exact_attention_81_gb300/csrc/ptx.cuh"]
+DECODE_SRC = ["exact_attention_81_gb300/csrc/fa_decode.cu", "exact_attention_81_gb300/csrc/ptx.cuh"]
+
+
+def profiled_traffic(kernel: str, src_files, workload: str):
+    """DRAM bytes per launch recorded under profiles/ for this kernel, or None when no
+    capture exists for the current source of the kernel."""
+    path = os.path.join(ROOT, "profiles", "traffic.md")
+    if not os.path.exists(path):
+        return None
+    want = source_hash(src_files)
+    pat = re.compile(r"^\|\s*" + re.escape(kernel) + r"\s*\|\s*" + re.escape(workload) +
+                     r"\s*\|\s*([0-9a-f]+)\s*\|\s*([0-9.eE+]+)\s*\|")
+    for line in open(path):
+        m = pat.match(line.strip())
+        if m and m.group(1) == want:
+            return float(m.group(2))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling in the background (200 ms period)."""
+
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        rows = []
+        for ts, line in self.samples:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                rows.append((ts, float(parts[2]), float(parts[3]), parts))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "window": "none"}
+        inside = [r for r in rows if t0 <= r[0] <= t1 + 0.25]
+        window = "timed"
+        if not inside:
+            after = [r for r in rows if r[0] >= t0]
+            inside = after[:2] if after else rows[-2:]
+            window = "nearest"
+        mhz = sorted(r[1] for r in inside)
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in inside:
+            for name, val in zip(names, r[3][6:10]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": mhz[len(mhz) // 2], "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": sorted(reasons), "samples": len(inside), "window": window}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_ours(args, rank, world, dist):
+    import torch
+    import exact_attention_81_gb300 as fa
+    from exact_attention_81_gb300.inputs import WORKLOADS, kvcache_inputs, workload_inputs
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pk = peaks()
+    w = WORKLOADS[args.workload]
+    stream = torch.cuda.current_stream()
+    q, k, v = workload_inputs(w, device=dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device=dev)
+
+    def step():
+        fa.fa_fwd(q, k, v, causal=w.causal, out=out, lse=lse)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    st = fa.get_last_device_error()
+    if st != fa.FA_OK:
+        raise RuntimeError(f"device error during warm-up: {fa.status_string(st)}")
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.5)
+    barrier()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    barrier()
+    t_wall1 = time.time()
+    ms_total = ev0.elapsed_time(ev1)
+    time.sleep(0.3)
+    sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall1)
+    st = fa.get_last_device_error()
+    if st != fa.FA_OK:
+        raise RuntimeError(f"device error in the timed region: {fa.status_string(st)}")
+
+    ms_step = ms_total / args.steps
+    if dist is not None:
+        t = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+    f = flops(w)
+    value = world * f / (ms_step * 1e-3) / 1e12
+
+    # e2e: pinned host buffers, H2D of Q/K/V and D2H of O/LSE inside the timed region.
+    hq = q.cpu().pin_memory()
+    hk = k.cpu().pin_memory()
+    hv = v.cpu().pin_memory()
+    ho = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        fa.fa_fwd(dq, dk, dv, causal=w.causal, out=out, lse=lse)
+        ho.copy_(out, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    for _ in range(3):
+        e2e_step()
+    barrier()
+    ev0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    ev1.record(stream)
+    barrier()
+    e2e_ms = ev0.elapsed_time(ev1) / e2e_steps
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = (q.numel() + k.numel() + v.numel()) * 2
+    d2h = out.numel() * 2 + lse.numel() * 4
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded iid N(0,1) bf16)",
+        "config": {"workload": f"{w.name}: B={w.B} Hq={w.Hq} Hkv={w.Hkv} Nq=Nk={w.Nq} "
+                               f"d={w.d} causal={w.causal} bf16",
+                   "batch": w.B, "heads": w.Hq, "seq_len": w.Nq, "head_dim": w.d,
+                   "causal": w.causal, "parallelism": f"replicas x{world} (independent heads)",
+                   "l2": f"inputs {h2d / 1e6:.0f} MB > L2 {L2_BYTES / 1e6:.0f} MB, no flush"},
+        "roofline": {"bound": "tensor", "achieved": round(f / (ms_step * 1e-3) / 1e12, 2),
+                     "peak": pk["bf16"], "unit": "TFLOP/s",
+                     "frac": round(f / (ms_step * 1e-3) / 1e12 / pk["bf16"], 4),
+                     "traffic": profiled_traffic("prefill_kernel<128,true>", PREFILL_SRC,
+                                                 w.name),
+                     "peak_basis": f"{pk['basis']} bf16 dense (burst)",
+                     "kernel": "prefill_kernel<128,true> (one launch per step)"},
+        "e2e": {"value": round(world * f / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOPS",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+
+    if not args.no_extra:
+        result["extra"] = extra_workloads(args, dev, pk, world, dist)
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w, q, k, v, args.cpu_seconds)
+    return result
+
+
+def time_calls(fn, steps, stream, warm=3):
+    import torch
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def extra_workloads(args, dev, pk, world, dist):
+    import torch
+    import exact_attention_81_gb300 as fa
+    from exact_attention_81_gb300.inputs import WORKLOADS, kvcache_inputs, workload_inputs
+    stream = torch.cuda.current_stream()
+    res = {}
+    for name in ("dense2k", "gqa16k"):
+        w = WORKLOADS[name]
+        q, k, v = workload_inputs(w, device=dev)
+        o = torch.empty_like(q)
+        l = torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device=dev)
+        ms = time_calls(lambda: fa.fa_fwd(q, k, v, causal=w.causal, out=o, lse=l),
+                        max(10, args.steps // 4), stream)
+        tf = flops(w) / (ms * 1e-3) / 1e12
+        res[name] = {"ms": round(ms, 4), "TFLOPS": round(tf, 2),
+                     "frac_of_bf16_peak": round(tf / pk["bf16"], 4)}
+        del q, k, v, o, l
+    w = WORKLOADS["decode"]
+    q, kc, vc, lens = kvcache_inputs(w.B, w.Nk, w.Hq, w.Hkv, w.d, seed=w.seed, device=dev)
+    ws = torch.empty(fa.fa_fwd_kvcache_workspace_size(w.B, w.Hq, w.Nk, w.d, 0), dtype=torch.uint8,
+                     device=dev)
+    o = torch.empty_like(q)
+    l = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
+    ms = time_calls(lambda: fa.fa_fwd_kvcache(q, kc, vc, lens, workspace=ws, out=o, lse=l),
+                    max(20, args.steps // 2), stream)
+    kv_bytes = int(lens.long().sum().item()) * w.Hkv * w.d * 2 * 2
+    io_bytes = q.numel() * 2 * 2 + l.numel() * 4
+    gbs = (kv_bytes + io_bytes) / (ms * 1e-3) / 1e9
+    res["decode"] = {"ms": round(ms, 4), "GB/s": round(gbs, 1),
+                     "algorithmic_bytes": kv_bytes + io_bytes,
+                     "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"],
+                                  "unit": "GB/s", "frac": round(gbs / pk["hbm"], 4),
+                                  "traffic": profiled_traffic("decode_kernel<128,4>", DECODE_SRC,
+                                                              "decode"),
+                                  "peak_basis": f"{pk['basis']} copy bandwidth"},
+                     "gpu_launches_per_call": 2}
+    st = fa.get_last_device_error()
+    if st != fa.FA_OK:
+        raise RuntimeError(f"device error in extra workloads: {fa.status_string(st)}")
+    return res
+
+
+# ----------------------------------------------------------------------------- oracle arm
+
+def cpu_sample_rows(w, n, seed=123):
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    rows = np.stack([rng.integers(0, w.B, n), rng.integers(0, w.Hq, n),
+                     rng.integers(0, w.Nq, n)], axis=1).astype(np.int32)
+    return rows
+
+
+def rows_flops(w, rows) -> float:
+    import numpy as np
+    i = rows[:, 2].astype(np.float64)
+    keys = np.minimum(i + 1 + (w.Nk - w.Nq), w.Nk) if w.causal else np.full_like(i, w.Nk)
+    # 4 * d per visible key: the causal-halved convention of the headline metric
+    return float(np.sum(4.0 * w.d * keys))
+
+
+def cpu_baseline(w, q, k, v, seconds):
+    """The fp64 oracle, as it stands, on a bounded sample of query rows of the workload."""
+    import oracle.oracle as ORACLE
+    hq, hk, hv = q.cpu(), k.cpu(), v.cpu()
+    threads = os.cpu_count() or 1
+    n = 32
+    while True:  # calibrate on a small sample, then time one sample of ~`seconds`
+        rows = cpu_sample_rows(w, n)
+        t0 = time.time()
+        ORACLE.attention_rows(hq, hk, hv, rows, w.scale, w.causal, nthreads=threads)
+        dt = time.time() - t0
+        if dt >= 0.5 or n >= 1 << 20:
+            break
+        n *= 4
+    n = max(n, int(n * seconds / max(dt, 1e-3)))
+    rows = cpu_sample_rows(w, n, seed=7)
+    t0 = time.time()
+    ORACLE.attention_rows(hq, hk, hv, rows, w.scale, w.causal, nthreads=threads)
+    dt = time.time() - t0
+    tflops = rows_flops(w, rows) / dt / 1e12
+    return {"value": tflops, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
+            "sample": f"{n} random query rows of {w.name} (fp64, {dt:.1f} s)"}
+
+
+def run_reference(args, w):
+    import numpy as np
+    import oracle.oracle as ORACLE
+    from exact_attention_81_gb300.inputs import workload_inputs
+    q, k, v = workload_inputs(w, device="cpu")
+    threads = os.cpu_count() or 1
+    # size one step so that warm-up + timed steps stay within a few minutes
+    n = 64
+    while True:
+        rows = cpu_sample_rows(w, n)
+        t0 = time.time()
+        ORACLE.attention_rows(q, k, v, rows, w.scale, w.causal, nthreads=threads)
+        dt = time.time() - t0
+        if dt >= 0.5 or n >= 1 << 20:
+            break
+        n *= 2
+    per_step_budget = 120.0 / max(1, args.steps + args.warmup)
+    n = max(16, int(n * min(4.0, per_step_budget / max(dt, 1e-3))))
+    steps = []
+    for s in range(args.warmup + args.steps):
+        rows = cpu_sample_rows(w, n, seed=1000 + s)
+        t0 = time.time()
+        ORACLE.attention_rows(q, k, v, rows, w.scale, w.causal, nthreads=threads)
+        dt = time.time() - t0
+        if s >= args.warmup:
+            steps.append((rows_flops(w, rows), dt))
+    total_f = sum(f for f, _ in steps)
+    total_t = sum(t for _, t in steps)
+    value = total_f / total_t / 1e12
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_t / len(steps) * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded iid N(0,1) bf16)",
+        "config": {"workload": f"{w.name}: B={w.B} Hq={w.Hq} Hkv={w.Hkv} Nq=Nk={w.Nq} "
+                               f"d={w.d} causal={w.causal} bf16"},
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
+                         "sample": f"{n} random query rows of {w.name} per step (fp64)"},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-extra", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    from exact_attention_81_gb300.inputs import WORKLOADS
+    w = WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args, w)), flush=True)
+        return
+
+    import __graft_entry__
+    __graft_entry__.build()
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as dist_mod
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist_mod.init_process_group("nccl")
+        dist = dist_mod
+    result = run_ours(args, rank, world, dist)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

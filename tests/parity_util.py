@@ -20,13 +20,14 @@ def to_np(t: torch.Tensor) -> np.ndarray:
 
 
 def compare(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
-    """o_* broadcastable [..., d], lse_* [...] with matching row order."""
+    """o_* [..., d] and lse_* [...] with the same row order (o.shape[:-1] == lse.shape)."""
     o = to_np(o_gpu) if isinstance(o_gpu, torch.Tensor) else np.asarray(o_gpu, np.float64)
     lse = to_np(lse_gpu) if isinstance(lse_gpu, torch.Tensor) else np.asarray(lse_gpu, np.float64)
     o_ref = np.asarray(o_ref, np.float64)
     lse_ref = np.asarray(lse_ref, np.float64)
     assert o.shape == o_ref.shape, f"{what}: O shape {o.shape} vs {o_ref.shape}"
     assert lse.shape == lse_ref.shape, f"{what}: LSE shape {lse.shape} vs {lse_ref.shape}"
+    assert o.shape[:-1] == lse.shape, f"{what}: O rows {o.shape[:-1]} vs LSE rows {lse.shape}"
     assert np.all(np.isfinite(o)), f"{what}: non-finite O"
     empty = ~np.isfinite(lse_ref)
     assert np.array_equal(~np.isfinite(lse), empty), f"{what}: -inf LSE rows differ"
@@ -56,3 +57,17 @@ def sample_rows(B, H, N, n, seed, must=()):
     while len(rows) < n + len(must):
         rows.add((int(rng.integers(B)), int(rng.integers(H)), int(rng.integers(N))))
     return np.array(sorted(rows), dtype=np.int32)
+
+
+def dense_rows(o, lse):
+    """Dense O [B,N,H,d] and LSE [B,H,N] -> row-aligned O [B,H,N,d] and LSE."""
+    if isinstance(o, torch.Tensor):
+        return o.permute(0, 2, 1, 3), lse
+    return np.transpose(o, (0, 2, 1, 3)), lse
+
+
+def varlen_rows(o, lse):
+    """Varlen O [T,H,d] and LSE [H,T] -> row-aligned O [H,T,d] and LSE."""
+    if isinstance(o, torch.Tensor):
+        return o.permute(1, 0, 2), lse
+    return np.transpose(o, (1, 0, 2)), lse

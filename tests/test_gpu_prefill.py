@@ -11,7 +11,7 @@ import oracle.oracle as ORACLE
 from exact_attention_81_gb300 import (FA_OK, fa_fwd, fa_fwd_varlen, get_last_device_error)
 from exact_attention_81_gb300.inputs import (WORKLOADS, dense_inputs, varlen_inputs,
                                              workload_inputs)
-from tests.parity_util import compare, sample_rows, to_np
+from tests.parity_util import compare, dense_rows, sample_rows, varlen_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -56,7 +56,7 @@ def test_dense_small(case):
     scale = 1.0 / math.sqrt(d)
     o, lse = _run_dense(q, k, v, causal)
     o_ref, lse_ref = _oracle_dense(q, k, v, causal, float(np.float32(scale)))
-    compare(o, lse, o_ref, lse_ref, f"dense {case}")
+    compare(*dense_rows(o, lse), *dense_rows(o_ref, lse_ref), f"dense {case}")
 
 
 def test_tiny_workload_and_golden_rows():
@@ -64,10 +64,11 @@ def test_tiny_workload_and_golden_rows():
     import json
     import os
     w = WORKLOADS["tiny"]
-    q, k, v = workload_inputs(w, device=DEV)
+    # drawn from the CPU generator, as the stored rows were (CPU and CUDA streams differ)
+    q, k, v = (t.to(DEV) for t in workload_inputs(w, device="cpu"))
     o, lse = _run_dense(q, k, v, w.causal)
     o_ref, lse_ref = _oracle_dense(q, k, v, w.causal, w.scale)
-    compare(o, lse, o_ref, lse_ref, "tiny")
+    compare(*dense_rows(o, lse), *dense_rows(o_ref, lse_ref), "tiny")
     g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "tiny_rows.json")))
     rows = g["rows"]
     compare(o[0, rows, 0], lse[0, 0, rows], np.array(g["o"]), np.array(g["lse"]), "golden rows")
@@ -78,7 +79,7 @@ def test_scale_argument():
     for scale in (0.03, 0.5):
         o, lse = _run_dense(q, k, v, True, scale=scale)
         o_ref, lse_ref = _oracle_dense(q, k, v, True, float(np.float32(scale)))
-        compare(o, lse, o_ref, lse_ref, f"scale {scale}")
+        compare(*dense_rows(o, lse), *dense_rows(o_ref, lse_ref), f"scale {scale}")
 
 
 def test_strided_views_and_guard_bands():
@@ -95,7 +96,7 @@ def test_strided_views_and_guard_bands():
     assert get_last_device_error() == FA_OK
     o_ref, lse_ref = _oracle_dense(q.contiguous(), k.contiguous(), v.contiguous(), True,
                                    float(np.float32(1 / math.sqrt(d))))
-    compare(o, lse, o_ref, lse_ref, "strided")
+    compare(*dense_rows(o, lse), *dense_rows(o_ref, lse_ref), "strided")
     mask = torch.ones_like(guard, dtype=torch.bool)
     mask[:, 8:N + 8, 1:H + 1] = False
     assert torch.all(guard[mask] == 7.0), "write outside the output view"
@@ -137,7 +138,8 @@ def test_varlen(case, causal):
     o_ref, lse_ref = ORACLE.attention_varlen(q.cpu(), k.cpu(), v.cpu(), cu_q.cpu(), cu_k.cpu(),
                                              float(np.float32(1 / math.sqrt(d))), causal)
     if total_q:
-        compare(o, lse, o_ref, lse_ref, f"varlen {case} causal={causal}")
+        compare(*varlen_rows(o, lse), *varlen_rows(o_ref, lse_ref),
+                f"varlen {case} causal={causal}")
     assert torch.all(o_buf[:4] == 3.0) and torch.all(o_buf[total_q + 4:] == 3.0)
 
 
