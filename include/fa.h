@@ -132,6 +132,37 @@ fa_status fa_fwd_kvcache(const void *q, const void *k_cache, const void *v_cache
                          cudaStream_t stream);
 
 /*
+ * Split-KV decode that allocates nothing.  Same computation, arguments and outputs as
+ * fa_fwd_kvcache, minus the workspace.  (The paper has no counterpart: this entry point
+ * exists for callers of this library, not for the method.)
+ *
+ * Some callers cannot allocate device memory at call time and have no buffer set aside
+ * to pass as a workspace -- for example code running as a plugin inside another runtime
+ * that hands it no workspace, or a serving loop that keeps cudaMalloc (which can
+ * synchronise the whole device) out of its decode step.  This call writes the split
+ * partials to a scratch array compiled into the library instead: a file-scope __device__
+ * array of FA_NOALLOC_SCRATCH_BYTES (64 MiB) that every GPU which loads the library holds
+ * until the process exits.  It calls no cudaMalloc, cudaFree or other allocating routine.
+ *   - A call whose partials need more than FA_NOALLOC_SCRATCH_BYTES
+ *     (fa_fwd_kvcache_workspace_size(B, Hq, Lmax, d, num_splits) > the maximum) is
+ *     rejected with FA_ERR_WORKSPACE before anything is enqueued; use fa_fwd_kvcache with
+ *     your own workspace for it, or fewer splits (num_splits > 0).
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make that first call
+ *     before any stream capture.
+ *   - All calls on a device share the one array, which keeps the last call's contents.
+ *     Nothing in it needs to start at zero (each partial is written before it is read),
+ *     but calls that overlap on the GPU -- on different streams, or from graphs running at
+ *     the same time -- race on it; the caller must keep them from overlapping.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (64u << 20)
+
+fa_status fa_fwd_kvcache_noalloc(const void *q, const void *k_cache, const void *v_cache,
+                                 const int *cache_seqlens, int B, int Lmax, int Hq, int Hkv,
+                                 int d, const int64_t cache_strides[3], float scale,
+                                 int num_splits, void *o, float *lse, cudaStream_t stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's error word.
  * Returns FA_OK when no kernel recorded a fault since the last read, FA_ERR_TIMEOUT when a
  * bounded device-side wait gave up (the kernel then stopped early and its outputs are
