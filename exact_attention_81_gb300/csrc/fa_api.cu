@@ -238,6 +238,7 @@ fa_status fa_fwd(const fa_fwd_params *p, cudaStream_t stream) {
   pa.scale_log2 = scale_log2(a.scale);
   pa.err = dev->err;
   pa.timeout_ns = g_timeout_ns;
+  pa.sched_slot = fa::next_prefill_sched_slot();
   const int grid = static_cast<int>(tiles < dev->sm_count ? tiles : dev->sm_count);
   cudaError_t e = fa::launch_prefill(a.d, a.causal != 0, tq, tk, tv, pa, grid, stream);
   return e == cudaSuccess ? FA_OK : cuda_fail("prefill kernel launch", e);
@@ -307,6 +308,7 @@ fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, fl
   pa.scale_log2 = scale_log2(scale);
   pa.err = dev->err;
   pa.timeout_ns = g_timeout_ns;
+  pa.sched_slot = fa::next_prefill_sched_slot();
   const int grid = static_cast<int>(tiles < dev->sm_count ? tiles : dev->sm_count);
   cudaError_t e = fa::launch_prefill(d, causal != 0, tq, tk, tv, pa, grid, stream);
   return e == cudaSuccess ? FA_OK : cuda_fail("prefill kernel launch", e);

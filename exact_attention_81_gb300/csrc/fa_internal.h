@@ -31,9 +31,13 @@ struct PrefillArgs {
   int mblocks;                // 256-row query blocks per (batch, head)
   int num_tiles;              // B * Hq * mblocks
   float scale_log2;           // scale * log2(e)
+  int sched_slot;             // this launch's tile-ticket counter slot
   unsigned int *err;          // device error word
   unsigned long long timeout_ns;
 };
+
+// Tile-ticket counter slot for the next prefill launch (round robin over the slots).
+int next_prefill_sched_slot();
 
 cudaError_t launch_prefill(int d, bool causal, const CUtensorMap &tq, const CUtensorMap &tk,
                            const CUtensorMap &tv, const PrefillArgs &a, int grid,

@@ -15,11 +15,14 @@
 // normalise once after the inner loop).  The epilogue writes O (bf16) and the natural-log
 // LSE = ln2 * (m + log2 l).  S and P never leave the SM.
 //
-// Warp roles (320 threads):
+// Warp roles (384 threads, three warpgroups):
 //   warps 0-3  softmax + correction + epilogue for sub-tile 0 (thread = query row)
 //   warps 4-7  the same for sub-tile 1
-//   warp  8    TMA producer: Q tiles and the K/V ring (one elected lane)
-//   warp  9    TMEM allocator and MMA issuer (one elected lane)
+//   warp  8    tile scheduler and TMA producer: Q tiles and the K/V ring (one lane)
+//   warp  9    TMEM allocator and MMA issuer (one lane)
+//   warps 10-11 idle
+// The third warpgroup gives registers back (setmaxnreg) so that the two softmax
+// warpgroups can hold a full 128-score row per thread without spilling.
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+d), O_1 [384,384+d).
 // P_t overwrites the first 64 columns of S_t as packed bf16 pairs and is the A operand of
 // the PV MMA straight from TMEM.
@@ -27,8 +30,12 @@
 // Causal masking ("FlashAttention 1-4 详解", FlashAttention 2 engineering notes: skip the
 // tiles above the diagonal, ~N^2/2 work) limits each sub-tile to the K/V tiles that hold a
 // visible key and masks only the tiles that straddle the diagonal or the sequence end.
-// Tiles are ordered head-major with the largest causal query blocks first, so CTAs that
-// run at the same time share one head's K/V in L2 and long tiles start early.
+// Tiles are ordered head-major with the largest causal query blocks first and handed out
+// dynamically: the producer lane of each CTA takes the next ticket from a per-launch
+// atomic counter and passes the tile to the other roles through a small shared-memory
+// ring.  CTAs that run at the same time therefore share a few heads' K/V in L2, long tiles
+// start early, and no CTA idles while another still holds several tiles.
+#include <atomic>
 #include <cmath>
 
 #include "fa_internal.h"
@@ -39,9 +46,13 @@ namespace {
 
 constexpr int BR = 128;             // query rows per sub-tile (MMA M)
 constexpr int BC = 128;             // keys per K/V tile
-constexpr int NTHREADS = 320;
+constexpr int NTHREADS = 384;
 constexpr int PRODUCER_WARP = 8;
 constexpr int MMA_WARP = 9;
+constexpr int SCHED_DEPTH = 4;      // tiles in flight between the scheduler and the roles
+constexpr int SOFTMAX_REGS = 216;   // 2 x 128 threads x 216
+constexpr int OTHER_REGS = 72;      //   + 128 threads x 72 = 384 threads x 168 at launch
+constexpr int NUM_SCHED_SLOTS = 256;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int BOX_BYTES = 128 * 128;  // one TMA box: 128 rows x 64 bf16 (128 B, swizzled)
 constexpr float LN2 = 0.6931471805599453f;
@@ -64,7 +75,14 @@ struct Cfg {
   static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, false, true);
 };
 
+// Per-launch tile-ticket counters: [slot][0] = next ticket, [slot][1] = CTAs finished.
+// The host gives each launch its own slot (round robin); the last CTA of a launch to
+// finish resets the slot to zero for its next user.
+__device__ unsigned int g_sched[NUM_SCHED_SLOTS][2];
+
 struct Bars {
+  uint64_t sched_full[SCHED_DEPTH], sched_empty[SCHED_DEPTH];
+  int sched_tile[SCHED_DEPTH];
   uint64_t q_full, q_empty;
   uint64_t kv_full[8], kv_empty[8];
   uint64_t s_full[2], p_ready[2], o_full[2], o_empty[2];
@@ -161,7 +179,9 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint3
 }
 
 // ------------------------------------------------------------------------------------
-// Producer: Q tiles and the K/V ring (ring order K_0, V_0, K_1, V_1, ...).
+// Scheduler + producer (one lane).  Takes tickets from the launch's counter, publishes each
+// tile to the scheduler ring, then issues its Q tile and its K/V ring loads (ring order
+// K_0, V_0, K_1, V_1, ...).  A ticket past the last tile is published as -1 (end).
 
 template <int D, bool CAUSAL>
 __device__ void producer_role(const PrefillArgs &a, const CUtensorMap *tmq,
@@ -169,7 +189,15 @@ __device__ void producer_role(const PrefillArgs &a, const CUtensorMap *tmq,
                               Bars *bars, const WaitCtl &wc) {
   using C = Cfg<D>;
   uint32_t kv_iter = 0, q_iter = 0;
-  for (int tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x) {
+  unsigned int *ctr = g_sched[a.sched_slot];
+  for (uint32_t k = 0;; ++k) {
+    const int ticket = static_cast<int>(atomicAdd(&ctr[0], 1u));
+    const int tile = ticket < a.num_tiles ? ticket : -1;
+    const int rs = static_cast<int>(k % SCHED_DEPTH);
+    if (!mbar_wait(&bars->sched_empty[rs], ((k / SCHED_DEPTH) & 1u) ^ 1u, wc)) goto out;
+    bars->sched_tile[rs] = tile;
+    mbar_arrive(&bars->sched_full[rs]);
+    if (tile < 0) break;
     const TileInfo ti = tile_info<CAUSAL>(a, tile);
     if (a.varlen && (ti.q_row0 == 0) && varlen_bad(a, ti.b)) atomicOr(a.err, DEVERR_BAD_CU_SEQLENS);
     const int n = max(ti.nkv[0], ti.nkv[1]);
@@ -200,6 +228,13 @@ __device__ void producer_role(const PrefillArgs &a, const CUtensorMap *tmq,
     }
   }
 out:
+  // This CTA takes no more tickets (it reached the end, or gave up): count it as finished.
+  // The last CTA of the launch to finish resets the counters for the slot's next launch.
+  __threadfence();
+  if (atomicAdd(&ctr[1], 1u) == gridDim.x - 1) {
+    atomicExch(&ctr[0], 0u);
+    atomicExch(&ctr[1], 0u);
+  }
   // Teardown: let every bulk copy this thread issued land before the CTA may exit.
   for (int s = 0; s < C::NSLOTS; ++s) {
     if (kv_iter > static_cast<uint32_t>(s)) {
@@ -208,6 +243,19 @@ out:
     }
   }
   if (q_iter > 0) mbar_wait_teardown(&bars->q_full, (q_iter - 1) & 1u, 1000000000ull);
+}
+
+// Consumer side of the scheduler ring: the k-th tile of this CTA (-1 = no more), or false
+// if the wait gave up.  WARP consumers are whole warps (all lanes call it).
+template <bool WARP>
+__device__ __forceinline__ bool next_tile(Bars *bars, uint32_t k, int &tile, const WaitCtl &wc) {
+  const int rs = static_cast<int>(k % SCHED_DEPTH);
+  bool ok = mbar_wait(&bars->sched_full[rs], (k / SCHED_DEPTH) & 1u, wc);
+  if (WARP) ok = __all_sync(0xffffffffu, ok);
+  if (!ok) return false;
+  tile = bars->sched_tile[rs];
+  mbar_arrive(&bars->sched_empty[rs]);
+  return true;
 }
 
 // ------------------------------------------------------------------------------------
@@ -226,7 +274,10 @@ __device__ void mma_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, uint32
   bool o_pending[2] = {false, false};
   const uint32_t q_smem[2] = {smem_u32(smem + C::Q_OFF), smem_u32(smem + C::Q_OFF + C::TILE_BYTES)};
   const uint32_t ring = smem_u32(smem + C::RING_OFF);
-  for (int tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x) {
+  for (uint32_t k = 0;; ++k) {
+    int tile;
+    if (!next_tile<false>(bars, k, tile, wc)) goto out;
+    if (tile < 0) break;
     const TileInfo ti = tile_info<CAUSAL>(a, tile);
     const int n = max(ti.nkv[0], ti.nkv[1]);
     if (n == 0) continue;
@@ -312,13 +363,17 @@ __device__ void softmax_role(const PrefillArgs &a, Bars *bars, uint32_t tmem, co
   uint32_t s_phase = 0, o_phase = 0;
   __nv_bfloat16 *obase = reinterpret_cast<__nv_bfloat16 *>(a.o);
 
-  for (int tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x) {
+  for (uint32_t k = 0;; ++k) {
+    int tile;
+    if (!next_tile<true>(bars, k, tile, wc)) return;
+    if (tile < 0) break;
     const TileInfo ti = tile_info<CAUSAL>(a, tile);
-    if (ti.nrows[t] == 0) continue;
-    const int nkv = ti.nkv[t];
+    const int nrows = t == 0 ? ti.nrows[0] : ti.nrows[1];
+    if (nrows == 0) continue;
+    const int nkv = t == 0 ? ti.nkv[0] : ti.nkv[1];
     const int first_row = ti.q_row0 + t * BR;
     const int row = first_row + rit;
-    const bool row_ok = rit < ti.nrows[t];
+    const bool row_ok = rit < nrows;
     // Last key index this row may see, and the smallest such index over the sub-tile.
     const int limit = CAUSAL ? min(row + ti.nk - ti.nq, ti.nk - 1) : ti.nk - 1;
     const int min_limit = CAUSAL ? min(first_row + ti.nk - ti.nq, ti.nk - 1) : ti.nk - 1;
@@ -455,6 +510,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int lane = static_cast<int>(threadIdx.x) & 31;
 
   if (threadIdx.x == 0) {
+    for (int i = 0; i < SCHED_DEPTH; ++i) {
+      mbar_init(&bars->sched_full[i], 1);
+      mbar_init(&bars->sched_empty[i], 1 + 256);  // MMA lane + every softmax thread
+    }
     mbar_init(&bars->q_full, 1);
     mbar_init(&bars->q_empty, 1);
     for (int s = 0; s < C::NSLOTS; ++s) {
@@ -486,19 +545,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t tmem = bars->tmem_base;
   const WaitCtl wc{&bars->abort, a.err, a.timeout_ns, DEVERR_PREFILL_TIMEOUT};
 
+  // Each register-split branch ends the kernel on its own; the two meet at a named barrier
+  // before TMEM is released.
   if (warp < PRODUCER_WARP) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(SOFTMAX_REGS));
     softmax_role<D, CAUSAL>(a, bars, tmem, wc, warp, lane);
-  } else if (warp == PRODUCER_WARP) {
-    if (lane == 0) producer_role<D, CAUSAL>(a, &tmq, &tmk, &tmv, smem, bars, wc);
+    __syncwarp();
+    tc_fence_before();
+    named_barrier(1, NTHREADS);
   } else {
-    if (lane == 0) mma_role<D, CAUSAL>(a, smem, bars, tmem, wc);
-  }
-  __syncwarp();
-  tc_fence_before();
-  __syncthreads();
-  if (warp == MMA_WARP) {
-    tc_fence_after();
-    tmem_dealloc(tmem, TMEM_COLS);
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(OTHER_REGS));
+    if (warp == PRODUCER_WARP) {
+      if (lane == 0) producer_role<D, CAUSAL>(a, &tmq, &tmk, &tmv, smem, bars, wc);
+    } else if (warp == MMA_WARP) {
+      if (lane == 0) mma_role<D, CAUSAL>(a, smem, bars, tmem, wc);
+    }
+    __syncwarp();
+    tc_fence_before();
+    named_barrier(1, NTHREADS);
+    if (warp == MMA_WARP) {
+      tc_fence_after();
+      tmem_dealloc(tmem, TMEM_COLS);
+    }
   }
 }
 
@@ -531,6 +599,11 @@ __global__ void fill_empty_kernel(__nv_bfloat16 *o, float *lse, int B, int N, in
 }
 
 }  // namespace
+
+int next_prefill_sched_slot() {
+  static std::atomic<unsigned int> seq{0};
+  return static_cast<int>(seq.fetch_add(1u) % NUM_SCHED_SLOTS);
+}
 
 int prefill_smem_bytes(int d) { return d == 64 ? Cfg<64>::SMEM_BYTES : Cfg<128>::SMEM_BYTES; }
 

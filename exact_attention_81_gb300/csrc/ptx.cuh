@@ -69,7 +69,7 @@ struct WaitCtl {
   unsigned int code;
 };
 
-static __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, const WaitCtl &c) {
+__device__ __forceinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, const WaitCtl &c) {
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -88,7 +88,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const 
 }
 
 // Wait used only on the teardown path: ignores the abort flag, bounded by a fixed time.
-static __device__ __noinline__ bool mbar_wait_teardown(uint64_t *bar, uint32_t parity,
+__device__ __forceinline__ bool mbar_wait_teardown(uint64_t *bar, uint32_t parity,
                                                 unsigned long long limit_ns) {
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity)) {

@@ -1,0 +1,50 @@
+"""Failure detection without faulting the GPU: with a 1 ns limit on device-side waits the
+kernels give up at their first unsatisfied wait, unwind (bounded teardown of their own
+bulk copies and MMAs, TMEM released) and report FA_ERR_TIMEOUT through the device error
+word.  The context stays usable: the next call with the default limit is bit-identical to
+one made before the failure (which also shows that the prefill tile-ticket counters were
+left clean)."""
+import pytest
+import torch
+
+from exact_attention_81_gb300 import (FA_ERR_TIMEOUT, FA_OK, fa_fwd, fa_fwd_kvcache,
+                                      get_last_device_error, set_wait_timeout_ns)
+from exact_attention_81_gb300.inputs import dense_inputs, kvcache_inputs
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _with_tiny_timeout(fn):
+    set_wait_timeout_ns(1)
+    try:
+        fn()
+        return get_last_device_error()
+    finally:
+        set_wait_timeout_ns(0)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_prefill_wait_timeout_reports_and_recovers(causal):
+    q, k, v = dense_inputs(2, 1500, 1500, 4, 2, 128, seed=71, device=DEV)
+    o_ok, l_ok = fa_fwd(q, k, v, causal=causal)
+    assert get_last_device_error() == FA_OK
+    st = _with_tiny_timeout(lambda: fa_fwd(q, k, v, causal=causal))
+    assert st == FA_ERR_TIMEOUT
+    assert get_last_device_error() == FA_OK  # the word was cleared by the read
+    for _ in range(2):
+        o2, l2 = fa_fwd(q, k, v, causal=causal)
+        assert get_last_device_error() == FA_OK
+        assert torch.equal(o2, o_ok) and torch.equal(l2, l_ok)
+
+
+def test_decode_wait_timeout_reports_and_recovers():
+    lens = torch.tensor([3000, 17, 4096, 1500], dtype=torch.int32)
+    q, kc, vc, lens = kvcache_inputs(4, 4096, 32, 8, 128, seed=72, lengths=lens, device=DEV)
+    o_ok, l_ok = fa_fwd_kvcache(q, kc, vc, lens)
+    assert get_last_device_error() == FA_OK
+    st = _with_tiny_timeout(lambda: fa_fwd_kvcache(q, kc, vc, lens))
+    assert st == FA_ERR_TIMEOUT
+    o2, l2 = fa_fwd_kvcache(q, kc, vc, lens)
+    assert get_last_device_error() == FA_OK
+    assert torch.equal(o2, o_ok) and torch.equal(l2, l_ok)
