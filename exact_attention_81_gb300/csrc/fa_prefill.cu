@@ -379,19 +379,20 @@ __device__ void softmax_role(const PrefillArgs &a, Bars *bars, uint32_t tmem, co
     const int min_limit = CAUSAL ? min(first_row + ti.nk - ti.nq, ti.nk - 1) : ti.nk - 1;
 
     float m = -INFINITY, l = 0.f;
+    const uint64_t c2 = f2_pack(c, c);
     for (int j = 0; j < nkv; ++j) {
       if (!warp_wait(&bars->s_full[t], s_phase, wc)) return;
       s_phase ^= 1u;
       tc_fence_after();
       float s[BC];
       {
-        uint32_t r[64];
-        tmem_ld_x64(tS, r);
+        uint32_t r0[64], r1[64];
+        tmem_ld_2x64(tS, tS + 64, r0, r1);
 #pragma unroll
-        for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(r[i]);
-        tmem_ld_x64(tS + 64, r);
-#pragma unroll
-        for (int i = 0; i < 64; ++i) s[64 + i] = __uint_as_float(r[i]);
+        for (int i = 0; i < 64; ++i) {
+          s[i] = __uint_as_float(r0[i]);
+          s[64 + i] = __uint_as_float(r1[i]);
+        }
       }
       const int kbase = j * BC;
       if (kbase + BC - 1 > min_limit) {
@@ -400,56 +401,73 @@ __device__ void softmax_role(const PrefillArgs &a, Bars *bars, uint32_t tmem, co
         for (int i = 0; i < BC; ++i)
           if (i > lim) s[i] = -INFINITY;
       }
-      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+      float mx0 = fmax3(s[0], s[1], s[2]), mx1 = fmax3(s[3], s[4], s[5]);
+      float mx2 = fmax3(s[6], s[7], s[8]), mx3 = fmax3(s[9], s[10], s[11]);
 #pragma unroll
-      for (int i = 4; i < BC; i += 4) {
-        mx0 = fmaxf(mx0, s[i]);
-        mx1 = fmaxf(mx1, s[i + 1]);
-        mx2 = fmaxf(mx2, s[i + 2]);
-        mx3 = fmaxf(mx3, s[i + 3]);
+      for (int i = 12; i < BC - 4; i += 8) {
+        mx0 = fmax3(mx0, s[i], s[i + 1]);
+        mx1 = fmax3(mx1, s[i + 2], s[i + 3]);
+        mx2 = fmax3(mx2, s[i + 4], s[i + 5]);
+        mx3 = fmax3(mx3, s[i + 6], s[i + 7]);
       }
-      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+      const float mx = fmaxf(fmax3(mx0, mx1, s[BC - 4]),
+                             fmax3(mx2, mx3, fmax3(s[BC - 3], s[BC - 2], s[BC - 1])));
       const float m_new = fmaxf(m, mx * c);
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      float alpha = 1.f;
-      if (j > 0) {
-        const bool grow = m_new > m;
-        if (grow) alpha = ex2_approx(m - m_use);
-        if (__any_sync(0xffffffffu, grow)) {
-          // Conditional rescale of the O accumulator held in TMEM.  PV_t(j-1) has
-          // completed: its commit precedes the one that signalled S_t(j).
-#pragma unroll
-          for (int cc = 0; cc < D; cc += 32) {
-            uint32_t r[32];
-            tmem_ld_x32(tO + cc, r);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-            tmem_st_x32(tO + cc, r);
-          }
-        }
-      }
-      const float neg = -m_use;
-      float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+      const bool grow = j > 0 && m_new > m;
+      const float alpha = grow ? ex2_approx(m - m_use) : 1.f;
+      // P = 2^(S c - m_new) with the FMA and the row sum on packed fp32 pairs.
+      const uint64_t neg2 = f2_pack(-m_use, -m_use);
+      uint64_t l2a = f2_pack(0.f, 0.f), l2b = l2a;
       uint32_t p[64];
 #pragma unroll
       for (int i = 0; i < 64; i += 2) {
-        const float p0 = ex2_approx(fmaf(s[2 * i], c, neg));
-        const float p1 = ex2_approx(fmaf(s[2 * i + 1], c, neg));
-        const float p2 = ex2_approx(fmaf(s[2 * i + 2], c, neg));
-        const float p3 = ex2_approx(fmaf(s[2 * i + 3], c, neg));
-        l0 += p0;
-        l1 += p1;
-        l2 += p2;
-        l3 += p3;
+        float x0, x1, x2, x3;
+        f2_unpack(f2_fma(f2_pack(s[2 * i], s[2 * i + 1]), c2, neg2), x0, x1);
+        f2_unpack(f2_fma(f2_pack(s[2 * i + 2], s[2 * i + 3]), c2, neg2), x2, x3);
+        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+        const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+        l2a = f2_add(l2a, f2_pack(p0, p1));
+        l2b = f2_add(l2b, f2_pack(p2, p3));
         p[i] = pack_bf16x2(p0, p1);
         p[i + 1] = pack_bf16x2(p2, p3);
       }
-      l = l * alpha + ((l0 + l1) + (l2 + l3));
+      {
+        float la, lb, lc, ld;
+        f2_unpack(l2a, la, lb);
+        f2_unpack(l2b, lc, ld);
+        l = l * alpha + ((la + lb) + (lc + ld));
+      }
       {
         uint32_t (&p0)[32] = *reinterpret_cast<uint32_t (*)[32]>(&p[0]);
         uint32_t (&p1)[32] = *reinterpret_cast<uint32_t (*)[32]>(&p[32]);
         tmem_st_x32(tS, p0);
         tmem_st_x32(tS + 32, p1);
+      }
+      if (__any_sync(0xffffffffu, grow)) {
+        // Conditional rescale of the O accumulator held in TMEM, done after P so that the
+        // whole O row fits in the registers the scores used (one TMEM round trip).
+        // PV_t(j-1) has completed: its commit precedes the one that signalled S_t(j).
+        if constexpr (D == 128) {
+          uint32_t o0[64], o1[64];
+          tmem_ld_2x64(tO, tO + 64, o0, o1);
+#pragma unroll
+          for (int i = 0; i < 64; ++i) {
+            o0[i] = __float_as_uint(__uint_as_float(o0[i]) * alpha);
+            o1[i] = __float_as_uint(__uint_as_float(o1[i]) * alpha);
+          }
+          tmem_st_x32(tO, *reinterpret_cast<uint32_t (*)[32]>(&o0[0]));
+          tmem_st_x32(tO + 32, *reinterpret_cast<uint32_t (*)[32]>(&o0[32]));
+          tmem_st_x32(tO + 64, *reinterpret_cast<uint32_t (*)[32]>(&o1[0]));
+          tmem_st_x32(tO + 96, *reinterpret_cast<uint32_t (*)[32]>(&o1[32]));
+        } else {
+          uint32_t o0[64];
+          tmem_ld_x64(tO, o0);
+#pragma unroll
+          for (int i = 0; i < 64; ++i) o0[i] = __float_as_uint(__uint_as_float(o0[i]) * alpha);
+          tmem_st_x32(tO, *reinterpret_cast<uint32_t (*)[32]>(&o0[0]));
+          tmem_st_x32(tO + 32, *reinterpret_cast<uint32_t (*)[32]>(&o0[32]));
+        }
       }
       tmem_wait_st();
       tc_fence_before();

@@ -230,6 +230,45 @@ __device__ __forceinline__ void tmem_st_x32(uint32_t taddr, const uint32_t (&r)[
       : "memory");
 }
 
+// Two 32 lanes x 64-column TMEM loads (taddr0, taddr1) completed by a single wait.
+__device__ __forceinline__ void tmem_ld_2x64(uint32_t taddr0, uint32_t taddr1, uint32_t (&r0)[64],
+                                             uint32_t (&r1)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%128];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%64, %65, %66, %67, %68, %69, %70, %71, %72, %73, %74, %75, %76, %77, %78, %79, %80, %81, %82, %83, %84, %85, %86, %87, %88, %89, %90, %91, %92, %93, %94, %95, %96, %97, %98, %99, %100, %101, %102, %103, %104, %105, %106, %107, %108, %109, %110, %111, %112, %113, %114, %115, %116, %117, %118, %119, %120, %121, %122, %123, %124, %125, %126, %127}, [%129];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r0[0]), "=r"(r0[1]), "=r"(r0[2]), "=r"(r0[3]), "=r"(r0[4]), "=r"(r0[5]), "=r"(r0[6]), "=r"(r0[7]), "=r"(r0[8]), "=r"(r0[9]), "=r"(r0[10]), "=r"(r0[11]), "=r"(r0[12]), "=r"(r0[13]), "=r"(r0[14]), "=r"(r0[15]), "=r"(r0[16]), "=r"(r0[17]), "=r"(r0[18]), "=r"(r0[19]), "=r"(r0[20]), "=r"(r0[21]), "=r"(r0[22]), "=r"(r0[23]), "=r"(r0[24]), "=r"(r0[25]), "=r"(r0[26]), "=r"(r0[27]), "=r"(r0[28]), "=r"(r0[29]), "=r"(r0[30]), "=r"(r0[31]), "=r"(r0[32]), "=r"(r0[33]), "=r"(r0[34]), "=r"(r0[35]), "=r"(r0[36]), "=r"(r0[37]), "=r"(r0[38]), "=r"(r0[39]), "=r"(r0[40]), "=r"(r0[41]), "=r"(r0[42]), "=r"(r0[43]), "=r"(r0[44]), "=r"(r0[45]), "=r"(r0[46]), "=r"(r0[47]), "=r"(r0[48]), "=r"(r0[49]), "=r"(r0[50]), "=r"(r0[51]), "=r"(r0[52]), "=r"(r0[53]), "=r"(r0[54]), "=r"(r0[55]), "=r"(r0[56]), "=r"(r0[57]), "=r"(r0[58]), "=r"(r0[59]), "=r"(r0[60]), "=r"(r0[61]), "=r"(r0[62]), "=r"(r0[63]), "=r"(r1[0]), "=r"(r1[1]), "=r"(r1[2]), "=r"(r1[3]), "=r"(r1[4]), "=r"(r1[5]), "=r"(r1[6]), "=r"(r1[7]), "=r"(r1[8]), "=r"(r1[9]), "=r"(r1[10]), "=r"(r1[11]), "=r"(r1[12]), "=r"(r1[13]), "=r"(r1[14]), "=r"(r1[15]), "=r"(r1[16]), "=r"(r1[17]), "=r"(r1[18]), "=r"(r1[19]), "=r"(r1[20]), "=r"(r1[21]), "=r"(r1[22]), "=r"(r1[23]), "=r"(r1[24]), "=r"(r1[25]), "=r"(r1[26]), "=r"(r1[27]), "=r"(r1[28]), "=r"(r1[29]), "=r"(r1[30]), "=r"(r1[31]), "=r"(r1[32]), "=r"(r1[33]), "=r"(r1[34]), "=r"(r1[35]), "=r"(r1[36]), "=r"(r1[37]), "=r"(r1[38]), "=r"(r1[39]), "=r"(r1[40]), "=r"(r1[41]), "=r"(r1[42]), "=r"(r1[43]), "=r"(r1[44]), "=r"(r1[45]), "=r"(r1[46]), "=r"(r1[47]), "=r"(r1[48]), "=r"(r1[49]), "=r"(r1[50]), "=r"(r1[51]), "=r"(r1[52]), "=r"(r1[53]), "=r"(r1[54]), "=r"(r1[55]), "=r"(r1[56]), "=r"(r1[57]), "=r"(r1[58]), "=r"(r1[59]), "=r"(r1[60]), "=r"(r1[61]), "=r"(r1[62]), "=r"(r1[63])
+      : "r"(taddr0), "r"(taddr1)
+      : "memory");
+}
+
+// Packed pairs of fp32 (two lanes of one 64-bit register) for the f32x2 arithmetic.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t r, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+// d = a * b + c on both halves (round to nearest).
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // ---------------------------------------------------------------------------------------
 // tcgen05.mma, kind::f16 (bf16 inputs, fp32 accumulation in TMEM), single CTA.
 // D[M x N] (+)= A[M x K] * B[K x N], K = 16 per instruction.
