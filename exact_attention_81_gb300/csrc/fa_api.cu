@@ -140,7 +140,7 @@ int decode_chunk(int Lmax, int num_splits) {
   if (num_splits > 0) {
     c = (static_cast<int64_t>(Lmax) + num_splits - 1) / num_splits;
   } else {
-    c = (static_cast<int64_t>(Lmax) + 31) / 32;  // about 32 splits of a full-length cache
+    c = (static_cast<int64_t>(Lmax) + 15) / 16;  // about 16 splits of a full-length cache
     if (c < 256) c = 256;
   }
   c = ((c + 127) / 128) * 128;

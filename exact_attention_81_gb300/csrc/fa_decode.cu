@@ -13,11 +13,16 @@
 //   * a producer warp streams 128-key K and V blocks of the unit with TMA (128B-swizzled
 //     boxes, 2 KB row stride of the cache handled by the tensor map) into a deep ring of
 //     shared-memory slots, so many blocks per SM are in flight at all times;
-//   * 8 compute warps evaluate the G = Hq/Hkv query heads of the group together:
-//       scores   thread = (key, 1/TPK of d), q of its slice in registers, TPK-lane reduce;
-//       softmax  warp g < G owns head g: block max, running (m, l), p = 2^(s - m);
-//       P V      thread = (4 consecutive d, one of NSL key slices), fp32 accumulators
-//                rescaled by 2^(m_old - m_new) per block (online softmax within a unit);
+//   * 8 compute warps evaluate the G = Hq/Hkv query heads of the group together; warp w
+//     owns keys [16w, 16w+16) of every block and keeps its own online-softmax state
+//     (running max m, sum l, fp32 P V accumulators), so a block needs no CTA-wide
+//     synchronisation:
+//       scores   lanes = (key, 1/TPK of d), q of the lane's slice in registers as packed
+//                fp32 pairs (fma.rn.f32x2 over pairs of d), TPK-lane reduce;
+//       softmax  warp-wide max per head, alpha = 2^(m_old - m_new), p = 2^(s - m_new);
+//       P V      lane = 4 consecutive d, packed-pair FMAs, accumulators rescaled by alpha;
+//     at the end of a unit the 8 warps' (m, l, O) are merged (the same LSE-weighted merge
+//     as the split combine);
 //   * each unit writes O_s / l_s (fp32) and LSE_s = ln2 (m + log2 l) to the workspace.
 // Only rows below cache_seqlens[b] are used: a block's tail rows are masked to -inf in the
 // scores and skipped in P V, so values past the visible prefix never enter the result.
@@ -34,8 +39,12 @@ namespace {
 
 constexpr int KB = 128;           // keys per block (one TMA tile per d-box)
 constexpr int NCOMPUTE = 256;     // compute threads (warps 0-7)
-constexpr int NTHREADS = NCOMPUTE + 32;
+constexpr int NTHREADS = 384;     // + warpgroup 2: the TMA producer (warp 8) and 3 idle warps
 constexpr int PRODUCER_WARP = 8;
+// Registers: the producer's warpgroup gives most of its share to the compute warpgroups
+// (2 x 128 x COMPUTE_REGS + 128 x PRODUCER_REGS = 384 threads x 168 at launch).
+constexpr int COMPUTE_REGS = 232;
+constexpr int PRODUCER_REGS = 40;
 constexpr int BOX_BYTES = KB * 128;
 constexpr float LN2 = 0.6931471805599453f;
 
@@ -46,34 +55,37 @@ template <int D, int G>
 struct DCfg {
   static constexpr int KCH = D / 64;
   static constexpr int BLOCK_BYTES = KCH * BOX_BYTES;         // one K or V block
-  static constexpr int TPK = cmax(4, G * D / 128);             // threads per key (scores)
-  static constexpr int DP = D / TPK;                           // d elements per thread
-  static constexpr int KPP = NCOMPUTE / TPK;                   // keys per pass
-  static constexpr int NPASS = KB / KPP;
-  static constexpr int DQ = D / 4;                             // d quads
-  static constexpr int NSL = NCOMPUTE / DQ;                    // key slices in P V
-  static constexpr int SBUF_BYTES = 2 * KB * G * 4;            // double-buffered scores
-  static constexpr int RED_BYTES = NSL * G * D * 4;            // cross-slice reduction
-  static constexpr int MISC_BYTES = 1024;                      // alpha, (m,l), barriers
+  static constexpr int NWARP = NCOMPUTE / 32;                  // compute warps
+  static constexpr int KPW = KB / NWARP;                       // keys of a block per warp
+  static constexpr int TPK = cmax(4, G * D / 128);             // lanes per key (scores)
+  static constexpr int DP = D / TPK;                           // d elements per lane
+  static constexpr int KPASS = 32 / TPK;                       // keys per pass of a warp
+  static constexpr int NPASS = KPW / KPASS;                    // passes per block
+  static constexpr int HPL = (G + TPK - 1) / TPK;              // heads whose p a lane makes
+  static constexpr int DQ = D / 4;                             // d quads (P V lanes)
+  static constexpr int KSPLIT = 32 / DQ;                       // key interleave in P V
+  static constexpr int PW_BYTES = NWARP * KPW * G * 4;         // per-warp probabilities
+  static constexpr int RED_BYTES = NWARP * G * D * 4;          // per-warp outputs at unit end
+  static constexpr int MISC_BYTES = 1024;                      // (m, l) per warp, barriers
   static constexpr int BUDGET = 227 * 1024 - 1024;             // minus alignment slack
   static constexpr int NSLOTS =
-      cmin(12, (BUDGET - SBUF_BYTES - RED_BYTES - MISC_BYTES) / BLOCK_BYTES);
+      cmin(12, (BUDGET - PW_BYTES - RED_BYTES - MISC_BYTES) / BLOCK_BYTES);
   static constexpr int RING_OFF = 0;
-  static constexpr int SBUF_OFF = NSLOTS * BLOCK_BYTES;
-  static constexpr int RED_OFF = SBUF_OFF + SBUF_BYTES;
+  static constexpr int PW_OFF = NSLOTS * BLOCK_BYTES;
+  static constexpr int RED_OFF = PW_OFF + PW_BYTES;
   static constexpr int MISC_OFF = RED_OFF + RED_BYTES;
   static constexpr int SMEM_BYTES = MISC_OFF + MISC_BYTES + 1024;
   static_assert(NSLOTS >= 2, "ring too small");
-  static_assert(KB % KPP == 0, "keys per pass must divide the block");
-  static_assert(TPK <= 32 && (32 % TPK) == 0, "threads per key must tile a warp");
-  static_assert(DP % 8 == 0, "each thread reads whole 16-byte chunks");
+  static_assert(KPW % KPASS == 0, "passes must cover a warp's keys");
+  static_assert(TPK <= 32 && (32 % TPK) == 0, "lanes per key must tile a warp");
+  static_assert(DP % 8 == 0, "each lane reads whole 16-byte chunks");
+  static_assert(DQ <= 32 && (32 % DQ) == 0, "d quads must tile a warp");
 };
 
 struct DBars {
   uint64_t full[12], empty[12];
   uint64_t sync;  // group barrier of the 256 compute threads (bounded wait)
-  float alpha[2][8];
-  float m[8], l[8];
+  float m[8][8], l[8][8];  // [warp][head] running max / sum at the end of a unit
   int abort;
 };
 
@@ -159,29 +171,29 @@ __device__ void compute(const DecodeArgs &a, uint8_t *smem, DBars *bars, const W
                         int tid) {
   using C = DCfg<D, G>;
   const int warp = tid >> 5, lane = tid & 31;
-  // scores mapping
-  const int kl = tid / C::TPK, part = tid % C::TPK;
-  const int d0 = part * C::DP;                 // first d of this thread's slice
-  const int sbox = d0 / 64;                    // box holding the slice
-  const int schunk0 = (d0 % 64) / 8;           // first 16-byte chunk in the 128-byte row
-  // P V mapping
-  const int dq = tid % C::DQ, ks = tid / C::DQ;
+  // scores mapping: lane = (key kl of the pass, slice `part` of d)
+  const int kl = lane / C::TPK, part = lane % C::TPK;
+  const int d0 = part * C::DP;
+  const int sbox = d0 / 64;
+  const int schunk0 = (d0 % 64) / 8;
+  // P V mapping: lane = (d quad dq, key interleave kpar)
+  const int dq = lane % C::DQ, kpar = lane / C::DQ;
   const int vbox = (4 * dq) / 64;
   const int vbyte = ((4 * dq) % 64) * 2;
   const int vchunk = vbyte / 16, vhalf = (vbyte % 16) / 8;
 
-  float *sbuf = reinterpret_cast<float *>(smem + C::SBUF_OFF);
+  float *pw = reinterpret_cast<float *>(smem + C::PW_OFF) + warp * (C::KPW * G);
   float *red = reinterpret_cast<float *>(smem + C::RED_OFF);
   const __nv_bfloat16 *qg = reinterpret_cast<const __nv_bfloat16 *>(a.q);
-  uint32_t it = 0, nblk_done = 0, sync_phase = 0;
+  uint32_t it = 0, sync_phase = 0;
 
   for (int u = blockIdx.x; u < a.num_units; u += gridDim.x) {
     const Unit w = unit_of(a, u);
     if (w.nkeys <= 0) continue;
     const int nblk = (w.nkeys + KB - 1) / KB;
 
-    // q slice of the G heads of group g, pre-scaled into the log2 domain.
-    float qr[G][C::DP];
+    // q slice of the G heads of group g in the log2 domain, as pairs (q[d], q[d+1]).
+    uint64_t q2[G][C::DP / 2];
 #pragma unroll
     for (int gg = 0; gg < G; ++gg) {
       const uint4 *src = reinterpret_cast<const uint4 *>(
@@ -191,23 +203,25 @@ __device__ void compute(const DecodeArgs &a, uint8_t *smem, DBars *bars, const W
         const uint4 x = src[v];
         const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          qr[gg][8 * v + 2 * e] = bf16lo_to_f32(xs[e]) * a.scale_log2;
-          qr[gg][8 * v + 2 * e + 1] = bf16hi_to_f32(xs[e]) * a.scale_log2;
-        }
+        for (int e = 0; e < 4; ++e)
+          q2[gg][4 * v + e] = f2_pack(bf16lo_to_f32(xs[e]) * a.scale_log2,
+                                      bf16hi_to_f32(xs[e]) * a.scale_log2);
       }
     }
-    float acc[G][4];
+    uint64_t acc[G][2];
+    float m[G], l[G];
 #pragma unroll
-    for (int gg = 0; gg < G; ++gg)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) acc[gg][i] = 0.f;
-    float m_run = -INFINITY, l_run = 0.f;  // meaningful in warp `warp` < G (head = warp)
+    for (int gg = 0; gg < G; ++gg) {
+      acc[gg][0] = acc[gg][1] = f2_pack(0.f, 0.f);
+      m[gg] = -INFINITY;
+      l[gg] = 0.f;
+    }
 
     for (int blk = 0; blk < nblk; ++blk) {
       const int nvalid = min(KB, w.nkeys - blk * KB);
-      float *sb = sbuf + (nblk_done & 1u) * (KB * G);
-      // ---- scores from the K block
+      const int kw0 = warp * C::KPW;  // first key of this warp in the block
+      // ---- scores of this warp's keys from the K block
+      float sc[C::NPASS][G];
       {
         const int slot = static_cast<int>(it % C::NSLOTS);
         if (!warp_wait(&bars->full[slot], (it / C::NSLOTS) & 1u, wc)) return;
@@ -215,11 +229,11 @@ __device__ void compute(const DecodeArgs &a, uint8_t *smem, DBars *bars, const W
         const uint8_t *kblk = smem + C::RING_OFF + slot * C::BLOCK_BYTES + sbox * BOX_BYTES;
 #pragma unroll
         for (int pass = 0; pass < C::NPASS; ++pass) {
-          const int key = pass * C::KPP + kl;
+          const int key = kw0 + pass * C::KPASS + kl;
           const uint8_t *krow = kblk + key * 128;
-          float part_s[G];
+          uint64_t s2[G];
 #pragma unroll
-          for (int gg = 0; gg < G; ++gg) part_s[gg] = 0.f;
+          for (int gg = 0; gg < G; ++gg) s2[gg] = f2_pack(0.f, 0.f);
 #pragma unroll
           for (int v = 0; v < C::DP / 8; ++v) {
             const int phys = (schunk0 + v) ^ (key & 7);
@@ -227,79 +241,88 @@ __device__ void compute(const DecodeArgs &a, uint8_t *smem, DBars *bars, const W
             const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float k0 = bf16lo_to_f32(xs[e]);
-              const float k1 = bf16hi_to_f32(xs[e]);
+              const uint64_t k2 = f2_pack(bf16lo_to_f32(xs[e]), bf16hi_to_f32(xs[e]));
 #pragma unroll
-              for (int gg = 0; gg < G; ++gg) {
-                part_s[gg] = fmaf(qr[gg][8 * v + 2 * e], k0, part_s[gg]);
-                part_s[gg] = fmaf(qr[gg][8 * v + 2 * e + 1], k1, part_s[gg]);
-              }
+              for (int gg = 0; gg < G; ++gg) s2[gg] = f2_fma(q2[gg][4 * v + e], k2, s2[gg]);
             }
           }
 #pragma unroll
-          for (int off = C::TPK / 2; off > 0; off >>= 1)
+          for (int gg = 0; gg < G; ++gg) {
+            float lo, hi;
+            f2_unpack(s2[gg], lo, hi);
+            float sv = lo + hi;
 #pragma unroll
-            for (int gg = 0; gg < G; ++gg)
-              part_s[gg] += __shfl_xor_sync(0xffffffffu, part_s[gg], off);
-          if (part == 0) {
-#pragma unroll
-            for (int gg = 0; gg < G; ++gg) sb[key * G + gg] = key < nvalid ? part_s[gg] : -INFINITY;
+            for (int off = C::TPK / 2; off > 0; off >>= 1)
+              sv += __shfl_xor_sync(0xffffffffu, sv, off);
+            sc[pass][gg] = key < nvalid ? sv : -INFINITY;
           }
         }
         release(&bars->empty[slot], lane);
       }
-      if (!group_sync(&bars->sync, sync_phase, wc)) return;
-      // ---- online softmax per head (warp g owns head g)
-      if (warp < G) {
-        float v[KB / 32];
-        float bmax = -INFINITY;
+      // ---- warp-level online softmax over the warp's keys
+      float alpha[G];
 #pragma unroll
-        for (int i = 0; i < KB / 32; ++i) {
-          v[i] = sb[(lane + 32 * i) * G + warp];
-          bmax = fmaxf(bmax, v[i]);
-        }
+      for (int gg = 0; gg < G; ++gg) {
+        float bm = sc[0][gg];
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-          bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, off));
-        const float m_new = fmaxf(m_run, bmax);
+        for (int pass = 1; pass < C::NPASS; ++pass) bm = fmaxf(bm, sc[pass][gg]);
+#pragma unroll
+        for (int off = C::TPK; off < 32; off <<= 1)
+          bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, off));
+        const float m_new = fmaxf(m[gg], bm);
         const float m_use = m_new == -INFINITY ? 0.f : m_new;
-        const float alpha = m_new > m_run ? ex2_approx(m_run - m_use) : 1.f;
-        float psum = 0.f;
+        alpha[gg] = m_new > m[gg] ? ex2_approx(m[gg] - m_use) : 1.f;
+        m[gg] = m_new;
+      }
+      __syncwarp();  // the previous block's P V reads of pw are done
+      float psum[C::HPL];
 #pragma unroll
-        for (int i = 0; i < KB / 32; ++i) {
-          const float p = ex2_approx(v[i] - m_use);
-          sb[(lane + 32 * i) * G + warp] = p;
-          psum += p;
+      for (int i = 0; i < C::HPL; ++i) {
+        psum[i] = 0.f;
+        const int gg = part + i * C::TPK;
+        if (gg < G) {
+          const float m_use = m[gg] == -INFINITY ? 0.f : m[gg];
+#pragma unroll
+          for (int pass = 0; pass < C::NPASS; ++pass) {
+            const float p = ex2_approx(sc[pass][gg] - m_use);
+            pw[(pass * C::KPASS + kl) * G + gg] = p;
+            psum[i] += p;
+          }
         }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) psum += __shfl_xor_sync(0xffffffffu, psum, off);
-        l_run = l_run * alpha + psum;
-        m_run = m_new;
-        if (lane == 0) bars->alpha[nblk_done & 1u][warp] = alpha;
+        for (int off = C::TPK; off < 32; off <<= 1)
+          psum[i] += __shfl_xor_sync(0xffffffffu, psum[i], off);
       }
-      if (!group_sync(&bars->sync, sync_phase, wc)) return;
-      // ---- P V from the V block
+#pragma unroll
+      for (int gg = 0; gg < G; ++gg)
+        l[gg] = l[gg] * alpha[gg] +
+                __shfl_sync(0xffffffffu, psum[gg / C::TPK], gg % C::TPK);
+      __syncwarp();  // pw visible to the whole warp
+      // ---- P V of this warp's keys from the V block
       {
         const int slot = static_cast<int>(it % C::NSLOTS);
         if (!warp_wait(&bars->full[slot], (it / C::NSLOTS) & 1u, wc)) return;
         ++it;
 #pragma unroll
         for (int gg = 0; gg < G; ++gg) {
-          const float al = bars->alpha[nblk_done & 1u][gg];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) acc[gg][i] *= al;
+          const uint64_t al2 = f2_pack(alpha[gg], alpha[gg]);
+          acc[gg][0] = f2_mul(acc[gg][0], al2);
+          acc[gg][1] = f2_mul(acc[gg][1], al2);
         }
         const uint8_t *vblk = smem + C::RING_OFF + slot * C::BLOCK_BYTES + vbox * BOX_BYTES;
-        for (int key = ks; key < nvalid; key += C::NSL) {
+        const int kend = min(C::KPW, nvalid - kw0);
+#pragma unroll 4
+        for (int kk = kpar; kk < kend; kk += C::KSPLIT) {
+          const int key = kw0 + kk;
           const int phys = vchunk ^ (key & 7);
           const uint2 x = *reinterpret_cast<const uint2 *>(vblk + key * 128 + phys * 16 + vhalf * 8);
-          const float v0 = bf16lo_to_f32(x.x), v1 = bf16hi_to_f32(x.x);
-          const float v2 = bf16lo_to_f32(x.y), v3 = bf16hi_to_f32(x.y);
+          const uint64_t v01 = f2_pack(bf16lo_to_f32(x.x), bf16hi_to_f32(x.x));
+          const uint64_t v23 = f2_pack(bf16lo_to_f32(x.y), bf16hi_to_f32(x.y));
           float p[G];
           if constexpr (G % 4 == 0) {
 #pragma unroll
             for (int g4 = 0; g4 < G; g4 += 4) {
-              const float4 pp = *reinterpret_cast<const float4 *>(sb + key * G + g4);
+              const float4 pp = *reinterpret_cast<const float4 *>(pw + kk * G + g4);
               p[g4] = pp.x;
               p[g4 + 1] = pp.y;
               p[g4 + 2] = pp.z;
@@ -307,41 +330,64 @@ __device__ void compute(const DecodeArgs &a, uint8_t *smem, DBars *bars, const W
             }
           } else {
 #pragma unroll
-            for (int gg = 0; gg < G; ++gg) p[gg] = sb[key * G + gg];
+            for (int gg = 0; gg < G; ++gg) p[gg] = pw[kk * G + gg];
           }
 #pragma unroll
           for (int gg = 0; gg < G; ++gg) {
-            acc[gg][0] = fmaf(p[gg], v0, acc[gg][0]);
-            acc[gg][1] = fmaf(p[gg], v1, acc[gg][1]);
-            acc[gg][2] = fmaf(p[gg], v2, acc[gg][2]);
-            acc[gg][3] = fmaf(p[gg], v3, acc[gg][3]);
+            const uint64_t p2 = f2_pack(p[gg], p[gg]);
+            acc[gg][0] = f2_fma(v01, p2, acc[gg][0]);
+            acc[gg][1] = f2_fma(v23, p2, acc[gg][1]);
           }
         }
         release(&bars->empty[slot], lane);
       }
-      ++nblk_done;
     }
 
-    // ---- unit end: reduce the NSL key slices, normalise, write the partial.
+    // ---- unit end: merge the warps' (m, l, O) and write the normalised partial.
+    float o4[G][4];
 #pragma unroll
-    for (int gg = 0; gg < G; ++gg)
-      *reinterpret_cast<float4 *>(red + (ks * G + gg) * D + 4 * dq) =
-          make_float4(acc[gg][0], acc[gg][1], acc[gg][2], acc[gg][3]);
-    if (warp < G && lane == 0) {
-      bars->m[warp] = m_run;
-      bars->l[warp] = l_run;
+    for (int gg = 0; gg < G; ++gg) {
+      f2_unpack(acc[gg][0], o4[gg][0], o4[gg][1]);
+      f2_unpack(acc[gg][1], o4[gg][2], o4[gg][3]);
+      if constexpr (C::KSPLIT > 1) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int off = C::DQ; off < 32; off <<= 1)
+            o4[gg][i] += __shfl_xor_sync(0xffffffffu, o4[gg][i], off);
+      }
+    }
+    if (kpar == 0) {
+#pragma unroll
+      for (int gg = 0; gg < G; ++gg)
+        *reinterpret_cast<float4 *>(red + (warp * G + gg) * D + 4 * dq) =
+            make_float4(o4[gg][0], o4[gg][1], o4[gg][2], o4[gg][3]);
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int gg = 0; gg < G; ++gg) {
+        bars->m[warp][gg] = m[gg];
+        bars->l[warp][gg] = l[gg];
+      }
     }
     if (!group_sync(&bars->sync, sync_phase, wc)) return;
     const int64_t row0 = (static_cast<int64_t>(w.b) * a.Hq + w.g * G) * a.maxch + w.c;
     for (int idx = tid; idx < G * D; idx += NCOMPUTE) {
       const int gg = idx / D, dd = idx - gg * D;
-      float sum = 0.f;
+      float M = -INFINITY;
 #pragma unroll
-      for (int s = 0; s < C::NSL; ++s) sum += red[(s * G + gg) * D + dd];
-      const float l = bars->l[gg];
+      for (int ww = 0; ww < C::NWARP; ++ww) M = fmaxf(M, bars->m[ww][gg]);
+      float L = 0.f, O = 0.f;
+#pragma unroll
+      for (int ww = 0; ww < C::NWARP; ++ww) {
+        const float mw = bars->m[ww][gg];
+        const float wgt = mw == -INFINITY ? 0.f : ex2_approx(mw - M);
+        L = fmaf(bars->l[ww][gg], wgt, L);
+        O = fmaf(red[(ww * G + gg) * D + dd], wgt, O);
+      }
       const int64_t row = row0 + static_cast<int64_t>(gg) * a.maxch;
-      a.o_part[row * D + dd] = sum / l;
-      if (dd == 0) a.lse_part[row] = (bars->m[gg] + log2f(l)) * LN2;
+      a.o_part[row * D + dd] = O / L;
+      if (dd == 0) a.lse_part[row] = (M + log2f(L)) * LN2;
     }
     if (!group_sync(&bars->sync, sync_phase, wc)) return;
   }
@@ -373,13 +419,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
   __syncthreads();
   const WaitCtl wc{&bars->abort, a.err, a.timeout_ns, DEVERR_DECODE_TIMEOUT};
+  // Each register-split branch ends on its own named barrier.
   if (warp < PRODUCER_WARP) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(COMPUTE_REGS));
     compute<D, G>(a, smem, bars, wc, tid);
-  } else if (lane == 0) {
-    producer<D, G>(a, &tmk, &tmv, smem, bars, wc);
+    __syncwarp();
+    named_barrier(1, NTHREADS);
+  } else {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(PRODUCER_REGS));
+    if (warp == PRODUCER_WARP && lane == 0) producer<D, G>(a, &tmk, &tmv, smem, bars, wc);
+    __syncwarp();
+    named_barrier(1, NTHREADS);
   }
-  __syncwarp();
-  __syncthreads();
 }
 
 template <int D, int G>

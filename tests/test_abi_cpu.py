@@ -118,8 +118,8 @@ def test_kvcache_rejects_bad_arguments(lib):
 
 def test_workspace_size(lib):
     ws = lib.fa_fwd_kvcache_workspace_size
-    # automatic chunking: ~32 splits of a full-length cache, chunk >= 256, multiple of 128
-    assert ws(64, 32, 32768, 128, 0) == 64 * 32 * 32 * 129 * 4
+    # automatic chunking: ~16 splits of a full-length cache, chunk >= 256, multiple of 128
+    assert ws(64, 32, 32768, 128, 0) == 64 * 32 * 16 * 129 * 4
     assert ws(1, 1, 100, 64, 0) == ((1 * 1 * 1 * 65 * 4 + 255) // 256) * 256
     assert ws(2, 4, 1000, 64, 3) == 2 * 4 * 3 * 65 * 4 // 256 * 256 + (256 if (2 * 4 * 3 * 65 * 4) % 256 else 0)
     assert ws(0, 4, 100, 64, 0) == 0
