@@ -148,23 +148,146 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- GPU arm
 
+DECODE_METRIC = "split-KV decode GB/s (bf16, KV cache read once) & % of GB300 HBM bandwidth"
+
+
+class DenseCase:
+    """One fa_fwd call over a dense workload; work = FLOPs."""
+
+    def __init__(self, w, dev):
+        import torch
+        from exact_attention_81_gb300.inputs import workload_inputs
+        self.w = w
+        self.q, self.k, self.v = workload_inputs(w, device=dev)
+        self.out = torch.empty_like(self.q)
+        self.lse = torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device=dev)
+        self.work = flops(w)
+        self.launches = 1
+
+    def step(self):
+        import exact_attention_81_gb300 as fa
+        fa.fa_fwd(self.q, self.k, self.v, causal=self.w.causal, out=self.out, lse=self.lse)
+
+    def e2e(self):
+        """Pinned host Q/K/V copied in, O/LSE copied out, every step."""
+        import torch
+        import exact_attention_81_gb300 as fa
+        hq, hk, hv = (t.cpu().pin_memory() for t in (self.q, self.k, self.v))
+        ho = torch.empty(self.out.shape, dtype=self.out.dtype, pin_memory=True)
+        hl = torch.empty(self.lse.shape, dtype=self.lse.dtype, pin_memory=True)
+        dq, dk, dv = (torch.empty_like(t) for t in (self.q, self.k, self.v))
+
+        def run():
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            fa.fa_fwd(dq, dk, dv, causal=self.w.causal, out=self.out, lse=self.lse)
+            ho.copy_(self.out, non_blocking=True)
+            hl.copy_(self.lse, non_blocking=True)
+        h2d = (self.q.numel() + self.k.numel() + self.v.numel()) * 2
+        d2h = self.out.numel() * 2 + self.lse.numel() * 4
+        return run, h2d, d2h
+
+    def describe(self, pk, ms_step, world):
+        w = self.w
+        tf = self.work / (ms_step * 1e-3) / 1e12
+        io = (self.q.numel() + self.k.numel() + self.v.numel()) * 2
+        return {
+            "metric": METRIC, "unit": "TFLOPS", "value": round(world * tf, 2),
+            "config": {"workload": f"{w.name}: B={w.B} Hq={w.Hq} Hkv={w.Hkv} Nq=Nk={w.Nq} "
+                                   f"d={w.d} causal={w.causal} bf16",
+                       "batch": w.B, "heads": w.Hq, "seq_len": w.Nq, "head_dim": w.d,
+                       "causal": w.causal,
+                       "parallelism": f"replicas x{world} (independent heads)",
+                       "l2": f"inputs {io / 1e6:.0f} MB > L2 {L2_BYTES / 1e6:.0f} MB, no flush"},
+            "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": pk["bf16"],
+                         "unit": "TFLOP/s", "frac": round(tf / pk["bf16"], 4),
+                         "traffic": profiled_traffic(f"prefill_kernel<{w.d},{str(w.causal).lower()}>",
+                                                     PREFILL_SRC, w.name),
+                         "peak_basis": f"{pk['basis']} bf16 dense (burst)",
+                         "kernel": f"prefill_kernel<{w.d},{str(w.causal).lower()}> "
+                                   "(one launch per step)"},
+        }
+
+    def e2e_value(self, ms, world):
+        return round(world * self.work / (ms * 1e-3) / 1e12, 2), "TFLOPS"
+
+
+class DecodeCase:
+    """One fa_fwd_kvcache call (split-KV decode + combine); work = bytes of the visible
+    K/V prefix, Q, O and LSE (the split partials are overhead, not counted)."""
+
+    def __init__(self, w, dev):
+        import torch
+        import exact_attention_81_gb300 as fa
+        from exact_attention_81_gb300.inputs import kvcache_workload_inputs
+        self.w = w
+        self.q, self.kc, self.vc, self.lens = kvcache_workload_inputs(w, device=dev)
+        self.ws = torch.empty(fa.fa_fwd_kvcache_workspace_size(w.B, w.Hq, w.Nk, w.d, 0),
+                              dtype=torch.uint8, device=dev)
+        self.out = torch.empty_like(self.q)
+        self.lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
+        kv = int(self.lens.long().sum().item()) * w.Hkv * w.d * 2 * 2
+        self.work = kv + self.q.numel() * 2 * 2 + self.lse.numel() * 4
+        self.launches = 2
+
+    def step(self):
+        import exact_attention_81_gb300 as fa
+        fa.fa_fwd_kvcache(self.q, self.kc, self.vc, self.lens, workspace=self.ws, out=self.out,
+                          lse=self.lse)
+
+    def e2e(self):
+        """The cache is resident state; each step copies the new queries in and the
+        output and LSE back."""
+        import torch
+        import exact_attention_81_gb300 as fa
+        hq = self.q.cpu().pin_memory()
+        ho = torch.empty(self.out.shape, dtype=self.out.dtype, pin_memory=True)
+        hl = torch.empty(self.lse.shape, dtype=self.lse.dtype, pin_memory=True)
+        dq = torch.empty_like(self.q)
+
+        def run():
+            dq.copy_(hq, non_blocking=True)
+            fa.fa_fwd_kvcache(dq, self.kc, self.vc, self.lens, workspace=self.ws,
+                              out=self.out, lse=self.lse)
+            ho.copy_(self.out, non_blocking=True)
+            hl.copy_(self.lse, non_blocking=True)
+        return run, self.q.numel() * 2, self.out.numel() * 2 + self.lse.numel() * 4
+
+    def describe(self, pk, ms_step, world):
+        w = self.w
+        gbs = self.work / (ms_step * 1e-3) / 1e9
+        return {
+            "metric": DECODE_METRIC, "unit": "GB/s", "value": round(world * gbs, 1),
+            "config": {"workload": f"{w.name}: B={w.B} Hq={w.Hq} Hkv={w.Hkv} cache={w.Nk} "
+                                   f"d={w.d} lengths U[{w.Nk // 32},{w.Nk}] bf16",
+                       "batch": w.B, "heads": w.Hq, "kv_heads": w.Hkv, "cache_len": w.Nk,
+                       "head_dim": w.d, "parallelism": f"replicas x{world}",
+                       "l2": f"K/V read {self.work / 1e9:.2f} GB > L2, no flush"},
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"],
+                         "unit": "GB/s", "frac": round(gbs / pk["hbm"], 4),
+                         "traffic": profiled_traffic(f"decode_kernel<{w.d},{w.Hq // w.Hkv}>",
+                                                     DECODE_SRC, w.name),
+                         "peak_basis": f"{pk['basis']} copy bandwidth",
+                         "kernel": f"decode_kernel<{w.d},{w.Hq // w.Hkv}> + combine_kernel"},
+        }
+
+    def e2e_value(self, ms, world):
+        return round(world * self.work / (ms * 1e-3) / 1e9, 1), "GB/s"
+
+
 def run_ours(args, rank, world, dist):
     import torch
     import exact_attention_81_gb300 as fa
-    from exact_attention_81_gb300.inputs import WORKLOADS, kvcache_inputs, workload_inputs
+    from exact_attention_81_gb300.inputs import WORKLOADS
 
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     pk = peaks()
     w = WORKLOADS[args.workload]
+    case = DecodeCase(w, dev) if w.kind == "kvcache" else DenseCase(w, dev)
     stream = torch.cuda.current_stream()
-    q, k, v = workload_inputs(w, device=dev)
-    out = torch.empty_like(q)
-    lse = torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device=dev)
-
-    def step():
-        fa.fa_fwd(q, k, v, causal=w.causal, out=out, lse=lse)
 
     def barrier():
         if dist is not None:
@@ -172,7 +295,7 @@ def run_ours(args, rank, world, dist):
         torch.cuda.synchronize()
 
     for _ in range(max(args.warmup, 3)):
-        step()
+        case.step()
     st = fa.get_last_device_error()
     if st != fa.FA_OK:
         raise RuntimeError(f"device error during warm-up: {fa.status_string(st)}")
@@ -186,7 +309,7 @@ def run_ours(args, rank, world, dist):
     t_wall0 = time.time()
     ev0.record(stream)
     for _ in range(args.steps):
-        step()
+        case.step()
     ev1.record(stream)
     barrier()
     t_wall1 = time.time()
@@ -197,38 +320,21 @@ def run_ours(args, rank, world, dist):
     st = fa.get_last_device_error()
     if st != fa.FA_OK:
         raise RuntimeError(f"device error in the timed region: {fa.status_string(st)}")
-
     ms_step = ms_total / args.steps
     if dist is not None:
         t = torch.tensor([ms_step], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms_step = float(t.item())
-    f = flops(w)
-    value = world * f / (ms_step * 1e-3) / 1e12
 
-    # e2e: pinned host buffers, H2D of Q/K/V and D2H of O/LSE inside the timed region.
-    hq = q.cpu().pin_memory()
-    hk = k.cpu().pin_memory()
-    hv = v.cpu().pin_memory()
-    ho = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-
-    def e2e_step():
-        dq.copy_(hq, non_blocking=True)
-        dk.copy_(hk, non_blocking=True)
-        dv.copy_(hv, non_blocking=True)
-        fa.fa_fwd(dq, dk, dv, causal=w.causal, out=out, lse=lse)
-        ho.copy_(out, non_blocking=True)
-        hl.copy_(lse, non_blocking=True)
-
+    # e2e through the public call with pinned host buffers.
+    e2e_run, h2d, d2h = case.e2e()
     e2e_steps = max(3, min(args.steps, 20))
     for _ in range(3):
-        e2e_step()
+        e2e_run()
     barrier()
     ev0.record(stream)
     for _ in range(e2e_steps):
-        e2e_step()
+        e2e_run()
     ev1.record(stream)
     barrier()
     e2e_ms = ev0.elapsed_time(ev1) / e2e_steps
@@ -236,38 +342,55 @@ def run_ours(args, rank, world, dist):
         t = torch.tensor([e2e_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_ms = float(t.item())
-    h2d = (q.numel() + k.numel() + v.numel()) * 2
-    d2h = out.numel() * 2 + lse.numel() * 4
+    e2e_val, e2e_unit = case.e2e_value(e2e_ms, world)
 
+    d = case.describe(pk, ms_step, world)
     result = {
-        "metric": METRIC, "value": round(value, 2), "unit": "TFLOPS", "n_gpus": world,
+        "metric": d["metric"], "value": d["value"], "unit": d["unit"], "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded iid N(0,1) bf16)",
-        "config": {"workload": f"{w.name}: B={w.B} Hq={w.Hq} Hkv={w.Hkv} Nq=Nk={w.Nq} "
-                               f"d={w.d} causal={w.causal} bf16",
-                   "batch": w.B, "heads": w.Hq, "seq_len": w.Nq, "head_dim": w.d,
-                   "causal": w.causal, "parallelism": f"replicas x{world} (independent heads)",
-                   "l2": f"inputs {h2d / 1e6:.0f} MB > L2 {L2_BYTES / 1e6:.0f} MB, no flush"},
-        "roofline": {"bound": "tensor", "achieved": round(f / (ms_step * 1e-3) / 1e12, 2),
-                     "peak": pk["bf16"], "unit": "TFLOP/s",
-                     "frac": round(f / (ms_step * 1e-3) / 1e12 / pk["bf16"], 4),
-                     "traffic": profiled_traffic("prefill_kernel<128,true>", PREFILL_SRC,
-                                                 w.name),
-                     "peak_basis": f"{pk['basis']} bf16 dense (burst)",
-                     "kernel": "prefill_kernel<128,true> (one launch per step)"},
-        "e2e": {"value": round(world * f / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOPS",
-                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-        "gpu_launches": args.steps,
+        "data": "synthetic (seeded iid N(0,1) bf16)", "config": d["config"],
+        "roofline": d["roofline"],
+        "e2e": {"value": e2e_val, "unit": e2e_unit, "ms_per_step": round(e2e_ms, 4),
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": args.steps * case.launches,
         "clocks": clocks,
     }
-
     if not args.no_extra:
         result["extra"] = extra_workloads(args, dev, pk, world, dist)
     if rank == 0 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(w, q, k, v, args.cpu_seconds)
+        if w.kind == "kvcache":
+            result["cpu_baseline"] = cpu_baseline_decode(case, args.cpu_seconds)
+        else:
+            result["cpu_baseline"] = cpu_baseline(w, case.q, case.k, case.v, args.cpu_seconds)
     return result
+
+
+def cpu_baseline_decode(case, seconds):
+    """The fp64 oracle on a bounded sample of the decode workload's batch entries."""
+    import math
+    import numpy as np
+    import oracle.oracle as ORACLE
+    w = case.w
+    threads = os.cpu_count() or 1
+    lens = case.lens.cpu()
+    scale = float(np.float32(1 / math.sqrt(w.d)))
+    nb = 1
+    while True:
+        sel = list(range(nb))
+        top = int(lens[:nb].max())
+        q = case.q[:nb].cpu()
+        kc = case.kc[:nb, :top].cpu()
+        vc = case.vc[:nb, :top].cpu()
+        t0 = time.time()
+        ORACLE.attention_kvcache(q, kc, vc, lens[:nb], scale, nthreads=threads)
+        dt = time.time() - t0
+        if dt >= seconds / 4 or nb >= w.B:
+            break
+        nb = min(w.B, nb * 2)
+    byts = int(lens[:nb].long().sum()) * w.Hkv * w.d * 4
+    return {"value": byts / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{nb} of {w.B} batch entries of {w.name} (fp64, {dt:.1f} s)"}
 
 
 def time_calls(fn, steps, stream, warm=3):
@@ -288,7 +411,7 @@ def time_calls(fn, steps, stream, warm=3):
 def extra_workloads(args, dev, pk, world, dist):
     import torch
     import exact_attention_81_gb300 as fa
-    from exact_attention_81_gb300.inputs import WORKLOADS, kvcache_inputs, workload_inputs
+    from exact_attention_81_gb300.inputs import WORKLOADS, kvcache_workload_inputs, workload_inputs
     stream = torch.cuda.current_stream()
     res = {}
     for name in ("dense2k", "gqa16k"):
@@ -303,7 +426,7 @@ def extra_workloads(args, dev, pk, world, dist):
                      "frac_of_bf16_peak": round(tf / pk["bf16"], 4)}
         del q, k, v, o, l
     w = WORKLOADS["decode"]
-    q, kc, vc, lens = kvcache_inputs(w.B, w.Nk, w.Hq, w.Hkv, w.d, seed=w.seed, device=dev)
+    q, kc, vc, lens = kvcache_workload_inputs(w, device=dev)
     ws = torch.empty(fa.fa_fwd_kvcache_workspace_size(w.B, w.Hq, w.Nk, w.d, 0), dtype=torch.uint8,
                      device=dev)
     o = torch.empty_like(q)
@@ -369,10 +492,46 @@ def cpu_baseline(w, q, k, v, seconds):
             "sample": f"{n} random query rows of {w.name} (fp64, {dt:.1f} s)"}
 
 
+def run_reference_decode(args, w):
+    """The fp64 oracle on a few batch entries of the decode workload per step."""
+    import math
+    import numpy as np
+    import oracle.oracle as ORACLE
+    from exact_attention_81_gb300.inputs import kvcache_workload_entry
+    threads = os.cpu_count() or 1
+    scale = float(np.float32(1 / math.sqrt(w.d)))
+    steps = []
+    for s in range(args.warmup + args.steps):
+        b = s % w.B
+        q, kc, vc, n = kvcache_workload_entry(w, b)
+        t0 = time.time()
+        ORACLE.attention_kvcache(q, kc, vc, [n], scale, nthreads=threads)
+        dt = time.time() - t0
+        if s >= args.warmup:
+            steps.append((n * w.Hkv * w.d * 4, dt))
+    value = sum(x for x, _ in steps) / sum(t for _, t in steps) / 1e9
+    return {
+        "impl": "reference", "metric": DECODE_METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(sum(t for _, t in steps) / len(steps) * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded iid N(0,1) bf16)",
+        "config": {"workload": f"{w.name}: B={w.B} Hq={w.Hq} Hkv={w.Hkv} cache={w.Nk} "
+                               f"d={w.d} lengths U[{w.Nk // 32},{w.Nk}] bf16"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": f"one batch entry of {w.name} per step (fp64)"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
 def run_reference(args, w):
     import numpy as np
     import oracle.oracle as ORACLE
     from exact_attention_81_gb300.inputs import workload_inputs
+    if w.kind == "kvcache":
+        return run_reference_decode(args, w)
     q, k, v = workload_inputs(w, device="cpu")
     threads = os.cpu_count() or 1
     # size one step so that warm-up + timed steps stay within a few minutes

@@ -44,6 +44,8 @@ WORKLOADS = {
     "causal8k": Workload("causal8k", "dense", 2, 32, 32, 8192, 8192, 128, True, 1003),
     "gqa16k": Workload("gqa16k", "dense", 1, 32, 8, 16384, 16384, 128, True, 1004),
     "decode": Workload("decode", "kvcache", 64, 32, 8, 1, 32768, 128, False, 1005),
+    # a smaller decode case (537 MB of cache) for profiling captures
+    "decode16": Workload("decode16", "kvcache", 16, 32, 8, 1, 8192, 128, False, 1006),
 }
 
 
@@ -108,3 +110,25 @@ def kvcache_inputs(B, Lmax, Hq, Hkv, d, seed, lengths=None, device="cpu", poison
             kc[b, n:] = float("nan")
             vc[b, n:] = float("nan")
     return q, kc, vc, lengths.to(device)
+
+
+def kvcache_workload_inputs(w: Workload, device="cpu", seed=None):
+    """Inputs of a decode workload: lengths uniform in [Lmax/32, Lmax] (the decode
+    workload's [1024, 32768]) from a CPU generator seeded like the tensors."""
+    s = w.seed if seed is None else seed
+    lens = decode_lengths(w.B, lo=max(1, w.Nk // 32), hi=w.Nk, seed=s)
+    return kvcache_inputs(w.B, w.Nk, w.Hq, w.Hkv, w.d, seed=s, lengths=lens, device=device)
+
+
+def kvcache_workload_entry(w: Workload, b: int, device="cpu", seed=None):
+    """Batch entry b of kvcache_workload_inputs(w) without drawing the others:
+    (q [1,1,Hq,d], k_cache [1,Lmax,Hkv,d], v_cache [1,Lmax,Hkv,d], length)."""
+    s = w.seed if seed is None else seed
+    lens = decode_lengths(w.B, lo=max(1, w.Nk // 32), hi=w.Nk, seed=s)
+    q = bf16_normal((w.B, 1, w.Hq, w.d), s, device)[b:b + 1]
+    kc = bf16_normal((w.Nk, w.Hkv, w.d), s * 1000003 + 2 * b + 1, device).unsqueeze(0)
+    vc = bf16_normal((w.Nk, w.Hkv, w.d), s * 1000003 + 2 * b + 2, device).unsqueeze(0)
+    n = int(lens[b])
+    kc[0, n:] = float("nan")
+    vc[0, n:] = float("nan")
+    return q, kc, vc, int(lens[b])
