@@ -151,6 +151,22 @@ class ClockSampler:
 DECODE_METRIC = "split-KV decode GB/s (bf16, KV cache read once) & % of GB300 HBM bandwidth"
 
 
+def max_over_ranks(ms: float, dist, device) -> float:
+    """Step time of the job: the slowest rank's (identity without a process group)."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(work_per_rank: float, ms_step: float, world: int, scale: float) -> float:
+    """Whole-job throughput under weak scaling: every rank processes `work_per_rank`
+    units per step; the job's step takes the slowest rank's time."""
+    return world * work_per_rank / (ms_step * 1e-3) / scale
+
+
 class DenseCase:
     """One fa_fwd call over a dense workload; work = FLOPs."""
 
@@ -193,7 +209,8 @@ class DenseCase:
         tf = self.work / (ms_step * 1e-3) / 1e12
         io = (self.q.numel() + self.k.numel() + self.v.numel()) * 2
         return {
-            "metric": METRIC, "unit": "TFLOPS", "value": round(world * tf, 2),
+            "metric": METRIC, "unit": "TFLOPS",
+            "value": round(job_value(self.work, ms_step, world, 1e12), 2),
             "config": {"workload": f"{w.name}: B={w.B} Hq={w.Hq} Hkv={w.Hkv} Nq=Nk={w.Nq} "
                                    f"d={w.d} causal={w.causal} bf16",
                        "batch": w.B, "heads": w.Hq, "seq_len": w.Nq, "head_dim": w.d,
@@ -210,7 +227,7 @@ class DenseCase:
         }
 
     def e2e_value(self, ms, world):
-        return round(world * self.work / (ms * 1e-3) / 1e12, 2), "TFLOPS"
+        return round(job_value(self.work, ms, world, 1e12), 2), "TFLOPS"
 
 
 class DecodeCase:
@@ -258,7 +275,8 @@ class DecodeCase:
         w = self.w
         gbs = self.work / (ms_step * 1e-3) / 1e9
         return {
-            "metric": DECODE_METRIC, "unit": "GB/s", "value": round(world * gbs, 1),
+            "metric": DECODE_METRIC, "unit": "GB/s",
+            "value": round(job_value(self.work, ms_step, world, 1e9), 1),
             "config": {"workload": f"{w.name}: B={w.B} Hq={w.Hq} Hkv={w.Hkv} cache={w.Nk} "
                                    f"d={w.d} lengths U[{w.Nk // 32},{w.Nk}] bf16",
                        "batch": w.B, "heads": w.Hq, "kv_heads": w.Hkv, "cache_len": w.Nk,
@@ -273,7 +291,7 @@ class DecodeCase:
         }
 
     def e2e_value(self, ms, world):
-        return round(world * self.work / (ms * 1e-3) / 1e9, 1), "GB/s"
+        return round(job_value(self.work, ms, world, 1e9), 1), "GB/s"
 
 
 def run_ours(args, rank, world, dist):
@@ -320,11 +338,7 @@ def run_ours(args, rank, world, dist):
     st = fa.get_last_device_error()
     if st != fa.FA_OK:
         raise RuntimeError(f"device error in the timed region: {fa.status_string(st)}")
-    ms_step = ms_total / args.steps
-    if dist is not None:
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(ms_total / args.steps, dist, dev)
 
     # e2e through the public call with pinned host buffers.
     e2e_run, h2d, d2h = case.e2e()
@@ -337,11 +351,7 @@ def run_ours(args, rank, world, dist):
         e2e_run()
     ev1.record(stream)
     barrier()
-    e2e_ms = ev0.elapsed_time(ev1) / e2e_steps
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(ev0.elapsed_time(ev1) / e2e_steps, dist, dev)
     e2e_val, e2e_unit = case.e2e_value(e2e_ms, world)
 
     d = case.describe(pk, ms_step, world)
