@@ -190,3 +190,22 @@ def test_full_size_workload(name):
         kk = k.float().repeat_interleave(G, dim=2)
         diag = (q.float() * kk).sum(-1) * w.scale  # [B, N, Hq]
         assert (lse >= diag.transpose(1, 2) - 1e-3).all()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("direction", ["rising", "falling"])
+def test_row_max_jumps_across_tiles(direction, causal):
+    """Key norms that rise (or fall) steeply along the sequence make each row's maximum
+    jump by far more than a factor 2^8 from one 128-key tile to the next (or never grow
+    after the first tile): both the rescale and the keep-the-reference paths of the online
+    softmax are exercised."""
+    B, N, H, d = 1, 700, 2, 64
+    q, k, v = dense_inputs(B, N, N, H, H, d, seed=91, device=DEV)
+    ramp = torch.linspace(0.2, 6.0, N, device=DEV)
+    if direction == "falling":
+        ramp = ramp.flip(0)
+    k = (k.float() * ramp[None, :, None, None]).to(torch.bfloat16)
+    scale = 0.9
+    o, lse = _run_dense(q, k, v, causal, scale=scale)
+    o_ref, lse_ref = _oracle_dense(q, k, v, causal, float(np.float32(scale)))
+    compare(*dense_rows(o, lse), *dense_rows(o_ref, lse_ref), f"max jumps {direction}")
