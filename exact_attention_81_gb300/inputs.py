@@ -49,19 +49,18 @@ WORKLOADS = {
 }
 
 
-def bf16_normal(shape, seed: int, device="cpu") -> torch.Tensor:
-    """iid N(0,1) float32 draws from a seeded generator, rounded to bf16."""
+def bf16_normal(shape, seed: int, device="cpu", dtype=torch.bfloat16) -> torch.Tensor:
+    """iid N(0,1) float32 draws from a seeded generator, rounded to bf16 (or fp16)."""
     g = torch.Generator(device=device)
     g.manual_seed(int(seed))
-    return torch.randn(tuple(shape), dtype=torch.float32, generator=g, device=device).to(
-        torch.bfloat16)
+    return torch.randn(tuple(shape), dtype=torch.float32, generator=g, device=device).to(dtype)
 
 
-def dense_inputs(B, Nq, Nk, Hq, Hkv, d, seed, device="cpu"):
+def dense_inputs(B, Nq, Nk, Hq, Hkv, d, seed, device="cpu", dtype=torch.bfloat16):
     """Q [B,Nq,Hq,d], K/V [B,Nk,Hkv,d] in the (batch, seqlen, nheads, headdim) layout."""
-    q = bf16_normal((B, Nq, Hq, d), seed, device)
-    k = bf16_normal((B, Nk, Hkv, d), seed + 7919, device)
-    v = bf16_normal((B, Nk, Hkv, d), seed + 15823, device)
+    q = bf16_normal((B, Nq, Hq, d), seed, device, dtype)
+    k = bf16_normal((B, Nk, Hkv, d), seed + 7919, device, dtype)
+    v = bf16_normal((B, Nk, Hkv, d), seed + 15823, device, dtype)
     return q, k, v
 
 
@@ -70,16 +69,16 @@ def workload_inputs(w: Workload, device="cpu", seed=None):
     return dense_inputs(w.B, w.Nq, w.Nk, w.Hq, w.Hkv, w.d, s, device)
 
 
-def varlen_inputs(seqlens_q, seqlens_k, Hq, Hkv, d, seed, device="cpu"):
+def varlen_inputs(seqlens_q, seqlens_k, Hq, Hkv, d, seed, device="cpu", dtype=torch.bfloat16):
     """Packed Q [total_q,Hq,d], K/V [total_k,Hkv,d] and int32 prefix sums [B+1]."""
     sq = torch.tensor([0] + list(seqlens_q), dtype=torch.int64)
     sk = torch.tensor([0] + list(seqlens_k), dtype=torch.int64)
     cu_q = torch.cumsum(sq, 0).to(torch.int32)
     cu_k = torch.cumsum(sk, 0).to(torch.int32)
     tq, tk = int(cu_q[-1]), int(cu_k[-1])
-    q = bf16_normal((tq, Hq, d), seed, device)
-    k = bf16_normal((tk, Hkv, d), seed + 7919, device)
-    v = bf16_normal((tk, Hkv, d), seed + 15823, device)
+    q = bf16_normal((tq, Hq, d), seed, device, dtype)
+    k = bf16_normal((tk, Hkv, d), seed + 7919, device, dtype)
+    v = bf16_normal((tk, Hkv, d), seed + 15823, device, dtype)
     return q, k, v, cu_q.to(device), cu_k.to(device)
 
 
@@ -90,7 +89,8 @@ def decode_lengths(B, lo=1024, hi=32768, seed=1005) -> torch.Tensor:
     return torch.randint(lo, hi + 1, (B,), generator=g, dtype=torch.int64).to(torch.int32)
 
 
-def kvcache_inputs(B, Lmax, Hq, Hkv, d, seed, lengths=None, device="cpu", poison=True):
+def kvcache_inputs(B, Lmax, Hq, Hkv, d, seed, lengths=None, device="cpu", poison=True,
+                   dtype=torch.bfloat16):
     """Q [B,1,Hq,d], padded caches [B,Lmax,Hkv,d], lengths int32 [B].
 
     Rows at or past lengths[b] are NaN when ``poison`` is set.  The cache is drawn
@@ -99,12 +99,12 @@ def kvcache_inputs(B, Lmax, Hq, Hkv, d, seed, lengths=None, device="cpu", poison
     if lengths is None:
         lengths = decode_lengths(B, seed=seed)
     lengths = torch.as_tensor(lengths, dtype=torch.int32).cpu()
-    q = bf16_normal((B, 1, Hq, d), seed, device)
-    kc = torch.empty((B, Lmax, Hkv, d), dtype=torch.bfloat16, device=device)
-    vc = torch.empty((B, Lmax, Hkv, d), dtype=torch.bfloat16, device=device)
+    q = bf16_normal((B, 1, Hq, d), seed, device, dtype)
+    kc = torch.empty((B, Lmax, Hkv, d), dtype=dtype, device=device)
+    vc = torch.empty((B, Lmax, Hkv, d), dtype=dtype, device=device)
     for b in range(B):
-        kc[b] = bf16_normal((Lmax, Hkv, d), seed * 1000003 + 2 * b + 1, device)
-        vc[b] = bf16_normal((Lmax, Hkv, d), seed * 1000003 + 2 * b + 2, device)
+        kc[b] = bf16_normal((Lmax, Hkv, d), seed * 1000003 + 2 * b + 1, device, dtype)
+        vc[b] = bf16_normal((Lmax, Hkv, d), seed * 1000003 + 2 * b + 2, device, dtype)
         if poison:
             n = int(lengths[b])
             kc[b, n:] = float("nan")

@@ -30,8 +30,10 @@
  *   - single-query decode attends to the first cache_seqlens[b] rows of the cache
  *     ("flash-attention", capabilities table, KV cache row; section 1 usage).
  *
- * Inputs are bf16 bit patterns (uint16).  Each is widened exactly to double, so the
- * oracle sees the same numbers the GPU sees; all arithmetic is IEEE double.
+ * Inputs are 16-bit float bit patterns (uint16): bf16 (elem = 0) or IEEE binary16
+ * (elem = 1), the two element types of the fused kernels ("flash-attention", section 5:
+ * fp16 / bf16 only).  Each is widened exactly to double, so the oracle sees the same
+ * numbers the GPU sees; all arithmetic is IEEE double.
  * Work is spread over threads by query row; the arithmetic of a row does not depend
  * on the thread count.
  */
@@ -49,6 +51,21 @@ static double bf16_to_double(uint16_t bits) {
     return (double)f;
 }
 
+/* IEEE binary16 bits -> exact double: sign, 5-bit exponent (bias 15), 10-bit fraction. */
+static double fp16_to_double(uint16_t bits) {
+    int sign = bits >> 15, e = (bits >> 10) & 0x1f, f = bits & 0x3ff;
+    double v;
+    if (e == 0) v = ldexp((double)f, -24);                 /* subnormal: f * 2^-24 */
+    else if (e == 31) v = f ? NAN : INFINITY;
+    else v = ldexp((double)(f | 0x400), e - 25);           /* (1024 + f) * 2^(e - 15 - 10) */
+    return sign ? -v : v;
+}
+
+/* Element type of the current job (0 bf16, 1 fp16); set per call before any worker runs. */
+static double widen(uint16_t bits, int elem) {
+    return elem ? fp16_to_double(bits) : bf16_to_double(bits);
+}
+
 /*
  * One query row against keys 0..nkeys-1 (the visible set).
  * q      : d bf16 values
@@ -60,7 +77,7 @@ static double bf16_to_double(uint16_t bits) {
  */
 static void attend_row(const uint16_t *q, const uint16_t *kbase, int64_t k_stride,
                        const uint16_t *vbase, int64_t v_stride, int64_t nkeys, int d,
-                       double scale, double *s, double *o, double *lse) {
+                       double scale, int elem, double *s, double *o, double *lse) {
     for (int c = 0; c < d; ++c) o[c] = 0.0;
     if (nkeys <= 0) {
         *lse = -INFINITY;
@@ -70,7 +87,7 @@ static void attend_row(const uint16_t *q, const uint16_t *kbase, int64_t k_strid
     for (int64_t j = 0; j < nkeys; ++j) {
         const uint16_t *kr = kbase + j * k_stride;
         double acc = 0.0;
-        for (int c = 0; c < d; ++c) acc += bf16_to_double(q[c]) * bf16_to_double(kr[c]);
+        for (int c = 0; c < d; ++c) acc += widen(q[c], elem) * widen(kr[c], elem);
         s[j] = scale * acc;
     }
     /* stable softmax: m = max_j s_j, l = sum_j e^{s_j - m}, P_j = e^{s_j - m} / l */
@@ -86,7 +103,7 @@ static void attend_row(const uint16_t *q, const uint16_t *kbase, int64_t k_strid
     /* O = P V */
     for (int64_t j = 0; j < nkeys; ++j) {
         const uint16_t *vr = vbase + j * v_stride;
-        for (int c = 0; c < d; ++c) o[c] += s[j] * bf16_to_double(vr[c]);
+        for (int c = 0; c < d; ++c) o[c] += s[j] * widen(vr[c], elem);
     }
     *lse = m + log(l);
 }
@@ -121,6 +138,7 @@ typedef struct {
     int64_t os[3];      /* output strides (b, n, h) for the full drivers */
     int64_t lse_s[3];   /* lse strides (b, h, n) */
     int mode;           /* 0 dense, 1 varlen, 2 kvcache */
+    int elem;           /* 0 bf16, 1 fp16 */
     int nthreads, tid;
     int64_t total;      /* number of (b, h, i) work items */
 } job_t;
@@ -189,7 +207,8 @@ static void *worker(void *arg) {
             nkeys = J->cache_len[b];
         }
         double lse;
-        attend_row(qrow, kbase, k_stride, vbase, v_stride, nkeys, J->d, J->scale, s, orow, &lse);
+        attend_row(qrow, kbase, k_stride, vbase, v_stride, nkeys, J->d, J->scale, J->elem, s, orow,
+                   &lse);
         double *odst;
         double *ldst;
         if (J->rows) {
@@ -239,8 +258,8 @@ static int run_threads(job_t *base) {
 int oracle_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int Nq, int Nk,
                int Hq, int Hkv, int d, const int64_t *q_strides, const int64_t *k_strides,
                const int64_t *v_strides, double scale, int causal, double *o, double *lse,
-               int nthreads) {
-    if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0) return -1;
+               int nthreads, int elem) {
+    if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || elem < 0 || elem > 1) return -1;
     job_t J;
     memset(&J, 0, sizeof J);
     J.q = q; J.k = k; J.v = v;
@@ -252,6 +271,7 @@ int oracle_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, i
     J.lse_s[0] = (int64_t)Hq * Nq; J.lse_s[1] = Nq; J.lse_s[2] = 1;
     J.mode = 0;
     J.nthreads = nthreads;
+    J.elem = elem;
     J.total = (int64_t)B * Nq * Hq;
     return run_threads(&J);
 }
@@ -263,8 +283,8 @@ int oracle_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, i
 int oracle_fwd_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int Nq, int Nk,
                     int Hq, int Hkv, int d, const int64_t *q_strides, const int64_t *k_strides,
                     const int64_t *v_strides, double scale, int causal, const int32_t *rows,
-                    int64_t n, double *o, double *lse, int nthreads) {
-    if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0) return -1;
+                    int64_t n, double *o, double *lse, int nthreads, int elem) {
+    if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || elem < 0 || elem > 1) return -1;
     job_t J;
     memset(&J, 0, sizeof J);
     J.q = q; J.k = k; J.v = v;
@@ -275,6 +295,7 @@ int oracle_fwd_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v, int
     J.o = o; J.lse = lse;
     J.mode = 0;
     J.nthreads = nthreads;
+    J.elem = elem;
     J.total = n;
     return run_threads(&J);
 }
@@ -287,8 +308,8 @@ int oracle_fwd_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v, int
 int oracle_fwd_varlen(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                       const int32_t *cu_q, const int32_t *cu_k, int B, int Hq, int Hkv, int d,
                       const int64_t *q_strides, const int64_t *k_strides, const int64_t *v_strides,
-                      double scale, int causal, double *o, double *lse, int nthreads) {
-    if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0) return -1;
+                      double scale, int causal, double *o, double *lse, int nthreads, int elem) {
+    if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || elem < 0 || elem > 1) return -1;
     job_t J;
     memset(&J, 0, sizeof J);
     J.q = q; J.k = k; J.v = v;
@@ -307,6 +328,7 @@ int oracle_fwd_varlen(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     J.lse_s[0] = 0; J.lse_s[1] = total_q; J.lse_s[2] = 1;
     J.mode = 1;
     J.nthreads = nthreads;
+    J.elem = elem;
     J.total = total_q * Hq;
     return run_threads(&J);
 }
@@ -319,8 +341,8 @@ int oracle_fwd_varlen(const uint16_t *q, const uint16_t *k, const uint16_t *v,
 int oracle_fwd_kvcache(const uint16_t *q, const uint16_t *kc, const uint16_t *vc,
                        const int32_t *cache_len, int B, int Lmax, int Hq, int Hkv, int d,
                        const int64_t *q_strides, const int64_t *k_strides, const int64_t *v_strides,
-                       double scale, double *o, double *lse, int nthreads) {
-    if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0) return -1;
+                       double scale, double *o, double *lse, int nthreads, int elem) {
+    if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || elem < 0 || elem > 1) return -1;
     for (int b = 0; b < B; ++b)
         if (cache_len[b] < 0 || cache_len[b] > Lmax) return -1;
     job_t J;
@@ -335,6 +357,7 @@ int oracle_fwd_kvcache(const uint16_t *q, const uint16_t *kc, const uint16_t *vc
     J.lse_s[0] = Hq; J.lse_s[1] = 1; J.lse_s[2] = 0;
     J.mode = 2;
     J.nthreads = nthreads;
+    J.elem = elem;
     J.total = (int64_t)B * Hq;
     return run_threads(&J);
 }
@@ -346,8 +369,10 @@ int oracle_fwd_kvcache(const uint16_t *q, const uint16_t *kc, const uint16_t *vc
 int oracle_row_probs(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int Nq, int Nk,
                      int Hq, int Hkv, int d, const int64_t *q_strides, const int64_t *k_strides,
                      const int64_t *v_strides, double scale, int causal, int b, int h, int i,
-                     double *p_out) {
-    if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || b >= B || h >= Hq || i >= Nq) return -1;
+                     double *p_out, int elem) {
+    if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || b >= B || h >= Hq || i >= Nq || elem < 0 ||
+        elem > 1)
+        return -1;
     int g = h / (Hq / Hkv);
     int64_t nkeys = visible_keys(i, Nq, Nk, causal);
     double *s = (double *)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
@@ -355,8 +380,8 @@ int oracle_row_probs(const uint16_t *q, const uint16_t *k, const uint16_t *v, in
     double lse;
     attend_row(q + b * q_strides[0] + (int64_t)i * q_strides[1] + h * q_strides[2],
                k + b * k_strides[0] + g * k_strides[2], k_strides[1],
-               v + b * v_strides[0] + g * v_strides[2], v_strides[1], nkeys, d, scale, s, orow,
-               &lse);
+               v + b * v_strides[0] + g * v_strides[2], v_strides[1], nkeys, d, scale, elem, s,
+               orow, &lse);
     for (int64_t j = 0; j < Nk; ++j) p_out[j] = j < nkeys ? s[j] : 0.0;
     free(s);
     free(orow);

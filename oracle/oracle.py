@@ -5,9 +5,10 @@ binding) never imports this module; only the tests, ``__graft_entry__.smoke()``
 and the CPU-baseline leg of ``bench.py`` do.  It shares no code with the CUDA
 path: the C source is compiled here with gcc into ``oracle/_build``.
 
-Every function takes bf16 inputs as their 16-bit patterns (numpy ``uint16``) so
-that the oracle reads exactly the numbers the GPU reads, widens them exactly to
-double and computes the plain definition of attention
+Every function takes bf16 or fp16 inputs (torch tensors, or their 16-bit patterns as
+numpy ``uint16`` with ``elem`` = 0 for bf16, 1 for fp16) so that the oracle reads
+exactly the numbers the GPU reads, widens them exactly to double and computes the
+plain definition of attention
 ("FlashAttention 1-4 详解", section 原算法: S = Q K^T, P = softmax(scale * S),
 O = P V; plus the natural-log log-sum-exp of each row of scaled scores).
 """
@@ -52,13 +53,14 @@ def _load():
             i = ctypes.c_int
             i64 = ctypes.c_int64
             d = ctypes.c_double
-            lib.oracle_fwd.argtypes = [p, p, p, i, i, i, i, i, i, p, p, p, d, i, p, p, i]
+            lib.oracle_fwd.argtypes = [p, p, p, i, i, i, i, i, i, p, p, p, d, i, p, p, i, i]
             lib.oracle_fwd_rows.argtypes = [p, p, p, i, i, i, i, i, i, p, p, p, d, i, p, i64,
-                                            p, p, i]
-            lib.oracle_fwd_varlen.argtypes = [p, p, p, p, p, i, i, i, i, p, p, p, d, i, p, p, i]
-            lib.oracle_fwd_kvcache.argtypes = [p, p, p, p, i, i, i, i, i, p, p, p, d, p, p, i]
+                                            p, p, i, i]
+            lib.oracle_fwd_varlen.argtypes = [p, p, p, p, p, i, i, i, i, p, p, p, d, i, p, p, i,
+                                              i]
+            lib.oracle_fwd_kvcache.argtypes = [p, p, p, p, i, i, i, i, i, p, p, p, d, p, p, i, i]
             lib.oracle_row_probs.argtypes = [p, p, p, i, i, i, i, i, i, p, p, p, d, i, i, i, i,
-                                             p]
+                                             p, i]
             for f in (lib.oracle_fwd, lib.oracle_fwd_rows, lib.oracle_fwd_varlen,
                       lib.oracle_fwd_kvcache, lib.oracle_row_probs):
                 f.restype = ctypes.c_int
@@ -70,15 +72,31 @@ def _threads(n):
     return int(n) if n else (os.cpu_count() or 1)
 
 
+_ELEM = {"torch.bfloat16": 0, "torch.float16": 1}
+
+
+def _elem_of(a, default=0) -> int:
+    return _ELEM.get(str(getattr(a, "dtype", "")), default)
+
+
 def _bits(a) -> np.ndarray:
-    """Accept a numpy uint16 array or a torch bf16 tensor; return uint16 bits."""
-    if hasattr(a, "dtype") and str(a.dtype) == "torch.bfloat16":
+    """Accept a numpy uint16 array or a torch bf16 / fp16 tensor; return uint16 bits."""
+    if str(getattr(a, "dtype", "")) in _ELEM:
         import torch  # local: only the tests hand torch tensors in
         a = a.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
     a = np.ascontiguousarray(a)
     if a.dtype != np.uint16:
-        raise TypeError("oracle inputs are bf16 bit patterns (uint16)")
+        raise TypeError("oracle inputs are 16-bit float bit patterns (uint16)")
     return a
+
+
+def _common_elem(*ts, elem=None) -> int:
+    if elem is not None:
+        return int(elem)
+    kinds = {_elem_of(t) for t in ts}
+    if len(kinds) != 1:
+        raise TypeError("q, k and v must share one element type")
+    return kinds.pop()
 
 
 def _strides4(a: np.ndarray):
@@ -91,11 +109,13 @@ def _ptr(a: np.ndarray):
     return a.ctypes.data_as(ctypes.c_void_p)
 
 
-def attention(q, k, v, scale: float, causal: bool = False, nthreads: int | None = None):
-    """Dense attention.  q [B,Nq,Hq,d], k/v [B,Nk,Hkv,d] (bf16 bits).
+def attention(q, k, v, scale: float, causal: bool = False, nthreads: int | None = None,
+              elem=None):
+    """Dense attention.  q [B,Nq,Hq,d], k/v [B,Nk,Hkv,d] (bf16 or fp16).
 
     Returns (O [B,Nq,Hq,d] float64, LSE [B,Hq,Nq] float64).
     """
+    el = _common_elem(q, k, v, elem=elem)
     q, k, v = _bits(q), _bits(k), _bits(v)
     B, Nq, Hq, d = q.shape
     _, Nk, Hkv, _ = k.shape
@@ -103,18 +123,19 @@ def attention(q, k, v, scale: float, causal: bool = False, nthreads: int | None 
     lse = np.zeros((B, Hq, Nq), np.float64)
     rc = _load().oracle_fwd(_ptr(q), _ptr(k), _ptr(v), B, Nq, Nk, Hq, Hkv, d, _strides4(q),
                             _strides4(k), _strides4(v), float(scale), int(bool(causal)),
-                            _ptr(o), _ptr(lse), _threads(nthreads))
+                            _ptr(o), _ptr(lse), _threads(nthreads), el)
     if rc != 0:
         raise ValueError("oracle_fwd rejected its arguments")
     return o, lse
 
 
 def attention_rows(q, k, v, rows, scale: float, causal: bool = False,
-                   nthreads: int | None = None):
+                   nthreads: int | None = None, elem=None):
     """Dense attention on selected rows; rows is an (n, 3) int array of (b, h, i).
 
     Returns (O [n, d] float64, LSE [n] float64).
     """
+    el = _common_elem(q, k, v, elem=elem)
     q, k, v = _bits(q), _bits(k), _bits(v)
     B, Nq, Hq, d = q.shape
     _, Nk, Hkv, _ = k.shape
@@ -125,18 +146,19 @@ def attention_rows(q, k, v, rows, scale: float, causal: bool = False,
     rc = _load().oracle_fwd_rows(_ptr(q), _ptr(k), _ptr(v), B, Nq, Nk, Hq, Hkv, d,
                                  _strides4(q), _strides4(k), _strides4(v), float(scale),
                                  int(bool(causal)), _ptr(rows), n, _ptr(o), _ptr(lse),
-                                 _threads(nthreads))
+                                 _threads(nthreads), el)
     if rc != 0:
         raise ValueError("oracle_fwd_rows rejected its arguments")
     return o, lse
 
 
 def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, causal: bool = False,
-                     nthreads: int | None = None):
+                     nthreads: int | None = None, elem=None):
     """Packed varlen attention.  q [total_q,Hq,d], k/v [total_k,Hkv,d].
 
     Returns (O [total_q,Hq,d] float64, LSE [Hq,total_q] float64).
     """
+    el = _common_elem(q, k, v, elem=elem)
     q, k, v = _bits(q), _bits(k), _bits(v)
     cu_q = np.ascontiguousarray(np.asarray(cu_seqlens_q, dtype=np.int32))
     cu_k = np.ascontiguousarray(np.asarray(cu_seqlens_k, dtype=np.int32))
@@ -152,18 +174,20 @@ def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, causal: 
     lse = np.zeros((Hq, total_q), np.float64)
     rc = _load().oracle_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_q), _ptr(cu_k), B, Hq,
                                    Hkv, d, st3(q), st3(k), st3(v), float(scale),
-                                   int(bool(causal)), _ptr(o), _ptr(lse), _threads(nthreads))
+                                   int(bool(causal)), _ptr(o), _ptr(lse), _threads(nthreads),
+                                   el)
     if rc != 0:
         raise ValueError("oracle_fwd_varlen rejected its arguments")
     return o, lse
 
 
 def attention_kvcache(q, k_cache, v_cache, cache_seqlens, scale: float,
-                      nthreads: int | None = None):
+                      nthreads: int | None = None, elem=None):
     """Single-query decode.  q [B,1,Hq,d], caches [B,Lmax,Hkv,d], lengths [B].
 
     Returns (O [B,Hq,d] float64, LSE [B,Hq] float64).
     """
+    el = _common_elem(q, k_cache, v_cache, elem=elem)
     q, kc, vc = _bits(q), _bits(k_cache), _bits(v_cache)
     lens = np.ascontiguousarray(np.asarray(cache_seqlens, dtype=np.int32))
     B, _, Hq, d = q.shape
@@ -172,21 +196,22 @@ def attention_kvcache(q, k_cache, v_cache, cache_seqlens, scale: float,
     lse = np.zeros((B, Hq), np.float64)
     rc = _load().oracle_fwd_kvcache(_ptr(q), _ptr(kc), _ptr(vc), _ptr(lens), B, Lmax, Hq, Hkv,
                                     d, _strides4(q), _strides4(kc), _strides4(vc),
-                                    float(scale), _ptr(o), _ptr(lse), _threads(nthreads))
+                                    float(scale), _ptr(o), _ptr(lse), _threads(nthreads), el)
     if rc != 0:
         raise ValueError("oracle_fwd_kvcache rejected its arguments")
     return o, lse
 
 
-def row_probs(q, k, v, b: int, h: int, i: int, scale: float, causal: bool = False):
+def row_probs(q, k, v, b: int, h: int, i: int, scale: float, causal: bool = False, elem=None):
     """Softmax probabilities P[i, :] of one dense row (zeros on invisible keys)."""
+    el = _common_elem(q, k, v, elem=elem)
     q, k, v = _bits(q), _bits(k), _bits(v)
     B, Nq, Hq, d = q.shape
     _, Nk, Hkv, _ = k.shape
     p = np.zeros((Nk,), np.float64)
     rc = _load().oracle_row_probs(_ptr(q), _ptr(k), _ptr(v), B, Nq, Nk, Hq, Hkv, d,
                                   _strides4(q), _strides4(k), _strides4(v), float(scale),
-                                  int(bool(causal)), b, h, i, _ptr(p))
+                                  int(bool(causal)), b, h, i, _ptr(p), el)
     if rc != 0:
         raise ValueError("oracle_row_probs rejected its arguments")
     return p

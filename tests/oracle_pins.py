@@ -382,6 +382,35 @@ def pin_lse_recompute(O):
         _close(P @ vv[0, :, h], o[0, :, h], 1e-12, "recomputed O")
 
 
-ALL_PINS = [pin_library, pin_uniform_scores, pin_single_key, pin_constant_v, pin_two_keys,
+def pin_library_fp16(O):
+    """fp16 inputs: the same library cross-check (torch converts fp16 to float64)."""
+    for n, (B, Nq, Nk, Hq, Hkv, d, causal) in enumerate(LIB_CASES[:3]):
+        q, k, v = dense_inputs(B, Nq, Nk, Hq, Hkv, d, seed=60 + n, dtype=torch.float16)
+        scale = 1.0 / math.sqrt(d)
+        o, lse = O.attention(q, k, v, scale, causal)
+        o_ref, lse_ref = _library_attention(q, k, v, scale, causal)
+        _close(o, o_ref, 1e-11, f"fp16 O vs torch SDPA case {n}")
+        _close(lse, lse_ref, 1e-11, f"fp16 LSE vs torch logsumexp case {n}")
+
+
+def pin_fp16_values(O):
+    """One visible key (causal row 0) built from special binary16 values -- normal,
+    subnormal, largest finite, negative: O = v_0 exactly and LSE = scale q_0 . k_0, with
+    the values converted by torch."""
+    vals = [1.0, -2.0, 65504.0, 2.0 ** -24, 0.333251953125, -6.103515625e-05, 1.5, -0.0]
+    v0 = torch.tensor(vals, dtype=torch.float16)
+    q0 = torch.tensor([0.5, -1.0, 2.0 ** -14, 3.0, 0.0, 1.0, -0.25, 2.0], dtype=torch.float16)
+    k0 = torch.tensor([1.0, 0.5, 1024.0, -0.125, 7.0, 2.0 ** -10, 4.0, -1.5], dtype=torch.float16)
+    q = torch.zeros((1, 2, 1, 8), dtype=torch.float16)
+    k = torch.zeros((1, 2, 1, 8), dtype=torch.float16)
+    v = torch.zeros((1, 2, 1, 8), dtype=torch.float16)
+    q[0, 0, 0], k[0, 0, 0], v[0, 0, 0] = q0, k0, v0
+    o, lse = O.attention(q, k, v, 0.5, True)
+    _close(o[0, 0, 0], v0.double().numpy(), 0.0, "fp16 single-key O")
+    _close(lse[0, 0, 0], 0.5 * float((q0.double() * k0.double()).sum()), 1e-12,
+           "fp16 single-key LSE")
+
+
+ALL_PINS = [pin_library, pin_library_fp16, pin_fp16_values, pin_uniform_scores, pin_single_key, pin_constant_v, pin_two_keys,
             pin_empty_rows, pin_hard_max, pin_probs, pin_shift, pin_permutation, pin_gqa,
             pin_varlen, pin_kvcache, pin_rows, pin_recurrence, pin_lse_recompute]

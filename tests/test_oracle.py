@@ -34,6 +34,10 @@ MUTATIONS = [
      "qrow = J->q + (J->cu_q[b] + i) * J->qs[1] + h * J->qs[2];",
      "qrow = J->q + (J->cu_k[b] + i) * J->qs[1] + h * J->qs[2];"),
     ("decode ignores cache length", "nkeys = J->cache_len[b];", "nkeys = J->Nk;"),
+    ("fp16 exponent bias off by one", "v = ldexp((double)(f | 0x400), e - 25);",
+     "v = ldexp((double)(f | 0x400), e - 24);"),
+    ("fp16 subnormals scaled as normals", "if (e == 0) v = ldexp((double)f, -24);",
+     "if (e == 0) v = ldexp((double)(f | 0x400), -25);"),
 ]
 
 
