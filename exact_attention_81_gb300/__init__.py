@@ -9,6 +9,8 @@ plus the upstream-style names ``flash_attn_func``, ``flash_attn_varlen_func`` an
 ``python -m exact_attention_81_gb300.build``.
 """
 from ._binding import (  # noqa: F401
+    FA_BF16,
+    FA_FP16,
     FA_ERR_CUDA,
     FA_ERR_INVALID_ARG,
     FA_ERR_TIMEOUT,

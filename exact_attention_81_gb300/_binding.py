@@ -25,6 +25,10 @@ FA_ERR_CUDA = 3
 FA_ERR_WORKSPACE = 4
 FA_ERR_TIMEOUT = 5
 
+FA_BF16 = 0
+FA_FP16 = 1
+_DTYPE = {torch.bfloat16: FA_BF16, torch.float16: FA_FP16}
+
 
 class FAError(RuntimeError):
     """A libfa call returned a non-zero fa_status."""
@@ -58,6 +62,7 @@ class FwdParams(ctypes.Structure):
         ("o_strides", ctypes.c_int64 * 3),
         ("scale", ctypes.c_float),
         ("causal", ctypes.c_int),
+        ("dtype", ctypes.c_int),
     ]
 
 
@@ -81,12 +86,12 @@ def load_library(path: str | None = None):
         lib.fa_fwd.argtypes = [ctypes.POINTER(FwdParams), vp]
         lib.fa_fwd.restype = i
         lib.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i,
-                                      vp]
+                                      i, vp]
         lib.fa_fwd_varlen.restype = i
         lib.fa_fwd_kvcache_workspace_size.argtypes = [i, i, i, i, i]
         lib.fa_fwd_kvcache_workspace_size.restype = sz
         lib.fa_fwd_kvcache.argtypes = [vp, vp, vp, vp, i, i, i, i, i, ctypes.POINTER(i64), f, i,
-                                       vp, sz, vp, vp, vp]
+                                       vp, sz, vp, vp, i, vp]
         lib.fa_fwd_kvcache.restype = i
         lib.fa_get_last_device_error.argtypes = [vp]
         lib.fa_get_last_device_error.restype = i
@@ -125,11 +130,14 @@ def _ptr(t) -> int | None:
     return None if t is None else int(t.data_ptr())
 
 
-def _require_bf16_cuda(name, t, ndim):
+def _require_bf16_cuda(name, t, ndim, dtype=None):
+    """A bf16 or fp16 CUDA tensor of `ndim` dimensions (of `dtype` when given)."""
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if t.dtype != torch.bfloat16 or not t.is_cuda:
-        raise TypeError(f"{name} must be a bf16 CUDA tensor")
+    if t.dtype not in _DTYPE or not t.is_cuda:
+        raise TypeError(f"{name} must be a bf16 or fp16 CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must have the element type of q ({dtype})")
     if t.dim() != ndim:
         raise ValueError(f"{name} must have {ndim} dimensions")
     if t.numel() > 0 and t.stride(-1) != 1:
@@ -147,16 +155,16 @@ def fa_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, 
     Returns (out [B,Nq,Hq,d] bf16, lse [B,Hq,Nq] fp32).
     """
     _require_bf16_cuda("q", q, 4)
-    _require_bf16_cuda("k", k, 4)
-    _require_bf16_cuda("v", v, 4)
+    _require_bf16_cuda("k", k, 4, q.dtype)
+    _require_bf16_cuda("v", v, 4, q.dtype)
     B, Nq, Hq, d = q.shape
     Nk, Hkv = k.shape[1], k.shape[2]
     if tuple(k.shape) != (B, Nk, Hkv, d) or tuple(v.shape) != (B, Nk, Hkv, d):
         raise ValueError("k and v must be [B, Nk, Hkv, d] matching q")
     if out is None:
-        out = torch.empty((B, Nq, Hq, d), dtype=torch.bfloat16, device=q.device)
+        out = torch.empty((B, Nq, Hq, d), dtype=q.dtype, device=q.device)
     else:
-        _require_bf16_cuda("out", out, 4)
+        _require_bf16_cuda("out", out, 4, q.dtype)
         if tuple(out.shape) != (B, Nq, Hq, d):
             raise ValueError("out must be [B, Nq, Hq, d]")
     if lse is None:
@@ -170,6 +178,7 @@ def fa_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, 
         getattr(p, name)[:] = list(t.stride()[:3])
     p.scale = default_scale(d) if scale is None else float(scale)
     p.causal = int(bool(causal))
+    p.dtype = _DTYPE[q.dtype]
     _check(load_library().fa_fwd(ctypes.byref(p), _stream_handle(stream)), "fa_fwd")
     return out, lse
 
@@ -182,8 +191,8 @@ def fa_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_se
     Returns (out [total_q,Hq,d] bf16, lse [Hq,total_q] fp32).
     """
     _require_bf16_cuda("q", q, 3)
-    _require_bf16_cuda("k", k, 3)
-    _require_bf16_cuda("v", v, 3)
+    _require_bf16_cuda("k", k, 3, q.dtype)
+    _require_bf16_cuda("v", v, 3, q.dtype)
     for name, t in (("q", q), ("k", k), ("v", v)):
         if not t.is_contiguous():
             raise ValueError(f"{name} must be contiguous for the varlen call")
@@ -196,14 +205,17 @@ def fa_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_se
     if cu_seqlens_k.numel() != B + 1:
         raise ValueError("cu_seqlens_q and cu_seqlens_k must have the same length")
     if out is None:
-        out = torch.empty((total_q, Hq, d), dtype=torch.bfloat16, device=q.device)
+        out = torch.empty((total_q, Hq, d), dtype=q.dtype, device=q.device)
+    else:
+        _require_bf16_cuda("out", out, 3, q.dtype)
     if lse is None:
         lse = torch.empty((Hq, total_q), dtype=torch.float32, device=q.device)
     sc = default_scale(d) if scale is None else float(scale)
     st = load_library().fa_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
                                       _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), B,
                                       int(max_seqlen_q), int(max_seqlen_k), total_q, total_k, Hq,
-                                      Hkv, d, sc, int(bool(causal)), _stream_handle(stream))
+                                      Hkv, d, sc, int(bool(causal)), _DTYPE[q.dtype],
+                                      _stream_handle(stream))
     _check(st, "fa_fwd_varlen")
     return out, lse
 
@@ -219,8 +231,8 @@ def fa_fwd_kvcache(q, k_cache, v_cache, cache_seqlens, scale: float | None = Non
     Returns (out [B,1,Hq,d] bf16, lse [B,Hq] fp32).
     """
     _require_bf16_cuda("q", q, 4)
-    _require_bf16_cuda("k_cache", k_cache, 4)
-    _require_bf16_cuda("v_cache", v_cache, 4)
+    _require_bf16_cuda("k_cache", k_cache, 4, q.dtype)
+    _require_bf16_cuda("v_cache", v_cache, 4, q.dtype)
     if k_cache.stride() != v_cache.stride() or k_cache.shape != v_cache.shape:
         raise ValueError("k_cache and v_cache must share shape and strides")
     if cache_seqlens.dtype != torch.int32 or not cache_seqlens.is_cuda:
@@ -230,7 +242,7 @@ def fa_fwd_kvcache(q, k_cache, v_cache, cache_seqlens, scale: float | None = Non
     B, _, Hq, d = q.shape
     Lmax, Hkv = k_cache.shape[1], k_cache.shape[2]
     if out is None:
-        out = torch.empty((B, 1, Hq, d), dtype=torch.bfloat16, device=q.device)
+        out = torch.empty((B, 1, Hq, d), dtype=q.dtype, device=q.device)
     if lse is None:
         lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
     need = fa_fwd_kvcache_workspace_size(B, Hq, Lmax, d, num_splits)
@@ -241,7 +253,7 @@ def fa_fwd_kvcache(q, k_cache, v_cache, cache_seqlens, scale: float | None = Non
     st = load_library().fa_fwd_kvcache(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cache_seqlens),
                                        B, Lmax, Hq, Hkv, d, strides, sc, int(num_splits),
                                        _ptr(workspace), workspace.numel(), _ptr(out), _ptr(lse),
-                                       _stream_handle(stream))
+                                       _DTYPE[q.dtype], _stream_handle(stream))
     _check(st, "fa_fwd_kvcache")
     return out, lse
 

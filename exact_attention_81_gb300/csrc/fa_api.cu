@@ -91,11 +91,11 @@ fa_status current_device(DeviceInfo **out) {
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// 4-D bf16 tensor map over a (batch, seq, head, d) tensor, dimensions ordered
+// 4-D 16-bit tensor map over a (batch, seq, head, d) tensor, dimensions ordered
 // {d, head, seq, batch}, box {64, 1, 128, 1} (64 columns x 128 rows of one head), 128-byte
 // swizzle, zero fill past the tensor edges.  sn/sh/sb are element strides.
 fa_status make_map(CUtensorMap *map, const void *base, int d, int64_t n, int64_t h, int64_t b,
-                   int64_t sn, int64_t sh, int64_t sb) {
+                   int64_t sn, int64_t sh, int64_t sb, int dtype) {
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(h),
                         static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(b)};
   // The stride of a dimension of extent 1 is never used; give it a legal value.
@@ -109,7 +109,9 @@ fa_status make_map(CUtensorMap *map, const void *base, int d, int64_t n, int64_t
       return FA_ERR_INVALID_ARG;
   cuuint32_t box[4] = {64, 1, 128, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims,
+  const CUtensorMapDataType ty =
+      dtype == FA_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUresult r = g_encode(map, ty, 4, const_cast<void *>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -131,6 +133,8 @@ float scale_log2(float scale) {
 }
 
 bool scale_ok(float s) { return std::isfinite(s) && s > 0.f; }
+
+bool dtype_ok(int t) { return t == FA_BF16 || t == FA_FP16; }
 
 int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 
@@ -178,6 +182,7 @@ fa_status fa_fwd(const fa_fwd_params *p, cudaStream_t stream) {
   if (a.B < 0 || a.Nq < 0 || a.Nk < 0 || a.Hq <= 0 || a.Hkv <= 0 || a.Hq % a.Hkv != 0)
     return FA_ERR_INVALID_ARG;
   if (a.d != 64 && a.d != 128) return FA_ERR_UNSUPPORTED;
+  if (!dtype_ok(a.dtype)) return FA_ERR_UNSUPPORTED;
   if (!scale_ok(a.scale)) return FA_ERR_INVALID_ARG;
   if (a.Nq > (1 << 30) || a.Nk > (1 << 30)) return FA_ERR_INVALID_ARG;
   if (a.B == 0 || a.Nq == 0) return FA_OK;
@@ -210,13 +215,13 @@ fa_status fa_fwd(const fa_fwd_params *p, cudaStream_t stream) {
   }
   CUtensorMap tq, tk, tv;
   if ((st = make_map(&tq, a.q, a.d, a.Nq, a.Hq, a.B, a.q_strides[1], a.q_strides[2],
-                     a.q_strides[0])) != FA_OK)
+                     a.q_strides[0], a.dtype)) != FA_OK)
     return st;
   if ((st = make_map(&tk, a.k, a.d, a.Nk, a.Hkv, a.B, a.k_strides[1], a.k_strides[2],
-                     a.k_strides[0])) != FA_OK)
+                     a.k_strides[0], a.dtype)) != FA_OK)
     return st;
   if ((st = make_map(&tv, a.v, a.d, a.Nk, a.Hkv, a.B, a.v_strides[1], a.v_strides[2],
-                     a.v_strides[0])) != FA_OK)
+                     a.v_strides[0], a.dtype)) != FA_OK)
     return st;
   fa::PrefillArgs pa{};
   pa.o = a.o;
@@ -240,18 +245,21 @@ fa_status fa_fwd(const fa_fwd_params *p, cudaStream_t stream) {
   pa.timeout_ns = g_timeout_ns;
   pa.sched_slot = fa::next_prefill_sched_slot();
   const int grid = static_cast<int>(tiles < dev->sm_count ? tiles : dev->sm_count);
-  cudaError_t e = fa::launch_prefill(a.d, a.causal != 0, tq, tk, tv, pa, grid, stream);
+  cudaError_t e =
+      fa::launch_prefill(a.d, a.causal != 0, a.dtype == FA_FP16, tq, tk, tv, pa, grid, stream);
   return e == cudaSuccess ? FA_OK : cuda_fail("prefill kernel launch", e);
 }
 
 fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
                         const int *cu_seqlens_q, const int *cu_seqlens_k, int B,
                         int max_seqlen_q, int max_seqlen_k, int total_q, int total_k, int Hq,
-                        int Hkv, int d, float scale, int causal, cudaStream_t stream) {
+                        int Hkv, int d, float scale, int causal, int dtype,
+                        cudaStream_t stream) {
   if (B < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || total_q < 0 || total_k < 0 || Hq <= 0 ||
       Hkv <= 0 || Hq % Hkv != 0)
     return FA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (!dtype_ok(dtype)) return FA_ERR_UNSUPPORTED;
   if (!scale_ok(scale)) return FA_ERR_INVALID_ARG;
   if (max_seqlen_q > (1 << 30) || total_q > (1 << 30) || total_k > (1 << 30))
     return FA_ERR_INVALID_ARG;
@@ -278,11 +286,14 @@ fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, fl
     return e == cudaSuccess ? FA_OK : cuda_fail("fill kernel launch", e);
   }
   CUtensorMap tq, tk, tv;
-  if ((st = make_map(&tq, q, d, total_q, Hq, 1, static_cast<int64_t>(Hq) * d, d, 0)) != FA_OK)
+  if ((st = make_map(&tq, q, d, total_q, Hq, 1, static_cast<int64_t>(Hq) * d, d, 0, dtype)) !=
+      FA_OK)
     return st;
-  if ((st = make_map(&tk, k, d, total_k, Hkv, 1, static_cast<int64_t>(Hkv) * d, d, 0)) != FA_OK)
+  if ((st = make_map(&tk, k, d, total_k, Hkv, 1, static_cast<int64_t>(Hkv) * d, d, 0, dtype)) !=
+      FA_OK)
     return st;
-  if ((st = make_map(&tv, v, d, total_k, Hkv, 1, static_cast<int64_t>(Hkv) * d, d, 0)) != FA_OK)
+  if ((st = make_map(&tv, v, d, total_k, Hkv, 1, static_cast<int64_t>(Hkv) * d, d, 0, dtype)) !=
+      FA_OK)
     return st;
   fa::PrefillArgs pa{};
   pa.o = o;
@@ -310,7 +321,8 @@ fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, fl
   pa.timeout_ns = g_timeout_ns;
   pa.sched_slot = fa::next_prefill_sched_slot();
   const int grid = static_cast<int>(tiles < dev->sm_count ? tiles : dev->sm_count);
-  cudaError_t e = fa::launch_prefill(d, causal != 0, tq, tk, tv, pa, grid, stream);
+  cudaError_t e =
+      fa::launch_prefill(d, causal != 0, dtype == FA_FP16, tq, tk, tv, pa, grid, stream);
   return e == cudaSuccess ? FA_OK : cuda_fail("prefill kernel launch", e);
 }
 
@@ -326,12 +338,13 @@ fa_status fa_fwd_kvcache(const void *q, const void *k_cache, const void *v_cache
                          const int *cache_seqlens, int B, int Lmax, int Hq, int Hkv, int d,
                          const int64_t cache_strides[3], float scale, int num_splits,
                          void *workspace, size_t workspace_bytes, void *o, float *lse,
-                         cudaStream_t stream) {
+                         int dtype, cudaStream_t stream) {
   if (B < 0 || Lmax < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || num_splits < 0)
     return FA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   const int group = Hq / Hkv;
   if (group != 1 && group != 2 && group != 4 && group != 8) return FA_ERR_UNSUPPORTED;
+  if (!dtype_ok(dtype)) return FA_ERR_UNSUPPORTED;
   if (!scale_ok(scale)) return FA_ERR_INVALID_ARG;
   if (Lmax > (1 << 30)) return FA_ERR_INVALID_ARG;
   if (B == 0) return FA_OK;
@@ -365,10 +378,10 @@ fa_status fa_fwd_kvcache(const void *q, const void *k_cache, const void *v_cache
   if (Lmax > 0) {
     CUtensorMap tk, tv;
     if ((st = make_map(&tk, k_cache, d, Lmax, Hkv, B, cache_strides[1], cache_strides[2],
-                       cache_strides[0])) != FA_OK)
+                       cache_strides[0], dtype)) != FA_OK)
       return st;
     if ((st = make_map(&tv, v_cache, d, Lmax, Hkv, B, cache_strides[1], cache_strides[2],
-                       cache_strides[0])) != FA_OK)
+                       cache_strides[0], dtype)) != FA_OK)
       return st;
     fa::DecodeArgs da{};
     da.q = q;
@@ -386,10 +399,11 @@ fa_status fa_fwd_kvcache(const void *q, const void *k_cache, const void *v_cache
     da.err = dev->err;
     da.timeout_ns = g_timeout_ns;
     const int grid = static_cast<int>(units < dev->sm_count ? units : dev->sm_count);
-    cudaError_t e = fa::launch_decode(d, group, tk, tv, da, grid, stream);
+    cudaError_t e = fa::launch_decode(d, group, dtype == FA_FP16, tk, tv, da, grid, stream);
     if (e != cudaSuccess) return cuda_fail("decode kernel launch", e);
   }
-  cudaError_t e = fa::launch_combine(d, o_part, lse_part, cache_seqlens, B, Hq, Lmax, chunk,
+  cudaError_t e = fa::launch_combine(d, dtype == FA_FP16, o_part, lse_part, cache_seqlens, B, Hq,
+                                     Lmax, chunk,
                                      maxch, o, lse, dev->err, stream);
   return e == cudaSuccess ? FA_OK : cuda_fail("combine kernel launch", e);
 }

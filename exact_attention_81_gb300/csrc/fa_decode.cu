@@ -166,7 +166,7 @@ __device__ __forceinline__ void release(uint64_t *bar, int lane) {
   if (lane == 0) mbar_arrive(bar);
 }
 
-template <int D, int G>
+template <int D, int G, bool F16>
 __device__ void compute(const DecodeArgs &a, uint8_t *smem, DBars *bars, const WaitCtl &wc,
                         int tid) {
   using C = DCfg<D, G>;
@@ -184,7 +184,7 @@ __device__ void compute(const DecodeArgs &a, uint8_t *smem, DBars *bars, const W
 
   float *pw = reinterpret_cast<float *>(smem + C::PW_OFF) + warp * (C::KPW * G);
   float *red = reinterpret_cast<float *>(smem + C::RED_OFF);
-  const __nv_bfloat16 *qg = reinterpret_cast<const __nv_bfloat16 *>(a.q);
+  const uint16_t *qg = reinterpret_cast<const uint16_t *>(a.q);  // bf16 or fp16 elements
   uint32_t it = 0, sync_phase = 0;
 
   for (int u = blockIdx.x; u < a.num_units; u += gridDim.x) {
@@ -204,8 +204,8 @@ __device__ void compute(const DecodeArgs &a, uint8_t *smem, DBars *bars, const W
         const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          q2[gg][4 * v + e] = f2_pack(bf16lo_to_f32(xs[e]) * a.scale_log2,
-                                      bf16hi_to_f32(xs[e]) * a.scale_log2);
+          q2[gg][4 * v + e] = f2_pack(lo_to_f32<F16>(xs[e]) * a.scale_log2,
+                                      hi_to_f32<F16>(xs[e]) * a.scale_log2);
       }
     }
     uint64_t acc[G][2];
@@ -241,7 +241,7 @@ __device__ void compute(const DecodeArgs &a, uint8_t *smem, DBars *bars, const W
             const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const uint64_t k2 = f2_pack(bf16lo_to_f32(xs[e]), bf16hi_to_f32(xs[e]));
+              const uint64_t k2 = f2_pack(lo_to_f32<F16>(xs[e]), hi_to_f32<F16>(xs[e]));
 #pragma unroll
               for (int gg = 0; gg < G; ++gg) s2[gg] = f2_fma(q2[gg][4 * v + e], k2, s2[gg]);
             }
@@ -316,8 +316,8 @@ __device__ void compute(const DecodeArgs &a, uint8_t *smem, DBars *bars, const W
           const int key = kw0 + kk;
           const int phys = vchunk ^ (key & 7);
           const uint2 x = *reinterpret_cast<const uint2 *>(vblk + key * 128 + phys * 16 + vhalf * 8);
-          const uint64_t v01 = f2_pack(bf16lo_to_f32(x.x), bf16hi_to_f32(x.x));
-          const uint64_t v23 = f2_pack(bf16lo_to_f32(x.y), bf16hi_to_f32(x.y));
+          const uint64_t v01 = f2_pack(lo_to_f32<F16>(x.x), hi_to_f32<F16>(x.x));
+          const uint64_t v23 = f2_pack(lo_to_f32<F16>(x.y), hi_to_f32<F16>(x.y));
           float p[G];
           if constexpr (G % 4 == 0) {
 #pragma unroll
@@ -393,7 +393,7 @@ __device__ void compute(const DecodeArgs &a, uint8_t *smem, DBars *bars, const W
   }
 }
 
-template <int D, int G>
+template <int D, int G, bool F16>
 __global__ void __launch_bounds__(NTHREADS, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   const DecodeArgs a) {
@@ -422,7 +422,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // Each register-split branch ends on its own named barrier.
   if (warp < PRODUCER_WARP) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(COMPUTE_REGS));
-    compute<D, G>(a, smem, bars, wc, tid);
+    compute<D, G, F16>(a, smem, bars, wc, tid);
     __syncwarp();
     named_barrier(1, NTHREADS);
   } else {
@@ -433,22 +433,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
 }
 
-template <int D, int G>
+template <int D, int G, bool F16>
 cudaError_t launch_decode_impl(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeArgs &a,
                                int grid, cudaStream_t stream) {
   constexpr int smem = DCfg<D, G>::SMEM_BYTES;
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, G>,
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, G, F16>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  decode_kernel<D, G><<<grid, NTHREADS, smem, stream>>>(tk, tv, a);
+  decode_kernel<D, G, F16><<<grid, NTHREADS, smem, stream>>>(tk, tv, a);
   return cudaGetLastError();
 }
 
 // One block per (batch, query head); thread = output column.
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(D)
     combine_kernel(const float *o_part, const float *lse_part, const int *cache_len, int Hq,
-                   int Lmax, int chunk, int maxch, __nv_bfloat16 *o, float *lse) {
+                   int Lmax, int chunk, int maxch, uint16_t *o, float *lse) {
   const int bh = blockIdx.x;
   const int b = bh / Hq;
   const int d = threadIdx.x;
@@ -457,7 +457,7 @@ __global__ void __launch_bounds__(D)
   const float *lp = lse_part + static_cast<int64_t>(bh) * maxch;
   const float *op = o_part + static_cast<int64_t>(bh) * maxch * D;
   if (nch == 0) {
-    o[static_cast<int64_t>(bh) * D + d] = __float2bfloat16(0.f);
+    o[static_cast<int64_t>(bh) * D + d] = 0;  // +0 in both bf16 and fp16
     if (d == 0) lse[bh] = -INFINITY;
     return;
   }
@@ -469,7 +469,8 @@ __global__ void __launch_bounds__(D)
     wsum += wgt;
     acc = fmaf(wgt, op[static_cast<int64_t>(c) * D + d], acc);
   }
-  o[static_cast<int64_t>(bh) * D + d] = __float2bfloat16_rn(acc / wsum);
+  o[static_cast<int64_t>(bh) * D + d] =
+      static_cast<uint16_t>(pack2<F16>(acc / wsum, 0.f) & 0xFFFFu);  // round to nearest even
   if (d == 0) lse[bh] = m + logf(wsum);
 }
 
@@ -492,36 +493,53 @@ int decode_smem_bytes(int d, int group) {
   }
 }
 
-cudaError_t launch_decode(int d, int group, const CUtensorMap &tk, const CUtensorMap &tv,
-                          const DecodeArgs &a, int grid, cudaStream_t stream) {
+template <bool F16>
+cudaError_t launch_decode_typed(int d, int group, const CUtensorMap &tk, const CUtensorMap &tv,
+                                const DecodeArgs &a, int grid, cudaStream_t stream) {
   if (d == 64) {
     switch (group) {
-      case 1: return launch_decode_impl<64, 1>(tk, tv, a, grid, stream);
-      case 2: return launch_decode_impl<64, 2>(tk, tv, a, grid, stream);
-      case 4: return launch_decode_impl<64, 4>(tk, tv, a, grid, stream);
-      default: return launch_decode_impl<64, 8>(tk, tv, a, grid, stream);
+      case 1: return launch_decode_impl<64, 1, F16>(tk, tv, a, grid, stream);
+      case 2: return launch_decode_impl<64, 2, F16>(tk, tv, a, grid, stream);
+      case 4: return launch_decode_impl<64, 4, F16>(tk, tv, a, grid, stream);
+      default: return launch_decode_impl<64, 8, F16>(tk, tv, a, grid, stream);
     }
   }
   switch (group) {
-    case 1: return launch_decode_impl<128, 1>(tk, tv, a, grid, stream);
-    case 2: return launch_decode_impl<128, 2>(tk, tv, a, grid, stream);
-    case 4: return launch_decode_impl<128, 4>(tk, tv, a, grid, stream);
-    default: return launch_decode_impl<128, 8>(tk, tv, a, grid, stream);
+    case 1: return launch_decode_impl<128, 1, F16>(tk, tv, a, grid, stream);
+    case 2: return launch_decode_impl<128, 2, F16>(tk, tv, a, grid, stream);
+    case 4: return launch_decode_impl<128, 4, F16>(tk, tv, a, grid, stream);
+    default: return launch_decode_impl<128, 8, F16>(tk, tv, a, grid, stream);
   }
 }
 
-cudaError_t launch_combine(int d, const float *o_part, const float *lse_part,
+cudaError_t launch_decode(int d, int group, bool f16, const CUtensorMap &tk,
+                          const CUtensorMap &tv, const DecodeArgs &a, int grid,
+                          cudaStream_t stream) {
+  return f16 ? launch_decode_typed<true>(d, group, tk, tv, a, grid, stream)
+             : launch_decode_typed<false>(d, group, tk, tv, a, grid, stream);
+}
+
+cudaError_t launch_combine(int d, bool f16, const float *o_part, const float *lse_part,
                            const int *cache_len, int B, int Hq, int Lmax, int chunk, int maxch,
                            void *o, float *lse, unsigned int * /*err*/, cudaStream_t stream) {
   const int blocks = B * Hq;
   if (blocks == 0) return cudaSuccess;
-  __nv_bfloat16 *ob = reinterpret_cast<__nv_bfloat16 *>(o);
-  if (d == 64)
-    combine_kernel<64><<<blocks, 64, 0, stream>>>(o_part, lse_part, cache_len, Hq, Lmax, chunk,
-                                                  maxch, ob, lse);
-  else
-    combine_kernel<128><<<blocks, 128, 0, stream>>>(o_part, lse_part, cache_len, Hq, Lmax,
-                                                    chunk, maxch, ob, lse);
+  uint16_t *ob = reinterpret_cast<uint16_t *>(o);
+  if (d == 64) {
+    if (f16)
+      combine_kernel<64, true><<<blocks, 64, 0, stream>>>(o_part, lse_part, cache_len, Hq, Lmax,
+                                                          chunk, maxch, ob, lse);
+    else
+      combine_kernel<64, false><<<blocks, 64, 0, stream>>>(o_part, lse_part, cache_len, Hq, Lmax,
+                                                           chunk, maxch, ob, lse);
+  } else {
+    if (f16)
+      combine_kernel<128, true><<<blocks, 128, 0, stream>>>(o_part, lse_part, cache_len, Hq,
+                                                            Lmax, chunk, maxch, ob, lse);
+    else
+      combine_kernel<128, false><<<blocks, 128, 0, stream>>>(o_part, lse_part, cache_len, Hq,
+                                                             Lmax, chunk, maxch, ob, lse);
+  }
   return cudaGetLastError();
 }
 

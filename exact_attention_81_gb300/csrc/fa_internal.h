@@ -39,9 +39,10 @@ struct PrefillArgs {
 // Tile-ticket counter slot for the next prefill launch (round robin over the slots).
 int next_prefill_sched_slot();
 
-cudaError_t launch_prefill(int d, bool causal, const CUtensorMap &tq, const CUtensorMap &tk,
-                           const CUtensorMap &tv, const PrefillArgs &a, int grid,
-                           cudaStream_t stream);
+// f16: inputs and output are fp16 instead of bf16.
+cudaError_t launch_prefill(int d, bool causal, bool f16, const CUtensorMap &tq,
+                           const CUtensorMap &tk, const CUtensorMap &tv, const PrefillArgs &a,
+                           int grid, cudaStream_t stream);
 
 // O = 0 and LSE = -inf for every row (no visible keys anywhere).
 cudaError_t launch_fill_empty(void *o, float *lse, int B, int N, int H, int d, int64_t o_sb,
@@ -63,10 +64,11 @@ struct DecodeArgs {
   unsigned long long timeout_ns;
 };
 
-cudaError_t launch_decode(int d, int group, const CUtensorMap &tk, const CUtensorMap &tv,
-                          const DecodeArgs &a, int grid, cudaStream_t stream);
+cudaError_t launch_decode(int d, int group, bool f16, const CUtensorMap &tk,
+                          const CUtensorMap &tv, const DecodeArgs &a, int grid,
+                          cudaStream_t stream);
 
-cudaError_t launch_combine(int d, const float *o_part, const float *lse_part,
+cudaError_t launch_combine(int d, bool f16, const float *o_part, const float *lse_part,
                            const int *cache_len, int B, int Hq, int Lmax, int chunk, int maxch,
                            void *o, float *lse, unsigned int *err, cudaStream_t stream);
 

@@ -62,7 +62,7 @@ __host__ __device__ constexpr uint32_t o_col(int t) {
   return static_cast<uint32_t>(256 + t * 128);
 }
 
-template <int D>
+template <int D, bool F16 = false>
 struct Cfg {
   static constexpr int KCH = D / 64;                     // 64-wide boxes per row
   static constexpr int TILE_BYTES = KCH * BOX_BYTES;     // one [128 x D] bf16 tile
@@ -71,8 +71,8 @@ struct Cfg {
   static constexpr int RING_OFF = 2 * TILE_BYTES;
   static constexpr int BAR_OFF = RING_OFF + NSLOTS * TILE_BYTES;
   static constexpr int SMEM_BYTES = BAR_OFF + 512 + 1024;  // barriers + alignment slack
-  static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BC, false, false);
-  static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, false, true);
+  static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BC, false, false, F16);
+  static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, false, true, F16);
 };
 
 // Per-launch tile-ticket counters: [slot][0] = next ticket, [slot][1] = CTAs finished.
@@ -155,26 +155,26 @@ __device__ __forceinline__ bool varlen_bad(const PrefillArgs &a, int b) {
 
 // S_t = Q_t K^T: D/16 MMAs of 128 x 128 x 16.  Both operands K-major, 128B-swizzled:
 // k-step kk lives in box kk/4 at byte offset 32*(kk%4) inside each 128-byte row.
-template <int D>
+template <int D, bool F16>
 __device__ __forceinline__ void issue_s(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint32_t off = static_cast<uint32_t>((kk >> 2) * BOX_BYTES + (kk & 3) * 32);
     mma_bf16_ss(d_tmem, sw128_desc(q_smem + off, 16, 1024), sw128_desc(k_smem + off, 16, 1024),
-                Cfg<D>::IDESC_S, kk > 0 ? 1u : 0u);
+                Cfg<D, F16>::IDESC_S, kk > 0 ? 1u : 0u);
   }
 }
 
 // O_t (+)= P_t V: BC/16 MMAs of 128 x D x 16.  P from TMEM (8 columns of bf16 pairs per
 // k-step); V MN-major, 128B-swizzled: 16 keys = 2048 bytes per k-step, d halves one box apart.
-template <int D>
+template <int D, bool F16>
 __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_smem,
                                          bool accumulate) {
 #pragma unroll
   for (int kk = 0; kk < BC / 16; ++kk) {
     mma_bf16_ts(o_tmem, p_tmem + static_cast<uint32_t>(kk * 8),
                 sw128_desc(v_smem + static_cast<uint32_t>(kk * 16 * 128), BOX_BYTES, 1024),
-                Cfg<D>::IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
+                Cfg<D, F16>::IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
@@ -265,7 +265,7 @@ __device__ __forceinline__ bool next_tile(Bars *bars, uint32_t k, int &tile, con
 // other sub-tile.  tcgen05.mma executes in issue order, so S_t(j+1) may overwrite the
 // TMEM columns that PV_t(j) reads P_t(j) from.
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool F16>
 __device__ void mma_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, uint32_t tmem,
                          const WaitCtl &wc) {
   using C = Cfg<D>;
@@ -291,7 +291,7 @@ __device__ void mma_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, uint32
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         if (ti.nkv[t] > 0) {
-          issue_s<D>(tmem + s_col(t), q_smem[t], ring + slot_k * C::TILE_BYTES);
+          issue_s<D, F16>(tmem + s_col(t), q_smem[t], ring + slot_k * C::TILE_BYTES);
           mma_commit(&bars->s_full[t]);
         }
       }
@@ -319,7 +319,7 @@ __device__ void mma_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, uint32
             if (!mbar_wait(&bars->p_ready[t], p_phase[t], wc)) goto out;
             p_phase[t] ^= 1u;
             tc_fence_after();
-            issue_pv<D>(tmem + o_col(t), tmem + s_col(t), ring + slot_v * C::TILE_BYTES, j > 0);
+            issue_pv<D, F16>(tmem + o_col(t), tmem + s_col(t), ring + slot_v * C::TILE_BYTES, j > 0);
             if (j == ti.nkv[t] - 1) {
               mma_commit(&bars->o_full[t]);
               o_pending[t] = true;
@@ -327,7 +327,7 @@ __device__ void mma_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, uint32
           }
           if (t == 1) mma_commit(&bars->kv_empty[slot_v]);
           if (j + 1 < ti.nkv[t]) {
-            issue_s<D>(tmem + s_col(t), q_smem[t], ring + slot_k * C::TILE_BYTES);
+            issue_s<D, F16>(tmem + s_col(t), q_smem[t], ring + slot_k * C::TILE_BYTES);
             mma_commit(&bars->s_full[t]);
           }
         }
@@ -350,7 +350,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const 
   return __all_sync(0xffffffffu, ok);
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool F16>
 __device__ void softmax_role(const PrefillArgs &a, Bars *bars, uint32_t tmem, const WaitCtl &wc,
                              int warp, int lane) {
   const int t = warp >> 2;
@@ -361,7 +361,7 @@ __device__ void softmax_role(const PrefillArgs &a, Bars *bars, uint32_t tmem, co
   const uint32_t tO = tmem + lane_off + o_col(t);
   const float c = a.scale_log2;
   uint32_t s_phase = 0, o_phase = 0;
-  __nv_bfloat16 *obase = reinterpret_cast<__nv_bfloat16 *>(a.o);
+  uint16_t *obase = reinterpret_cast<uint16_t *>(a.o);  // bf16 or fp16 elements
 
   for (uint32_t k = 0;; ++k) {
     int tile;
@@ -429,8 +429,8 @@ __device__ void softmax_role(const PrefillArgs &a, Bars *bars, uint32_t tmem, co
         const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
         l2a = f2_add(l2a, f2_pack(p0, p1));
         l2b = f2_add(l2b, f2_pack(p2, p3));
-        p[i] = pack_bf16x2(p0, p1);
-        p[i + 1] = pack_bf16x2(p2, p3);
+        p[i] = pack2<F16>(p0, p1);
+        p[i + 1] = pack2<F16>(p2, p3);
       }
       {
         float la, lb, lc, ld;
@@ -477,7 +477,7 @@ __device__ void softmax_role(const PrefillArgs &a, Bars *bars, uint32_t tmem, co
 
     // Epilogue: O / l -> bf16, LSE = ln2 * (m + log2 l).
     const int64_t tok = static_cast<int64_t>(ti.q_tok) + row;
-    __nv_bfloat16 *orow = obase + static_cast<int64_t>(ti.b) * a.o_sb + tok * a.o_sn +
+    uint16_t *orow = obase + static_cast<int64_t>(ti.b) * a.o_sb + tok * a.o_sn +
                           static_cast<int64_t>(ti.h) * a.o_sh;
     if (nkv > 0) {
       if (!warp_wait(&bars->o_full[t], o_phase, wc)) return;
@@ -493,10 +493,10 @@ __device__ void softmax_role(const PrefillArgs &a, Bars *bars, uint32_t tmem, co
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv_l, __uint_as_float(r[8 * v + 1]) * inv_l);
-            w.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv_l, __uint_as_float(r[8 * v + 3]) * inv_l);
-            w.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv_l, __uint_as_float(r[8 * v + 5]) * inv_l);
-            w.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv_l, __uint_as_float(r[8 * v + 7]) * inv_l);
+            w.x = pack2<F16>(__uint_as_float(r[8 * v + 0]) * inv_l, __uint_as_float(r[8 * v + 1]) * inv_l);
+            w.y = pack2<F16>(__uint_as_float(r[8 * v + 2]) * inv_l, __uint_as_float(r[8 * v + 3]) * inv_l);
+            w.z = pack2<F16>(__uint_as_float(r[8 * v + 4]) * inv_l, __uint_as_float(r[8 * v + 5]) * inv_l);
+            w.w = pack2<F16>(__uint_as_float(r[8 * v + 6]) * inv_l, __uint_as_float(r[8 * v + 7]) * inv_l);
             dst[v] = w;
           }
         }
@@ -515,7 +515,7 @@ __device__ void softmax_role(const PrefillArgs &a, Bars *bars, uint32_t tmem, co
   }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool F16>
 __global__ void __launch_bounds__(NTHREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv, const PrefillArgs a) {
@@ -567,7 +567,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // before TMEM is released.
   if (warp < PRODUCER_WARP) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(SOFTMAX_REGS));
-    softmax_role<D, CAUSAL>(a, bars, tmem, wc, warp, lane);
+    softmax_role<D, CAUSAL, F16>(a, bars, tmem, wc, warp, lane);
     __syncwarp();
     tc_fence_before();
     named_barrier(1, NTHREADS);
@@ -576,7 +576,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (warp == PRODUCER_WARP) {
       if (lane == 0) producer_role<D, CAUSAL>(a, &tmq, &tmk, &tmv, smem, bars, wc);
     } else if (warp == MMA_WARP) {
-      if (lane == 0) mma_role<D, CAUSAL>(a, smem, bars, tmem, wc);
+      if (lane == 0) mma_role<D, CAUSAL, F16>(a, smem, bars, tmem, wc);
     }
     __syncwarp();
     tc_fence_before();
@@ -588,19 +588,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool F16>
 cudaError_t launch_impl(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                         const PrefillArgs &a, int grid, cudaStream_t stream) {
   constexpr int smem = Cfg<D>::SMEM_BYTES;
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, CAUSAL>,
+  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, CAUSAL, F16>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  prefill_kernel<D, CAUSAL><<<grid, NTHREADS, smem, stream>>>(tq, tk, tv, a);
+  prefill_kernel<D, CAUSAL, F16><<<grid, NTHREADS, smem, stream>>>(tq, tk, tv, a);
   return cudaGetLastError();
 }
 
 // O = 0 and LSE = -inf for B x N x H rows.
-__global__ void fill_empty_kernel(__nv_bfloat16 *o, float *lse, int B, int N, int H, int d,
+__global__ void fill_empty_kernel(uint16_t *o, float *lse, int B, int N, int H, int d,
                                   int64_t o_sb, int64_t o_sn, int64_t o_sh, int64_t lse_sb,
                                   int64_t lse_sh) {
   const int64_t rows = static_cast<int64_t>(B) * N * H;
@@ -610,8 +610,8 @@ __global__ void fill_empty_kernel(__nv_bfloat16 *o, float *lse, int B, int N, in
     const int64_t bn = r / H;
     const int n = static_cast<int>(bn % N);
     const int b = static_cast<int>(bn / N);
-    __nv_bfloat16 *orow = o + b * o_sb + n * o_sn + h * o_sh;
-    for (int c = 0; c < d; ++c) orow[c] = __float2bfloat16(0.f);
+    uint16_t *orow = o + b * o_sb + n * o_sn + h * o_sh;
+    for (int c = 0; c < d; ++c) orow[c] = 0;  // +0 in both bf16 and fp16
     lse[b * lse_sb + h * lse_sh + n] = -INFINITY;
   }
 }
@@ -625,15 +625,23 @@ int next_prefill_sched_slot() {
 
 int prefill_smem_bytes(int d) { return d == 64 ? Cfg<64>::SMEM_BYTES : Cfg<128>::SMEM_BYTES; }
 
-cudaError_t launch_prefill(int d, bool causal, const CUtensorMap &tq, const CUtensorMap &tk,
-                           const CUtensorMap &tv, const PrefillArgs &a, int grid,
-                           cudaStream_t stream) {
+template <bool F16>
+cudaError_t launch_typed(int d, bool causal, const CUtensorMap &tq, const CUtensorMap &tk,
+                         const CUtensorMap &tv, const PrefillArgs &a, int grid,
+                         cudaStream_t stream) {
   if (d == 64) {
-    return causal ? launch_impl<64, true>(tq, tk, tv, a, grid, stream)
-                  : launch_impl<64, false>(tq, tk, tv, a, grid, stream);
+    return causal ? launch_impl<64, true, F16>(tq, tk, tv, a, grid, stream)
+                  : launch_impl<64, false, F16>(tq, tk, tv, a, grid, stream);
   }
-  return causal ? launch_impl<128, true>(tq, tk, tv, a, grid, stream)
-                : launch_impl<128, false>(tq, tk, tv, a, grid, stream);
+  return causal ? launch_impl<128, true, F16>(tq, tk, tv, a, grid, stream)
+                : launch_impl<128, false, F16>(tq, tk, tv, a, grid, stream);
+}
+
+cudaError_t launch_prefill(int d, bool causal, bool f16, const CUtensorMap &tq,
+                           const CUtensorMap &tk, const CUtensorMap &tv, const PrefillArgs &a,
+                           int grid, cudaStream_t stream) {
+  return f16 ? launch_typed<true>(d, causal, tq, tk, tv, a, grid, stream)
+             : launch_typed<false>(d, causal, tq, tk, tv, a, grid, stream);
 }
 
 cudaError_t launch_fill_empty(void *o, float *lse, int B, int N, int H, int d, int64_t o_sb,
@@ -643,7 +651,7 @@ cudaError_t launch_fill_empty(void *o, float *lse, int B, int N, int H, int d, i
   if (rows == 0) return cudaSuccess;
   const int threads = 256;
   const int blocks = static_cast<int>(std::min<int64_t>((rows + threads - 1) / threads, 4096));
-  fill_empty_kernel<<<blocks, threads, 0, stream>>>(reinterpret_cast<__nv_bfloat16 *>(o), lse, B,
+  fill_empty_kernel<<<blocks, threads, 0, stream>>>(reinterpret_cast<uint16_t *>(o), lse, B,
                                                     N, H, d, o_sb, o_sn, o_sh, lse_sb, lse_sh);
   return cudaGetLastError();
 }

@@ -312,14 +312,14 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
       : "memory");
 }
 
-// Instruction descriptor for kind::f16 with bf16 A/B and fp32 D.
-//   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format (1 = bf16),
+// Instruction descriptor for kind::f16 with bf16 (or fp16) A/B and fp32 D.
+//   bits 4-5 D format (1 = f32), 7-9 A format and 10-12 B format (1 = bf16, 0 = f16),
 //   15 A major (0 = K-major), 16 B major (1 = MN-major), 17-22 N >> 3, 24-28 M >> 4.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major,
-                                                      bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
-         ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
-         (static_cast<uint32_t>(M >> 4) << 24);
+                                                      bool b_mn_major, bool f16 = false) {
+  return (1u << 4) | ((f16 ? 0u : 1u) << 7) | ((f16 ? 0u : 1u) << 10) |
+         ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand.
@@ -358,6 +358,37 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float bf16lo_to_f32(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf16hi_to_f32(uint32_t x) {
   return __uint_as_float(x & 0xFFFF0000u);
+}
+
+// Packs two floats to f16x2 with round-to-nearest-even; `lo` goes to the low half.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ float f16lo_to_f32(uint32_t x) {
+  float f;
+  asm("{\n.reg .b16 lo, hi;\nmov.b32 {lo, hi}, %1;\ncvt.f32.f16 %0, lo;\n}" : "=f"(f) : "r"(x));
+  return f;
+}
+__device__ __forceinline__ float f16hi_to_f32(uint32_t x) {
+  float f;
+  asm("{\n.reg .b16 lo, hi;\nmov.b32 {lo, hi}, %1;\ncvt.f32.f16 %0, hi;\n}" : "=f"(f) : "r"(x));
+  return f;
+}
+
+// The two 16-bit element types of the kernels: bf16 (F16 = false) or fp16 (F16 = true).
+template <bool F16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  return F16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
+}
+template <bool F16>
+__device__ __forceinline__ float lo_to_f32(uint32_t x) {
+  return F16 ? f16lo_to_f32(x) : bf16lo_to_f32(x);
+}
+template <bool F16>
+__device__ __forceinline__ float hi_to_f32(uint32_t x) {
+  return F16 ? f16hi_to_f32(x) : bf16hi_to_f32(x);
 }
 
 }  // namespace fa

@@ -14,7 +14,8 @@
  * 数学推导) on chip.
  *
  * Conventions shared by every call
- *   - Element type: Q, K, V and O are bf16 (IEEE bfloat16 bit patterns); LSE is fp32.
+ *   - Element type: Q, K, V and O are all bf16 or all fp16 (fa_dtype, "flash-attention"
+ *     section 5: fp16 / bf16 only); LSE is fp32.  S, l and O accumulate in fp32.
  *   - Head dimension d must be 64 or 128 (a subset of the upstream limit "d <= 256 and
  *     a multiple of 8" -- "flash-attention", section 5).
  *   - Grouped-query attention: Hkv must divide Hq; query head h reads key/value head
@@ -45,11 +46,17 @@
 extern "C" {
 #endif
 
+/* Element type of Q, K, V and O. */
+typedef enum fa_dtype {
+    FA_BF16 = 0, /* bfloat16 */
+    FA_FP16 = 1  /* IEEE binary16 */
+} fa_dtype;
+
 typedef enum fa_status {
     FA_OK = 0,
     FA_ERR_INVALID_ARG = 1, /* null pointer, bad size, Hq % Hkv != 0, misaligned pointer/stride */
-    FA_ERR_UNSUPPORTED = 2, /* d not in {64, 128}, decode group size not in {1,2,4,8},
-                               or the current device is not an sm_103 GPU */
+    FA_ERR_UNSUPPORTED = 2, /* d not in {64, 128}, dtype not a fa_dtype, decode group size
+                               not in {1,2,4,8}, or the current device is not an sm_103 GPU */
     FA_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed: see fa_last_cuda_error() */
     FA_ERR_WORKSPACE = 4,   /* workspace pointer null or smaller than required */
     FA_ERR_TIMEOUT = 5      /* a device-side wait gave up (reported by fa_get_last_device_error) */
@@ -57,8 +64,8 @@ typedef enum fa_status {
 
 /*
  * Dense batched attention, the flash_attn_func call of "flash-attention" section 1:
- * q/k/v in the (batch, seqlen, nheads, headdim) layout.
- *   q   : [B, Nq, Hq,  d] bf16, element (b,n,h,c) at q + b*q_strides[0] + n*q_strides[1]
+ * q/k/v in the (batch, seqlen, nheads, headdim) layout; element type `dtype` (fa_dtype).
+ *   q   : [B, Nq, Hq,  d], element (b,n,h,c) at q + b*q_strides[0] + n*q_strides[1]
  *                                                    + h*q_strides[2] + c
  *   k, v: [B, Nk, Hkv, d] bf16, same convention with k_strides / v_strides
  *   o   : [B, Nq, Hq,  d] bf16 output, same convention with o_strides
@@ -78,6 +85,7 @@ typedef struct fa_fwd_params {
     int64_t q_strides[3], k_strides[3], v_strides[3], o_strides[3]; /* (b, n, h) */
     float scale;
     int causal;
+    int dtype; /* fa_dtype of q, k, v and o */
 } fa_fwd_params;
 
 fa_status fa_fwd(const fa_fwd_params *p, cudaStream_t stream);
@@ -95,12 +103,14 @@ fa_status fa_fwd(const fa_fwd_params *p, cudaStream_t stream);
  *         fa_get_last_device_error).
  *   o   : [total_q, Hq, d] bf16 output, contiguous
  *   lse : [Hq, total_q] fp32 output, contiguous
- * Each sequence is attended on its own; causal alignment is per sequence.
+ * Each sequence is attended on its own; causal alignment is per sequence.  dtype is the
+ * fa_dtype of q, k, v and o.
  */
 fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
                         const int *cu_seqlens_q, const int *cu_seqlens_k, int B,
                         int max_seqlen_q, int max_seqlen_k, int total_q, int total_k, int Hq,
-                        int Hkv, int d, float scale, int causal, cudaStream_t stream);
+                        int Hkv, int d, float scale, int causal, int dtype,
+                        cudaStream_t stream);
 
 /*
  * Single-query decode against a padded KV cache, the flash_attn_with_kvcache call of
@@ -121,7 +131,7 @@ fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, fl
  *                  256-byte aligned; owned by the caller, overwritten by the call.
  *   o            : [B, 1, Hq, d] bf16 output, contiguous
  *   lse          : [B, Hq] fp32 output, contiguous
- * Hq / Hkv must be 1, 2, 4 or 8.
+ * Hq / Hkv must be 1, 2, 4 or 8.  dtype is the fa_dtype of q, the caches and o.
  */
 size_t fa_fwd_kvcache_workspace_size(int B, int Hq, int Lmax, int d, int num_splits);
 
@@ -129,11 +139,11 @@ fa_status fa_fwd_kvcache(const void *q, const void *k_cache, const void *v_cache
                          const int *cache_seqlens, int B, int Lmax, int Hq, int Hkv, int d,
                          const int64_t cache_strides[3], float scale, int num_splits,
                          void *workspace, size_t workspace_bytes, void *o, float *lse,
-                         cudaStream_t stream);
+                         int dtype, cudaStream_t stream);
 
 /*
  * Split-KV decode that allocates nothing.  Same computation, arguments and outputs as
- * fa_fwd_kvcache, minus the workspace.  (The paper has no counterpart: this entry point
+ * fa_fwd_kvcache with bf16 inputs, minus the workspace.  (The paper has no counterpart: this entry point
  * exists for callers of this library, not for the method.)
  *
  * Some callers cannot allocate device memory at call time and have no buffer set aside

@@ -51,7 +51,7 @@ def _params(**kw):
 
 
 @pytest.mark.parametrize("change,status", [
-    ({"d": 96}, 2), ({"d": 256}, 2), ({"Hkv": 3}, 1), ({"Hq": 0}, 1), ({"B": -1}, 1),
+    ({"d": 96}, 2), ({"d": 256}, 2), ({"dtype": 2}, 2), ({"dtype": -1}, 2), ({"Hkv": 3}, 1), ({"Hq": 0}, 1), ({"B": -1}, 1),
     ({"scale": 0.0}, 1), ({"scale": float("nan")}, 1), ({"scale": -1.0}, 1),
     ({"q": 4098}, 1), ({"o": 4100}, 1), ({"lse": 4098}, 1), ({"q": None}, 1),
     ({"k": None}, 1), ({"Nq": -5}, 1),
@@ -76,15 +76,16 @@ def test_fwd_empty_batch_is_noop(lib):
 def test_varlen_rejects_bad_arguments(lib):
     f = lib.fa_fwd_varlen
     good = dict(q=4096, k=4096, v=4096, o=4096, lse=4096, cq=4096, ck=4096, B=2, mq=10, mk=10,
-                tq=20, tk=20, Hq=4, Hkv=2, d=64, scale=0.1, causal=1)
+                tq=20, tk=20, Hq=4, Hkv=2, d=64, scale=0.1, causal=1, dtype=0)
 
     def call(**kw):
         a = dict(good, **kw)
         return f(a["q"], a["k"], a["v"], a["o"], a["lse"], a["cq"], a["ck"], a["B"], a["mq"],
                  a["mk"], a["tq"], a["tk"], a["Hq"], a["Hkv"], a["d"], a["scale"], a["causal"],
-                 None)
+                 a["dtype"], None)
 
     assert call(d=80) == 2
+    assert call(dtype=3) == 2
     assert call(Hkv=3) == 1
     assert call(cq=None) == 1
     assert call(q=4097) == 1
@@ -98,13 +99,14 @@ def test_kvcache_rejects_bad_arguments(lib):
 
     def call(**kw):
         a = dict(q=4096, kc=4096, vc=4096, lens=4096, B=2, L=1024, Hq=32, Hkv=8, d=128,
-                 scale=0.1, ns=0, ws=4096, wsb=1 << 30, o=4096, lse=4096)
+                 scale=0.1, ns=0, ws=4096, wsb=1 << 30, o=4096, lse=4096, dtype=0)
         a.update(kw)
         return lib.fa_fwd_kvcache(a["q"], a["kc"], a["vc"], a["lens"], a["B"], a["L"], a["Hq"],
                                   a["Hkv"], a["d"], strides, a["scale"], a["ns"], a["ws"],
-                                  a["wsb"], a["o"], a["lse"], None)
+                                  a["wsb"], a["o"], a["lse"], a["dtype"], None)
 
     assert call(Hq=32, Hkv=2) == 2          # group of 16 not supported by decode
+    assert call(dtype=5) == 2
     assert call(d=32) == 2
     assert call(Hkv=5) == 1
     assert call(ns=-1) == 1
