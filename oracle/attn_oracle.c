@@ -28,7 +28,19 @@
  *   - variable-length batches are packed along the token axis and delimited by the
  *     prefix sums cu_seqlens ("flash-attention", capabilities table, varlen row);
  *   - single-query decode attends to the first cache_seqlens[b] rows of the cache
- *     ("flash-attention", capabilities table, KV cache row; section 1 usage).
+ *     ("flash-attention", capabilities table, KV cache row; section 1 usage); the query
+ *     sits at position cache_seqlens[b] - 1 (bottom-right alignment with Nq = 1).
+ *
+ * Score modifiers ("flash-attention", capabilities table: causal / sliding window /
+ * ALiBi / softcap; the pages name them and give no formulas, so the plain readings
+ * below are taken).  With pos = i + (Nk - Nq) the bottom-right position of query i:
+ *   - sliding window (wl, wr): key j is visible when pos - wl <= j <= pos + wr; a
+ *     negative bound is unbounded; causal is the window (-1, 0);
+ *   - softcap c > 0: the scaled score z = scale * q . k_j becomes c * tanh(z / c);
+ *   - ALiBi slope a (per batch and query head): the score (after the softcap) gets
+ *     - a * |pos - j| added.
+ * The softmax and the log-sum-exp are then taken over the modified scores of the
+ * visible keys.
  *
  * Inputs are 16-bit float bit patterns (uint16): bf16 (elem = 0) or IEEE binary16
  * (elem = 1), the two element types of the fused kernels ("flash-attention", section 5:
@@ -66,29 +78,42 @@ static double widen(uint16_t bits, int elem) {
     return elem ? fp16_to_double(bits) : bf16_to_double(bits);
 }
 
+/* Score modifiers of one row: softcap (0 = off) and the ALiBi slope (has_alibi). */
+typedef struct {
+    double softcap;
+    int has_alibi;
+    double slope;
+} score_mod_t;
+
 /*
- * One query row against keys 0..nkeys-1 (the visible set).
- * q      : d bf16 values
+ * One query row against the visible keys lo..hi-1.
+ * q      : d values
  * krow(j): key j at kbase + j * k_stride, d values
  * vrow(j): value j at vbase + j * v_stride, d values
- * s      : scratch of nkeys doubles; on return it holds the probabilities P_j
+ * pos    : bottom-right position of the query (for the ALiBi distance)
+ * s      : scratch of hi - lo doubles; on return it holds the probabilities P_j
  * o      : d doubles, o = sum_j P_j v_j
- * lse    : natural-log sum of exp of the scaled scores
+ * lse    : natural-log sum of exp of the (modified) scaled scores
  */
 static void attend_row(const uint16_t *q, const uint16_t *kbase, int64_t k_stride,
-                       const uint16_t *vbase, int64_t v_stride, int64_t nkeys, int d,
-                       double scale, int elem, double *s, double *o, double *lse) {
+                       const uint16_t *vbase, int64_t v_stride, int64_t lo, int64_t hi,
+                       int64_t pos, int d, double scale, const score_mod_t *mod, int elem,
+                       double *s, double *o, double *lse) {
+    int64_t nkeys = hi - lo;
     for (int c = 0; c < d; ++c) o[c] = 0.0;
     if (nkeys <= 0) {
         *lse = -INFINITY;
         return;
     }
-    /* S = scale * q . k_j */
-    for (int64_t j = 0; j < nkeys; ++j) {
+    /* S = scale * q . k_j, then the softcap and the ALiBi bias */
+    for (int64_t j = lo; j < hi; ++j) {
         const uint16_t *kr = kbase + j * k_stride;
         double acc = 0.0;
         for (int c = 0; c < d; ++c) acc += widen(q[c], elem) * widen(kr[c], elem);
-        s[j] = scale * acc;
+        double z = scale * acc;
+        if (mod->softcap > 0.0) z = mod->softcap * tanh(z / mod->softcap);
+        if (mod->has_alibi) z -= mod->slope * fabs((double)(pos - j));
+        s[j - lo] = z;
     }
     /* stable softmax: m = max_j s_j, l = sum_j e^{s_j - m}, P_j = e^{s_j - m} / l */
     double m = s[0];
@@ -102,19 +127,23 @@ static void attend_row(const uint16_t *q, const uint16_t *kbase, int64_t k_strid
     for (int64_t j = 0; j < nkeys; ++j) s[j] /= l;
     /* O = P V */
     for (int64_t j = 0; j < nkeys; ++j) {
-        const uint16_t *vr = vbase + j * v_stride;
+        const uint16_t *vr = vbase + (lo + j) * v_stride;
         for (int c = 0; c < d; ++c) o[c] += s[j] * widen(vr[c], elem);
     }
     *lse = m + log(l);
 }
 
-/* Number of keys query i may see: all Nk, or (causal, bottom-right) i + Nk - Nq + 1. */
-static int64_t visible_keys(int64_t i, int64_t Nq, int64_t Nk, int causal) {
-    if (!causal) return Nk;
-    int64_t last = i + (Nk - Nq);
-    if (last < 0) return 0;
-    if (last >= Nk) return Nk;
-    return last + 1;
+/*
+ * Keys visible to the query at bottom-right position pos among Nk keys under the window
+ * (wl, wr) (negative = unbounded): [*lo, *hi), empty when *hi <= *lo.
+ */
+static void visible_range(int64_t pos, int64_t Nk, int64_t wl, int64_t wr, int64_t *lo,
+                          int64_t *hi) {
+    int64_t a = 0, b = Nk;
+    if (wl >= 0 && pos - wl > a) a = pos - wl;
+    if (wr >= 0 && pos + wr + 1 < b) b = pos + wr + 1;
+    *lo = a;
+    *hi = b > a ? b : a;
 }
 
 /* ------------------------------------------------------------------------- */
@@ -124,8 +153,14 @@ typedef struct {
     /* dense layout: element (b, n, h, c) at base + b*s[0] + n*s[1] + h*s[2] + c */
     const uint16_t *q, *k, *v;
     int64_t qs[3], ks[3], vs[3];
-    int B, Nq, Nk, Hq, Hkv, d, causal;
+    int B, Nq, Nk, Hq, Hkv, d;
     double scale;
+    /* window bounds (causal already folded in as wr = 0), softcap, ALiBi slopes
+       (slope of (b, h) at alibi[b * alibi_sb + h], NULL = none) */
+    int64_t wl, wr;
+    double softcap;
+    const double *alibi;
+    int64_t alibi_sb;
     /* varlen: prefix sums over the packed token axis (B+1 entries) */
     const int32_t *cu_q, *cu_k;
     /* kv cache: visible prefix length per batch entry */
@@ -180,35 +215,43 @@ static void *worker(void *arg) {
         decode_index(J, w, &b, &h, &i);
         int g = h / group; /* key/value head shared by this query head */
         const uint16_t *qrow, *kbase, *vbase;
-        int64_t nkeys, k_stride, v_stride;
+        int64_t nk, pos, k_stride, v_stride;
         if (J->mode == 0) {
             qrow = J->q + b * J->qs[0] + i * J->qs[1] + h * J->qs[2];
             kbase = J->k + b * J->ks[0] + g * J->ks[2];
             vbase = J->v + b * J->vs[0] + g * J->vs[2];
             k_stride = J->ks[1];
             v_stride = J->vs[1];
-            nkeys = visible_keys(i, J->Nq, J->Nk, J->causal);
+            pos = i + (J->Nk - J->Nq);
+            nk = J->Nk;
         } else if (J->mode == 1) {
             int64_t nq = J->cu_q[b + 1] - J->cu_q[b];
-            int64_t nk = J->cu_k[b + 1] - J->cu_k[b];
+            nk = J->cu_k[b + 1] - J->cu_k[b];
             qrow = J->q + (J->cu_q[b] + i) * J->qs[1] + h * J->qs[2];
             kbase = J->k + J->cu_k[b] * J->ks[1] + g * J->ks[2];
             vbase = J->v + J->cu_k[b] * J->vs[1] + g * J->vs[2];
             k_stride = J->ks[1];
             v_stride = J->vs[1];
-            nkeys = visible_keys(i, nq, nk, J->causal);
+            pos = i + (nk - nq);
         } else {
-            /* decode: one query per batch entry sees the whole cached prefix */
+            /* decode: one query per batch entry, the last of a sequence of cache_len[b] */
             qrow = J->q + b * J->qs[0] + h * J->qs[2];
             kbase = J->k + b * J->ks[0] + g * J->ks[2];
             vbase = J->v + b * J->vs[0] + g * J->vs[2];
             k_stride = J->ks[1];
             v_stride = J->vs[1];
-            nkeys = J->cache_len[b];
+            nk = J->cache_len[b];
+            pos = nk - 1;
         }
+        int64_t lo, hi;
+        visible_range(pos, nk, J->wl, J->wr, &lo, &hi);
+        score_mod_t mod;
+        mod.softcap = J->softcap;
+        mod.has_alibi = J->alibi != NULL;
+        mod.slope = J->alibi ? J->alibi[b * J->alibi_sb + h] : 0.0;
         double lse;
-        attend_row(qrow, kbase, k_stride, vbase, v_stride, nkeys, J->d, J->scale, J->elem, s, orow,
-                   &lse);
+        attend_row(qrow, kbase, k_stride, vbase, v_stride, lo, hi, pos, J->d, J->scale, &mod,
+                   J->elem, s, orow, &lse);
         double *odst;
         double *ldst;
         if (J->rows) {
@@ -249,6 +292,28 @@ static int run_threads(job_t *base) {
 
 /* ------------------------------------------------------------------------- */
 /* Exported entry points (called through ctypes by oracle/oracle.py).        */
+/*
+ * Every entry point ends with the element type and the score modifiers:
+ *   elem          : 0 bf16, 1 fp16
+ *   window_left/right : sliding-window bounds, negative = unbounded (causal != 0 sets the
+ *                   right bound to 0)
+ *   softcap       : 0 = off, else > 0
+ *   alibi         : NULL or per-(batch, query head) slopes, slope of (b, h) at
+ *                   alibi[b * alibi_sb + h] (alibi_sb = 0 shares one row of Hq slopes)
+ */
+
+static int set_common(job_t *J, int Hq, int Hkv, int d, int elem, int causal, int window_left,
+                      int window_right, double softcap, const double *alibi, int64_t alibi_sb) {
+    if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || elem < 0 || elem > 1) return -1;
+    if (!(softcap >= 0.0) || alibi_sb < 0) return -1;
+    J->elem = elem;
+    J->wl = window_left < 0 ? -1 : window_left;
+    J->wr = causal ? 0 : (window_right < 0 ? -1 : window_right);
+    J->softcap = softcap;
+    J->alibi = alibi;
+    J->alibi_sb = alibi_sb;
+    return 0;
+}
 
 /*
  * Dense batched attention.  q: [B, Nq, Hq, d], k/v: [B, Nk, Hkv, d] with element
@@ -258,20 +323,22 @@ static int run_threads(job_t *base) {
 int oracle_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int Nq, int Nk,
                int Hq, int Hkv, int d, const int64_t *q_strides, const int64_t *k_strides,
                const int64_t *v_strides, double scale, int causal, double *o, double *lse,
-               int nthreads, int elem) {
-    if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || elem < 0 || elem > 1) return -1;
+               int nthreads, int elem, int window_left, int window_right, double softcap,
+               const double *alibi, int64_t alibi_sb) {
     job_t J;
     memset(&J, 0, sizeof J);
+    if (set_common(&J, Hq, Hkv, d, elem, causal, window_left, window_right, softcap, alibi,
+                   alibi_sb) != 0)
+        return -1;
     J.q = q; J.k = k; J.v = v;
     for (int a = 0; a < 3; ++a) { J.qs[a] = q_strides[a]; J.ks[a] = k_strides[a]; J.vs[a] = v_strides[a]; }
-    J.B = B; J.Nq = Nq; J.Nk = Nk; J.Hq = Hq; J.Hkv = Hkv; J.d = d; J.causal = causal;
+    J.B = B; J.Nq = Nq; J.Nk = Nk; J.Hq = Hq; J.Hkv = Hkv; J.d = d;
     J.scale = scale;
     J.o = o; J.lse = lse;
     J.os[0] = (int64_t)Nq * Hq * d; J.os[1] = (int64_t)Hq * d; J.os[2] = d;
     J.lse_s[0] = (int64_t)Hq * Nq; J.lse_s[1] = Nq; J.lse_s[2] = 1;
     J.mode = 0;
     J.nthreads = nthreads;
-    J.elem = elem;
     J.total = (int64_t)B * Nq * Hq;
     return run_threads(&J);
 }
@@ -283,19 +350,21 @@ int oracle_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, i
 int oracle_fwd_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int Nq, int Nk,
                     int Hq, int Hkv, int d, const int64_t *q_strides, const int64_t *k_strides,
                     const int64_t *v_strides, double scale, int causal, const int32_t *rows,
-                    int64_t n, double *o, double *lse, int nthreads, int elem) {
-    if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || elem < 0 || elem > 1) return -1;
+                    int64_t n, double *o, double *lse, int nthreads, int elem, int window_left,
+                    int window_right, double softcap, const double *alibi, int64_t alibi_sb) {
     job_t J;
     memset(&J, 0, sizeof J);
+    if (set_common(&J, Hq, Hkv, d, elem, causal, window_left, window_right, softcap, alibi,
+                   alibi_sb) != 0)
+        return -1;
     J.q = q; J.k = k; J.v = v;
     for (int a = 0; a < 3; ++a) { J.qs[a] = q_strides[a]; J.ks[a] = k_strides[a]; J.vs[a] = v_strides[a]; }
-    J.B = B; J.Nq = Nq; J.Nk = Nk; J.Hq = Hq; J.Hkv = Hkv; J.d = d; J.causal = causal;
+    J.B = B; J.Nq = Nq; J.Nk = Nk; J.Hq = Hq; J.Hkv = Hkv; J.d = d;
     J.scale = scale;
     J.rows = rows; J.nrows = n;
     J.o = o; J.lse = lse;
     J.mode = 0;
     J.nthreads = nthreads;
-    J.elem = elem;
     J.total = n;
     return run_threads(&J);
 }
@@ -308,10 +377,14 @@ int oracle_fwd_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v, int
 int oracle_fwd_varlen(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                       const int32_t *cu_q, const int32_t *cu_k, int B, int Hq, int Hkv, int d,
                       const int64_t *q_strides, const int64_t *k_strides, const int64_t *v_strides,
-                      double scale, int causal, double *o, double *lse, int nthreads, int elem) {
-    if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || elem < 0 || elem > 1) return -1;
+                      double scale, int causal, double *o, double *lse, int nthreads, int elem,
+                      int window_left, int window_right, double softcap, const double *alibi,
+                      int64_t alibi_sb) {
     job_t J;
     memset(&J, 0, sizeof J);
+    if (set_common(&J, Hq, Hkv, d, elem, causal, window_left, window_right, softcap, alibi,
+                   alibi_sb) != 0)
+        return -1;
     J.q = q; J.k = k; J.v = v;
     for (int a = 0; a < 3; ++a) { J.qs[a] = q_strides[a]; J.ks[a] = k_strides[a]; J.vs[a] = v_strides[a]; }
     int64_t total_q = cu_q[B];
@@ -320,7 +393,7 @@ int oracle_fwd_varlen(const uint16_t *q, const uint16_t *k, const uint16_t *v,
         int nk = cu_k[b + 1] - cu_k[b];
         if (nk > max_k) max_k = nk;
     }
-    J.B = B; J.Nq = 0; J.Nk = max_k; J.Hq = Hq; J.Hkv = Hkv; J.d = d; J.causal = causal;
+    J.B = B; J.Nq = 0; J.Nk = max_k; J.Hq = Hq; J.Hkv = Hkv; J.d = d;
     J.scale = scale;
     J.cu_q = cu_q; J.cu_k = cu_k;
     J.o = o; J.lse = lse;
@@ -328,7 +401,6 @@ int oracle_fwd_varlen(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     J.lse_s[0] = 0; J.lse_s[1] = total_q; J.lse_s[2] = 1;
     J.mode = 1;
     J.nthreads = nthreads;
-    J.elem = elem;
     J.total = total_q * Hq;
     return run_threads(&J);
 }
@@ -336,20 +408,25 @@ int oracle_fwd_varlen(const uint16_t *q, const uint16_t *k, const uint16_t *v,
 /*
  * Single-query decode over a padded KV cache.  q: [B, 1, Hq, d] (strides given),
  * k/v cache: [B, Lmax, Hkv, d] (strides given), cache_len: B visible lengths.
- * o: [B, Hq, d] doubles, lse: [B, Hq] doubles.
+ * o: [B, Hq, d] doubles, lse: [B, Hq] doubles.  The query is the last token of its
+ * sequence, so only the left window bound can hide a cached key.
  */
 int oracle_fwd_kvcache(const uint16_t *q, const uint16_t *kc, const uint16_t *vc,
                        const int32_t *cache_len, int B, int Lmax, int Hq, int Hkv, int d,
                        const int64_t *q_strides, const int64_t *k_strides, const int64_t *v_strides,
-                       double scale, double *o, double *lse, int nthreads, int elem) {
-    if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || elem < 0 || elem > 1) return -1;
-    for (int b = 0; b < B; ++b)
-        if (cache_len[b] < 0 || cache_len[b] > Lmax) return -1;
+                       double scale, double *o, double *lse, int nthreads, int elem,
+                       int window_left, int window_right, double softcap, const double *alibi,
+                       int64_t alibi_sb) {
     job_t J;
     memset(&J, 0, sizeof J);
+    if (set_common(&J, Hq, Hkv, d, elem, 0, window_left, window_right, softcap, alibi,
+                   alibi_sb) != 0)
+        return -1;
+    for (int b = 0; b < B; ++b)
+        if (cache_len[b] < 0 || cache_len[b] > Lmax) return -1;
     J.q = q; J.k = kc; J.v = vc;
     for (int a = 0; a < 3; ++a) { J.qs[a] = q_strides[a]; J.ks[a] = k_strides[a]; J.vs[a] = v_strides[a]; }
-    J.B = B; J.Nq = 1; J.Nk = Lmax; J.Hq = Hq; J.Hkv = Hkv; J.d = d; J.causal = 0;
+    J.B = B; J.Nq = 1; J.Nk = Lmax; J.Hq = Hq; J.Hkv = Hkv; J.d = d;
     J.scale = scale;
     J.cache_len = cache_len;
     J.o = o; J.lse = lse;
@@ -357,7 +434,6 @@ int oracle_fwd_kvcache(const uint16_t *q, const uint16_t *kc, const uint16_t *vc
     J.lse_s[0] = Hq; J.lse_s[1] = 1; J.lse_s[2] = 0;
     J.mode = 2;
     J.nthreads = nthreads;
-    J.elem = elem;
     J.total = (int64_t)B * Hq;
     return run_threads(&J);
 }
@@ -369,20 +445,29 @@ int oracle_fwd_kvcache(const uint16_t *q, const uint16_t *kc, const uint16_t *vc
 int oracle_row_probs(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int Nq, int Nk,
                      int Hq, int Hkv, int d, const int64_t *q_strides, const int64_t *k_strides,
                      const int64_t *v_strides, double scale, int causal, int b, int h, int i,
-                     double *p_out, int elem) {
-    if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || b >= B || h >= Hq || i >= Nq || elem < 0 ||
-        elem > 1)
+                     double *p_out, int elem, int window_left, int window_right, double softcap,
+                     const double *alibi, int64_t alibi_sb) {
+    job_t J;
+    memset(&J, 0, sizeof J);
+    if (set_common(&J, Hq, Hkv, d, elem, causal, window_left, window_right, softcap, alibi,
+                   alibi_sb) != 0)
         return -1;
+    if (b < 0 || b >= B || h < 0 || h >= Hq || i < 0 || i >= Nq) return -1;
     int g = h / (Hq / Hkv);
-    int64_t nkeys = visible_keys(i, Nq, Nk, causal);
+    int64_t pos = (int64_t)i + (Nk - Nq), lo, hi;
+    visible_range(pos, Nk, J.wl, J.wr, &lo, &hi);
+    score_mod_t mod;
+    mod.softcap = softcap;
+    mod.has_alibi = alibi != NULL;
+    mod.slope = alibi ? alibi[b * alibi_sb + h] : 0.0;
     double *s = (double *)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
     double *orow = (double *)malloc(sizeof(double) * (size_t)d);
     double lse;
     attend_row(q + b * q_strides[0] + (int64_t)i * q_strides[1] + h * q_strides[2],
                k + b * k_strides[0] + g * k_strides[2], k_strides[1],
-               v + b * v_strides[0] + g * v_strides[2], v_strides[1], nkeys, d, scale, elem, s,
-               orow, &lse);
-    for (int64_t j = 0; j < Nk; ++j) p_out[j] = j < nkeys ? s[j] : 0.0;
+               v + b * v_strides[0] + g * v_strides[2], v_strides[1], lo, hi, pos, d, scale,
+               &mod, elem, s, orow, &lse);
+    for (int64_t j = 0; j < Nk; ++j) p_out[j] = (j >= lo && j < hi) ? s[j - lo] : 0.0;
     free(s);
     free(orow);
     return 0;

@@ -11,6 +11,11 @@ exactly the numbers the GPU reads, widens them exactly to double and computes th
 plain definition of attention
 ("FlashAttention 1-4 详解", section 原算法: S = Q K^T, P = softmax(scale * S),
 O = P V; plus the natural-log log-sum-exp of each row of scaled scores).
+
+Every function also takes the score modifiers of "flash-attention" (capabilities table:
+sliding window, ALiBi, softcap): ``window=(left, right)`` (negative = unbounded; causal
+sets right = 0), ``softcap`` (0 = off) and ``alibi_slopes`` (fp32 ``[Hq]`` or ``[B, Hq]``),
+read as described in attn_oracle.c.
 """
 from __future__ import annotations
 
@@ -53,14 +58,17 @@ def _load():
             i = ctypes.c_int
             i64 = ctypes.c_int64
             d = ctypes.c_double
-            lib.oracle_fwd.argtypes = [p, p, p, i, i, i, i, i, i, p, p, p, d, i, p, p, i, i]
+            mod = [i, i, d, p, i64]  # window_left, window_right, softcap, alibi, alibi_sb
+            lib.oracle_fwd.argtypes = [p, p, p, i, i, i, i, i, i, p, p, p, d, i, p, p, i,
+                                       i] + mod
             lib.oracle_fwd_rows.argtypes = [p, p, p, i, i, i, i, i, i, p, p, p, d, i, p, i64,
-                                            p, p, i, i]
+                                            p, p, i, i] + mod
             lib.oracle_fwd_varlen.argtypes = [p, p, p, p, p, i, i, i, i, p, p, p, d, i, p, p, i,
-                                              i]
-            lib.oracle_fwd_kvcache.argtypes = [p, p, p, p, i, i, i, i, i, p, p, p, d, p, p, i, i]
+                                              i] + mod
+            lib.oracle_fwd_kvcache.argtypes = [p, p, p, p, i, i, i, i, i, p, p, p, d, p, p, i,
+                                               i] + mod
             lib.oracle_row_probs.argtypes = [p, p, p, i, i, i, i, i, i, p, p, p, d, i, i, i, i,
-                                             p, i]
+                                             p, i] + mod
             for f in (lib.oracle_fwd, lib.oracle_fwd_rows, lib.oracle_fwd_varlen,
                       lib.oracle_fwd_kvcache, lib.oracle_row_probs):
                 f.restype = ctypes.c_int
@@ -99,6 +107,35 @@ def _common_elem(*ts, elem=None) -> int:
     return kinds.pop()
 
 
+class _Mod:
+    """Marshalled score modifiers; keeps the slope array alive for the call."""
+
+    def __init__(self, B, Hq, window=(-1, -1), softcap=0.0, alibi_slopes=None):
+        wl, wr = (-1, -1) if window is None else window
+        self.wl, self.wr = int(wl), int(wr)
+        self.softcap = float(softcap or 0.0)
+        self.slopes = None
+        self.sb = 0
+        if alibi_slopes is not None:
+            a = alibi_slopes
+            if hasattr(a, "detach"):
+                a = a.detach().cpu().numpy()
+            a = np.asarray(a)
+            if a.dtype != np.float32:
+                raise TypeError("ALiBi slopes are fp32")
+            if a.ndim == 1 and a.shape[0] == Hq:
+                self.sb = 0
+            elif a.ndim == 2 and a.shape == (B, Hq):
+                self.sb = Hq
+            else:
+                raise ValueError("ALiBi slopes must be [Hq] or [B, Hq]")
+            self.slopes = np.ascontiguousarray(a.astype(np.float64))
+
+    def args(self):
+        ptr = _ptr(self.slopes) if self.slopes is not None else None
+        return (self.wl, self.wr, self.softcap, ptr, self.sb)
+
+
 def _strides4(a: np.ndarray):
     """(b, n, h) element strides of a contiguous [B, N, H, d] array."""
     s = [x // a.itemsize for x in a.strides]
@@ -110,7 +147,7 @@ def _ptr(a: np.ndarray):
 
 
 def attention(q, k, v, scale: float, causal: bool = False, nthreads: int | None = None,
-              elem=None):
+              elem=None, window=(-1, -1), softcap=0.0, alibi_slopes=None):
     """Dense attention.  q [B,Nq,Hq,d], k/v [B,Nk,Hkv,d] (bf16 or fp16).
 
     Returns (O [B,Nq,Hq,d] float64, LSE [B,Hq,Nq] float64).
@@ -119,18 +156,20 @@ def attention(q, k, v, scale: float, causal: bool = False, nthreads: int | None 
     q, k, v = _bits(q), _bits(k), _bits(v)
     B, Nq, Hq, d = q.shape
     _, Nk, Hkv, _ = k.shape
+    mod = _Mod(B, Hq, window, softcap, alibi_slopes)
     o = np.zeros((B, Nq, Hq, d), np.float64)
     lse = np.zeros((B, Hq, Nq), np.float64)
     rc = _load().oracle_fwd(_ptr(q), _ptr(k), _ptr(v), B, Nq, Nk, Hq, Hkv, d, _strides4(q),
                             _strides4(k), _strides4(v), float(scale), int(bool(causal)),
-                            _ptr(o), _ptr(lse), _threads(nthreads), el)
+                            _ptr(o), _ptr(lse), _threads(nthreads), el, *mod.args())
     if rc != 0:
         raise ValueError("oracle_fwd rejected its arguments")
     return o, lse
 
 
 def attention_rows(q, k, v, rows, scale: float, causal: bool = False,
-                   nthreads: int | None = None, elem=None):
+                   nthreads: int | None = None, elem=None, window=(-1, -1), softcap=0.0,
+                   alibi_slopes=None):
     """Dense attention on selected rows; rows is an (n, 3) int array of (b, h, i).
 
     Returns (O [n, d] float64, LSE [n] float64).
@@ -141,19 +180,21 @@ def attention_rows(q, k, v, rows, scale: float, causal: bool = False,
     _, Nk, Hkv, _ = k.shape
     rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 3))
     n = rows.shape[0]
+    mod = _Mod(B, Hq, window, softcap, alibi_slopes)
     o = np.zeros((n, d), np.float64)
     lse = np.zeros((n,), np.float64)
     rc = _load().oracle_fwd_rows(_ptr(q), _ptr(k), _ptr(v), B, Nq, Nk, Hq, Hkv, d,
                                  _strides4(q), _strides4(k), _strides4(v), float(scale),
                                  int(bool(causal)), _ptr(rows), n, _ptr(o), _ptr(lse),
-                                 _threads(nthreads), el)
+                                 _threads(nthreads), el, *mod.args())
     if rc != 0:
         raise ValueError("oracle_fwd_rows rejected its arguments")
     return o, lse
 
 
 def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, causal: bool = False,
-                     nthreads: int | None = None, elem=None):
+                     nthreads: int | None = None, elem=None, window=(-1, -1), softcap=0.0,
+                     alibi_slopes=None):
     """Packed varlen attention.  q [total_q,Hq,d], k/v [total_k,Hkv,d].
 
     Returns (O [total_q,Hq,d] float64, LSE [Hq,total_q] float64).
@@ -170,19 +211,21 @@ def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, causal: 
         s = [x // a.itemsize for x in a.strides]
         return (ctypes.c_int64 * 3)(0, s[0], s[1])
 
+    mod = _Mod(B, Hq, window, softcap, alibi_slopes)
     o = np.zeros((total_q, Hq, d), np.float64)
     lse = np.zeros((Hq, total_q), np.float64)
     rc = _load().oracle_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_q), _ptr(cu_k), B, Hq,
                                    Hkv, d, st3(q), st3(k), st3(v), float(scale),
                                    int(bool(causal)), _ptr(o), _ptr(lse), _threads(nthreads),
-                                   el)
+                                   el, *mod.args())
     if rc != 0:
         raise ValueError("oracle_fwd_varlen rejected its arguments")
     return o, lse
 
 
 def attention_kvcache(q, k_cache, v_cache, cache_seqlens, scale: float,
-                      nthreads: int | None = None, elem=None):
+                      nthreads: int | None = None, elem=None, window=(-1, -1), softcap=0.0,
+                      alibi_slopes=None):
     """Single-query decode.  q [B,1,Hq,d], caches [B,Lmax,Hkv,d], lengths [B].
 
     Returns (O [B,Hq,d] float64, LSE [B,Hq] float64).
@@ -192,26 +235,30 @@ def attention_kvcache(q, k_cache, v_cache, cache_seqlens, scale: float,
     lens = np.ascontiguousarray(np.asarray(cache_seqlens, dtype=np.int32))
     B, _, Hq, d = q.shape
     _, Lmax, Hkv, _ = kc.shape
+    mod = _Mod(B, Hq, window, softcap, alibi_slopes)
     o = np.zeros((B, Hq, d), np.float64)
     lse = np.zeros((B, Hq), np.float64)
     rc = _load().oracle_fwd_kvcache(_ptr(q), _ptr(kc), _ptr(vc), _ptr(lens), B, Lmax, Hq, Hkv,
                                     d, _strides4(q), _strides4(kc), _strides4(vc),
-                                    float(scale), _ptr(o), _ptr(lse), _threads(nthreads), el)
+                                    float(scale), _ptr(o), _ptr(lse), _threads(nthreads), el,
+                                    *mod.args())
     if rc != 0:
         raise ValueError("oracle_fwd_kvcache rejected its arguments")
     return o, lse
 
 
-def row_probs(q, k, v, b: int, h: int, i: int, scale: float, causal: bool = False, elem=None):
+def row_probs(q, k, v, b: int, h: int, i: int, scale: float, causal: bool = False, elem=None,
+              window=(-1, -1), softcap=0.0, alibi_slopes=None):
     """Softmax probabilities P[i, :] of one dense row (zeros on invisible keys)."""
     el = _common_elem(q, k, v, elem=elem)
     q, k, v = _bits(q), _bits(k), _bits(v)
     B, Nq, Hq, d = q.shape
     _, Nk, Hkv, _ = k.shape
+    mod = _Mod(B, Hq, window, softcap, alibi_slopes)
     p = np.zeros((Nk,), np.float64)
     rc = _load().oracle_row_probs(_ptr(q), _ptr(k), _ptr(v), B, Nq, Nk, Hq, Hkv, d,
                                   _strides4(q), _strides4(k), _strides4(v), float(scale),
-                                  int(bool(causal)), b, h, i, _ptr(p), el)
+                                  int(bool(causal)), b, h, i, _ptr(p), el, *mod.args())
     if rc != 0:
         raise ValueError("oracle_row_probs rejected its arguments")
     return p

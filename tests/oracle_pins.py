@@ -411,6 +411,246 @@ def pin_fp16_values(O):
            "fp16 single-key LSE")
 
 
+# --------------------------------------------------------------------------
+# score modifiers: sliding window, softcap, ALiBi ("flash-attention", capabilities table:
+# causal / sliding window / ALiBi / softcap).  The pages name these and give no formulas;
+# the readings pinned here are: with pos = i + Nk - Nq, key j is visible when
+# pos - wl <= j <= pos + wr (negative bound = unbounded); the scaled score z becomes
+# c * tanh(z / c) under a softcap c; ALiBi then adds -slope * |pos - j|.
+
+def _visible_count(pos, Nk, wl, wr):
+    lo = 0 if wl < 0 else max(pos - wl, 0)
+    hi = Nk - 1 if wr < 0 else min(pos + wr, Nk - 1)
+    return lo, max(hi - lo + 1, 0)
+
+
+def pin_window_uniform(O):
+    """Q = 0 under a window: O is the mean of the visible V rows and LSE = ln(#visible);
+    rows whose window holds no key give O = 0, LSE = -inf."""
+    for (Nq, Nk, wl, wr) in [(30, 30, 4, 0), (30, 30, 3, 5), (12, 40, 7, 2), (40, 12, 0, 3),
+                             (25, 25, 0, 0), (20, 33, -1, 6), (20, 33, 9, -1)]:
+        H, d = 2, 16
+        _, k, v = dense_inputs(1, Nq, Nk, H, H, d, seed=200 + Nq + wl)
+        q = torch.zeros((1, Nq, H, d), dtype=torch.bfloat16)
+        o, lse = O.attention(q, k, v, 0.5, False, window=(wl, wr))
+        vv = _np(v)
+        for i in range(Nq):
+            lo, n = _visible_count(i + Nk - Nq, Nk, wl, wr)
+            for h in range(H):
+                if n == 0:
+                    assert np.all(o[0, i, h] == 0.0) and lse[0, h, i] == -np.inf, "empty window"
+                    continue
+                _close(o[0, i, h], vv[0, lo:lo + n, h].mean(axis=0), 1e-13, "window mean O")
+                _close(lse[0, h, i], math.log(n), 1e-13, "window LSE")
+
+
+def pin_window_diagonal(O):
+    """Window (0, 0): each row sees only the key at its own position, so O = v_pos and
+    LSE = scale * q_i . k_pos."""
+    B, Nq, Nk, H, d = 1, 10, 14, 2, 16
+    q, k, v = dense_inputs(B, Nq, Nk, H, H, d, seed=210)
+    o, lse = O.attention(q, k, v, 0.4, False, window=(0, 0))
+    qq, kk, vv = _np(q), _np(k), _np(v)
+    for i in range(Nq):
+        pos = i + Nk - Nq
+        for h in range(H):
+            _close(o[0, i, h], vv[0, pos, h], 1e-14, "diagonal O")
+            _close(lse[0, h, i], 0.4 * float(np.dot(qq[0, i, h], kk[0, pos, h])), 1e-12,
+                   "diagonal LSE")
+
+
+def pin_window_library(O):
+    """Random inputs under a band mask: torch SDPA (float64) with the boolean mask of the
+    visible keys; windows that cover everything reduce to the unmasked / causal results."""
+    for n, (Nq, Nk, wl, wr) in enumerate([(33, 33, 5, 2), (20, 45, 10, 0), (45, 20, 3, 4),
+                                          (64, 64, 0, 7)]):
+        H, d = 2, 32
+        q, k, v = dense_inputs(1, Nq, Nk, H, H, d, seed=220 + n)
+        o, lse = O.attention(q, k, v, 0.2, False, window=(wl, wr))
+        pos = torch.arange(Nq)[:, None] + (Nk - Nq)
+        j = torch.arange(Nk)[None, :]
+        band = (j >= pos - wl) & (j <= pos + wr)
+        qq, kk, vv = (_f64(t).permute(0, 2, 1, 3) for t in (q, k, v))
+        scores = (qq @ kk.transpose(-1, -2) * 0.2).masked_fill(~band, float("-inf"))
+        lse_ref = torch.logsumexp(scores, dim=-1)
+        rows = band.any(dim=1)
+        o_ref = F.scaled_dot_product_attention(qq[:, :, rows], kk, vv, attn_mask=band[rows],
+                                               scale=0.2)
+        _close(o[0][rows.numpy()], o_ref.permute(0, 2, 1, 3)[0].numpy(), 1e-12, "band O")
+        _close(lse, lse_ref.numpy(), 1e-12, "band LSE")
+    q, k, v = dense_inputs(1, 30, 30, 2, 2, 16, seed=230)
+    for causal, win in [(False, (30, 30)), (True, (-1, -1)), (False, (-1, 0)), (False, (99, 0))]:
+        o1, l1 = O.attention(q, k, v, 0.3, causal, window=win)
+        o2, l2 = O.attention(q, k, v, 0.3, causal or win[1] == 0)
+        _close(o1, o2, 0.0, f"window {win} vs plain O")
+        _close(l1, l2, 0.0, f"window {win} vs plain LSE")
+
+
+def pin_softcap_limits(O):
+    """Softcap: Q = 0 keeps every score at 0 (uniform); a very large cap changes nothing
+    measurable; keys with scores far above the cap all saturate at the cap, so they share
+    the probability equally: LSE = log(m e^c + (n - m)) with the other keys at score 0."""
+    _, k, v = dense_inputs(1, 9, 9, 1, 1, 16, seed=240)
+    q0 = torch.zeros((1, 9, 1, 16), dtype=torch.bfloat16)
+    _, l0 = O.attention(q0, k, v, 0.5, False, softcap=3.0)
+    _close(l0, np.full((1, 1, 9), math.log(9)), 1e-13, "softcap uniform LSE")
+    q, k, v = dense_inputs(1, 17, 23, 2, 2, 16, seed=241)
+    o1, l1 = O.attention(q, k, v, 0.25, True, softcap=1e6)
+    o2, l2 = O.attention(q, k, v, 0.25, True)
+    _close(o1, o2, 1e-9, "large softcap O")
+    _close(l1, l2, 1e-9, "large softcap LSE")
+    # keys 0..2 along +e0 with huge scores, keys 3..7 orthogonal (score 0)
+    n, m, cap = 8, 3, 2.5
+    q = torch.zeros((1, 1, 1, 8), dtype=torch.bfloat16)
+    k = torch.zeros((1, n, 1, 8), dtype=torch.bfloat16)
+    v = torch.zeros((1, n, 1, 8), dtype=torch.bfloat16)
+    q[0, 0, 0, 0] = 64.0
+    for j in range(m):
+        k[0, j, 0, 0] = 32.0 * (j + 1)
+    for j in range(m, n):
+        k[0, j, 0, 1 + (j - m) % 7] = 1.0
+    for j in range(n):
+        v[0, j, 0, j % 8] = 1.0
+    o, lse = O.attention(q, k, v, 1.0, False, softcap=cap)
+    z = m * math.exp(cap) + (n - m)
+    _close(lse[0, 0, 0], math.log(z), 1e-12, "saturated softcap LSE")
+    p_hi, p_lo = math.exp(cap) / z, 1.0 / z
+    _close(o[0, 0, 0], np.array([p_hi if j < m else p_lo for j in range(n)]), 1e-12,
+           "saturated softcap O")
+
+
+def _alibi_geometric(pos, lo, hi, a):
+    """sum_{j=lo}^{hi-1} e^{-a |pos - j|} by geometric series (lo <= pos < hi assumed)."""
+    left = pos - lo            # keys below pos: distances 1..left
+    right = hi - 1 - pos       # keys above pos: distances 1..right
+    r = math.exp(-a)
+    g = lambda n: r * (1.0 - r ** n) / (1.0 - r) if n > 0 else 0.0
+    return 1.0 + g(left) + g(right)
+
+
+def pin_alibi_geometric(O):
+    """Q = 0 with ALiBi: P_j = e^{-a |pos - j|} / Z with Z a two-sided geometric sum, so with
+    one-hot V rows O reproduces P; per-(batch, head) slopes read with their batch stride."""
+    B, Nq, Nk, H = 2, 6, 8, 3
+    d = 16
+    slopes = np.array([[0.5, 0.25, 1.0], [0.125, 2.0, 0.75]], np.float32)
+    q = torch.zeros((B, Nq, H, d), dtype=torch.bfloat16)
+    k = bf16_normal((B, Nk, H, d), seed=250)
+    v = torch.zeros((B, Nk, H, d), dtype=torch.bfloat16)
+    for j in range(Nk):
+        v[:, j, :, j] = 1.0
+    for causal in (False, True):
+        o, lse = O.attention(q, k, v, 0.3, causal, alibi_slopes=slopes)
+        for b in range(B):
+            for h in range(H):
+                a = float(slopes[b, h])
+                for i in range(Nq):
+                    pos = i + Nk - Nq
+                    hi = pos + 1 if causal else Nk
+                    zsum = _alibi_geometric(pos, 0, hi, a)
+                    _close(lse[b, h, i], math.log(zsum), 1e-13, "ALiBi geometric LSE")
+                    p = np.array([math.exp(-a * abs(pos - j)) / zsum if j < hi else 0.0
+                                  for j in range(Nk)])
+                    _close(o[b, i, h, :Nk], p, 1e-13, "ALiBi geometric P")
+    o1, l1 = O.attention(q, k, v, 0.3, True, alibi_slopes=np.zeros(H, np.float32))
+    o2, l2 = O.attention(q, k, v, 0.3, True)
+    _close(o1, o2, 0.0, "zero-slope ALiBi O")
+    _close(l1, l2, 0.0, "zero-slope ALiBi LSE")
+
+
+def pin_alibi_library(O):
+    """Random inputs with ALiBi: torch SDPA (float64) with the additive bias
+    -a |pos - j| as a float mask, causal and not, Nq != Nk, GQA."""
+    for n, (Nq, Nk, causal) in enumerate([(40, 40, True), (25, 50, False), (50, 30, True)]):
+        Hq, Hkv, d = 4, 2, 32
+        q, k, v = dense_inputs(1, Nq, Nk, Hq, Hkv, d, seed=260 + n)
+        slopes = (2.0 ** -np.arange(1, Hq + 1)).astype(np.float32)
+        o, lse = O.attention(q, k, v, 0.2, causal, alibi_slopes=slopes)
+        pos = torch.arange(Nq)[:, None] + (Nk - Nq)
+        j = torch.arange(Nk)[None, :]
+        bias = -torch.tensor(slopes, dtype=torch.float64)[:, None, None] * (pos - j).abs()
+        if causal:
+            bias = bias.masked_fill(~(j <= pos), float("-inf"))
+        qq = _f64(q).permute(0, 2, 1, 3)
+        kk = _f64(k).permute(0, 2, 1, 3).repeat_interleave(Hq // Hkv, dim=1)
+        vv = _f64(v).permute(0, 2, 1, 3).repeat_interleave(Hq // Hkv, dim=1)
+        lse_ref = torch.logsumexp(qq @ kk.transpose(-1, -2) * 0.2 + bias, dim=-1)
+        rows = torch.isfinite(lse_ref[0, 0])
+        o_ref = F.scaled_dot_product_attention(qq[:, :, rows], kk, vv,
+                                               attn_mask=bias[None][:, :, rows], scale=0.2)
+        _close(o[0][rows.numpy()], o_ref.permute(0, 2, 1, 3)[0].numpy(), 1e-12, "ALiBi O")
+        _close(lse, lse_ref.numpy(), 1e-12, "ALiBi LSE")
+
+
+def pin_mod_bruteforce(O):
+    """All three modifiers at once on tiny rows, brute force in plain Python: window,
+    then softcap on the scaled score, then the ALiBi bias, then the softmax."""
+    B, Nq, Nk, H, d = 1, 5, 7, 2, 4
+    q, k, v = dense_inputs(B, Nq, Nk, H, H, d, seed=270)
+    qq, kk, vv = _np(q), _np(k), _np(v)
+    scale, cap, wl, wr = 0.9, 1.5, 3, 1
+    slopes = np.array([0.3, 0.7], np.float32)
+    o, lse = O.attention(q, k, v, scale, False, window=(wl, wr), softcap=cap,
+                         alibi_slopes=slopes)
+    for i in range(Nq):
+        pos = i + Nk - Nq
+        for h in range(H):
+            zs, vs = [], []
+            for j in range(Nk):
+                if not (pos - wl <= j <= pos + wr):
+                    continue
+                zdot = sum(float(qq[0, i, h, c]) * float(kk[0, j, h, c]) for c in range(d))
+                z = cap * math.tanh(scale * zdot / cap) - float(slopes[h]) * abs(pos - j)
+                zs.append(z)
+                vs.append(vv[0, j, h])
+            mx = max(zs)
+            w = [math.exp(z - mx) for z in zs]
+            tot = sum(w)
+            _close(lse[0, h, i], mx + math.log(tot), 1e-12, "brute-force LSE")
+            _close(o[0, i, h], sum(wj * vj for wj, vj in zip(w, vs)) / tot, 1e-12,
+                   "brute-force O")
+
+
+def pin_mod_paths(O):
+    """Decode with modifiers equals dense attention of one query at the last position of
+    a sequence of cache_seqlens[b] keys; varlen with modifiers equals per-sequence dense."""
+    B, Lmax, Hq, Hkv, d = 3, 40, 4, 2, 16
+    lens = [40, 1, 23]
+    q = bf16_normal((B, 1, Hq, d), seed=280)
+    kc = bf16_normal((B, Lmax, Hkv, d), seed=281)
+    vc = bf16_normal((B, Lmax, Hkv, d), seed=282)
+    slopes = np.array([[0.1, 0.2, 0.3, 0.4], [0.5, 0.6, 0.7, 0.8], [0.05, 0.0, 1.0, 0.25]],
+                      np.float32)
+    for kw in [dict(window=(5, -1)), dict(softcap=2.0), dict(alibi_slopes=slopes),
+               dict(window=(17, 0), softcap=1.0, alibi_slopes=slopes)]:
+        o, lse = O.attention_kvcache(q, kc, vc, lens, 0.25, **kw)
+        for b, n in enumerate(lens):
+            kwb = dict(kw)
+            if "alibi_slopes" in kw:
+                kwb["alibi_slopes"] = slopes[b]
+            ob, lb = O.attention(q[b:b + 1].contiguous(), kc[b:b + 1, :n].contiguous(),
+                                 vc[b:b + 1, :n].contiguous(), 0.25, False, **kwb)
+            _close(o[b], ob[0, 0], 0.0, f"decode {kw.keys()} batch {b} O")
+            _close(lse[b], lb[0, :, 0], 0.0, f"decode {kw.keys()} batch {b} LSE")
+    sq, sk = [5, 0, 19, 33], [7, 3, 19, 20]
+    q, k, v, cu_q, cu_k = varlen_inputs(sq, sk, 4, 2, 16, seed=283)
+    for causal, kw in [(False, dict(window=(4, 2))), (True, dict(softcap=1.5)),
+                       (True, dict(alibi_slopes=slopes[0], window=(6, -1)))]:
+        o, lse = O.attention_varlen(q, k, v, cu_q, cu_k, 0.25, causal, **kw)
+        for b in range(len(sq)):
+            a, e = int(cu_q[b]), int(cu_q[b + 1])
+            ka, ke = int(cu_k[b]), int(cu_k[b + 1])
+            if e == a:
+                continue
+            ob, lb = O.attention(q[a:e].unsqueeze(0).contiguous(),
+                                 k[ka:ke].unsqueeze(0).contiguous(),
+                                 v[ka:ke].unsqueeze(0).contiguous(), 0.25, causal, **kw)
+            _close(o[a:e], ob[0], 0.0, f"varlen mod seq {b} O")
+            _close(lse[:, a:e], lb[0], 0.0, f"varlen mod seq {b} LSE")
+
+
 ALL_PINS = [pin_library, pin_library_fp16, pin_fp16_values, pin_uniform_scores, pin_single_key, pin_constant_v, pin_two_keys,
             pin_empty_rows, pin_hard_max, pin_probs, pin_shift, pin_permutation, pin_gqa,
-            pin_varlen, pin_kvcache, pin_rows, pin_recurrence, pin_lse_recompute]
+            pin_varlen, pin_kvcache, pin_rows, pin_recurrence, pin_lse_recompute,
+            pin_window_uniform, pin_window_diagonal, pin_window_library, pin_softcap_limits,
+            pin_alibi_geometric, pin_alibi_library, pin_mod_bruteforce, pin_mod_paths]

@@ -19,25 +19,50 @@ def test_oracle_pin(pin):
 # Plausible slips in the oracle's C source.  Each one, planted in a copy built in a
 # temporary directory, must make at least one pin fail.
 MUTATIONS = [
-    ("scale dropped", "s[j] = scale * acc;", "s[j] = acc;"),
+    ("scale dropped", "double z = scale * acc;", "double z = acc;"),
     ("exponent sign flipped", "s[j] = exp(s[j] - m);", "s[j] = exp(m - s[j]);"),
     ("normalisation dropped", "for (int64_t j = 0; j < nkeys; ++j) s[j] /= l;", ""),
     ("max term dropped from LSE", "*lse = m + log(l);", "*lse = log(l);"),
     ("keys read from V", "const uint16_t *kr = kbase + j * k_stride;",
      "const uint16_t *kr = vbase + j * v_stride;"),
-    ("values read from K", "const uint16_t *vr = vbase + j * v_stride;",
-     "const uint16_t *vr = kbase + j * k_stride;"),
+    ("values read from K", "const uint16_t *vr = vbase + (lo + j) * v_stride;",
+     "const uint16_t *vr = kbase + (lo + j) * k_stride;"),
+    ("values not offset by the window start", "const uint16_t *vr = vbase + (lo + j) * v_stride;",
+     "const uint16_t *vr = vbase + j * v_stride;"),
     ("GQA head index wrong", "int g = h / group;", "int g = h % J->Hkv;"),
-    ("causal aligned top-left", "int64_t last = i + (Nk - Nq);", "int64_t last = i;"),
-    ("causal off by one", "return last + 1;", "return last;"),
+    ("causal aligned top-left", "pos = i + (J->Nk - J->Nq);", "pos = i;"),
+    ("causal off by one", "if (wr >= 0 && pos + wr + 1 < b) b = pos + wr + 1;",
+     "if (wr >= 0 && pos + wr < b) b = pos + wr;"),
     ("varlen query offset from key offsets",
      "qrow = J->q + (J->cu_q[b] + i) * J->qs[1] + h * J->qs[2];",
      "qrow = J->q + (J->cu_k[b] + i) * J->qs[1] + h * J->qs[2];"),
-    ("decode ignores cache length", "nkeys = J->cache_len[b];", "nkeys = J->Nk;"),
+    ("decode ignores cache length", "nk = J->cache_len[b];", "nk = J->Nk;"),
     ("fp16 exponent bias off by one", "v = ldexp((double)(f | 0x400), e - 25);",
      "v = ldexp((double)(f | 0x400), e - 24);"),
     ("fp16 subnormals scaled as normals", "if (e == 0) v = ldexp((double)f, -24);",
      "if (e == 0) v = ldexp((double)(f | 0x400), -25);"),
+    ("window left bound off by one", "if (wl >= 0 && pos - wl > a) a = pos - wl;",
+     "if (wl >= 0 && pos - wl + 1 > a) a = pos - wl + 1;"),
+    ("window right bound ignored",
+     "J->wr = causal ? 0 : (window_right < 0 ? -1 : window_right);",
+     "J->wr = causal ? 0 : -1;"),
+    ("softcap applied to the unscaled score",
+     "if (mod->softcap > 0.0) z = mod->softcap * tanh(z / mod->softcap);",
+     "if (mod->softcap > 0.0) z = mod->softcap * tanh(acc / mod->softcap) * scale;"),
+    ("softcap not scaled back", "if (mod->softcap > 0.0) z = mod->softcap * tanh(z / mod->softcap);",
+     "if (mod->softcap > 0.0) z = tanh(z / mod->softcap);"),
+    ("ALiBi bias added", "z -= mod->slope * fabs((double)(pos - j));",
+     "z += mod->slope * fabs((double)(pos - j));"),
+    ("ALiBi distance from the window start", "z -= mod->slope * fabs((double)(pos - j));",
+     "z -= mod->slope * fabs((double)(j - lo));"),
+    ("ALiBi applied before the softcap",
+     "if (mod->softcap > 0.0) z = mod->softcap * tanh(z / mod->softcap);\n        if (mod->has_alibi) z -= mod->slope * fabs((double)(pos - j));",
+     "if (mod->has_alibi) z -= mod->slope * fabs((double)(pos - j));\n        if (mod->softcap > 0.0) z = mod->softcap * tanh(z / mod->softcap);"),
+    ("ALiBi batch stride ignored", "mod.slope = J->alibi ? J->alibi[b * J->alibi_sb + h] : 0.0;",
+     "mod.slope = J->alibi ? J->alibi[h] : 0.0;"),
+    ("ALiBi slope per kv head", "mod.slope = J->alibi ? J->alibi[b * J->alibi_sb + h] : 0.0;",
+     "mod.slope = J->alibi ? J->alibi[b * J->alibi_sb + g] : 0.0;"),
+    ("decode query at the cache start", "pos = nk - 1;", "pos = 0;"),
 ]
 
 
