@@ -42,6 +42,16 @@ def flops(w) -> float:
     return f / 2 if w.causal else f
 
 
+def window_pairs(Nq, Nk, wl, wr) -> int:
+    """Number of (query, key) pairs a sliding window (wl, wr) leaves visible (bottom-right
+    positions, negative bound = unbounded)."""
+    import numpy as np
+    pos = np.arange(Nq, dtype=np.int64) + (Nk - Nq)
+    lo = np.maximum(pos - wl, 0) if wl >= 0 else np.zeros_like(pos)
+    hi = np.minimum(pos + wr, Nk - 1) if wr >= 0 else np.full_like(pos, Nk - 1)
+    return int(np.maximum(hi - lo + 1, 0).sum())
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -53,10 +63,16 @@ def peaks():
 
 
 def source_hash(files) -> str:
+    """sha256[:12] of the kernel sources with comments and blank lines removed, so that
+    a recorded capture stays valid across edits that change no code."""
     h = hashlib.sha256()
     for f in files:
-        with open(os.path.join(ROOT, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, f), encoding="utf-8") as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        code = "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+        h.update(code.encode())
     return h.hexdigest()[:12]
 
 
@@ -435,6 +451,26 @@ def extra_workloads(args, dev, pk, world, dist):
         res[name] = {"ms": round(ms, 4), "TFLOPS": round(tf, 2),
                      "frac_of_bf16_peak": round(tf / pk["bf16"], 4)}
         del q, k, v, o, l
+    # variants of the headline workload: fp16 inputs, a 4096-key sliding window, softcap +
+    # ALiBi (FLOPs: 4 d per visible (query, key) pair; the causal convention N^2/2 otherwise)
+    w = WORKLOADS["causal8k"]
+    slopes = torch.tensor([2.0 ** (-8.0 * (h + 1) / w.Hq) for h in range(w.Hq)],
+                          dtype=torch.float32, device=dev)
+    for name, dtype, kw, work in [
+            ("causal8k_fp16", torch.float16, {}, flops(w)),
+            ("causal8k_window4096", torch.bfloat16, {"window_size": (4096, 0)},
+             4.0 * w.d * w.B * w.Hq * window_pairs(w.Nq, w.Nk, 4096, 0)),
+            ("causal8k_softcap_alibi", torch.bfloat16,
+             {"softcap": 30.0, "alibi_slopes": slopes}, flops(w))]:
+        q, k, v = workload_inputs(w, device=dev, dtype=dtype)
+        o = torch.empty_like(q)
+        l = torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device=dev)
+        ms = time_calls(lambda: fa.fa_fwd(q, k, v, causal=True, out=o, lse=l, **kw),
+                        max(10, args.steps // 4), stream)
+        tf = work / (ms * 1e-3) / 1e12
+        res[name] = {"ms": round(ms, 4), "TFLOPS": round(tf, 2),
+                     "frac_of_bf16_peak": round(tf / pk["bf16"], 4)}
+        del q, k, v, o, l
     w = WORKLOADS["decode"]
     q, kc, vc, lens = kvcache_workload_inputs(w, device=dev)
     ws = torch.empty(fa.fa_fwd_kvcache_workspace_size(w.B, w.Hq, w.Nk, w.d, 0), dtype=torch.uint8,
@@ -454,6 +490,14 @@ def extra_workloads(args, dev, pk, world, dist):
                                                               "decode"),
                                   "peak_basis": f"{pk['basis']} copy bandwidth"},
                      "gpu_launches_per_call": 2}
+    ms = time_calls(lambda: fa.fa_fwd_kvcache(q, kc, vc, lens, workspace=ws, out=o, lse=l,
+                                              window_size=(4095, -1)),
+                    max(20, args.steps // 2), stream)
+    kv_bytes = int(lens.clamp(max=4096).long().sum().item()) * w.Hkv * w.d * 2 * 2
+    gbs = (kv_bytes + io_bytes) / (ms * 1e-3) / 1e9
+    res["decode_window4096"] = {"ms": round(ms, 4), "GB/s": round(gbs, 1),
+                                "algorithmic_bytes": kv_bytes + io_bytes,
+                                "frac_of_hbm": round(gbs / pk["hbm"], 4)}
     st = fa.get_last_device_error()
     if st != fa.FA_OK:
         raise RuntimeError(f"device error in extra workloads: {fa.status_string(st)}")

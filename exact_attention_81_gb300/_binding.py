@@ -41,6 +41,19 @@ class FAError(RuntimeError):
         super().__init__(msg)
 
 
+class ScoreMod(ctypes.Structure):
+    """Mirror of fa_score_mod (sliding window, softcap, ALiBi; zero-filled = none)."""
+
+    _fields_ = [
+        ("use_window", ctypes.c_int),
+        ("window_left", ctypes.c_int),
+        ("window_right", ctypes.c_int),
+        ("softcap", ctypes.c_float),
+        ("alibi_slopes", ctypes.c_void_p),
+        ("alibi_batch_stride", ctypes.c_int64),
+    ]
+
+
 class FwdParams(ctypes.Structure):
     """Mirror of fa_fwd_params."""
 
@@ -63,6 +76,7 @@ class FwdParams(ctypes.Structure):
         ("scale", ctypes.c_float),
         ("causal", ctypes.c_int),
         ("dtype", ctypes.c_int),
+        ("mod", ScoreMod),
     ]
 
 
@@ -85,13 +99,14 @@ def load_library(path: str | None = None):
                              ctypes.c_size_t)
         lib.fa_fwd.argtypes = [ctypes.POINTER(FwdParams), vp]
         lib.fa_fwd.restype = i
+        pmod = ctypes.POINTER(ScoreMod)
         lib.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i,
-                                      i, vp]
+                                      i, pmod, vp]
         lib.fa_fwd_varlen.restype = i
         lib.fa_fwd_kvcache_workspace_size.argtypes = [i, i, i, i, i]
         lib.fa_fwd_kvcache_workspace_size.restype = sz
         lib.fa_fwd_kvcache.argtypes = [vp, vp, vp, vp, i, i, i, i, i, ctypes.POINTER(i64), f, i,
-                                       vp, sz, vp, vp, i, vp]
+                                       vp, sz, vp, vp, i, pmod, vp]
         lib.fa_fwd_kvcache.restype = i
         lib.fa_get_last_device_error.argtypes = [vp]
         lib.fa_get_last_device_error.restype = i
@@ -148,11 +163,37 @@ def default_scale(d: int) -> float:
     return 1.0 / math.sqrt(d)
 
 
-def fa_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
-           stream=None):
-    """Dense attention.  q [B,Nq,Hq,d], k/v [B,Nk,Hkv,d] (bf16, CUDA).
+def _score_mod(B, Hq, device, window_size=None, softcap=0.0, alibi_slopes=None) -> ScoreMod:
+    """fa_score_mod from the Python arguments.  window_size = (left, right), negative =
+    unbounded; alibi_slopes an fp32 CUDA tensor [Hq] or [B, Hq] (kept alive by the caller)."""
+    m = ScoreMod()
+    if window_size is not None:
+        wl, wr = (int(x) for x in window_size)
+        if wl >= 0 or wr >= 0:
+            m.use_window, m.window_left, m.window_right = 1, wl, wr
+    m.softcap = float(softcap or 0.0)
+    if alibi_slopes is not None:
+        a = alibi_slopes
+        if not isinstance(a, torch.Tensor) or a.dtype != torch.float32 or not a.is_cuda:
+            raise TypeError("alibi_slopes must be an fp32 CUDA tensor")
+        if a.device != device:
+            raise ValueError("alibi_slopes must be on the device of q")
+        if a.dim() == 1 and a.shape[0] == Hq and a.is_contiguous():
+            m.alibi_batch_stride = 0
+        elif a.dim() == 2 and tuple(a.shape) == (B, Hq) and a.stride(1) == 1:
+            m.alibi_batch_stride = a.stride(0)
+        else:
+            raise ValueError("alibi_slopes must be [Hq] or [B, Hq] with unit stride over heads")
+        m.alibi_slopes = a.data_ptr()
+    return m
 
-    Returns (out [B,Nq,Hq,d] bf16, lse [B,Hq,Nq] fp32).
+
+def fa_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
+           stream=None, window_size=None, softcap: float = 0.0, alibi_slopes=None):
+    """Dense attention.  q [B,Nq,Hq,d], k/v [B,Nk,Hkv,d] (bf16 or fp16, CUDA).
+
+    window_size (left, right), softcap and alibi_slopes are the score modifiers of
+    fa_score_mod.  Returns (out [B,Nq,Hq,d], lse [B,Hq,Nq] fp32).
     """
     _require_bf16_cuda("q", q, 4)
     _require_bf16_cuda("k", k, 4, q.dtype)
@@ -179,13 +220,14 @@ def fa_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, 
     p.scale = default_scale(d) if scale is None else float(scale)
     p.causal = int(bool(causal))
     p.dtype = _DTYPE[q.dtype]
+    p.mod = _score_mod(B, Hq, q.device, window_size, softcap, alibi_slopes)
     _check(load_library().fa_fwd(ctypes.byref(p), _stream_handle(stream)), "fa_fwd")
     return out, lse
 
 
 def fa_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int,
                   causal: bool = False, scale: float | None = None, out=None, lse=None,
-                  stream=None):
+                  stream=None, window_size=None, softcap: float = 0.0, alibi_slopes=None):
     """Packed varlen attention.  q [total_q,Hq,d], k/v [total_k,Hkv,d], cu_seqlens int32 [B+1].
 
     Returns (out [total_q,Hq,d] bf16, lse [Hq,total_q] fp32).
@@ -211,11 +253,12 @@ def fa_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_se
     if lse is None:
         lse = torch.empty((Hq, total_q), dtype=torch.float32, device=q.device)
     sc = default_scale(d) if scale is None else float(scale)
+    mod = _score_mod(B, Hq, q.device, window_size, softcap, alibi_slopes)
     st = load_library().fa_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
                                       _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), B,
                                       int(max_seqlen_q), int(max_seqlen_k), total_q, total_k, Hq,
                                       Hkv, d, sc, int(bool(causal)), _DTYPE[q.dtype],
-                                      _stream_handle(stream))
+                                      ctypes.byref(mod), _stream_handle(stream))
     _check(st, "fa_fwd_varlen")
     return out, lse
 
@@ -225,7 +268,8 @@ def fa_fwd_kvcache_workspace_size(B: int, Hq: int, Lmax: int, d: int, num_splits
 
 
 def fa_fwd_kvcache(q, k_cache, v_cache, cache_seqlens, scale: float | None = None,
-                   num_splits: int = 0, workspace=None, out=None, lse=None, stream=None):
+                   num_splits: int = 0, workspace=None, out=None, lse=None, stream=None,
+                   window_size=None, softcap: float = 0.0, alibi_slopes=None):
     """Single-query decode.  q [B,1,Hq,d], caches [B,Lmax,Hkv,d], cache_seqlens int32 [B].
 
     Returns (out [B,1,Hq,d] bf16, lse [B,Hq] fp32).
@@ -250,10 +294,11 @@ def fa_fwd_kvcache(q, k_cache, v_cache, cache_seqlens, scale: float | None = Non
         workspace = torch.empty((max(need, 256),), dtype=torch.uint8, device=q.device)
     strides = (ctypes.c_int64 * 3)(*k_cache.stride()[:3])
     sc = default_scale(d) if scale is None else float(scale)
+    mod = _score_mod(B, Hq, q.device, window_size, softcap, alibi_slopes)
     st = load_library().fa_fwd_kvcache(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cache_seqlens),
                                        B, Lmax, Hq, Hkv, d, strides, sc, int(num_splits),
                                        _ptr(workspace), workspace.numel(), _ptr(out), _ptr(lse),
-                                       _DTYPE[q.dtype], _stream_handle(stream))
+                                       _DTYPE[q.dtype], ctypes.byref(mod), _stream_handle(stream))
     _check(st, "fa_fwd_kvcache")
     return out, lse
 
@@ -270,27 +315,32 @@ def set_wait_timeout_ns(ns: int):
 
 # Names of the upstream Python API ("flash-attention", section 1), mapped onto the C calls.
 def flash_attn_func(q, k, v, dropout_p: float = 0.0, softmax_scale=None, causal=False,
-                    return_lse=False):
+                    window_size=(-1, -1), softcap=0.0, alibi_slopes=None, return_lse=False):
     if dropout_p != 0.0:
         raise NotImplementedError("dropout is not part of this forward path")
-    o, lse = fa_fwd(q, k, v, causal=causal, scale=softmax_scale)
+    o, lse = fa_fwd(q, k, v, causal=causal, scale=softmax_scale, window_size=window_size,
+                    softcap=softcap, alibi_slopes=alibi_slopes)
     return (o, lse) if return_lse else o
 
 
 def flash_attn_varlen_func(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
                            dropout_p: float = 0.0, softmax_scale=None, causal=False,
+                           window_size=(-1, -1), softcap=0.0, alibi_slopes=None,
                            return_lse=False):
     if dropout_p != 0.0:
         raise NotImplementedError("dropout is not part of this forward path")
     o, lse = fa_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
-                           causal=causal, scale=softmax_scale)
+                           causal=causal, scale=softmax_scale, window_size=window_size,
+                           softcap=softcap, alibi_slopes=alibi_slopes)
     return (o, lse) if return_lse else o
 
 
 def flash_attn_with_kvcache(q, k_cache, v_cache, cache_seqlens, softmax_scale=None,
-                            causal=True, num_splits=0, return_lse=False):
+                            causal=True, window_size=(-1, -1), softcap=0.0, alibi_slopes=None,
+                            num_splits=0, return_lse=False):
     # With one query per sequence, bottom-right causal alignment lets it see the whole
     # visible prefix, so `causal` does not change the result.
     o, lse = fa_fwd_kvcache(q, k_cache, v_cache, cache_seqlens, scale=softmax_scale,
-                            num_splits=num_splits)
+                            num_splits=num_splits, window_size=window_size, softcap=softcap,
+                            alibi_slopes=alibi_slopes)
     return (o, lse) if return_lse else o

@@ -5,6 +5,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -152,6 +153,64 @@ int decode_chunk(int Lmax, int num_splits) {
   return static_cast<int>(c);
 }
 
+// Score modifiers as the kernels take them.
+struct ModPlan {
+  int mask = fa::MASK_NONE;  // prefill kernel mode
+  int wl = -1, wr = -1;      // window bounds in keys (-1 = unbounded); causal folded into wr
+  float softcap = 0.f;
+  const float *alibi = nullptr;
+  int64_t alibi_sb = 0;
+};
+
+constexpr int kMaxWindow = 1 << 30;  // longer windows are unbounded for every valid length
+
+// Validates `m` (may be null) and folds `causal` into the window.
+fa_status plan_mod(const fa_score_mod *m, int causal, ModPlan *out) {
+  ModPlan p;
+  if (m != nullptr) {
+    if (!std::isfinite(m->softcap) || m->softcap < 0.f) return FA_ERR_INVALID_ARG;
+    if (m->alibi_slopes != nullptr && (!aligned(m->alibi_slopes, 4) || m->alibi_batch_stride < 0))
+      return FA_ERR_INVALID_ARG;
+    if (m->use_window) {
+      p.wl = m->window_left < 0 ? -1 : std::min(m->window_left, kMaxWindow);
+      p.wr = m->window_right < 0 ? -1 : std::min(m->window_right, kMaxWindow);
+    }
+    p.softcap = m->softcap;
+    p.alibi = m->alibi_slopes;
+    p.alibi_sb = m->alibi_batch_stride;
+  }
+  if (causal) p.wr = 0;
+  if (p.softcap == 0.f && p.alibi == nullptr && p.wl < 0)
+    p.mask = p.wr < 0 ? fa::MASK_NONE : (p.wr == 0 ? fa::MASK_CAUSAL : fa::MASK_MOD);
+  else
+    p.mask = fa::MASK_MOD;
+  *out = p;
+  return FA_OK;
+}
+
+void apply_mod(const ModPlan &m, float scale, fa::PrefillArgs *pa) {
+  pa->wl = m.wl;
+  pa->wr = m.wr;
+  // raw score s: softcap * tanh(scale * s / softcap), then * log2(e)
+  pa->sc_in = m.softcap > 0.f ? scale / m.softcap : 0.f;
+  pa->sc_out = m.softcap > 0.f ? static_cast<float>(m.softcap * 1.4426950408889634) : 0.f;
+  pa->alibi = m.alibi;
+  pa->alibi_sb = m.alibi_sb;
+  pa->desc = m.wr >= 0;
+}
+
+// Keys per split when the caller leaves it to the library.  Long chunks amortise the
+// per-unit work (the group's query slice, the merge of the 8 warps, the partial write):
+// 2048 keys (16 blocks) measured best; they are halved, down to 256, only while the units
+// ((batch, kv head) pairs x chunks) would not fill 4 waves of the SMs.  The result never
+// needs more than ws_chunks chunks, the count the workspace was sized for.
+int auto_chunk(int Leff, int64_t pairs, int sm_count, int ws_chunks) {
+  int c = 2048;
+  while (c > 256 && pairs * ceil_div(Leff, c) < 4ll * sm_count) c /= 2;
+  const int fit = (ceil_div(Leff, ws_chunks) + 127) / 128 * 128;
+  return std::max(c, fit);
+}
+
 }  // namespace
 
 extern "C" {
@@ -203,9 +262,12 @@ fa_status fa_fwd(const fa_fwd_params *p, cudaStream_t stream) {
   const int mblocks = ceil_div(a.Nq, 256);
   const int64_t tiles = static_cast<int64_t>(a.B) * a.Hq * mblocks;
   if (tiles > INT32_MAX) return FA_ERR_INVALID_ARG;
+  ModPlan mod;
+  fa_status st = plan_mod(&a.mod, a.causal, &mod);
+  if (st != FA_OK) return st;
 
   DeviceInfo *dev = nullptr;
-  fa_status st = current_device(&dev);
+  st = current_device(&dev);
   if (st != FA_OK) return st;
   const int64_t lse_sb = static_cast<int64_t>(a.Hq) * a.Nq, lse_sh = a.Nq;
   if (a.Nk == 0) {
@@ -244,9 +306,10 @@ fa_status fa_fwd(const fa_fwd_params *p, cudaStream_t stream) {
   pa.err = dev->err;
   pa.timeout_ns = g_timeout_ns;
   pa.sched_slot = fa::next_prefill_sched_slot();
+  apply_mod(mod, a.scale, &pa);
   const int grid = static_cast<int>(tiles < dev->sm_count ? tiles : dev->sm_count);
   cudaError_t e =
-      fa::launch_prefill(a.d, a.causal != 0, a.dtype == FA_FP16, tq, tk, tv, pa, grid, stream);
+      fa::launch_prefill(a.d, mod.mask, a.dtype == FA_FP16, tq, tk, tv, pa, grid, stream);
   return e == cudaSuccess ? FA_OK : cuda_fail("prefill kernel launch", e);
 }
 
@@ -254,7 +317,7 @@ fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, fl
                         const int *cu_seqlens_q, const int *cu_seqlens_k, int B,
                         int max_seqlen_q, int max_seqlen_k, int total_q, int total_k, int Hq,
                         int Hkv, int d, float scale, int causal, int dtype,
-                        cudaStream_t stream) {
+                        const fa_score_mod *mod_in, cudaStream_t stream) {
   if (B < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || total_q < 0 || total_k < 0 || Hq <= 0 ||
       Hkv <= 0 || Hq % Hkv != 0)
     return FA_ERR_INVALID_ARG;
@@ -275,9 +338,12 @@ fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, fl
   const int mblocks = ceil_div(max_seqlen_q, 256);
   const int64_t tiles = static_cast<int64_t>(B) * Hq * mblocks;
   if (tiles > INT32_MAX) return FA_ERR_INVALID_ARG;
+  ModPlan mod;
+  fa_status st = plan_mod(mod_in, causal, &mod);
+  if (st != FA_OK) return st;
 
   DeviceInfo *dev = nullptr;
-  fa_status st = current_device(&dev);
+  st = current_device(&dev);
   if (st != FA_OK) return st;
   const int64_t o_sn = static_cast<int64_t>(Hq) * d, o_sh = d;
   if (total_k == 0) {
@@ -320,9 +386,10 @@ fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, fl
   pa.err = dev->err;
   pa.timeout_ns = g_timeout_ns;
   pa.sched_slot = fa::next_prefill_sched_slot();
+  apply_mod(mod, scale, &pa);
   const int grid = static_cast<int>(tiles < dev->sm_count ? tiles : dev->sm_count);
   cudaError_t e =
-      fa::launch_prefill(d, causal != 0, dtype == FA_FP16, tq, tk, tv, pa, grid, stream);
+      fa::launch_prefill(d, mod.mask, dtype == FA_FP16, tq, tk, tv, pa, grid, stream);
   return e == cudaSuccess ? FA_OK : cuda_fail("prefill kernel launch", e);
 }
 
@@ -338,7 +405,7 @@ fa_status fa_fwd_kvcache(const void *q, const void *k_cache, const void *v_cache
                          const int *cache_seqlens, int B, int Lmax, int Hq, int Hkv, int d,
                          const int64_t cache_strides[3], float scale, int num_splits,
                          void *workspace, size_t workspace_bytes, void *o, float *lse,
-                         int dtype, cudaStream_t stream) {
+                         int dtype, const fa_score_mod *mod_in, cudaStream_t stream) {
   if (B < 0 || Lmax < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || num_splits < 0)
     return FA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
@@ -354,6 +421,9 @@ fa_status fa_fwd_kvcache(const void *q, const void *k_cache, const void *v_cache
     return FA_ERR_INVALID_ARG;
   int chunk = 128, maxch = 0;
   float *o_part = nullptr, *lse_part = nullptr;
+  ModPlan mod;
+  fa_status st = plan_mod(mod_in, 0, &mod);  // the right bound never hides a cached key
+  if (st != FA_OK) return st;
   if (Lmax > 0) {
     if (k_cache == nullptr || v_cache == nullptr || cache_strides == nullptr)
       return FA_ERR_INVALID_ARG;
@@ -364,17 +434,24 @@ fa_status fa_fwd_kvcache(const void *q, const void *k_cache, const void *v_cache
     const size_t need = fa_fwd_kvcache_workspace_size(B, Hq, Lmax, d, num_splits);
     if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256))
       return FA_ERR_WORKSPACE;
+  }
+
+  DeviceInfo *dev = nullptr;
+  st = current_device(&dev);
+  if (st != FA_OK) return st;
+  if (Lmax > 0) {
     chunk = decode_chunk(Lmax, num_splits);
-    maxch = ceil_div(Lmax, chunk);
+    maxch = ceil_div(Lmax, chunk);  // the workspace holds this many chunks per (b, h)
+    // A window limits every sequence to its last wl + 1 keys: the chunks split that range.
+    const int Leff = mod.wl >= 0 ? std::min(Lmax, mod.wl + 1) : Lmax;
+    if (num_splits == 0)
+      chunk = auto_chunk(Leff, static_cast<int64_t>(B) * Hkv, dev->sm_count, maxch);
+    maxch = ceil_div(Leff, chunk);
     o_part = static_cast<float *>(workspace);
     lse_part = o_part + static_cast<int64_t>(B) * Hq * maxch * d;
   }
   const int64_t units = static_cast<int64_t>(maxch) * B * Hkv;
   if (units > INT32_MAX) return FA_ERR_INVALID_ARG;
-
-  DeviceInfo *dev = nullptr;
-  fa_status st = current_device(&dev);
-  if (st != FA_OK) return st;
   if (Lmax > 0) {
     CUtensorMap tk, tv;
     if ((st = make_map(&tk, k_cache, d, Lmax, Hkv, B, cache_strides[1], cache_strides[2],
@@ -398,13 +475,20 @@ fa_status fa_fwd_kvcache(const void *q, const void *k_cache, const void *v_cache
     da.scale_log2 = scale_log2(scale);
     da.err = dev->err;
     da.timeout_ns = g_timeout_ns;
+    da.wl = mod.wl;
+    // the score arrives as scale * q.k * log2(e): softcap * tanh(z / softcap) * log2(e)
+    da.sc_in = mod.softcap > 0.f
+                   ? static_cast<float>(1.0 / (mod.softcap * 1.4426950408889634))
+                   : 0.f;
+    da.sc_out = mod.softcap > 0.f ? static_cast<float>(mod.softcap * 1.4426950408889634) : 0.f;
+    da.alibi = mod.alibi;
+    da.alibi_sb = mod.alibi_sb;
     const int grid = static_cast<int>(units < dev->sm_count ? units : dev->sm_count);
     cudaError_t e = fa::launch_decode(d, group, dtype == FA_FP16, tk, tv, da, grid, stream);
     if (e != cudaSuccess) return cuda_fail("decode kernel launch", e);
   }
   cudaError_t e = fa::launch_combine(d, dtype == FA_FP16, o_part, lse_part, cache_seqlens, B, Hq,
-                                     Lmax, chunk,
-                                     maxch, o, lse, dev->err, stream);
+                                     Lmax, chunk, maxch, mod.wl, o, lse, dev->err, stream);
   return e == cudaSuccess ? FA_OK : cuda_fail("combine kernel launch", e);
 }
 

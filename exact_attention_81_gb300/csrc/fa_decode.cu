@@ -93,6 +93,13 @@ struct Unit {
   int b, g, c, len, key0, nkeys;
 };
 
+// First key visible to the decode query of a sequence of len keys (position len - 1).
+__device__ __forceinline__ int first_visible(int len, int wl) {
+  return wl >= 0 ? max(len - 1 - wl, 0) : 0;
+}
+
+// Unit u = (chunk c, batch b, kv head g).  Chunks tile the visible keys [first, len) from
+// the first visible key on, so a window only moves the start.
 __device__ __forceinline__ Unit unit_of(const DecodeArgs &a, int u) {
   Unit w;
   const int bg = a.B * a.Hkv;
@@ -102,12 +109,12 @@ __device__ __forceinline__ Unit unit_of(const DecodeArgs &a, int u) {
   w.g = r - w.b * a.Hkv;
   const int len_raw = a.cache_len[w.b];
   w.len = min(max(len_raw, 0), a.Lmax);
-  w.key0 = w.c * a.chunk;
+  w.key0 = first_visible(w.len, a.wl) + w.c * a.chunk;
   w.nkeys = min(a.chunk, w.len - w.key0);  // <= 0: nothing to do
   return w;
 }
 
-template <int D, int G>
+template <int D, int G, bool MOD>
 __device__ void producer(const DecodeArgs &a, const CUtensorMap *tmk, const CUtensorMap *tmv,
                          uint8_t *smem, DBars *bars, const WaitCtl &wc) {
   using C = DCfg<D, G>;
@@ -166,7 +173,9 @@ __device__ __forceinline__ void release(uint64_t *bar, int lane) {
   if (lane == 0) mbar_arrive(bar);
 }
 
-template <int D, int G, bool F16>
+// MOD: the launch has a softcap or ALiBi slopes (uniform runtime branches inside; the plain
+// instances carry none of that state).  A window needs no kernel support beyond unit_of.
+template <int D, int G, bool F16, bool MOD>
 __device__ void compute(const DecodeArgs &a, uint8_t *smem, DBars *bars, const WaitCtl &wc,
                         int tid) {
   using C = DCfg<D, G>;
@@ -185,6 +194,8 @@ __device__ void compute(const DecodeArgs &a, uint8_t *smem, DBars *bars, const W
   float *pw = reinterpret_cast<float *>(smem + C::PW_OFF) + warp * (C::KPW * G);
   float *red = reinterpret_cast<float *>(smem + C::RED_OFF);
   const uint16_t *qg = reinterpret_cast<const uint16_t *>(a.q);  // bf16 or fp16 elements
+  const bool softcap = MOD && a.sc_out != 0.f;
+  const bool alibi = MOD && a.alibi != nullptr;
   uint32_t it = 0, sync_phase = 0;
 
   for (int u = blockIdx.x; u < a.num_units; u += gridDim.x) {
@@ -216,6 +227,9 @@ __device__ void compute(const DecodeArgs &a, uint8_t *smem, DBars *bars, const W
       m[gg] = -INFINITY;
       l[gg] = 0.f;
     }
+    // ALiBi slopes of the group's query heads (read where used: G more live registers
+    // would spill at G = 8).
+    const float *slopes = alibi ? a.alibi + w.b * a.alibi_sb + w.g * G : nullptr;
 
     for (int blk = 0; blk < nblk; ++blk) {
       const int nvalid = min(KB, w.nkeys - blk * KB);
@@ -254,6 +268,10 @@ __device__ void compute(const DecodeArgs &a, uint8_t *smem, DBars *bars, const W
 #pragma unroll
             for (int off = C::TPK / 2; off > 0; off >>= 1)
               sv += __shfl_xor_sync(0xffffffffu, sv, off);
+            if (softcap) sv = tanh_ex2(sv * a.sc_in) * a.sc_out;
+            if (alibi)  // - slope * distance from the query at position len - 1, log2 units
+              sv = fmaf(slopes[gg] * -1.4426950408889634f,
+                        static_cast<float>(w.len - 1 - (w.key0 + blk * KB + key)), sv);
             sc[pass][gg] = key < nvalid ? sv : -INFINITY;
           }
         }
@@ -393,7 +411,7 @@ __device__ void compute(const DecodeArgs &a, uint8_t *smem, DBars *bars, const W
   }
 }
 
-template <int D, int G, bool F16>
+template <int D, int G, bool F16, bool MOD>
 __global__ void __launch_bounds__(NTHREADS, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   const DecodeArgs a) {
@@ -422,12 +440,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // Each register-split branch ends on its own named barrier.
   if (warp < PRODUCER_WARP) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(COMPUTE_REGS));
-    compute<D, G, F16>(a, smem, bars, wc, tid);
+    compute<D, G, F16, MOD>(a, smem, bars, wc, tid);
     __syncwarp();
     named_barrier(1, NTHREADS);
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(PRODUCER_REGS));
-    if (warp == PRODUCER_WARP && lane == 0) producer<D, G>(a, &tmk, &tmv, smem, bars, wc);
+    if (warp == PRODUCER_WARP && lane == 0) producer<D, G, MOD>(a, &tmk, &tmv, smem, bars, wc);
     __syncwarp();
     named_barrier(1, NTHREADS);
   }
@@ -437,10 +455,11 @@ template <int D, int G, bool F16>
 cudaError_t launch_decode_impl(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeArgs &a,
                                int grid, cudaStream_t stream) {
   constexpr int smem = DCfg<D, G>::SMEM_BYTES;
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, G, F16>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  const bool mod = a.sc_out != 0.f || a.alibi != nullptr;
+  auto kern = mod ? decode_kernel<D, G, F16, true> : decode_kernel<D, G, F16, false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  decode_kernel<D, G, F16><<<grid, NTHREADS, smem, stream>>>(tk, tv, a);
+  kern<<<grid, NTHREADS, smem, stream>>>(tk, tv, a);
   return cudaGetLastError();
 }
 
@@ -448,12 +467,12 @@ cudaError_t launch_decode_impl(const CUtensorMap &tk, const CUtensorMap &tv, con
 template <int D, bool F16>
 __global__ void __launch_bounds__(D)
     combine_kernel(const float *o_part, const float *lse_part, const int *cache_len, int Hq,
-                   int Lmax, int chunk, int maxch, uint16_t *o, float *lse) {
+                   int Lmax, int chunk, int maxch, int wl, uint16_t *o, float *lse) {
   const int bh = blockIdx.x;
   const int b = bh / Hq;
   const int d = threadIdx.x;
   const int len = min(max(cache_len[b], 0), Lmax);
-  const int nch = (len + chunk - 1) / chunk;
+  const int nch = (len - first_visible(len, wl) + chunk - 1) / chunk;  // chunks of [first, len)
   const float *lp = lse_part + static_cast<int64_t>(bh) * maxch;
   const float *op = o_part + static_cast<int64_t>(bh) * maxch * D;
   if (nch == 0) {
@@ -521,24 +540,25 @@ cudaError_t launch_decode(int d, int group, bool f16, const CUtensorMap &tk,
 
 cudaError_t launch_combine(int d, bool f16, const float *o_part, const float *lse_part,
                            const int *cache_len, int B, int Hq, int Lmax, int chunk, int maxch,
-                           void *o, float *lse, unsigned int * /*err*/, cudaStream_t stream) {
+                           int wl, void *o, float *lse, unsigned int * /*err*/,
+                           cudaStream_t stream) {
   const int blocks = B * Hq;
   if (blocks == 0) return cudaSuccess;
   uint16_t *ob = reinterpret_cast<uint16_t *>(o);
   if (d == 64) {
     if (f16)
       combine_kernel<64, true><<<blocks, 64, 0, stream>>>(o_part, lse_part, cache_len, Hq, Lmax,
-                                                          chunk, maxch, ob, lse);
+                                                          chunk, maxch, wl, ob, lse);
     else
       combine_kernel<64, false><<<blocks, 64, 0, stream>>>(o_part, lse_part, cache_len, Hq, Lmax,
-                                                           chunk, maxch, ob, lse);
+                                                           chunk, maxch, wl, ob, lse);
   } else {
     if (f16)
       combine_kernel<128, true><<<blocks, 128, 0, stream>>>(o_part, lse_part, cache_len, Hq,
-                                                            Lmax, chunk, maxch, ob, lse);
+                                                            Lmax, chunk, maxch, wl, ob, lse);
     else
       combine_kernel<128, false><<<blocks, 128, 0, stream>>>(o_part, lse_part, cache_len, Hq,
-                                                             Lmax, chunk, maxch, ob, lse);
+                                                             Lmax, chunk, maxch, wl, ob, lse);
   }
   return cudaGetLastError();
 }

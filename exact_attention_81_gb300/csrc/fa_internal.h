@@ -34,13 +34,26 @@ struct PrefillArgs {
   int sched_slot;             // this launch's tile-ticket counter slot
   unsigned int *err;          // device error word
   unsigned long long timeout_ns;
+  // Score modifiers (read by the MASK_MOD kernel only).
+  int wl, wr;                 // window bounds in keys, -1 = unbounded (causal folded: wr = 0)
+  float sc_in, sc_out;        // softcap: s -> tanh(s * sc_in) * sc_out (log2 units); 0 = off
+  const float *alibi;         // slopes of (b, h) at alibi[b * alibi_sb + h], or null
+  int64_t alibi_sb;
+  int desc;                   // hand out query blocks last-first (right-bounded windows)
+};
+
+// Masking mode of a prefill launch.
+enum PrefillMask : int {
+  MASK_NONE = 0,    // every key visible (tail of the key range masked)
+  MASK_CAUSAL = 1,  // bottom-right causal
+  MASK_MOD = 2,     // sliding window, softcap and/or ALiBi
 };
 
 // Tile-ticket counter slot for the next prefill launch (round robin over the slots).
 int next_prefill_sched_slot();
 
 // f16: inputs and output are fp16 instead of bf16.
-cudaError_t launch_prefill(int d, bool causal, bool f16, const CUtensorMap &tq,
+cudaError_t launch_prefill(int d, int mask, bool f16, const CUtensorMap &tq,
                            const CUtensorMap &tk, const CUtensorMap &tv, const PrefillArgs &a,
                            int grid, cudaStream_t stream);
 
@@ -57,20 +70,27 @@ struct DecodeArgs {
   float *lse_part;            // [B*Hq, maxch] fp32 partial LSE (natural log)
   int B, Hq, Hkv, Lmax;
   int chunk;                  // keys per split (multiple of 128)
-  int maxch;                  // ceil(Lmax / chunk)
+  int maxch;                  // chunks of the longest visible range: ceil(Leff / chunk)
   int num_units;              // maxch * B * Hkv
   float scale_log2;
   unsigned int *err;
   unsigned long long timeout_ns;
+  // Score modifiers (uniform runtime branches).
+  int wl;                     // left window bound in keys, -1 = unbounded
+  float sc_in, sc_out;        // softcap on the log2-domain score: tanh(s * sc_in) * sc_out
+  const float *alibi;         // slopes of (b, h) at alibi[b * alibi_sb + h], or null
+  int64_t alibi_sb;
 };
 
 cudaError_t launch_decode(int d, int group, bool f16, const CUtensorMap &tk,
                           const CUtensorMap &tv, const DecodeArgs &a, int grid,
                           cudaStream_t stream);
 
+// wl: the decode launch's left window bound (-1 = unbounded); chunks tile the visible keys
+// [max(len - 1 - wl, 0), len) of each sequence.
 cudaError_t launch_combine(int d, bool f16, const float *o_part, const float *lse_part,
                            const int *cache_len, int B, int Hq, int Lmax, int chunk, int maxch,
-                           void *o, float *lse, unsigned int *err, cudaStream_t stream);
+                           int wl, void *o, float *lse, unsigned int *err, cudaStream_t stream);
 
 // Shared-memory bytes the kernels request (for host-side checks).
 int prefill_smem_bytes(int d);

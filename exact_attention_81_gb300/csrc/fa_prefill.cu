@@ -30,6 +30,11 @@
 // Causal masking ("FlashAttention 1-4 详解", FlashAttention 2 engineering notes: skip the
 // tiles above the diagonal, ~N^2/2 work) limits each sub-tile to the K/V tiles that hold a
 // visible key and masks only the tiles that straddle the diagonal or the sequence end.
+// The score modifiers of the capabilities table of "flash-attention" (sliding window,
+// softcap, ALiBi) run in a third mask mode, MASK_MOD: a 256-row block streams only the K/V
+// tiles between its first row's window start and its last row's window end, each
+// sub-tile joins the stream steps its rows can see, and the scores are softcapped and
+// biased in the log2 domain before the row max.
 // Tiles are ordered head-major with the largest causal query blocks first and handed out
 // dynamically: the producer lane of each CTA takes the next ticket from a per-launch
 // atomic counter and passes the tile to the other roles through a small shared-memory
@@ -98,15 +103,19 @@ struct TileInfo {
   int tma_b;        // batch coordinate of the TMA maps (0 for varlen)
   int nq, nk;       // sequence lengths
   int nrows[2];     // valid query rows per sub-tile
-  int nkv[2];       // K/V tiles visited per sub-tile
+  // The block streams K/V tiles kv0, kv0+1, ...; sub-tile t takes part in stream steps
+  // [js[t], je[t]) and so visits nkv[t] = je[t] - js[t] tiles (0: its rows see no key).
+  int kv0;
+  int js[2], je[2], nkv[2];
 };
 
-template <bool CAUSAL>
+template <int MASK>
 __device__ __forceinline__ TileInfo tile_info(const PrefillArgs &a, int tile) {
   TileInfo ti;
   const int bh = tile / a.mblocks;
   const int r = tile - bh * a.mblocks;
-  const int mb = CAUSAL ? (a.mblocks - 1 - r) : r;
+  const bool desc = MASK == MASK_CAUSAL || (MASK == MASK_MOD && a.desc);
+  const int mb = desc ? (a.mblocks - 1 - r) : r;
   ti.b = bh / a.Hq;
   ti.h = bh - ti.b * a.Hq;
   ti.hk = ti.h / a.group;
@@ -129,19 +138,41 @@ __device__ __forceinline__ TileInfo tile_info(const PrefillArgs &a, int tile) {
     ti.tma_b = ti.b;
   }
   const int nkv_all = (ti.nk + BC - 1) / BC;
+  int lo[2], hi[2];  // K/V tile range [lo, hi) of each sub-tile
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     const int first = ti.q_row0 + t * BR;
     const int nr = min(max(ti.nq - first, 0), BR);
     ti.nrows[t] = nr;
+    lo[t] = 0;
+    hi[t] = 0;
     if (nr == 0) {
-      ti.nkv[t] = 0;
-    } else if (!CAUSAL) {
-      ti.nkv[t] = nkv_all;
-    } else {
+    } else if (MASK == MASK_NONE) {
+      hi[t] = nkv_all;
+    } else if (MASK == MASK_CAUSAL) {
       const long long last_key = static_cast<long long>(first) + nr - 1 + ti.nk - ti.nq;
-      ti.nkv[t] = last_key < 0 ? 0 : min(static_cast<int>(last_key / BC) + 1, nkv_all);
+      hi[t] = last_key < 0 ? 0 : min(static_cast<int>(last_key / BC) + 1, nkv_all);
+    } else {
+      // Keys some row of the sub-tile may see: from the first row's window start to the
+      // last row's window end, clipped to the sequence.
+      const long long off = static_cast<long long>(ti.nk) - ti.nq;
+      const long long klo = a.wl >= 0 ? max(first + off - a.wl, 0ll) : 0ll;
+      const long long khi = a.wr >= 0 ? min(first + nr - 1 + off + a.wr, ti.nk - 1ll)
+                                      : ti.nk - 1ll;
+      if (klo <= khi) {
+        lo[t] = static_cast<int>(klo / BC);
+        hi[t] = static_cast<int>(khi / BC) + 1;
+      }
     }
+  }
+  const bool act0 = hi[0] > lo[0], act1 = hi[1] > lo[1];
+  ti.kv0 = act0 ? (act1 ? min(lo[0], lo[1]) : lo[0]) : (act1 ? lo[1] : 0);
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const bool act = hi[t] > lo[t];
+    ti.js[t] = act ? lo[t] - ti.kv0 : 0;
+    ti.je[t] = act ? hi[t] - ti.kv0 : 0;
+    ti.nkv[t] = ti.je[t] - ti.js[t];
   }
   return ti;
 }
@@ -183,7 +214,7 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint3
 // tile to the scheduler ring, then issues its Q tile and its K/V ring loads (ring order
 // K_0, V_0, K_1, V_1, ...).  A ticket past the last tile is published as -1 (end).
 
-template <int D, bool CAUSAL>
+template <int D, int MASK>
 __device__ void producer_role(const PrefillArgs &a, const CUtensorMap *tmq,
                               const CUtensorMap *tmk, const CUtensorMap *tmv, uint8_t *smem,
                               Bars *bars, const WaitCtl &wc) {
@@ -198,9 +229,9 @@ __device__ void producer_role(const PrefillArgs &a, const CUtensorMap *tmq,
     bars->sched_tile[rs] = tile;
     mbar_arrive(&bars->sched_full[rs]);
     if (tile < 0) break;
-    const TileInfo ti = tile_info<CAUSAL>(a, tile);
+    const TileInfo ti = tile_info<MASK>(a, tile);
     if (a.varlen && (ti.q_row0 == 0) && varlen_bad(a, ti.b)) atomicOr(a.err, DEVERR_BAD_CU_SEQLENS);
-    const int n = max(ti.nkv[0], ti.nkv[1]);
+    const int n = max(ti.je[0], ti.je[1]);
     if (n == 0) continue;
     if (q_iter > 0 && !mbar_wait(&bars->q_empty, (q_iter - 1) & 1u, wc)) goto out;
     mbar_arrive_expect_tx(&bars->q_full, 2 * C::TILE_BYTES);
@@ -221,8 +252,8 @@ __device__ void producer_role(const PrefillArgs &a, const CUtensorMap *tmq,
 #pragma unroll
         for (int c = 0; c < C::KCH; ++c)
           tma_load_4d(smem + C::RING_OFF + slot * C::TILE_BYTES + c * BOX_BYTES,
-                      which ? tmv : tmk, &bars->kv_full[slot], c * 64, ti.hk, ti.k_tok + j * BC,
-                      ti.tma_b);
+                      which ? tmv : tmk, &bars->kv_full[slot], c * 64, ti.hk,
+                      ti.k_tok + (ti.kv0 + j) * BC, ti.tma_b);
         ++kv_iter;
       }
     }
@@ -263,9 +294,10 @@ __device__ __forceinline__ bool next_tile(Bars *bars, uint32_t k, int &tile, con
 //   PV_0(j), S_0(j+1), PV_1(j), S_1(j+1)
 // so that each softmax group finds its next S ready while the tensor core works on the
 // other sub-tile.  tcgen05.mma executes in issue order, so S_t(j+1) may overwrite the
-// TMEM columns that PV_t(j) reads P_t(j) from.
+// TMEM columns that PV_t(j) reads P_t(j) from.  Sub-tile t takes part only in the steps
+// [js[t], je[t]) of the block's K/V stream.
 
-template <int D, bool CAUSAL, bool F16>
+template <int D, int MASK, bool F16>
 __device__ void mma_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, uint32_t tmem,
                          const WaitCtl &wc) {
   using C = Cfg<D>;
@@ -278,8 +310,8 @@ __device__ void mma_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, uint32
     int tile;
     if (!next_tile<false>(bars, k, tile, wc)) goto out;
     if (tile < 0) break;
-    const TileInfo ti = tile_info<CAUSAL>(a, tile);
-    const int n = max(ti.nkv[0], ti.nkv[1]);
+    const TileInfo ti = tile_info<MASK>(a, tile);
+    const int n = max(ti.je[0], ti.je[1]);
     if (n == 0) continue;
     if (!mbar_wait(&bars->q_full, q_iter & 1u, wc)) goto out;
     ++q_iter;
@@ -290,7 +322,7 @@ __device__ void mma_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, uint32
       tc_fence_after();
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
-        if (ti.nkv[t] > 0) {
+        if (ti.js[t] == 0 && ti.je[t] > 0) {
           issue_s<D, F16>(tmem + s_col(t), q_smem[t], ring + slot_k * C::TILE_BYTES);
           mma_commit(&bars->s_full[t]);
         }
@@ -309,8 +341,8 @@ __device__ void mma_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, uint32
         tc_fence_after();
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-          if (j < ti.nkv[t]) {
-            if (j == 0 && o_pending[t]) {
+          if (j >= ti.js[t] && j < ti.je[t]) {
+            if (j == ti.js[t] && o_pending[t]) {
               // O_t still holds the previous tile's result until its epilogue has read it.
               if (!mbar_wait(&bars->o_empty[t], oe_phase[t], wc)) goto out;
               oe_phase[t] ^= 1u;
@@ -319,14 +351,15 @@ __device__ void mma_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, uint32
             if (!mbar_wait(&bars->p_ready[t], p_phase[t], wc)) goto out;
             p_phase[t] ^= 1u;
             tc_fence_after();
-            issue_pv<D, F16>(tmem + o_col(t), tmem + s_col(t), ring + slot_v * C::TILE_BYTES, j > 0);
-            if (j == ti.nkv[t] - 1) {
+            issue_pv<D, F16>(tmem + o_col(t), tmem + s_col(t), ring + slot_v * C::TILE_BYTES,
+                             j > ti.js[t]);
+            if (j == ti.je[t] - 1) {
               mma_commit(&bars->o_full[t]);
               o_pending[t] = true;
             }
           }
           if (t == 1) mma_commit(&bars->kv_empty[slot_v]);
-          if (j + 1 < ti.nkv[t]) {
+          if (j + 1 >= ti.js[t] && j + 1 < ti.je[t]) {
             issue_s<D, F16>(tmem + s_col(t), q_smem[t], ring + slot_k * C::TILE_BYTES);
             mma_commit(&bars->s_full[t]);
           }
@@ -350,16 +383,22 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const 
   return __all_sync(0xffffffffu, ok);
 }
 
-template <int D, bool CAUSAL, bool F16>
+template <int D, int MASK, bool F16>
 __device__ void softmax_role(const PrefillArgs &a, Bars *bars, uint32_t tmem, const WaitCtl &wc,
                              int warp, int lane) {
+  constexpr bool CAUSAL = MASK == MASK_CAUSAL;
+  constexpr bool MOD = MASK == MASK_MOD;
   const int t = warp >> 2;
   const int wq = warp & 3;
   const int rit = wq * 32 + lane;  // row inside the sub-tile = TMEM lane
   const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
   const uint32_t tS = tmem + lane_off + s_col(t);
   const uint32_t tO = tmem + lane_off + o_col(t);
-  const float c = a.scale_log2;
+  // With a softcap or ALiBi the scores are moved to the log2 domain before the max, and
+  // the exp2 argument needs no further scaling.
+  const bool softcap = MOD && a.sc_out != 0.f;
+  const bool alibi = MOD && a.alibi != nullptr;
+  const float c = (softcap || alibi) ? 1.f : a.scale_log2;
   uint32_t s_phase = 0, o_phase = 0;
   uint16_t *obase = reinterpret_cast<uint16_t *>(a.o);  // bf16 or fp16 elements
 
@@ -367,16 +406,28 @@ __device__ void softmax_role(const PrefillArgs &a, Bars *bars, uint32_t tmem, co
     int tile;
     if (!next_tile<true>(bars, k, tile, wc)) return;
     if (tile < 0) break;
-    const TileInfo ti = tile_info<CAUSAL>(a, tile);
+    const TileInfo ti = tile_info<MASK>(a, tile);
     const int nrows = t == 0 ? ti.nrows[0] : ti.nrows[1];
     if (nrows == 0) continue;
     const int nkv = t == 0 ? ti.nkv[0] : ti.nkv[1];
+    const int kt0 = ti.kv0 + (t == 0 ? ti.js[0] : ti.js[1]);  // first K/V tile of this sub-tile
     const int first_row = ti.q_row0 + t * BR;
     const int row = first_row + rit;
     const bool row_ok = rit < nrows;
-    // Last key index this row may see, and the smallest such index over the sub-tile.
-    const int limit = CAUSAL ? min(row + ti.nk - ti.nq, ti.nk - 1) : ti.nk - 1;
-    const int min_limit = CAUSAL ? min(first_row + ti.nk - ti.nq, ti.nk - 1) : ti.nk - 1;
+    const int off = ti.nk - ti.nq;  // bottom-right alignment: row i sits at key position i + off
+    // Keys [lo, limit] this row may see; tiles inside [all_lo, min_limit] need no mask.
+    int lo = 0, all_lo = 0, limit, min_limit;
+    if constexpr (MOD) {
+      lo = a.wl >= 0 ? max(row + off - a.wl, 0) : 0;
+      all_lo = a.wl >= 0 ? max(first_row + BR - 1 + off - a.wl, 0) : 0;
+      limit = a.wr >= 0 ? min(row + off + a.wr, ti.nk - 1) : ti.nk - 1;
+      min_limit = a.wr >= 0 ? min(first_row + off + a.wr, ti.nk - 1) : ti.nk - 1;
+    } else {
+      limit = CAUSAL ? min(row + off, ti.nk - 1) : ti.nk - 1;
+      min_limit = CAUSAL ? min(first_row + off, ti.nk - 1) : ti.nk - 1;
+    }
+    float slope2 = 0.f;  // ALiBi slope in log2 units
+    if (alibi) slope2 = a.alibi[ti.b * a.alibi_sb + ti.h] * 1.4426950408889634f;
 
     float m = -INFINITY, l = 0.f;
     const uint64_t c2 = f2_pack(c, c);
@@ -394,8 +445,28 @@ __device__ void softmax_role(const PrefillArgs &a, Bars *bars, uint32_t tmem, co
           s[64 + i] = __uint_as_float(r1[i]);
         }
       }
-      const int kbase = j * BC;
-      if (kbase + BC - 1 > min_limit) {
+      const int kbase = (kt0 + j) * BC;
+      if constexpr (MOD) {
+        if (softcap) {
+          // softcap * tanh(scale * q.k / softcap), in log2 units
+#pragma unroll
+          for (int i = 0; i < BC; ++i) s[i] = tanh_ex2(s[i] * a.sc_in) * a.sc_out;
+        }
+        if (alibi) {
+          // - slope * |pos - key|, pos = row + off; the key of column i is kbase + i
+          const float cs = softcap ? 1.f : a.scale_log2;
+          const float dist0 = static_cast<float>(row + off - kbase);
+#pragma unroll
+          for (int i = 0; i < BC; ++i)
+            s[i] = fmaf(s[i], cs, -slope2 * fabsf(dist0 - static_cast<float>(i)));
+        }
+        if (kbase < all_lo || kbase + BC - 1 > min_limit) {
+          const int l0 = lo - kbase, lim = limit - kbase;
+#pragma unroll
+          for (int i = 0; i < BC; ++i)
+            if (i < l0 || i > lim) s[i] = -INFINITY;
+        }
+      } else if (kbase + BC - 1 > min_limit) {
         const int lim = limit - kbase;
 #pragma unroll
         for (int i = 0; i < BC; ++i)
@@ -515,7 +586,7 @@ __device__ void softmax_role(const PrefillArgs &a, Bars *bars, uint32_t tmem, co
   }
 }
 
-template <int D, bool CAUSAL, bool F16>
+template <int D, int MASK, bool F16>
 __global__ void __launch_bounds__(NTHREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv, const PrefillArgs a) {
@@ -567,16 +638,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // before TMEM is released.
   if (warp < PRODUCER_WARP) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(SOFTMAX_REGS));
-    softmax_role<D, CAUSAL, F16>(a, bars, tmem, wc, warp, lane);
+    softmax_role<D, MASK, F16>(a, bars, tmem, wc, warp, lane);
     __syncwarp();
     tc_fence_before();
     named_barrier(1, NTHREADS);
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(OTHER_REGS));
     if (warp == PRODUCER_WARP) {
-      if (lane == 0) producer_role<D, CAUSAL>(a, &tmq, &tmk, &tmv, smem, bars, wc);
+      if (lane == 0) producer_role<D, MASK>(a, &tmq, &tmk, &tmv, smem, bars, wc);
     } else if (warp == MMA_WARP) {
-      if (lane == 0) mma_role<D, CAUSAL, F16>(a, smem, bars, tmem, wc);
+      if (lane == 0) mma_role<D, MASK, F16>(a, smem, bars, tmem, wc);
     }
     __syncwarp();
     tc_fence_before();
@@ -588,14 +659,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
 }
 
-template <int D, bool CAUSAL, bool F16>
+template <int D, int MASK, bool F16>
 cudaError_t launch_impl(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                         const PrefillArgs &a, int grid, cudaStream_t stream) {
   constexpr int smem = Cfg<D>::SMEM_BYTES;
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, CAUSAL, F16>,
+  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, MASK, F16>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  prefill_kernel<D, CAUSAL, F16><<<grid, NTHREADS, smem, stream>>>(tq, tk, tv, a);
+  prefill_kernel<D, MASK, F16><<<grid, NTHREADS, smem, stream>>>(tq, tk, tv, a);
   return cudaGetLastError();
 }
 
@@ -625,23 +696,25 @@ int next_prefill_sched_slot() {
 
 int prefill_smem_bytes(int d) { return d == 64 ? Cfg<64>::SMEM_BYTES : Cfg<128>::SMEM_BYTES; }
 
-template <bool F16>
-cudaError_t launch_typed(int d, bool causal, const CUtensorMap &tq, const CUtensorMap &tk,
-                         const CUtensorMap &tv, const PrefillArgs &a, int grid,
-                         cudaStream_t stream) {
-  if (d == 64) {
-    return causal ? launch_impl<64, true, F16>(tq, tk, tv, a, grid, stream)
-                  : launch_impl<64, false, F16>(tq, tk, tv, a, grid, stream);
+template <int D, bool F16>
+cudaError_t launch_mask(int mask, const CUtensorMap &tq, const CUtensorMap &tk,
+                        const CUtensorMap &tv, const PrefillArgs &a, int grid,
+                        cudaStream_t stream) {
+  switch (mask) {
+    case MASK_NONE: return launch_impl<D, MASK_NONE, F16>(tq, tk, tv, a, grid, stream);
+    case MASK_CAUSAL: return launch_impl<D, MASK_CAUSAL, F16>(tq, tk, tv, a, grid, stream);
+    default: return launch_impl<D, MASK_MOD, F16>(tq, tk, tv, a, grid, stream);
   }
-  return causal ? launch_impl<128, true, F16>(tq, tk, tv, a, grid, stream)
-                : launch_impl<128, false, F16>(tq, tk, tv, a, grid, stream);
 }
 
-cudaError_t launch_prefill(int d, bool causal, bool f16, const CUtensorMap &tq,
+cudaError_t launch_prefill(int d, int mask, bool f16, const CUtensorMap &tq,
                            const CUtensorMap &tk, const CUtensorMap &tv, const PrefillArgs &a,
                            int grid, cudaStream_t stream) {
-  return f16 ? launch_typed<true>(d, causal, tq, tk, tv, a, grid, stream)
-             : launch_typed<false>(d, causal, tq, tk, tv, a, grid, stream);
+  if (d == 64)
+    return f16 ? launch_mask<64, true>(mask, tq, tk, tv, a, grid, stream)
+               : launch_mask<64, false>(mask, tq, tk, tv, a, grid, stream);
+  return f16 ? launch_mask<128, true>(mask, tq, tk, tv, a, grid, stream)
+             : launch_mask<128, false>(mask, tq, tk, tv, a, grid, stream);
 }
 
 cudaError_t launch_fill_empty(void *o, float *lse, int B, int N, int H, int d, int64_t o_sb,

@@ -348,6 +348,20 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// 1/x, approximate (rcp.approx.ftz.f32).
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// tanh(x) = 1 - 2 / (1 + e^{2x}) with e^{2x} = 2^{2 x log2 e}.  Absolute error a few
+// units of 2^-24; saturates to +-1 (e^{2x} -> inf or 0) for large |x|.
+__device__ __forceinline__ float tanh_ex2(float x) {
+  const float e = ex2_approx(x * 2.8853900817779268f);
+  return 1.f - 2.f * rcp_approx(1.f + e);
+}
+
 // Packs two floats to bf16x2 with round-to-nearest-even; `lo` goes to the low half.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;

@@ -64,9 +64,9 @@ def dense_inputs(B, Nq, Nk, Hq, Hkv, d, seed, device="cpu", dtype=torch.bfloat16
     return q, k, v
 
 
-def workload_inputs(w: Workload, device="cpu", seed=None):
+def workload_inputs(w: Workload, device="cpu", seed=None, dtype=torch.bfloat16):
     s = w.seed if seed is None else seed
-    return dense_inputs(w.B, w.Nq, w.Nk, w.Hq, w.Hkv, w.d, s, device)
+    return dense_inputs(w.B, w.Nq, w.Nk, w.Hq, w.Hkv, w.d, s, device, dtype)
 
 
 def varlen_inputs(seqlens_q, seqlens_k, Hq, Hkv, d, seed, device="cpu", dtype=torch.bfloat16):

@@ -63,6 +63,34 @@ typedef enum fa_status {
 } fa_status;
 
 /*
+ * Score modifiers: the sliding window, softcap and ALiBi variants named in the
+ * capabilities table of "flash-attention" (causal / sliding window / ALiBi / softcap).
+ * The pages give no formulas; this library reads them as follows.  With
+ * pos = i + (Nk - Nq) the bottom-right position of query i (for decode, the query is the
+ * last of cache_seqlens[b] tokens: pos = cache_seqlens[b] - 1):
+ *   - window: key j is visible when pos - window_left <= j <= pos + window_right; a
+ *     negative bound is unbounded.  causal != 0 forces window_right = 0.  Used only when
+ *     use_window != 0 (so a zero-filled struct changes nothing).
+ *   - softcap > 0: the scaled score z = scale * q . k_j becomes softcap * tanh(z / softcap).
+ *     0 disables it; negative or non-finite values are rejected (FA_ERR_INVALID_ARG).
+ *   - alibi_slopes: NULL, or DEVICE fp32 slopes, slope of (batch b, query head h) at
+ *     alibi_slopes[b * alibi_batch_stride + h] (stride 0 shares one row of Hq slopes).
+ *     The score (after the softcap) gets -slope * |pos - j| added.  4-byte aligned;
+ *     alibi_batch_stride >= 0.
+ * The softmax and the LSE are then taken over the modified scores of the visible keys;
+ * rows that see no key give O = 0 and LSE = -inf.  A NULL fa_score_mod pointer (or a
+ * zero-filled struct) means no modifier.
+ */
+typedef struct fa_score_mod {
+    int use_window;
+    int window_left;
+    int window_right;
+    float softcap;
+    const float *alibi_slopes;
+    int64_t alibi_batch_stride;
+} fa_score_mod;
+
+/*
  * Dense batched attention, the flash_attn_func call of "flash-attention" section 1:
  * q/k/v in the (batch, seqlen, nheads, headdim) layout; element type `dtype` (fa_dtype).
  *   q   : [B, Nq, Hq,  d], element (b,n,h,c) at q + b*q_strides[0] + n*q_strides[1]
@@ -72,8 +100,8 @@ typedef enum fa_status {
  *   lse : [B, Hq, Nq] fp32 output, contiguous
  * Strides are in elements; the head dimension has unit stride.
  * scale multiplies the scores before the softmax (usually 1/sqrt(d)); causal != 0
- * applies the bottom-right causal mask.  Nk = 0 is allowed (O = 0, LSE = -inf);
- * B = 0 or Nq = 0 is a no-op.
+ * applies the bottom-right causal mask; mod holds the score modifiers (zero-filled = none).
+ * Nk = 0 is allowed (O = 0, LSE = -inf); B = 0 or Nq = 0 is a no-op.
  */
 typedef struct fa_fwd_params {
     const void *q;
@@ -86,6 +114,7 @@ typedef struct fa_fwd_params {
     float scale;
     int causal;
     int dtype; /* fa_dtype of q, k, v and o */
+    fa_score_mod mod;
 } fa_fwd_params;
 
 fa_status fa_fwd(const fa_fwd_params *p, cudaStream_t stream);
@@ -103,14 +132,15 @@ fa_status fa_fwd(const fa_fwd_params *p, cudaStream_t stream);
  *         fa_get_last_device_error).
  *   o   : [total_q, Hq, d] bf16 output, contiguous
  *   lse : [Hq, total_q] fp32 output, contiguous
- * Each sequence is attended on its own; causal alignment is per sequence.  dtype is the
- * fa_dtype of q, k, v and o.
+ * Each sequence is attended on its own; causal and window alignment is per sequence.
+ * dtype is the fa_dtype of q, k, v and o; mod the score modifiers (NULL = none; host
+ * memory, read during the call).
  */
 fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
                         const int *cu_seqlens_q, const int *cu_seqlens_k, int B,
                         int max_seqlen_q, int max_seqlen_k, int total_q, int total_k, int Hq,
                         int Hkv, int d, float scale, int causal, int dtype,
-                        cudaStream_t stream);
+                        const fa_score_mod *mod, cudaStream_t stream);
 
 /*
  * Single-query decode against a padded KV cache, the flash_attn_with_kvcache call of
@@ -132,6 +162,9 @@ fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, fl
  *   o            : [B, 1, Hq, d] bf16 output, contiguous
  *   lse          : [B, Hq] fp32 output, contiguous
  * Hq / Hkv must be 1, 2, 4 or 8.  dtype is the fa_dtype of q, the caches and o.
+ * mod: score modifiers (NULL = none; host memory, read during the call).  Only the left
+ * window bound can hide a cached key (the query is the last position); cache rows before
+ * the window start take no part in the result.
  */
 size_t fa_fwd_kvcache_workspace_size(int B, int Hq, int Lmax, int d, int num_splits);
 
@@ -139,7 +172,7 @@ fa_status fa_fwd_kvcache(const void *q, const void *k_cache, const void *v_cache
                          const int *cache_seqlens, int B, int Lmax, int Hq, int Hkv, int d,
                          const int64_t cache_strides[3], float scale, int num_splits,
                          void *workspace, size_t workspace_bytes, void *o, float *lse,
-                         int dtype, cudaStream_t stream);
+                         int dtype, const fa_score_mod *mod, cudaStream_t stream);
 
 /*
  * Split-KV decode that allocates nothing.  Same computation, arguments and outputs as

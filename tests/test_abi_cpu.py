@@ -61,6 +61,24 @@ def test_fwd_rejects_bad_arguments(lib, change, status):
     assert lib.fa_fwd(ctypes.byref(p), None) == status
 
 
+def _mod(**kw):
+    from exact_attention_81_gb300._binding import ScoreMod
+    m = ScoreMod()
+    for k, v in kw.items():
+        setattr(m, k, v)
+    return m
+
+
+@pytest.mark.parametrize("mod", [
+    dict(softcap=-0.5), dict(softcap=float("nan")), dict(softcap=float("inf")),
+    dict(alibi_slopes=4097), dict(alibi_slopes=4096, alibi_batch_stride=-1),
+])
+def test_fwd_rejects_bad_score_mod(lib, mod):
+    p = _params()
+    p.mod = _mod(**mod)
+    assert lib.fa_fwd(ctypes.byref(p), None) == 1
+
+
 def test_fwd_rejects_misaligned_stride(lib):
     p = _params()
     p.q_strides[1] = 4 * 128 + 4  # not a multiple of 8 elements
@@ -82,7 +100,7 @@ def test_varlen_rejects_bad_arguments(lib):
         a = dict(good, **kw)
         return f(a["q"], a["k"], a["v"], a["o"], a["lse"], a["cq"], a["ck"], a["B"], a["mq"],
                  a["mk"], a["tq"], a["tk"], a["Hq"], a["Hkv"], a["d"], a["scale"], a["causal"],
-                 a["dtype"], None)
+                 a["dtype"], a.get("mod"), None)
 
     assert call(d=80) == 2
     assert call(dtype=3) == 2
@@ -92,6 +110,8 @@ def test_varlen_rejects_bad_arguments(lib):
     assert call(tq=-1) == 1
     assert call(B=0) == 0
     assert call(tq=0) == 0
+    assert call(mod=ctypes.byref(_mod(softcap=-1.0))) == 1
+    assert call(mod=ctypes.byref(_mod(alibi_slopes=4098))) == 1
 
 
 def test_kvcache_rejects_bad_arguments(lib):
@@ -103,7 +123,7 @@ def test_kvcache_rejects_bad_arguments(lib):
         a.update(kw)
         return lib.fa_fwd_kvcache(a["q"], a["kc"], a["vc"], a["lens"], a["B"], a["L"], a["Hq"],
                                   a["Hkv"], a["d"], strides, a["scale"], a["ns"], a["ws"],
-                                  a["wsb"], a["o"], a["lse"], a["dtype"], None)
+                                  a["wsb"], a["o"], a["lse"], a["dtype"], a.get("mod"), None)
 
     assert call(Hq=32, Hkv=2) == 2          # group of 16 not supported by decode
     assert call(dtype=5) == 2
@@ -116,6 +136,8 @@ def test_kvcache_rejects_bad_arguments(lib):
     assert call(wsb=need - 1) == 4
     assert call(ws=4096 + 16) == 4          # workspace must be 256-byte aligned
     assert call(B=0) == 0
+    assert call(mod=ctypes.byref(_mod(softcap=float("inf")))) == 1
+    assert call(mod=ctypes.byref(_mod(alibi_slopes=4096, alibi_batch_stride=-32))) == 1
 
 
 def test_workspace_size(lib):
