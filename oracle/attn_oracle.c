@@ -472,3 +472,99 @@ int oracle_row_probs(const uint16_t *q, const uint16_t *k, const uint16_t *v, in
     free(orow);
     return 0;
 }
+
+/* ------------------------------------------------------------------------- */
+/* KV-cache extras: rotary embedding of the new key and the query.            */
+/*
+ * "flash-attention" (section 1, usage: the decode call updates the KV cache in place and
+ * applies rotary in the same step; capabilities table, KV cache row).  The pages give no
+ * formula; the rotation read here is the standard rotary position embedding: dimension
+ * pairs (a, b) of the first rotary_dim dimensions -- (i, i + rotary_dim/2), or (2i, 2i+1)
+ * when interleaved -- turn by the angle whose cosine and sine are the table entries of
+ * the token's position p:
+ *     y_a = x_a cos - x_b sin,   y_b = x_a sin + x_b cos.
+ * Dimensions from rotary_dim on are copied.  The result is stored in the element type of
+ * the cache, so it is rounded once, to nearest even.  Because that rounding turns a real
+ * number into a 16-bit code, it is evaluated in the precision the kernel uses: fp32, with
+ * the products and sums grouped as written below (one fused multiply-add per output), so
+ * that both sides round the same fp32 value.
+ */
+
+/* fp32 -> bf16 bits, round to nearest even (NaN stays NaN). */
+static uint16_t f32_to_bf16_bits(float f) {
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7fffffffu) > 0x7f800000u) return (uint16_t)((u >> 16) | 0x40u);
+    uint32_t lsb = (u >> 16) & 1u;
+    u += 0x7fffu + lsb;
+    return (uint16_t)(u >> 16);
+}
+
+/* fp32 -> IEEE binary16 bits, round to nearest even, with subnormals and overflow to inf. */
+static uint16_t f32_to_fp16_bits(float f) {
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    uint16_t sign = (uint16_t)((u >> 16) & 0x8000u);
+    uint32_t a = u & 0x7fffffffu;
+    if (a > 0x7f800000u) return (uint16_t)(sign | 0x7e00u);          /* NaN */
+    if (a >= 0x477ff000u) return (uint16_t)(sign | 0x7c00u);         /* rounds to >= 65520: inf */
+    int e = (int)(a >> 23) - 127;                                    /* unbiased exponent */
+    uint32_t m = (a & 0x7fffffu) | 0x800000u;                        /* 24-bit significand */
+    if (a < 0x00800000u) return sign;                                /* fp32 subnormal: far below fp16 */
+    int shift;                                                       /* bits to drop */
+    uint32_t base;
+    if (e >= -14) {                                                  /* fp16 normal */
+        shift = 13;
+        base = (uint32_t)(e + 15) << 10;
+        m &= 0x7fffffu;                                              /* drop the implicit one */
+    } else {                                                         /* fp16 subnormal: units of 2^-24 */
+        shift = 13 + (-14 - e);
+        if (shift > 24) return sign;
+        base = 0;
+    }
+    uint32_t q = m >> shift, rem = m & ((1u << shift) - 1u), half = 1u << (shift - 1);
+    if (rem > half || (rem == half && (q & 1u))) q += 1u;
+    return (uint16_t)(sign | (base + q));                            /* a carry moves into the exponent */
+}
+
+static uint16_t f32_to_bits(float f, int elem) {
+    return elem ? f32_to_fp16_bits(f) : f32_to_bf16_bits(f);
+}
+
+/*
+ * Rotary embedding of `rows` vectors of d elements: row r at x + r * x_stride, position
+ * pos[r], tables cos/sin [*, rotary_dim / 2] fp32 (row p at p * rotary_dim / 2).  Writes
+ * out (row r at out + r * d, contiguous).  Returns 0, or -1 on bad arguments.
+ */
+int oracle_rotary(const uint16_t *x, int64_t x_stride, int64_t rows, int d, const int32_t *pos,
+                  const float *cos_t, const float *sin_t, int rotary_dim, int interleaved,
+                  uint16_t *out, int elem) {
+    if (d <= 0 || rotary_dim <= 0 || rotary_dim > d || (rotary_dim & 1) || elem < 0 || elem > 1)
+        return -1;
+    int half = rotary_dim / 2;
+    for (int64_t r = 0; r < rows; ++r) {
+        const uint16_t *xr = x + r * x_stride;
+        uint16_t *orow = out + r * d;
+        for (int c = 0; c < d; ++c) orow[c] = xr[c];
+        const float *cr = cos_t + (int64_t)pos[r] * half;
+        const float *sr = sin_t + (int64_t)pos[r] * half;
+        for (int i = 0; i < half; ++i) {
+            int ia = interleaved ? 2 * i : i;
+            int ib = interleaved ? 2 * i + 1 : i + half;
+            float xa = (float)widen(xr[ia], elem), xb = (float)widen(xr[ib], elem);
+            float c = cr[i], s = sr[i];
+            float ya = fmaf(xa, c, -(xb * s));
+            float yb = fmaf(xa, s, xb * c);
+            orow[ia] = f32_to_bits(ya, elem);
+            orow[ib] = f32_to_bits(yb, elem);
+        }
+    }
+    return 0;
+}
+
+/* fp32 values -> 16-bit codes (round to nearest even), exposed for the pins. */
+int oracle_round16(const float *x, int64_t n, uint16_t *out, int elem) {
+    if (elem < 0 || elem > 1) return -1;
+    for (int64_t i = 0; i < n; ++i) out[i] = f32_to_bits(x[i], elem);
+    return 0;
+}

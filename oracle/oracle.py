@@ -69,8 +69,11 @@ def _load():
                                                i] + mod
             lib.oracle_row_probs.argtypes = [p, p, p, i, i, i, i, i, i, p, p, p, d, i, i, i, i,
                                              p, i] + mod
+            lib.oracle_rotary.argtypes = [p, i64, i64, i, p, p, p, i, i, p, i]
+            lib.oracle_round16.argtypes = [p, i64, p, i]
             for f in (lib.oracle_fwd, lib.oracle_fwd_rows, lib.oracle_fwd_varlen,
-                      lib.oracle_fwd_kvcache, lib.oracle_row_probs):
+                      lib.oracle_fwd_kvcache, lib.oracle_row_probs, lib.oracle_rotary,
+                      lib.oracle_round16):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -262,3 +265,115 @@ def row_probs(q, k, v, b: int, h: int, i: int, scale: float, causal: bool = Fals
     if rc != 0:
         raise ValueError("oracle_row_probs rejected its arguments")
     return p
+
+
+# --------------------------------------------------------------------------
+# KV-cache extras ("flash-attention", section 1: the decode call appends the new key and
+# value to the cache in place and applies rotary in the same step; capabilities table,
+# KV cache row: in-place append, paged KV).
+
+
+def round16(x, elem: int = 0) -> np.ndarray:
+    """fp32 values -> bf16 (elem 0) or fp16 (elem 1) bit patterns, round to nearest even."""
+    x = np.ascontiguousarray(np.asarray(x, np.float32))
+    out = np.zeros(x.shape, np.uint16)
+    if _load().oracle_round16(_ptr(x), x.size, _ptr(out), int(elem)) != 0:
+        raise ValueError("oracle_round16 rejected its arguments")
+    return out
+
+
+def rotary(x, positions, cos, sin, interleaved: bool = False, elem=None) -> np.ndarray:
+    """Rotary embedding of vectors x [..., d] (16-bit) at integer positions [...] with fp32
+    tables cos/sin [P, rotary_dim / 2]; returns uint16 bits of the same shape."""
+    el = _common_elem(x, elem=elem)
+    xb = _bits(x)
+    d = xb.shape[-1]
+    rows = xb.reshape(-1, d)
+    pos = np.ascontiguousarray(np.asarray(positions, np.int32).reshape(-1))
+    cos = np.ascontiguousarray(np.asarray(cos, np.float32))
+    sin = np.ascontiguousarray(np.asarray(sin, np.float32))
+    if pos.shape[0] != rows.shape[0] or cos.shape != sin.shape or cos.ndim != 2:
+        raise ValueError("rotary: one position per row and tables [P, rotary_dim / 2]")
+    if pos.size and (pos.min() < 0 or pos.max() >= cos.shape[0]):
+        raise ValueError("rotary: position outside the tables")
+    out = np.zeros(rows.shape, np.uint16)
+    rc = _load().oracle_rotary(_ptr(rows), d, rows.shape[0], d, _ptr(pos), _ptr(cos),
+                               _ptr(sin), 2 * cos.shape[1], int(bool(interleaved)),
+                               _ptr(out), el)
+    if rc != 0:
+        raise ValueError("oracle_rotary rejected its arguments")
+    return out.reshape(xb.shape)
+
+
+def kvcache_step(q, k_cache, v_cache, cache_seqlens, scale: float, k_new=None, v_new=None,
+                 rotary_cos=None, rotary_sin=None, rotary_interleaved: bool = False,
+                 block_table=None, nthreads: int | None = None, elem=None, window=(-1, -1),
+                 softcap=0.0, alibi_slopes=None):
+    """One decode step against a KV cache, the way the decode call reads it:
+
+    1. with k_new / v_new ([B, 1, Hkv, d]): the new key (rotated when tables are given)
+       and value are written at logical row cache_seqlens[b] of sequence b, and the query
+       is rotated at the same position;
+    2. the query attends to logical rows [0, cache_seqlens[b] (+ 1 after an append)).
+
+    Contiguous caches are [B, Lmax, Hkv, d]; paged ones (block_table [B, nblk] int32) are
+    [num_pages, page_size, Hkv, d], logical row r of sequence b being row r % page_size of
+    page block_table[b, r // page_size].
+
+    Returns (O [B, Hq, d] float64, LSE [B, Hq] float64, k_cache, v_cache) with the caches
+    after the append as uint16 bits in the caller's layout.
+    """
+    el = _common_elem(q, k_cache, v_cache, elem=elem)
+    qb, kc, vc = _bits(q).copy(), _bits(k_cache).copy(), _bits(v_cache).copy()
+    lens = np.asarray(cache_seqlens, np.int64).reshape(-1).copy()
+    B, _, Hq, d = qb.shape
+    Hkv = kc.shape[2]
+    bt = None if block_table is None else np.asarray(block_table, np.int64)
+    if bt is None:
+        Lmax = kc.shape[1]
+    else:
+        page = kc.shape[1]
+        Lmax = bt.shape[1] * page
+
+    def locate(b, r):
+        """(page or batch index, row) of logical row r of sequence b."""
+        if bt is None:
+            return b, r
+        pg = int(bt[b, r // page])
+        if pg < 0 or pg >= kc.shape[0]:
+            raise ValueError("block table entry outside the cache")
+        return pg, r % page
+
+    if (k_new is None) != (v_new is None):
+        raise ValueError("k_new and v_new go together")
+    if rotary_cos is not None and k_new is None:
+        raise ValueError("rotary applies to an appended key")
+    if np.any(lens < 0) or np.any(lens > Lmax):
+        raise ValueError("cache length outside [0, Lmax]")
+    if k_new is not None:
+        kn, vn = _bits(k_new).copy(), _bits(v_new).copy()
+        if np.any(lens + 1 > Lmax):
+            raise ValueError("no room for the appended row")
+        if rotary_cos is not None:
+            kn = rotary(kn, np.repeat(lens, Hkv).reshape(B, 1, Hkv), rotary_cos, rotary_sin,
+                        rotary_interleaved, elem=el)
+            qb = rotary(qb, np.repeat(lens, Hq).reshape(B, 1, Hq), rotary_cos, rotary_sin,
+                        rotary_interleaved, elem=el)
+        for b in range(B):
+            i0, r = locate(b, int(lens[b]))
+            kc[i0, r] = kn[b, 0]
+            vc[i0, r] = vn[b, 0]
+        lens = lens + 1
+    if bt is None:
+        kl, vl = kc, vc
+    else:
+        kl = np.full((B, Lmax, Hkv, d), 0x7fc0, np.uint16)  # NaN in both 16-bit types
+        vl = kl.copy()
+        for b in range(B):
+            for r in range(int(lens[b])):
+                i0, rr = locate(b, r)
+                kl[b, r] = kc[i0, rr]
+                vl[b, r] = vc[i0, rr]
+    o, lse = attention_kvcache(qb, kl, vl, lens.astype(np.int32), scale, nthreads, el,
+                               window=window, softcap=softcap, alibi_slopes=alibi_slopes)
+    return o, lse, kc, vc

@@ -649,8 +649,154 @@ def pin_mod_paths(O):
             _close(lse[:, a:e], lb[0], 0.0, f"varlen mod seq {b} LSE")
 
 
+# --------------------------------------------------------------------------
+# KV-cache extras: rounding to the cache type, rotary embedding, in-place append, paged
+# caches ("flash-attention", section 1 and capabilities table, KV cache row).  Readings:
+# the new key and value of a decode step go to logical row cache_seqlens[b]; rotary turns
+# dimension pairs (i, i + r/2) (or (2i, 2i+1) interleaved) of q and the new key by the
+# table angle of that same position; results are rounded once to the element type.
+
+def _spacing(x, dtype):
+    """One ulp of the 16-bit type at |x| (normal range)."""
+    bits = 8 if dtype == torch.bfloat16 else 11
+    ax = np.abs(x)
+    return np.exp2(np.floor(np.log2(np.where(ax > 0, ax, 1.0))) - (bits - 1))
+
+
+def _to64(bits, dtype):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(dtype).double().numpy()
+
+
+def _rope_tables(P, half):
+    inv = 10000.0 ** (-np.arange(half) / half)
+    ang = np.arange(P)[:, None] * inv[None, :]
+    return np.cos(ang).astype(np.float32), np.sin(ang).astype(np.float32)
+
+
+def pin_round16_library(O):
+    """fp32 -> bf16 / fp16 rounding equals torch's conversion (round to nearest even),
+    including ties, subnormals and overflow to inf."""
+    rng = np.random.default_rng(5)
+    x = (rng.normal(size=50000) * 10.0 ** rng.integers(-9, 6, size=50000)).astype(np.float32)
+    special = np.array([65504, 65519.99, 65520, 2.0 ** -24, 2.0 ** -25, 3 * 2.0 ** -26,
+                        2.0 ** -14, -0.0, 1e30, np.inf, -np.inf, 1 + 2.0 ** -8,
+                        1 + 3 * 2.0 ** -8, 1 + 2.0 ** -11, 1 + 3 * 2.0 ** -11], np.float32)
+    x = np.concatenate([x, special])
+    for elem, dt in ((0, torch.bfloat16), (1, torch.float16)):
+        ref = torch.from_numpy(x).to(dt).view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(O.round16(x, elem), ref), f"round16 elem {elem} vs torch"
+
+
+def pin_rotary(O):
+    """Rotary: angle 0 is the identity and a quarter turn maps (x_a, x_b) to (-x_b, x_a)
+    exactly; random angles agree with the rotation evaluated in float64 to one ulp of the
+    element type (fixes the sign, the pairing and the table row); interleaved pairs equal
+    half-split pairs after the matching permutation of dimensions; dimensions past
+    rotary_dim are copied."""
+    rd, half, d = 48, 24, 64
+    cos, sin = _rope_tables(128, half)
+    for elem, dt in ((0, torch.bfloat16), (1, torch.float16)):
+        x = bf16_normal((6, 4, d), seed=300 + elem, dtype=dt)
+        xb = x.view(torch.int16).numpy().view(np.uint16)
+        x64 = x.double().numpy()
+        pos = np.repeat(np.array([0, 1, 5, 17, 100, 3], np.int32)[:, None], 4, axis=1)
+        y = O.rotary(x, pos, cos, sin)
+        assert np.array_equal(y[0], xb[0]), "position 0 is not the identity"
+        assert np.array_equal(y[..., rd:], xb[..., rd:]), "dimensions past rotary_dim changed"
+        cq, sq = np.zeros((1, half), np.float32), np.ones((1, half), np.float32)
+        yq = _to64(O.rotary(x, np.zeros((6, 4), np.int32), cq, sq), dt)
+        assert np.array_equal(yq[..., :half], -x64[..., half:rd]), "quarter turn, first half"
+        assert np.array_equal(yq[..., half:rd], x64[..., :half]), "quarter turn, second half"
+        c, s_ = cos[pos].astype(np.float64), sin[pos].astype(np.float64)
+        xa, xc = x64[..., :half], x64[..., half:rd]
+        exact = np.concatenate([xa * c - xc * s_, xa * s_ + xc * c], axis=-1)
+        got = _to64(y, dt)[..., :rd]
+        assert np.all(np.abs(got - exact) <= _spacing(exact, dt)), "rotation vs float64"
+        perm = np.concatenate([np.arange(0, rd, 2), np.arange(1, rd, 2), np.arange(rd, d)])
+        xi = x[..., torch.from_numpy(np.argsort(perm))].contiguous()  # interleaved layout
+        yi = O.rotary(xi, pos, cos, sin, interleaved=True)
+        assert np.array_equal(yi[..., perm], y), "interleaved vs half-split pairs"
+
+
+def _kv_case(seed, B=3, Lmax=40, Hq=4, Hkv=2, d=16):
+    q = bf16_normal((B, 1, Hq, d), seed=seed)
+    kc = bf16_normal((B, Lmax, Hkv, d), seed=seed + 1)
+    vc = bf16_normal((B, Lmax, Hkv, d), seed=seed + 2)
+    kn = bf16_normal((B, 1, Hkv, d), seed=seed + 3)
+    vn = bf16_normal((B, 1, Hkv, d), seed=seed + 4)
+    return q, kc, vc, kn, vn
+
+
+def pin_kv_append(O):
+    """Append: the caches change only at row cache_seqlens[b], which holds the new key and
+    value; the query then sees that row (decode over length + 1).  Rotary turns the new key
+    and the query by the angle of position cache_seqlens[b]: with tables that turn only
+    that row by a quarter, both come out as exact quarter turns."""
+    q, kc, vc, kn, vn = _kv_case(310)
+    lens = [0, 17, 39]
+    o, lse, kc2, vc2 = O.kvcache_step(q, kc, vc, lens, 0.25, k_new=kn, v_new=vn)
+    ke, ve = kc.clone(), vc.clone()
+    for b, n in enumerate(lens):
+        ke[b, n], ve[b, n] = kn[b, 0], vn[b, 0]
+    bits = lambda t: t.view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(kc2, bits(ke)) and np.array_equal(vc2, bits(ve)), "appended caches"
+    o_ref, l_ref = O.attention_kvcache(q, ke, ve, [n + 1 for n in lens], 0.25)
+    _close(o, o_ref, 0.0, "append O")
+    _close(lse, l_ref, 0.0, "append LSE")
+    half = 8
+    cos, sin = np.ones((64, half), np.float32), np.zeros((64, half), np.float32)
+    for n in lens:
+        cos[n], sin[n] = 0.0, 1.0
+    o, lse, kc3, _ = O.kvcache_step(q, kc, vc, lens, 0.25, k_new=kn, v_new=vn, rotary_cos=cos,
+                                    rotary_sin=sin)
+    quarter = lambda t: torch.cat([-t[..., half:], t[..., :half]], dim=-1)
+    kq = ke.clone()
+    for b, n in enumerate(lens):
+        kq[b, n] = quarter(kn[b, 0])
+    assert np.array_equal(kc3, bits(kq)), "rotated key not a quarter turn at its position"
+    o_ref, l_ref = O.attention_kvcache(quarter(q).contiguous(), kq, ve, [n + 1 for n in lens],
+                                       0.25)
+    _close(o, o_ref, 0.0, "rotary append O")
+    _close(lse, l_ref, 0.0, "rotary append LSE")
+
+
+def pin_kv_paged(O):
+    """A paged cache (pages of 8 rows in a shuffled pool, block table per sequence) gives
+    the same step as the contiguous cache it holds, before and after an append, with the
+    score modifiers too; the appended row lands in the page the table names."""
+    q, kc, vc, kn, vn = _kv_case(320)
+    B, Lmax, Hkv, d = kc.shape
+    P, nblk = 8, Lmax // 8
+    rng = np.random.default_rng(321)
+    order = rng.permutation(B * nblk + 3)[:B * nblk].reshape(B, nblk).astype(np.int32)
+    kp = torch.full((B * nblk + 3, P, Hkv, d), float("nan"), dtype=torch.bfloat16)
+    vp = kp.clone()
+    for b in range(B):
+        for j in range(nblk):
+            kp[order[b, j]] = kc[b, j * P:(j + 1) * P]
+            vp[order[b, j]] = vc[b, j * P:(j + 1) * P]
+    lens = [0, 23, 39]
+    cos, sin = _rope_tables(64, 8)
+    for kw in [dict(), dict(window=(9, -1), softcap=3.0)]:
+        o1, l1, k1, v1 = O.kvcache_step(q, kc, vc, lens, 0.3, k_new=kn, v_new=vn,
+                                        rotary_cos=cos, rotary_sin=sin, **kw)
+        o2, l2, k2, v2 = O.kvcache_step(q, kp, vp, lens, 0.3, k_new=kn, v_new=vn,
+                                        rotary_cos=cos, rotary_sin=sin, block_table=order, **kw)
+        _close(o2, o1, 0.0, "paged O")
+        _close(l2, l1, 0.0, "paged LSE")
+        for b in range(B):
+            for j in range(nblk):
+                assert np.array_equal(k2[order[b, j]], k1[b, j * P:(j + 1) * P]), "paged keys"
+                assert np.array_equal(v2[order[b, j]], v1[b, j * P:(j + 1) * P]), "paged values"
+        o3, l3, _, _ = O.kvcache_step(q, kp, vp, lens, 0.3, block_table=order, **kw)
+        o4, l4 = O.attention_kvcache(q, kc, vc, lens, 0.3, **kw)
+        _close(o3, o4, 0.0, "paged without append O")
+        _close(l3, l4, 0.0, "paged without append LSE")
+
+
 ALL_PINS = [pin_library, pin_library_fp16, pin_fp16_values, pin_uniform_scores, pin_single_key, pin_constant_v, pin_two_keys,
             pin_empty_rows, pin_hard_max, pin_probs, pin_shift, pin_permutation, pin_gqa,
             pin_varlen, pin_kvcache, pin_rows, pin_recurrence, pin_lse_recompute,
             pin_window_uniform, pin_window_diagonal, pin_window_library, pin_softcap_limits,
-            pin_alibi_geometric, pin_alibi_library, pin_mod_bruteforce, pin_mod_paths]
+            pin_alibi_geometric, pin_alibi_library, pin_mod_bruteforce, pin_mod_paths,
+            pin_round16_library, pin_rotary, pin_kv_append, pin_kv_paged]

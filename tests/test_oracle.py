@@ -63,30 +63,53 @@ MUTATIONS = [
     ("ALiBi slope per kv head", "mod.slope = J->alibi ? J->alibi[b * J->alibi_sb + h] : 0.0;",
      "mod.slope = J->alibi ? J->alibi[b * J->alibi_sb + g] : 0.0;"),
     ("decode query at the cache start", "pos = nk - 1;", "pos = 0;"),
+    ("rotary sine sign flipped", "float ya = fmaf(xa, c, -(xb * s));",
+     "float ya = fmaf(xa, c, xb * s);"),
+    ("rotary pairs swapped between layouts", "int ia = interleaved ? 2 * i : i;",
+     "int ia = interleaved ? i : 2 * i;"),
+    ("rotary table row not scaled by the pair count",
+     "const float *cr = cos_t + (int64_t)pos[r] * half;",
+     "const float *cr = cos_t + (int64_t)pos[r];"),
+    ("bf16 rounding truncates", "u += 0x7fffu + lsb;", "u += 0u * lsb;"),
+    ("fp16 rounding ties away from zero",
+     "if (rem > half || (rem == half && (q & 1u))) q += 1u;", "if (rem >= half) q += 1u;"),
+    ("appended row one past the length", "i0, r = locate(b, int(lens[b]))",
+     "i0, r = locate(b, int(lens[b]) + 1)", "py"),
+    ("rotary at the next position", "kn = rotary(kn, np.repeat(lens, Hkv)",
+     "kn = rotary(kn, np.repeat(lens + 1, Hkv)", "py"),
+    ("query not rotated", "qb = rotary(qb, np.repeat(lens, Hq)",
+     "qb = qb if True else rotary(qb, np.repeat(lens, Hq)", "py"),
+    ("paged row taken from the page number", "return pg, r % page", "return pg, r // page", "py"),
 ]
 
 
-def _mutated_oracle(tmp_path, old, new):
-    src = open(os.path.join(ROOT, "oracle", "attn_oracle.c")).read()
-    assert src.count(old) == 1, f"mutation anchor not unique: {old!r}"
+def _mutated_oracle(tmp_path, old, new, where="c"):
+    """A copy of the oracle with `old` replaced by `new` in attn_oracle.c (where="c") or
+    oracle.py (where="py"), built in tmp_path."""
+    files = {"c": "attn_oracle.c", "py": "oracle.py"}
     d = tmp_path / "mut"
     d.mkdir()
-    (d / "attn_oracle.c").write_text(src.replace(old, new))
-    shutil.copy(os.path.join(ROOT, "oracle", "oracle.py"), d / "oracle.py")
+    for key, name in files.items():
+        src = open(os.path.join(ROOT, "oracle", name)).read()
+        if key == where:
+            assert src.count(old) == 1, f"mutation anchor not unique: {old!r}"
+            src = src.replace(old, new)
+        (d / name).write_text(src)
     spec = importlib.util.spec_from_file_location("oracle_mutant", str(d / "oracle.py"))
     mod = importlib.util.module_from_spec(spec)
     spec.loader.exec_module(mod)
     return mod
 
 
-@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
-def test_pins_catch_planted_slip(tmp_path, name, old, new):
-    mod = _mutated_oracle(tmp_path, old, new)
+@pytest.mark.parametrize("mutation", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_pins_catch_planted_slip(tmp_path, mutation):
+    name, old, new = mutation[:3]
+    mod = _mutated_oracle(tmp_path, old, new, *mutation[3:])
     caught = []
     for pin in P.ALL_PINS:
         try:
             pin(mod)
-        except (AssertionError, ValueError, FloatingPointError):
+        except (AssertionError, ValueError, FloatingPointError, IndexError):
             caught.append(pin.__name__)
     assert caught, f"no pin fails when the oracle has the slip: {name}"
 
