@@ -498,6 +498,31 @@ def extra_workloads(args, dev, pk, world, dist):
     res["decode_window4096"] = {"ms": round(ms, 4), "GB/s": round(gbs, 1),
                                 "algorithmic_bytes": kv_bytes + io_bytes,
                                 "frac_of_hbm": round(gbs / pk["hbm"], 4)}
+    # the decode workload as a paged cache (pages of 256 rows in shuffled order over the same
+    # memory), one appended token per sequence with rotary on the query and the new key
+    page = 256
+    nblk = w.Nk // page
+    perm = torch.randperm(w.B * nblk, generator=torch.Generator().manual_seed(7))
+    table = perm.reshape(w.B, nblk).to(torch.int32).to(dev)
+    kp = kc.view(w.B * nblk, page, w.Hkv, w.d)
+    vp = vc.view(w.B * nblk, page, w.Hkv, w.d)
+    lens_a = lens.clamp(max=w.Nk - 1)
+    kn = torch.randn((w.B, 1, w.Hkv, w.d), device=dev).to(torch.bfloat16)
+    vn = torch.randn((w.B, 1, w.Hkv, w.d), device=dev).to(torch.bfloat16)
+    ang = torch.arange(w.Nk, device=dev, dtype=torch.float64)[:, None] * \
+        10000.0 ** (-torch.arange(w.d // 2, device=dev, dtype=torch.float64) / (w.d // 2))
+    cos, sin = ang.cos().float().contiguous(), ang.sin().float().contiguous()
+    ms = time_calls(lambda: fa.fa_fwd_kvcache(q, kp, vp, lens_a, workspace=ws, out=o, lse=l,
+                                              k_new=kn, v_new=vn, rotary_cos=cos,
+                                              rotary_sin=sin, block_table=table),
+                    max(20, args.steps // 2), stream)
+    kv_bytes = int((lens_a.long() + 1).sum().item()) * w.Hkv * w.d * 2 * 2
+    new_bytes = 2 * kn.numel() * 2 * 2  # new rows read and written
+    gbs = (kv_bytes + io_bytes + new_bytes) / (ms * 1e-3) / 1e9
+    res["decode_paged_append_rotary"] = {"ms": round(ms, 4), "GB/s": round(gbs, 1),
+                                         "algorithmic_bytes": kv_bytes + io_bytes + new_bytes,
+                                         "frac_of_hbm": round(gbs / pk["hbm"], 4),
+                                         "gpu_launches_per_call": 3}
     st = fa.get_last_device_error()
     if st != fa.FA_OK:
         raise RuntimeError(f"device error in extra workloads: {fa.status_string(st)}")

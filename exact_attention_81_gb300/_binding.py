@@ -54,6 +54,25 @@ class ScoreMod(ctypes.Structure):
     ]
 
 
+class KvCacheExtras(ctypes.Structure):
+    """Mirror of fa_kvcache_extras (in-place append, rotary, paged cache)."""
+
+    _fields_ = [
+        ("k_new", ctypes.c_void_p),
+        ("v_new", ctypes.c_void_p),
+        ("new_strides", ctypes.c_int64 * 3),
+        ("rotary_cos", ctypes.c_void_p),
+        ("rotary_sin", ctypes.c_void_p),
+        ("rotary_dim", ctypes.c_int),
+        ("rotary_positions", ctypes.c_int),
+        ("rotary_interleaved", ctypes.c_int),
+        ("block_table", ctypes.c_void_p),
+        ("block_table_stride", ctypes.c_int),
+        ("page_size", ctypes.c_int),
+        ("num_pages", ctypes.c_int),
+    ]
+
+
 class FwdParams(ctypes.Structure):
     """Mirror of fa_fwd_params."""
 
@@ -106,7 +125,8 @@ def load_library(path: str | None = None):
         lib.fa_fwd_kvcache_workspace_size.argtypes = [i, i, i, i, i]
         lib.fa_fwd_kvcache_workspace_size.restype = sz
         lib.fa_fwd_kvcache.argtypes = [vp, vp, vp, vp, i, i, i, i, i, ctypes.POINTER(i64), f, i,
-                                       vp, sz, vp, vp, i, pmod, vp]
+                                       vp, sz, vp, vp, i, pmod, ctypes.POINTER(KvCacheExtras),
+                                       vp]
         lib.fa_fwd_kvcache.restype = i
         lib.fa_get_last_device_error.argtypes = [vp]
         lib.fa_get_last_device_error.restype = i
@@ -267,12 +287,56 @@ def fa_fwd_kvcache_workspace_size(B: int, Hq: int, Lmax: int, d: int, num_splits
     return int(load_library().fa_fwd_kvcache_workspace_size(B, Hq, Lmax, d, num_splits))
 
 
+def _kv_extras(q, k_cache, B, Hkv, d, k_new, v_new, rotary_cos, rotary_sin,
+               rotary_interleaved, block_table):
+    """fa_kvcache_extras from the Python arguments, or None when none is used."""
+    if k_new is None and v_new is None and rotary_cos is None and block_table is None:
+        return None
+    ex = KvCacheExtras()
+    if (k_new is None) != (v_new is None):
+        raise ValueError("k_new and v_new go together")
+    if k_new is not None:
+        for name, t in (("k_new", k_new), ("v_new", v_new)):
+            _require_bf16_cuda(name, t, 4, q.dtype)
+            if tuple(t.shape) != (B, 1, Hkv, d):
+                raise ValueError(f"{name} must be [B, 1, Hkv, d]")
+        if k_new.stride() != v_new.stride():
+            raise ValueError("k_new and v_new must share strides")
+        ex.k_new, ex.v_new = k_new.data_ptr(), v_new.data_ptr()
+        ex.new_strides[:] = list(k_new.stride()[:3])
+    if (rotary_cos is None) != (rotary_sin is None):
+        raise ValueError("rotary_cos and rotary_sin go together")
+    if rotary_cos is not None:
+        for name, t in (("rotary_cos", rotary_cos), ("rotary_sin", rotary_sin)):
+            if t.dtype != torch.float32 or not t.is_cuda or t.dim() != 2 or not t.is_contiguous():
+                raise TypeError(f"{name} must be a contiguous fp32 CUDA tensor [P, rotary_dim/2]")
+        if rotary_cos.shape != rotary_sin.shape:
+            raise ValueError("rotary_cos and rotary_sin must have the same shape")
+        ex.rotary_cos, ex.rotary_sin = rotary_cos.data_ptr(), rotary_sin.data_ptr()
+        ex.rotary_positions, ex.rotary_dim = rotary_cos.shape[0], 2 * rotary_cos.shape[1]
+        ex.rotary_interleaved = int(bool(rotary_interleaved))
+    if block_table is not None:
+        if block_table.dtype != torch.int32 or not block_table.is_cuda or block_table.dim() != 2 \
+                or block_table.stride(1) != 1 or block_table.shape[0] != B:
+            raise TypeError("block_table must be an int32 CUDA tensor [B, blocks_per_seq]")
+        ex.block_table = block_table.data_ptr()
+        ex.block_table_stride = block_table.stride(0)
+        ex.page_size = k_cache.shape[1]
+        ex.num_pages = k_cache.shape[0]
+    return ex
+
+
 def fa_fwd_kvcache(q, k_cache, v_cache, cache_seqlens, scale: float | None = None,
                    num_splits: int = 0, workspace=None, out=None, lse=None, stream=None,
-                   window_size=None, softcap: float = 0.0, alibi_slopes=None):
-    """Single-query decode.  q [B,1,Hq,d], caches [B,Lmax,Hkv,d], cache_seqlens int32 [B].
+                   window_size=None, softcap: float = 0.0, alibi_slopes=None, k_new=None,
+                   v_new=None, rotary_cos=None, rotary_sin=None, rotary_interleaved=False,
+                   block_table=None):
+    """Single-query decode.  q [B,1,Hq,d], caches [B,Lmax,Hkv,d] (paged: [num_pages,
+    page_size, Hkv, d] with block_table int32 [B, blocks_per_seq]), cache_seqlens int32 [B].
 
-    Returns (out [B,1,Hq,d] bf16, lse [B,Hq] fp32).
+    k_new / v_new [B,1,Hkv,d] are appended in place at row cache_seqlens[b] first (the
+    caches are modified); rotary_cos / rotary_sin fp32 [P, rotary_dim/2] turn the query and
+    the new key at that position.  Returns (out [B,1,Hq,d], lse [B,Hq] fp32).
     """
     _require_bf16_cuda("q", q, 4)
     _require_bf16_cuda("k_cache", k_cache, 4, q.dtype)
@@ -284,7 +348,10 @@ def fa_fwd_kvcache(q, k_cache, v_cache, cache_seqlens, scale: float | None = Non
     if not q.is_contiguous():
         raise ValueError("q must be contiguous")
     B, _, Hq, d = q.shape
-    Lmax, Hkv = k_cache.shape[1], k_cache.shape[2]
+    Hkv = k_cache.shape[2]
+    Lmax = k_cache.shape[1] if block_table is None else block_table.shape[1] * k_cache.shape[1]
+    ex = _kv_extras(q, k_cache, B, Hkv, d, k_new, v_new, rotary_cos, rotary_sin,
+                    rotary_interleaved, block_table)
     if out is None:
         out = torch.empty((B, 1, Hq, d), dtype=q.dtype, device=q.device)
     if lse is None:
@@ -298,7 +365,9 @@ def fa_fwd_kvcache(q, k_cache, v_cache, cache_seqlens, scale: float | None = Non
     st = load_library().fa_fwd_kvcache(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cache_seqlens),
                                        B, Lmax, Hq, Hkv, d, strides, sc, int(num_splits),
                                        _ptr(workspace), workspace.numel(), _ptr(out), _ptr(lse),
-                                       _DTYPE[q.dtype], ctypes.byref(mod), _stream_handle(stream))
+                                       _DTYPE[q.dtype], ctypes.byref(mod),
+                                       None if ex is None else ctypes.byref(ex),
+                                       _stream_handle(stream))
     _check(st, "fa_fwd_kvcache")
     return out, lse
 
@@ -335,12 +404,16 @@ def flash_attn_varlen_func(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, ma
     return (o, lse) if return_lse else o
 
 
-def flash_attn_with_kvcache(q, k_cache, v_cache, cache_seqlens, softmax_scale=None,
-                            causal=True, window_size=(-1, -1), softcap=0.0, alibi_slopes=None,
-                            num_splits=0, return_lse=False):
+def flash_attn_with_kvcache(q, k_cache, v_cache, k=None, v=None, rotary_cos=None,
+                            rotary_sin=None, cache_seqlens=None, block_table=None,
+                            softmax_scale=None, causal=True, window_size=(-1, -1), softcap=0.0,
+                            rotary_interleaved=False, alibi_slopes=None, num_splits=0,
+                            return_lse=False):
     # With one query per sequence, bottom-right causal alignment lets it see the whole
     # visible prefix, so `causal` does not change the result.
     o, lse = fa_fwd_kvcache(q, k_cache, v_cache, cache_seqlens, scale=softmax_scale,
                             num_splits=num_splits, window_size=window_size, softcap=softcap,
-                            alibi_slopes=alibi_slopes)
+                            alibi_slopes=alibi_slopes, k_new=k, v_new=v, rotary_cos=rotary_cos,
+                            rotary_sin=rotary_sin, rotary_interleaved=rotary_interleaved,
+                            block_table=block_table)
     return (o, lse) if return_lse else o

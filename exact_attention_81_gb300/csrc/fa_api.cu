@@ -405,7 +405,8 @@ fa_status fa_fwd_kvcache(const void *q, const void *k_cache, const void *v_cache
                          const int *cache_seqlens, int B, int Lmax, int Hq, int Hkv, int d,
                          const int64_t cache_strides[3], float scale, int num_splits,
                          void *workspace, size_t workspace_bytes, void *o, float *lse,
-                         int dtype, const fa_score_mod *mod_in, cudaStream_t stream) {
+                         int dtype, const fa_score_mod *mod_in, const fa_kvcache_extras *ex,
+                         cudaStream_t stream) {
   if (B < 0 || Lmax < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || num_splits < 0)
     return FA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
@@ -424,11 +425,36 @@ fa_status fa_fwd_kvcache(const void *q, const void *k_cache, const void *v_cache
   ModPlan mod;
   fa_status st = plan_mod(mod_in, 0, &mod);  // the right bound never hides a cached key
   if (st != FA_OK) return st;
+  const bool append = ex != nullptr && (ex->k_new != nullptr || ex->v_new != nullptr);
+  const bool rotary = ex != nullptr && (ex->rotary_cos != nullptr || ex->rotary_sin != nullptr);
+  const bool paged = ex != nullptr && ex->block_table != nullptr;
+  if (append) {
+    if (ex->k_new == nullptr || ex->v_new == nullptr || Lmax == 0) return FA_ERR_INVALID_ARG;
+    if (!aligned(ex->k_new, 2) || !aligned(ex->v_new, 2)) return FA_ERR_INVALID_ARG;
+    if (ex->new_strides[0] < 0 || ex->new_strides[2] < 0) return FA_ERR_INVALID_ARG;
+  }
+  if (rotary) {
+    if (!append || ex->rotary_cos == nullptr || ex->rotary_sin == nullptr)
+      return FA_ERR_INVALID_ARG;
+    if (ex->rotary_dim < 2 || ex->rotary_dim > d || (ex->rotary_dim & 1) ||
+        ex->rotary_positions < 1 || !aligned(ex->rotary_cos, 4) || !aligned(ex->rotary_sin, 4))
+      return FA_ERR_INVALID_ARG;
+    if (o == q) return FA_ERR_INVALID_ARG;  // the rotated query is staged in o
+  }
+  int num_rows = Lmax, num_outer = B;  // extents of the cache tensors: (row, batch or page)
+  if (paged) {
+    if (ex->page_size <= 0 || ex->page_size % 128 != 0 || ex->num_pages < 1 ||
+        !aligned(ex->block_table, 4) ||
+        static_cast<int64_t>(ex->block_table_stride) * ex->page_size < Lmax)
+      return FA_ERR_INVALID_ARG;
+    num_rows = ex->page_size;
+    num_outer = ex->num_pages;
+  }
   if (Lmax > 0) {
     if (k_cache == nullptr || v_cache == nullptr || cache_strides == nullptr)
       return FA_ERR_INVALID_ARG;
     if (!aligned(k_cache, 16) || !aligned(v_cache, 16)) return FA_ERR_INVALID_ARG;
-    if (!stride_ok(cache_strides[0], B) || !stride_ok(cache_strides[1], Lmax) ||
+    if (!stride_ok(cache_strides[0], num_outer) || !stride_ok(cache_strides[1], num_rows) ||
         !stride_ok(cache_strides[2], Hkv))
       return FA_ERR_INVALID_ARG;
     const size_t need = fa_fwd_kvcache_workspace_size(B, Hq, Lmax, d, num_splits);
@@ -443,7 +469,10 @@ fa_status fa_fwd_kvcache(const void *q, const void *k_cache, const void *v_cache
     chunk = decode_chunk(Lmax, num_splits);
     maxch = ceil_div(Lmax, chunk);  // the workspace holds this many chunks per (b, h)
     // A window limits every sequence to its last wl + 1 keys: the chunks split that range.
-    const int Leff = mod.wl >= 0 ? std::min(Lmax, mod.wl + 1) : Lmax;
+    // (with page-aligned unit starts the range may begin up to 127 keys earlier)
+    const int kalign = paged ? 128 : 1;
+    const int Leff = mod.wl >= 0 ? std::min<int64_t>(Lmax, static_cast<int64_t>(mod.wl) + kalign)
+                                 : Lmax;
     if (num_splits == 0)
       chunk = auto_chunk(Leff, static_cast<int64_t>(B) * Hkv, dev->sm_count, maxch);
     maxch = ceil_div(Leff, chunk);
@@ -454,14 +483,46 @@ fa_status fa_fwd_kvcache(const void *q, const void *k_cache, const void *v_cache
   if (units > INT32_MAX) return FA_ERR_INVALID_ARG;
   if (Lmax > 0) {
     CUtensorMap tk, tv;
-    if ((st = make_map(&tk, k_cache, d, Lmax, Hkv, B, cache_strides[1], cache_strides[2],
-                       cache_strides[0], dtype)) != FA_OK)
+    if ((st = make_map(&tk, k_cache, d, num_rows, Hkv, num_outer, cache_strides[1],
+                       cache_strides[2], cache_strides[0], dtype)) != FA_OK)
       return st;
-    if ((st = make_map(&tv, v_cache, d, Lmax, Hkv, B, cache_strides[1], cache_strides[2],
-                       cache_strides[0], dtype)) != FA_OK)
+    if ((st = make_map(&tv, v_cache, d, num_rows, Hkv, num_outer, cache_strides[1],
+                       cache_strides[2], cache_strides[0], dtype)) != FA_OK)
       return st;
+    if (append) {
+      fa::AppendArgs ap{};
+      ap.k_new = ex->k_new;
+      ap.v_new = ex->v_new;
+      ap.n_sb = ex->new_strides[0];
+      ap.n_sh = ex->new_strides[2];
+      ap.k_cache = const_cast<void *>(k_cache);
+      ap.v_cache = const_cast<void *>(v_cache);
+      ap.c_s0 = cache_strides[0];
+      ap.c_s1 = cache_strides[1];
+      ap.c_s2 = cache_strides[2];
+      ap.cache_len = cache_seqlens;
+      ap.B = B;
+      ap.Hq = Hq;
+      ap.Hkv = Hkv;
+      ap.d = d;
+      ap.Lmax = Lmax;
+      ap.block_table = paged ? ex->block_table : nullptr;
+      ap.bt_stride = paged ? ex->block_table_stride : 0;
+      ap.page_size = paged ? ex->page_size : 1;
+      ap.num_pages = paged ? ex->num_pages : 0;
+      ap.cos = rotary ? ex->rotary_cos : nullptr;
+      ap.sin = rotary ? ex->rotary_sin : nullptr;
+      ap.rot_dim = rotary ? ex->rotary_dim : 0;
+      ap.rot_positions = rotary ? ex->rotary_positions : 0;
+      ap.rot_interleaved = rotary ? ex->rotary_interleaved != 0 : 0;
+      ap.q = q;
+      ap.q_rot = rotary ? o : nullptr;
+      ap.err = dev->err;
+      cudaError_t e = fa::launch_append(dtype == FA_FP16, ap, stream);
+      if (e != cudaSuccess) return cuda_fail("append kernel launch", e);
+    }
     fa::DecodeArgs da{};
-    da.q = q;
+    da.q = rotary ? o : q;
     da.cache_len = cache_seqlens;
     da.o_part = o_part;
     da.lse_part = lse_part;
@@ -483,12 +544,19 @@ fa_status fa_fwd_kvcache(const void *q, const void *k_cache, const void *v_cache
     da.sc_out = mod.softcap > 0.f ? static_cast<float>(mod.softcap * 1.4426950408889634) : 0.f;
     da.alibi = mod.alibi;
     da.alibi_sb = mod.alibi_sb;
+    da.len_add = append ? 1 : 0;
+    da.block_table = paged ? ex->block_table : nullptr;
+    da.bt_stride = paged ? ex->block_table_stride : 0;
+    da.page_size = paged ? ex->page_size : 1;
+    da.num_pages = paged ? ex->num_pages : 0;
+    da.kalign = paged ? 128 : 1;
     const int grid = static_cast<int>(units < dev->sm_count ? units : dev->sm_count);
     cudaError_t e = fa::launch_decode(d, group, dtype == FA_FP16, tk, tv, da, grid, stream);
     if (e != cudaSuccess) return cuda_fail("decode kernel launch", e);
   }
-  cudaError_t e = fa::launch_combine(d, dtype == FA_FP16, o_part, lse_part, cache_seqlens, B, Hq,
-                                     Lmax, chunk, maxch, mod.wl, o, lse, dev->err, stream);
+  cudaError_t e = fa::launch_combine(d, dtype == FA_FP16, o_part, lse_part, cache_seqlens,
+                                     append ? 1 : 0, B, Hq, Lmax, chunk, maxch, mod.wl,
+                                     paged ? 128 : 1, o, lse, dev->err, stream);
   return e == cudaSuccess ? FA_OK : cuda_fail("combine kernel launch", e);
 }
 
@@ -505,7 +573,9 @@ fa_status fa_get_last_device_error(cudaStream_t stream) {
   e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero);
   if (e != cudaSuccess) return cuda_fail("cudaMemcpyToSymbol", e);
   if (word & (fa::DEVERR_PREFILL_TIMEOUT | fa::DEVERR_DECODE_TIMEOUT)) return FA_ERR_TIMEOUT;
-  if (word & (fa::DEVERR_BAD_CU_SEQLENS | fa::DEVERR_BAD_CACHE_LEN)) return FA_ERR_INVALID_ARG;
+  if (word & (fa::DEVERR_BAD_CU_SEQLENS | fa::DEVERR_BAD_CACHE_LEN | fa::DEVERR_BAD_APPEND |
+              fa::DEVERR_BAD_BLOCK_TABLE))
+    return FA_ERR_INVALID_ARG;
   return FA_OK;
 }
 

@@ -98,8 +98,9 @@ __device__ __forceinline__ int first_visible(int len, int wl) {
   return wl >= 0 ? max(len - 1 - wl, 0) : 0;
 }
 
-// Unit u = (chunk c, batch b, kv head g).  Chunks tile the visible keys [first, len) from
-// the first visible key on, so a window only moves the start.
+// Unit u = (chunk c, batch b, kv head g).  Chunks tile the keys [first, len) from the
+// first visible key on (rounded down to a page-safe multiple of 128 for paged caches), so
+// a window only moves the start.  len counts an appended row.
 __device__ __forceinline__ Unit unit_of(const DecodeArgs &a, int u) {
   Unit w;
   const int bg = a.B * a.Hkv;
@@ -107,9 +108,9 @@ __device__ __forceinline__ Unit unit_of(const DecodeArgs &a, int u) {
   const int r = u - w.c * bg;
   w.b = r / a.Hkv;
   w.g = r - w.b * a.Hkv;
-  const int len_raw = a.cache_len[w.b];
+  const int len_raw = a.cache_len[w.b] + a.len_add;
   w.len = min(max(len_raw, 0), a.Lmax);
-  w.key0 = first_visible(w.len, a.wl) + w.c * a.chunk;
+  w.key0 = decode_first_key(w.len, a.wl, a.kalign) + w.c * a.chunk;
   w.nkeys = min(a.chunk, w.len - w.key0);  // <= 0: nothing to do
   return w;
 }
@@ -123,7 +124,7 @@ __device__ void producer(const DecodeArgs &a, const CUtensorMap *tmk, const CUte
   for (int u = blockIdx.x; u < a.num_units; u += gridDim.x) {
     const Unit w = unit_of(a, u);
     if (w.c == 0 && w.g == 0) {
-      const int len_raw = a.cache_len[w.b];
+      const int len_raw = a.cache_len[w.b] + a.len_add;
       if (len_raw < 0 || len_raw > a.Lmax) atomicOr(a.err, DEVERR_BAD_CACHE_LEN);
     }
     if (w.nkeys <= 0) continue;
@@ -135,11 +136,20 @@ __device__ void producer(const DecodeArgs &a, const CUtensorMap *tmk, const CUte
         const uint32_t use = it / C::NSLOTS;
         if (!mbar_wait(&bars->empty[slot], (use & 1u) ^ 1u, wc)) goto out;
         mbar_arrive_expect_tx(&bars->full[slot], C::BLOCK_BYTES);
+        // (row, batch) of the block, or (row in page, page) for a paged cache: a block
+        // never crosses a page (unit starts and page sizes are multiples of 128).
+        int row = w.key0 + blk * KB, outer = w.b;
+        if (a.block_table != nullptr) {
+          outer = a.block_table[static_cast<int64_t>(w.b) * a.bt_stride + row / a.page_size];
+          if (which == 0 && (outer < 0 || outer >= a.num_pages))  // read back as zeros
+            atomicOr(a.err, DEVERR_BAD_BLOCK_TABLE);
+          row %= a.page_size;
+        }
 #pragma unroll
         for (int cc = 0; cc < C::KCH; ++cc)
           tma_load_4d_hint(smem + C::RING_OFF + slot * C::BLOCK_BYTES + cc * BOX_BYTES,
-                           which ? tmv : tmk, &bars->full[slot], cc * 64, w.g, w.key0 + blk * KB,
-                           w.b, policy);
+                           which ? tmv : tmk, &bars->full[slot], cc * 64, w.g, row, outer,
+                           policy);
         ++it;
       }
     }
@@ -173,8 +183,9 @@ __device__ __forceinline__ void release(uint64_t *bar, int lane) {
   if (lane == 0) mbar_arrive(bar);
 }
 
-// MOD: the launch has a softcap or ALiBi slopes (uniform runtime branches inside; the plain
-// instances carry none of that state).  A window needs no kernel support beyond unit_of.
+// MOD: the launch has a softcap, ALiBi slopes, or a window over a paged cache (whose unit
+// starts are page-aligned, so keys before the window are masked); uniform runtime branches
+// inside, and the plain instances carry none of that state.
 template <int D, int G, bool F16, bool MOD>
 __device__ void compute(const DecodeArgs &a, uint8_t *smem, DBars *bars, const WaitCtl &wc,
                         int tid) {
@@ -230,6 +241,8 @@ __device__ void compute(const DecodeArgs &a, uint8_t *smem, DBars *bars, const W
     // ALiBi slopes of the group's query heads (read where used: G more live registers
     // would spill at G = 8).
     const float *slopes = alibi ? a.alibi + w.b * a.alibi_sb + w.g * G : nullptr;
+    // Keys below `first` are streamed only to keep blocks page-aligned: masked.
+    const int first = MOD ? first_visible(w.len, a.wl) : 0;
 
     for (int blk = 0; blk < nblk; ++blk) {
       const int nvalid = min(KB, w.nkeys - blk * KB);
@@ -272,7 +285,8 @@ __device__ void compute(const DecodeArgs &a, uint8_t *smem, DBars *bars, const W
             if (alibi)  // - slope * distance from the query at position len - 1, log2 units
               sv = fmaf(slopes[gg] * -1.4426950408889634f,
                         static_cast<float>(w.len - 1 - (w.key0 + blk * KB + key)), sv);
-            sc[pass][gg] = key < nvalid ? sv : -INFINITY;
+            const bool seen = key < nvalid && (!MOD || w.key0 + blk * KB + key >= first);
+            sc[pass][gg] = seen ? sv : -INFINITY;
           }
         }
         release(&bars->empty[slot], lane);
@@ -455,7 +469,7 @@ template <int D, int G, bool F16>
 cudaError_t launch_decode_impl(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeArgs &a,
                                int grid, cudaStream_t stream) {
   constexpr int smem = DCfg<D, G>::SMEM_BYTES;
-  const bool mod = a.sc_out != 0.f || a.alibi != nullptr;
+  const bool mod = a.sc_out != 0.f || a.alibi != nullptr || (a.wl >= 0 && a.kalign > 1);
   auto kern = mod ? decode_kernel<D, G, F16, true> : decode_kernel<D, G, F16, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -466,13 +480,14 @@ cudaError_t launch_decode_impl(const CUtensorMap &tk, const CUtensorMap &tv, con
 // One block per (batch, query head); thread = output column.
 template <int D, bool F16>
 __global__ void __launch_bounds__(D)
-    combine_kernel(const float *o_part, const float *lse_part, const int *cache_len, int Hq,
-                   int Lmax, int chunk, int maxch, int wl, uint16_t *o, float *lse) {
+    combine_kernel(const float *o_part, const float *lse_part, const int *cache_len,
+                   int len_add, int Hq, int Lmax, int chunk, int maxch, int wl, int kalign,
+                   uint16_t *o, float *lse) {
   const int bh = blockIdx.x;
   const int b = bh / Hq;
   const int d = threadIdx.x;
-  const int len = min(max(cache_len[b], 0), Lmax);
-  const int nch = (len - first_visible(len, wl) + chunk - 1) / chunk;  // chunks of [first, len)
+  const int len = min(max(cache_len[b] + len_add, 0), Lmax);
+  const int nch = (len - decode_first_key(len, wl, kalign) + chunk - 1) / chunk;
   const float *lp = lse_part + static_cast<int64_t>(bh) * maxch;
   const float *op = o_part + static_cast<int64_t>(bh) * maxch * D;
   if (nch == 0) {
@@ -493,7 +508,86 @@ __global__ void __launch_bounds__(D)
   if (d == 0) lse[bh] = m + logf(wsum);
 }
 
+// ------------------------------------------------------------------------------------
+// In-place append ("flash-attention", section 1: the decode call writes the new key and
+// value into the cache and applies rotary in the same step).  One block per sequence;
+// thread = (head, dimension).  The new rows go to logical row cache_len[b]; with rotary
+// tables the new key and the query are turned by the angle of that position.
+
+// Element c of x after the rotary turn (c >= rot_dim: copied), rounded to the element type.
+// The grouping is fixed (one fused multiply-add per output, the product inside it rounded
+// first) so that the rounding decision is reproducible.
+template <bool F16>
+__device__ __forceinline__ uint16_t rotary_elem(const uint16_t *x, int c, int rot_dim,
+                                                bool interleaved, const float *cs,
+                                                const float *sn) {
+  if (c >= rot_dim) return x[c];
+  const int half = rot_dim / 2;
+  const bool first = interleaved ? (c & 1) == 0 : c < half;
+  const int i = interleaved ? c >> 1 : (first ? c : c - half);
+  const int ia = interleaved ? 2 * i : i;
+  const int ib = interleaved ? 2 * i + 1 : i + half;
+  const float xa = lo_to_f32<F16>(x[ia]), xb = lo_to_f32<F16>(x[ib]);
+  const float co = cs[i], si = sn[i];
+  const float y = first ? __fmaf_rn(xa, co, -__fmul_rn(xb, si))
+                        : __fmaf_rn(xa, si, __fmul_rn(xb, co));
+  return static_cast<uint16_t>(pack2<F16>(y, 0.f) & 0xFFFFu);
+}
+
+template <bool F16>
+__global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
+  const int b = blockIdx.x;
+  const int len = a.cache_len[b];
+  const bool rot = a.cos != nullptr;
+  bool ok = len >= 0 && len < a.Lmax && (!rot || len < a.rot_positions);
+  int64_t row = 0;  // element offset of the cache row
+  if (ok) {
+    if (a.block_table != nullptr) {
+      const int page = a.block_table[static_cast<int64_t>(b) * a.bt_stride + len / a.page_size];
+      ok = page >= 0 && page < a.num_pages;
+      row = static_cast<int64_t>(page) * a.c_s0 + static_cast<int64_t>(len % a.page_size) * a.c_s1;
+    } else {
+      row = static_cast<int64_t>(b) * a.c_s0 + static_cast<int64_t>(len) * a.c_s1;
+    }
+  }
+  if (!ok && threadIdx.x == 0) atomicOr(a.err, DEVERR_BAD_APPEND);
+  const int half = a.rot_dim / 2;
+  const float *cs = rot && ok ? a.cos + static_cast<int64_t>(len) * half : nullptr;
+  const float *sn = rot && ok ? a.sin + static_cast<int64_t>(len) * half : nullptr;
+  if (ok) {
+    const uint16_t *kn = reinterpret_cast<const uint16_t *>(a.k_new) + b * a.n_sb;
+    const uint16_t *vn = reinterpret_cast<const uint16_t *>(a.v_new) + b * a.n_sb;
+    uint16_t *kc = reinterpret_cast<uint16_t *>(a.k_cache) + row;
+    uint16_t *vc = reinterpret_cast<uint16_t *>(a.v_cache) + row;
+    for (int idx = threadIdx.x; idx < a.Hkv * a.d; idx += blockDim.x) {
+      const int h = idx / a.d, c = idx - h * a.d;
+      const uint16_t *kr = kn + h * a.n_sh;
+      kc[h * a.c_s2 + c] = rot ? rotary_elem<F16>(kr, c, a.rot_dim, a.rot_interleaved, cs, sn)
+                               : kr[c];
+      vc[h * a.c_s2 + c] = vn[h * a.n_sh + c];
+    }
+  }
+  if (rot) {  // the query at the same position (copied unturned if the append was refused)
+    const uint16_t *q = reinterpret_cast<const uint16_t *>(a.q) + static_cast<int64_t>(b) * a.Hq * a.d;
+    uint16_t *qr = reinterpret_cast<uint16_t *>(a.q_rot) + static_cast<int64_t>(b) * a.Hq * a.d;
+    for (int idx = threadIdx.x; idx < a.Hq * a.d; idx += blockDim.x) {
+      const int h = idx / a.d, c = idx - h * a.d;
+      qr[idx] = ok ? rotary_elem<F16>(q + h * a.d, c, a.rot_dim, a.rot_interleaved, cs, sn)
+                   : q[idx];
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_append(bool f16, const AppendArgs &a, cudaStream_t stream) {
+  if (a.B == 0) return cudaSuccess;
+  if (f16)
+    append_kernel<true><<<a.B, 256, 0, stream>>>(a);
+  else
+    append_kernel<false><<<a.B, 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
 
 int decode_smem_bytes(int d, int group) {
   if (d == 64) {
@@ -539,27 +633,16 @@ cudaError_t launch_decode(int d, int group, bool f16, const CUtensorMap &tk,
 }
 
 cudaError_t launch_combine(int d, bool f16, const float *o_part, const float *lse_part,
-                           const int *cache_len, int B, int Hq, int Lmax, int chunk, int maxch,
-                           int wl, void *o, float *lse, unsigned int * /*err*/,
-                           cudaStream_t stream) {
+                           const int *cache_len, int len_add, int B, int Hq, int Lmax, int chunk,
+                           int maxch, int wl, int kalign, void *o, float *lse,
+                           unsigned int * /*err*/, cudaStream_t stream) {
   const int blocks = B * Hq;
   if (blocks == 0) return cudaSuccess;
   uint16_t *ob = reinterpret_cast<uint16_t *>(o);
-  if (d == 64) {
-    if (f16)
-      combine_kernel<64, true><<<blocks, 64, 0, stream>>>(o_part, lse_part, cache_len, Hq, Lmax,
-                                                          chunk, maxch, wl, ob, lse);
-    else
-      combine_kernel<64, false><<<blocks, 64, 0, stream>>>(o_part, lse_part, cache_len, Hq, Lmax,
-                                                           chunk, maxch, wl, ob, lse);
-  } else {
-    if (f16)
-      combine_kernel<128, true><<<blocks, 128, 0, stream>>>(o_part, lse_part, cache_len, Hq,
-                                                            Lmax, chunk, maxch, wl, ob, lse);
-    else
-      combine_kernel<128, false><<<blocks, 128, 0, stream>>>(o_part, lse_part, cache_len, Hq,
-                                                             Lmax, chunk, maxch, wl, ob, lse);
-  }
+  auto kern = d == 64 ? (f16 ? combine_kernel<64, true> : combine_kernel<64, false>)
+                      : (f16 ? combine_kernel<128, true> : combine_kernel<128, false>);
+  kern<<<blocks, d, 0, stream>>>(o_part, lse_part, cache_len, len_add, Hq, Lmax, chunk, maxch,
+                                 wl, kalign, ob, lse);
   return cudaGetLastError();
 }
 

@@ -15,6 +15,8 @@ enum : unsigned int {
   DEVERR_DECODE_TIMEOUT = 2u,   // a bounded wait in the decode kernel gave up
   DEVERR_BAD_CU_SEQLENS = 4u,   // varlen prefix sums out of range (sequence skipped)
   DEVERR_BAD_CACHE_LEN = 8u,    // cache_seqlens outside [0, Lmax] (clamped)
+  DEVERR_BAD_APPEND = 16u,      // no room for an appended row / position past the tables
+  DEVERR_BAD_BLOCK_TABLE = 32u, // a block-table entry outside [0, num_pages)
 };
 
 // Arguments of the fused prefill kernel (dense and varlen share it).
@@ -80,17 +82,50 @@ struct DecodeArgs {
   float sc_in, sc_out;        // softcap on the log2-domain score: tanh(s * sc_in) * sc_out
   const float *alibi;         // slopes of (b, h) at alibi[b * alibi_sb + h], or null
   int64_t alibi_sb;
+  // KV-cache extras.
+  int len_add;                // 1 after an in-place append (length = cache_len + 1)
+  const int *block_table;     // paged cache: page of logical block j of b at [b*bt_stride + j]
+  int bt_stride, page_size, num_pages;
+  int kalign;                 // unit starts rounded down to a multiple of this (128 if paged)
 };
+
+// First key a decode unit streams: the first visible key, rounded down to `align` so that a
+// 128-key block never crosses a page.  Keys before the first visible one are masked.
+__host__ __device__ inline int decode_first_key(int len, int wl, int align) {
+  const int first = (wl >= 0 && len - 1 - wl > 0) ? len - 1 - wl : 0;
+  return first - first % align;
+}
+
+// In-place append of one new key/value row per sequence, with optional rotary embedding
+// of the new key and of the query (the rotated query goes to q_rot).
+struct AppendArgs {
+  const void *k_new, *v_new;
+  int64_t n_sb, n_sh;         // element strides (batch, head) of k_new / v_new
+  void *k_cache, *v_cache;
+  int64_t c_s0, c_s1, c_s2;   // cache strides: (batch or page, row, head)
+  const int *cache_len;
+  int B, Hq, Hkv, d, Lmax;
+  const int *block_table;
+  int bt_stride, page_size, num_pages;
+  const float *cos, *sin;     // rotary tables [rot_positions, rot_dim / 2], or null
+  int rot_dim, rot_positions, rot_interleaved;
+  const void *q;              // [B, 1, Hq, d] contiguous
+  void *q_rot;                // rotated query [B, 1, Hq, d] (when rotary)
+  unsigned int *err;
+};
+
+cudaError_t launch_append(bool f16, const AppendArgs &a, cudaStream_t stream);
 
 cudaError_t launch_decode(int d, int group, bool f16, const CUtensorMap &tk,
                           const CUtensorMap &tv, const DecodeArgs &a, int grid,
                           cudaStream_t stream);
 
-// wl: the decode launch's left window bound (-1 = unbounded); chunks tile the visible keys
-// [max(len - 1 - wl, 0), len) of each sequence.
+// wl, kalign, len_add: as in DecodeArgs; chunks tile the keys [decode_first_key, len) of
+// each sequence, len = cache_len + len_add.
 cudaError_t launch_combine(int d, bool f16, const float *o_part, const float *lse_part,
-                           const int *cache_len, int B, int Hq, int Lmax, int chunk, int maxch,
-                           int wl, void *o, float *lse, unsigned int *err, cudaStream_t stream);
+                           const int *cache_len, int len_add, int B, int Hq, int Lmax, int chunk,
+                           int maxch, int wl, int kalign, void *o, float *lse, unsigned int *err,
+                           cudaStream_t stream);
 
 // Shared-memory bytes the kernels request (for host-side checks).
 int prefill_smem_bytes(int d);

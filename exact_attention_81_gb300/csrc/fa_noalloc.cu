@@ -61,6 +61,6 @@ extern "C" fa_status fa_fwd_kvcache_noalloc(const void *q, const void *k_cache,
   const fa_status st = scratch_for_current_device(&scratch);
   if (st != FA_OK) return st;
   return fa_fwd_kvcache(q, k_cache, v_cache, cache_seqlens, B, Lmax, Hq, Hkv, d, cache_strides,
-                        scale, num_splits, scratch, FA_NOALLOC_SCRATCH_BYTES, o, lse, FA_BF16, nullptr,
+                        scale, num_splits, scratch, FA_NOALLOC_SCRATCH_BYTES, o, lse, FA_BF16, nullptr, nullptr,
                         stream);
 }

@@ -164,15 +164,63 @@ fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, fl
  * Hq / Hkv must be 1, 2, 4 or 8.  dtype is the fa_dtype of q, the caches and o.
  * mod: score modifiers (NULL = none; host memory, read during the call).  Only the left
  * window bound can hide a cached key (the query is the last position); cache rows before
- * the window start take no part in the result.
+ * the window start take no part in the result.  ex: append / rotary / paged cache
+ * (fa_kvcache_extras below; NULL = none; host memory, read during the call).
  */
 size_t fa_fwd_kvcache_workspace_size(int B, int Hq, int Lmax, int d, int num_splits);
+
+/*
+ * Decode-step extras of fa_fwd_kvcache ("flash-attention", section 1: the decode call
+ * updates the KV cache in place and applies rotary in the same step; capabilities table,
+ * KV cache row: in-place append, paged KV).  The pages give no formulas; this library
+ * reads them as follows.  A NULL pointer (or a zero-filled struct) means none of them.
+ *
+ * In-place append (k_new, v_new non-NULL): one new token per sequence.  Its key and value
+ * ([B, 1, Hkv, d], element strides new_strides (b, n, h), the type of the cache) are
+ * written to logical cache row cache_seqlens[b] BEFORE the attention, which then covers
+ * cache_seqlens[b] + 1 keys.  cache_seqlens itself is not modified.  A sequence whose row
+ * would fall outside the cache (cache_seqlens[b] >= Lmax, or a block-table entry outside
+ * [0, num_pages)) is not written and is flagged in the device error word.
+ *
+ * Rotary (rotary_cos, rotary_sin non-NULL; only with an append): DEVICE fp32 tables
+ * [rotary_positions, rotary_dim / 2].  The query and the new key are turned by the angle
+ * of position p = cache_seqlens[b]: dimension pairs (a, b) of the first rotary_dim
+ * dimensions -- (i, i + rotary_dim/2), or (2i, 2i+1) with rotary_interleaved -- become
+ *     y_a = x_a cos[p][i] - x_b sin[p][i],   y_b = x_a sin[p][i] + x_b cos[p][i],
+ * evaluated in fp32 (one fused multiply-add per output) and rounded to the element type
+ * (nearest even); the other dimensions are copied.  The rotated key is what the cache
+ * keeps.  The rotated query is staged in `o` (which the call overwrites with the result
+ * at the end), so o must not alias q.  rotary_dim is even, 2 <= rotary_dim <= d;
+ * cache_seqlens[b] < rotary_positions (a sequence breaking this is flagged and not
+ * appended).
+ *
+ * Paged cache (block_table non-NULL): k_cache / v_cache are [num_pages, page_size, Hkv, d]
+ * with element strides cache_strides (page, row, head); logical row r of sequence b is
+ * row r % page_size of page block_table[b * block_table_stride + r / page_size].  Lmax
+ * is the logical maximum length, at most block_table_stride * page_size.  page_size is a
+ * multiple of 128; entries outside [0, num_pages) are flagged (their rows read as 0).
+ */
+typedef struct fa_kvcache_extras {
+    const void *k_new;
+    const void *v_new;
+    int64_t new_strides[3];
+    const float *rotary_cos;
+    const float *rotary_sin;
+    int rotary_dim;
+    int rotary_positions;
+    int rotary_interleaved;
+    const int *block_table;
+    int block_table_stride;
+    int page_size;
+    int num_pages;
+} fa_kvcache_extras;
 
 fa_status fa_fwd_kvcache(const void *q, const void *k_cache, const void *v_cache,
                          const int *cache_seqlens, int B, int Lmax, int Hq, int Hkv, int d,
                          const int64_t cache_strides[3], float scale, int num_splits,
                          void *workspace, size_t workspace_bytes, void *o, float *lse,
-                         int dtype, const fa_score_mod *mod, cudaStream_t stream);
+                         int dtype, const fa_score_mod *mod, const fa_kvcache_extras *ex,
+                         cudaStream_t stream);
 
 /*
  * Split-KV decode that allocates nothing.  Same computation, arguments and outputs as

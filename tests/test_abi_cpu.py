@@ -123,7 +123,8 @@ def test_kvcache_rejects_bad_arguments(lib):
         a.update(kw)
         return lib.fa_fwd_kvcache(a["q"], a["kc"], a["vc"], a["lens"], a["B"], a["L"], a["Hq"],
                                   a["Hkv"], a["d"], strides, a["scale"], a["ns"], a["ws"],
-                                  a["wsb"], a["o"], a["lse"], a["dtype"], a.get("mod"), None)
+                                  a["wsb"], a["o"], a["lse"], a["dtype"], a.get("mod"),
+                                  a.get("ex"), None)
 
     assert call(Hq=32, Hkv=2) == 2          # group of 16 not supported by decode
     assert call(dtype=5) == 2
@@ -137,6 +138,24 @@ def test_kvcache_rejects_bad_arguments(lib):
     assert call(ws=4096 + 16) == 4          # workspace must be 256-byte aligned
     assert call(B=0) == 0
     assert call(mod=ctypes.byref(_mod(softcap=float("inf")))) == 1
+    from exact_attention_81_gb300._binding import KvCacheExtras
+
+    def ex(**kw):
+        e = KvCacheExtras()
+        for k, v in kw.items():
+            setattr(e, k, v)
+        return ctypes.byref(e)
+    assert call(ex=ex(k_new=4096)) == 1                                  # v_new missing
+    assert call(ex=ex(rotary_cos=4096, rotary_sin=4096, rotary_dim=64,
+                      rotary_positions=10)) == 1                         # rotary without append
+    assert call(ex=ex(k_new=4096, v_new=4096, rotary_cos=4096, rotary_sin=4096,
+                      rotary_dim=63, rotary_positions=10)) == 1          # odd rotary_dim
+    assert call(ex=ex(k_new=4096, v_new=4096, rotary_cos=4096, rotary_sin=4096,
+                      rotary_dim=256, rotary_positions=10)) == 1         # rotary_dim > d
+    assert call(ex=ex(block_table=4096, block_table_stride=8, page_size=100,
+                      num_pages=4)) == 1                                 # page not 128-multiple
+    assert call(ex=ex(block_table=4096, block_table_stride=4, page_size=128,
+                      num_pages=4)) == 1                                 # table shorter than Lmax
     assert call(mod=ctypes.byref(_mod(alibi_slopes=4096, alibi_batch_stride=-32))) == 1
 
 
