@@ -568,3 +568,161 @@ int oracle_round16(const float *x, int64_t n, uint16_t *out, int elem) {
     for (int64_t i = 0; i < n; ++i) out[i] = f32_to_bits(x[i], elem);
     return 0;
 }
+
+/* ------------------------------------------------------------------------- */
+/* Backward pass.                                                             */
+/*
+ * Gradients of the attention output with respect to Q, K and V for an upstream gradient
+ * dO ("flash-attention", sections 2.3 and 4: the backward pass keeps only q, k, v, out
+ * and softmax_lse and recomputes P = exp(S * scale - LSE); "FlashAttention 1-4 详解",
+ * FlashAttention 2: parallel over K/V column blocks, dK and dV accumulated per key,
+ * dQ accumulated across key blocks).  The plain chain rule through O = P V,
+ * P = softmax(S), S = scale Q K^T:
+ *     dV_j  = sum_i P_ij dO_i
+ *     dP_ij = dO_i . v_j
+ *     D_i   = sum_j P_ij dP_ij          (= dO_i . O_i)
+ *     dS_ij = P_ij (dP_ij - D_i)
+ *     dQ_i  = scale sum_j dS_ij k_j
+ *     dK_j  = scale sum_i dS_ij q_i
+ * Masked pairs have P = 0 and contribute nothing; with grouped-query attention dK and dV
+ * of a key/value head sum over the query heads that read it.
+ * Two passes, each over independent items: pass 1 per query row (its LSE, D_i and
+ * dQ_i), pass 2 per key row (dK_j and dV_j, with P recomputed from pass 1's LSE).
+ */
+
+typedef struct {
+    const uint16_t *q, *k, *v, *dout;
+    int64_t qs[3], ks[3], vs[3], dos[3];
+    int B, Nq, Nk, Hq, Hkv, d, causal, elem;
+    double scale;
+    double *lse, *D;          /* [B, Hq, Nq] (pass 1 output, pass 2 input) */
+    double *dq, *dk, *dv;     /* contiguous [B, N, H, d] */
+    int pass, nthreads, tid;
+} bwd_job_t;
+
+static double dot16(const uint16_t *a, const uint16_t *b, int d, int elem) {
+    double acc = 0.0;
+    for (int c = 0; c < d; ++c) acc += widen(a[c], elem) * widen(b[c], elem);
+    return acc;
+}
+
+/* Keys visible to query i: [0, hi) (bottom-right causal or all). */
+static int64_t bwd_key_end(const bwd_job_t *J, int64_t i) {
+    if (!J->causal) return J->Nk;
+    int64_t last = i + (J->Nk - J->Nq);
+    return last < 0 ? 0 : (last + 1 < J->Nk ? last + 1 : J->Nk);
+}
+
+static void *bwd_worker(void *arg) {
+    bwd_job_t *J = (bwd_job_t *)arg;
+    const int d = J->d, G = J->Hq / J->Hkv;
+    double *s = (double *)malloc(sizeof(double) * (size_t)(J->Nk > 0 ? J->Nk : 1));
+    double *dp = (double *)malloc(sizeof(double) * (size_t)(J->Nk > 0 ? J->Nk : 1));
+    if (J->pass == 1) {
+        int64_t total = (int64_t)J->B * J->Hq * J->Nq;
+        for (int64_t w = J->tid; w < total; w += J->nthreads) {
+            int b = (int)(w / ((int64_t)J->Hq * J->Nq));
+            int h = (int)((w / J->Nq) % J->Hq);
+            int64_t i = w % J->Nq, g = h / G, n = bwd_key_end(J, i);
+            const uint16_t *qi = J->q + b * J->qs[0] + i * J->qs[1] + h * J->qs[2];
+            const uint16_t *doi = J->dout + b * J->dos[0] + i * J->dos[1] + h * J->dos[2];
+            double *dqi = J->dq + (((int64_t)b * J->Nq + i) * J->Hq + h) * d;
+            int64_t li = ((int64_t)b * J->Hq + h) * J->Nq + i;
+            for (int c = 0; c < d; ++c) dqi[c] = 0.0;
+            if (n == 0) { J->lse[li] = -INFINITY; J->D[li] = 0.0; continue; }
+            double m = -INFINITY;
+            for (int64_t j = 0; j < n; ++j) {
+                s[j] = J->scale * dot16(qi, J->k + b * J->ks[0] + j * J->ks[1] + g * J->ks[2], d, J->elem);
+                if (s[j] > m) m = s[j];
+            }
+            double l = 0.0;
+            for (int64_t j = 0; j < n; ++j) {
+                double e = exp(s[j] - m);
+                s[j] = e;
+                l += e;
+            }
+            double Di = 0.0;
+            for (int64_t j = 0; j < n; ++j) {
+                s[j] /= l;                                                   /* P_ij */
+                dp[j] = dot16(doi, J->v + b * J->vs[0] + j * J->vs[1] + g * J->vs[2], d, J->elem);
+                Di += s[j] * dp[j];
+            }
+            for (int64_t j = 0; j < n; ++j) {
+                double ds = s[j] * (dp[j] - Di);
+                const uint16_t *kj = J->k + b * J->ks[0] + j * J->ks[1] + g * J->ks[2];
+                for (int c = 0; c < d; ++c) dqi[c] += J->scale * ds * widen(kj[c], J->elem);
+            }
+            J->lse[li] = m + log(l);
+            J->D[li] = Di;
+        }
+    } else {
+        int64_t total = (int64_t)J->B * J->Hkv * J->Nk;
+        for (int64_t w = J->tid; w < total; w += J->nthreads) {
+            int b = (int)(w / ((int64_t)J->Hkv * J->Nk));
+            int g = (int)((w / J->Nk) % J->Hkv);
+            int64_t j = w % J->Nk;
+            const uint16_t *kj = J->k + b * J->ks[0] + j * J->ks[1] + g * J->ks[2];
+            const uint16_t *vj = J->v + b * J->vs[0] + j * J->vs[1] + g * J->vs[2];
+            double *dkj = J->dk + (((int64_t)b * J->Nk + j) * J->Hkv + g) * d;
+            double *dvj = J->dv + (((int64_t)b * J->Nk + j) * J->Hkv + g) * d;
+            for (int c = 0; c < d; ++c) { dkj[c] = 0.0; dvj[c] = 0.0; }
+            for (int h = g * G; h < (g + 1) * G; ++h) {
+                for (int64_t i = 0; i < J->Nq; ++i) {
+                    if (j >= bwd_key_end(J, i)) continue;
+                    int64_t li = ((int64_t)b * J->Hq + h) * J->Nq + i;
+                    const uint16_t *qi = J->q + b * J->qs[0] + i * J->qs[1] + h * J->qs[2];
+                    const uint16_t *doi = J->dout + b * J->dos[0] + i * J->dos[1] + h * J->dos[2];
+                    double p = exp(J->scale * dot16(qi, kj, d, J->elem) - J->lse[li]);
+                    double ds = p * (dot16(doi, vj, d, J->elem) - J->D[li]);
+                    for (int c = 0; c < d; ++c) {
+                        dvj[c] += p * widen(doi[c], J->elem);
+                        dkj[c] += J->scale * ds * widen(qi[c], J->elem);
+                    }
+                }
+            }
+        }
+    }
+    free(s);
+    free(dp);
+    return NULL;
+}
+
+static int bwd_run(bwd_job_t *base) {
+    int n = base->nthreads < 1 ? 1 : (base->nthreads > 512 ? 512 : base->nthreads);
+    pthread_t th[512];
+    bwd_job_t jobs[512];
+    for (int t = 0; t < n; ++t) { jobs[t] = *base; jobs[t].nthreads = n; jobs[t].tid = t; }
+    for (int t = 1; t < n; ++t)
+        if (pthread_create(&th[t], NULL, bwd_worker, &jobs[t]) != 0) return -1;
+    bwd_worker(&jobs[0]);
+    for (int t = 1; t < n; ++t) pthread_join(th[t], NULL);
+    return 0;
+}
+
+/*
+ * Backward of dense batched attention.  q, dout: [B, Nq, Hq, d]; k, v: [B, Nk, Hkv, d]
+ * (element strides (b, n, h) given).  Outputs, contiguous doubles: dq [B, Nq, Hq, d],
+ * dk, dv [B, Nk, Hkv, d], and the lse and D = rowsum(dO * O) of each row [B, Hq, Nq].
+ */
+int oracle_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *dout,
+               int B, int Nq, int Nk, int Hq, int Hkv, int d, const int64_t *q_strides,
+               const int64_t *k_strides, const int64_t *v_strides, const int64_t *do_strides,
+               double scale, int causal, double *dq, double *dk, double *dv, double *lse,
+               double *D, int nthreads, int elem) {
+    if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || elem < 0 || elem > 1) return -1;
+    bwd_job_t J;
+    memset(&J, 0, sizeof J);
+    J.q = q; J.k = k; J.v = v; J.dout = dout;
+    for (int a = 0; a < 3; ++a) {
+        J.qs[a] = q_strides[a]; J.ks[a] = k_strides[a]; J.vs[a] = v_strides[a];
+        J.dos[a] = do_strides[a];
+    }
+    J.B = B; J.Nq = Nq; J.Nk = Nk; J.Hq = Hq; J.Hkv = Hkv; J.d = d; J.causal = causal;
+    J.elem = elem; J.scale = scale;
+    J.lse = lse; J.D = D; J.dq = dq; J.dk = dk; J.dv = dv;
+    J.nthreads = nthreads;
+    J.pass = 1;
+    if (bwd_run(&J) != 0) return -1;
+    J.pass = 2;
+    return bwd_run(&J);
+}

@@ -70,6 +70,9 @@ def _load():
             lib.oracle_row_probs.argtypes = [p, p, p, i, i, i, i, i, i, p, p, p, d, i, i, i, i,
                                              p, i] + mod
             lib.oracle_rotary.argtypes = [p, i64, i64, i, p, p, p, i, i, p, i]
+            lib.oracle_bwd.argtypes = [p, p, p, p, i, i, i, i, i, i, p, p, p, p, d, i, p, p, p,
+                                       p, p, i, i]
+            lib.oracle_bwd.restype = ctypes.c_int
             lib.oracle_round16.argtypes = [p, i64, p, i]
             for f in (lib.oracle_fwd, lib.oracle_fwd_rows, lib.oracle_fwd_varlen,
                       lib.oracle_fwd_kvcache, lib.oracle_row_probs, lib.oracle_rotary,
@@ -377,3 +380,35 @@ def kvcache_step(q, k_cache, v_cache, cache_seqlens, scale: float, k_new=None, v
     o, lse = attention_kvcache(qb, kl, vl, lens.astype(np.int32), scale, nthreads, el,
                                window=window, softcap=softcap, alibi_slopes=alibi_slopes)
     return o, lse, kc, vc
+
+
+# --------------------------------------------------------------------------
+# Backward pass ("flash-attention", sections 2.3 and 4: gradients recomputed from q, k, v,
+# out and softmax_lse; "FlashAttention 1-4 详解", FlashAttention 2 backward).
+
+
+def attention_bwd(q, k, v, dout, scale: float, causal: bool = False,
+                  nthreads: int | None = None, elem=None):
+    """Gradients of dense attention for the upstream gradient dout [B,Nq,Hq,d].
+
+    Returns (dQ [B,Nq,Hq,d], dK [B,Nk,Hkv,d], dV [B,Nk,Hkv,d], LSE [B,Hq,Nq],
+    D [B,Hq,Nq]) in float64, D_i = dO_i . O_i.
+    """
+    el = _common_elem(q, k, v, dout, elem=elem)
+    q, k, v, dout = _bits(q), _bits(k), _bits(v), _bits(dout)
+    B, Nq, Hq, d = q.shape
+    _, Nk, Hkv, _ = k.shape
+    if dout.shape != q.shape:
+        raise ValueError("dout must have the shape of q")
+    dq = np.zeros((B, Nq, Hq, d), np.float64)
+    dk = np.zeros((B, Nk, Hkv, d), np.float64)
+    dv = np.zeros((B, Nk, Hkv, d), np.float64)
+    lse = np.zeros((B, Hq, Nq), np.float64)
+    D = np.zeros((B, Hq, Nq), np.float64)
+    rc = _load().oracle_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), B, Nq, Nk, Hq, Hkv, d,
+                            _strides4(q), _strides4(k), _strides4(v), _strides4(dout),
+                            float(scale), int(bool(causal)), _ptr(dq), _ptr(dk), _ptr(dv),
+                            _ptr(lse), _ptr(D), _threads(nthreads), el)
+    if rc != 0:
+        raise ValueError("oracle_bwd rejected its arguments")
+    return dq, dk, dv, lse, D

@@ -794,9 +794,89 @@ def pin_kv_paged(O):
         _close(l3, l4, 0.0, "paged without append LSE")
 
 
+# --------------------------------------------------------------------------
+# Backward pass: the chain rule through O = P V, P = softmax(scale Q K^T).
+
+BWD_CASES = [
+    # B, Nq, Nk, Hq, Hkv, d, causal
+    (1, 33, 33, 2, 2, 16, False),
+    (2, 40, 40, 4, 2, 32, True),
+    (1, 20, 45, 4, 1, 16, True),   # Nq < Nk, bottom-right causal
+    (1, 45, 20, 2, 2, 16, True),   # Nq > Nk: leading rows see no key
+    (1, 130, 130, 1, 1, 64, True),
+]
+
+
+def pin_bwd_library(O):
+    """float64 torch autograd through scaled_dot_product_attention (a library routine the
+    oracle does not call), GQA as repeated heads, bottom-right causal mask."""
+    for n, (B, Nq, Nk, Hq, Hkv, d, causal) in enumerate(BWD_CASES):
+        q, k, v = dense_inputs(B, Nq, Nk, Hq, Hkv, d, seed=400 + n)
+        do = bf16_normal((B, Nq, Hq, d), seed=410 + n)
+        scale = 1.0 / math.sqrt(d)
+        dq, dk, dv, lse, D = O.attention_bwd(q, k, v, do, scale, causal)
+        G = Hq // Hkv
+        qq = _f64(q).permute(0, 2, 1, 3).requires_grad_()
+        kk = _f64(k).permute(0, 2, 1, 3).requires_grad_()
+        vv = _f64(v).permute(0, 2, 1, 3).requires_grad_()
+        mask = _bottom_right_mask(Nq, Nk) if causal else None
+        rows = mask.any(dim=1) if causal else torch.ones(Nq, dtype=torch.bool)
+        out = F.scaled_dot_product_attention(qq[:, :, rows], kk.repeat_interleave(G, dim=1),
+                                             vv.repeat_interleave(G, dim=1),
+                                             attn_mask=None if mask is None else mask[rows],
+                                             scale=scale)
+        out.backward(_f64(do).permute(0, 2, 1, 3)[:, :, rows])
+        _close(dq, qq.grad.permute(0, 2, 1, 3).numpy(), 1e-11, f"dQ vs autograd case {n}")
+        _close(dk, kk.grad.permute(0, 2, 1, 3).numpy(), 1e-11, f"dK vs autograd case {n}")
+        _close(dv, vv.grad.permute(0, 2, 1, 3).numpy(), 1e-11, f"dV vs autograd case {n}")
+        o_f, l_f = O.attention(q, k, v, scale, causal)
+        _close(lse, l_f, 1e-12, f"backward LSE vs forward case {n}")
+        D_ref = np.einsum("bnhd,bnhd->bhn", _np(do), o_f)
+        _close(D, D_ref, 1e-11, f"D = rowsum(dO * O) case {n}")
+
+
+def pin_bwd_closed_forms(O):
+    """sum_j dV_j = sum of dO over rows that see a key (each row of P sums to one);
+    constant V rows give dP_ij = D_i, so dS = 0 and dQ = dK = 0; causal row 0 sees one key,
+    so its dQ is 0; shifting every key by one vector (an exact bf16 shift) changes no
+    gradient; GQA gradients equal MHA with repeated K/V heads, dK and dV summed per group."""
+    B, N, Hq, Hkv, d = 1, 30, 4, 2, 16
+    q, k, v = dense_inputs(B, N, N, Hq, Hkv, d, seed=420)
+    do = bf16_normal((B, N, Hq, d), seed=421)
+    for causal in (False, True):
+        dq, dk, dv, _, _ = O.attention_bwd(q, k, v, do, 0.3, causal)
+        G = Hq // Hkv
+        tot = _np(do).reshape(B, N, Hkv, G, d).sum(axis=(1, 3))
+        _close(dv.sum(axis=1), tot, 1e-11, "sum of dV")
+        if causal:
+            _close(dq[:, 0], np.zeros((B, Hq, d)), 1e-14, "causal row 0 dQ")
+    c = bf16_normal((1, 1, Hkv, d), seed=422)
+    vc = c.expand(B, N, Hkv, d).contiguous()
+    dq, dk, dv, _, _ = O.attention_bwd(q, k, vc, do, 0.3, True)
+    _close(dq, np.zeros_like(dq), 1e-13, "constant V gives dQ = 0")
+    _close(dk, np.zeros_like(dk), 1e-13, "constant V gives dK = 0")
+    gen = torch.Generator().manual_seed(423)
+    ki = torch.randint(-8, 9, (B, N, Hkv, d), generator=gen).to(torch.bfloat16)
+    u = torch.randint(-8, 9, (1, 1, Hkv, d), generator=gen).to(torch.bfloat16)
+    ks = (ki.float() + u.float()).to(torch.bfloat16)
+    assert torch.equal(ks.float(), ki.float() + u.float()), "setup: the shift must be exact"
+    g1 = O.attention_bwd(q, ki, v, do, 0.05, True)
+    g2 = O.attention_bwd(q, ks, v, do, 0.05, True)
+    for a, b_, name in zip(g1[:3], g2[:3], ("dQ", "dK", "dV")):
+        _close(a, b_, 1e-11, f"{name} under a key shift")
+    g1 = O.attention_bwd(q, k, v, do, 0.3, True)
+    kr = k.repeat_interleave(Hq // Hkv, dim=2).contiguous()
+    vr = v.repeat_interleave(Hq // Hkv, dim=2).contiguous()
+    dq2, dk2, dv2, _, _ = O.attention_bwd(q, kr, vr, do, 0.3, True)
+    _close(g1[0], dq2, 1e-12, "GQA dQ vs MHA")
+    _close(g1[1], dk2.reshape(B, N, Hkv, Hq // Hkv, d).sum(axis=3), 1e-12, "GQA dK vs MHA")
+    _close(g1[2], dv2.reshape(B, N, Hkv, Hq // Hkv, d).sum(axis=3), 1e-12, "GQA dV vs MHA")
+
+
 ALL_PINS = [pin_library, pin_library_fp16, pin_fp16_values, pin_uniform_scores, pin_single_key, pin_constant_v, pin_two_keys,
             pin_empty_rows, pin_hard_max, pin_probs, pin_shift, pin_permutation, pin_gqa,
             pin_varlen, pin_kvcache, pin_rows, pin_recurrence, pin_lse_recompute,
             pin_window_uniform, pin_window_diagonal, pin_window_library, pin_softcap_limits,
             pin_alibi_geometric, pin_alibi_library, pin_mod_bruteforce, pin_mod_paths,
-            pin_round16_library, pin_rotary, pin_kv_append, pin_kv_paged]
+            pin_round16_library, pin_rotary, pin_kv_append, pin_kv_paged, pin_bwd_library,
+            pin_bwd_closed_forms]

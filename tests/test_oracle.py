@@ -73,6 +73,21 @@ MUTATIONS = [
     ("bf16 rounding truncates", "u += 0x7fffu + lsb;", "u += 0u * lsb;"),
     ("fp16 rounding ties away from zero",
      "if (rem > half || (rem == half && (q & 1u))) q += 1u;", "if (rem >= half) q += 1u;"),
+    ("dS without the D term (pass 1)", "double ds = s[j] * (dp[j] - Di);",
+     "double ds = s[j] * dp[j];"),
+    ("dS without the D term (pass 2)",
+     "double ds = p * (dot16(doi, vj, d, J->elem) - J->D[li]);",
+     "double ds = p * dot16(doi, vj, d, J->elem);"),
+    ("dK without the scale", "dkj[c] += J->scale * ds * widen(qi[c], J->elem);",
+     "dkj[c] += ds * widen(qi[c], J->elem);"),
+    ("dV from dS instead of P", "dvj[c] += p * widen(doi[c], J->elem);",
+     "dvj[c] += ds * widen(doi[c], J->elem);"),
+    ("dQ built from the query", "dqi[c] += J->scale * ds * widen(kj[c], J->elem);",
+     "dqi[c] += J->scale * ds * widen(qi[c], J->elem);"),
+    ("GQA dK and dV from one query head", "for (int h = g * G; h < (g + 1) * G; ++h) {",
+     "for (int h = g * G; h < g * G + 1; ++h) {"),
+    ("causal mask ignored in the key pass", "if (j >= bwd_key_end(J, i)) continue;",
+     "if (j >= J->Nk) continue;"),
     ("appended row one past the length", "i0, r = locate(b, int(lens[b]))",
      "i0, r = locate(b, int(lens[b]) + 1)", "py"),
     ("rotary at the next position", "kn = rotary(kn, np.repeat(lens, Hkv)",
