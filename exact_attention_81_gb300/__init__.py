@@ -3,9 +3,9 @@
 O = softmax(scale * Q K^T) V and the per-row log-sum-exp, computed tile by tile with the
 online-softmax recurrence in hand-written CUDA kernels (libfa.so, C ABI in include/fa.h).
 This package is the thin Python binding: ``fa_fwd`` (dense, batched, GQA, causal),
-``fa_fwd_varlen`` (packed sequences) and ``fa_fwd_kvcache`` (single-query split-KV decode),
-plus the upstream-style names ``flash_attn_func``, ``flash_attn_varlen_func`` and
-``flash_attn_with_kvcache``.  Build the library with
+``fa_fwd_varlen`` (packed sequences), ``fa_fwd_kvcache`` (single-query split-KV decode)
+and ``fa_bwd`` (gradients of ``fa_fwd``), plus the upstream-style names
+``flash_attn_func``, ``flash_attn_varlen_func`` and ``flash_attn_with_kvcache``.  Build the library with
 ``python -m exact_attention_81_gb300.build``.
 """
 from ._binding import (  # noqa: F401
@@ -18,6 +18,8 @@ from ._binding import (  # noqa: F401
     FA_ERR_WORKSPACE,
     FA_OK,
     FAError,
+    fa_bwd,
+    fa_bwd_workspace_size,
     fa_fwd,
     fa_fwd_kvcache,
     fa_fwd_kvcache_workspace_size,

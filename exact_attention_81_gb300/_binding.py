@@ -99,6 +99,24 @@ class FwdParams(ctypes.Structure):
     ]
 
 
+class BwdParams(ctypes.Structure):
+    """Mirror of fa_bwd_params."""
+
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("o", ctypes.c_void_p), ("dout", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+        ("dq", ctypes.c_void_p), ("dk", ctypes.c_void_p), ("dv", ctypes.c_void_p),
+        ("B", ctypes.c_int), ("Nq", ctypes.c_int), ("Nk", ctypes.c_int), ("Hq", ctypes.c_int),
+        ("Hkv", ctypes.c_int), ("d", ctypes.c_int),
+        ("q_strides", ctypes.c_int64 * 3), ("k_strides", ctypes.c_int64 * 3),
+        ("v_strides", ctypes.c_int64 * 3), ("o_strides", ctypes.c_int64 * 3),
+        ("do_strides", ctypes.c_int64 * 3), ("dq_strides", ctypes.c_int64 * 3),
+        ("dk_strides", ctypes.c_int64 * 3), ("dv_strides", ctypes.c_int64 * 3),
+        ("scale", ctypes.c_float), ("causal", ctypes.c_int), ("dtype", ctypes.c_int),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+
 _lib = None
 _lock = threading.Lock()
 
@@ -138,8 +156,16 @@ def load_library(path: str | None = None):
         lib.fa_set_wait_timeout_ns.restype = None
         lib.fa_fwd_params_size.argtypes = []
         lib.fa_fwd_params_size.restype = sz
+        lib.fa_bwd.argtypes = [ctypes.POINTER(BwdParams), vp]
+        lib.fa_bwd.restype = i
+        lib.fa_bwd_workspace_size.argtypes = [i, i, i, i]
+        lib.fa_bwd_workspace_size.restype = sz
+        lib.fa_bwd_params_size.argtypes = []
+        lib.fa_bwd_params_size.restype = sz
         if lib.fa_fwd_params_size() != ctypes.sizeof(FwdParams):
             raise RuntimeError("fa_fwd_params layout mismatch between libfa.so and the binding")
+        if lib.fa_bwd_params_size() != ctypes.sizeof(BwdParams):
+            raise RuntimeError("fa_bwd_params layout mismatch between libfa.so and the binding")
         if path is None:
             _lib = lib
         return lib
@@ -370,6 +396,51 @@ def fa_fwd_kvcache(q, k_cache, v_cache, cache_seqlens, scale: float | None = Non
                                        _stream_handle(stream))
     _check(st, "fa_fwd_kvcache")
     return out, lse
+
+
+def fa_bwd_workspace_size(B: int, Nq: int, Hq: int, d: int) -> int:
+    return int(load_library().fa_bwd_workspace_size(B, Nq, Hq, d))
+
+
+def fa_bwd(q, k, v, out, lse, dout, causal: bool = False, scale: float | None = None,
+           dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Backward of fa_fwd: q/out/dout [B,Nq,Hq,d], k/v [B,Nk,Hkv,d] (bf16 or fp16, CUDA),
+    lse [B,Hq,Nq] fp32 from the forward call.  Returns (dq, dk, dv)."""
+    _require_bf16_cuda("q", q, 4)
+    for name, t in (("k", k), ("v", v), ("out", out), ("dout", dout)):
+        _require_bf16_cuda(name, t, 4, q.dtype)
+    B, Nq, Hq, d = q.shape
+    Nk, Hkv = k.shape[1], k.shape[2]
+    if tuple(k.shape) != (B, Nk, Hkv, d) or tuple(v.shape) != (B, Nk, Hkv, d):
+        raise ValueError("k and v must be [B, Nk, Hkv, d] matching q")
+    if tuple(out.shape) != tuple(q.shape) or tuple(dout.shape) != tuple(q.shape):
+        raise ValueError("out and dout must have the shape of q")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, Hq, Nq) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [B, Hq, Nq] tensor")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for name, t, ref in (("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
+        _require_bf16_cuda(name, t, 4, q.dtype)
+        if t.shape != ref.shape:
+            raise ValueError(f"{name} must have the shape of {name[1:]}")
+    need = fa_bwd_workspace_size(B, Nq, Hq, d)
+    if workspace is None:
+        workspace = torch.empty((max(need, 256),), dtype=torch.uint8, device=q.device)
+    p = BwdParams()
+    p.q, p.k, p.v, p.o, p.dout = _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout)
+    p.lse, p.dq, p.dk, p.dv = _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv)
+    p.B, p.Nq, p.Nk, p.Hq, p.Hkv, p.d = B, Nq, Nk, Hq, Hkv, d
+    for name, t in (("q_strides", q), ("k_strides", k), ("v_strides", v), ("o_strides", out),
+                    ("do_strides", dout), ("dq_strides", dq), ("dk_strides", dk),
+                    ("dv_strides", dv)):
+        getattr(p, name)[:] = list(t.stride()[:3])
+    p.scale = default_scale(d) if scale is None else float(scale)
+    p.causal = int(bool(causal))
+    p.dtype = _DTYPE[q.dtype]
+    p.workspace, p.workspace_bytes = _ptr(workspace), workspace.numel()
+    _check(load_library().fa_bwd(ctypes.byref(p), _stream_handle(stream)), "fa_bwd")
+    return dq, dk, dv
 
 
 def get_last_device_error(stream=None) -> int:

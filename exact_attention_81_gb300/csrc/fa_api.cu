@@ -124,6 +124,27 @@ fa_status make_map(CUtensorMap *map, const void *base, int d, int64_t n, int64_t
   return FA_OK;
 }
 
+// 4-D fp32 tensor map over a contiguous (batch, seq, head, d) accumulator, box
+// {32, 1, 128, 1} (32 floats = 128 bytes x 128 rows), 128-byte swizzle: the target of the
+// backward pass's dQ reductions.
+fa_status make_map_f32(CUtensorMap *map, void *base, int d, int64_t n, int64_t h, int64_t b) {
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(h),
+                        static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(b)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(h * d) * 4,
+                           static_cast<cuuint64_t>(n * h * d) * 4};
+  cuuint32_t box[4] = {32, 1, 128, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(g_cuda_msg, sizeof g_cuda_msg, "cuTensorMapEncodeTiled (fp32) failed (CUresult %d)",
+             static_cast<int>(r));
+    return FA_ERR_CUDA;
+  }
+  return FA_OK;
+}
+
 bool stride_ok(int64_t s, int64_t extent) {
   if (extent <= 1) return s >= 0;
   return s > 0 && (s % 8) == 0 && s < (int64_t(1) << 38);
@@ -560,6 +581,115 @@ fa_status fa_fwd_kvcache(const void *q, const void *k_cache, const void *v_cache
   return e == cudaSuccess ? FA_OK : cuda_fail("combine kernel launch", e);
 }
 
+size_t fa_bwd_params_size(void) { return sizeof(fa_bwd_params); }
+
+size_t fa_bwd_workspace_size(int B, int Nq, int Hq, int d) {
+  if (B <= 0 || Nq <= 0 || Hq <= 0 || d <= 0) return 0;
+  const int64_t acc = static_cast<int64_t>(B) * Nq * Hq * d * 4;
+  const int64_t vec = static_cast<int64_t>(B) * Hq * Nq * 4;
+  return static_cast<size_t>((acc + 255) / 256 * 256 + (vec + 255) / 256 * 256);
+}
+
+fa_status fa_bwd(const fa_bwd_params *p, cudaStream_t stream) {
+  if (p == nullptr) return FA_ERR_INVALID_ARG;
+  const fa_bwd_params &a = *p;
+  if (a.B < 0 || a.Nq < 0 || a.Nk < 0 || a.Hq <= 0 || a.Hkv <= 0 || a.Hq % a.Hkv != 0)
+    return FA_ERR_INVALID_ARG;
+  if (a.d != 64 && a.d != 128) return FA_ERR_UNSUPPORTED;
+  if (!dtype_ok(a.dtype)) return FA_ERR_UNSUPPORTED;
+  if (!scale_ok(a.scale)) return FA_ERR_INVALID_ARG;
+  if (a.Nq > (1 << 30) || a.Nk > (1 << 30)) return FA_ERR_INVALID_ARG;
+  if (a.B == 0 || (a.Nq == 0 && a.Nk == 0)) return FA_OK;
+  const bool q_side = a.Nq > 0, k_side = a.Nk > 0;
+  if (q_side) {
+    if (a.q == nullptr || a.o == nullptr || a.dout == nullptr || a.dq == nullptr ||
+        a.lse == nullptr)
+      return FA_ERR_INVALID_ARG;
+    if (!aligned(a.q, 16) || !aligned(a.o, 16) || !aligned(a.dout, 16) || !aligned(a.dq, 16) ||
+        !aligned(a.lse, 4))
+      return FA_ERR_INVALID_ARG;
+    for (const int64_t *st : {a.q_strides, a.o_strides, a.do_strides, a.dq_strides})
+      if (!stride_ok(st[0], a.B) || !stride_ok(st[1], a.Nq) || !stride_ok(st[2], a.Hq))
+        return FA_ERR_INVALID_ARG;
+  }
+  if (k_side) {
+    if (a.k == nullptr || a.v == nullptr || a.dk == nullptr || a.dv == nullptr)
+      return FA_ERR_INVALID_ARG;
+    if (!aligned(a.k, 16) || !aligned(a.v, 16) || !aligned(a.dk, 16) || !aligned(a.dv, 16))
+      return FA_ERR_INVALID_ARG;
+    for (const int64_t *st : {a.k_strides, a.v_strides, a.dk_strides, a.dv_strides})
+      if (!stride_ok(st[0], a.B) || !stride_ok(st[1], a.Nk) || !stride_ok(st[2], a.Hkv))
+        return FA_ERR_INVALID_ARG;
+  }
+  const size_t need = fa_bwd_workspace_size(a.B, a.Nq, a.Hq, a.d);
+  if (q_side && k_side &&
+      (a.workspace == nullptr || a.workspace_bytes < need || !aligned(a.workspace, 256)))
+    return FA_ERR_WORKSPACE;
+  const int kblocks = ceil_div(a.Nk, 128);
+  const int64_t units = static_cast<int64_t>(kblocks) * a.B * a.Hkv;
+  if (units > INT32_MAX) return FA_ERR_INVALID_ARG;
+
+  DeviceInfo *dev = nullptr;
+  fa_status st = current_device(&dev);
+  if (st != FA_OK) return st;
+  cudaError_t e;
+  if (!k_side) {  // no keys: dQ = 0
+    e = fa::launch_zero16(a.dq, a.B, a.Nq, a.Hq, a.d, a.dq_strides, stream);
+    return e == cudaSuccess ? FA_OK : cuda_fail("zero kernel launch", e);
+  }
+  if (!q_side) {  // no queries: dK = dV = 0
+    e = fa::launch_zero16(a.dk, a.B, a.Nk, a.Hkv, a.d, a.dk_strides, stream);
+    if (e == cudaSuccess) e = fa::launch_zero16(a.dv, a.B, a.Nk, a.Hkv, a.d, a.dv_strides, stream);
+    return e == cudaSuccess ? FA_OK : cuda_fail("zero kernel launch", e);
+  }
+  float *dq_acc = static_cast<float *>(a.workspace);
+  const int64_t acc_bytes = (static_cast<int64_t>(a.B) * a.Nq * a.Hq * a.d * 4 + 255) / 256 * 256;
+  float *dvec = reinterpret_cast<float *>(static_cast<char *>(a.workspace) + acc_bytes);
+  CUtensorMap tq, tk, tv, tdo, tdq;
+  if ((st = make_map(&tq, a.q, a.d, a.Nq, a.Hq, a.B, a.q_strides[1], a.q_strides[2],
+                     a.q_strides[0], a.dtype)) != FA_OK ||
+      (st = make_map(&tdo, a.dout, a.d, a.Nq, a.Hq, a.B, a.do_strides[1], a.do_strides[2],
+                     a.do_strides[0], a.dtype)) != FA_OK ||
+      (st = make_map(&tk, a.k, a.d, a.Nk, a.Hkv, a.B, a.k_strides[1], a.k_strides[2],
+                     a.k_strides[0], a.dtype)) != FA_OK ||
+      (st = make_map(&tv, a.v, a.d, a.Nk, a.Hkv, a.B, a.v_strides[1], a.v_strides[2],
+                     a.v_strides[0], a.dtype)) != FA_OK ||
+      (st = make_map_f32(&tdq, dq_acc, a.d, a.Nq, a.Hq, a.B)) != FA_OK)
+    return st;
+  const bool f16 = a.dtype == FA_FP16;
+  e = fa::launch_bwd_pre(a.d, f16, a.o, a.dout, a.B, a.Nq, a.Hq, a.o_strides, a.do_strides, dvec,
+                         dq_acc, stream);
+  if (e != cudaSuccess) return cuda_fail("backward preprocessing launch", e);
+  fa::BwdArgs ba{};
+  ba.lse = a.lse;
+  ba.dvec = dvec;
+  ba.dk = a.dk;
+  ba.dv = a.dv;
+  ba.dk_sb = a.dk_strides[0];
+  ba.dk_sn = a.dk_strides[1];
+  ba.dk_sh = a.dk_strides[2];
+  ba.dv_sb = a.dv_strides[0];
+  ba.dv_sn = a.dv_strides[1];
+  ba.dv_sh = a.dv_strides[2];
+  ba.B = a.B;
+  ba.Nq = a.Nq;
+  ba.Nk = a.Nk;
+  ba.Hq = a.Hq;
+  ba.Hkv = a.Hkv;
+  ba.group = a.Hq / a.Hkv;
+  ba.kblocks = kblocks;
+  ba.num_units = static_cast<int>(units);
+  ba.scale = a.scale;
+  ba.scale_log2 = scale_log2(a.scale);
+  ba.err = dev->err;
+  ba.timeout_ns = g_timeout_ns;
+  const int grid = static_cast<int>(units < dev->sm_count ? units : dev->sm_count);
+  e = fa::launch_bwd(a.d, a.causal != 0, f16, tq, tk, tv, tdo, tdq, ba, grid, stream);
+  if (e != cudaSuccess) return cuda_fail("backward kernel launch", e);
+  e = fa::launch_bwd_post(a.d, f16, dq_acc, a.scale, a.dq, a.B, a.Nq, a.Hq, a.dq_strides, stream);
+  return e == cudaSuccess ? FA_OK : cuda_fail("backward postprocessing launch", e);
+}
+
 fa_status fa_get_last_device_error(cudaStream_t stream) {
   DeviceInfo *dev = nullptr;
   fa_status st = current_device(&dev);
@@ -572,7 +702,8 @@ fa_status fa_get_last_device_error(cudaStream_t stream) {
   const unsigned int zero = 0;
   e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero);
   if (e != cudaSuccess) return cuda_fail("cudaMemcpyToSymbol", e);
-  if (word & (fa::DEVERR_PREFILL_TIMEOUT | fa::DEVERR_DECODE_TIMEOUT)) return FA_ERR_TIMEOUT;
+  if (word & (fa::DEVERR_PREFILL_TIMEOUT | fa::DEVERR_DECODE_TIMEOUT | fa::DEVERR_BWD_TIMEOUT))
+    return FA_ERR_TIMEOUT;
   if (word & (fa::DEVERR_BAD_CU_SEQLENS | fa::DEVERR_BAD_CACHE_LEN | fa::DEVERR_BAD_APPEND |
               fa::DEVERR_BAD_BLOCK_TABLE))
     return FA_ERR_INVALID_ARG;

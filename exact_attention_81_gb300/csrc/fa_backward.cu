@@ -1,0 +1,625 @@
+// fa_backward.cu -- backward pass of exact attention for sm_103a.
+//
+// "flash-attention" (ai-reference-codex.pages.dev), sections 2.3 and 4: the backward pass
+// keeps only q, k, v, out and softmax_lse, recomputes P = exp(S * scale - LSE) tile by tile
+// instead of storing it, and is parallel over K/V column blocks: each block keeps its dK and
+// dV on chip for the whole pass while dQ, which every key block contributes to, is
+// accumulated in global memory ("FlashAttention 1-4 详解", FlashAttention 2 backward).
+// With D_i = rowsum(dO_i * O_i) (computed by a preprocessing kernel):
+//     S^T  = K Q^T,  P^T = 2^(S^T scale log2e - LSE_i log2e)        (masked pairs: 0)
+//     dP^T = V dO^T, dS^T = P^T * (dP^T - D_i)
+//     dV  += P^T dO,  dK += dS^T Q,  dQ += dS K
+// and finally dK *= scale, dQ *= scale (a postprocessing kernel converts dQ).
+//
+// Work unit = (batch b, kv head g, 128-key block j), persistent CTAs in key-block order
+// (with causal masking the first key blocks see the most queries).  A unit visits every
+// 128-query block i of every query head of group g whose rows can see a key of block j.
+// Keys are the MMA rows (TMEM lanes) of S^T, dP^T, dV and dK, so the dK and dV
+// accumulators stay in TMEM across the unit.
+//
+// Roles (192 threads):
+//   warps 0-3  P^T and dS^T (thread = key row), the dQ epilogue (thread = query row) and
+//              the dK / dV epilogue at the end of a unit
+//   warp  4    producer: K, V (once per unit), Q, dO (per step) by TMA; LSE and D vectors
+//   warp  5    TMEM allocator and MMA issuer (one lane)
+// TMEM: S^T [0,128), dP^T [128,256) (then dS^T, then dQ), dV [256,256+d), dK [384,384+d).
+// P^T and dS^T are written back as packed 16-bit pairs over the first 64 columns of their
+// fp32 sources and feed the dV and dK MMAs from TMEM; dS is also written to shared memory
+// (queries contiguous, the MN-major A operand of the dQ MMA).  Each step's dQ tile goes
+// through shared memory to a TMA bulk reduce-add into an fp32 accumulator.
+#include <cmath>
+
+#include "fa_internal.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int BKEY = 128;         // keys per unit
+constexpr int BQ = 128;           // queries per step
+constexpr int NTHREADS = 192;
+constexpr int NCOMPUTE = 128;
+constexpr int PRODUCER_WARP = 4;
+constexpr int MMA_WARP = 5;
+constexpr int BOX = 128 * 128;    // one 128-byte-swizzled box: 128 rows x 128 bytes
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t T_ST = 0, T_DP = 128, T_DV = 256, T_DK = 384;
+constexpr float LOG2E = 1.4426950408889634f;
+
+template <int D, bool F16>
+struct BCfg {
+  static constexpr int KCH = D / 64;
+  static constexpr int TILE = KCH * BOX;            // [128 x D] 16-bit tile
+  static constexpr int K_OFF = 0;
+  static constexpr int V_OFF = TILE;
+  static constexpr int Q_OFF = 2 * TILE;
+  static constexpr int DO_OFF = 3 * TILE;
+  static constexpr int DS_OFF = 4 * TILE;           // dS: 2 boxes (query halves) x 128 keys
+  static constexpr int DQ_OFF = DS_OFF + 2 * BOX;   // fp32 dQ staging: D/32 boxes
+  static constexpr int VEC_OFF = DQ_OFF + (D / 32) * BOX;  // lse2[128], dvec[128]
+  static constexpr int BAR_OFF = VEC_OFF + 2 * BQ * 4;
+  static constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;
+  static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, false, false, F16);
+  static constexpr uint32_t IDESC_ACC = idesc_bf16_f32(128, D, false, true, F16);
+  static constexpr uint32_t IDESC_DQ = idesc_bf16_f32(128, D, true, true, F16);
+};
+
+struct BBars {
+  uint64_t kv_full, kv_empty, q_full, q_empty, vec_full, vec_empty;
+  uint64_t s_full, p_ready, dq_full, dq_empty, acc_full, acc_empty, mma_done;
+  uint64_t cgrp;  // group barrier of the 128 compute threads (bounded wait)
+  uint32_t tmem_base;
+  int abort;
+};
+
+struct BUnit {
+  int b, g, j;
+  int i0, nqb;   // query blocks [i0, nqb) of each head of the group
+  int nit;       // steps: group * (nqb - i0)
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ BUnit bunit_of(const BwdArgs &a, int u) {
+  BUnit w;
+  const int bg = a.B * a.Hkv;
+  w.j = u / bg;
+  const int r = u - w.j * bg;
+  w.b = r / a.Hkv;
+  w.g = r - w.b * a.Hkv;
+  w.nqb = (a.Nq + BQ - 1) / BQ;
+  w.i0 = 0;
+  if (CAUSAL) {
+    // first query block holding a row that sees key j*128: i*128 + 127 + (Nk - Nq) >= j*128
+    const long long t = static_cast<long long>(w.j) * BKEY - (a.Nk - a.Nq) - (BQ - 1);
+    w.i0 = t <= 0 ? 0 : static_cast<int>((t + BQ - 1) / BQ);
+    if (w.i0 > w.nqb) w.i0 = w.nqb;
+  }
+  w.nit = a.group * (w.nqb - w.i0);
+  return w;
+}
+
+// Step t of a unit: query head and query block.
+__device__ __forceinline__ void bstep(const BwdArgs &a, const BUnit &w, int t, int &h, int &i) {
+  const int per = w.nqb - w.i0;
+  h = w.g * a.group + t / per;
+  i = w.i0 + t % per;
+}
+
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const WaitCtl &wc) {
+  const bool ok = mbar_wait(bar, parity, wc);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Barrier among the 128 compute threads, built on an mbarrier so that the wait is bounded:
+// a warp that has given up never leaves the others blocked.
+__device__ __forceinline__ bool group_sync(uint64_t *bar, uint32_t &phase, const WaitCtl &wc) {
+  mbar_arrive(bar);
+  const bool ok = warp_wait(bar, phase, wc);
+  phase ^= 1u;
+  return ok;
+}
+
+// M=128 x N=128 x K=D product of two K-major 128-byte-swizzled tiles (S^T and dP^T).
+template <int D, bool F16>
+__device__ __forceinline__ void issue_kmajor(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem) {
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = static_cast<uint32_t>((kk >> 2) * BOX + (kk & 3) * 32);
+    mma_bf16_ss(d_tmem, sw128_desc(a_smem + off, 16, 1024), sw128_desc(b_smem + off, 16, 1024),
+                BCfg<D, F16>::IDESC_S, kk > 0 ? 1u : 0u);
+  }
+}
+
+// D[128 keys x D] (+)= A[128 keys x 128 queries] (TMEM, packed pairs) * B[128 queries x D]
+// (MN-major tile: rows = queries, D contiguous).  dV and dK.
+template <int D, bool F16>
+__device__ __forceinline__ void issue_acc(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem,
+                                          bool accumulate) {
+#pragma unroll
+  for (int kk = 0; kk < BQ / 16; ++kk)
+    mma_bf16_ts(d_tmem, a_tmem + static_cast<uint32_t>(kk * 8),
+                sw128_desc(b_smem + static_cast<uint32_t>(kk * 16 * 128), BOX, 1024),
+                BCfg<D, F16>::IDESC_ACC, (accumulate || kk > 0) ? 1u : 0u);
+}
+
+// dQ[128 queries x D] = dS[128 queries x 128 keys] (shared memory, MN-major: rows = keys,
+// queries contiguous) * K[128 keys x D] (MN-major: rows = keys, D contiguous).
+template <int D, bool F16>
+__device__ __forceinline__ void issue_dq(uint32_t d_tmem, uint32_t ds_smem, uint32_t k_smem) {
+#pragma unroll
+  for (int kk = 0; kk < BKEY / 16; ++kk) {
+    const uint32_t off = static_cast<uint32_t>(kk * 16 * 128);
+    mma_bf16_ss(d_tmem, sw128_desc(ds_smem + off, BOX, 1024), sw128_desc(k_smem + off, BOX, 1024),
+                BCfg<D, F16>::IDESC_DQ, kk > 0 ? 1u : 0u);
+  }
+}
+
+// ------------------------------------------------------------------------------------
+// Producer warp.
+
+template <int D, bool CAUSAL, bool F16>
+__device__ void bwd_producer(const BwdArgs &a, const CUtensorMap *tq, const CUtensorMap *tk,
+                             const CUtensorMap *tv, const CUtensorMap *tdo, uint8_t *smem,
+                             BBars *bars, const WaitCtl &wc, int lane) {
+  using C = BCfg<D, F16>;
+  float *lse2 = reinterpret_cast<float *>(smem + C::VEC_OFF);
+  float *dvec = lse2 + BQ;
+  uint32_t kv_n = 0, q_n = 0;
+  for (int u = blockIdx.x; u < a.num_units; u += gridDim.x) {
+    const BUnit w = bunit_of<CAUSAL>(a, u);
+    if (w.nit == 0) continue;
+    if (kv_n > 0 && !warp_wait(&bars->kv_empty, (kv_n - 1) & 1u, wc)) goto out;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&bars->kv_full, 2 * C::TILE);
+#pragma unroll
+      for (int c = 0; c < C::KCH; ++c) {
+        tma_load_4d(smem + C::K_OFF + c * BOX, tk, &bars->kv_full, c * 64, w.g, w.j * BKEY, w.b);
+        tma_load_4d(smem + C::V_OFF + c * BOX, tv, &bars->kv_full, c * 64, w.g, w.j * BKEY, w.b);
+      }
+    }
+    ++kv_n;
+    for (int t = 0; t < w.nit; ++t) {
+      int h, i;
+      bstep(a, w, t, h, i);
+      if (q_n > 0 && !warp_wait(&bars->q_empty, (q_n - 1) & 1u, wc)) goto out;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars->q_full, 2 * C::TILE);
+#pragma unroll
+        for (int c = 0; c < C::KCH; ++c) {
+          tma_load_4d(smem + C::Q_OFF + c * BOX, tq, &bars->q_full, c * 64, h, i * BQ, w.b);
+          tma_load_4d(smem + C::DO_OFF + c * BOX, tdo, &bars->q_full, c * 64, h, i * BQ, w.b);
+        }
+      }
+      // LSE (log2 domain; rows past Nq or with no visible key give P = 0) and D.
+      if (q_n > 0 && !warp_wait(&bars->vec_empty, (q_n - 1) & 1u, wc)) goto out;
+      const int64_t base = (static_cast<int64_t>(w.b) * a.Hq + h) * a.Nq;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int qi = lane * 4 + e, q = i * BQ + qi;
+        float l2 = INFINITY, dd = 0.f;
+        if (q < a.Nq) {
+          const float l = a.lse[base + q];
+          l2 = l == -INFINITY ? INFINITY : l * LOG2E;
+          dd = a.dvec[base + q];
+        }
+        lse2[qi] = l2;
+        dvec[qi] = dd;
+      }
+      __syncwarp();
+      mbar_arrive(&bars->vec_full);
+      ++q_n;
+    }
+  }
+out:
+  // Teardown: the last bulk copies issued must land before the CTA may exit.
+  if (lane == 0) {
+    if (kv_n > 0) mbar_wait_teardown(&bars->kv_full, (kv_n - 1) & 1u, 1000000000ull);
+    if (q_n > 0) mbar_wait_teardown(&bars->q_full, (q_n - 1) & 1u, 1000000000ull);
+  }
+}
+
+// ------------------------------------------------------------------------------------
+// MMA issuer (one lane).
+
+template <int D, bool CAUSAL, bool F16>
+__device__ void bwd_mma(const BwdArgs &a, uint8_t *smem, BBars *bars, uint32_t tmem,
+                        const WaitCtl &wc) {
+  using C = BCfg<D, F16>;
+  const uint32_t sK = smem_u32(smem + C::K_OFF), sV = smem_u32(smem + C::V_OFF);
+  const uint32_t sQ = smem_u32(smem + C::Q_OFF), sDO = smem_u32(smem + C::DO_OFF);
+  const uint32_t sDS = smem_u32(smem + C::DS_OFF);
+  uint32_t kv_n = 0, it = 0, acc_n = 0;
+  for (int u = blockIdx.x; u < a.num_units; u += gridDim.x) {
+    const BUnit w = bunit_of<CAUSAL>(a, u);
+    if (w.nit == 0) continue;
+    if (!mbar_wait(&bars->kv_full, kv_n & 1u, wc)) goto out;
+    ++kv_n;
+    if (acc_n > 0 && !mbar_wait(&bars->acc_empty, (acc_n - 1) & 1u, wc)) goto out;
+    for (int t = 0; t < w.nit; ++t) {
+      if (!mbar_wait(&bars->q_full, it & 1u, wc)) goto out;
+      tc_fence_after();
+      issue_kmajor<D, F16>(tmem + T_ST, sK, sQ);                  // S^T = K Q^T
+      // dP^T overwrites the previous step's dQ: wait until the epilogue has read it.
+      if (it > 0 && !mbar_wait(&bars->dq_empty, (it - 1) & 1u, wc)) goto out;
+      tc_fence_after();
+      issue_kmajor<D, F16>(tmem + T_DP, sV, sDO);                 // dP^T = V dO^T
+      mma_commit(&bars->s_full);
+      if (!mbar_wait(&bars->p_ready, it & 1u, wc)) goto out;
+      tc_fence_after();
+      issue_acc<D, F16>(tmem + T_DV, tmem + T_ST, sDO, t > 0);    // dV += P^T dO
+      issue_acc<D, F16>(tmem + T_DK, tmem + T_DP, sQ, t > 0);     // dK += dS^T Q
+      issue_dq<D, F16>(tmem + T_DP, sDS, sK);                     // dQ = dS K
+      mma_commit(&bars->q_empty);
+      mma_commit(&bars->dq_full);
+      ++it;
+    }
+    mma_commit(&bars->kv_empty);
+    mma_commit(&bars->acc_full);
+    ++acc_n;
+  }
+out:
+  mma_commit(&bars->mma_done);
+  mbar_wait_teardown(&bars->mma_done, 0u, 1000000000ull);
+}
+
+// ------------------------------------------------------------------------------------
+// Compute warps.
+
+template <int D, bool CAUSAL, bool F16>
+__device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *smem, BBars *bars,
+                            uint32_t tmem, const WaitCtl &wc, int tid) {
+  using C = BCfg<D, F16>;
+  const int warp = tid >> 5;
+  const int r = tid;  // TMEM lane: key row of S^T / dP^T / dV / dK, query row of dQ
+  const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+  const float *lse2 = reinterpret_cast<const float *>(smem + C::VEC_OFF);
+  const float *dvec = lse2 + BQ;
+  uint8_t *ds_s = smem + C::DS_OFF;
+  uint8_t *dq_s = smem + C::DQ_OFF;
+  const int off = a.Nk - a.Nq;  // bottom-right alignment: query q sits at key position q + off
+  uint32_t it = 0, acc_n = 0, grp = 0;
+  for (int u = blockIdx.x; u < a.num_units; u += gridDim.x) {
+    const BUnit w = bunit_of<CAUSAL>(a, u);
+    const int key = w.j * BKEY + r;
+    uint16_t *dkrow = reinterpret_cast<uint16_t *>(a.dk) + w.b * a.dk_sb + key * a.dk_sn +
+                      w.g * a.dk_sh;
+    uint16_t *dvrow = reinterpret_cast<uint16_t *>(a.dv) + w.b * a.dv_sb + key * a.dv_sn +
+                      w.g * a.dv_sh;
+    if (w.nit == 0) {  // no query sees these keys: zero gradients
+      if (key < a.Nk) {
+#pragma unroll
+        for (int v = 0; v < D / 8; ++v) {
+          reinterpret_cast<uint4 *>(dkrow)[v] = make_uint4(0u, 0u, 0u, 0u);
+          reinterpret_cast<uint4 *>(dvrow)[v] = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      continue;
+    }
+    for (int t = 0; t < w.nit; ++t) {
+      int h, i;
+      bstep(a, w, t, h, i);
+      if (!warp_wait(&bars->vec_full, it & 1u, wc)) return;
+      if (!warp_wait(&bars->s_full, it & 1u, wc)) return;
+      tc_fence_after();
+      // P^T and dS^T of this key row, 32 queries at a time.
+      const int q0 = i * BQ;
+      const bool full = !CAUSAL || (w.j * BKEY + BKEY - 1 <= q0 + off);  // no pair masked
+#pragma unroll 1
+      for (int c = 0; c < BQ / 32; ++c) {
+        uint32_t sr[32], dr[32];
+        tmem_ld_x32(tmem + lane_off + T_ST + c * 32, sr);
+        tmem_ld_x32(tmem + lane_off + T_DP + c * 32, dr);
+        uint32_t pp[16], dd[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float p[2], ds[2];
+#pragma unroll
+          for (int x = 0; x < 2; ++x) {
+            const int qi = c * 32 + e + x;
+            const bool vis = key < a.Nk && (full || key <= q0 + qi + off);
+            const float pv = ex2_approx(fmaf(__uint_as_float(sr[e + x]), a.scale_log2, -lse2[qi]));
+            p[x] = vis ? pv : 0.f;
+            ds[x] = p[x] * (__uint_as_float(dr[e + x]) - dvec[qi]);
+          }
+          pp[e / 2] = pack2<F16>(p[0], p[1]);
+          dd[e / 2] = pack2<F16>(ds[0], ds[1]);
+        }
+        tmem_st_x16(tmem + lane_off + T_ST + c * 16, pp);
+        tmem_st_x16(tmem + lane_off + T_DP + c * 16, dd);
+        // dS to shared memory: row = key, queries contiguous (box c/2, granules (c%2)*4..+3)
+        uint8_t *box = ds_s + (c >> 1) * BOX + r * 128;
+#pragma unroll
+        for (int gi = 0; gi < 4; ++gi) {
+          const int gran = (c & 1) * 4 + gi;
+          *reinterpret_cast<uint4 *>(box + ((gran ^ (r & 7)) << 4)) =
+              make_uint4(dd[4 * gi], dd[4 * gi + 1], dd[4 * gi + 2], dd[4 * gi + 3]);
+        }
+      }
+      mbar_arrive(&bars->vec_empty);
+      tmem_wait_st();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bars->p_ready);
+      // dQ epilogue: TMEM -> shared memory (fp32, 128-byte swizzle) -> TMA reduce-add.
+      if (!warp_wait(&bars->dq_full, it & 1u, wc)) return;
+      tc_fence_after();
+      if (tid == 0) bulk_wait_read();  // the previous reduction has read the staging tile
+      if (!group_sync(&bars->cgrp, grp, wc)) return;
+#pragma unroll 1
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t qr[32];
+        tmem_ld_x32(tmem + lane_off + T_DP + cc * 32, qr);
+        uint8_t *box = dq_s + cc * BOX + r * 128;
+#pragma unroll
+        for (int gran = 0; gran < 8; ++gran)
+          *reinterpret_cast<uint4 *>(box + ((gran ^ (r & 7)) << 4)) =
+              make_uint4(qr[4 * gran], qr[4 * gran + 1], qr[4 * gran + 2], qr[4 * gran + 3]);
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->dq_empty);
+      fence_proxy_async_smem();
+      if (!group_sync(&bars->cgrp, grp, wc)) return;
+      if (tid == 0) {
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc)
+          tma_reduce_add_4d(tdq, dq_s + cc * BOX, cc * 32, h, q0, w.b);
+        bulk_commit_group();
+      }
+      ++it;
+    }
+    // Unit end: dV and scale * dK of this key row -> global memory.
+    if (!warp_wait(&bars->acc_full, acc_n & 1u, wc)) return;
+    tc_fence_after();
+#pragma unroll 1
+    for (int cc = 0; cc < D / 32; ++cc) {
+      uint32_t vr[32], kr[32];
+      tmem_ld_x32(tmem + lane_off + T_DV + cc * 32, vr);
+      tmem_ld_x32(tmem + lane_off + T_DK + cc * 32, kr);
+      if (key < a.Nk) {
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          uint4 wv, wk;
+          wv.x = pack2<F16>(__uint_as_float(vr[8 * v + 0]), __uint_as_float(vr[8 * v + 1]));
+          wv.y = pack2<F16>(__uint_as_float(vr[8 * v + 2]), __uint_as_float(vr[8 * v + 3]));
+          wv.z = pack2<F16>(__uint_as_float(vr[8 * v + 4]), __uint_as_float(vr[8 * v + 5]));
+          wv.w = pack2<F16>(__uint_as_float(vr[8 * v + 6]), __uint_as_float(vr[8 * v + 7]));
+          wk.x = pack2<F16>(__uint_as_float(kr[8 * v + 0]) * a.scale, __uint_as_float(kr[8 * v + 1]) * a.scale);
+          wk.y = pack2<F16>(__uint_as_float(kr[8 * v + 2]) * a.scale, __uint_as_float(kr[8 * v + 3]) * a.scale);
+          wk.z = pack2<F16>(__uint_as_float(kr[8 * v + 4]) * a.scale, __uint_as_float(kr[8 * v + 5]) * a.scale);
+          wk.w = pack2<F16>(__uint_as_float(kr[8 * v + 6]) * a.scale, __uint_as_float(kr[8 * v + 7]) * a.scale);
+          reinterpret_cast<uint4 *>(dvrow + cc * 32)[v] = wv;
+          reinterpret_cast<uint4 *>(dkrow + cc * 32)[v] = wk;
+        }
+      }
+    }
+    tc_fence_before();
+    mbar_arrive(&bars->acc_empty);
+    ++acc_n;
+  }
+}
+
+template <int D, bool CAUSAL, bool F16>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+               const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+               const __grid_constant__ CUtensorMap tdq, const BwdArgs a) {
+  using C = BCfg<D, F16>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  BBars *bars = reinterpret_cast<BBars *>(smem + C::BAR_OFF);
+  const int tid = static_cast<int>(threadIdx.x);
+  const int warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    mbar_init(&bars->kv_full, 1);
+    mbar_init(&bars->kv_empty, 1);
+    mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 1);
+    mbar_init(&bars->vec_full, 32);
+    mbar_init(&bars->vec_empty, NCOMPUTE);
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->p_ready, NCOMPUTE);
+    mbar_init(&bars->dq_full, 1);
+    mbar_init(&bars->dq_empty, NCOMPUTE);
+    mbar_init(&bars->acc_full, 1);
+    mbar_init(&bars->acc_empty, NCOMPUTE);
+    mbar_init(&bars->mma_done, 1);
+    mbar_init(&bars->cgrp, NCOMPUTE);
+    bars->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == PRODUCER_WARP && lane == 0) {
+    tma_prefetch_desc(&tq);
+    tma_prefetch_desc(&tk);
+    tma_prefetch_desc(&tv);
+    tma_prefetch_desc(&tdo);
+    tma_prefetch_desc(&tdq);
+  }
+  if (warp == MMA_WARP) {
+    tmem_alloc(&bars->tmem_base, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const WaitCtl wc{&bars->abort, a.err, a.timeout_ns, DEVERR_BWD_TIMEOUT};
+  if (warp < PRODUCER_WARP) {
+    bwd_compute<D, CAUSAL, F16>(a, &tdq, smem, bars, tmem, wc, tid);
+    if (tid == 0) bulk_wait_all();  // every dQ reduction has landed
+  } else if (warp == PRODUCER_WARP) {
+    bwd_producer<D, CAUSAL, F16>(a, &tq, &tk, &tv, &tdo, smem, bars, wc, lane);
+  } else if (lane == 0) {
+    bwd_mma<D, CAUSAL, F16>(a, smem, bars, tmem, wc);
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------------------------
+// Preprocessing: D = rowsum(dO * O) (one warp per row) and a zeroed dQ accumulator.
+
+template <int D, bool F16>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t *o, const uint16_t *dout,
+                                                      int B, int Nq, int Hq, int64_t os0,
+                                                      int64_t os1, int64_t os2, int64_t ds0,
+                                                      int64_t ds1, int64_t ds2, float *dvec,
+                                                      float *dq_acc) {
+  const int lane = threadIdx.x & 31;
+  const int64_t rows = static_cast<int64_t>(B) * Nq * Hq;
+  for (int64_t rw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / 32; rw < rows;
+       rw += static_cast<int64_t>(gridDim.x) * blockDim.x / 32) {
+    const int h = static_cast<int>(rw % Hq);
+    const int64_t bn = rw / Hq;
+    const int n = static_cast<int>(bn % Nq);
+    const int b = static_cast<int>(bn / Nq);
+    const uint16_t *orow = o + b * os0 + n * os1 + h * os2;
+    const uint16_t *drow = dout + b * ds0 + n * ds1 + h * ds2;
+    float acc = 0.f;
+#pragma unroll
+    for (int c = lane * 2; c < D; c += 64) {
+      const uint32_t ov = *reinterpret_cast<const uint32_t *>(orow + c);
+      const uint32_t dv = *reinterpret_cast<const uint32_t *>(drow + c);
+      acc = fmaf(lo_to_f32<F16>(ov), lo_to_f32<F16>(dv), acc);
+      acc = fmaf(hi_to_f32<F16>(ov), hi_to_f32<F16>(dv), acc);
+    }
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+    if (lane == 0) dvec[(static_cast<int64_t>(b) * Hq + h) * Nq + n] = acc;
+    float *qrow = dq_acc + (bn * Hq + h) * D;
+#pragma unroll
+    for (int c = lane * 4; c < D; c += 128)
+      *reinterpret_cast<float4 *>(qrow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+// dQ = scale * accumulator, 8 elements per thread.
+template <bool F16>
+__global__ void __launch_bounds__(256) bwd_post_kernel(const float *acc, float scale, uint16_t *dq,
+                                                       int B, int Nq, int Hq, int d, int64_t s0,
+                                                       int64_t s1, int64_t s2) {
+  const int64_t total = static_cast<int64_t>(B) * Nq * Hq * (d / 8);
+  for (int64_t x = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; x < total;
+       x += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int c8 = static_cast<int>(x % (d / 8));
+    const int64_t row = x / (d / 8);  // (b, n, h)
+    const int h = static_cast<int>(row % Hq);
+    const int64_t bn = row / Hq;
+    const int n = static_cast<int>(bn % Nq);
+    const int b = static_cast<int>(bn / Nq);
+    const float4 v0 = reinterpret_cast<const float4 *>(acc + row * d)[2 * c8];
+    const float4 v1 = reinterpret_cast<const float4 *>(acc + row * d)[2 * c8 + 1];
+    uint4 w;
+    w.x = pack2<F16>(v0.x * scale, v0.y * scale);
+    w.y = pack2<F16>(v0.z * scale, v0.w * scale);
+    w.z = pack2<F16>(v1.x * scale, v1.y * scale);
+    w.w = pack2<F16>(v1.z * scale, v1.w * scale);
+    *reinterpret_cast<uint4 *>(dq + b * s0 + n * s1 + h * s2 + c8 * 8) = w;
+  }
+}
+
+__global__ void zero16_kernel(uint16_t *x, int B, int N, int H, int d, int64_t s0, int64_t s1,
+                              int64_t s2) {
+  const int64_t total = static_cast<int64_t>(B) * N * H * (d / 8);
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < total;
+       t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int c8 = static_cast<int>(t % (d / 8));
+    const int64_t row = t / (d / 8);
+    const int h = static_cast<int>(row % H);
+    const int64_t bn = row / H;
+    const int n = static_cast<int>(bn % N);
+    const int b = static_cast<int>(bn / N);
+    *reinterpret_cast<uint4 *>(x + b * s0 + n * s1 + h * s2 + c8 * 8) = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+int grid_for(int64_t items, int threads) {
+  const int64_t g = (items + threads - 1) / threads;
+  return static_cast<int>(g < 1 ? 1 : (g > 8192 ? 8192 : g));
+}
+
+template <int D, bool CAUSAL, bool F16>
+cudaError_t launch_bwd_impl(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                            const CUtensorMap &tdo, const CUtensorMap &tdq, const BwdArgs &a,
+                            int grid, cudaStream_t stream) {
+  constexpr int smem = BCfg<D, F16>::SMEM_BYTES;
+  static_assert(smem <= 232448, "backward kernel shared memory");
+  cudaError_t e = cudaFuncSetAttribute(bwd_kernel<D, CAUSAL, F16>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  bwd_kernel<D, CAUSAL, F16><<<grid, NTHREADS, smem, stream>>>(tq, tk, tv, tdo, tdq, a);
+  return cudaGetLastError();
+}
+
+template <int D, bool F16>
+cudaError_t launch_bwd_d(bool causal, const CUtensorMap &tq, const CUtensorMap &tk,
+                         const CUtensorMap &tv, const CUtensorMap &tdo, const CUtensorMap &tdq,
+                         const BwdArgs &a, int grid, cudaStream_t stream) {
+  return causal ? launch_bwd_impl<D, true, F16>(tq, tk, tv, tdo, tdq, a, grid, stream)
+                : launch_bwd_impl<D, false, F16>(tq, tk, tv, tdo, tdq, a, grid, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(int d, bool causal, bool f16, const CUtensorMap &tq, const CUtensorMap &tk,
+                       const CUtensorMap &tv, const CUtensorMap &tdo, const CUtensorMap &tdq,
+                       const BwdArgs &a, int grid, cudaStream_t stream) {
+  if (d == 64)
+    return f16 ? launch_bwd_d<64, true>(causal, tq, tk, tv, tdo, tdq, a, grid, stream)
+               : launch_bwd_d<64, false>(causal, tq, tk, tv, tdo, tdq, a, grid, stream);
+  return f16 ? launch_bwd_d<128, true>(causal, tq, tk, tv, tdo, tdq, a, grid, stream)
+             : launch_bwd_d<128, false>(causal, tq, tk, tv, tdo, tdq, a, grid, stream);
+}
+
+cudaError_t launch_bwd_pre(int d, bool f16, const void *o, const void *dout, int B, int Nq,
+                           int Hq, const int64_t o_st[3], const int64_t do_st[3], float *dvec,
+                           float *dq_acc, cudaStream_t stream) {
+  const int64_t rows = static_cast<int64_t>(B) * Nq * Hq;
+  if (rows == 0) return cudaSuccess;
+  const int grid = grid_for(rows * 32, 256);
+  const uint16_t *op = reinterpret_cast<const uint16_t *>(o);
+  const uint16_t *dp = reinterpret_cast<const uint16_t *>(dout);
+#define FA_PRE(DD, FF)                                                                    \
+  bwd_pre_kernel<DD, FF><<<grid, 256, 0, stream>>>(op, dp, B, Nq, Hq, o_st[0], o_st[1],  \
+                                                   o_st[2], do_st[0], do_st[1], do_st[2], \
+                                                   dvec, dq_acc)
+  if (d == 64) {
+    if (f16) FA_PRE(64, true); else FA_PRE(64, false);
+  } else {
+    if (f16) FA_PRE(128, true); else FA_PRE(128, false);
+  }
+#undef FA_PRE
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_post(int d, bool f16, const float *dq_acc, float scale, void *dq, int B,
+                            int Nq, int Hq, const int64_t dq_st[3], cudaStream_t stream) {
+  const int64_t items = static_cast<int64_t>(B) * Nq * Hq * (d / 8);
+  if (items == 0) return cudaSuccess;
+  uint16_t *out = reinterpret_cast<uint16_t *>(dq);
+  if (f16)
+    bwd_post_kernel<true><<<grid_for(items, 256), 256, 0, stream>>>(dq_acc, scale, out, B, Nq,
+                                                                    Hq, d, dq_st[0], dq_st[1],
+                                                                    dq_st[2]);
+  else
+    bwd_post_kernel<false><<<grid_for(items, 256), 256, 0, stream>>>(dq_acc, scale, out, B, Nq,
+                                                                     Hq, d, dq_st[0], dq_st[1],
+                                                                     dq_st[2]);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_zero16(void *x, int B, int N, int H, int d, const int64_t st[3],
+                          cudaStream_t stream) {
+  const int64_t items = static_cast<int64_t>(B) * N * H * (d / 8);
+  if (items == 0) return cudaSuccess;
+  zero16_kernel<<<grid_for(items, 256), 256, 0, stream>>>(reinterpret_cast<uint16_t *>(x), B, N,
+                                                          H, d, st[0], st[1], st[2]);
+  return cudaGetLastError();
+}
+
+}  // namespace fa

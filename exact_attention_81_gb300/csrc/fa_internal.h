@@ -17,6 +17,7 @@ enum : unsigned int {
   DEVERR_BAD_CACHE_LEN = 8u,    // cache_seqlens outside [0, Lmax] (clamped)
   DEVERR_BAD_APPEND = 16u,      // no room for an appended row / position past the tables
   DEVERR_BAD_BLOCK_TABLE = 32u, // a block-table entry outside [0, num_pages)
+  DEVERR_BWD_TIMEOUT = 64u,     // a bounded wait in the backward kernel gave up
 };
 
 // Arguments of the fused prefill kernel (dense and varlen share it).
@@ -126,6 +127,39 @@ cudaError_t launch_combine(int d, bool f16, const float *o_part, const float *ls
                            const int *cache_len, int len_add, int B, int Hq, int Lmax, int chunk,
                            int maxch, int wl, int kalign, void *o, float *lse, unsigned int *err,
                            cudaStream_t stream);
+
+// Backward pass: main kernel arguments (one work unit = batch, kv head, 128-key block).
+struct BwdArgs {
+  const float *lse;           // [B, Hq, Nq] natural-log LSE of the forward pass
+  const float *dvec;          // [B, Hq, Nq] D = rowsum(dO * O)
+  void *dk, *dv;              // outputs [B, Nk, Hkv, d], element strides below
+  int64_t dk_sb, dk_sn, dk_sh, dv_sb, dv_sn, dv_sh;
+  int B, Nq, Nk, Hq, Hkv, group;
+  int kblocks;                // ceil(Nk / 128)
+  int num_units;              // kblocks * B * Hkv
+  float scale, scale_log2;
+  unsigned int *err;
+  unsigned long long timeout_ns;
+};
+
+// D = rowsum(dO * O) per query row and a zeroed fp32 dQ accumulator [B, Nq, Hq, d].
+cudaError_t launch_bwd_pre(int d, bool f16, const void *o, const void *dout, int B, int Nq,
+                           int Hq, const int64_t o_st[3], const int64_t do_st[3], float *dvec,
+                           float *dq_acc, cudaStream_t stream);
+
+// tq, tk, tv, tdo: 16-bit maps like the forward's; tdq: fp32 map of the dQ accumulator
+// (box 32 x 128 rows, 128-byte swizzle).
+cudaError_t launch_bwd(int d, bool causal, bool f16, const CUtensorMap &tq, const CUtensorMap &tk,
+                       const CUtensorMap &tv, const CUtensorMap &tdo, const CUtensorMap &tdq,
+                       const BwdArgs &a, int grid, cudaStream_t stream);
+
+// dQ = scale * accumulator, rounded to the element type, into a strided [B, Nq, Hq, d].
+cudaError_t launch_bwd_post(int d, bool f16, const float *dq_acc, float scale, void *dq, int B,
+                            int Nq, int Hq, const int64_t dq_st[3], cudaStream_t stream);
+
+// Zeroes a strided 16-bit [B, N, H, d] tensor.
+cudaError_t launch_zero16(void *x, int B, int N, int H, int d, const int64_t st[3],
+                          cudaStream_t stream);
 
 // Shared-memory bytes the kernels request (for host-side checks).
 int prefill_smem_bytes(int d);

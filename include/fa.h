@@ -254,6 +254,47 @@ fa_status fa_fwd_kvcache_noalloc(const void *q, const void *k_cache, const void 
                                  int num_splits, void *o, float *lse, cudaStream_t stream);
 
 /*
+ * Backward pass of fa_fwd (dense batched attention, causal or not, GQA), the gradients the
+ * flash-attention page describes (sections 2.3 and 4): the forward keeps q, k, v, out and
+ * softmax_lse; the backward recomputes P = exp(S * scale - LSE) block by block instead of
+ * storing it, runs parallel over key blocks with dK and dV kept on chip, and accumulates
+ * dQ across key blocks (in fp32, in the workspace).  For an upstream gradient dO:
+ *     D_i = rowsum(dO_i * O_i),  dS = P * (dO V^T - D),
+ *     dV = P^T dO,  dK = scale dS^T Q,  dQ = scale dS K
+ * (GQA: dK and dV of a key/value head sum over the query heads that read it).
+ *   q, o, dout, dq : [B, Nq, Hq, d] (strides as in fa_fwd_params)
+ *   k, v, dk, dv   : [B, Nk, Hkv, d]
+ *   lse            : [B, Hq, Nq] fp32, the LSE fa_fwd wrote for the same q, k, v
+ *   workspace      : DEVICE, fa_bwd_workspace_size(B, Nq, Hq, d) bytes, 256-byte aligned,
+ *                    owned by the caller (the fp32 dQ accumulator and the D vector)
+ * All 16-bit tensors share the element type `dtype`; P and dS enter the tensor cores as
+ * 16-bit values, every product is accumulated in fp32.  dQ sums key blocks in an
+ * unspecified order (two calls may differ in the last bits of dQ); dK and dV do not.
+ * The score modifiers (fa_score_mod) have no backward here.  Nk = 0 gives dQ = 0;
+ * Nq = 0 gives dK = dV = 0; B = 0 is a no-op.
+ */
+typedef struct fa_bwd_params {
+    const void *q, *k, *v, *o, *dout;
+    const float *lse;
+    void *dq, *dk, *dv;
+    int B, Nq, Nk, Hq, Hkv, d;
+    int64_t q_strides[3], k_strides[3], v_strides[3], o_strides[3], do_strides[3];
+    int64_t dq_strides[3], dk_strides[3], dv_strides[3];
+    float scale;
+    int causal;
+    int dtype;
+    void *workspace;
+    size_t workspace_bytes;
+} fa_bwd_params;
+
+size_t fa_bwd_workspace_size(int B, int Nq, int Hq, int d);
+
+fa_status fa_bwd(const fa_bwd_params *p, cudaStream_t stream);
+
+/* sizeof(fa_bwd_params), for bindings that check their struct layout. */
+size_t fa_bwd_params_size(void);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's error word.
  * Returns FA_OK when no kernel recorded a fault since the last read, FA_ERR_TIMEOUT when a
  * bounded device-side wait gave up (the kernel then stopped early and its outputs are

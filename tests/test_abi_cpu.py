@@ -31,8 +31,41 @@ def test_header_symbols_exported(lib):
 
 
 def test_struct_layout(lib):
-    from exact_attention_81_gb300._binding import FwdParams
+    from exact_attention_81_gb300._binding import BwdParams, FwdParams
     assert lib.fa_fwd_params_size() == ctypes.sizeof(FwdParams)
+    assert lib.fa_bwd_params_size() == ctypes.sizeof(BwdParams)
+
+
+def _bwd_params(**kw):
+    from exact_attention_81_gb300._binding import BwdParams
+    p = BwdParams()
+    for name in ("q", "k", "v", "o", "dout", "lse", "dq", "dk", "dv"):
+        setattr(p, name, 4096)
+    p.B, p.Nq, p.Nk, p.Hq, p.Hkv, p.d = 1, 128, 128, 4, 2, 128
+    for name in ("q_strides", "o_strides", "do_strides", "dq_strides"):
+        getattr(p, name)[:] = [128 * 4 * 128, 4 * 128, 128]
+    for name in ("k_strides", "v_strides", "dk_strides", "dv_strides"):
+        getattr(p, name)[:] = [128 * 2 * 128, 2 * 128, 128]
+    p.scale, p.causal, p.dtype = 0.088, 1, 0
+    p.workspace, p.workspace_bytes = 4096, 1 << 30
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+@pytest.mark.parametrize("change,status", [
+    ({"d": 96}, 2), ({"dtype": 3}, 2), ({"Hkv": 3}, 1), ({"scale": 0.0}, 1), ({"dout": None}, 1),
+    ({"lse": None}, 1), ({"dk": 4100}, 1), ({"workspace": None}, 4), ({"workspace_bytes": 16}, 4),
+    ({"workspace": 4096 + 64}, 4), ({"B": 0}, 0),
+])
+def test_bwd_rejects_bad_arguments(lib, change, status):
+    assert lib.fa_bwd(ctypes.byref(_bwd_params(**change)), None) == status
+
+
+def test_bwd_workspace_size(lib):
+    ws = lib.fa_bwd_workspace_size
+    assert ws(2, 1000, 4, 128) == 2 * 1000 * 4 * 128 * 4 + ((2 * 4 * 1000 * 4 + 255) // 256) * 256
+    assert ws(0, 10, 4, 128) == 0
 
 
 def _params(**kw):

@@ -1,0 +1,111 @@
+"""GPU parity of the backward pass (fa_bwd) against the fp64 oracle.
+
+The forward bounds have no stated counterpart for gradients, so the bar is the pages' own
+("flash-attention", section 5, tests: the error of the fused kernel is at most twice the
+error of a PyTorch baseline run in the input precision): for each of dQ, dK and dV,
+    max |g_gpu - g_oracle| <= 2 * max |g_baseline - g_oracle| + 1e-4,
+where the baseline is the same attention written with torch ops on the CPU in bf16 / fp16
+(matmuls in the input type, softmax in fp32 then rounded, as upstream's reference does)
+and differentiated by autograd.  Query rows that see no key must get dQ = 0 exactly.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.oracle as ORACLE
+from exact_attention_81_gb300 import FA_OK, fa_bwd, fa_fwd, get_last_device_error
+from exact_attention_81_gb300.inputs import WORKLOADS, bf16_normal, dense_inputs
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _mask(Nq, Nk):
+    i = torch.arange(Nq)[:, None]
+    j = torch.arange(Nk)[None, :]
+    return j <= i + (Nk - Nq)
+
+
+def _baseline(q, k, v, do, scale, causal):
+    """PyTorch attention in the input precision on the CPU, differentiated by autograd."""
+    dt = q.dtype
+    Hq, Hkv = q.shape[2], k.shape[2]
+    G = Hq // Hkv
+    qq = q.cpu().permute(0, 2, 1, 3).detach().requires_grad_()
+    kk = k.cpu().permute(0, 2, 1, 3).detach().requires_grad_()
+    vv = v.cpu().permute(0, 2, 1, 3).detach().requires_grad_()
+    s = torch.matmul(qq, kk.repeat_interleave(G, 1).transpose(-1, -2)) * scale
+    if causal:
+        s = s.masked_fill(~_mask(q.shape[1], k.shape[1]), float("-inf"))
+    p = torch.softmax(s.float(), dim=-1).nan_to_num(0.0).to(dt)
+    o = torch.matmul(p, vv.repeat_interleave(G, 1))
+    o.backward(do.cpu().permute(0, 2, 1, 3))
+    return (qq.grad.permute(0, 2, 1, 3), kk.grad.permute(0, 2, 1, 3),
+            vv.grad.permute(0, 2, 1, 3))
+
+
+def _check(q, k, v, do, scale, causal, what):
+    o, lse = fa_fwd(q, k, v, causal=causal, scale=scale)
+    dq, dk, dv = fa_bwd(q, k, v, o, lse, do, causal=causal, scale=scale)
+    assert get_last_device_error() == FA_OK
+    ref = ORACLE.attention_bwd(q.cpu(), k.cpu(), v.cpu(), do.cpu(), scale, causal)[:3]
+    base = _baseline(q, k, v, do, scale, causal)
+    report = {}
+    for name, g, r, b in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref, base):
+        g = g.double().cpu().numpy()
+        b = b.double().numpy()
+        assert np.all(np.isfinite(g)), f"{what}: non-finite {name}"
+        e_gpu = float(np.abs(g - r).max())
+        e_base = float(np.abs(b - r).max())
+        report[name] = (e_gpu, e_base)
+        assert e_gpu <= 2 * e_base + 1e-4, \
+            f"{what}: max|d{name}| = {e_gpu:.3e} > 2 x baseline {e_base:.3e}"
+    return report, (dq, dk, dv)
+
+
+@pytest.mark.parametrize("case", [
+    # B, Nq, Nk, Hq, Hkv, d, causal, dtype
+    (1, 128, 128, 1, 1, 128, False, torch.bfloat16),
+    (2, 256, 256, 4, 2, 128, True, torch.bfloat16),
+    (1, 300, 300, 2, 2, 64, True, torch.bfloat16),
+    (1, 200, 517, 4, 1, 128, True, torch.bfloat16),
+    (2, 384, 384, 8, 2, 128, False, torch.float16),
+    (1, 129, 1000, 2, 2, 128, False, torch.bfloat16),
+    (1, 640, 640, 2, 1, 64, False, torch.float16),
+])
+def test_backward(case):
+    B, Nq, Nk, Hq, Hkv, d, causal, dt = case
+    q, k, v = dense_inputs(B, Nq, Nk, Hq, Hkv, d, seed=700 + Nq + d, device=DEV, dtype=dt)
+    do = bf16_normal((B, Nq, Hq, d), seed=710 + Nq, device=DEV, dtype=dt)
+    _check(q, k, v, do, float(np.float32(1 / math.sqrt(d))), causal, f"bwd {case}")
+
+
+def test_backward_rows_without_keys():
+    """Causal with Nq > Nk (bottom-right): query rows i < Nq - Nk see no key, their dQ is
+    exactly 0 and they add nothing to dK and dV."""
+    B, Nq, Nk, H, d = 1, 700, 130, 2, 128
+    q, k, v = dense_inputs(B, Nq, Nk, H, H, d, seed=722, device=DEV)
+    do = bf16_normal((B, Nq, H, d), seed=723, device=DEV)
+    _, (dq, dk, dv) = _check(q, k, v, do, 0.088, True, "bwd Nq > Nk")
+    assert torch.all(dq[:, :Nq - Nk] == 0), "rows that see no key must have dQ = 0"
+
+
+def test_backward_full_size_one_head():
+    """The causal 8k workload: the gradients of head (0, 0), whose dK / dV depend only on
+    that head (no GQA), against the oracle and the baseline on that head alone."""
+    w = WORKLOADS["causal8k"]
+    q, k, v = dense_inputs(w.B, w.Nq, w.Nk, w.Hq, w.Hkv, w.d, seed=w.seed, device=DEV)
+    do = bf16_normal((w.B, w.Nq, w.Hq, w.d), seed=w.seed + 9, device=DEV)
+    o, lse = fa_fwd(q, k, v, causal=True)
+    dq, dk, dv = fa_bwd(q, k, v, o, lse, do, causal=True)
+    assert get_last_device_error() == FA_OK
+    sl = (slice(0, 1), slice(None), slice(0, 1))
+    q1, k1, v1, do1 = (t[sl].contiguous() for t in (q, k, v, do))
+    ref = ORACLE.attention_bwd(q1.cpu(), k1.cpu(), v1.cpu(), do1.cpu(), w.scale, True)[:3]
+    base = _baseline(q1, k1, v1, do1, w.scale, True)
+    for name, g, r, b in zip(("dQ", "dK", "dV"), (dq[sl], dk[sl], dv[sl]), ref, base):
+        e_gpu = float(np.abs(g.double().cpu().numpy() - r).max())
+        e_base = float(np.abs(b.double().numpy() - r).max())
+        assert e_gpu <= 2 * e_base + 1e-4, f"causal8k {name}: {e_gpu:.3e} vs {e_base:.3e}"

@@ -7,9 +7,9 @@ left clean)."""
 import pytest
 import torch
 
-from exact_attention_81_gb300 import (FA_ERR_TIMEOUT, FA_OK, fa_fwd, fa_fwd_kvcache,
+from exact_attention_81_gb300 import (FA_ERR_TIMEOUT, FA_OK, fa_bwd, fa_fwd, fa_fwd_kvcache,
                                       get_last_device_error, set_wait_timeout_ns)
-from exact_attention_81_gb300.inputs import dense_inputs, kvcache_inputs
+from exact_attention_81_gb300.inputs import bf16_normal, dense_inputs, kvcache_inputs
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -48,3 +48,20 @@ def test_decode_wait_timeout_reports_and_recovers():
     o2, l2 = fa_fwd_kvcache(q, kc, vc, lens)
     assert get_last_device_error() == FA_OK
     assert torch.equal(o2, o_ok) and torch.equal(l2, l_ok)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_wait_timeout_reports_and_recovers(causal):
+    q, k, v = dense_inputs(2, 700, 700, 4, 2, 128, seed=73, device=DEV)
+    do = bf16_normal((2, 700, 4, 128), seed=74, device=DEV)
+    o, lse = fa_fwd(q, k, v, causal=causal)
+    g_ok = fa_bwd(q, k, v, o, lse, do, causal=causal)
+    assert get_last_device_error() == FA_OK
+    st = _with_tiny_timeout(lambda: fa_bwd(q, k, v, o, lse, do, causal=causal))
+    assert st == FA_ERR_TIMEOUT
+    g2 = fa_bwd(q, k, v, o, lse, do, causal=causal)
+    assert get_last_device_error() == FA_OK
+    # dK and dV are written by one key block each: bit-identical; dQ sums key blocks in
+    # an unspecified order
+    assert torch.equal(g2[1], g_ok[1]) and torch.equal(g2[2], g_ok[2])
+    assert (g2[0].float() - g_ok[0].float()).abs().max().item() <= 1e-2
