@@ -17,16 +17,23 @@
 // Keys are the MMA rows (TMEM lanes) of S^T, dP^T, dV and dK, so the dK and dV
 // accumulators stay in TMEM across the unit.
 //
-// Roles (192 threads):
-//   warps 0-3  P^T and dS^T (thread = key row), the dQ epilogue (thread = query row) and
-//              the dK / dV epilogue at the end of a unit
-//   warp  4    producer: K, V (once per unit), Q, dO (per step) by TMA; LSE and D vectors
-//   warp  5    TMEM allocator and MMA issuer (one lane)
+// Roles (384 threads, three warpgroups):
+//   warps 0-7  P^T and dS^T (thread = key row; warps 0-3 take queries 0-63 of the step,
+//              warps 4-7 queries 64-127), the dQ epilogue (thread = query row, half of the
+//              d columns each) and the dK / dV epilogue at the end of a unit
+//   warp  8    producer: K, V (once per unit), Q, dO (per step) by TMA; LSE and D vectors
+//   warp  9    TMEM allocator and MMA issuer (one lane)
+//   warps 10-11 idle: the third warpgroup gives registers back (setmaxnreg) so that the
+//              compute warps hold a 64-query row of P and its dS without spilling
 // TMEM: S^T [0,128), dP^T [128,256) (then dS^T, then dQ), dV [256,256+d), dK [384,384+d).
-// P^T and dS^T are written back as packed 16-bit pairs over the first 64 columns of their
-// fp32 sources and feed the dV and dK MMAs from TMEM; dS is also written to shared memory
-// (queries contiguous, the MN-major A operand of the dQ MMA).  Each step's dQ tile goes
-// through shared memory to a TMA bulk reduce-add into an fp32 accumulator.
+// P^T and dS^T are written back as packed 16-bit pairs, each query half over the first
+// columns of its own fp32 source (queries 0-63 at +0, 64-127 at +64), and feed the dV and
+// dK MMAs from TMEM; dS is also written to shared memory (queries contiguous, the MN-major
+// A operand of the dQ MMA).  Each step's dQ tile goes through shared memory to a TMA bulk
+// reduce-add into an fp32 accumulator.
+// Per step the MMA issuer runs S^T (as soon as Q has landed), dP^T (once dO has landed
+// and the previous dQ has been read), then dK, dV and dQ: dK and dV release Q and dO so
+// that the next step's loads overlap the dQ product and its epilogue.
 #include <cmath>
 
 #include "fa_internal.h"
@@ -37,10 +44,12 @@ namespace {
 
 constexpr int BKEY = 128;         // keys per unit
 constexpr int BQ = 128;           // queries per step
-constexpr int NTHREADS = 192;
-constexpr int NCOMPUTE = 128;
-constexpr int PRODUCER_WARP = 4;
-constexpr int MMA_WARP = 5;
+constexpr int NTHREADS = 384;
+constexpr int NCOMPUTE = 256;
+constexpr int COMPUTE_REGS = 216;  // 2 x 128 threads x 216
+constexpr int OTHER_REGS = 72;     //   + 128 threads x 72 = 384 threads x 168 at launch
+constexpr int PRODUCER_WARP = 8;
+constexpr int MMA_WARP = 9;
 constexpr int BOX = 128 * 128;    // one 128-byte-swizzled box: 128 rows x 128 bytes
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t T_ST = 0, T_DP = 128, T_DV = 256, T_DK = 384;
@@ -65,9 +74,9 @@ struct BCfg {
 };
 
 struct BBars {
-  uint64_t kv_full, kv_empty, q_full, q_empty, vec_full, vec_empty;
-  uint64_t s_full, p_ready, dq_full, dq_empty, acc_full, acc_empty, mma_done;
-  uint64_t cgrp;  // group barrier of the 128 compute threads (bounded wait)
+  uint64_t kv_full, kv_empty, q_full, q_empty, do_full, do_empty, vec_full, vec_empty;
+  uint64_t st_full, dp_full, p_ready, dq_full, dq_empty, acc_full, acc_empty, mma_done;
+  uint64_t cgrp;  // group barrier of the compute threads (bounded wait)
   uint32_t tmem_base;
   int abort;
 };
@@ -110,7 +119,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const 
   return __all_sync(0xffffffffu, ok);
 }
 
-// Barrier among the 128 compute threads, built on an mbarrier so that the wait is bounded:
+// Barrier among the compute threads, built on an mbarrier so that the wait is bounded:
 // a warp that has given up never leaves the others blocked.
 __device__ __forceinline__ bool group_sync(uint64_t *bar, uint32_t &phase, const WaitCtl &wc) {
   mbar_arrive(bar);
@@ -130,6 +139,12 @@ __device__ __forceinline__ void issue_kmajor(uint32_t d_tmem, uint32_t a_smem, u
   }
 }
 
+// TMEM column of the packed pair holding queries (2c, 2c+1): each 64-query half sits at the
+// start of its own 64 fp32 source columns.
+__host__ __device__ constexpr uint32_t packed_col(int query) {
+  return static_cast<uint32_t>((query < 64 ? 0 : 64) + (query & 63) / 2);
+}
+
 // D[128 keys x D] (+)= A[128 keys x 128 queries] (TMEM, packed pairs) * B[128 queries x D]
 // (MN-major tile: rows = queries, D contiguous).  dV and dK.
 template <int D, bool F16>
@@ -137,7 +152,7 @@ __device__ __forceinline__ void issue_acc(uint32_t d_tmem, uint32_t a_tmem, uint
                                           bool accumulate) {
 #pragma unroll
   for (int kk = 0; kk < BQ / 16; ++kk)
-    mma_bf16_ts(d_tmem, a_tmem + static_cast<uint32_t>(kk * 8),
+    mma_bf16_ts(d_tmem, a_tmem + packed_col(kk * 16),
                 sw128_desc(b_smem + static_cast<uint32_t>(kk * 16 * 128), BOX, 1024),
                 BCfg<D, F16>::IDESC_ACC, (accumulate || kk > 0) ? 1u : 0u);
 }
@@ -183,12 +198,17 @@ __device__ void bwd_producer(const BwdArgs &a, const CUtensorMap *tq, const CUte
       bstep(a, w, t, h, i);
       if (q_n > 0 && !warp_wait(&bars->q_empty, (q_n - 1) & 1u, wc)) goto out;
       if (lane == 0) {
-        mbar_arrive_expect_tx(&bars->q_full, 2 * C::TILE);
+        mbar_arrive_expect_tx(&bars->q_full, C::TILE);
 #pragma unroll
-        for (int c = 0; c < C::KCH; ++c) {
+        for (int c = 0; c < C::KCH; ++c)
           tma_load_4d(smem + C::Q_OFF + c * BOX, tq, &bars->q_full, c * 64, h, i * BQ, w.b);
-          tma_load_4d(smem + C::DO_OFF + c * BOX, tdo, &bars->q_full, c * 64, h, i * BQ, w.b);
-        }
+      }
+      if (q_n > 0 && !warp_wait(&bars->do_empty, (q_n - 1) & 1u, wc)) goto out;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars->do_full, C::TILE);
+#pragma unroll
+        for (int c = 0; c < C::KCH; ++c)
+          tma_load_4d(smem + C::DO_OFF + c * BOX, tdo, &bars->do_full, c * 64, h, i * BQ, w.b);
       }
       // LSE (log2 domain; rows past Nq or with no visible key give P = 0) and D.
       if (q_n > 0 && !warp_wait(&bars->vec_empty, (q_n - 1) & 1u, wc)) goto out;
@@ -215,6 +235,7 @@ out:
   if (lane == 0) {
     if (kv_n > 0) mbar_wait_teardown(&bars->kv_full, (kv_n - 1) & 1u, 1000000000ull);
     if (q_n > 0) mbar_wait_teardown(&bars->q_full, (q_n - 1) & 1u, 1000000000ull);
+    if (q_n > 0) mbar_wait_teardown(&bars->do_full, (q_n - 1) & 1u, 1000000000ull);
   }
 }
 
@@ -239,17 +260,20 @@ __device__ void bwd_mma(const BwdArgs &a, uint8_t *smem, BBars *bars, uint32_t t
       if (!mbar_wait(&bars->q_full, it & 1u, wc)) goto out;
       tc_fence_after();
       issue_kmajor<D, F16>(tmem + T_ST, sK, sQ);                  // S^T = K Q^T
+      mma_commit(&bars->st_full);
+      if (!mbar_wait(&bars->do_full, it & 1u, wc)) goto out;
       // dP^T overwrites the previous step's dQ: wait until the epilogue has read it.
       if (it > 0 && !mbar_wait(&bars->dq_empty, (it - 1) & 1u, wc)) goto out;
       tc_fence_after();
       issue_kmajor<D, F16>(tmem + T_DP, sV, sDO);                 // dP^T = V dO^T
-      mma_commit(&bars->s_full);
+      mma_commit(&bars->dp_full);
       if (!mbar_wait(&bars->p_ready, it & 1u, wc)) goto out;
       tc_fence_after();
-      issue_acc<D, F16>(tmem + T_DV, tmem + T_ST, sDO, t > 0);    // dV += P^T dO
       issue_acc<D, F16>(tmem + T_DK, tmem + T_DP, sQ, t > 0);     // dK += dS^T Q
-      issue_dq<D, F16>(tmem + T_DP, sDS, sK);                     // dQ = dS K
       mma_commit(&bars->q_empty);
+      issue_acc<D, F16>(tmem + T_DV, tmem + T_ST, sDO, t > 0);    // dV += P^T dO
+      mma_commit(&bars->do_empty);
+      issue_dq<D, F16>(tmem + T_DP, sDS, sK);                     // dQ = dS K
       mma_commit(&bars->dq_full);
       ++it;
     }
@@ -263,15 +287,16 @@ out:
 }
 
 // ------------------------------------------------------------------------------------
-// Compute warps.
+// Compute warps: warp w handles TMEM lanes 32 (w % 4) .. +31 and column half w / 4.
 
 template <int D, bool CAUSAL, bool F16>
 __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *smem, BBars *bars,
                             uint32_t tmem, const WaitCtl &wc, int tid) {
   using C = BCfg<D, F16>;
   const int warp = tid >> 5;
-  const int r = tid;  // TMEM lane: key row of S^T / dP^T / dV / dK, query row of dQ
-  const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+  const int half = warp >> 2;                 // query half (P, dS) / d half (dQ, dK, dV)
+  const int r = (warp & 3) * 32 + (tid & 31); // TMEM lane: key row, or query row for dQ
+  const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
   const float *lse2 = reinterpret_cast<const float *>(smem + C::VEC_OFF);
   const float *dvec = lse2 + BQ;
   uint8_t *ds_s = smem + C::DS_OFF;
@@ -288,7 +313,7 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
     if (w.nit == 0) {  // no query sees these keys: zero gradients
       if (key < a.Nk) {
 #pragma unroll
-        for (int v = 0; v < D / 8; ++v) {
+        for (int v = half * (D / 16); v < (half + 1) * (D / 16); ++v) {
           reinterpret_cast<uint4 *>(dkrow)[v] = make_uint4(0u, 0u, 0u, 0u);
           reinterpret_cast<uint4 *>(dvrow)[v] = make_uint4(0u, 0u, 0u, 0u);
         }
@@ -298,39 +323,49 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
     for (int t = 0; t < w.nit; ++t) {
       int h, i;
       bstep(a, w, t, h, i);
-      if (!warp_wait(&bars->vec_full, it & 1u, wc)) return;
-      if (!warp_wait(&bars->s_full, it & 1u, wc)) return;
-      tc_fence_after();
-      // P^T and dS^T of this key row, 32 queries at a time.
       const int q0 = i * BQ;
       const bool full = !CAUSAL || (w.j * BKEY + BKEY - 1 <= q0 + off);  // no pair masked
-#pragma unroll 1
-      for (int c = 0; c < BQ / 32; ++c) {
-        uint32_t sr[32], dr[32];
-        tmem_ld_x32(tmem + lane_off + T_ST + c * 32, sr);
-        tmem_ld_x32(tmem + lane_off + T_DP + c * 32, dr);
-        uint32_t pp[16], dd[16];
+      // P^T of this key row for the 64 queries of this half (kept in registers for dS).
+      if (!warp_wait(&bars->vec_full, it & 1u, wc)) return;
+      if (!warp_wait(&bars->st_full, it & 1u, wc)) return;
+      tc_fence_after();
+      float p[64];
+#pragma unroll
+      for (int c2 = 0; c2 < 2; ++c2) {
+        const int qc = half * 64 + c2 * 32;  // first query of the chunk
+        uint32_t sr[32];
+        tmem_ld_x32(tmem + lane_off + T_ST + qc, sr);
+        uint32_t pp[16];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int qi = qc + e;
+          const bool vis = key < a.Nk && (full || key <= q0 + qi + off);
+          const float pv = ex2_approx(fmaf(__uint_as_float(sr[e]), a.scale_log2, -lse2[qi]));
+          p[c2 * 32 + e] = vis ? pv : 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < 16; ++e) pp[e] = pack2<F16>(p[c2 * 32 + 2 * e], p[c2 * 32 + 2 * e + 1]);
+        tmem_st_x16(tmem + lane_off + T_ST + packed_col(qc), pp);
+      }
+      // dS^T = P^T (dP^T - D): to TMEM (dK) and to shared memory with queries contiguous (dQ).
+      if (!warp_wait(&bars->dp_full, it & 1u, wc)) return;
+      tc_fence_after();
+#pragma unroll
+      for (int c2 = 0; c2 < 2; ++c2) {
+        const int qc = half * 64 + c2 * 32;
+        uint32_t dr[32], dd[16];
+        tmem_ld_x32(tmem + lane_off + T_DP + qc, dr);
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          float p[2], ds[2];
-#pragma unroll
-          for (int x = 0; x < 2; ++x) {
-            const int qi = c * 32 + e + x;
-            const bool vis = key < a.Nk && (full || key <= q0 + qi + off);
-            const float pv = ex2_approx(fmaf(__uint_as_float(sr[e + x]), a.scale_log2, -lse2[qi]));
-            p[x] = vis ? pv : 0.f;
-            ds[x] = p[x] * (__uint_as_float(dr[e + x]) - dvec[qi]);
-          }
-          pp[e / 2] = pack2<F16>(p[0], p[1]);
-          dd[e / 2] = pack2<F16>(ds[0], ds[1]);
+          const float d0 = p[c2 * 32 + e] * (__uint_as_float(dr[e]) - dvec[qc + e]);
+          const float d1 = p[c2 * 32 + e + 1] * (__uint_as_float(dr[e + 1]) - dvec[qc + e + 1]);
+          dd[e / 2] = pack2<F16>(d0, d1);
         }
-        tmem_st_x16(tmem + lane_off + T_ST + c * 16, pp);
-        tmem_st_x16(tmem + lane_off + T_DP + c * 16, dd);
-        // dS to shared memory: row = key, queries contiguous (box c/2, granules (c%2)*4..+3)
-        uint8_t *box = ds_s + (c >> 1) * BOX + r * 128;
+        tmem_st_x16(tmem + lane_off + T_DP + packed_col(qc), dd);
+        uint8_t *box = ds_s + half * BOX + r * 128;  // box = query half
 #pragma unroll
         for (int gi = 0; gi < 4; ++gi) {
-          const int gran = (c & 1) * 4 + gi;
+          const int gran = c2 * 4 + gi;
           *reinterpret_cast<uint4 *>(box + ((gran ^ (r & 7)) << 4)) =
               make_uint4(dd[4 * gi], dd[4 * gi + 1], dd[4 * gi + 2], dd[4 * gi + 3]);
         }
@@ -345,8 +380,9 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
       tc_fence_after();
       if (tid == 0) bulk_wait_read();  // the previous reduction has read the staging tile
       if (!group_sync(&bars->cgrp, grp, wc)) return;
-#pragma unroll 1
-      for (int cc = 0; cc < D / 32; ++cc) {
+#pragma unroll
+      for (int c2 = 0; c2 < D / 64; ++c2) {
+        const int cc = half * (D / 64) + c2;  // 32-column box of dQ
         uint32_t qr[32];
         tmem_ld_x32(tmem + lane_off + T_DP + cc * 32, qr);
         uint8_t *box = dq_s + cc * BOX + r * 128;
@@ -367,11 +403,12 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
       }
       ++it;
     }
-    // Unit end: dV and scale * dK of this key row -> global memory.
+    // Unit end: dV and scale * dK of this key row (this warp's half of d) -> global memory.
     if (!warp_wait(&bars->acc_full, acc_n & 1u, wc)) return;
     tc_fence_after();
-#pragma unroll 1
-    for (int cc = 0; cc < D / 32; ++cc) {
+#pragma unroll
+    for (int c2 = 0; c2 < D / 64; ++c2) {
+      const int cc = half * (D / 64) + c2;
       uint32_t vr[32], kr[32];
       tmem_ld_x32(tmem + lane_off + T_DV + cc * 32, vr);
       tmem_ld_x32(tmem + lane_off + T_DK + cc * 32, kr);
@@ -415,9 +452,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     mbar_init(&bars->kv_empty, 1);
     mbar_init(&bars->q_full, 1);
     mbar_init(&bars->q_empty, 1);
+    mbar_init(&bars->do_full, 1);
+    mbar_init(&bars->do_empty, 1);
     mbar_init(&bars->vec_full, 32);
     mbar_init(&bars->vec_empty, NCOMPUTE);
-    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->st_full, 1);
+    mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->p_ready, NCOMPUTE);
     mbar_init(&bars->dq_full, 1);
     mbar_init(&bars->dq_empty, NCOMPUTE);
@@ -444,20 +484,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
   const WaitCtl wc{&bars->abort, a.err, a.timeout_ns, DEVERR_BWD_TIMEOUT};
+  // Each register-split branch ends on its own; the two meet at a named barrier before
+  // TMEM is released.
   if (warp < PRODUCER_WARP) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(COMPUTE_REGS));
     bwd_compute<D, CAUSAL, F16>(a, &tdq, smem, bars, tmem, wc, tid);
     if (tid == 0) bulk_wait_all();  // every dQ reduction has landed
-  } else if (warp == PRODUCER_WARP) {
-    bwd_producer<D, CAUSAL, F16>(a, &tq, &tk, &tv, &tdo, smem, bars, wc, lane);
-  } else if (lane == 0) {
-    bwd_mma<D, CAUSAL, F16>(a, smem, bars, tmem, wc);
-  }
-  __syncwarp();
-  tc_fence_before();
-  __syncthreads();
-  if (warp == MMA_WARP) {
-    tc_fence_after();
-    tmem_dealloc(tmem, TMEM_COLS);
+    __syncwarp();
+    tc_fence_before();
+    named_barrier(1, NTHREADS);
+  } else {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(OTHER_REGS));
+    if (warp == PRODUCER_WARP) {
+      bwd_producer<D, CAUSAL, F16>(a, &tq, &tk, &tv, &tdo, smem, bars, wc, lane);
+    } else if (warp == MMA_WARP && lane == 0) {
+      bwd_mma<D, CAUSAL, F16>(a, smem, bars, tmem, wc);
+    }
+    __syncwarp();
+    tc_fence_before();
+    named_barrier(1, NTHREADS);
+    if (warp == MMA_WARP) {
+      tc_fence_after();
+      tmem_dealloc(tmem, TMEM_COLS);
+    }
   }
 }
 
