@@ -46,8 +46,8 @@ constexpr int BKEY = 128;         // keys per unit
 constexpr int BQ = 128;           // queries per step
 constexpr int NTHREADS = 384;
 constexpr int NCOMPUTE = 256;
-constexpr int COMPUTE_REGS = 216;  // 2 x 128 threads x 216
-constexpr int OTHER_REGS = 72;     //   + 128 threads x 72 = 384 threads x 168 at launch
+constexpr int COMPUTE_REGS = 200;  // 2 x 128 threads x 200
+constexpr int OTHER_REGS = 96;     //   + 128 threads x 96 <= 384 threads x 168 at launch
 constexpr int PRODUCER_WARP = 8;
 constexpr int MMA_WARP = 9;
 constexpr int BOX = 128 * 128;    // one 128-byte-swizzled box: 128 rows x 128 bytes
@@ -325,42 +325,39 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
       bstep(a, w, t, h, i);
       const int q0 = i * BQ;
       const bool full = !CAUSAL || (w.j * BKEY + BKEY - 1 <= q0 + off);  // no pair masked
-      // P^T of this key row for the 64 queries of this half (kept in registers for dS).
+      // P^T and dS^T = P^T (dP^T - D) of this key row for the 64 queries of this half,
+      // 32 at a time: P^T and dS^T to TMEM (dV, dK), dS to shared memory with queries
+      // contiguous (dQ).
       if (!warp_wait(&bars->vec_full, it & 1u, wc)) return;
       if (!warp_wait(&bars->st_full, it & 1u, wc)) return;
-      tc_fence_after();
-      float p[64];
-#pragma unroll
-      for (int c2 = 0; c2 < 2; ++c2) {
-        const int qc = half * 64 + c2 * 32;  // first query of the chunk
-        uint32_t sr[32];
-        tmem_ld_x32(tmem + lane_off + T_ST + qc, sr);
-        uint32_t pp[16];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int qi = qc + e;
-          const bool vis = key < a.Nk && (full || key <= q0 + qi + off);
-          const float pv = ex2_approx(fmaf(__uint_as_float(sr[e]), a.scale_log2, -lse2[qi]));
-          p[c2 * 32 + e] = vis ? pv : 0.f;
-        }
-#pragma unroll
-        for (int e = 0; e < 16; ++e) pp[e] = pack2<F16>(p[c2 * 32 + 2 * e], p[c2 * 32 + 2 * e + 1]);
-        tmem_st_x16(tmem + lane_off + T_ST + packed_col(qc), pp);
-      }
-      // dS^T = P^T (dP^T - D): to TMEM (dK) and to shared memory with queries contiguous (dQ).
       if (!warp_wait(&bars->dp_full, it & 1u, wc)) return;
       tc_fence_after();
-#pragma unroll
+#pragma unroll 1
       for (int c2 = 0; c2 < 2; ++c2) {
-        const int qc = half * 64 + c2 * 32;
-        uint32_t dr[32], dd[16];
-        tmem_ld_x32(tmem + lane_off + T_DP + qc, dr);
+        const int qc = half * 64 + c2 * 32;  // first query of the chunk
+        uint32_t sr[32], dr[32];
+        tmem_ld_2x32(tmem + lane_off + T_ST + qc, tmem + lane_off + T_DP + qc, sr, dr);
+        uint32_t pp[16], dd[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float d0 = p[c2 * 32 + e] * (__uint_as_float(dr[e]) - dvec[qc + e]);
-          const float d1 = p[c2 * 32 + e + 1] * (__uint_as_float(dr[e + 1]) - dvec[qc + e + 1]);
-          dd[e / 2] = pack2<F16>(d0, d1);
+        for (int e4 = 0; e4 < 32; e4 += 4) {
+          const float4 l4 = *reinterpret_cast<const float4 *>(lse2 + qc + e4);
+          const float4 d4 = *reinterpret_cast<const float4 *>(dvec + qc + e4);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
+          float p[4], ds[4];
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            const int qi = qc + e4 + x;
+            const bool vis = key < a.Nk && (full || key <= q0 + qi + off);
+            const float pv = ex2_approx(fmaf(__uint_as_float(sr[e4 + x]), a.scale_log2, -lv[x]));
+            p[x] = vis ? pv : 0.f;
+            ds[x] = p[x] * (__uint_as_float(dr[e4 + x]) - dv[x]);
+          }
+          pp[e4 / 2] = pack2<F16>(p[0], p[1]);
+          pp[e4 / 2 + 1] = pack2<F16>(p[2], p[3]);
+          dd[e4 / 2] = pack2<F16>(ds[0], ds[1]);
+          dd[e4 / 2 + 1] = pack2<F16>(ds[2], ds[3]);
         }
+        tmem_st_x16(tmem + lane_off + T_ST + packed_col(qc), pp);
         tmem_st_x16(tmem + lane_off + T_DP + packed_col(qc), dd);
         uint8_t *box = ds_s + half * BOX + r * 128;  // box = query half
 #pragma unroll
