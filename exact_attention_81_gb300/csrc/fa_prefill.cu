@@ -55,8 +55,8 @@ constexpr int NTHREADS = 384;
 constexpr int PRODUCER_WARP = 8;
 constexpr int MMA_WARP = 9;
 constexpr int SCHED_DEPTH = 4;      // tiles in flight between the scheduler and the roles
-constexpr int SOFTMAX_REGS = 216;   // 2 x 128 threads x 216
-constexpr int OTHER_REGS = 72;      //   + 128 threads x 72 = 384 threads x 168 at launch
+constexpr int SOFTMAX_REGS = 200;   // 2 x 128 threads x 200
+constexpr int OTHER_REGS = 104;     //   + 128 threads x 104 = 384 threads x 168 at launch
 constexpr int NUM_SCHED_SLOTS = 256;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int BOX_BYTES = 128 * 128;  // one TMA box: 128 rows x 64 bf16 (128 B, swizzled)
