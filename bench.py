@@ -10,12 +10,15 @@ causal.  One step = one fa_fwd call over that whole workload with inputs residen
   e2e           the same metric through the public call with pinned host buffers, the
                 host->device copies of Q/K/V and the device->host copy of O/LSE timed
   cpu_baseline  the fp64 oracle on a bounded sample of rows, on this host's cores
-  extra         the other workloads (dense 2k, GQA 16k causal, split-KV decode) measured
-                the same way, decode against HBM bandwidth
+  extra         the other workloads (dense 2k, GQA 16k causal, split-KV decode) and the
+                variants (fp16, sliding window, softcap + ALiBi, backward, windowed and
+                paged decode with append + rotary) measured the same way, decode against
+                HBM bandwidth
 Under torchrun (N > 1) every rank runs the full workload on its own GPU (weak scaling;
 the (batch, head) units are independent, so there is no collective on the data path);
 the step time is the max over ranks.
 `--impl reference` times the fp64 CPU oracle instead (rank 0 only).
+`--backward` makes the timed step the backward pass (fa_bwd) of the chosen dense workload.
 """
 from __future__ import annotations
 
@@ -34,6 +37,7 @@ sys.path.insert(0, ROOT)
 
 HEADLINE = "causal8k"
 METRIC = "attention fwd TFLOPS (bf16 causal N=8192 d=128) & % of GB300 BF16 peak"
+BWD_METRIC = "attention bwd TFLOPS (dQ, dK, dV; 2.5 x forward FLOPs) & % of GB300 BF16 peak"
 L2_BYTES = 129 * 1024 * 1024
 
 
@@ -246,6 +250,68 @@ class DenseCase:
         return round(job_value(self.work, ms, world, 1e12), 2), "TFLOPS"
 
 
+BWD_SRC = ["exact_attention_81_gb300/csrc/fa_backward.cu", "exact_attention_81_gb300/csrc/ptx.cuh"]
+
+
+class BwdCase(DenseCase):
+    """One fa_bwd call (D preprocessing, bwd_kernel, dQ conversion) on the forward output of
+    a dense workload; work = the five matmuls' FLOPs, 2.5 x the forward's."""
+
+    def __init__(self, w, dev):
+        super().__init__(w, dev)
+        import torch
+        import exact_attention_81_gb300 as fa
+        g = torch.Generator(device=dev).manual_seed(w.seed + 9)
+        self.do = torch.randn(self.q.shape, device=dev, generator=g).to(torch.bfloat16)
+        fa.fa_fwd(self.q, self.k, self.v, causal=w.causal, out=self.out, lse=self.lse)
+        self.dq, self.dk, self.dv = (torch.empty_like(t) for t in (self.q, self.k, self.v))
+        self.ws = torch.empty(fa.fa_bwd_workspace_size(w.B, w.Nq, w.Hq, w.d),
+                              dtype=torch.uint8, device=dev)
+        self.work = 2.5 * flops(w)
+        self.launches = 3
+
+    def step(self):
+        import exact_attention_81_gb300 as fa
+        fa.fa_bwd(self.q, self.k, self.v, self.out, self.lse, self.do, causal=self.w.causal,
+                  dq=self.dq, dk=self.dk, dv=self.dv, workspace=self.ws)
+
+    def e2e(self):
+        """Pinned host Q/K/V/O/LSE/dO copied in, dQ/dK/dV copied out, every step."""
+        import torch
+        import exact_attention_81_gb300 as fa
+        srcs = (self.q, self.k, self.v, self.out, self.lse, self.do)
+        hosts = [t.cpu().pin_memory() for t in srcs]
+        devs = [torch.empty_like(t) for t in srcs]
+        outs = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                for t in (self.dq, self.dk, self.dv)]
+
+        def run():
+            for dst, h in zip(devs, hosts):
+                dst.copy_(h, non_blocking=True)
+            fa.fa_bwd(*devs, causal=self.w.causal, dq=self.dq, dk=self.dk, dv=self.dv,
+                      workspace=self.ws)
+            for h, t in zip(outs, (self.dq, self.dk, self.dv)):
+                h.copy_(t, non_blocking=True)
+        h2d = sum(t.numel() * t.element_size() for t in srcs)
+        d2h = sum(t.numel() * t.element_size() for t in (self.dq, self.dk, self.dv))
+        return run, h2d, d2h
+
+    def describe(self, pk, ms_step, world):
+        d = super().describe(pk, ms_step, world)
+        w = self.w
+        tf = self.work / (ms_step * 1e-3) / 1e12
+        kern = f"bwd_kernel<{w.d},{str(w.causal).lower()}>"
+        d["metric"] = BWD_METRIC
+        d["roofline"] = {
+            "bound": "tensor", "achieved": round(tf, 2), "peak": pk["bf16"], "unit": "TFLOP/s",
+            "frac": round(tf / pk["bf16"], 4),
+            "traffic": profiled_traffic(kern, BWD_SRC, w.name),
+            "peak_basis": f"{pk['basis']} bf16 dense (burst)",
+            "kernel": f"{kern} + preprocessing + dQ conversion (3 launches per step; achieved "
+                      "uses the step time)"}
+        return d
+
+
 class DecodeCase:
     """One fa_fwd_kvcache call (split-KV decode + combine); work = bytes of the visible
     K/V prefix, Q, O and LSE (the split partials are overhead, not counted)."""
@@ -320,7 +386,10 @@ def run_ours(args, rank, world, dist):
     dev = torch.device("cuda", local)
     pk = peaks()
     w = WORKLOADS[args.workload]
-    case = DecodeCase(w, dev) if w.kind == "kvcache" else DenseCase(w, dev)
+    if w.kind == "kvcache":
+        case = DecodeCase(w, dev)
+    else:
+        case = BwdCase(w, dev) if args.backward else DenseCase(w, dev)
     stream = torch.cuda.current_stream()
 
     def barrier():
@@ -387,9 +456,33 @@ def run_ours(args, rank, world, dist):
     if rank == 0 and not args.no_cpu_baseline:
         if w.kind == "kvcache":
             result["cpu_baseline"] = cpu_baseline_decode(case, args.cpu_seconds)
+        elif args.backward:
+            result["cpu_baseline"] = cpu_baseline_bwd(case, args.cpu_seconds)
         else:
             result["cpu_baseline"] = cpu_baseline(w, case.q, case.k, case.v, args.cpu_seconds)
     return result
+
+
+def cpu_baseline_bwd(case, seconds):
+    """The fp64 oracle's backward on a bounded sample: whole heads of batch 0, one after
+    the other, until `seconds` of CPU time have been spent."""
+    import oracle.oracle as ORACLE
+    w = case.w
+    threads = os.cpu_count() or 1
+    fl, dt, heads = 0.0, 0.0, 0
+    while dt < seconds and heads < w.Hkv:
+        g = heads
+        G = w.Hq // w.Hkv
+        q, do = (t[0:1, :, g * G:(g + 1) * G].contiguous().cpu() for t in (case.q, case.do))
+        k, v = (t[0:1, :, g:g + 1].contiguous().cpu() for t in (case.k, case.v))
+        t0 = time.time()
+        ORACLE.attention_bwd(q, k, v, do, w.scale, w.causal, nthreads=threads)
+        dt += time.time() - t0
+        fl += 2.5 * 4.0 * w.Nq * w.Nk * w.d * G / (2 if w.causal else 1)
+        heads += 1
+    return {"value": fl / dt / 1e12, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
+            "sample": f"backward of {heads} kv head(s) of batch 0 of {w.name} "
+                      f"(fp64, {dt:.1f} s)"}
 
 
 def cpu_baseline_decode(case, seconds):
@@ -678,6 +771,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the backward pass (fa_bwd) of the dense workload instead")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
