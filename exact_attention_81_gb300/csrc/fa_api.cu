@@ -158,6 +158,10 @@ bool scale_ok(float s) { return std::isfinite(s) && s > 0.f; }
 
 bool dtype_ok(int t) { return t == FA_BF16 || t == FA_FP16; }
 
+// Head dimensions served: multiples of 8 up to 128 (the kernels run at width 64 or 128;
+// the tensor maps give the columns past d as zeros).
+bool head_dim_ok(int d) { return d >= 8 && d <= 128 && d % 8 == 0; }
+
 int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 
 // Keys per split for the decode path (a multiple of the 128-key block).
@@ -261,7 +265,7 @@ fa_status fa_fwd(const fa_fwd_params *p, cudaStream_t stream) {
   const fa_fwd_params &a = *p;
   if (a.B < 0 || a.Nq < 0 || a.Nk < 0 || a.Hq <= 0 || a.Hkv <= 0 || a.Hq % a.Hkv != 0)
     return FA_ERR_INVALID_ARG;
-  if (a.d != 64 && a.d != 128) return FA_ERR_UNSUPPORTED;
+  if (!head_dim_ok(a.d)) return FA_ERR_UNSUPPORTED;
   if (!dtype_ok(a.dtype)) return FA_ERR_UNSUPPORTED;
   if (!scale_ok(a.scale)) return FA_ERR_INVALID_ARG;
   if (a.Nq > (1 << 30) || a.Nk > (1 << 30)) return FA_ERR_INVALID_ARG;
@@ -327,10 +331,12 @@ fa_status fa_fwd(const fa_fwd_params *p, cudaStream_t stream) {
   pa.err = dev->err;
   pa.timeout_ns = g_timeout_ns;
   pa.sched_slot = fa::next_prefill_sched_slot();
+  pa.d = a.d;
   apply_mod(mod, a.scale, &pa);
   const int grid = static_cast<int>(tiles < dev->sm_count ? tiles : dev->sm_count);
   cudaError_t e =
-      fa::launch_prefill(a.d, mod.mask, a.dtype == FA_FP16, tq, tk, tv, pa, grid, stream);
+      fa::launch_prefill(fa::kernel_d(a.d), mod.mask, a.dtype == FA_FP16, tq, tk, tv, pa, grid,
+                         stream);
   return e == cudaSuccess ? FA_OK : cuda_fail("prefill kernel launch", e);
 }
 
@@ -342,7 +348,7 @@ fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, fl
   if (B < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || total_q < 0 || total_k < 0 || Hq <= 0 ||
       Hkv <= 0 || Hq % Hkv != 0)
     return FA_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (!head_dim_ok(d)) return FA_ERR_UNSUPPORTED;
   if (!dtype_ok(dtype)) return FA_ERR_UNSUPPORTED;
   if (!scale_ok(scale)) return FA_ERR_INVALID_ARG;
   if (max_seqlen_q > (1 << 30) || total_q > (1 << 30) || total_k > (1 << 30))
@@ -407,10 +413,12 @@ fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, fl
   pa.err = dev->err;
   pa.timeout_ns = g_timeout_ns;
   pa.sched_slot = fa::next_prefill_sched_slot();
+  pa.d = d;
   apply_mod(mod, scale, &pa);
   const int grid = static_cast<int>(tiles < dev->sm_count ? tiles : dev->sm_count);
   cudaError_t e =
-      fa::launch_prefill(d, mod.mask, dtype == FA_FP16, tq, tk, tv, pa, grid, stream);
+      fa::launch_prefill(fa::kernel_d(d), mod.mask, dtype == FA_FP16, tq, tk, tv, pa, grid,
+                         stream);
   return e == cudaSuccess ? FA_OK : cuda_fail("prefill kernel launch", e);
 }
 
@@ -418,7 +426,7 @@ size_t fa_fwd_kvcache_workspace_size(int B, int Hq, int Lmax, int d, int num_spl
   if (B <= 0 || Hq <= 0 || Lmax <= 0 || d <= 0 || num_splits < 0) return 0;
   const int chunk = decode_chunk(Lmax, num_splits);
   const int64_t maxch = (static_cast<int64_t>(Lmax) + chunk - 1) / chunk;
-  const int64_t bytes = static_cast<int64_t>(B) * Hq * maxch * (d + 1) * 4;
+  const int64_t bytes = static_cast<int64_t>(B) * Hq * maxch * (fa::kernel_d(d) + 1) * 4;
   return static_cast<size_t>((bytes + 255) / 256 * 256);
 }
 
@@ -430,7 +438,7 @@ fa_status fa_fwd_kvcache(const void *q, const void *k_cache, const void *v_cache
                          cudaStream_t stream) {
   if (B < 0 || Lmax < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || num_splits < 0)
     return FA_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (!head_dim_ok(d)) return FA_ERR_UNSUPPORTED;
   const int group = Hq / Hkv;
   if (group != 1 && group != 2 && group != 4 && group != 8) return FA_ERR_UNSUPPORTED;
   if (!dtype_ok(dtype)) return FA_ERR_UNSUPPORTED;
@@ -498,7 +506,7 @@ fa_status fa_fwd_kvcache(const void *q, const void *k_cache, const void *v_cache
       chunk = auto_chunk(Leff, static_cast<int64_t>(B) * Hkv, dev->sm_count, maxch);
     maxch = ceil_div(Leff, chunk);
     o_part = static_cast<float *>(workspace);
-    lse_part = o_part + static_cast<int64_t>(B) * Hq * maxch * d;
+    lse_part = o_part + static_cast<int64_t>(B) * Hq * maxch * fa::kernel_d(d);
   }
   const int64_t units = static_cast<int64_t>(maxch) * B * Hkv;
   if (units > INT32_MAX) return FA_ERR_INVALID_ARG;
@@ -553,6 +561,7 @@ fa_status fa_fwd_kvcache(const void *q, const void *k_cache, const void *v_cache
     da.Lmax = Lmax;
     da.chunk = chunk;
     da.maxch = maxch;
+    da.d = d;
     da.num_units = static_cast<int>(units);
     da.scale_log2 = scale_log2(scale);
     da.err = dev->err;
@@ -572,10 +581,12 @@ fa_status fa_fwd_kvcache(const void *q, const void *k_cache, const void *v_cache
     da.num_pages = paged ? ex->num_pages : 0;
     da.kalign = paged ? 128 : 1;
     const int grid = static_cast<int>(units < dev->sm_count ? units : dev->sm_count);
-    cudaError_t e = fa::launch_decode(d, group, dtype == FA_FP16, tk, tv, da, grid, stream);
+    cudaError_t e =
+        fa::launch_decode(fa::kernel_d(d), group, dtype == FA_FP16, tk, tv, da, grid, stream);
     if (e != cudaSuccess) return cuda_fail("decode kernel launch", e);
   }
-  cudaError_t e = fa::launch_combine(d, dtype == FA_FP16, o_part, lse_part, cache_seqlens,
+  cudaError_t e = fa::launch_combine(fa::kernel_d(d), d, dtype == FA_FP16, o_part, lse_part,
+                                     cache_seqlens,
                                      append ? 1 : 0, B, Hq, Lmax, chunk, maxch, mod.wl,
                                      paged ? 128 : 1, o, lse, dev->err, stream);
   return e == cudaSuccess ? FA_OK : cuda_fail("combine kernel launch", e);
@@ -595,7 +606,7 @@ fa_status fa_bwd(const fa_bwd_params *p, cudaStream_t stream) {
   const fa_bwd_params &a = *p;
   if (a.B < 0 || a.Nq < 0 || a.Nk < 0 || a.Hq <= 0 || a.Hkv <= 0 || a.Hq % a.Hkv != 0)
     return FA_ERR_INVALID_ARG;
-  if (a.d != 64 && a.d != 128) return FA_ERR_UNSUPPORTED;
+  if (!head_dim_ok(a.d)) return FA_ERR_UNSUPPORTED;
   if (!dtype_ok(a.dtype)) return FA_ERR_UNSUPPORTED;
   if (!scale_ok(a.scale)) return FA_ERR_INVALID_ARG;
   if (a.Nq > (1 << 30) || a.Nk > (1 << 30)) return FA_ERR_INVALID_ARG;
@@ -678,13 +689,15 @@ fa_status fa_bwd(const fa_bwd_params *p, cudaStream_t stream) {
   ba.Hkv = a.Hkv;
   ba.group = a.Hq / a.Hkv;
   ba.kblocks = kblocks;
+  ba.d = a.d;
   ba.num_units = static_cast<int>(units);
   ba.scale = a.scale;
   ba.scale_log2 = scale_log2(a.scale);
   ba.err = dev->err;
   ba.timeout_ns = g_timeout_ns;
   const int grid = static_cast<int>(units < dev->sm_count ? units : dev->sm_count);
-  e = fa::launch_bwd(a.d, a.causal != 0, f16, tq, tk, tv, tdo, tdq, ba, grid, stream);
+  e = fa::launch_bwd(fa::kernel_d(a.d), a.causal != 0, f16, tq, tk, tv, tdo, tdq, ba, grid,
+                     stream);
   if (e != cudaSuccess) return cuda_fail("backward kernel launch", e);
   e = fa::launch_bwd_post(a.d, f16, dq_acc, a.scale, a.dq, a.B, a.Nq, a.Hq, a.dq_strides, stream);
   return e == cudaSuccess ? FA_OK : cuda_fail("backward postprocessing launch", e);

@@ -316,6 +316,7 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
       if (key < a.Nk) {
 #pragma unroll
         for (int v = half * (D / 16); v < (half + 1) * (D / 16); ++v) {
+          if (8 * v >= a.d) break;
           reinterpret_cast<uint4 *>(dkrow)[v] = make_uint4(0u, 0u, 0u, 0u);
           reinterpret_cast<uint4 *>(dvrow)[v] = make_uint4(0u, 0u, 0u, 0u);
         }
@@ -414,6 +415,7 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
       if (key < a.Nk) {
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
+          if (cc * 32 + 8 * v >= a.d) break;  // columns past d are padding
           uint4 wv, wk;
           wv.x = pack2<F16>(__uint_as_float(vr[8 * v + 0]), __uint_as_float(vr[8 * v + 1]));
           wv.y = pack2<F16>(__uint_as_float(vr[8 * v + 2]), __uint_as_float(vr[8 * v + 3]));
@@ -512,9 +514,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // ------------------------------------------------------------------------------------
 // Preprocessing: D = rowsum(dO * O) (one warp per row) and a zeroed dQ accumulator.
 
-template <int D, bool F16>
+template <bool F16>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t *o, const uint16_t *dout,
-                                                      int B, int Nq, int Hq, int64_t os0,
+                                                      int B, int Nq, int Hq, int d, int64_t os0,
                                                       int64_t os1, int64_t os2, int64_t ds0,
                                                       int64_t ds1, int64_t ds2, float *dvec,
                                                       float *dq_acc) {
@@ -529,8 +531,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t *o, const u
     const uint16_t *orow = o + b * os0 + n * os1 + h * os2;
     const uint16_t *drow = dout + b * ds0 + n * ds1 + h * ds2;
     float acc = 0.f;
-#pragma unroll
-    for (int c = lane * 2; c < D; c += 64) {
+    for (int c = lane * 2; c < d; c += 64) {
       const uint32_t ov = *reinterpret_cast<const uint32_t *>(orow + c);
       const uint32_t dv = *reinterpret_cast<const uint32_t *>(drow + c);
       acc = fmaf(lo_to_f32<F16>(ov), lo_to_f32<F16>(dv), acc);
@@ -539,9 +540,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t *o, const u
 #pragma unroll
     for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
     if (lane == 0) dvec[(static_cast<int64_t>(b) * Hq + h) * Nq + n] = acc;
-    float *qrow = dq_acc + (bn * Hq + h) * D;
-#pragma unroll
-    for (int c = lane * 4; c < D; c += 128)
+    float *qrow = dq_acc + (bn * Hq + h) * d;
+    for (int c = lane * 4; c < d; c += 128)
       *reinterpret_cast<float4 *>(qrow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 }
@@ -632,16 +632,9 @@ cudaError_t launch_bwd_pre(int d, bool f16, const void *o, const void *dout, int
   const int grid = grid_for(rows * 32, 256);
   const uint16_t *op = reinterpret_cast<const uint16_t *>(o);
   const uint16_t *dp = reinterpret_cast<const uint16_t *>(dout);
-#define FA_PRE(DD, FF)                                                                    \
-  bwd_pre_kernel<DD, FF><<<grid, 256, 0, stream>>>(op, dp, B, Nq, Hq, o_st[0], o_st[1],  \
-                                                   o_st[2], do_st[0], do_st[1], do_st[2], \
-                                                   dvec, dq_acc)
-  if (d == 64) {
-    if (f16) FA_PRE(64, true); else FA_PRE(64, false);
-  } else {
-    if (f16) FA_PRE(128, true); else FA_PRE(128, false);
-  }
-#undef FA_PRE
+  auto kern = f16 ? bwd_pre_kernel<true> : bwd_pre_kernel<false>;
+  kern<<<grid, 256, 0, stream>>>(op, dp, B, Nq, Hq, d, o_st[0], o_st[1], o_st[2], do_st[0],
+                                 do_st[1], do_st[2], dvec, dq_acc);
   return cudaGetLastError();
 }
 

@@ -219,10 +219,10 @@ __device__ void compute(const DecodeArgs &a, uint8_t *smem, DBars *bars, const W
 #pragma unroll
     for (int gg = 0; gg < G; ++gg) {
       const uint4 *src = reinterpret_cast<const uint4 *>(
-          qg + (static_cast<int64_t>(w.b) * a.Hq + w.g * G + gg) * D + d0);
+          qg + (static_cast<int64_t>(w.b) * a.Hq + w.g * G + gg) * a.d + d0);
 #pragma unroll
       for (int v = 0; v < C::DP / 8; ++v) {
-        const uint4 x = src[v];
+        const uint4 x = d0 + 8 * v < a.d ? src[v] : make_uint4(0u, 0u, 0u, 0u);  // padding
         const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e)
@@ -482,7 +482,7 @@ template <int D, bool F16>
 __global__ void __launch_bounds__(D)
     combine_kernel(const float *o_part, const float *lse_part, const int *cache_len,
                    int len_add, int Hq, int Lmax, int chunk, int maxch, int wl, int kalign,
-                   uint16_t *o, float *lse) {
+                   int d_out, uint16_t *o, float *lse) {
   const int bh = blockIdx.x;
   const int b = bh / Hq;
   const int d = threadIdx.x;
@@ -491,7 +491,7 @@ __global__ void __launch_bounds__(D)
   const float *lp = lse_part + static_cast<int64_t>(bh) * maxch;
   const float *op = o_part + static_cast<int64_t>(bh) * maxch * D;
   if (nch == 0) {
-    o[static_cast<int64_t>(bh) * D + d] = 0;  // +0 in both bf16 and fp16
+    if (d < d_out) o[static_cast<int64_t>(bh) * d_out + d] = 0;  // +0 in bf16 and fp16
     if (d == 0) lse[bh] = -INFINITY;
     return;
   }
@@ -503,8 +503,9 @@ __global__ void __launch_bounds__(D)
     wsum += wgt;
     acc = fmaf(wgt, op[static_cast<int64_t>(c) * D + d], acc);
   }
-  o[static_cast<int64_t>(bh) * D + d] =
-      static_cast<uint16_t>(pack2<F16>(acc / wsum, 0.f) & 0xFFFFu);  // round to nearest even
+  if (d < d_out)
+    o[static_cast<int64_t>(bh) * d_out + d] =
+        static_cast<uint16_t>(pack2<F16>(acc / wsum, 0.f) & 0xFFFFu);  // round to nearest even
   if (d == 0) lse[bh] = m + logf(wsum);
 }
 
@@ -632,7 +633,7 @@ cudaError_t launch_decode(int d, int group, bool f16, const CUtensorMap &tk,
              : launch_decode_typed<false>(d, group, tk, tv, a, grid, stream);
 }
 
-cudaError_t launch_combine(int d, bool f16, const float *o_part, const float *lse_part,
+cudaError_t launch_combine(int d, int d_out, bool f16, const float *o_part, const float *lse_part,
                            const int *cache_len, int len_add, int B, int Hq, int Lmax, int chunk,
                            int maxch, int wl, int kalign, void *o, float *lse,
                            unsigned int * /*err*/, cudaStream_t stream) {
@@ -642,7 +643,7 @@ cudaError_t launch_combine(int d, bool f16, const float *o_part, const float *ls
   auto kern = d == 64 ? (f16 ? combine_kernel<64, true> : combine_kernel<64, false>)
                       : (f16 ? combine_kernel<128, true> : combine_kernel<128, false>);
   kern<<<blocks, d, 0, stream>>>(o_part, lse_part, cache_len, len_add, Hq, Lmax, chunk, maxch,
-                                 wl, kalign, ob, lse);
+                                 wl, kalign, d_out, ob, lse);
   return cudaGetLastError();
 }
 

@@ -35,6 +35,8 @@ struct PrefillArgs {
   int num_tiles;              // B * Hq * mblocks
   float scale_log2;           // scale * log2(e)
   int sched_slot;             // this launch's tile-ticket counter slot
+  int d;                      // head dimension of the tensors (the kernel's D may be larger:
+                              // the columns past d arrive as zeros and are not stored)
   unsigned int *err;          // device error word
   unsigned long long timeout_ns;
   // Score modifiers (read by the MASK_MOD kernel only).
@@ -74,6 +76,7 @@ struct DecodeArgs {
   int B, Hq, Hkv, Lmax;
   int chunk;                  // keys per split (multiple of 128)
   int maxch;                  // chunks of the longest visible range: ceil(Leff / chunk)
+  int d;                      // head dimension of q and the caches (<= the kernel's D)
   int num_units;              // maxch * B * Hkv
   float scale_log2;
   unsigned int *err;
@@ -123,10 +126,14 @@ cudaError_t launch_decode(int d, int group, bool f16, const CUtensorMap &tk,
 
 // wl, kalign, len_add: as in DecodeArgs; chunks tile the keys [decode_first_key, len) of
 // each sequence, len = cache_len + len_add.
-cudaError_t launch_combine(int d, bool f16, const float *o_part, const float *lse_part,
+// d: the kernel width of the partials (64 or 128); d_out: the head dimension of o.
+cudaError_t launch_combine(int d, int d_out, bool f16, const float *o_part, const float *lse_part,
                            const int *cache_len, int len_add, int B, int Hq, int Lmax, int chunk,
                            int maxch, int wl, int kalign, void *o, float *lse, unsigned int *err,
                            cudaStream_t stream);
+
+// Width of the kernel instance that serves head dimension d (8 <= d <= 128, d % 8 == 0).
+inline int kernel_d(int d) { return d <= 64 ? 64 : 128; }
 
 // Backward pass: main kernel arguments (one work unit = batch, kv head, 128-key block).
 struct BwdArgs {
@@ -136,6 +143,7 @@ struct BwdArgs {
   int64_t dk_sb, dk_sn, dk_sh, dv_sb, dv_sn, dv_sh;
   int B, Nq, Nk, Hq, Hkv, group;
   int kblocks;                // ceil(Nk / 128)
+  int d;                      // head dimension of the tensors (<= the kernel's D)
   int num_units;              // kblocks * B * Hkv
   float scale, scale_log2;
   unsigned int *err;

@@ -563,6 +563,7 @@ __device__ void softmax_role(const PrefillArgs &a, Bars *bars, uint32_t tmem, co
           uint4 *dst = reinterpret_cast<uint4 *>(orow + cc);
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
+            if (cc + 8 * v >= a.d) break;  // columns past d are padding
             uint4 w;
             w.x = pack2<F16>(__uint_as_float(r[8 * v + 0]) * inv_l, __uint_as_float(r[8 * v + 1]) * inv_l);
             w.y = pack2<F16>(__uint_as_float(r[8 * v + 2]) * inv_l, __uint_as_float(r[8 * v + 3]) * inv_l);
@@ -577,7 +578,8 @@ __device__ void softmax_role(const PrefillArgs &a, Bars *bars, uint32_t tmem, co
     } else if (row_ok) {
       uint4 *dst = reinterpret_cast<uint4 *>(orow);
 #pragma unroll
-      for (int v = 0; v < D / 8; ++v) dst[v] = make_uint4(0u, 0u, 0u, 0u);
+      for (int v = 0; v < D / 8; ++v)
+        if (8 * v < a.d) dst[v] = make_uint4(0u, 0u, 0u, 0u);
     }
     if (row_ok) {
       const float lse = l > 0.f ? (m + log2f(l)) * LN2 : -INFINITY;

@@ -54,7 +54,8 @@ def _bwd_params(**kw):
 
 
 @pytest.mark.parametrize("change,status", [
-    ({"d": 96}, 2), ({"dtype": 3}, 2), ({"Hkv": 3}, 1), ({"scale": 0.0}, 1), ({"dout": None}, 1),
+    ({"d": 100}, 2), ({"d": 136}, 2), ({"dtype": 3}, 2), ({"Hkv": 3}, 1), ({"scale": 0.0}, 1),
+    ({"dout": None}, 1),
     ({"lse": None}, 1), ({"dk": 4100}, 1), ({"workspace": None}, 4), ({"workspace_bytes": 16}, 4),
     ({"workspace": 4096 + 64}, 4), ({"B": 0}, 0),
 ])
@@ -84,7 +85,7 @@ def _params(**kw):
 
 
 @pytest.mark.parametrize("change,status", [
-    ({"d": 96}, 2), ({"d": 256}, 2), ({"dtype": 2}, 2), ({"dtype": -1}, 2), ({"Hkv": 3}, 1), ({"Hq": 0}, 1), ({"B": -1}, 1),
+    ({"d": 100}, 2), ({"d": 256}, 2), ({"d": 0}, 2), ({"d": 4}, 2), ({"dtype": 2}, 2), ({"dtype": -1}, 2), ({"Hkv": 3}, 1), ({"Hq": 0}, 1), ({"B": -1}, 1),
     ({"scale": 0.0}, 1), ({"scale": float("nan")}, 1), ({"scale": -1.0}, 1),
     ({"q": 4098}, 1), ({"o": 4100}, 1), ({"lse": 4098}, 1), ({"q": None}, 1),
     ({"k": None}, 1), ({"Nq": -5}, 1),
@@ -135,7 +136,8 @@ def test_varlen_rejects_bad_arguments(lib):
                  a["mk"], a["tq"], a["tk"], a["Hq"], a["Hkv"], a["d"], a["scale"], a["causal"],
                  a["dtype"], a.get("mod"), None)
 
-    assert call(d=80) == 2
+    assert call(d=84) == 2
+    assert call(d=136) == 2
     assert call(dtype=3) == 2
     assert call(Hkv=3) == 1
     assert call(cq=None) == 1
@@ -161,7 +163,8 @@ def test_kvcache_rejects_bad_arguments(lib):
 
     assert call(Hq=32, Hkv=2) == 2          # group of 16 not supported by decode
     assert call(dtype=5) == 2
-    assert call(d=32) == 2
+    assert call(d=36) == 2
+    assert call(d=160) == 2
     assert call(Hkv=5) == 1
     assert call(ns=-1) == 1
     assert call(lens=None) == 1
