@@ -579,6 +579,12 @@ def extra_workloads(args, dev, pk, world, dist):
     res["causal8k_backward"] = {"ms": round(ms, 4), "TFLOPS": round(tf, 2),
                                 "frac_of_bf16_peak": round(tf / pk["bf16"], 4),
                                 "gpu_launches_per_call": 3}
+    ms = time_calls(lambda: fa.fa_bwd(q, k, v, o, l, do, causal=True, dq=dq, dk=dk, dv=dv,
+                                      workspace=bws, deterministic=True),
+                    max(10, args.steps // 4), stream)
+    tf = 2.5 * flops(w) / (ms * 1e-3) / 1e12
+    res["causal8k_backward_deterministic"] = {"ms": round(ms, 4), "TFLOPS": round(tf, 2),
+                                              "frac_of_bf16_peak": round(tf / pk["bf16"], 4)}
     del q, k, v, do, o, l, dq, dk, dv, bws
     w = WORKLOADS["decode"]
     q, kc, vc, lens = kvcache_workload_inputs(w, device=dev)

@@ -114,6 +114,7 @@ class BwdParams(ctypes.Structure):
         ("dk_strides", ctypes.c_int64 * 3), ("dv_strides", ctypes.c_int64 * 3),
         ("scale", ctypes.c_float), ("causal", ctypes.c_int), ("dtype", ctypes.c_int),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("deterministic", ctypes.c_int),
     ]
 
 
@@ -403,9 +404,10 @@ def fa_bwd_workspace_size(B: int, Nq: int, Hq: int, d: int) -> int:
 
 
 def fa_bwd(q, k, v, out, lse, dout, causal: bool = False, scale: float | None = None,
-           dq=None, dk=None, dv=None, workspace=None, stream=None):
+           dq=None, dk=None, dv=None, workspace=None, stream=None, deterministic=False):
     """Backward of fa_fwd: q/out/dout [B,Nq,Hq,d], k/v [B,Nk,Hkv,d] (bf16 or fp16, CUDA),
-    lse [B,Hq,Nq] fp32 from the forward call.  Returns (dq, dk, dv)."""
+    lse [B,Hq,Nq] fp32 from the forward call.  deterministic fixes the order in which the
+    key blocks add into dQ.  Returns (dq, dk, dv)."""
     _require_bf16_cuda("q", q, 4)
     for name, t in (("k", k), ("v", v), ("out", out), ("dout", dout)):
         _require_bf16_cuda(name, t, 4, q.dtype)
@@ -439,6 +441,7 @@ def fa_bwd(q, k, v, out, lse, dout, causal: bool = False, scale: float | None = 
     p.causal = int(bool(causal))
     p.dtype = _DTYPE[q.dtype]
     p.workspace, p.workspace_bytes = _ptr(workspace), workspace.numel()
+    p.deterministic = int(bool(deterministic))
     _check(load_library().fa_bwd(ctypes.byref(p), _stream_handle(stream)), "fa_bwd")
     return dq, dk, dv
 

@@ -594,11 +594,15 @@ fa_status fa_fwd_kvcache(const void *q, const void *k_cache, const void *v_cache
 
 size_t fa_bwd_params_size(void) { return sizeof(fa_bwd_params); }
 
+// Workspace of fa_bwd: fp32 dQ accumulator [B, Nq, Hq, d], D [B, Hq, Nq], and one counter
+// per (batch, query head, 128-row query block), each part 256-byte aligned.
 size_t fa_bwd_workspace_size(int B, int Nq, int Hq, int d) {
   if (B <= 0 || Nq <= 0 || Hq <= 0 || d <= 0) return 0;
   const int64_t acc = static_cast<int64_t>(B) * Nq * Hq * d * 4;
   const int64_t vec = static_cast<int64_t>(B) * Hq * Nq * 4;
-  return static_cast<size_t>((acc + 255) / 256 * 256 + (vec + 255) / 256 * 256);
+  const int64_t sem = static_cast<int64_t>(B) * Hq * ((Nq + 127) / 128) * 4;
+  return static_cast<size_t>((acc + 255) / 256 * 256 + (vec + 255) / 256 * 256 +
+                             (sem + 255) / 256 * 256);
 }
 
 fa_status fa_bwd(const fa_bwd_params *p, cudaStream_t stream) {
@@ -656,6 +660,9 @@ fa_status fa_bwd(const fa_bwd_params *p, cudaStream_t stream) {
   float *dq_acc = static_cast<float *>(a.workspace);
   const int64_t acc_bytes = (static_cast<int64_t>(a.B) * a.Nq * a.Hq * a.d * 4 + 255) / 256 * 256;
   float *dvec = reinterpret_cast<float *>(static_cast<char *>(a.workspace) + acc_bytes);
+  const int64_t vec_bytes = (static_cast<int64_t>(a.B) * a.Hq * a.Nq * 4 + 255) / 256 * 256;
+  int *sem = reinterpret_cast<int *>(static_cast<char *>(a.workspace) + acc_bytes + vec_bytes);
+  const int nsem = a.deterministic ? a.B * a.Hq * ceil_div(a.Nq, 128) : 0;
   CUtensorMap tq, tk, tv, tdo, tdq;
   if ((st = make_map(&tq, a.q, a.d, a.Nq, a.Hq, a.B, a.q_strides[1], a.q_strides[2],
                      a.q_strides[0], a.dtype)) != FA_OK ||
@@ -669,7 +676,7 @@ fa_status fa_bwd(const fa_bwd_params *p, cudaStream_t stream) {
     return st;
   const bool f16 = a.dtype == FA_FP16;
   e = fa::launch_bwd_pre(a.d, f16, a.o, a.dout, a.B, a.Nq, a.Hq, a.o_strides, a.do_strides, dvec,
-                         dq_acc, stream);
+                         dq_acc, sem, nsem, stream);
   if (e != cudaSuccess) return cuda_fail("backward preprocessing launch", e);
   fa::BwdArgs ba{};
   ba.lse = a.lse;
@@ -690,6 +697,7 @@ fa_status fa_bwd(const fa_bwd_params *p, cudaStream_t stream) {
   ba.group = a.Hq / a.Hkv;
   ba.kblocks = kblocks;
   ba.d = a.d;
+  ba.sem = a.deterministic ? sem : nullptr;
   ba.num_units = static_cast<int>(units);
   ba.scale = a.scale;
   ba.scale_log2 = scale_log2(a.scale);

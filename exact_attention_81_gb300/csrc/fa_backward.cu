@@ -121,6 +121,24 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const 
   return __all_sync(0xffffffffu, ok);
 }
 
+// Waits (bounded) until *ctr == target, then orders later TMA global accesses after it.
+__device__ __forceinline__ bool wait_counter(int *ctr, int target, const WaitCtl &c) {
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+    if (v >= target) break;
+    if (*c.abort) return false;
+    if (globaltimer_ns() - t0 > c.timeout_ns) {
+      *c.abort = 1;
+      atomicOr(c.err, c.code);
+      return false;
+    }
+  }
+  fence_proxy_async_global();
+  return true;
+}
+
 // Barrier among the compute threads, built on an mbarrier so that the wait is bounded:
 // a warp that has given up never leaves the others blocked.
 __device__ __forceinline__ bool group_sync(uint64_t *bar, uint32_t &phase, const WaitCtl &wc) {
@@ -396,10 +414,20 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
       fence_proxy_async_smem();
       if (!group_sync(&bars->cgrp, grp, wc)) return;
       if (tid == 0) {
+        int *sem = a.sem ? a.sem + (static_cast<int64_t>(w.b) * a.Hq + h) * w.nqb + i : nullptr;
+        // Deterministic order: key block j adds after blocks 0 .. j-1 (the blocks that reach
+        // query block i are a prefix 0 .. jmax).
+        if (sem != nullptr && !wait_counter(sem, w.j, wc)) return;
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc)
           tma_reduce_add_4d(tdq, dq_s + cc * BOX, cc * 32, h, q0, w.b);
         bulk_commit_group();
+        if (sem != nullptr) {
+          bulk_wait_all();             // the additions have been performed
+          fence_proxy_async_global();
+          __threadfence();
+          atomicAdd(sem, 1);
+        }
       }
       ++it;
     }
@@ -519,7 +547,9 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t *o, const u
                                                       int B, int Nq, int Hq, int d, int64_t os0,
                                                       int64_t os1, int64_t os2, int64_t ds0,
                                                       int64_t ds1, int64_t ds2, float *dvec,
-                                                      float *dq_acc) {
+                                                      float *dq_acc, int *sem, int nsem) {
+  for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < nsem; t += gridDim.x * blockDim.x)
+    sem[t] = 0;
   const int lane = threadIdx.x & 31;
   const int64_t rows = static_cast<int64_t>(B) * Nq * Hq;
   for (int64_t rw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / 32; rw < rows;
@@ -626,7 +656,7 @@ cudaError_t launch_bwd(int d, bool causal, bool f16, const CUtensorMap &tq, cons
 
 cudaError_t launch_bwd_pre(int d, bool f16, const void *o, const void *dout, int B, int Nq,
                            int Hq, const int64_t o_st[3], const int64_t do_st[3], float *dvec,
-                           float *dq_acc, cudaStream_t stream) {
+                           float *dq_acc, int *sem, int nsem, cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(B) * Nq * Hq;
   if (rows == 0) return cudaSuccess;
   const int grid = grid_for(rows * 32, 256);
@@ -634,7 +664,7 @@ cudaError_t launch_bwd_pre(int d, bool f16, const void *o, const void *dout, int
   const uint16_t *dp = reinterpret_cast<const uint16_t *>(dout);
   auto kern = f16 ? bwd_pre_kernel<true> : bwd_pre_kernel<false>;
   kern<<<grid, 256, 0, stream>>>(op, dp, B, Nq, Hq, d, o_st[0], o_st[1], o_st[2], do_st[0],
-                                 do_st[1], do_st[2], dvec, dq_acc);
+                                 do_st[1], do_st[2], dvec, dq_acc, sem, nsem);
   return cudaGetLastError();
 }
 

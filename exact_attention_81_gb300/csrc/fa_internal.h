@@ -144,6 +144,7 @@ struct BwdArgs {
   int B, Nq, Nk, Hq, Hkv, group;
   int kblocks;                // ceil(Nk / 128)
   int d;                      // head dimension of the tensors (<= the kernel's D)
+  int *sem;                   // deterministic dQ: additions done per (b, h, query block), or null
   int num_units;              // kblocks * B * Hkv
   float scale, scale_log2;
   unsigned int *err;
@@ -153,7 +154,7 @@ struct BwdArgs {
 // D = rowsum(dO * O) per query row and a zeroed fp32 dQ accumulator [B, Nq, Hq, d].
 cudaError_t launch_bwd_pre(int d, bool f16, const void *o, const void *dout, int B, int Nq,
                            int Hq, const int64_t o_st[3], const int64_t do_st[3], float *dvec,
-                           float *dq_acc, cudaStream_t stream);
+                           float *dq_acc, int *sem, int nsem, cudaStream_t stream);
 
 // tq, tk, tv, tdo: 16-bit maps like the forward's; tdq: fp32 map of the dQ accumulator
 // (box 32 x 128 rows, 128-byte swizzle).

@@ -158,6 +158,12 @@ __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// Orders global-memory accesses of the generic proxy and the async proxy (TMA) of this
+// thread with respect to each other.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // Orders this thread's generic-proxy shared-memory writes before later async-proxy reads
 // (TMA stores / reductions, tcgen05.mma operands).
 __device__ __forceinline__ void fence_proxy_async_smem() {

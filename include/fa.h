@@ -268,10 +268,14 @@ fa_status fa_fwd_kvcache_noalloc(const void *q, const void *k_cache, const void 
  *   k, v, dk, dv   : [B, Nk, Hkv, d]
  *   lse            : [B, Hq, Nq] fp32, the LSE fa_fwd wrote for the same q, k, v
  *   workspace      : DEVICE, fa_bwd_workspace_size(B, Nq, Hq, d) bytes, 256-byte aligned,
- *                    owned by the caller (the fp32 dQ accumulator and the D vector)
+ *                    owned by the caller (the fp32 dQ accumulator, the D vector and the
+ *                    counters that order the dQ additions in deterministic mode)
  * All 16-bit tensors share the element type `dtype`; P and dS enter the tensor cores as
- * 16-bit values, every product is accumulated in fp32.  dQ sums key blocks in an
- * unspecified order (two calls may differ in the last bits of dQ); dK and dV do not.
+ * 16-bit values, every product is accumulated in fp32.  dQ sums the key blocks' parts in
+ * an unspecified order (two calls may differ in the last bits of dQ) unless
+ * deterministic != 0, which fixes the order (key block 0, 1, 2, ...) at some cost in
+ * speed ("flash-attention" section 5: deterministic backward, slower); dK and dV are
+ * always deterministic.
  * The score modifiers (fa_score_mod) have no backward here.  Nk = 0 gives dQ = 0;
  * Nq = 0 gives dK = dV = 0; B = 0 is a no-op.
  */
@@ -287,6 +291,7 @@ typedef struct fa_bwd_params {
     int dtype;
     void *workspace;
     size_t workspace_bytes;
+    int deterministic;
 } fa_bwd_params;
 
 size_t fa_bwd_workspace_size(int B, int Nq, int Hq, int d);

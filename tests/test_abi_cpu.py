@@ -65,7 +65,8 @@ def test_bwd_rejects_bad_arguments(lib, change, status):
 
 def test_bwd_workspace_size(lib):
     ws = lib.fa_bwd_workspace_size
-    assert ws(2, 1000, 4, 128) == 2 * 1000 * 4 * 128 * 4 + ((2 * 4 * 1000 * 4 + 255) // 256) * 256
+    assert ws(2, 1000, 4, 128) == (2 * 1000 * 4 * 128 * 4 + ((2 * 4 * 1000 * 4 + 255) // 256) * 256
+                                   + 256)  # 2 x 4 x 8 block counters
     assert ws(0, 10, 4, 128) == 0
 
 

@@ -46,9 +46,10 @@ def _baseline(q, k, v, do, scale, causal):
             vv.grad.permute(0, 2, 1, 3))
 
 
-def _check(q, k, v, do, scale, causal, what):
+def _check(q, k, v, do, scale, causal, what, deterministic=False):
     o, lse = fa_fwd(q, k, v, causal=causal, scale=scale)
-    dq, dk, dv = fa_bwd(q, k, v, o, lse, do, causal=causal, scale=scale)
+    dq, dk, dv = fa_bwd(q, k, v, o, lse, do, causal=causal, scale=scale,
+                        deterministic=deterministic)
     assert get_last_device_error() == FA_OK
     ref = ORACLE.attention_bwd(q.cpu(), k.cpu(), v.cpu(), do.cpu(), scale, causal)[:3]
     base = _baseline(q, k, v, do, scale, causal)
@@ -80,6 +81,24 @@ def test_backward(case):
     q, k, v = dense_inputs(B, Nq, Nk, Hq, Hkv, d, seed=700 + Nq + d, device=DEV, dtype=dt)
     do = bf16_normal((B, Nq, Hq, d), seed=710 + Nq, device=DEV, dtype=dt)
     _check(q, k, v, do, float(np.float32(1 / math.sqrt(d))), causal, f"bwd {case}")
+
+
+@pytest.mark.parametrize("case", [
+    (2, 700, 700, 4, 2, 128, True), (1, 300, 900, 4, 1, 128, True), (2, 513, 513, 2, 2, 64, False)])
+def test_backward_deterministic(case):
+    """deterministic=True: the key blocks add into dQ in a fixed order, so two calls give
+    bit-identical gradients, within the same bar against the oracle."""
+    B, Nq, Nk, Hq, Hkv, d, causal = case
+    q, k, v = dense_inputs(B, Nq, Nk, Hq, Hkv, d, seed=730 + Nq, device=DEV)
+    do = bf16_normal((B, Nq, Hq, d), seed=731 + Nq, device=DEV)
+    scale = float(np.float32(1 / math.sqrt(d)))
+    _, g1 = _check(q, k, v, do, scale, causal, f"deterministic {case}", deterministic=True)
+    o, lse = fa_fwd(q, k, v, causal=causal, scale=scale)
+    for _ in range(2):
+        g2 = fa_bwd(q, k, v, o, lse, do, causal=causal, scale=scale, deterministic=True)
+        assert get_last_device_error() == FA_OK
+        for a, b in zip(g1, g2):
+            assert torch.equal(a, b), "deterministic backward differs between calls"
 
 
 def test_backward_rows_without_keys():
