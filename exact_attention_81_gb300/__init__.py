@@ -19,6 +19,7 @@ from ._binding import (  # noqa: F401
     FA_OK,
     FAError,
     fa_bwd,
+    fa_bwd_varlen,
     fa_bwd_workspace_size,
     fa_fwd,
     fa_fwd_kvcache,

@@ -159,6 +159,9 @@ def load_library(path: str | None = None):
         lib.fa_fwd_params_size.restype = sz
         lib.fa_bwd.argtypes = [ctypes.POINTER(BwdParams), vp]
         lib.fa_bwd.restype = i
+        lib.fa_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i,
+                                      i, i, i, f, i, i, vp, sz, i, vp]
+        lib.fa_bwd_varlen.restype = i
         lib.fa_bwd_workspace_size.argtypes = [i, i, i, i]
         lib.fa_bwd_workspace_size.restype = sz
         lib.fa_bwd_params_size.argtypes = []
@@ -443,6 +446,38 @@ def fa_bwd(q, k, v, out, lse, dout, causal: bool = False, scale: float | None = 
     p.workspace, p.workspace_bytes = _ptr(workspace), workspace.numel()
     p.deterministic = int(bool(deterministic))
     _check(load_library().fa_bwd(ctypes.byref(p), _stream_handle(stream)), "fa_bwd")
+    return dq, dk, dv
+
+
+def fa_bwd_varlen(q, k, v, out, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
+                  max_seqlen_k: int, causal: bool = False, scale: float | None = None, dq=None,
+                  dk=None, dv=None, workspace=None, stream=None, deterministic=False):
+    """Backward of fa_fwd_varlen: q/out/dout [total_q,Hq,d], k/v [total_k,Hkv,d] contiguous,
+    lse [Hq,total_q] fp32 from the forward call.  Returns (dq, dk, dv)."""
+    _require_bf16_cuda("q", q, 3)
+    for name, t in (("k", k), ("v", v), ("out", out), ("dout", dout)):
+        _require_bf16_cuda(name, t, 3, q.dtype)
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out), ("dout", dout)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous for the varlen call")
+    total_q, Hq, d = q.shape
+    total_k, Hkv = k.shape[0], k.shape[1]
+    B = cu_seqlens_q.numel() - 1
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (Hq, total_q) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [Hq, total_q] tensor")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = fa_bwd_workspace_size(B, int(max_seqlen_q), Hq, d)
+    if workspace is None:
+        workspace = torch.empty((max(need, 256),), dtype=torch.uint8, device=q.device)
+    sc = default_scale(d) if scale is None else float(scale)
+    st = load_library().fa_bwd_varlen(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+        _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), B, int(max_seqlen_q), int(max_seqlen_k),
+        total_q, total_k, Hq, Hkv, d, sc, int(bool(causal)), _DTYPE[q.dtype], _ptr(workspace),
+        workspace.numel(), int(bool(deterministic)), _stream_handle(stream))
+    _check(st, "fa_bwd_varlen")
     return dq, dk, dv
 
 

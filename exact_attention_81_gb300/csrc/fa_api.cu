@@ -681,6 +681,10 @@ fa_status fa_bwd(const fa_bwd_params *p, cudaStream_t stream) {
   fa::BwdArgs ba{};
   ba.lse = a.lse;
   ba.dvec = dvec;
+  ba.lse_sb = static_cast<int64_t>(a.Hq) * a.Nq;
+  ba.lse_sh = a.Nq;
+  ba.varlen = 0;
+  ba.qblocks = ceil_div(a.Nq, 128);
   ba.dk = a.dk;
   ba.dv = a.dv;
   ba.dk_sb = a.dk_strides[0];
@@ -708,6 +712,112 @@ fa_status fa_bwd(const fa_bwd_params *p, cudaStream_t stream) {
                      stream);
   if (e != cudaSuccess) return cuda_fail("backward kernel launch", e);
   e = fa::launch_bwd_post(a.d, f16, dq_acc, a.scale, a.dq, a.B, a.Nq, a.Hq, a.dq_strides, stream);
+  return e == cudaSuccess ? FA_OK : cuda_fail("backward postprocessing launch", e);
+}
+
+fa_status fa_bwd_varlen(const void *q, const void *k, const void *v, const void *o,
+                        const void *dout, const float *lse, void *dq, void *dk, void *dv,
+                        const int *cu_seqlens_q, const int *cu_seqlens_k, int B,
+                        int max_seqlen_q, int max_seqlen_k, int total_q, int total_k, int Hq,
+                        int Hkv, int d, float scale, int causal, int dtype, void *workspace,
+                        size_t workspace_bytes, int deterministic, cudaStream_t stream) {
+  if (B < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || total_q < 0 || total_k < 0 || Hq <= 0 ||
+      Hkv <= 0 || Hq % Hkv != 0)
+    return FA_ERR_INVALID_ARG;
+  if (!head_dim_ok(d)) return FA_ERR_UNSUPPORTED;
+  if (!dtype_ok(dtype)) return FA_ERR_UNSUPPORTED;
+  if (!scale_ok(scale)) return FA_ERR_INVALID_ARG;
+  if (max_seqlen_q > (1 << 30) || max_seqlen_k > (1 << 30) || total_q > (1 << 30) ||
+      total_k > (1 << 30))
+    return FA_ERR_INVALID_ARG;
+  if (B == 0 || (total_q == 0 && total_k == 0)) return FA_OK;
+  if (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr || !aligned(cu_seqlens_q, 4) ||
+      !aligned(cu_seqlens_k, 4))
+    return FA_ERR_INVALID_ARG;
+  const bool q_side = total_q > 0, k_side = total_k > 0;
+  if (q_side && (q == nullptr || o == nullptr || dout == nullptr || dq == nullptr ||
+                 lse == nullptr || !aligned(q, 16) || !aligned(o, 16) || !aligned(dout, 16) ||
+                 !aligned(dq, 16) || !aligned(lse, 4)))
+    return FA_ERR_INVALID_ARG;
+  if (k_side && (k == nullptr || v == nullptr || dk == nullptr || dv == nullptr ||
+                 !aligned(k, 16) || !aligned(v, 16) || !aligned(dk, 16) || !aligned(dv, 16)))
+    return FA_ERR_INVALID_ARG;
+  // The dense size for (B, max_seqlen_q) covers every part of the packed layout.
+  const size_t need = fa_bwd_workspace_size(B, max_seqlen_q, Hq, d);
+  if (q_side && k_side &&
+      (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256)))
+    return FA_ERR_WORKSPACE;
+  const int kblocks = ceil_div(max_seqlen_k, 128);
+  const int64_t units = static_cast<int64_t>(kblocks) * B * Hkv;
+  if (units > INT32_MAX) return FA_ERR_INVALID_ARG;
+
+  DeviceInfo *dev = nullptr;
+  fa_status st = current_device(&dev);
+  if (st != FA_OK) return st;
+  cudaError_t e;
+  const int64_t qst[3] = {0, static_cast<int64_t>(Hq) * d, d};
+  const int64_t kst[3] = {0, static_cast<int64_t>(Hkv) * d, d};
+  if (!k_side || max_seqlen_k == 0) {  // no keys: dQ = 0
+    e = fa::launch_zero16(dq, 1, total_q, Hq, d, qst, stream);
+    return e == cudaSuccess ? FA_OK : cuda_fail("zero kernel launch", e);
+  }
+  if (!q_side || max_seqlen_q == 0) {  // no queries: dK = dV = 0
+    e = fa::launch_zero16(dk, 1, total_k, Hkv, d, kst, stream);
+    if (e == cudaSuccess) e = fa::launch_zero16(dv, 1, total_k, Hkv, d, kst, stream);
+    return e == cudaSuccess ? FA_OK : cuda_fail("zero kernel launch", e);
+  }
+  float *dq_acc = static_cast<float *>(workspace);
+  const int64_t acc_bytes = (static_cast<int64_t>(total_q) * Hq * d * 4 + 255) / 256 * 256;
+  float *dvec = reinterpret_cast<float *>(static_cast<char *>(workspace) + acc_bytes);
+  const int64_t vec_bytes = (static_cast<int64_t>(Hq) * total_q * 4 + 255) / 256 * 256;
+  int *sem = reinterpret_cast<int *>(static_cast<char *>(workspace) + acc_bytes + vec_bytes);
+  const int qblocks = ceil_div(max_seqlen_q, 128);
+  const int nsem = deterministic ? B * Hq * qblocks : 0;
+  CUtensorMap tq, tk, tv, tdo, tdq;
+  if ((st = make_map(&tq, q, d, total_q, Hq, 1, qst[1], d, 0, dtype)) != FA_OK ||
+      (st = make_map(&tdo, dout, d, total_q, Hq, 1, qst[1], d, 0, dtype)) != FA_OK ||
+      (st = make_map(&tk, k, d, total_k, Hkv, 1, kst[1], d, 0, dtype)) != FA_OK ||
+      (st = make_map(&tv, v, d, total_k, Hkv, 1, kst[1], d, 0, dtype)) != FA_OK ||
+      (st = make_map_f32(&tdq, dq_acc, d, total_q, Hq, 1)) != FA_OK)
+    return st;
+  const bool f16 = dtype == FA_FP16;
+  e = fa::launch_bwd_pre(d, f16, o, dout, 1, total_q, Hq, qst, qst, dvec, dq_acc, sem, nsem,
+                         stream);
+  if (e != cudaSuccess) return cuda_fail("backward preprocessing launch", e);
+  fa::BwdArgs ba{};
+  ba.lse = lse;
+  ba.dvec = dvec;
+  ba.lse_sb = 0;
+  ba.lse_sh = total_q;
+  ba.varlen = 1;
+  ba.cu_q = cu_seqlens_q;
+  ba.cu_k = cu_seqlens_k;
+  ba.total_q = total_q;
+  ba.total_k = total_k;
+  ba.qblocks = qblocks;
+  ba.dk = dk;
+  ba.dv = dv;
+  ba.dk_sb = ba.dv_sb = 0;
+  ba.dk_sn = ba.dv_sn = kst[1];
+  ba.dk_sh = ba.dv_sh = d;
+  ba.B = B;
+  ba.Nq = max_seqlen_q;
+  ba.Nk = max_seqlen_k;
+  ba.Hq = Hq;
+  ba.Hkv = Hkv;
+  ba.group = Hq / Hkv;
+  ba.kblocks = kblocks;
+  ba.d = d;
+  ba.sem = deterministic ? sem : nullptr;
+  ba.num_units = static_cast<int>(units);
+  ba.scale = scale;
+  ba.scale_log2 = scale_log2(scale);
+  ba.err = dev->err;
+  ba.timeout_ns = g_timeout_ns;
+  const int grid = static_cast<int>(units < dev->sm_count ? units : dev->sm_count);
+  e = fa::launch_bwd(fa::kernel_d(d), causal != 0, f16, tq, tk, tv, tdo, tdq, ba, grid, stream);
+  if (e != cudaSuccess) return cuda_fail("backward kernel launch", e);
+  e = fa::launch_bwd_post(d, f16, dq_acc, scale, dq, 1, total_q, Hq, qst, stream);
   return e == cudaSuccess ? FA_OK : cuda_fail("backward postprocessing launch", e);
 }
 

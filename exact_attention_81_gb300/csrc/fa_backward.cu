@@ -85,8 +85,13 @@ struct BBars {
 
 struct BUnit {
   int b, g, j;
-  int i0, nqb;   // query blocks [i0, nqb) of each head of the group
-  int nit;       // steps: group * (nqb - i0)
+  int nq, nk;          // lengths of the sequence
+  int q_tok, k_tok;    // packed-token offsets of the sequence (varlen), else 0
+  int tma_b;           // batch coordinate of the tensor maps (0 for varlen)
+  bool skip;           // key block j lies past the sequence's keys: nothing to do
+  bool bad;            // varlen prefix sums out of range: the sequence is skipped
+  int i0, nqb;         // query blocks [i0, nqb) of each head of the group
+  int nit;             // steps: group * (nqb - i0)
 };
 
 template <bool CAUSAL>
@@ -97,15 +102,35 @@ __device__ __forceinline__ BUnit bunit_of(const BwdArgs &a, int u) {
   const int r = u - w.j * bg;
   w.b = r / a.Hkv;
   w.g = r - w.b * a.Hkv;
-  w.nqb = (a.Nq + BQ - 1) / BQ;
+  if (a.varlen) {
+    const int q0 = a.cu_q[w.b], q1 = a.cu_q[w.b + 1];
+    const int k0 = a.cu_k[w.b], k1 = a.cu_k[w.b + 1];
+    const bool bad = q0 < 0 || q1 < q0 || q1 > a.total_q || k0 < 0 || k1 < k0 ||
+                     k1 > a.total_k || (q1 - q0) > a.Nq || (k1 - k0) > a.Nk;
+    w.nq = bad ? 0 : q1 - q0;
+    w.nk = bad ? 0 : k1 - k0;
+    w.q_tok = bad ? 0 : q0;
+    w.k_tok = bad ? 0 : k0;
+    w.tma_b = 0;
+    w.bad = bad;
+  } else {
+    w.bad = false;
+    w.nq = a.Nq;
+    w.nk = a.Nk;
+    w.q_tok = 0;
+    w.k_tok = 0;
+    w.tma_b = w.b;
+  }
+  w.skip = w.j * BKEY >= w.nk;
+  w.nqb = (w.nq + BQ - 1) / BQ;
   w.i0 = 0;
   if (CAUSAL) {
-    // first query block holding a row that sees key j*128: i*128 + 127 + (Nk - Nq) >= j*128
-    const long long t = static_cast<long long>(w.j) * BKEY - (a.Nk - a.Nq) - (BQ - 1);
+    // first query block holding a row that sees key j*128: i*128 + 127 + (nk - nq) >= j*128
+    const long long t = static_cast<long long>(w.j) * BKEY - (w.nk - w.nq) - (BQ - 1);
     w.i0 = t <= 0 ? 0 : static_cast<int>((t + BQ - 1) / BQ);
     if (w.i0 > w.nqb) w.i0 = w.nqb;
   }
-  w.nit = a.group * (w.nqb - w.i0);
+  w.nit = w.skip ? 0 : a.group * (w.nqb - w.i0);
   return w;
 }
 
@@ -202,14 +227,17 @@ __device__ void bwd_producer(const BwdArgs &a, const CUtensorMap *tq, const CUte
   uint32_t kv_n = 0, q_n = 0;
   for (int u = blockIdx.x; u < a.num_units; u += gridDim.x) {
     const BUnit w = bunit_of<CAUSAL>(a, u);
+    if (w.bad && w.j == 0 && w.g == 0 && lane == 0) atomicOr(a.err, DEVERR_BAD_CU_SEQLENS);
     if (w.nit == 0) continue;
     if (kv_n > 0 && !warp_wait(&bars->kv_empty, (kv_n - 1) & 1u, wc)) goto out;
     if (lane == 0) {
       mbar_arrive_expect_tx(&bars->kv_full, 2 * C::TILE);
 #pragma unroll
       for (int c = 0; c < C::KCH; ++c) {
-        tma_load_4d(smem + C::K_OFF + c * BOX, tk, &bars->kv_full, c * 64, w.g, w.j * BKEY, w.b);
-        tma_load_4d(smem + C::V_OFF + c * BOX, tv, &bars->kv_full, c * 64, w.g, w.j * BKEY, w.b);
+        tma_load_4d(smem + C::K_OFF + c * BOX, tk, &bars->kv_full, c * 64, w.g,
+                    w.k_tok + w.j * BKEY, w.tma_b);
+        tma_load_4d(smem + C::V_OFF + c * BOX, tv, &bars->kv_full, c * 64, w.g,
+                    w.k_tok + w.j * BKEY, w.tma_b);
       }
     }
     ++kv_n;
@@ -221,23 +249,25 @@ __device__ void bwd_producer(const BwdArgs &a, const CUtensorMap *tq, const CUte
         mbar_arrive_expect_tx(&bars->q_full, C::TILE);
 #pragma unroll
         for (int c = 0; c < C::KCH; ++c)
-          tma_load_4d(smem + C::Q_OFF + c * BOX, tq, &bars->q_full, c * 64, h, i * BQ, w.b);
+          tma_load_4d(smem + C::Q_OFF + c * BOX, tq, &bars->q_full, c * 64, h,
+                      w.q_tok + i * BQ, w.tma_b);
       }
       if (q_n > 0 && !warp_wait(&bars->do_empty, (q_n - 1) & 1u, wc)) goto out;
       if (lane == 0) {
         mbar_arrive_expect_tx(&bars->do_full, C::TILE);
 #pragma unroll
         for (int c = 0; c < C::KCH; ++c)
-          tma_load_4d(smem + C::DO_OFF + c * BOX, tdo, &bars->do_full, c * 64, h, i * BQ, w.b);
+          tma_load_4d(smem + C::DO_OFF + c * BOX, tdo, &bars->do_full, c * 64, h,
+                      w.q_tok + i * BQ, w.tma_b);
       }
       // LSE (log2 domain; rows past Nq or with no visible key give P = 0) and D.
       if (q_n > 0 && !warp_wait(&bars->vec_empty, (q_n - 1) & 1u, wc)) goto out;
-      const int64_t base = (static_cast<int64_t>(w.b) * a.Hq + h) * a.Nq;
+      const int64_t base = w.b * a.lse_sb + h * a.lse_sh + w.q_tok;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int qi = lane * 4 + e, q = i * BQ + qi;
         float l2 = INFINITY, dd = 0.f;
-        if (q < a.Nq) {
+        if (q < w.nq) {  // rows past the sequence (the next one's, for varlen) get P = 0
           const float l = a.lse[base + q];
           l2 = l == -INFINITY ? INFINITY : l * LOG2E;
           dd = a.dvec[base + q];
@@ -321,17 +351,18 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
   const float *dvec = lse2 + BQ;
   uint8_t *ds_s = smem + C::DS_OFF;
   uint8_t *dq_s = smem + C::DQ_OFF;
-  const int off = a.Nk - a.Nq;  // bottom-right alignment: query q sits at key position q + off
   uint32_t it = 0, acc_n = 0, grp = 0;
   for (int u = blockIdx.x; u < a.num_units; u += gridDim.x) {
     const BUnit w = bunit_of<CAUSAL>(a, u);
+    if (w.skip) continue;
+    const int off = w.nk - w.nq;  // bottom-right alignment: query q sits at key position q + off
     const int key = w.j * BKEY + r;
-    uint16_t *dkrow = reinterpret_cast<uint16_t *>(a.dk) + w.b * a.dk_sb + key * a.dk_sn +
-                      w.g * a.dk_sh;
-    uint16_t *dvrow = reinterpret_cast<uint16_t *>(a.dv) + w.b * a.dv_sb + key * a.dv_sn +
-                      w.g * a.dv_sh;
+    uint16_t *dkrow = reinterpret_cast<uint16_t *>(a.dk) + w.b * a.dk_sb +
+                      (w.k_tok + key) * a.dk_sn + w.g * a.dk_sh;
+    uint16_t *dvrow = reinterpret_cast<uint16_t *>(a.dv) + w.b * a.dv_sb +
+                      (w.k_tok + key) * a.dv_sn + w.g * a.dv_sh;
     if (w.nit == 0) {  // no query sees these keys: zero gradients
-      if (key < a.Nk) {
+      if (key < w.nk) {
 #pragma unroll
         for (int v = half * (D / 16); v < (half + 1) * (D / 16); ++v) {
           if (8 * v >= a.d) break;
@@ -368,7 +399,7 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
 #pragma unroll
           for (int x = 0; x < 4; ++x) {
             const int qi = qc + e4 + x;
-            const bool vis = key < a.Nk && (full || key <= q0 + qi + off);
+            const bool vis = key < w.nk && (full || key <= q0 + qi + off);
             const float pv = ex2_approx(fmaf(__uint_as_float(sr[e4 + x]), a.scale_log2, -lv[x]));
             p[x] = vis ? pv : 0.f;
             ds[x] = p[x] * (__uint_as_float(dr[e4 + x]) - dv[x]);
@@ -414,13 +445,13 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
       fence_proxy_async_smem();
       if (!group_sync(&bars->cgrp, grp, wc)) return;
       if (tid == 0) {
-        int *sem = a.sem ? a.sem + (static_cast<int64_t>(w.b) * a.Hq + h) * w.nqb + i : nullptr;
+        int *sem = a.sem ? a.sem + (static_cast<int64_t>(w.b) * a.Hq + h) * a.qblocks + i : nullptr;
         // Deterministic order: key block j adds after blocks 0 .. j-1 (the blocks that reach
         // query block i are a prefix 0 .. jmax).
         if (sem != nullptr && !wait_counter(sem, w.j, wc)) return;
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc)
-          tma_reduce_add_4d(tdq, dq_s + cc * BOX, cc * 32, h, q0, w.b);
+          tma_reduce_add_4d(tdq, dq_s + cc * BOX, cc * 32, h, w.q_tok + q0, w.tma_b);
         bulk_commit_group();
         if (sem != nullptr) {
           bulk_wait_all();             // the additions have been performed
@@ -440,7 +471,7 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
       uint32_t vr[32], kr[32];
       tmem_ld_x32(tmem + lane_off + T_DV + cc * 32, vr);
       tmem_ld_x32(tmem + lane_off + T_DK + cc * 32, kr);
-      if (key < a.Nk) {
+      if (key < w.nk) {
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
           if (cc * 32 + 8 * v >= a.d) break;  // columns past d are padding

@@ -137,8 +137,13 @@ inline int kernel_d(int d) { return d <= 64 ? 64 : 128; }
 
 // Backward pass: main kernel arguments (one work unit = batch, kv head, 128-key block).
 struct BwdArgs {
-  const float *lse;           // [B, Hq, Nq] natural-log LSE of the forward pass
-  const float *dvec;          // [B, Hq, Nq] D = rowsum(dO * O)
+  const float *lse;           // natural-log LSE of the forward pass, [B, Hq, Nq] or [Hq, total_q]
+  const float *dvec;          // D = rowsum(dO * O), same layout as lse
+  int64_t lse_sb, lse_sh;     // lse / dvec offset = b*lse_sb + h*lse_sh + token
+  int varlen;                 // packed sequences delimited by cu_q / cu_k (device)
+  const int *cu_q, *cu_k;
+  int total_q, total_k;
+  int qblocks;                // ceil(Nq / 128): query blocks of the longest sequence
   void *dk, *dv;              // outputs [B, Nk, Hkv, d], element strides below
   int64_t dk_sb, dk_sn, dk_sh, dv_sb, dv_sn, dv_sh;
   int B, Nq, Nk, Hq, Hkv, group;

@@ -298,6 +298,21 @@ size_t fa_bwd_workspace_size(int B, int Nq, int Hq, int d);
 
 fa_status fa_bwd(const fa_bwd_params *p, cudaStream_t stream);
 
+/*
+ * Backward of fa_fwd_varlen (packed sequences delimited by cu_seqlens): the same gradients,
+ * per sequence.  q, o, dout, dq: [total_q, Hq, d]; k, v, dk, dv: [total_k, Hkv, d], all
+ * contiguous; lse: [Hq, total_q] fp32 from fa_fwd_varlen; cu_seqlens_q / _k: DEVICE int32
+ * [B+1] as for fa_fwd_varlen (a sequence that breaks their rules is skipped and flagged in
+ * the device error word).  workspace: fa_bwd_workspace_size(B, max_seqlen_q, Hq, d) bytes.
+ * deterministic as in fa_bwd_params.
+ */
+fa_status fa_bwd_varlen(const void *q, const void *k, const void *v, const void *o,
+                        const void *dout, const float *lse, void *dq, void *dk, void *dv,
+                        const int *cu_seqlens_q, const int *cu_seqlens_k, int B,
+                        int max_seqlen_q, int max_seqlen_k, int total_q, int total_k, int Hq,
+                        int Hkv, int d, float scale, int causal, int dtype, void *workspace,
+                        size_t workspace_bytes, int deterministic, cudaStream_t stream);
+
 /* sizeof(fa_bwd_params), for bindings that check their struct layout. */
 size_t fa_bwd_params_size(void);
 

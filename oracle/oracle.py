@@ -412,3 +412,27 @@ def attention_bwd(q, k, v, dout, scale: float, causal: bool = False,
     if rc != 0:
         raise ValueError("oracle_bwd rejected its arguments")
     return dq, dk, dv, lse, D
+
+
+def attention_varlen_bwd(q, k, v, dout, cu_seqlens_q, cu_seqlens_k, scale: float,
+                         causal: bool = False, nthreads: int | None = None, elem=None):
+    """Gradients of packed varlen attention: each sequence is an independent dense problem
+    (capabilities table, varlen row), so this applies attention_bwd sequence by sequence.
+    q, dout [total_q, Hq, d]; k, v [total_k, Hkv, d].  Returns (dQ, dK, dV) float64 in the
+    packed layouts."""
+    import torch  # local: only the tests hand torch tensors in
+    cu_q = [int(x) for x in np.asarray(cu_seqlens_q).reshape(-1)]
+    cu_k = [int(x) for x in np.asarray(cu_seqlens_k).reshape(-1)]
+    dq = np.zeros(tuple(q.shape), np.float64)
+    dk = np.zeros(tuple(k.shape), np.float64)
+    dv = np.zeros(tuple(v.shape), np.float64)
+    for b in range(len(cu_q) - 1):
+        a, e = cu_q[b], cu_q[b + 1]
+        ka, ke = cu_k[b], cu_k[b + 1]
+        if e == a or ke == ka:
+            continue  # no queries or no keys: every gradient of the sequence is 0
+        g = attention_bwd(q[a:e].unsqueeze(0).contiguous(), k[ka:ke].unsqueeze(0).contiguous(),
+                          v[ka:ke].unsqueeze(0).contiguous(),
+                          dout[a:e].unsqueeze(0).contiguous(), scale, causal, nthreads, elem)
+        dq[a:e], dk[ka:ke], dv[ka:ke] = g[0][0], g[1][0], g[2][0]
+    return dq, dk, dv

@@ -15,8 +15,9 @@ import pytest
 import torch
 
 import oracle.oracle as ORACLE
-from exact_attention_81_gb300 import FA_OK, fa_bwd, fa_fwd, get_last_device_error
-from exact_attention_81_gb300.inputs import WORKLOADS, bf16_normal, dense_inputs
+from exact_attention_81_gb300 import (FA_OK, fa_bwd, fa_bwd_varlen, fa_fwd, fa_fwd_varlen,
+                                      get_last_device_error)
+from exact_attention_81_gb300.inputs import WORKLOADS, bf16_normal, dense_inputs, varlen_inputs
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -128,3 +129,50 @@ def test_backward_full_size_one_head():
         e_gpu = float(np.abs(g.double().cpu().numpy() - r).max())
         e_base = float(np.abs(b.double().numpy() - r).max())
         assert e_gpu <= 2 * e_base + 1e-4, f"causal8k {name}: {e_gpu:.3e} vs {e_base:.3e}"
+
+
+def _baseline_varlen(q, k, v, do, cu_q, cu_k, scale, causal):
+    """The PyTorch baseline sequence by sequence, in the packed layouts."""
+    outs = [torch.zeros(t.shape, dtype=t.dtype) for t in (q, k, v)]
+    cq, ck = cu_q.tolist(), cu_k.tolist()
+    for b in range(len(cq) - 1):
+        a, e, ka, ke = cq[b], cq[b + 1], ck[b], ck[b + 1]
+        if e == a or ke == ka:
+            continue
+        g = _baseline(q[a:e].unsqueeze(0), k[ka:ke].unsqueeze(0), v[ka:ke].unsqueeze(0),
+                      do[a:e].unsqueeze(0), scale, causal)
+        outs[0][a:e], outs[1][ka:ke], outs[2][ka:ke] = g[0][0], g[1][0], g[2][0]
+    return outs
+
+
+@pytest.mark.parametrize("causal,deterministic,dt", [(True, False, torch.bfloat16),
+                                                     (False, False, torch.bfloat16),
+                                                     (True, True, torch.bfloat16),
+                                                     (True, False, torch.float16)])
+def test_backward_varlen(causal, deterministic, dt):
+    sq = [5, 0, 333, 128, 129, 700, 1]
+    sk = [7, 3, 333, 400, 200, 700, 0]
+    Hq, Hkv, d = 4, 2, 128
+    q, k, v, cu_q, cu_k = varlen_inputs(sq, sk, Hq, Hkv, d, seed=740, device=DEV, dtype=dt)
+    do = bf16_normal(tuple(q.shape), seed=741, device=DEV, dtype=dt)
+    scale = float(np.float32(1 / math.sqrt(d)))
+    o, lse = fa_fwd_varlen(q, k, v, cu_q, cu_k, max(sq), max(sk), causal=causal, scale=scale)
+    g = fa_bwd_varlen(q, k, v, o, lse, do, cu_q, cu_k, max(sq), max(sk), causal=causal,
+                      scale=scale, deterministic=deterministic)
+    assert get_last_device_error() == FA_OK
+    ref = ORACLE.attention_varlen_bwd(q.cpu(), k.cpu(), v.cpu(), do.cpu(), cu_q.cpu(),
+                                      cu_k.cpu(), scale, causal)
+    base = _baseline_varlen(q.cpu(), k.cpu(), v.cpu(), do.cpu(), cu_q.cpu(), cu_k.cpu(), scale,
+                            causal)
+    for name, a, r, b in zip(("dQ", "dK", "dV"), g, ref, base):
+        a = a.double().cpu().numpy()
+        e_gpu = float(np.abs(a - r).max())
+        e_base = float(np.abs(b.double().numpy() - r).max())
+        assert e_gpu <= 2 * e_base + 1e-4, f"varlen {name}: {e_gpu:.3e} vs {e_base:.3e}"
+    # sequences without keys give dQ = 0; keys no query sees give dK = dV = 0
+    assert torch.all(g[0][cu_q[6]:cu_q[7]] == 0)
+    assert torch.all(g[1][cu_k[1]:cu_k[2]] == 0) and torch.all(g[2][cu_k[1]:cu_k[2]] == 0)
+    if deterministic:
+        g2 = fa_bwd_varlen(q, k, v, o, lse, do, cu_q, cu_k, max(sq), max(sk), causal=causal,
+                           scale=scale, deterministic=True)
+        assert all(torch.equal(x, y) for x, y in zip(g, g2))
