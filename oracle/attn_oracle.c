@@ -586,6 +586,10 @@ int oracle_round16(const float *x, int64_t n, uint16_t *out, int elem) {
  *     dK_j  = scale sum_i dS_ij q_i
  * Masked pairs have P = 0 and contribute nothing; with grouped-query attention dK and dV
  * of a key/value head sum over the query heads that read it.
+ * With the score modifiers the softmax runs over z_ij (window, softcap, ALiBi as in the
+ * forward) and the chain rule passes through z(s), s = scale q . k: the ALiBi bias does not
+ * depend on q or k, a softcap c gives dz/ds = 1 - tanh^2(s / c), so dS above becomes
+ * P_ij (dP_ij - D_i) dz/ds before it enters dQ and dK.
  * Two passes, each over independent items: pass 1 per query row (its LSE, D_i and
  * dQ_i), pass 2 per key row (dK_j and dV_j, with P recomputed from pass 1's LSE).
  */
@@ -593,8 +597,12 @@ int oracle_round16(const float *x, int64_t n, uint16_t *out, int elem) {
 typedef struct {
     const uint16_t *q, *k, *v, *dout;
     int64_t qs[3], ks[3], vs[3], dos[3];
-    int B, Nq, Nk, Hq, Hkv, d, causal, elem;
+    int B, Nq, Nk, Hq, Hkv, d, elem;
     double scale;
+    int64_t wl, wr;           /* window bounds (causal folded in as wr = 0), -1 = unbounded */
+    double softcap;
+    const double *alibi;      /* slope of (b, h) at alibi[b * alibi_sb + h], or NULL */
+    int64_t alibi_sb;
     double *lse, *D;          /* [B, Hq, Nq] (pass 1 output, pass 2 input) */
     double *dq, *dk, *dv;     /* contiguous [B, N, H, d] */
     int pass, nthreads, tid;
@@ -606,11 +614,18 @@ static double dot16(const uint16_t *a, const uint16_t *b, int d, int elem) {
     return acc;
 }
 
-/* Keys visible to query i: [0, hi) (bottom-right causal or all). */
-static int64_t bwd_key_end(const bwd_job_t *J, int64_t i) {
-    if (!J->causal) return J->Nk;
-    int64_t last = i + (J->Nk - J->Nq);
-    return last < 0 ? 0 : (last + 1 < J->Nk ? last + 1 : J->Nk);
+/* Modified score z of raw dot product acc for query position pos and key j, and dz/ds. */
+static double bwd_score(const bwd_job_t *J, double acc, double slope, int64_t pos, int64_t j,
+                        double *dzds) {
+    double z = J->scale * acc;
+    *dzds = 1.0;
+    if (J->softcap > 0.0) {
+        double t = tanh(z / J->softcap);
+        z = J->softcap * t;
+        *dzds = 1.0 - t * t;
+    }
+    if (J->alibi) z -= slope * fabs((double)(pos - j));
+    return z;
 }
 
 static void *bwd_worker(void *arg) {
@@ -623,7 +638,10 @@ static void *bwd_worker(void *arg) {
         for (int64_t w = J->tid; w < total; w += J->nthreads) {
             int b = (int)(w / ((int64_t)J->Hq * J->Nq));
             int h = (int)((w / J->Nq) % J->Hq);
-            int64_t i = w % J->Nq, g = h / G, n = bwd_key_end(J, i);
+            int64_t i = w % J->Nq, g = h / G, pos = i + (J->Nk - J->Nq), lo, hi;
+            visible_range(pos, J->Nk, J->wl, J->wr, &lo, &hi);
+            int64_t n = hi - lo;
+            double slope = J->alibi ? J->alibi[b * J->alibi_sb + h] : 0.0;
             const uint16_t *qi = J->q + b * J->qs[0] + i * J->qs[1] + h * J->qs[2];
             const uint16_t *doi = J->dout + b * J->dos[0] + i * J->dos[1] + h * J->dos[2];
             double *dqi = J->dq + (((int64_t)b * J->Nq + i) * J->Hq + h) * d;
@@ -631,9 +649,12 @@ static void *bwd_worker(void *arg) {
             for (int c = 0; c < d; ++c) dqi[c] = 0.0;
             if (n == 0) { J->lse[li] = -INFINITY; J->D[li] = 0.0; continue; }
             double m = -INFINITY;
-            for (int64_t j = 0; j < n; ++j) {
-                s[j] = J->scale * dot16(qi, J->k + b * J->ks[0] + j * J->ks[1] + g * J->ks[2], d, J->elem);
-                if (s[j] > m) m = s[j];
+            for (int64_t t = 0; t < n; ++t) {
+                int64_t j = lo + t;
+                double dz;
+                s[t] = bwd_score(J, dot16(qi, J->k + b * J->ks[0] + j * J->ks[1] + g * J->ks[2], d,
+                                          J->elem), slope, pos, j, &dz);
+                if (s[t] > m) m = s[t];
             }
             double l = 0.0;
             for (int64_t j = 0; j < n; ++j) {
@@ -642,14 +663,18 @@ static void *bwd_worker(void *arg) {
                 l += e;
             }
             double Di = 0.0;
-            for (int64_t j = 0; j < n; ++j) {
-                s[j] /= l;                                                   /* P_ij */
-                dp[j] = dot16(doi, J->v + b * J->vs[0] + j * J->vs[1] + g * J->vs[2], d, J->elem);
-                Di += s[j] * dp[j];
+            for (int64_t t = 0; t < n; ++t) {
+                int64_t j = lo + t;
+                s[t] /= l;                                                   /* P_ij */
+                dp[t] = dot16(doi, J->v + b * J->vs[0] + j * J->vs[1] + g * J->vs[2], d, J->elem);
+                Di += s[t] * dp[t];
             }
-            for (int64_t j = 0; j < n; ++j) {
-                double ds = s[j] * (dp[j] - Di);
+            for (int64_t t = 0; t < n; ++t) {
+                int64_t j = lo + t;
                 const uint16_t *kj = J->k + b * J->ks[0] + j * J->ks[1] + g * J->ks[2];
+                double dz;
+                bwd_score(J, dot16(qi, kj, d, J->elem), slope, pos, j, &dz);
+                double ds = s[t] * (dp[t] - Di) * dz;
                 for (int c = 0; c < d; ++c) dqi[c] += J->scale * ds * widen(kj[c], J->elem);
             }
             J->lse[li] = m + log(l);
@@ -667,13 +692,18 @@ static void *bwd_worker(void *arg) {
             double *dvj = J->dv + (((int64_t)b * J->Nk + j) * J->Hkv + g) * d;
             for (int c = 0; c < d; ++c) { dkj[c] = 0.0; dvj[c] = 0.0; }
             for (int h = g * G; h < (g + 1) * G; ++h) {
+                double slope = J->alibi ? J->alibi[b * J->alibi_sb + h] : 0.0;
                 for (int64_t i = 0; i < J->Nq; ++i) {
-                    if (j >= bwd_key_end(J, i)) continue;
+                    int64_t pos = i + (J->Nk - J->Nq), lo, hi;
+                    visible_range(pos, J->Nk, J->wl, J->wr, &lo, &hi);
+                    if (j < lo || j >= hi) continue;
                     int64_t li = ((int64_t)b * J->Hq + h) * J->Nq + i;
                     const uint16_t *qi = J->q + b * J->qs[0] + i * J->qs[1] + h * J->qs[2];
                     const uint16_t *doi = J->dout + b * J->dos[0] + i * J->dos[1] + h * J->dos[2];
-                    double p = exp(J->scale * dot16(qi, kj, d, J->elem) - J->lse[li]);
-                    double ds = p * (dot16(doi, vj, d, J->elem) - J->D[li]);
+                    double dz;
+                    double z = bwd_score(J, dot16(qi, kj, d, J->elem), slope, pos, j, &dz);
+                    double p = exp(z - J->lse[li]);
+                    double ds = p * (dot16(doi, vj, d, J->elem) - J->D[li]) * dz;
                     for (int c = 0; c < d; ++c) {
                         dvj[c] += p * widen(doi[c], J->elem);
                         dkj[c] += J->scale * ds * widen(qi[c], J->elem);
@@ -708,16 +738,23 @@ int oracle_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const ui
                int B, int Nq, int Nk, int Hq, int Hkv, int d, const int64_t *q_strides,
                const int64_t *k_strides, const int64_t *v_strides, const int64_t *do_strides,
                double scale, int causal, double *dq, double *dk, double *dv, double *lse,
-               double *D, int nthreads, int elem) {
+               double *D, int nthreads, int elem, int window_left, int window_right,
+               double softcap, const double *alibi, int64_t alibi_sb) {
     if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || elem < 0 || elem > 1) return -1;
+    if (!(softcap >= 0.0) || alibi_sb < 0) return -1;
     bwd_job_t J;
     memset(&J, 0, sizeof J);
+    J.wl = window_left < 0 ? -1 : window_left;
+    J.wr = causal ? 0 : (window_right < 0 ? -1 : window_right);
+    J.softcap = softcap;
+    J.alibi = alibi;
+    J.alibi_sb = alibi_sb;
     J.q = q; J.k = k; J.v = v; J.dout = dout;
     for (int a = 0; a < 3; ++a) {
         J.qs[a] = q_strides[a]; J.ks[a] = k_strides[a]; J.vs[a] = v_strides[a];
         J.dos[a] = do_strides[a];
     }
-    J.B = B; J.Nq = Nq; J.Nk = Nk; J.Hq = Hq; J.Hkv = Hkv; J.d = d; J.causal = causal;
+    J.B = B; J.Nq = Nq; J.Nk = Nk; J.Hq = Hq; J.Hkv = Hkv; J.d = d;
     J.elem = elem; J.scale = scale;
     J.lse = lse; J.D = D; J.dq = dq; J.dk = dk; J.dv = dv;
     J.nthreads = nthreads;

@@ -71,7 +71,7 @@ def _load():
                                              p, i] + mod
             lib.oracle_rotary.argtypes = [p, i64, i64, i, p, p, p, i, i, p, i]
             lib.oracle_bwd.argtypes = [p, p, p, p, i, i, i, i, i, i, p, p, p, p, d, i, p, p, p,
-                                       p, p, i, i]
+                                       p, p, i, i] + mod
             lib.oracle_bwd.restype = ctypes.c_int
             lib.oracle_round16.argtypes = [p, i64, p, i]
             for f in (lib.oracle_fwd, lib.oracle_fwd_rows, lib.oracle_fwd_varlen,
@@ -388,7 +388,8 @@ def kvcache_step(q, k_cache, v_cache, cache_seqlens, scale: float, k_new=None, v
 
 
 def attention_bwd(q, k, v, dout, scale: float, causal: bool = False,
-                  nthreads: int | None = None, elem=None):
+                  nthreads: int | None = None, elem=None, window=(-1, -1), softcap=0.0,
+                  alibi_slopes=None):
     """Gradients of dense attention for the upstream gradient dout [B,Nq,Hq,d].
 
     Returns (dQ [B,Nq,Hq,d], dK [B,Nk,Hkv,d], dV [B,Nk,Hkv,d], LSE [B,Hq,Nq],
@@ -400,6 +401,7 @@ def attention_bwd(q, k, v, dout, scale: float, causal: bool = False,
     _, Nk, Hkv, _ = k.shape
     if dout.shape != q.shape:
         raise ValueError("dout must have the shape of q")
+    mod = _Mod(B, Hq, window, softcap, alibi_slopes)
     dq = np.zeros((B, Nq, Hq, d), np.float64)
     dk = np.zeros((B, Nk, Hkv, d), np.float64)
     dv = np.zeros((B, Nk, Hkv, d), np.float64)
@@ -408,14 +410,15 @@ def attention_bwd(q, k, v, dout, scale: float, causal: bool = False,
     rc = _load().oracle_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), B, Nq, Nk, Hq, Hkv, d,
                             _strides4(q), _strides4(k), _strides4(v), _strides4(dout),
                             float(scale), int(bool(causal)), _ptr(dq), _ptr(dk), _ptr(dv),
-                            _ptr(lse), _ptr(D), _threads(nthreads), el)
+                            _ptr(lse), _ptr(D), _threads(nthreads), el, *mod.args())
     if rc != 0:
         raise ValueError("oracle_bwd rejected its arguments")
     return dq, dk, dv, lse, D
 
 
 def attention_varlen_bwd(q, k, v, dout, cu_seqlens_q, cu_seqlens_k, scale: float,
-                         causal: bool = False, nthreads: int | None = None, elem=None):
+                         causal: bool = False, nthreads: int | None = None, elem=None,
+                         window=(-1, -1), softcap=0.0, alibi_slopes=None):
     """Gradients of packed varlen attention: each sequence is an independent dense problem
     (capabilities table, varlen row), so this applies attention_bwd sequence by sequence.
     q, dout [total_q, Hq, d]; k, v [total_k, Hkv, d].  Returns (dQ, dK, dV) float64 in the
@@ -431,8 +434,14 @@ def attention_varlen_bwd(q, k, v, dout, cu_seqlens_q, cu_seqlens_k, scale: float
         ka, ke = cu_k[b], cu_k[b + 1]
         if e == a or ke == ka:
             continue  # no queries or no keys: every gradient of the sequence is 0
+        sl = None
+        if alibi_slopes is not None:
+            sl = np.asarray(alibi_slopes.detach().cpu() if hasattr(alibi_slopes, "detach")
+                            else alibi_slopes, np.float32)
+            sl = sl[b] if sl.ndim == 2 else sl
         g = attention_bwd(q[a:e].unsqueeze(0).contiguous(), k[ka:ke].unsqueeze(0).contiguous(),
                           v[ka:ke].unsqueeze(0).contiguous(),
-                          dout[a:e].unsqueeze(0).contiguous(), scale, causal, nthreads, elem)
+                          dout[a:e].unsqueeze(0).contiguous(), scale, causal, nthreads, elem,
+                          window=window, softcap=softcap, alibi_slopes=sl)
         dq[a:e], dk[ka:ke], dv[ka:ke] = g[0][0], g[1][0], g[2][0]
     return dq, dk, dv

@@ -873,10 +873,57 @@ def pin_bwd_closed_forms(O):
     _close(g1[2], dv2.reshape(B, N, Hkv, Hq // Hkv, d).sum(axis=3), 1e-12, "GQA dV vs MHA")
 
 
+
+def pin_bwd_modifiers(O):
+    """Backward with the score modifiers: float64 torch autograd through the explicit
+    attention (z = scale q.k, softcap c tanh(z / c), ALiBi -slope |pos - j|, window mask,
+    softmax, P V); every row sees at least one key."""
+    cases = [
+        dict(Nq=33, Nk=33, causal=False, window=(5, 2)),
+        dict(Nq=30, Nk=30, causal=True, softcap=2.0),
+        dict(Nq=20, Nk=45, causal=True, alibi=True),
+        dict(Nq=40, Nk=40, causal=False, window=(9, 3), softcap=1.5, alibi=True),
+    ]
+    for n, c in enumerate(cases):
+        B, Hq, Hkv, d = 2, 4, 2, 16
+        Nq, Nk = c["Nq"], c["Nk"]
+        q, k, v = dense_inputs(B, Nq, Nk, Hq, Hkv, d, seed=430 + n)
+        do = bf16_normal((B, Nq, Hq, d), seed=440 + n)
+        scale, cap = 0.35, c.get("softcap", 0.0)
+        slopes = np.array([[0.3, 0.1, 0.7, 0.05], [0.2, 0.5, 0.01, 0.9]], np.float32) \
+            if c.get("alibi") else None
+        wl, wr = c.get("window", (-1, -1))
+        dq, dk, dv, _, _ = O.attention_bwd(q, k, v, do, scale, c["causal"], window=(wl, wr),
+                                           softcap=cap, alibi_slopes=slopes)
+        G = Hq // Hkv
+        qq = _f64(q).permute(0, 2, 1, 3).requires_grad_()
+        kk = _f64(k).permute(0, 2, 1, 3).requires_grad_()
+        vv = _f64(v).permute(0, 2, 1, 3).requires_grad_()
+        z = torch.matmul(qq, kk.repeat_interleave(G, 1).transpose(-1, -2)) * scale
+        if cap > 0:
+            z = cap * torch.tanh(z / cap)
+        pos = torch.arange(Nq)[:, None] + (Nk - Nq)
+        j = torch.arange(Nk)[None, :]
+        if slopes is not None:
+            z = z - torch.tensor(slopes, dtype=torch.float64)[:, :, None, None] * \
+                (pos - j).abs().double()
+        vis = torch.ones(Nq, Nk, dtype=torch.bool)
+        if wl >= 0:
+            vis &= j >= pos - wl
+        if wr >= 0 or c["causal"]:
+            vis &= j <= pos + (0 if c["causal"] else wr)
+        assert bool(vis.any(dim=1).all()), "setup: every row must see a key"
+        p = torch.softmax(z.masked_fill(~vis, float("-inf")), dim=-1)
+        torch.matmul(p, vv.repeat_interleave(G, 1)).backward(_f64(do).permute(0, 2, 1, 3))
+        _close(dq, qq.grad.permute(0, 2, 1, 3).numpy(), 1e-11, f"modifier dQ case {n}")
+        _close(dk, kk.grad.permute(0, 2, 1, 3).numpy(), 1e-11, f"modifier dK case {n}")
+        _close(dv, vv.grad.permute(0, 2, 1, 3).numpy(), 1e-11, f"modifier dV case {n}")
+
+
 ALL_PINS = [pin_library, pin_library_fp16, pin_fp16_values, pin_uniform_scores, pin_single_key, pin_constant_v, pin_two_keys,
             pin_empty_rows, pin_hard_max, pin_probs, pin_shift, pin_permutation, pin_gqa,
             pin_varlen, pin_kvcache, pin_rows, pin_recurrence, pin_lse_recompute,
             pin_window_uniform, pin_window_diagonal, pin_window_library, pin_softcap_limits,
             pin_alibi_geometric, pin_alibi_library, pin_mod_bruteforce, pin_mod_paths,
             pin_round16_library, pin_rotary, pin_kv_append, pin_kv_paged, pin_bwd_library,
-            pin_bwd_closed_forms]
+            pin_bwd_closed_forms, pin_bwd_modifiers]

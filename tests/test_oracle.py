@@ -73,11 +73,19 @@ MUTATIONS = [
     ("bf16 rounding truncates", "u += 0x7fffu + lsb;", "u += 0u * lsb;"),
     ("fp16 rounding ties away from zero",
      "if (rem > half || (rem == half && (q & 1u))) q += 1u;", "if (rem >= half) q += 1u;"),
-    ("dS without the D term (pass 1)", "double ds = s[j] * (dp[j] - Di);",
-     "double ds = s[j] * dp[j];"),
+    ("dS without the D term (pass 1)", "double ds = s[t] * (dp[t] - Di) * dz;",
+     "double ds = s[t] * dp[t] * dz;"),
     ("dS without the D term (pass 2)",
-     "double ds = p * (dot16(doi, vj, d, J->elem) - J->D[li]);",
-     "double ds = p * dot16(doi, vj, d, J->elem);"),
+     "double ds = p * (dot16(doi, vj, d, J->elem) - J->D[li]) * dz;",
+     "double ds = p * dot16(doi, vj, d, J->elem) * dz;"),
+    ("softcap derivative dropped (pass 1)", "double ds = s[t] * (dp[t] - Di) * dz;",
+     "double ds = s[t] * (dp[t] - Di);"),
+    ("softcap derivative dropped (pass 2)",
+     "double ds = p * (dot16(doi, vj, d, J->elem) - J->D[li]) * dz;",
+     "double ds = p * (dot16(doi, vj, d, J->elem) - J->D[li]);"),
+    ("softcap derivative without the square", "*dzds = 1.0 - t * t;", "*dzds = 1.0 - t;"),
+    ("ALiBi missing from the backward scores", "if (J->alibi) z -= slope * fabs((double)(pos - j));",
+     "if (J->alibi) z -= 0.0 * slope;"),
     ("dK without the scale", "dkj[c] += J->scale * ds * widen(qi[c], J->elem);",
      "dkj[c] += ds * widen(qi[c], J->elem);"),
     ("dV from dS instead of P", "dvj[c] += p * widen(doi[c], J->elem);",
@@ -86,7 +94,7 @@ MUTATIONS = [
      "dqi[c] += J->scale * ds * widen(qi[c], J->elem);"),
     ("GQA dK and dV from one query head", "for (int h = g * G; h < (g + 1) * G; ++h) {",
      "for (int h = g * G; h < g * G + 1; ++h) {"),
-    ("causal mask ignored in the key pass", "if (j >= bwd_key_end(J, i)) continue;",
+    ("window ignored in the key pass", "if (j < lo || j >= hi) continue;",
      "if (j >= J->Nk) continue;"),
     ("appended row one past the length", "i0, r = locate(b, int(lens[b]))",
      "i0, r = locate(b, int(lens[b]) + 1)", "py"),
