@@ -585,6 +585,18 @@ def extra_workloads(args, dev, pk, world, dist):
     tf = 2.5 * flops(w) / (ms * 1e-3) / 1e12
     res["causal8k_backward_deterministic"] = {"ms": round(ms, 4), "TFLOPS": round(tf, 2),
                                               "frac_of_bf16_peak": round(tf / pk["bf16"], 4)}
+    # backward with the modifiers (FLOPs: 10 d per visible pair; the causal convention else)
+    for name, kw, work in [
+            ("causal8k_backward_window4096", {"window_size": (4096, 0)},
+             10.0 * w.d * w.B * w.Hq * window_pairs(w.Nq, w.Nk, 4096, 0)),
+            ("causal8k_backward_softcap_alibi", {"softcap": 30.0, "alibi_slopes": slopes},
+             2.5 * flops(w))]:
+        o, l = fa.fa_fwd(q, k, v, causal=True, **kw)
+        ms = time_calls(lambda: fa.fa_bwd(q, k, v, o, l, do, causal=True, dq=dq, dk=dk, dv=dv,
+                                          workspace=bws, **kw), max(10, args.steps // 4), stream)
+        tf = work / (ms * 1e-3) / 1e12
+        res[name] = {"ms": round(ms, 4), "TFLOPS": round(tf, 2),
+                     "frac_of_bf16_peak": round(tf / pk["bf16"], 4)}
     del q, k, v, do, o, l, dq, dk, dv, bws
     w = WORKLOADS["decode"]
     q, kc, vc, lens = kvcache_workload_inputs(w, device=dev)

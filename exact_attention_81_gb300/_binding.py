@@ -115,6 +115,7 @@ class BwdParams(ctypes.Structure):
         ("scale", ctypes.c_float), ("causal", ctypes.c_int), ("dtype", ctypes.c_int),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("deterministic", ctypes.c_int),
+        ("mod", ScoreMod),
     ]
 
 
@@ -160,7 +161,7 @@ def load_library(path: str | None = None):
         lib.fa_bwd.argtypes = [ctypes.POINTER(BwdParams), vp]
         lib.fa_bwd.restype = i
         lib.fa_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i,
-                                      i, i, i, f, i, i, vp, sz, i, vp]
+                                      i, i, i, f, i, i, vp, sz, i, pmod, vp]
         lib.fa_bwd_varlen.restype = i
         lib.fa_bwd_workspace_size.argtypes = [i, i, i, i]
         lib.fa_bwd_workspace_size.restype = sz
@@ -407,7 +408,8 @@ def fa_bwd_workspace_size(B: int, Nq: int, Hq: int, d: int) -> int:
 
 
 def fa_bwd(q, k, v, out, lse, dout, causal: bool = False, scale: float | None = None,
-           dq=None, dk=None, dv=None, workspace=None, stream=None, deterministic=False):
+           dq=None, dk=None, dv=None, workspace=None, stream=None, deterministic=False,
+           window_size=None, softcap: float = 0.0, alibi_slopes=None):
     """Backward of fa_fwd: q/out/dout [B,Nq,Hq,d], k/v [B,Nk,Hkv,d] (bf16 or fp16, CUDA),
     lse [B,Hq,Nq] fp32 from the forward call.  deterministic fixes the order in which the
     key blocks add into dQ.  Returns (dq, dk, dv)."""
@@ -445,13 +447,15 @@ def fa_bwd(q, k, v, out, lse, dout, causal: bool = False, scale: float | None = 
     p.dtype = _DTYPE[q.dtype]
     p.workspace, p.workspace_bytes = _ptr(workspace), workspace.numel()
     p.deterministic = int(bool(deterministic))
+    p.mod = _score_mod(B, Hq, q.device, window_size, softcap, alibi_slopes)
     _check(load_library().fa_bwd(ctypes.byref(p), _stream_handle(stream)), "fa_bwd")
     return dq, dk, dv
 
 
 def fa_bwd_varlen(q, k, v, out, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
                   max_seqlen_k: int, causal: bool = False, scale: float | None = None, dq=None,
-                  dk=None, dv=None, workspace=None, stream=None, deterministic=False):
+                  dk=None, dv=None, workspace=None, stream=None, deterministic=False,
+                  window_size=None, softcap: float = 0.0, alibi_slopes=None):
     """Backward of fa_fwd_varlen: q/out/dout [total_q,Hq,d], k/v [total_k,Hkv,d] contiguous,
     lse [Hq,total_q] fp32 from the forward call.  Returns (dq, dk, dv)."""
     _require_bf16_cuda("q", q, 3)
@@ -472,11 +476,12 @@ def fa_bwd_varlen(q, k, v, out, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqle
     if workspace is None:
         workspace = torch.empty((max(need, 256),), dtype=torch.uint8, device=q.device)
     sc = default_scale(d) if scale is None else float(scale)
+    mod = _score_mod(B, Hq, q.device, window_size, softcap, alibi_slopes)
     st = load_library().fa_bwd_varlen(
         _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
         _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), B, int(max_seqlen_q), int(max_seqlen_k),
         total_q, total_k, Hq, Hkv, d, sc, int(bool(causal)), _DTYPE[q.dtype], _ptr(workspace),
-        workspace.numel(), int(bool(deterministic)), _stream_handle(stream))
+        workspace.numel(), int(bool(deterministic)), ctypes.byref(mod), _stream_handle(stream))
     _check(st, "fa_bwd_varlen")
     return dq, dk, dv
 

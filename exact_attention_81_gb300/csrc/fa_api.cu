@@ -213,14 +213,20 @@ fa_status plan_mod(const fa_score_mod *m, int causal, ModPlan *out) {
   return FA_OK;
 }
 
-void apply_mod(const ModPlan &m, float scale, fa::PrefillArgs *pa) {
-  pa->wl = m.wl;
-  pa->wr = m.wr;
+// The modifier fields shared by the forward and backward argument blocks.
+template <class Args>
+void set_mod_fields(const ModPlan &m, float scale, Args *a) {
+  a->wl = m.wl;
+  a->wr = m.wr;
   // raw score s: softcap * tanh(scale * s / softcap), then * log2(e)
-  pa->sc_in = m.softcap > 0.f ? scale / m.softcap : 0.f;
-  pa->sc_out = m.softcap > 0.f ? static_cast<float>(m.softcap * 1.4426950408889634) : 0.f;
-  pa->alibi = m.alibi;
-  pa->alibi_sb = m.alibi_sb;
+  a->sc_in = m.softcap > 0.f ? scale / m.softcap : 0.f;
+  a->sc_out = m.softcap > 0.f ? static_cast<float>(m.softcap * 1.4426950408889634) : 0.f;
+  a->alibi = m.alibi;
+  a->alibi_sb = m.alibi_sb;
+}
+
+void apply_mod(const ModPlan &m, float scale, fa::PrefillArgs *pa) {
+  set_mod_fields(m, scale, pa);
   pa->desc = m.wr >= 0;
 }
 
@@ -640,6 +646,9 @@ fa_status fa_bwd(const fa_bwd_params *p, cudaStream_t stream) {
   if (q_side && k_side &&
       (a.workspace == nullptr || a.workspace_bytes < need || !aligned(a.workspace, 256)))
     return FA_ERR_WORKSPACE;
+  ModPlan mod;
+  fa_status mst = plan_mod(&a.mod, a.causal, &mod);
+  if (mst != FA_OK) return mst;
   const int kblocks = ceil_div(a.Nk, 128);
   const int64_t units = static_cast<int64_t>(kblocks) * a.B * a.Hkv;
   if (units > INT32_MAX) return FA_ERR_INVALID_ARG;
@@ -702,14 +711,14 @@ fa_status fa_bwd(const fa_bwd_params *p, cudaStream_t stream) {
   ba.kblocks = kblocks;
   ba.d = a.d;
   ba.sem = a.deterministic ? sem : nullptr;
+  set_mod_fields(mod, a.scale, &ba);
   ba.num_units = static_cast<int>(units);
   ba.scale = a.scale;
   ba.scale_log2 = scale_log2(a.scale);
   ba.err = dev->err;
   ba.timeout_ns = g_timeout_ns;
   const int grid = static_cast<int>(units < dev->sm_count ? units : dev->sm_count);
-  e = fa::launch_bwd(fa::kernel_d(a.d), a.causal != 0, f16, tq, tk, tv, tdo, tdq, ba, grid,
-                     stream);
+  e = fa::launch_bwd(fa::kernel_d(a.d), mod.mask, f16, tq, tk, tv, tdo, tdq, ba, grid, stream);
   if (e != cudaSuccess) return cuda_fail("backward kernel launch", e);
   e = fa::launch_bwd_post(a.d, f16, dq_acc, a.scale, a.dq, a.B, a.Nq, a.Hq, a.dq_strides, stream);
   return e == cudaSuccess ? FA_OK : cuda_fail("backward postprocessing launch", e);
@@ -720,7 +729,8 @@ fa_status fa_bwd_varlen(const void *q, const void *k, const void *v, const void 
                         const int *cu_seqlens_q, const int *cu_seqlens_k, int B,
                         int max_seqlen_q, int max_seqlen_k, int total_q, int total_k, int Hq,
                         int Hkv, int d, float scale, int causal, int dtype, void *workspace,
-                        size_t workspace_bytes, int deterministic, cudaStream_t stream) {
+                        size_t workspace_bytes, int deterministic, const fa_score_mod *mod_in,
+                        cudaStream_t stream) {
   if (B < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || total_q < 0 || total_k < 0 || Hq <= 0 ||
       Hkv <= 0 || Hq % Hkv != 0)
     return FA_ERR_INVALID_ARG;
@@ -750,9 +760,12 @@ fa_status fa_bwd_varlen(const void *q, const void *k, const void *v, const void 
   const int kblocks = ceil_div(max_seqlen_k, 128);
   const int64_t units = static_cast<int64_t>(kblocks) * B * Hkv;
   if (units > INT32_MAX) return FA_ERR_INVALID_ARG;
+  ModPlan mod;
+  fa_status st = plan_mod(mod_in, causal, &mod);
+  if (st != FA_OK) return st;
 
   DeviceInfo *dev = nullptr;
-  fa_status st = current_device(&dev);
+  st = current_device(&dev);
   if (st != FA_OK) return st;
   cudaError_t e;
   const int64_t qst[3] = {0, static_cast<int64_t>(Hq) * d, d};
@@ -809,13 +822,14 @@ fa_status fa_bwd_varlen(const void *q, const void *k, const void *v, const void 
   ba.kblocks = kblocks;
   ba.d = d;
   ba.sem = deterministic ? sem : nullptr;
+  set_mod_fields(mod, scale, &ba);
   ba.num_units = static_cast<int>(units);
   ba.scale = scale;
   ba.scale_log2 = scale_log2(scale);
   ba.err = dev->err;
   ba.timeout_ns = g_timeout_ns;
   const int grid = static_cast<int>(units < dev->sm_count ? units : dev->sm_count);
-  e = fa::launch_bwd(fa::kernel_d(d), causal != 0, f16, tq, tk, tv, tdo, tdq, ba, grid, stream);
+  e = fa::launch_bwd(fa::kernel_d(d), mod.mask, f16, tq, tk, tv, tdo, tdq, ba, grid, stream);
   if (e != cudaSuccess) return cuda_fail("backward kernel launch", e);
   e = fa::launch_bwd_post(d, f16, dq_acc, scale, dq, 1, total_q, Hq, qst, stream);
   return e == cudaSuccess ? FA_OK : cuda_fail("backward postprocessing launch", e);

@@ -36,6 +36,7 @@
 // Per step the MMA issuer runs S^T (as soon as Q has landed), dP^T (once dO has landed
 // and the previous dQ has been read), then dK, dV and dQ: dK and dV release Q and dO so
 // that the next step's loads overlap the dQ product and its epilogue.
+#include <climits>
 #include <cmath>
 
 #include "fa_internal.h"
@@ -90,11 +91,12 @@ struct BUnit {
   int tma_b;           // batch coordinate of the tensor maps (0 for varlen)
   bool skip;           // key block j lies past the sequence's keys: nothing to do
   bool bad;            // varlen prefix sums out of range: the sequence is skipped
-  int i0, nqb;         // query blocks [i0, nqb) of each head of the group
-  int nit;             // steps: group * (nqb - i0)
+  int nqb;             // query blocks of the sequence
+  int ilo, ihi;        // query blocks [ilo, ihi) of each head of the group reach key block j
+  int nit;             // steps: group * (ihi - ilo)
 };
 
-template <bool CAUSAL>
+template <int MASK>
 __device__ __forceinline__ BUnit bunit_of(const BwdArgs &a, int u) {
   BUnit w;
   const int bg = a.B * a.Hkv;
@@ -123,22 +125,33 @@ __device__ __forceinline__ BUnit bunit_of(const BwdArgs &a, int u) {
   }
   w.skip = w.j * BKEY >= w.nk;
   w.nqb = (w.nq + BQ - 1) / BQ;
-  w.i0 = 0;
-  if (CAUSAL) {
-    // first query block holding a row that sees key j*128: i*128 + 127 + (nk - nq) >= j*128
-    const long long t = static_cast<long long>(w.j) * BKEY - (w.nk - w.nq) - (BQ - 1);
-    w.i0 = t <= 0 ? 0 : static_cast<int>((t + BQ - 1) / BQ);
-    if (w.i0 > w.nqb) w.i0 = w.nqb;
+  w.ilo = 0;
+  w.ihi = w.nqb;
+  const long long off = static_cast<long long>(w.nk) - w.nq;
+  const int wr = MASK == MASK_CAUSAL ? 0 : (MASK == MASK_MOD ? a.wr : -1);
+  const int wl = MASK == MASK_MOD ? a.wl : -1;
+  if (wr >= 0) {
+    // first query block holding a row that sees a key of the block:
+    // i*128 + 127 + off + wr >= j*128
+    const long long t = static_cast<long long>(w.j) * BKEY - off - wr - (BQ - 1);
+    w.ilo = t <= 0 ? 0 : static_cast<int>(min((t + BQ - 1) / BQ, static_cast<long long>(w.nqb)));
   }
-  w.nit = w.skip ? 0 : a.group * (w.nqb - w.i0);
+  if (wl >= 0) {
+    // last query block holding a row that sees a key of the block: i*128 + off - wl <= kmax
+    const long long kmax = min(static_cast<long long>(w.j) * BKEY + BKEY - 1, w.nk - 1ll);
+    const long long t = kmax - off + wl;
+    w.ihi = t < 0 ? 0 : static_cast<int>(min(t / BQ + 1, static_cast<long long>(w.nqb)));
+  }
+  if (w.ihi < w.ilo) w.ihi = w.ilo;
+  w.nit = w.skip ? 0 : a.group * (w.ihi - w.ilo);
   return w;
 }
 
 // Step t of a unit: query head and query block.
 __device__ __forceinline__ void bstep(const BwdArgs &a, const BUnit &w, int t, int &h, int &i) {
-  const int per = w.nqb - w.i0;
+  const int per = w.ihi - w.ilo;
   h = w.g * a.group + t / per;
-  i = w.i0 + t % per;
+  i = w.ilo + t % per;
 }
 
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const WaitCtl &wc) {
@@ -217,7 +230,7 @@ __device__ __forceinline__ void issue_dq(uint32_t d_tmem, uint32_t ds_smem, uint
 // ------------------------------------------------------------------------------------
 // Producer warp.
 
-template <int D, bool CAUSAL, bool F16>
+template <int D, int MASK, bool F16>
 __device__ void bwd_producer(const BwdArgs &a, const CUtensorMap *tq, const CUtensorMap *tk,
                              const CUtensorMap *tv, const CUtensorMap *tdo, uint8_t *smem,
                              BBars *bars, const WaitCtl &wc, int lane) {
@@ -226,7 +239,7 @@ __device__ void bwd_producer(const BwdArgs &a, const CUtensorMap *tq, const CUte
   float *dvec = lse2 + BQ;
   uint32_t kv_n = 0, q_n = 0;
   for (int u = blockIdx.x; u < a.num_units; u += gridDim.x) {
-    const BUnit w = bunit_of<CAUSAL>(a, u);
+    const BUnit w = bunit_of<MASK>(a, u);
     if (w.bad && w.j == 0 && w.g == 0 && lane == 0) atomicOr(a.err, DEVERR_BAD_CU_SEQLENS);
     if (w.nit == 0) continue;
     if (kv_n > 0 && !warp_wait(&bars->kv_empty, (kv_n - 1) & 1u, wc)) goto out;
@@ -292,7 +305,7 @@ out:
 // ------------------------------------------------------------------------------------
 // MMA issuer (one lane).
 
-template <int D, bool CAUSAL, bool F16>
+template <int D, int MASK, bool F16>
 __device__ void bwd_mma(const BwdArgs &a, uint8_t *smem, BBars *bars, uint32_t tmem,
                         const WaitCtl &wc) {
   using C = BCfg<D, F16>;
@@ -301,7 +314,7 @@ __device__ void bwd_mma(const BwdArgs &a, uint8_t *smem, BBars *bars, uint32_t t
   const uint32_t sDS = smem_u32(smem + C::DS_OFF);
   uint32_t kv_n = 0, it = 0, acc_n = 0;
   for (int u = blockIdx.x; u < a.num_units; u += gridDim.x) {
-    const BUnit w = bunit_of<CAUSAL>(a, u);
+    const BUnit w = bunit_of<MASK>(a, u);
     if (w.nit == 0) continue;
     if (!mbar_wait(&bars->kv_full, kv_n & 1u, wc)) goto out;
     ++kv_n;
@@ -339,7 +352,7 @@ out:
 // ------------------------------------------------------------------------------------
 // Compute warps: warp w handles TMEM lanes 32 (w % 4) .. +31 and column half w / 4.
 
-template <int D, bool CAUSAL, bool F16>
+template <int D, int MASK, bool F16>
 __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *smem, BBars *bars,
                             uint32_t tmem, const WaitCtl &wc, int tid) {
   using C = BCfg<D, F16>;
@@ -353,7 +366,7 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
   uint8_t *dq_s = smem + C::DQ_OFF;
   uint32_t it = 0, acc_n = 0, grp = 0;
   for (int u = blockIdx.x; u < a.num_units; u += gridDim.x) {
-    const BUnit w = bunit_of<CAUSAL>(a, u);
+    const BUnit w = bunit_of<MASK>(a, u);
     if (w.skip) continue;
     const int off = w.nk - w.nq;  // bottom-right alignment: query q sits at key position q + off
     const int key = w.j * BKEY + r;
@@ -376,7 +389,22 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
       int h, i;
       bstep(a, w, t, h, i);
       const int q0 = i * BQ;
-      const bool full = !CAUSAL || (w.j * BKEY + BKEY - 1 <= q0 + off);  // no pair masked
+      const int kb = w.j * BKEY;
+      bool full;  // no pair of the 128 x 128 block masked
+      if constexpr (MASK == MASK_NONE) {
+        full = kb + BKEY <= w.nk;
+      } else if constexpr (MASK == MASK_CAUSAL) {
+        full = kb + BKEY <= w.nk && kb + BKEY - 1 <= q0 + off;
+      } else {
+        full = kb + BKEY <= w.nk && (a.wr < 0 || kb + BKEY - 1 <= q0 + off + a.wr) &&
+               (a.wl < 0 || kb >= q0 + BQ - 1 + off - a.wl);
+      }
+      // this key row's visible query positions (modifiers): key - wr - off <= q <= key + wl - off
+      const int qv_lo = MASK == MASK_MOD && a.wr >= 0 ? key - a.wr - off : INT_MIN;
+      const int qv_hi = MASK == MASK_MOD && a.wl >= 0 ? key + a.wl - off : INT_MAX;
+      const bool softcap = MASK == MASK_MOD && a.sc_out != 0.f;
+      const bool alibi = MASK == MASK_MOD && a.alibi != nullptr;
+      const float slope2 = alibi ? a.alibi[w.b * a.alibi_sb + h] * LOG2E : 0.f;
       // P^T and dS^T = P^T (dP^T - D) of this key row for the 64 queries of this half,
       // 32 at a time: P^T and dS^T to TMEM (dV, dK), dS to shared memory with queries
       // contiguous (dQ).
@@ -399,10 +427,28 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
 #pragma unroll
           for (int x = 0; x < 4; ++x) {
             const int qi = qc + e4 + x;
-            const bool vis = key < w.nk && (full || key <= q0 + qi + off);
-            const float pv = ex2_approx(fmaf(__uint_as_float(sr[e4 + x]), a.scale_log2, -lv[x]));
+            const float sv = __uint_as_float(sr[e4 + x]);
+            float z2, dz = 1.f;  // score in log2 units and dz/ds
+            if constexpr (MASK == MASK_MOD) {
+              if (softcap) {
+                const float t = tanh_ex2(sv * a.sc_in);
+                z2 = t * a.sc_out;
+                dz = 1.f - t * t;
+              } else {
+                z2 = sv * a.scale_log2;
+              }
+              if (alibi) z2 = fmaf(-slope2, fabsf(static_cast<float>(q0 + qi + off - key)), z2);
+            } else {
+              z2 = sv * a.scale_log2;
+            }
+            bool vis;
+            if constexpr (MASK == MASK_MOD)
+              vis = full || (key < w.nk && q0 + qi >= qv_lo && q0 + qi <= qv_hi);
+            else
+              vis = full || (key < w.nk && (MASK == MASK_NONE || key <= q0 + qi + off));
+            const float pv = ex2_approx(z2 - lv[x]);
             p[x] = vis ? pv : 0.f;
-            ds[x] = p[x] * (__uint_as_float(dr[e4 + x]) - dv[x]);
+            ds[x] = p[x] * (__uint_as_float(dr[e4 + x]) - dv[x]) * dz;
           }
           pp[e4 / 2] = pack2<F16>(p[0], p[1]);
           pp[e4 / 2 + 1] = pack2<F16>(p[2], p[3]);
@@ -446,9 +492,12 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
       if (!group_sync(&bars->cgrp, grp, wc)) return;
       if (tid == 0) {
         int *sem = a.sem ? a.sem + (static_cast<int64_t>(w.b) * a.Hq + h) * a.qblocks + i : nullptr;
-        // Deterministic order: key block j adds after blocks 0 .. j-1 (the blocks that reach
-        // query block i are a prefix 0 .. jmax).
-        if (sem != nullptr && !wait_counter(sem, w.j, wc)) return;
+        // Deterministic order: the key blocks that reach query block i are an interval
+        // jmin .. jmax (jmin = 0 unless a left window bound cuts the first keys); block j
+        // adds after jmin .. j-1.
+        int jmin = 0;
+        if (MASK == MASK_MOD && a.wl >= 0) jmin = max(q0 + off - a.wl, 0) / BKEY;
+        if (sem != nullptr && !wait_counter(sem, w.j - jmin, wc)) return;
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc)
           tma_reduce_add_4d(tdq, dq_s + cc * BOX, cc * 32, h, w.q_tok + q0, w.tma_b);
@@ -495,7 +544,7 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
   }
 }
 
-template <int D, bool CAUSAL, bool F16>
+template <int D, int MASK, bool F16>
 __global__ void __launch_bounds__(NTHREADS, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -548,7 +597,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // TMEM is released.
   if (warp < PRODUCER_WARP) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(COMPUTE_REGS));
-    bwd_compute<D, CAUSAL, F16>(a, &tdq, smem, bars, tmem, wc, tid);
+    bwd_compute<D, MASK, F16>(a, &tdq, smem, bars, tmem, wc, tid);
     if (tid == 0) bulk_wait_all();  // every dQ reduction has landed
     __syncwarp();
     tc_fence_before();
@@ -556,9 +605,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(OTHER_REGS));
     if (warp == PRODUCER_WARP) {
-      bwd_producer<D, CAUSAL, F16>(a, &tq, &tk, &tv, &tdo, smem, bars, wc, lane);
+      bwd_producer<D, MASK, F16>(a, &tq, &tk, &tv, &tdo, smem, bars, wc, lane);
     } else if (warp == MMA_WARP && lane == 0) {
-      bwd_mma<D, CAUSAL, F16>(a, smem, bars, tmem, wc);
+      bwd_mma<D, MASK, F16>(a, smem, bars, tmem, wc);
     }
     __syncwarp();
     tc_fence_before();
@@ -652,37 +701,41 @@ int grid_for(int64_t items, int threads) {
   return static_cast<int>(g < 1 ? 1 : (g > 8192 ? 8192 : g));
 }
 
-template <int D, bool CAUSAL, bool F16>
+template <int D, int MASK, bool F16>
 cudaError_t launch_bwd_impl(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                             const CUtensorMap &tdo, const CUtensorMap &tdq, const BwdArgs &a,
                             int grid, cudaStream_t stream) {
   constexpr int smem = BCfg<D, F16>::SMEM_BYTES;
   static_assert(smem <= 232448, "backward kernel shared memory");
-  cudaError_t e = cudaFuncSetAttribute(bwd_kernel<D, CAUSAL, F16>,
+  cudaError_t e = cudaFuncSetAttribute(bwd_kernel<D, MASK, F16>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  bwd_kernel<D, CAUSAL, F16><<<grid, NTHREADS, smem, stream>>>(tq, tk, tv, tdo, tdq, a);
+  bwd_kernel<D, MASK, F16><<<grid, NTHREADS, smem, stream>>>(tq, tk, tv, tdo, tdq, a);
   return cudaGetLastError();
 }
 
 template <int D, bool F16>
-cudaError_t launch_bwd_d(bool causal, const CUtensorMap &tq, const CUtensorMap &tk,
+cudaError_t launch_bwd_d(int mask, const CUtensorMap &tq, const CUtensorMap &tk,
                          const CUtensorMap &tv, const CUtensorMap &tdo, const CUtensorMap &tdq,
                          const BwdArgs &a, int grid, cudaStream_t stream) {
-  return causal ? launch_bwd_impl<D, true, F16>(tq, tk, tv, tdo, tdq, a, grid, stream)
-                : launch_bwd_impl<D, false, F16>(tq, tk, tv, tdo, tdq, a, grid, stream);
+  switch (mask) {
+    case MASK_NONE: return launch_bwd_impl<D, MASK_NONE, F16>(tq, tk, tv, tdo, tdq, a, grid, stream);
+    case MASK_CAUSAL:
+      return launch_bwd_impl<D, MASK_CAUSAL, F16>(tq, tk, tv, tdo, tdq, a, grid, stream);
+    default: return launch_bwd_impl<D, MASK_MOD, F16>(tq, tk, tv, tdo, tdq, a, grid, stream);
+  }
 }
 
 }  // namespace
 
-cudaError_t launch_bwd(int d, bool causal, bool f16, const CUtensorMap &tq, const CUtensorMap &tk,
+cudaError_t launch_bwd(int d, int mask, bool f16, const CUtensorMap &tq, const CUtensorMap &tk,
                        const CUtensorMap &tv, const CUtensorMap &tdo, const CUtensorMap &tdq,
                        const BwdArgs &a, int grid, cudaStream_t stream) {
   if (d == 64)
-    return f16 ? launch_bwd_d<64, true>(causal, tq, tk, tv, tdo, tdq, a, grid, stream)
-               : launch_bwd_d<64, false>(causal, tq, tk, tv, tdo, tdq, a, grid, stream);
-  return f16 ? launch_bwd_d<128, true>(causal, tq, tk, tv, tdo, tdq, a, grid, stream)
-             : launch_bwd_d<128, false>(causal, tq, tk, tv, tdo, tdq, a, grid, stream);
+    return f16 ? launch_bwd_d<64, true>(mask, tq, tk, tv, tdo, tdq, a, grid, stream)
+               : launch_bwd_d<64, false>(mask, tq, tk, tv, tdo, tdq, a, grid, stream);
+  return f16 ? launch_bwd_d<128, true>(mask, tq, tk, tv, tdo, tdq, a, grid, stream)
+             : launch_bwd_d<128, false>(mask, tq, tk, tv, tdo, tdq, a, grid, stream);
 }
 
 cudaError_t launch_bwd_pre(int d, bool f16, const void *o, const void *dout, int B, int Nq,

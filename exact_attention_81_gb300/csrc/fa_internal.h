@@ -150,6 +150,11 @@ struct BwdArgs {
   int kblocks;                // ceil(Nk / 128)
   int d;                      // head dimension of the tensors (<= the kernel's D)
   int *sem;                   // deterministic dQ: additions done per (b, h, query block), or null
+  // Score modifiers (read by the MASK_MOD kernel only), as in PrefillArgs.
+  int wl, wr;
+  float sc_in, sc_out;        // softcap: z2 = tanh(s * sc_in) * sc_out, dz/ds = 1 - tanh^2
+  const float *alibi;
+  int64_t alibi_sb;
   int num_units;              // kblocks * B * Hkv
   float scale, scale_log2;
   unsigned int *err;
@@ -163,7 +168,7 @@ cudaError_t launch_bwd_pre(int d, bool f16, const void *o, const void *dout, int
 
 // tq, tk, tv, tdo: 16-bit maps like the forward's; tdq: fp32 map of the dQ accumulator
 // (box 32 x 128 rows, 128-byte swizzle).
-cudaError_t launch_bwd(int d, bool causal, bool f16, const CUtensorMap &tq, const CUtensorMap &tk,
+cudaError_t launch_bwd(int d, int mask, bool f16, const CUtensorMap &tq, const CUtensorMap &tk,
                        const CUtensorMap &tv, const CUtensorMap &tdo, const CUtensorMap &tdq,
                        const BwdArgs &a, int grid, cudaStream_t stream);
 

@@ -276,8 +276,10 @@ fa_status fa_fwd_kvcache_noalloc(const void *q, const void *k_cache, const void 
  * deterministic != 0, which fixes the order (key block 0, 1, 2, ...) at some cost in
  * speed ("flash-attention" section 5: deterministic backward, slower); dK and dV are
  * always deterministic.
- * The score modifiers (fa_score_mod) have no backward here.  Nk = 0 gives dQ = 0;
- * Nq = 0 gives dK = dV = 0; B = 0 is a no-op.
+ * With score modifiers (mod, the same as the forward call's) the gradients pass through
+ * them: the window and the ALiBi bias change which pairs count and P, a softcap c
+ * multiplies dS by 1 - tanh^2(s / c).  Nk = 0 gives dQ = 0; Nq = 0 gives dK = dV = 0;
+ * B = 0 is a no-op.
  */
 typedef struct fa_bwd_params {
     const void *q, *k, *v, *o, *dout;
@@ -292,6 +294,7 @@ typedef struct fa_bwd_params {
     void *workspace;
     size_t workspace_bytes;
     int deterministic;
+    fa_score_mod mod; /* the forward call's score modifiers (zero-filled = none) */
 } fa_bwd_params;
 
 size_t fa_bwd_workspace_size(int B, int Nq, int Hq, int d);
@@ -304,14 +307,15 @@ fa_status fa_bwd(const fa_bwd_params *p, cudaStream_t stream);
  * contiguous; lse: [Hq, total_q] fp32 from fa_fwd_varlen; cu_seqlens_q / _k: DEVICE int32
  * [B+1] as for fa_fwd_varlen (a sequence that breaks their rules is skipped and flagged in
  * the device error word).  workspace: fa_bwd_workspace_size(B, max_seqlen_q, Hq, d) bytes.
- * deterministic as in fa_bwd_params.
+ * deterministic as in fa_bwd_params; mod: the forward call's score modifiers (NULL = none).
  */
 fa_status fa_bwd_varlen(const void *q, const void *k, const void *v, const void *o,
                         const void *dout, const float *lse, void *dq, void *dk, void *dv,
                         const int *cu_seqlens_q, const int *cu_seqlens_k, int B,
                         int max_seqlen_q, int max_seqlen_k, int total_q, int total_k, int Hq,
                         int Hkv, int d, float scale, int causal, int dtype, void *workspace,
-                        size_t workspace_bytes, int deterministic, cudaStream_t stream);
+                        size_t workspace_bytes, int deterministic, const fa_score_mod *mod,
+                        cudaStream_t stream);
 
 /* sizeof(fa_bwd_params), for bindings that check their struct layout. */
 size_t fa_bwd_params_size(void);
