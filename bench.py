@@ -533,7 +533,7 @@ def extra_workloads(args, dev, pk, world, dist):
     from exact_attention_81_gb300.inputs import WORKLOADS, kvcache_workload_inputs, workload_inputs
     stream = torch.cuda.current_stream()
     res = {}
-    for name in ("dense2k", "gqa16k"):
+    for name in ("dense2k", "gqa16k", "causal8k_d256"):
         w = WORKLOADS[name]
         q, k, v = workload_inputs(w, device=dev)
         o = torch.empty_like(q)

@@ -158,9 +158,11 @@ bool scale_ok(float s) { return std::isfinite(s) && s > 0.f; }
 
 bool dtype_ok(int t) { return t == FA_BF16 || t == FA_FP16; }
 
-// Head dimensions served: multiples of 8 up to 128 (the kernels run at width 64 or 128;
-// the tensor maps give the columns past d as zeros).
-bool head_dim_ok(int d) { return d >= 8 && d <= 128 && d % 8 == 0; }
+// Head dimensions served: multiples of 8 up to max_d (the kernels run at width 64, 128 or
+// 256; the tensor maps give the columns past d as zeros).  The forward calls take up to
+// 256, decode and backward up to 128.
+bool head_dim_ok(int d, int max_d = 128) { return d >= 8 && d <= max_d && d % 8 == 0; }
+constexpr int kMaxPrefillD = 256;
 
 int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 
@@ -271,7 +273,7 @@ fa_status fa_fwd(const fa_fwd_params *p, cudaStream_t stream) {
   const fa_fwd_params &a = *p;
   if (a.B < 0 || a.Nq < 0 || a.Nk < 0 || a.Hq <= 0 || a.Hkv <= 0 || a.Hq % a.Hkv != 0)
     return FA_ERR_INVALID_ARG;
-  if (!head_dim_ok(a.d)) return FA_ERR_UNSUPPORTED;
+  if (!head_dim_ok(a.d, kMaxPrefillD)) return FA_ERR_UNSUPPORTED;
   if (!dtype_ok(a.dtype)) return FA_ERR_UNSUPPORTED;
   if (!scale_ok(a.scale)) return FA_ERR_INVALID_ARG;
   if (a.Nq > (1 << 30) || a.Nk > (1 << 30)) return FA_ERR_INVALID_ARG;
@@ -290,7 +292,7 @@ fa_status fa_fwd(const fa_fwd_params *p, cudaStream_t stream) {
         !stride_ok(a.v_strides[1], a.Nk) || !stride_ok(a.v_strides[2], a.Hkv))
       return FA_ERR_INVALID_ARG;
   }
-  const int mblocks = ceil_div(a.Nq, 256);
+  const int mblocks = ceil_div(a.Nq, fa::prefill_tile_rows(fa::kernel_d(a.d)));
   const int64_t tiles = static_cast<int64_t>(a.B) * a.Hq * mblocks;
   if (tiles > INT32_MAX) return FA_ERR_INVALID_ARG;
   ModPlan mod;
@@ -354,7 +356,7 @@ fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, fl
   if (B < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || total_q < 0 || total_k < 0 || Hq <= 0 ||
       Hkv <= 0 || Hq % Hkv != 0)
     return FA_ERR_INVALID_ARG;
-  if (!head_dim_ok(d)) return FA_ERR_UNSUPPORTED;
+  if (!head_dim_ok(d, kMaxPrefillD)) return FA_ERR_UNSUPPORTED;
   if (!dtype_ok(dtype)) return FA_ERR_UNSUPPORTED;
   if (!scale_ok(scale)) return FA_ERR_INVALID_ARG;
   if (max_seqlen_q > (1 << 30) || total_q > (1 << 30) || total_k > (1 << 30))
@@ -368,7 +370,7 @@ fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, fl
     return FA_ERR_INVALID_ARG;
   if (total_k > 0 && (k == nullptr || v == nullptr || !aligned(k, 16) || !aligned(v, 16)))
     return FA_ERR_INVALID_ARG;
-  const int mblocks = ceil_div(max_seqlen_q, 256);
+  const int mblocks = ceil_div(max_seqlen_q, fa::prefill_tile_rows(fa::kernel_d(d)));
   const int64_t tiles = static_cast<int64_t>(B) * Hq * mblocks;
   if (tiles > INT32_MAX) return FA_ERR_INVALID_ARG;
   ModPlan mod;

@@ -31,7 +31,7 @@ struct PrefillArgs {
   int varlen;
   const int *cu_q, *cu_k;     // varlen prefix sums (device)
   int total_q, total_k;
-  int mblocks;                // 256-row query blocks per (batch, head)
+  int mblocks;                // query blocks (prefill_tile_rows rows) per (batch, head)
   int num_tiles;              // B * Hq * mblocks
   float scale_log2;           // scale * log2(e)
   int sched_slot;             // this launch's tile-ticket counter slot
@@ -132,8 +132,13 @@ cudaError_t launch_combine(int d, int d_out, bool f16, const float *o_part, cons
                            int maxch, int wl, int kalign, void *o, float *lse, unsigned int *err,
                            cudaStream_t stream);
 
-// Width of the kernel instance that serves head dimension d (8 <= d <= 128, d % 8 == 0).
-inline int kernel_d(int d) { return d <= 64 ? 64 : 128; }
+// Width of the kernel instance that serves head dimension d (8 <= d <= 256, d % 8 == 0;
+// widths above 128 exist for the prefill kernel only).
+inline int kernel_d(int d) { return d <= 64 ? 64 : (d <= 128 ? 128 : 256); }
+
+// Query rows of one prefill work tile for kernel width kd: two 128-row sub-tiles, one
+// when the head dimension is above 128 (TMEM holds a single D-wide accumulator then).
+inline int prefill_tile_rows(int kd) { return kd > 128 ? 128 : 256; }
 
 // Backward pass: main kernel arguments (one work unit = batch, kv head, 128-key block).
 struct BwdArgs {

@@ -57,6 +57,7 @@ constexpr int MMA_WARP = 9;
 constexpr int SCHED_DEPTH = 4;      // tiles in flight between the scheduler and the roles
 constexpr int SOFTMAX_REGS = 200;   // 2 x 128 threads x 200
 constexpr int OTHER_REGS = 104;     //   + 128 threads x 104 = 384 threads x 168 at launch
+constexpr int IDLE_REGS = 24;       // wide kernel: the unused second softmax warpgroup
 constexpr int NUM_SCHED_SLOTS = 256;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int BOX_BYTES = 128 * 128;  // one TMA box: 128 rows x 64 bf16 (128 B, swizzled)
@@ -67,18 +68,25 @@ __host__ __device__ constexpr uint32_t o_col(int t) {
   return static_cast<uint32_t>(256 + t * 128);
 }
 
+// D <= 128: two query sub-tiles per work tile, ring slots of one [128 x D] K or V tile.
+// D = 256 ("wide"): one sub-tile with S double-buffered in TMEM (S_0, S_1, O = 512
+// columns), ring slots of half a tile (the d halves), PV as two N = 128 products.
 template <int D, bool F16 = false>
 struct Cfg {
+  static constexpr bool WIDE = D > 128;
+  static constexpr int NSUB = WIDE ? 1 : 2;              // query sub-tiles per work tile
   static constexpr int KCH = D / 64;                     // 64-wide boxes per row
   static constexpr int TILE_BYTES = KCH * BOX_BYTES;     // one [128 x D] bf16 tile
-  static constexpr int NSLOTS = D == 128 ? 4 : 8;        // K/V ring depth
+  static constexpr int SLOT_BYTES = WIDE ? TILE_BYTES / 2 : TILE_BYTES;
+  static constexpr int NSLOTS = WIDE ? 5 : (D == 128 ? 4 : 8);  // K/V ring depth
   static constexpr int Q_OFF = 0;
-  static constexpr int RING_OFF = 2 * TILE_BYTES;
-  static constexpr int BAR_OFF = RING_OFF + NSLOTS * TILE_BYTES;
+  static constexpr int RING_OFF = NSUB * TILE_BYTES;
+  static constexpr int BAR_OFF = RING_OFF + NSLOTS * SLOT_BYTES;
   static constexpr int SMEM_BYTES = BAR_OFF + 512 + 1024;  // barriers + alignment slack
   static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BC, false, false, F16);
-  static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, false, true, F16);
+  static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, WIDE ? 128 : D, false, true, F16);
 };
+static_assert(Cfg<256>::SMEM_BYTES <= 227 * 1024, "wide prefill exceeds shared memory");
 
 // Per-launch tile-ticket counters: [slot][0] = next ticket, [slot][1] = CTAs finished.
 // The host gives each launch its own slot (round robin); the last CTA of a launch to
@@ -90,7 +98,8 @@ struct Bars {
   int sched_tile[SCHED_DEPTH];
   uint64_t q_full, q_empty;
   uint64_t kv_full[8], kv_empty[8];
-  uint64_t s_full[2], p_ready[2], o_full[2], o_empty[2];
+  uint64_t s_full[2], p_ready[2], o_full[2], o_empty[2];  // per sub-tile (wide: per S buffer)
+  uint64_t pv_done;  // wide: PV(j) complete, before the softmax of j + 1 rescales O
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
@@ -98,7 +107,7 @@ struct Bars {
 
 struct TileInfo {
   int b, h, hk;
-  int q_row0;       // first query row of the 256-row block, within its sequence
+  int q_row0;       // first query row of the block (NSUB x 128 rows), within its sequence
   int q_tok, k_tok; // packed-token offset of the sequence (varlen), else 0
   int tma_b;        // batch coordinate of the TMA maps (0 for varlen)
   int nq, nk;       // sequence lengths
@@ -109,7 +118,7 @@ struct TileInfo {
   int js[2], je[2], nkv[2];
 };
 
-template <int MASK>
+template <int MASK, int NSUB>
 __device__ __forceinline__ TileInfo tile_info(const PrefillArgs &a, int tile) {
   TileInfo ti;
   const int bh = tile / a.mblocks;
@@ -119,7 +128,7 @@ __device__ __forceinline__ TileInfo tile_info(const PrefillArgs &a, int tile) {
   ti.b = bh / a.Hq;
   ti.h = bh - ti.b * a.Hq;
   ti.hk = ti.h / a.group;
-  ti.q_row0 = mb * 2 * BR;
+  ti.q_row0 = mb * NSUB * BR;
   if (a.varlen) {
     const int q0 = a.cu_q[ti.b], q1 = a.cu_q[ti.b + 1];
     const int k0 = a.cu_k[ti.b], k1 = a.cu_k[ti.b + 1];
@@ -142,7 +151,7 @@ __device__ __forceinline__ TileInfo tile_info(const PrefillArgs &a, int tile) {
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     const int first = ti.q_row0 + t * BR;
-    const int nr = min(max(ti.nq - first, 0), BR);
+    const int nr = t < NSUB ? min(max(ti.nq - first, 0), BR) : 0;
     ti.nrows[t] = nr;
     lo[t] = 0;
     hi[t] = 0;
@@ -221,6 +230,19 @@ __device__ void producer_role(const PrefillArgs &a, const CUtensorMap *tmq,
   using C = Cfg<D>;
   uint32_t kv_iter = 0, q_iter = 0;
   unsigned int *ctr = g_sched[a.sched_slot];
+  // One ring slot: `boxes` 64-column boxes of rows [row0, row0 + 128) from map m, the first
+  // at column c0.  False if the wait gave up.
+  auto load_slot = [&](const CUtensorMap *m, int c0, int boxes, int hk, int row0, int b) {
+    const int slot = static_cast<int>(kv_iter % C::NSLOTS);
+    const uint32_t use = kv_iter / C::NSLOTS;
+    if (!mbar_wait(&bars->kv_empty[slot], (use & 1u) ^ 1u, wc)) return false;
+    mbar_arrive_expect_tx(&bars->kv_full[slot], C::SLOT_BYTES);
+    for (int c = 0; c < boxes; ++c)
+      tma_load_4d(smem + C::RING_OFF + slot * C::SLOT_BYTES + c * BOX_BYTES, m,
+                  &bars->kv_full[slot], (c0 + c) * 64, hk, row0, b);
+    ++kv_iter;
+    return true;
+  };
   for (uint32_t k = 0;; ++k) {
     const int ticket = static_cast<int>(atomicAdd(&ctr[0], 1u));
     const int tile = ticket < a.num_tiles ? ticket : -1;
@@ -229,33 +251,38 @@ __device__ void producer_role(const PrefillArgs &a, const CUtensorMap *tmq,
     bars->sched_tile[rs] = tile;
     mbar_arrive(&bars->sched_full[rs]);
     if (tile < 0) break;
-    const TileInfo ti = tile_info<MASK>(a, tile);
+    const TileInfo ti = tile_info<MASK, C::NSUB>(a, tile);
     if (a.varlen && (ti.q_row0 == 0) && varlen_bad(a, ti.b)) atomicOr(a.err, DEVERR_BAD_CU_SEQLENS);
     const int n = max(ti.je[0], ti.je[1]);
     if (n == 0) continue;
     if (q_iter > 0 && !mbar_wait(&bars->q_empty, (q_iter - 1) & 1u, wc)) goto out;
-    mbar_arrive_expect_tx(&bars->q_full, 2 * C::TILE_BYTES);
+    mbar_arrive_expect_tx(&bars->q_full, C::NSUB * C::TILE_BYTES);
 #pragma unroll
-    for (int t = 0; t < 2; ++t)
+    for (int t = 0; t < C::NSUB; ++t)
 #pragma unroll
       for (int c = 0; c < C::KCH; ++c)
         tma_load_4d(smem + C::Q_OFF + t * C::TILE_BYTES + c * BOX_BYTES, tmq, &bars->q_full,
                     c * 64, ti.h, ti.q_tok + ti.q_row0 + t * BR, ti.tma_b);
     ++q_iter;
-    for (int j = 0; j < n; ++j) {
-#pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const int slot = static_cast<int>(kv_iter % C::NSLOTS);
-        const uint32_t use = kv_iter / C::NSLOTS;
-        if (!mbar_wait(&bars->kv_empty[slot], (use & 1u) ^ 1u, wc)) goto out;
-        mbar_arrive_expect_tx(&bars->kv_full[slot], C::TILE_BYTES);
-#pragma unroll
-        for (int c = 0; c < C::KCH; ++c)
-          tma_load_4d(smem + C::RING_OFF + slot * C::TILE_BYTES + c * BOX_BYTES,
-                      which ? tmv : tmk, &bars->kv_full[slot], c * 64, ti.hk,
-                      ti.k_tok + (ti.kv0 + j) * BC, ti.tma_b);
-        ++kv_iter;
-      }
+    const int krow = ti.k_tok + ti.kv0 * BC;
+    if constexpr (C::WIDE) {
+      // Ring order K_0, K_1, V_0, K_2, V_1, ..., V_{n-1} (the MMA issues S one step ahead),
+      // each tile as two slots: d columns [0, 128) then [128, 256).
+      bool ok = load_slot(tmk, 0, 2, ti.hk, krow, ti.tma_b) &&
+                load_slot(tmk, 2, 2, ti.hk, krow, ti.tma_b);
+      for (int j = 1; ok && j < n; ++j)
+        ok = load_slot(tmk, 0, 2, ti.hk, krow + j * BC, ti.tma_b) &&
+             load_slot(tmk, 2, 2, ti.hk, krow + j * BC, ti.tma_b) &&
+             load_slot(tmv, 0, 2, ti.hk, krow + (j - 1) * BC, ti.tma_b) &&
+             load_slot(tmv, 2, 2, ti.hk, krow + (j - 1) * BC, ti.tma_b);
+      ok = ok && load_slot(tmv, 0, 2, ti.hk, krow + (n - 1) * BC, ti.tma_b) &&
+           load_slot(tmv, 2, 2, ti.hk, krow + (n - 1) * BC, ti.tma_b);
+      if (!ok) goto out;
+    } else {
+      for (int j = 0; j < n; ++j)
+        if (!load_slot(tmk, 0, C::KCH, ti.hk, krow + j * BC, ti.tma_b) ||
+            !load_slot(tmv, 0, C::KCH, ti.hk, krow + j * BC, ti.tma_b))
+          goto out;
     }
   }
 out:
@@ -310,7 +337,7 @@ __device__ void mma_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, uint32
     int tile;
     if (!next_tile<false>(bars, k, tile, wc)) goto out;
     if (tile < 0) break;
-    const TileInfo ti = tile_info<MASK>(a, tile);
+    const TileInfo ti = tile_info<MASK, 2>(a, tile);
     const int n = max(ti.je[0], ti.je[1]);
     if (n == 0) continue;
     if (!mbar_wait(&bars->q_full, q_iter & 1u, wc)) goto out;
@@ -375,6 +402,98 @@ out:
   mbar_wait_teardown(&bars->mma_done, 0u, 1000000000ull);
 }
 
+// MMA issuer of the wide kernel (one sub-tile, S double-buffered in TMEM columns
+// [0,128) and [128,256), O in [256,512)).  Order per tile of n K/V steps:
+//   S(0), S(1), PV(0), S(2), PV(1), S(3), ..., PV(n-1)
+// so the tensor core computes S(j+1) while the softmax works on S(j).  S(j+2) reuses the
+// buffer of S(j) right after PV(j), which reads P(j) from it (issue order).  Every PV but
+// the tile's last is committed to pv_done: the softmax of step j+1 waits for it before it
+// rescales O.
+template <int D, int MASK, bool F16>
+__device__ void mma_role_wide(const PrefillArgs &a, uint8_t *smem, Bars *bars, uint32_t tmem,
+                              const WaitCtl &wc) {
+  using C = Cfg<D, F16>;
+  uint32_t kv_iter = 0, q_iter = 0;
+  uint32_t p_phase = 0u, oe_phase = 0u;  // p_phase: bit b for S buffer b
+  bool o_pending = false;
+  const uint32_t q_smem = smem_u32(smem + C::Q_OFF);
+  const uint32_t ring = smem_u32(smem + C::RING_OFF);
+  // Next ring slot (its load has landed): its shared address, or 0 if the wait gave up.
+  auto take = [&](int &slot) -> uint32_t {
+    slot = static_cast<int>(kv_iter % C::NSLOTS);
+    if (!mbar_wait(&bars->kv_full[slot], (kv_iter / C::NSLOTS) & 1u, wc)) return 0u;
+    ++kv_iter;
+    tc_fence_after();
+    return ring + static_cast<uint32_t>(slot * C::SLOT_BYTES);
+  };
+  // S(buf) = Q K^T over d in two halves (one slot each): 8 K-steps of 16 per half.
+  auto issue_s_wide = [&](int buf) -> bool {
+#pragma unroll 1
+    for (int h = 0; h < 2; ++h) {
+      int slot;
+      const uint32_t k_smem = take(slot);
+      if (k_smem == 0u) return false;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t off = static_cast<uint32_t>((kk >> 2) * BOX_BYTES + (kk & 3) * 32);
+        mma_bf16_ss(tmem + s_col(buf),
+                    sw128_desc(q_smem + static_cast<uint32_t>(2 * h * BOX_BYTES) + off, 16, 1024),
+                    sw128_desc(k_smem + off, 16, 1024), C::IDESC_S, (h | kk) ? 1u : 0u);
+      }
+      mma_commit(&bars->kv_empty[slot]);
+    }
+    mma_commit(&bars->s_full[buf]);
+    return true;
+  };
+  for (uint32_t k = 0;; ++k) {
+    int tile;
+    if (!next_tile<false>(bars, k, tile, wc)) goto out;
+    if (tile < 0) break;
+    {
+      const TileInfo ti = tile_info<MASK, 1>(a, tile);
+      const int n = ti.je[0];
+      if (n == 0) continue;
+      if (!mbar_wait(&bars->q_full, q_iter & 1u, wc)) goto out;
+      ++q_iter;
+      tc_fence_after();
+      if (!issue_s_wide(0)) goto out;
+      if (n > 1 && !issue_s_wide(1)) goto out;
+      for (int j = 0; j < n; ++j) {
+        const int buf = j & 1;
+        if (j == 0 && o_pending) {
+          // O still holds the previous tile's result until its epilogue has read it.
+          if (!mbar_wait(&bars->o_empty[0], oe_phase, wc)) goto out;
+          oe_phase ^= 1u;
+          o_pending = false;
+        }
+        if (!mbar_wait(&bars->p_ready[buf], (p_phase >> buf) & 1u, wc)) goto out;
+        p_phase ^= 1u << buf;
+        tc_fence_after();
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+          int slot;
+          const uint32_t v_smem = take(slot);
+          if (v_smem == 0u) goto out;
+          issue_pv<D, F16>(tmem + o_col(0) + static_cast<uint32_t>(h * 128), tmem + s_col(buf),
+                           v_smem, j > 0);
+          mma_commit(&bars->kv_empty[slot]);
+        }
+        if (j == n - 1) {
+          mma_commit(&bars->o_full[0]);
+          o_pending = true;
+        } else {
+          mma_commit(&bars->pv_done);
+        }
+        if (j + 2 < n && !issue_s_wide(buf)) goto out;
+      }
+      mma_commit(&bars->q_empty);
+    }
+  }
+out:
+  mma_commit(&bars->mma_done);
+  mbar_wait_teardown(&bars->mma_done, 0u, 1000000000ull);
+}
+
 // ------------------------------------------------------------------------------------
 // Softmax / correction / epilogue: one thread per query row of its sub-tile.
 
@@ -386,27 +505,29 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const 
 template <int D, int MASK, bool F16>
 __device__ void softmax_role(const PrefillArgs &a, Bars *bars, uint32_t tmem, const WaitCtl &wc,
                              int warp, int lane) {
+  using C = Cfg<D, F16>;
   constexpr bool CAUSAL = MASK == MASK_CAUSAL;
   constexpr bool MOD = MASK == MASK_MOD;
   const int t = warp >> 2;
   const int wq = warp & 3;
   const int rit = wq * 32 + lane;  // row inside the sub-tile = TMEM lane
   const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-  const uint32_t tS = tmem + lane_off + s_col(t);
   const uint32_t tO = tmem + lane_off + o_col(t);
   // With a softcap or ALiBi the scores are moved to the log2 domain before the max, and
   // the exp2 argument needs no further scaling.
   const bool softcap = MOD && a.sc_out != 0.f;
   const bool alibi = MOD && a.alibi != nullptr;
   const float c = (softcap || alibi) ? 1.f : a.scale_log2;
-  uint32_t s_phase = 0, o_phase = 0;
+  // S buffer phases, bit b for buffer b (one buffer per sub-tile; the wide kernel's single
+  // sub-tile alternates between two).
+  uint32_t s_phase = 0, o_phase = 0, pv_phase = 0;
   uint16_t *obase = reinterpret_cast<uint16_t *>(a.o);  // bf16 or fp16 elements
 
   for (uint32_t k = 0;; ++k) {
     int tile;
     if (!next_tile<true>(bars, k, tile, wc)) return;
     if (tile < 0) break;
-    const TileInfo ti = tile_info<MASK>(a, tile);
+    const TileInfo ti = tile_info<MASK, C::NSUB>(a, tile);
     const int nrows = t == 0 ? ti.nrows[0] : ti.nrows[1];
     if (nrows == 0) continue;
     const int nkv = t == 0 ? ti.nkv[0] : ti.nkv[1];
@@ -432,8 +553,10 @@ __device__ void softmax_role(const PrefillArgs &a, Bars *bars, uint32_t tmem, co
     float m = -INFINITY, l = 0.f;
     const uint64_t c2 = f2_pack(c, c);
     for (int j = 0; j < nkv; ++j) {
-      if (!warp_wait(&bars->s_full[t], s_phase, wc)) return;
-      s_phase ^= 1u;
+      const int sb = C::WIDE ? (j & 1) : t;  // S buffer, and its s_full / p_ready barriers
+      const uint32_t tS = tmem + lane_off + s_col(sb);
+      if (!warp_wait(&bars->s_full[sb], (s_phase >> sb) & 1u, wc)) return;
+      s_phase ^= 1u << sb;
       tc_fence_after();
       float s[BC];
       {
@@ -515,22 +638,35 @@ __device__ void softmax_role(const PrefillArgs &a, Bars *bars, uint32_t tmem, co
         tmem_st_x32(tS, p0);
         tmem_st_x32(tS + 32, p1);
       }
+      if constexpr (C::WIDE) {
+        // S(j) was issued before PV(j-1): wait for PV(j-1) before touching O.
+        if (j > 0) {
+          if (!warp_wait(&bars->pv_done, pv_phase, wc)) return;
+          pv_phase ^= 1u;
+          tc_fence_after();
+        }
+      }
       if (__any_sync(0xffffffffu, grow)) {
         // Conditional rescale of the O accumulator held in TMEM, done after P so that the
         // whole O row fits in the registers the scores used (one TMEM round trip).
-        // PV_t(j-1) has completed: its commit precedes the one that signalled S_t(j).
-        if constexpr (D == 128) {
-          uint32_t o0[64], o1[64];
-          tmem_ld_2x64(tO, tO + 64, o0, o1);
+        // Two sub-tiles: PV_t(j-1) has completed, its commit precedes the one that
+        // signalled S_t(j).
+        if constexpr (D >= 128) {
+#pragma unroll 1
+          for (int h = 0; h < D / 128; ++h) {
+            const uint32_t tOh = tO + static_cast<uint32_t>(h * 128);
+            uint32_t o0[64], o1[64];
+            tmem_ld_2x64(tOh, tOh + 64, o0, o1);
 #pragma unroll
-          for (int i = 0; i < 64; ++i) {
-            o0[i] = __float_as_uint(__uint_as_float(o0[i]) * alpha);
-            o1[i] = __float_as_uint(__uint_as_float(o1[i]) * alpha);
+            for (int i = 0; i < 64; ++i) {
+              o0[i] = __float_as_uint(__uint_as_float(o0[i]) * alpha);
+              o1[i] = __float_as_uint(__uint_as_float(o1[i]) * alpha);
+            }
+            tmem_st_x32(tOh, *reinterpret_cast<uint32_t (*)[32]>(&o0[0]));
+            tmem_st_x32(tOh + 32, *reinterpret_cast<uint32_t (*)[32]>(&o0[32]));
+            tmem_st_x32(tOh + 64, *reinterpret_cast<uint32_t (*)[32]>(&o1[0]));
+            tmem_st_x32(tOh + 96, *reinterpret_cast<uint32_t (*)[32]>(&o1[32]));
           }
-          tmem_st_x32(tO, *reinterpret_cast<uint32_t (*)[32]>(&o0[0]));
-          tmem_st_x32(tO + 32, *reinterpret_cast<uint32_t (*)[32]>(&o0[32]));
-          tmem_st_x32(tO + 64, *reinterpret_cast<uint32_t (*)[32]>(&o1[0]));
-          tmem_st_x32(tO + 96, *reinterpret_cast<uint32_t (*)[32]>(&o1[32]));
         } else {
           uint32_t o0[64];
           tmem_ld_x64(tO, o0);
@@ -542,7 +678,7 @@ __device__ void softmax_role(const PrefillArgs &a, Bars *bars, uint32_t tmem, co
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&bars->p_ready[t]);
+      mbar_arrive(&bars->p_ready[sb]);
       m = m_new;
     }
 
@@ -603,7 +739,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < SCHED_DEPTH; ++i) {
       mbar_init(&bars->sched_full[i], 1);
-      mbar_init(&bars->sched_empty[i], 1 + 256);  // MMA lane + every softmax thread
+      mbar_init(&bars->sched_empty[i], 1 + 128 * C::NSUB);  // MMA lane + every softmax thread
     }
     mbar_init(&bars->q_full, 1);
     mbar_init(&bars->q_empty, 1);
@@ -617,6 +753,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(&bars->o_full[t], 1);
       mbar_init(&bars->o_empty[t], 128);
     }
+    mbar_init(&bars->pv_done, 1);
     mbar_init(&bars->mma_done, 1);
     bars->abort = 0;
     fence_barrier_init();
@@ -638,18 +775,30 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   // Each register-split branch ends the kernel on its own; the two meet at a named barrier
   // before TMEM is released.
+  // Wide kernel: the second softmax warpgroup has no sub-tile and only gives its registers
+  // back; the producer / MMA warpgroup then keeps its launch registers.
+  // Registers: 128 x (200 + 24 + 168) = 50176 <= 384 x 168 = 64512.
   if (warp < PRODUCER_WARP) {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(SOFTMAX_REGS));
-    softmax_role<D, MASK, F16>(a, bars, tmem, wc, warp, lane);
+    if (C::WIDE && warp >= 4) {
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(IDLE_REGS));
+    } else {
+      asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(SOFTMAX_REGS));
+      softmax_role<D, MASK, F16>(a, bars, tmem, wc, warp, lane);
+    }
     __syncwarp();
     tc_fence_before();
     named_barrier(1, NTHREADS);
   } else {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(OTHER_REGS));
+    if constexpr (!C::WIDE) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(OTHER_REGS));
     if (warp == PRODUCER_WARP) {
       if (lane == 0) producer_role<D, MASK>(a, &tmq, &tmk, &tmv, smem, bars, wc);
     } else if (warp == MMA_WARP) {
-      if (lane == 0) mma_role<D, MASK, F16>(a, smem, bars, tmem, wc);
+      if (lane == 0) {
+        if constexpr (C::WIDE)
+          mma_role_wide<D, MASK, F16>(a, smem, bars, tmem, wc);
+        else
+          mma_role<D, MASK, F16>(a, smem, bars, tmem, wc);
+      }
     }
     __syncwarp();
     tc_fence_before();
@@ -696,7 +845,9 @@ int next_prefill_sched_slot() {
   return static_cast<int>(seq.fetch_add(1u) % NUM_SCHED_SLOTS);
 }
 
-int prefill_smem_bytes(int d) { return d == 64 ? Cfg<64>::SMEM_BYTES : Cfg<128>::SMEM_BYTES; }
+int prefill_smem_bytes(int d) {
+  return d == 64 ? Cfg<64>::SMEM_BYTES : (d == 128 ? Cfg<128>::SMEM_BYTES : Cfg<256>::SMEM_BYTES);
+}
 
 template <int D, bool F16>
 cudaError_t launch_mask(int mask, const CUtensorMap &tq, const CUtensorMap &tk,
@@ -715,6 +866,9 @@ cudaError_t launch_prefill(int d, int mask, bool f16, const CUtensorMap &tq,
   if (d == 64)
     return f16 ? launch_mask<64, true>(mask, tq, tk, tv, a, grid, stream)
                : launch_mask<64, false>(mask, tq, tk, tv, a, grid, stream);
+  if (d == 256)
+    return f16 ? launch_mask<256, true>(mask, tq, tk, tv, a, grid, stream)
+               : launch_mask<256, false>(mask, tq, tk, tv, a, grid, stream);
   return f16 ? launch_mask<128, true>(mask, tq, tk, tv, a, grid, stream)
              : launch_mask<128, false>(mask, tq, tk, tv, a, grid, stream);
 }

@@ -46,6 +46,8 @@ WORKLOADS = {
     "decode": Workload("decode", "kvcache", 64, 32, 8, 1, 32768, 128, False, 1005),
     # a smaller decode case (537 MB of cache) for profiling captures
     "decode16": Workload("decode16", "kvcache", 16, 32, 8, 1, 8192, 128, False, 1006),
+    # the causal 8k shape at head dimension 256 (half the heads: the same bytes per token)
+    "causal8k_d256": Workload("causal8k_d256", "dense", 2, 16, 16, 8192, 8192, 256, True, 1007),
 }
 
 

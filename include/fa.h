@@ -56,7 +56,8 @@ typedef enum fa_dtype {
 typedef enum fa_status {
     FA_OK = 0,
     FA_ERR_INVALID_ARG = 1, /* null pointer, bad size, Hq % Hkv != 0, misaligned pointer/stride */
-    FA_ERR_UNSUPPORTED = 2, /* d not a multiple of 8 in [8, 128], dtype not a fa_dtype,
+    FA_ERR_UNSUPPORTED = 2, /* d not a multiple of 8 in [8, 256] (fa_fwd, fa_fwd_varlen) or
+                               [8, 128] (decode, backward), dtype not a fa_dtype,
                                decode group size not in {1,2,4,8}, or the current device is
                                not an sm_103 GPU */
     FA_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed: see fa_last_cuda_error() */
@@ -100,7 +101,8 @@ typedef struct fa_score_mod {
  *   k, v: [B, Nk, Hkv, d] bf16, same convention with k_strides / v_strides
  *   o   : [B, Nq, Hq,  d] bf16 output, same convention with o_strides
  *   lse : [B, Hq, Nq] fp32 output, contiguous
- * Strides are in elements; the head dimension has unit stride.
+ * Strides are in elements; the head dimension has unit stride.  d: a multiple of 8 up to
+ * 256 (the capabilities table of "flash-attention": head_dim <= 256, multiple of 8).
  * scale multiplies the scores before the softmax (usually 1/sqrt(d)); causal != 0
  * applies the bottom-right causal mask; mod holds the score modifiers (zero-filled = none).
  * Nk = 0 is allowed (O = 0, LSE = -inf); B = 0 or Nq = 0 is a no-op.

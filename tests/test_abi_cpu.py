@@ -86,7 +86,7 @@ def _params(**kw):
 
 
 @pytest.mark.parametrize("change,status", [
-    ({"d": 100}, 2), ({"d": 256}, 2), ({"d": 0}, 2), ({"d": 4}, 2), ({"dtype": 2}, 2), ({"dtype": -1}, 2), ({"Hkv": 3}, 1), ({"Hq": 0}, 1), ({"B": -1}, 1),
+    ({"d": 100}, 2), ({"d": 264}, 2), ({"d": 252}, 2), ({"d": 0}, 2), ({"d": 4}, 2), ({"dtype": 2}, 2), ({"dtype": -1}, 2), ({"Hkv": 3}, 1), ({"Hq": 0}, 1), ({"B": -1}, 1),
     ({"scale": 0.0}, 1), ({"scale": float("nan")}, 1), ({"scale": -1.0}, 1),
     ({"q": 4098}, 1), ({"o": 4100}, 1), ({"lse": 4098}, 1), ({"q": None}, 1),
     ({"k": None}, 1), ({"Nq": -5}, 1),
@@ -138,7 +138,7 @@ def test_varlen_rejects_bad_arguments(lib):
                  a["dtype"], a.get("mod"), None)
 
     assert call(d=84) == 2
-    assert call(d=136) == 2
+    assert call(d=264) == 2
     assert call(dtype=3) == 2
     assert call(Hkv=3) == 1
     assert call(cq=None) == 1

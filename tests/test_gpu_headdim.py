@@ -122,3 +122,79 @@ def test_backward_head_dims(d, causal):
     q, k, v = dense_inputs(1, 300, 300, 4, 2, d, seed=870 + d, device=DEV)
     do = bf16_normal((1, 300, 4, d), seed=871 + d, device=DEV)
     _check_bwd(q, k, v, do, _scale(d), causal, f"bwd d={d} causal={causal}")
+
+
+# Head dimensions above 128 (forward only): the wide kernel, one 128-row sub-tile per work
+# tile with S double-buffered in TMEM and K / V moved as d halves.
+
+@pytest.mark.parametrize("d,causal", [(256, False), (256, True), (192, True), (136, False),
+                                      (248, True)])
+def test_dense_wide_head_dims(d, causal):
+    q, k, v = dense_inputs(2, 333, 300, 4, 2, d, seed=880 + d, device=DEV)
+    o, lse = fa_fwd(q, k, v, causal=causal)
+    assert get_last_device_error() == FA_OK
+    assert o.shape[-1] == d
+    o_ref, lse_ref = ORACLE.attention(q.cpu(), k.cpu(), v.cpu(), _scale(d), causal)
+    compare(*dense_rows(o, lse), *dense_rows(o_ref, lse_ref), f"wide d={d} causal={causal}")
+
+
+def test_dense_wide_long_causal():
+    """Many K/V steps per tile (both S buffers, the ring wrapping many times, rescales)."""
+    d = 256
+    q, k, v = dense_inputs(1, 1100, 1100, 2, 1, d, seed=890, device=DEV)
+    o, lse = fa_fwd(q, k, v, causal=True)
+    assert get_last_device_error() == FA_OK
+    o_ref, lse_ref = ORACLE.attention(q.cpu(), k.cpu(), v.cpu(), _scale(d), True)
+    compare(*dense_rows(o, lse), *dense_rows(o_ref, lse_ref), "wide d=256 N=1100 causal")
+
+
+def test_dense_wide_fp16_gqa():
+    d = 256
+    q, k, v = dense_inputs(2, 256, 640, 8, 2, d, seed=891, device=DEV, dtype=torch.float16)
+    o, lse = fa_fwd(q, k, v, causal=False)
+    assert get_last_device_error() == FA_OK
+    o_ref, lse_ref = ORACLE.attention(q.cpu(), k.cpu(), v.cpu(), _scale(d), False)
+    compare(*dense_rows(o, lse), *dense_rows(o_ref, lse_ref), "wide fp16 GQA")
+
+
+@pytest.mark.parametrize("mod", [dict(window_size=(100, 20)), dict(softcap=15.0),
+                                 dict(window_size=(300, -1), softcap=8.0, alibi=True)])
+def test_dense_wide_modifiers(mod):
+    d, Hq = 256, 4
+    mod = dict(mod)
+    slopes = None
+    if mod.pop("alibi", False):
+        slopes = torch.tensor(2.0 ** (-8.0 * np.arange(1, Hq + 1) / Hq), dtype=torch.float32)
+    q, k, v = dense_inputs(1, 500, 500, Hq, 2, d, seed=892, device=DEV)
+    o, lse = fa_fwd(q, k, v, causal=True, alibi_slopes=None if slopes is None else
+                    slopes.to(DEV), **mod)
+    assert get_last_device_error() == FA_OK
+    o_ref, lse_ref = ORACLE.attention(q.cpu(), k.cpu(), v.cpu(), _scale(d), True,
+                                      window=mod.get("window_size", (-1, -1)),
+                                      softcap=mod.get("softcap", 0.0), alibi_slopes=slopes)
+    compare(*dense_rows(o, lse), *dense_rows(o_ref, lse_ref), f"wide {sorted(mod)}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_wide_head_dims(causal):
+    d = 256
+    sq, sk = [5, 0, 333, 129, 1], [7, 3, 333, 200, 0]
+    q, k, v, cu_q, cu_k = varlen_inputs(sq, sk, 4, 2, d, seed=893, device=DEV)
+    o, lse = fa_fwd_varlen(q, k, v, cu_q, cu_k, max(sq), max(sk), causal=causal)
+    assert get_last_device_error() == FA_OK
+    o_ref, lse_ref = ORACLE.attention_varlen(q.cpu(), k.cpu(), v.cpu(), cu_q.cpu(), cu_k.cpu(),
+                                             _scale(d), causal)
+    compare(*varlen_rows(o, lse), *varlen_rows(o_ref, lse_ref), f"varlen wide causal={causal}")
+
+
+def test_wide_head_dims_not_served_by_decode_and_backward():
+    from exact_attention_81_gb300 import FAError
+    d = 256
+    q, k, v = dense_inputs(1, 128, 128, 2, 2, d, seed=894, device=DEV)
+    o, lse = fa_fwd(q, k, v)
+    with pytest.raises(FAError):
+        fa_bwd(q, k, v, o, lse, torch.ones_like(q))
+    lens = torch.tensor([100], dtype=torch.int32)
+    qd, kc, vc, lens = kvcache_inputs(1, 256, 2, 2, d, seed=895, lengths=lens, device=DEV)
+    with pytest.raises(FAError):
+        fa_fwd_kvcache(qd, kc, vc, lens)
