@@ -193,6 +193,7 @@ __device__ __forceinline__ bool varlen_bad(const PrefillArgs &a, int b) {
          (q1 - q0) > a.Nq;
 }
 
+// Both issue helpers are warp-collective (the whole MMA warp runs them, one lane issues).
 // S_t = Q_t K^T: D/16 MMAs of 128 x 128 x 16.  Both operands K-major, 128B-swizzled:
 // k-step kk lives in box kk/4 at byte offset 32*(kk%4) inside each 128-byte row.
 template <int D, bool F16>
@@ -200,8 +201,8 @@ __device__ __forceinline__ void issue_s(uint32_t d_tmem, uint32_t q_smem, uint32
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint32_t off = static_cast<uint32_t>((kk >> 2) * BOX_BYTES + (kk & 3) * 32);
-    mma_bf16_ss(d_tmem, sw128_desc(q_smem + off, 16, 1024), sw128_desc(k_smem + off, 16, 1024),
-                Cfg<D, F16>::IDESC_S, kk > 0 ? 1u : 0u);
+    mma_bf16_ss_w(d_tmem, sw128_desc(q_smem + off, 16, 1024),
+                  sw128_desc(k_smem + off, 16, 1024), Cfg<D, F16>::IDESC_S, kk > 0 ? 1u : 0u);
   }
 }
 
@@ -212,9 +213,9 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint3
                                          bool accumulate) {
 #pragma unroll
   for (int kk = 0; kk < BC / 16; ++kk) {
-    mma_bf16_ts(o_tmem, p_tmem + static_cast<uint32_t>(kk * 8),
-                sw128_desc(v_smem + static_cast<uint32_t>(kk * 16 * 128), BOX_BYTES, 1024),
-                Cfg<D, F16>::IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
+    mma_bf16_ts_w(o_tmem, p_tmem + static_cast<uint32_t>(kk * 8),
+                  sw128_desc(v_smem + static_cast<uint32_t>(kk * 16 * 128), BOX_BYTES, 1024),
+                  Cfg<D, F16>::IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
@@ -303,6 +304,24 @@ out:
   if (q_iter > 0) mbar_wait_teardown(&bars->q_full, (q_iter - 1) & 1u, 1000000000ull);
 }
 
+// Bounded wait by a whole warp; every lane gets the same answer.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const WaitCtl &wc) {
+  const bool ok = mbar_wait(bar, parity, wc);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Scheduler-ring consumer for the MMA warp: all lanes read the tile, one lane arrives (the
+// ring counts one arrival for the MMA warp).
+__device__ __forceinline__ bool next_tile_mma(Bars *bars, uint32_t k, int &tile, int lane,
+                                              const WaitCtl &wc) {
+  const int rs = static_cast<int>(k % SCHED_DEPTH);
+  if (!warp_wait(&bars->sched_full[rs], (k / SCHED_DEPTH) & 1u, wc)) return false;
+  tile = bars->sched_tile[rs];
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&bars->sched_empty[rs]);
+  return true;
+}
+
 // Consumer side of the scheduler ring: the k-th tile of this CTA (-1 = no more), or false
 // if the wait gave up.  WARP consumers are whole warps (all lanes call it).
 template <bool WARP>
@@ -326,7 +345,7 @@ __device__ __forceinline__ bool next_tile(Bars *bars, uint32_t k, int &tile, con
 
 template <int D, int MASK, bool F16>
 __device__ void mma_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, uint32_t tmem,
-                         const WaitCtl &wc) {
+                         const WaitCtl &wc, int lane) {
   using C = Cfg<D>;
   uint32_t kv_iter = 0, q_iter = 0;
   uint32_t p_phase[2] = {0u, 0u}, oe_phase[2] = {0u, 0u};
@@ -335,34 +354,34 @@ __device__ void mma_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, uint32
   const uint32_t ring = smem_u32(smem + C::RING_OFF);
   for (uint32_t k = 0;; ++k) {
     int tile;
-    if (!next_tile<false>(bars, k, tile, wc)) goto out;
+    if (!next_tile_mma(bars, k, tile, lane, wc)) goto out;
     if (tile < 0) break;
     const TileInfo ti = tile_info<MASK, 2>(a, tile);
     const int n = max(ti.je[0], ti.je[1]);
     if (n == 0) continue;
-    if (!mbar_wait(&bars->q_full, q_iter & 1u, wc)) goto out;
+    if (!warp_wait(&bars->q_full, q_iter & 1u, wc)) goto out;
     ++q_iter;
     {
       int slot_k = static_cast<int>(kv_iter % C::NSLOTS);
-      if (!mbar_wait(&bars->kv_full[slot_k], (kv_iter / C::NSLOTS) & 1u, wc)) goto out;
+      if (!warp_wait(&bars->kv_full[slot_k], (kv_iter / C::NSLOTS) & 1u, wc)) goto out;
       ++kv_iter;
       tc_fence_after();
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         if (ti.js[t] == 0 && ti.je[t] > 0) {
           issue_s<D, F16>(tmem + s_col(t), q_smem[t], ring + slot_k * C::TILE_BYTES);
-          mma_commit(&bars->s_full[t]);
+          mma_commit_w(&bars->s_full[t]);
         }
       }
-      mma_commit(&bars->kv_empty[slot_k]);
+      mma_commit_w(&bars->kv_empty[slot_k]);
       for (int j = 0; j < n; ++j) {
         const int slot_v = static_cast<int>(kv_iter % C::NSLOTS);
-        if (!mbar_wait(&bars->kv_full[slot_v], (kv_iter / C::NSLOTS) & 1u, wc)) goto out;
+        if (!warp_wait(&bars->kv_full[slot_v], (kv_iter / C::NSLOTS) & 1u, wc)) goto out;
         ++kv_iter;
         slot_k = -1;
         if (j + 1 < n) {
           slot_k = static_cast<int>(kv_iter % C::NSLOTS);
-          if (!mbar_wait(&bars->kv_full[slot_k], (kv_iter / C::NSLOTS) & 1u, wc)) goto out;
+          if (!warp_wait(&bars->kv_full[slot_k], (kv_iter / C::NSLOTS) & 1u, wc)) goto out;
           ++kv_iter;
         }
         tc_fence_after();
@@ -371,34 +390,34 @@ __device__ void mma_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, uint32
           if (j >= ti.js[t] && j < ti.je[t]) {
             if (j == ti.js[t] && o_pending[t]) {
               // O_t still holds the previous tile's result until its epilogue has read it.
-              if (!mbar_wait(&bars->o_empty[t], oe_phase[t], wc)) goto out;
+              if (!warp_wait(&bars->o_empty[t], oe_phase[t], wc)) goto out;
               oe_phase[t] ^= 1u;
               o_pending[t] = false;
             }
-            if (!mbar_wait(&bars->p_ready[t], p_phase[t], wc)) goto out;
+            if (!warp_wait(&bars->p_ready[t], p_phase[t], wc)) goto out;
             p_phase[t] ^= 1u;
             tc_fence_after();
             issue_pv<D, F16>(tmem + o_col(t), tmem + s_col(t), ring + slot_v * C::TILE_BYTES,
                              j > ti.js[t]);
             if (j == ti.je[t] - 1) {
-              mma_commit(&bars->o_full[t]);
+              mma_commit_w(&bars->o_full[t]);
               o_pending[t] = true;
             }
           }
-          if (t == 1) mma_commit(&bars->kv_empty[slot_v]);
+          if (t == 1) mma_commit_w(&bars->kv_empty[slot_v]);
           if (j + 1 >= ti.js[t] && j + 1 < ti.je[t]) {
             issue_s<D, F16>(tmem + s_col(t), q_smem[t], ring + slot_k * C::TILE_BYTES);
-            mma_commit(&bars->s_full[t]);
+            mma_commit_w(&bars->s_full[t]);
           }
         }
-        if (slot_k >= 0) mma_commit(&bars->kv_empty[slot_k]);
+        if (slot_k >= 0) mma_commit_w(&bars->kv_empty[slot_k]);
       }
     }
-    mma_commit(&bars->q_empty);
+    mma_commit_w(&bars->q_empty);
   }
 out:
   // Teardown: every MMA issued so far must finish before TMEM is released.
-  mma_commit(&bars->mma_done);
+  mma_commit_w(&bars->mma_done);
   mbar_wait_teardown(&bars->mma_done, 0u, 1000000000ull);
 }
 
@@ -411,7 +430,7 @@ out:
 // rescales O.
 template <int D, int MASK, bool F16>
 __device__ void mma_role_wide(const PrefillArgs &a, uint8_t *smem, Bars *bars, uint32_t tmem,
-                              const WaitCtl &wc) {
+                              const WaitCtl &wc, int lane) {
   using C = Cfg<D, F16>;
   uint32_t kv_iter = 0, q_iter = 0;
   uint32_t p_phase = 0u, oe_phase = 0u;  // p_phase: bit b for S buffer b
@@ -421,7 +440,7 @@ __device__ void mma_role_wide(const PrefillArgs &a, uint8_t *smem, Bars *bars, u
   // Next ring slot (its load has landed): its shared address, or 0 if the wait gave up.
   auto take = [&](int &slot) -> uint32_t {
     slot = static_cast<int>(kv_iter % C::NSLOTS);
-    if (!mbar_wait(&bars->kv_full[slot], (kv_iter / C::NSLOTS) & 1u, wc)) return 0u;
+    if (!warp_wait(&bars->kv_full[slot], (kv_iter / C::NSLOTS) & 1u, wc)) return 0u;
     ++kv_iter;
     tc_fence_after();
     return ring + static_cast<uint32_t>(slot * C::SLOT_BYTES);
@@ -436,24 +455,24 @@ __device__ void mma_role_wide(const PrefillArgs &a, uint8_t *smem, Bars *bars, u
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         const uint32_t off = static_cast<uint32_t>((kk >> 2) * BOX_BYTES + (kk & 3) * 32);
-        mma_bf16_ss(tmem + s_col(buf),
+        mma_bf16_ss_w(tmem + s_col(buf),
                     sw128_desc(q_smem + static_cast<uint32_t>(2 * h * BOX_BYTES) + off, 16, 1024),
                     sw128_desc(k_smem + off, 16, 1024), C::IDESC_S, (h | kk) ? 1u : 0u);
       }
-      mma_commit(&bars->kv_empty[slot]);
+      mma_commit_w(&bars->kv_empty[slot]);
     }
-    mma_commit(&bars->s_full[buf]);
+    mma_commit_w(&bars->s_full[buf]);
     return true;
   };
   for (uint32_t k = 0;; ++k) {
     int tile;
-    if (!next_tile<false>(bars, k, tile, wc)) goto out;
+    if (!next_tile_mma(bars, k, tile, lane, wc)) goto out;
     if (tile < 0) break;
     {
       const TileInfo ti = tile_info<MASK, 1>(a, tile);
       const int n = ti.je[0];
       if (n == 0) continue;
-      if (!mbar_wait(&bars->q_full, q_iter & 1u, wc)) goto out;
+      if (!warp_wait(&bars->q_full, q_iter & 1u, wc)) goto out;
       ++q_iter;
       tc_fence_after();
       if (!issue_s_wide(0)) goto out;
@@ -462,11 +481,11 @@ __device__ void mma_role_wide(const PrefillArgs &a, uint8_t *smem, Bars *bars, u
         const int buf = j & 1;
         if (j == 0 && o_pending) {
           // O still holds the previous tile's result until its epilogue has read it.
-          if (!mbar_wait(&bars->o_empty[0], oe_phase, wc)) goto out;
+          if (!warp_wait(&bars->o_empty[0], oe_phase, wc)) goto out;
           oe_phase ^= 1u;
           o_pending = false;
         }
-        if (!mbar_wait(&bars->p_ready[buf], (p_phase >> buf) & 1u, wc)) goto out;
+        if (!warp_wait(&bars->p_ready[buf], (p_phase >> buf) & 1u, wc)) goto out;
         p_phase ^= 1u << buf;
         tc_fence_after();
 #pragma unroll 1
@@ -476,31 +495,26 @@ __device__ void mma_role_wide(const PrefillArgs &a, uint8_t *smem, Bars *bars, u
           if (v_smem == 0u) goto out;
           issue_pv<D, F16>(tmem + o_col(0) + static_cast<uint32_t>(h * 128), tmem + s_col(buf),
                            v_smem, j > 0);
-          mma_commit(&bars->kv_empty[slot]);
+          mma_commit_w(&bars->kv_empty[slot]);
         }
         if (j == n - 1) {
-          mma_commit(&bars->o_full[0]);
+          mma_commit_w(&bars->o_full[0]);
           o_pending = true;
         } else {
-          mma_commit(&bars->pv_done);
+          mma_commit_w(&bars->pv_done);
         }
         if (j + 2 < n && !issue_s_wide(buf)) goto out;
       }
-      mma_commit(&bars->q_empty);
+      mma_commit_w(&bars->q_empty);
     }
   }
 out:
-  mma_commit(&bars->mma_done);
+  mma_commit_w(&bars->mma_done);
   mbar_wait_teardown(&bars->mma_done, 0u, 1000000000ull);
 }
 
 // ------------------------------------------------------------------------------------
 // Softmax / correction / epilogue: one thread per query row of its sub-tile.
-
-__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const WaitCtl &wc) {
-  const bool ok = mbar_wait(bar, parity, wc);
-  return __all_sync(0xffffffffu, ok);
-}
 
 template <int D, int MASK, bool F16>
 __device__ void softmax_role(const PrefillArgs &a, Bars *bars, uint32_t tmem, const WaitCtl &wc,
@@ -793,12 +807,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (warp == PRODUCER_WARP) {
       if (lane == 0) producer_role<D, MASK>(a, &tmq, &tmk, &tmv, smem, bars, wc);
     } else if (warp == MMA_WARP) {
-      if (lane == 0) {
-        if constexpr (C::WIDE)
-          mma_role_wide<D, MASK, F16>(a, smem, bars, tmem, wc);
-        else
-          mma_role<D, MASK, F16>(a, smem, bars, tmem, wc);
-      }
+      if constexpr (C::WIDE)
+        mma_role_wide<D, MASK, F16>(a, smem, bars, tmem, wc, lane);
+      else
+        mma_role<D, MASK, F16>(a, smem, bars, tmem, wc, lane);
     }
     __syncwarp();
     tc_fence_before();
