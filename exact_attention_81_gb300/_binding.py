@@ -156,6 +156,8 @@ def load_library(path: str | None = None):
         lib.fa_last_cuda_error.restype = ctypes.c_char_p
         lib.fa_set_wait_timeout_ns.argtypes = [ctypes.c_ulonglong]
         lib.fa_set_wait_timeout_ns.restype = None
+        lib.fa_set_fault_injection.argtypes = [ctypes.c_int]
+        lib.fa_set_fault_injection.restype = None
         lib.fa_fwd_params_size.argtypes = []
         lib.fa_fwd_params_size.restype = sz
         lib.fa_bwd.argtypes = [ctypes.POINTER(BwdParams), vp]
@@ -494,6 +496,11 @@ def get_last_device_error(stream=None) -> int:
 def set_wait_timeout_ns(ns: int):
     """Limit on device-side waits for later launches (0 = default)."""
     load_library().fa_set_wait_timeout_ns(int(ns))
+
+
+def set_fault_injection(withhold_loads: bool):
+    """Testing aid: later kernels issue no loads, so their waits run into the limit."""
+    load_library().fa_set_fault_injection(int(bool(withhold_loads)))
 
 
 # Names of the upstream Python API ("flash-attention", section 1), mapped onto the C calls.

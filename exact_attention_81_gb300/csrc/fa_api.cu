@@ -33,6 +33,7 @@ struct DeviceInfo {
 std::mutex g_mutex;
 DeviceInfo g_dev[kMaxDevices];
 unsigned long long g_timeout_ns = kDefaultTimeoutNs;
+int g_inject = 0;  // fa_set_fault_injection
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                    const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -268,6 +269,8 @@ void fa_set_wait_timeout_ns(unsigned long long ns) {
   g_timeout_ns = ns == 0 ? kDefaultTimeoutNs : ns;
 }
 
+void fa_set_fault_injection(int withhold_loads) { g_inject = withhold_loads != 0; }
+
 fa_status fa_fwd(const fa_fwd_params *p, cudaStream_t stream) {
   if (p == nullptr) return FA_ERR_INVALID_ARG;
   const fa_fwd_params &a = *p;
@@ -338,6 +341,7 @@ fa_status fa_fwd(const fa_fwd_params *p, cudaStream_t stream) {
   pa.scale_log2 = scale_log2(a.scale);
   pa.err = dev->err;
   pa.timeout_ns = g_timeout_ns;
+  pa.inject = g_inject;
   pa.sched_slot = fa::next_prefill_sched_slot();
   pa.d = a.d;
   apply_mod(mod, a.scale, &pa);
@@ -420,6 +424,7 @@ fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, fl
   pa.scale_log2 = scale_log2(scale);
   pa.err = dev->err;
   pa.timeout_ns = g_timeout_ns;
+  pa.inject = g_inject;
   pa.sched_slot = fa::next_prefill_sched_slot();
   pa.d = d;
   apply_mod(mod, scale, &pa);
@@ -574,6 +579,7 @@ fa_status fa_fwd_kvcache(const void *q, const void *k_cache, const void *v_cache
     da.scale_log2 = scale_log2(scale);
     da.err = dev->err;
     da.timeout_ns = g_timeout_ns;
+    da.inject = g_inject;
     da.wl = mod.wl;
     // the score arrives as scale * q.k * log2(e): softcap * tanh(z / softcap) * log2(e)
     da.sc_in = mod.softcap > 0.f
@@ -719,6 +725,7 @@ fa_status fa_bwd(const fa_bwd_params *p, cudaStream_t stream) {
   ba.scale_log2 = scale_log2(a.scale);
   ba.err = dev->err;
   ba.timeout_ns = g_timeout_ns;
+  ba.inject = g_inject;
   const int grid = static_cast<int>(units < dev->sm_count ? units : dev->sm_count);
   e = fa::launch_bwd(fa::kernel_d(a.d), mod.mask, f16, tq, tk, tv, tdo, tdq, ba, grid, stream);
   if (e != cudaSuccess) return cuda_fail("backward kernel launch", e);
@@ -830,6 +837,7 @@ fa_status fa_bwd_varlen(const void *q, const void *k, const void *v, const void 
   ba.scale_log2 = scale_log2(scale);
   ba.err = dev->err;
   ba.timeout_ns = g_timeout_ns;
+  ba.inject = g_inject;
   const int grid = static_cast<int>(units < dev->sm_count ? units : dev->sm_count);
   e = fa::launch_bwd(fa::kernel_d(d), mod.mask, f16, tq, tk, tv, tdo, tdq, ba, grid, stream);
   if (e != cudaSuccess) return cuda_fail("backward kernel launch", e);

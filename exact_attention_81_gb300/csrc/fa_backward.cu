@@ -186,13 +186,14 @@ __device__ __forceinline__ bool group_sync(uint64_t *bar, uint32_t &phase, const
   return ok;
 }
 
+// The issue helpers are warp-collective (the whole MMA warp runs them, one lane issues).
 // M=128 x N=128 x K=D product of two K-major 128-byte-swizzled tiles (S^T and dP^T).
 template <int D, bool F16>
 __device__ __forceinline__ void issue_kmajor(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem) {
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint32_t off = static_cast<uint32_t>((kk >> 2) * BOX + (kk & 3) * 32);
-    mma_bf16_ss(d_tmem, sw128_desc(a_smem + off, 16, 1024), sw128_desc(b_smem + off, 16, 1024),
+    mma_bf16_ss_w(d_tmem, sw128_desc(a_smem + off, 16, 1024), sw128_desc(b_smem + off, 16, 1024),
                 BCfg<D, F16>::IDESC_S, kk > 0 ? 1u : 0u);
   }
 }
@@ -210,7 +211,7 @@ __device__ __forceinline__ void issue_acc(uint32_t d_tmem, uint32_t a_tmem, uint
                                           bool accumulate) {
 #pragma unroll
   for (int kk = 0; kk < BQ / 16; ++kk)
-    mma_bf16_ts(d_tmem, a_tmem + packed_col(kk * 16),
+    mma_bf16_ts_w(d_tmem, a_tmem + packed_col(kk * 16),
                 sw128_desc(b_smem + static_cast<uint32_t>(kk * 16 * 128), BOX, 1024),
                 BCfg<D, F16>::IDESC_ACC, (accumulate || kk > 0) ? 1u : 0u);
 }
@@ -222,7 +223,7 @@ __device__ __forceinline__ void issue_dq(uint32_t d_tmem, uint32_t ds_smem, uint
 #pragma unroll
   for (int kk = 0; kk < BKEY / 16; ++kk) {
     const uint32_t off = static_cast<uint32_t>(kk * 16 * 128);
-    mma_bf16_ss(d_tmem, sw128_desc(ds_smem + off, BOX, 1024), sw128_desc(k_smem + off, BOX, 1024),
+    mma_bf16_ss_w(d_tmem, sw128_desc(ds_smem + off, BOX, 1024), sw128_desc(k_smem + off, BOX, 1024),
                 BCfg<D, F16>::IDESC_DQ, kk > 0 ? 1u : 0u);
   }
 }
@@ -238,6 +239,7 @@ __device__ void bwd_producer(const BwdArgs &a, const CUtensorMap *tq, const CUte
   float *lse2 = reinterpret_cast<float *>(smem + C::VEC_OFF);
   float *dvec = lse2 + BQ;
   uint32_t kv_n = 0, q_n = 0;
+  if (a.inject) goto out;  // failure injection: load nothing, the consumers' waits run out
   for (int u = blockIdx.x; u < a.num_units; u += gridDim.x) {
     const BUnit w = bunit_of<MASK>(a, u);
     if (w.bad && w.j == 0 && w.g == 0 && lane == 0) atomicOr(a.err, DEVERR_BAD_CU_SEQLENS);
@@ -303,7 +305,8 @@ out:
 }
 
 // ------------------------------------------------------------------------------------
-// MMA issuer (one lane).
+// MMA issuer: the whole warp runs the loop, one elected lane issues (an issuing loop
+// confined to one lane is starved by the compute warps of its sub-partition).
 
 template <int D, int MASK, bool F16>
 __device__ void bwd_mma(const BwdArgs &a, uint8_t *smem, BBars *bars, uint32_t tmem,
@@ -316,36 +319,36 @@ __device__ void bwd_mma(const BwdArgs &a, uint8_t *smem, BBars *bars, uint32_t t
   for (int u = blockIdx.x; u < a.num_units; u += gridDim.x) {
     const BUnit w = bunit_of<MASK>(a, u);
     if (w.nit == 0) continue;
-    if (!mbar_wait(&bars->kv_full, kv_n & 1u, wc)) goto out;
+    if (!warp_wait(&bars->kv_full, kv_n & 1u, wc)) goto out;
     ++kv_n;
-    if (acc_n > 0 && !mbar_wait(&bars->acc_empty, (acc_n - 1) & 1u, wc)) goto out;
+    if (acc_n > 0 && !warp_wait(&bars->acc_empty, (acc_n - 1) & 1u, wc)) goto out;
     for (int t = 0; t < w.nit; ++t) {
-      if (!mbar_wait(&bars->q_full, it & 1u, wc)) goto out;
+      if (!warp_wait(&bars->q_full, it & 1u, wc)) goto out;
       tc_fence_after();
       issue_kmajor<D, F16>(tmem + T_ST, sK, sQ);                  // S^T = K Q^T
-      mma_commit(&bars->st_full);
-      if (!mbar_wait(&bars->do_full, it & 1u, wc)) goto out;
+      mma_commit_w(&bars->st_full);
+      if (!warp_wait(&bars->do_full, it & 1u, wc)) goto out;
       // dP^T overwrites the previous step's dQ: wait until the epilogue has read it.
-      if (it > 0 && !mbar_wait(&bars->dq_empty, (it - 1) & 1u, wc)) goto out;
+      if (it > 0 && !warp_wait(&bars->dq_empty, (it - 1) & 1u, wc)) goto out;
       tc_fence_after();
       issue_kmajor<D, F16>(tmem + T_DP, sV, sDO);                 // dP^T = V dO^T
-      mma_commit(&bars->dp_full);
-      if (!mbar_wait(&bars->p_ready, it & 1u, wc)) goto out;
+      mma_commit_w(&bars->dp_full);
+      if (!warp_wait(&bars->p_ready, it & 1u, wc)) goto out;
       tc_fence_after();
       issue_acc<D, F16>(tmem + T_DK, tmem + T_DP, sQ, t > 0);     // dK += dS^T Q
-      mma_commit(&bars->q_empty);
+      mma_commit_w(&bars->q_empty);
       issue_acc<D, F16>(tmem + T_DV, tmem + T_ST, sDO, t > 0);    // dV += P^T dO
-      mma_commit(&bars->do_empty);
+      mma_commit_w(&bars->do_empty);
       issue_dq<D, F16>(tmem + T_DP, sDS, sK);                     // dQ = dS K
-      mma_commit(&bars->dq_full);
+      mma_commit_w(&bars->dq_full);
       ++it;
     }
-    mma_commit(&bars->kv_empty);
-    mma_commit(&bars->acc_full);
+    mma_commit_w(&bars->kv_empty);
+    mma_commit_w(&bars->acc_full);
     ++acc_n;
   }
 out:
-  mma_commit(&bars->mma_done);
+  mma_commit_w(&bars->mma_done);
   mbar_wait_teardown(&bars->mma_done, 0u, 1000000000ull);
 }
 
@@ -606,7 +609,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(OTHER_REGS));
     if (warp == PRODUCER_WARP) {
       bwd_producer<D, MASK, F16>(a, &tq, &tk, &tv, &tdo, smem, bars, wc, lane);
-    } else if (warp == MMA_WARP && lane == 0) {
+    } else if (warp == MMA_WARP) {
       bwd_mma<D, MASK, F16>(a, smem, bars, tmem, wc);
     }
     __syncwarp();

@@ -121,6 +121,7 @@ __device__ void producer(const DecodeArgs &a, const CUtensorMap *tmk, const CUte
   using C = DCfg<D, G>;
   uint32_t it = 0;
   const uint64_t policy = policy_evict_first();  // every cache byte is read once
+  if (a.inject) goto out;  // failure injection: load nothing, the consumers' waits run out
   for (int u = blockIdx.x; u < a.num_units; u += gridDim.x) {
     const Unit w = unit_of(a, u);
     if (w.c == 0 && w.g == 0) {

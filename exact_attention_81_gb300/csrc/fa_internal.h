@@ -39,6 +39,7 @@ struct PrefillArgs {
                               // the columns past d arrive as zeros and are not stored)
   unsigned int *err;          // device error word
   unsigned long long timeout_ns;
+  int inject;                 // failure injection: the producer issues no load at all
   // Score modifiers (read by the MASK_MOD kernel only).
   int wl, wr;                 // window bounds in keys, -1 = unbounded (causal folded: wr = 0)
   float sc_in, sc_out;        // softcap: s -> tanh(s * sc_in) * sc_out (log2 units); 0 = off
@@ -81,6 +82,7 @@ struct DecodeArgs {
   float scale_log2;
   unsigned int *err;
   unsigned long long timeout_ns;
+  int inject;                 // failure injection: the producer issues no load at all
   // Score modifiers (uniform runtime branches).
   int wl;                     // left window bound in keys, -1 = unbounded
   float sc_in, sc_out;        // softcap on the log2-domain score: tanh(s * sc_in) * sc_out
@@ -164,6 +166,7 @@ struct BwdArgs {
   float scale, scale_log2;
   unsigned int *err;
   unsigned long long timeout_ns;
+  int inject;                 // failure injection: the producer issues no load at all
 };
 
 // D = rowsum(dO * O) per query row and a zeroed fp32 dQ accumulator [B, Nq, Hq, d].

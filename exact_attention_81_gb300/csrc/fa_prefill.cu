@@ -245,6 +245,9 @@ __device__ void producer_role(const PrefillArgs &a, const CUtensorMap *tmq,
     return true;
   };
   for (uint32_t k = 0;; ++k) {
+    // Failure injection: publish nothing and load nothing; every other role's first wait
+    // runs into the wait limit.
+    if (a.inject) break;
     const int ticket = static_cast<int>(atomicAdd(&ctr[0], 1u));
     const int tile = ticket < a.num_tiles ? ticket : -1;
     const int rs = static_cast<int>(k % SCHED_DEPTH);

@@ -348,6 +348,16 @@ const char *fa_last_cuda_error(void);
  */
 void fa_set_wait_timeout_ns(unsigned long long ns);
 
+/*
+ * Failure injection, a testing aid (process-wide, for kernels launched after the call):
+ * with withhold_loads != 0 the producer role of every attention kernel issues no load, so
+ * the other roles' first waits cannot complete and run into the wait limit (set a short
+ * one with fa_set_wait_timeout_ns); the call then reports FA_ERR_TIMEOUT through
+ * fa_get_last_device_error and its outputs are unspecified.  Nothing faults and the
+ * context stays usable.  0 (the default) turns it off.
+ */
+void fa_set_fault_injection(int withhold_loads);
+
 #ifdef __cplusplus
 }
 #endif

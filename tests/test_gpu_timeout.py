@@ -1,14 +1,15 @@
-"""Failure detection without faulting the GPU: with a 1 ns limit on device-side waits the
-kernels give up at their first unsatisfied wait, unwind (bounded teardown of their own
-bulk copies and MMAs, TMEM released) and report FA_ERR_TIMEOUT through the device error
-word.  The context stays usable: the next call with the default limit is bit-identical to
-one made before the failure (which also shows that the prefill tile-ticket counters were
-left clean)."""
+"""Failure detection without faulting the GPU: with failure injection on, every kernel's
+producer issues no load, so the other roles wait for data that never arrives; with a short
+limit on device-side waits they give up, unwind (bounded teardown of their own bulk copies
+and MMAs, TMEM released) and report FA_ERR_TIMEOUT through the device error word.  The
+context stays usable: the next call without injection is bit-identical to one made before
+the failure (which also shows that the prefill tile-ticket counters were left clean)."""
 import pytest
 import torch
 
 from exact_attention_81_gb300 import (FA_ERR_TIMEOUT, FA_OK, fa_bwd, fa_fwd, fa_fwd_kvcache,
-                                      get_last_device_error, set_wait_timeout_ns)
+                                      get_last_device_error, set_fault_injection,
+                                      set_wait_timeout_ns)
 from exact_attention_81_gb300.inputs import bf16_normal, dense_inputs, kvcache_inputs
 
 pytestmark = pytest.mark.gpu
@@ -16,11 +17,14 @@ DEV = "cuda"
 
 
 def _with_tiny_timeout(fn):
-    set_wait_timeout_ns(1)
+    """Run fn with the producers withholding every load and a 200 us wait limit."""
+    set_wait_timeout_ns(200_000)
+    set_fault_injection(True)
     try:
         fn()
         return get_last_device_error()
     finally:
+        set_fault_injection(False)
         set_wait_timeout_ns(0)
 
 
