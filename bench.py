@@ -101,7 +101,8 @@ def profiled_traffic(kernel: str, src_files, workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason sampling in the background (200 ms period)."""
+    """nvidia-smi clock / throttle-reason sampling in the background (25 ms period: the
+    timed region of a default run lasts well under a second)."""
 
     QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -117,7 +118,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "25"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -149,7 +150,7 @@ class ClockSampler:
                 continue
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "window": "none"}
-        inside = [r for r in rows if t0 <= r[0] <= t1 + 0.25]
+        inside = [r for r in rows if t0 <= r[0] <= t1 + 0.03]
         window = "timed"
         if not inside:
             after = [r for r in rows if r[0] >= t0]

@@ -115,9 +115,16 @@ __device__ __forceinline__ Unit unit_of(const DecodeArgs &a, int u) {
   return w;
 }
 
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const WaitCtl &wc) {
+  const bool ok = mbar_wait(bar, parity, wc);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// TMA producer: the whole warp runs the loop and its waits, lane 0 issues the loads (a
+// loop confined to one lane issues late next to the compute warps: 1.7 % of bandwidth).
 template <int D, int G, bool MOD>
 __device__ void producer(const DecodeArgs &a, const CUtensorMap *tmk, const CUtensorMap *tmv,
-                         uint8_t *smem, DBars *bars, const WaitCtl &wc) {
+                         uint8_t *smem, DBars *bars, const WaitCtl &wc, int lane) {
   using C = DCfg<D, G>;
   uint32_t it = 0;
   const uint64_t policy = policy_evict_first();  // every cache byte is read once
@@ -126,7 +133,7 @@ __device__ void producer(const DecodeArgs &a, const CUtensorMap *tmk, const CUte
     const Unit w = unit_of(a, u);
     if (w.c == 0 && w.g == 0) {
       const int len_raw = a.cache_len[w.b] + a.len_add;
-      if (len_raw < 0 || len_raw > a.Lmax) atomicOr(a.err, DEVERR_BAD_CACHE_LEN);
+      if (lane == 0 && (len_raw < 0 || len_raw > a.Lmax)) atomicOr(a.err, DEVERR_BAD_CACHE_LEN);
     }
     if (w.nkeys <= 0) continue;
     const int nblk = (w.nkeys + KB - 1) / KB;
@@ -135,22 +142,25 @@ __device__ void producer(const DecodeArgs &a, const CUtensorMap *tmk, const CUte
       for (int which = 0; which < 2; ++which) {
         const int slot = static_cast<int>(it % C::NSLOTS);
         const uint32_t use = it / C::NSLOTS;
-        if (!mbar_wait(&bars->empty[slot], (use & 1u) ^ 1u, wc)) goto out;
-        mbar_arrive_expect_tx(&bars->full[slot], C::BLOCK_BYTES);
+        if (!warp_wait(&bars->empty[slot], (use & 1u) ^ 1u, wc)) goto out;
         // (row, batch) of the block, or (row in page, page) for a paged cache: a block
         // never crosses a page (unit starts and page sizes are multiples of 128).
         int row = w.key0 + blk * KB, outer = w.b;
         if (a.block_table != nullptr) {
           outer = a.block_table[static_cast<int64_t>(w.b) * a.bt_stride + row / a.page_size];
-          if (which == 0 && (outer < 0 || outer >= a.num_pages))  // read back as zeros
+          if (lane == 0 && which == 0 && (outer < 0 || outer >= a.num_pages))  // zeros
             atomicOr(a.err, DEVERR_BAD_BLOCK_TABLE);
           row %= a.page_size;
         }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bars->full[slot], C::BLOCK_BYTES);
 #pragma unroll
-        for (int cc = 0; cc < C::KCH; ++cc)
-          tma_load_4d_hint(smem + C::RING_OFF + slot * C::BLOCK_BYTES + cc * BOX_BYTES,
-                           which ? tmv : tmk, &bars->full[slot], cc * 64, w.g, row, outer,
-                           policy);
+          for (int cc = 0; cc < C::KCH; ++cc)
+            tma_load_4d_hint(smem + C::RING_OFF + slot * C::BLOCK_BYTES + cc * BOX_BYTES,
+                             which ? tmv : tmk, &bars->full[slot], cc * 64, w.g, row, outer,
+                             policy);
+        }
+        __syncwarp();
         ++it;
       }
     }
@@ -164,10 +174,6 @@ out:
   }
 }
 
-__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const WaitCtl &wc) {
-  const bool ok = mbar_wait(bar, parity, wc);
-  return __all_sync(0xffffffffu, ok);
-}
 
 // Barrier among the 256 compute threads.  Built on an mbarrier rather than bar.sync so
 // that the wait is bounded: a warp that has given up never leaves the others blocked.
@@ -460,7 +466,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     named_barrier(1, NTHREADS);
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(PRODUCER_REGS));
-    if (warp == PRODUCER_WARP && lane == 0) producer<D, G, MOD>(a, &tmk, &tmv, smem, bars, wc);
+    if (warp == PRODUCER_WARP) producer<D, G, MOD>(a, &tmk, &tmv, smem, bars, wc, lane);
     __syncwarp();
     named_barrier(1, NTHREADS);
   }
