@@ -445,3 +445,93 @@ def attention_varlen_bwd(q, k, v, dout, cu_seqlens_q, cu_seqlens_k, scale: float
                           window=window, softcap=softcap, alibi_slopes=sl)
         dq[a:e], dk[ka:ke], dv[ka:ke] = g[0][0], g[1][0], g[2][0]
     return dq, dk, dv
+
+
+# ---------------------------------------------------------------------------------------
+# FP8 inputs ("FlashAttention 1-4 详解", FlashAttention 3 engineering notes: FP8 tensor
+# cores in the forward pass).  The 8-bit code is E4M3 as torch.float8_e4m3fn stores it:
+# sign bit, 4 exponent bits with bias 7, 3 mantissa bits; exponent field 0 holds the
+# subnormals m/8 * 2^-6; S.1111.111 is NaN; there is no infinity (largest value 448).
+
+def e4m3_values() -> np.ndarray:
+    """The 256 E4M3 code points as float64 (NaN for the two NaN codes)."""
+    out = np.empty(256, dtype=np.float64)
+    for code in range(256):
+        sign = -1.0 if code & 0x80 else 1.0
+        e = (code >> 3) & 0xF
+        m = code & 0x7
+        if e == 0xF and m == 0x7:
+            out[code] = np.nan
+        elif e == 0:
+            out[code] = sign * (m / 8.0) * 2.0 ** (1 - 7)
+        else:
+            out[code] = sign * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+    return out
+
+
+def _u8(a) -> np.ndarray:
+    """Accept a numpy uint8 array or a torch float8_e4m3fn / uint8 tensor; return codes."""
+    if hasattr(a, "detach"):
+        import torch  # local: only the tests hand torch tensors in
+        t = a.detach().cpu().contiguous()
+        if t.dtype != torch.uint8:
+            t = t.view(torch.uint8)
+        a = t.numpy()
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint8:
+        raise TypeError("FP8 oracle inputs are E4M3 codes (uint8)")
+    return a
+
+
+def e4m3_to_bf16_bits(codes) -> np.ndarray:
+    """E4M3 codes -> bf16 bit patterns of the same values.  Exact: a finite E4M3 value has
+    at most 4 significant bits and an exponent in [-9, 8], both inside bf16."""
+    v = e4m3_values()[_u8(codes)].astype(np.float32)
+    bits = v.view(np.uint32)
+    finite = np.isfinite(v)
+    if np.any(bits[finite] & 0xFFFF):
+        raise ValueError("E4M3 value not exact in bf16")
+    return (bits >> 16).astype(np.uint16)
+
+
+def attention_fp8(q, k, v, scale: float, causal: bool = False, q_descale=None,
+                  k_descale=None, v_descale=None, nthreads: int | None = None,
+                  window=(-1, -1), softcap=0.0, alibi_slopes=None):
+    """Dense attention of E4M3 inputs q [B,Nq,Hq,d], k/v [B,Nk,Hkv,d] with descale factors
+    per (batch, kv head) ([B, Hkv] fp32, None = 1): the values attended are dq * Q, dk * K
+    and dv * V.  So the scores are (scale * dq * dk) q.k, the plain definition with that
+    score scale, and O is dv times the attention of the unscaled V (O is linear in V; the
+    LSE does not depend on V).  Returns (O [B,Nq,Hq,d], LSE [B,Hq,Nq]) in float64."""
+    qb, kb, vb = (e4m3_to_bf16_bits(t) for t in (q, k, v))
+    B, Nq, Hq, d = qb.shape
+    Hkv = kb.shape[2]
+    G = Hq // Hkv
+
+    def desc(x):
+        if x is None:
+            return np.ones((B, Hkv), dtype=np.float64)
+        if hasattr(x, "detach"):
+            x = x.detach().cpu().numpy()
+        return np.asarray(x, dtype=np.float32).astype(np.float64).reshape(B, Hkv)
+
+    dq, dk, dv = desc(q_descale), desc(k_descale), desc(v_descale)
+    slopes = None
+    if alibi_slopes is not None:
+        s = alibi_slopes.detach().cpu().numpy() if hasattr(alibi_slopes, "detach") \
+            else np.asarray(alibi_slopes)
+        slopes = np.broadcast_to(s.astype(np.float32), (B, Hq))
+    o_all = np.empty((B, Nq, Hq, d))
+    lse_all = np.empty((B, Hq, Nq))
+    for b in range(B):
+        for g in range(Hkv):
+            hs = slice(g * G, (g + 1) * G)
+            sigma = float(np.float32(scale)) * dq[b, g] * dk[b, g]
+            o, lse = attention(np.ascontiguousarray(qb[b:b + 1, :, hs]),
+                               np.ascontiguousarray(kb[b:b + 1, :, g:g + 1]),
+                               np.ascontiguousarray(vb[b:b + 1, :, g:g + 1]), sigma, causal,
+                               nthreads, elem=0, window=window, softcap=softcap,
+                               alibi_slopes=None if slopes is None else
+                               np.ascontiguousarray(slopes[b, hs]))
+            o_all[b, :, hs] = o[0] * dv[b, g]
+            lse_all[b, hs] = lse[0]
+    return o_all, lse_all

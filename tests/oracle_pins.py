@@ -920,10 +920,61 @@ def pin_bwd_modifiers(O):
         _close(dv, vv.grad.permute(0, 2, 1, 3).numpy(), 1e-11, f"modifier dV case {n}")
 
 
+def _e4m3_codes(shape, seed):
+    """Random E4M3 codes with exponent fields 0..8 (subnormals up to 3.75 in magnitude, so
+    that the scores stay small enough for an absolute 1e-12 comparison)."""
+    g = np.random.default_rng(seed)
+    sign = g.integers(0, 2, size=shape) << 7
+    exp = g.integers(0, 9, size=shape) << 3
+    man = g.integers(0, 8, size=shape)
+    return (sign | exp | man).astype(np.uint8)
+
+
+def pin_e4m3_decode(O):
+    """The E4M3 decoder against torch.float8_e4m3fn for all 256 codes, and the exact
+    re-encoding of every finite value as bf16."""
+    codes = torch.arange(256, dtype=torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = O.e4m3_values()
+    assert np.array_equal(np.isnan(got), np.isnan(ref)), "E4M3 NaN codes"
+    fin = ~np.isnan(ref)
+    assert np.array_equal(got[fin], ref[fin]), "E4M3 values differ from torch.float8_e4m3fn"
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9 and got[0x38] == 1.0
+    bits = O.e4m3_to_bf16_bits(np.arange(256, dtype=np.uint8)[fin])
+    back = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64)
+    assert np.array_equal(back.numpy(), ref[fin]), "bf16 re-encoding not exact"
+
+
+def pin_fp8_bruteforce(O):
+    """FP8 attention against the definition written out in torch float64 on values decoded
+    by torch: scores scale * (dq q).(dk k), bottom-right causal mask, softmax, P (dv V)."""
+    for n, (B, Nq, Nk, Hq, Hkv, d, causal) in enumerate(
+            [(2, 7, 9, 4, 2, 16, True), (1, 11, 5, 2, 1, 8, False), (2, 9, 9, 6, 3, 32, True)]):
+        q, k, v = (_e4m3_codes(s, 600 + 3 * n + i) for i, s in enumerate(
+            [(B, Nq, Hq, d), (B, Nk, Hkv, d), (B, Nk, Hkv, d)]))
+        g = np.random.default_rng(610 + n)
+        dq, dk, dv = (g.uniform(0.02, 0.5, size=(B, Hkv)).astype(np.float32) for _ in range(3))
+        scale = 0.3
+        o, lse = O.attention_fp8(q, k, v, scale, causal, dq, dk, dv)
+        val = lambda c: torch.from_numpy(c).view(torch.float8_e4m3fn).to(torch.float64)
+        G = Hq // Hkv
+        qq = val(q) * torch.from_numpy(dq.astype(np.float64)).repeat_interleave(G, 1)[:, None, :, None]
+        kk = (val(k) * torch.from_numpy(dk.astype(np.float64))[:, None, :, None]).repeat_interleave(G, 2)
+        vv = (val(v) * torch.from_numpy(dv.astype(np.float64))[:, None, :, None]).repeat_interleave(G, 2)
+        z = torch.einsum("bihc,bjhc->bhij", qq, kk) * float(np.float32(scale))
+        if causal:
+            z = z.masked_fill(~_bottom_right_mask(Nq, Nk), float("-inf"))
+        ref_lse = torch.logsumexp(z, dim=-1)
+        ref_o = torch.einsum("bhij,bjhc->bihc", torch.softmax(z, dim=-1).nan_to_num(0.0), vv)
+        _close(o, ref_o.numpy(), 1e-12, f"fp8 case {n} O")
+        fin = torch.isfinite(ref_lse).numpy()
+        _close(lse[fin], ref_lse.numpy()[fin], 1e-12, f"fp8 case {n} LSE")
+
+
 ALL_PINS = [pin_library, pin_library_fp16, pin_fp16_values, pin_uniform_scores, pin_single_key, pin_constant_v, pin_two_keys,
             pin_empty_rows, pin_hard_max, pin_probs, pin_shift, pin_permutation, pin_gqa,
             pin_varlen, pin_kvcache, pin_rows, pin_recurrence, pin_lse_recompute,
             pin_window_uniform, pin_window_diagonal, pin_window_library, pin_softcap_limits,
             pin_alibi_geometric, pin_alibi_library, pin_mod_bruteforce, pin_mod_paths,
             pin_round16_library, pin_rotary, pin_kv_append, pin_kv_paged, pin_bwd_library,
-            pin_bwd_closed_forms, pin_bwd_modifiers]
+            pin_bwd_closed_forms, pin_bwd_modifiers, pin_e4m3_decode, pin_fp8_bruteforce]

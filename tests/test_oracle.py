@@ -103,6 +103,16 @@ MUTATIONS = [
     ("query not rotated", "qb = rotary(qb, np.repeat(lens, Hq)",
      "qb = qb if True else rotary(qb, np.repeat(lens, Hq)", "py"),
     ("paged row taken from the page number", "return pg, r % page", "return pg, r // page", "py"),
+    ("E4M3 exponent bias off by one", "out[code] = sign * (1.0 + m / 8.0) * 2.0 ** (e - 7)",
+     "out[code] = sign * (1.0 + m / 8.0) * 2.0 ** (e - 8)", "py"),
+    ("E4M3 subnormals scaled as normals", "out[code] = sign * (m / 8.0) * 2.0 ** (1 - 7)",
+     "out[code] = sign * (1.0 + m / 8.0) * 2.0 ** (0 - 7)", "py"),
+    ("FP8 K descale ignored", "sigma = float(np.float32(scale)) * dq[b, g] * dk[b, g]",
+     "sigma = float(np.float32(scale)) * dq[b, g]", "py"),
+    ("FP8 V descale on the wrong head group", "o_all[b, :, hs] = o[0] * dv[b, g]",
+     "o_all[b, :, hs] = o[0] * dv[b, 0]", "py"),
+    ("FP8 query heads of the wrong group", "hs = slice(g * G, (g + 1) * G)",
+     "hs = slice(g, g + G)", "py"),
 ]
 
 
