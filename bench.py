@@ -565,6 +565,23 @@ def extra_workloads(args, dev, pk, world, dist):
         res[name] = {"ms": round(ms, 4), "TFLOPS": round(tf, 2),
                      "frac_of_bf16_peak": round(tf / pk["bf16"], 4)}
         del q, k, v, o, l
+    # FP8 (E4M3) inputs on the headline shape; peak: the measured bf16 peak times the
+    # nominal fp8 / bf16 ratio of the part (4.5 / 2.25 PFLOP/s dense)
+    from exact_attention_81_gb300.inputs import fp8_inputs
+    q8, k8, v8, dq8, dk8, dv8 = fp8_inputs(w.B, w.Nq, w.Nk, w.Hq, w.Hkv, w.d, w.seed, device=dev)
+    o = torch.empty(q8.shape, dtype=torch.bfloat16, device=dev)
+    l = torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device=dev)
+    ws8 = torch.empty(fa.fa_fwd_fp8_workspace_size(w.B, w.Nk, w.Hkv, w.d), dtype=torch.uint8,
+                      device=dev)
+    ms = time_calls(lambda: fa.fa_fwd_fp8(q8, k8, v8, causal=True, q_descale=dq8, k_descale=dk8,
+                                          v_descale=dv8, out=o, lse=l, workspace=ws8),
+                    max(10, args.steps // 4), stream)
+    tf = flops(w) / (ms * 1e-3) / 1e12
+    res["causal8k_fp8"] = {"ms": round(ms, 4), "TFLOPS": round(tf, 2),
+                           "frac_of_fp8_peak": round(tf / (2.0 * pk["bf16"]), 4),
+                           "peak_basis": "2 x measured bf16 (nominal fp8 / bf16 ratio)",
+                           "gpu_launches_per_call": 2}
+    del q8, k8, v8, o, l, ws8
     # backward pass of the headline workload (FLOPs: five matmuls, 2.5 x the forward)
     w = WORKLOADS["causal8k"]
     q, k, v = workload_inputs(w, device=dev)

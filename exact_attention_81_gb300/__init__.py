@@ -10,6 +10,7 @@ and ``fa_bwd`` (gradients of ``fa_fwd``), plus the upstream-style names
 """
 from ._binding import (  # noqa: F401
     FA_BF16,
+    FA_E4M3,
     FA_FP16,
     FA_ERR_CUDA,
     FA_ERR_INVALID_ARG,
@@ -22,6 +23,8 @@ from ._binding import (  # noqa: F401
     fa_bwd_varlen,
     fa_bwd_workspace_size,
     fa_fwd,
+    fa_fwd_fp8,
+    fa_fwd_fp8_workspace_size,
     fa_fwd_kvcache,
     fa_fwd_kvcache_workspace_size,
     fa_fwd_varlen,

@@ -27,6 +27,7 @@ FA_ERR_TIMEOUT = 5
 
 FA_BF16 = 0
 FA_FP16 = 1
+FA_E4M3 = 2
 _DTYPE = {torch.bfloat16: FA_BF16, torch.float16: FA_FP16}
 
 
@@ -158,6 +159,10 @@ def load_library(path: str | None = None):
         lib.fa_set_wait_timeout_ns.restype = None
         lib.fa_set_fault_injection.argtypes = [ctypes.c_int]
         lib.fa_set_fault_injection.restype = None
+        lib.fa_fwd_fp8_workspace_size.argtypes = [i, i, i, i]
+        lib.fa_fwd_fp8_workspace_size.restype = sz
+        lib.fa_fwd_fp8.argtypes = [ctypes.POINTER(FwdParams), vp, vp, vp, vp, sz, vp]
+        lib.fa_fwd_fp8.restype = i
         lib.fa_fwd_params_size.argtypes = []
         lib.fa_fwd_params_size.restype = sz
         lib.fa_bwd.argtypes = [ctypes.POINTER(BwdParams), vp]
@@ -275,6 +280,63 @@ def fa_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, 
     p.dtype = _DTYPE[q.dtype]
     p.mod = _score_mod(B, Hq, q.device, window_size, softcap, alibi_slopes)
     _check(load_library().fa_fwd(ctypes.byref(p), _stream_handle(stream)), "fa_fwd")
+    return out, lse
+
+
+def fa_fwd_fp8_workspace_size(B: int, Nk: int, Hkv: int, d: int) -> int:
+    return int(load_library().fa_fwd_fp8_workspace_size(B, Nk, Hkv, d))
+
+
+def fa_fwd_fp8(q, k, v, causal: bool = False, scale: float | None = None, q_descale=None,
+               k_descale=None, v_descale=None, out=None, lse=None, workspace=None, stream=None,
+               window_size=None, softcap: float = 0.0, alibi_slopes=None):
+    """FP8 dense attention.  q [B,Nq,Hq,d], k/v [B,Nk,Hkv,d] torch.float8_e4m3fn (CUDA),
+    d a multiple of 16 up to 128; q/k/v_descale fp32 [B, Hkv] CUDA tensors or None (= 1).
+    Returns (out [B,Nq,Hq,d] bf16, lse [B,Hq,Nq] fp32)."""
+    f8 = torch.float8_e4m3fn
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != f8 or not t.is_cuda or t.dim() != 4:
+            raise TypeError(f"{name} must be a 4-D torch.float8_e4m3fn CUDA tensor")
+        if t.stride(3) != 1:
+            raise ValueError(f"{name} must have a unit-stride head dimension")
+    B, Nq, Hq, d = q.shape
+    Nk, Hkv = k.shape[1], k.shape[2]
+    if tuple(k.shape) != (B, Nk, Hkv, d) or tuple(v.shape) != (B, Nk, Hkv, d):
+        raise ValueError("k and v must be [B, Nk, Hkv, d] matching q")
+    keep = []
+    ptrs = []
+    for name, t in (("q_descale", q_descale), ("k_descale", k_descale), ("v_descale", v_descale)):
+        if t is None:
+            ptrs.append(None)
+            continue
+        if t.dtype != torch.float32 or not t.is_cuda or t.numel() != B * Hkv:
+            raise TypeError(f"{name} must be an fp32 CUDA tensor of B * Hkv elements")
+        t = t.contiguous()
+        keep.append(t)
+        ptrs.append(_ptr(t))
+    if out is None:
+        out = torch.empty((B, Nq, Hq, d), dtype=torch.bfloat16, device=q.device)
+    elif out.dtype != torch.bfloat16 or tuple(out.shape) != (B, Nq, Hq, d) or out.stride(3) != 1:
+        raise ValueError("out must be a bf16 [B, Nq, Hq, d] tensor with unit-stride d")
+    if lse is None:
+        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
+    elif lse.dtype != torch.float32 or tuple(lse.shape) != (B, Hq, Nq) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [B, Hq, Nq] tensor")
+    need = fa_fwd_fp8_workspace_size(B, Nk, Hkv, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    p = FwdParams()
+    p.q, p.k, p.v, p.o, p.lse = _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse)
+    p.B, p.Nq, p.Nk, p.Hq, p.Hkv, p.d = B, Nq, Nk, Hq, Hkv, d
+    for name, t in (("q_strides", q), ("k_strides", k), ("v_strides", v), ("o_strides", out)):
+        getattr(p, name)[:] = list(t.stride()[:3])
+    p.scale = default_scale(d) if scale is None else float(scale)
+    p.causal = int(bool(causal))
+    p.dtype = FA_E4M3
+    p.mod = _score_mod(B, Hq, q.device, window_size, softcap, alibi_slopes)
+    st = load_library().fa_fwd_fp8(ctypes.byref(p), *ptrs, _ptr(workspace), workspace.numel(),
+                                   _stream_handle(stream))
+    _check(st, "fa_fwd_fp8")
     return out, lse
 
 

@@ -101,18 +101,21 @@ fa_status make_map(CUtensorMap *map, const void *base, int d, int64_t n, int64_t
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(h),
                         static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(b)};
   // The stride of a dimension of extent 1 is never used; give it a legal value.
-  const int64_t bh = h > 1 ? sh * 2 : static_cast<int64_t>(d) * 2;
-  const int64_t bn = n > 1 ? sn * 2 : bh * h;
-  const int64_t bb = b > 1 ? sb * 2 : bn * n;
+  const int64_t es = dtype == FA_E4M3 ? 1 : 2;  // bytes per element
+  const int64_t bh = h > 1 ? sh * es : static_cast<int64_t>(d) * es;
+  const int64_t bn = n > 1 ? sn * es : bh * h;
+  const int64_t bb = b > 1 ? sb * es : bn * n;
   cuuint64_t strides[3] = {static_cast<cuuint64_t>(bh), static_cast<cuuint64_t>(bn),
                            static_cast<cuuint64_t>(bb)};
   for (int i = 0; i < 3; ++i)
     if (strides[i] == 0 || (strides[i] % 16) != 0 || strides[i] >= (cuuint64_t(1) << 40))
       return FA_ERR_INVALID_ARG;
-  cuuint32_t box[4] = {64, 1, 128, 1};
+  // 128-byte box rows: 64 16-bit or 128 8-bit elements
+  cuuint32_t box[4] = {dtype == FA_E4M3 ? 128u : 64u, 1, 128, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUtensorMapDataType ty =
-      dtype == FA_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+      dtype == FA_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+      : (dtype == FA_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
   CUresult r = g_encode(map, ty, 4, const_cast<void *>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -128,6 +131,27 @@ fa_status make_map(CUtensorMap *map, const void *base, int d, int64_t n, int64_t
 // 4-D fp32 tensor map over a contiguous (batch, seq, head, d) accumulator, box
 // {32, 1, 128, 1} (32 floats = 128 bytes x 128 rows), 128-byte swizzle: the target of the
 // backward pass's dQ reductions.
+// 4-D 8-bit map over the transposed V [B, Hkv, d, nk_pad] written by launch_transpose_v:
+// dims {keys, d, kv head, batch}, box {128 keys, 128 rows of d} (rows past d read as 0).
+fa_status make_map_vt(CUtensorMap *map, void *base, int nk_pad, int d, int Hkv, int B) {
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(nk_pad), static_cast<cuuint64_t>(d),
+                        static_cast<cuuint64_t>(Hkv), static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(nk_pad),
+                           static_cast<cuuint64_t>(nk_pad) * d,
+                           static_cast<cuuint64_t>(nk_pad) * d * Hkv};
+  cuuint32_t box[4] = {128, 128, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, base, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(g_cuda_msg, sizeof g_cuda_msg, "cuTensorMapEncodeTiled failed (CUresult %d)",
+             static_cast<int>(r));
+    return FA_ERR_CUDA;
+  }
+  return FA_OK;
+}
+
 fa_status make_map_f32(CUtensorMap *map, void *base, int d, int64_t n, int64_t h, int64_t b) {
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(h),
                         static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(b)};
@@ -271,6 +295,45 @@ void fa_set_wait_timeout_ns(unsigned long long ns) {
 
 void fa_set_fault_injection(int withhold_loads) { g_inject = withhold_loads != 0; }
 
+// Keys padded to a multiple of 16 (the byte stride of a transposed V row).
+int64_t nk_pad16(int64_t nk) { return (nk + 15) / 16 * 16; }
+
+// Byte strides of 8-bit tensors: multiples of 16 (tensor-map rule).
+bool stride_ok_16b(int64_t s, int64_t extent) {
+  if (extent <= 1) return s >= 0;
+  return s > 0 && (s % 16) == 0 && s < (int64_t(1) << 38);
+}
+
+// Prefill arguments of a dense call (fa_fwd, fa_fwd_fp8).
+fa::PrefillArgs dense_args(const fa_fwd_params &a, int mblocks, int64_t tiles,
+                           const DeviceInfo *dev, const ModPlan &mod) {
+  fa::PrefillArgs pa{};
+  pa.o = a.o;
+  pa.lse = a.lse;
+  pa.o_sb = a.o_strides[0];
+  pa.o_sn = a.o_strides[1];
+  pa.o_sh = a.o_strides[2];
+  pa.lse_sb = static_cast<int64_t>(a.Hq) * a.Nq;
+  pa.lse_sh = a.Nq;
+  pa.B = a.B;
+  pa.Hq = a.Hq;
+  pa.Hkv = a.Hkv;
+  pa.group = a.Hq / a.Hkv;
+  pa.Nq = a.Nq;
+  pa.Nk = a.Nk;
+  pa.varlen = 0;
+  pa.mblocks = mblocks;
+  pa.num_tiles = static_cast<int>(tiles);
+  pa.scale_log2 = scale_log2(a.scale);
+  pa.err = dev->err;
+  pa.timeout_ns = g_timeout_ns;
+  pa.inject = g_inject;
+  pa.sched_slot = fa::next_prefill_sched_slot();
+  pa.d = a.d;
+  apply_mod(mod, a.scale, &pa);
+  return pa;
+}
+
 fa_status fa_fwd(const fa_fwd_params *p, cudaStream_t stream) {
   if (p == nullptr) return FA_ERR_INVALID_ARG;
   const fa_fwd_params &a = *p;
@@ -321,34 +384,85 @@ fa_status fa_fwd(const fa_fwd_params *p, cudaStream_t stream) {
   if ((st = make_map(&tv, a.v, a.d, a.Nk, a.Hkv, a.B, a.v_strides[1], a.v_strides[2],
                      a.v_strides[0], a.dtype)) != FA_OK)
     return st;
-  fa::PrefillArgs pa{};
-  pa.o = a.o;
-  pa.lse = a.lse;
-  pa.o_sb = a.o_strides[0];
-  pa.o_sn = a.o_strides[1];
-  pa.o_sh = a.o_strides[2];
-  pa.lse_sb = lse_sb;
-  pa.lse_sh = lse_sh;
-  pa.B = a.B;
-  pa.Hq = a.Hq;
-  pa.Hkv = a.Hkv;
-  pa.group = a.Hq / a.Hkv;
-  pa.Nq = a.Nq;
-  pa.Nk = a.Nk;
-  pa.varlen = 0;
-  pa.mblocks = mblocks;
-  pa.num_tiles = static_cast<int>(tiles);
-  pa.scale_log2 = scale_log2(a.scale);
-  pa.err = dev->err;
-  pa.timeout_ns = g_timeout_ns;
-  pa.inject = g_inject;
-  pa.sched_slot = fa::next_prefill_sched_slot();
-  pa.d = a.d;
-  apply_mod(mod, a.scale, &pa);
+  const fa::PrefillArgs pa = dense_args(a, mblocks, tiles, dev, mod);
   const int grid = static_cast<int>(tiles < dev->sm_count ? tiles : dev->sm_count);
   cudaError_t e =
       fa::launch_prefill(fa::kernel_d(a.d), mod.mask, a.dtype == FA_FP16, tq, tk, tv, pa, grid,
                          stream);
+  return e == cudaSuccess ? FA_OK : cuda_fail("prefill kernel launch", e);
+}
+
+size_t fa_fwd_fp8_workspace_size(int B, int Nk, int Hkv, int d) {
+  if (B <= 0 || Nk <= 0 || Hkv <= 0 || d <= 0) return 0;
+  const int64_t bytes = static_cast<int64_t>(B) * Hkv * d * nk_pad16(Nk);
+  return static_cast<size_t>((bytes + 255) / 256 * 256);
+}
+
+fa_status fa_fwd_fp8(const fa_fwd_params *p, const float *q_descale, const float *k_descale,
+                     const float *v_descale, void *workspace, size_t workspace_bytes,
+                     cudaStream_t stream) {
+  if (p == nullptr) return FA_ERR_INVALID_ARG;
+  const fa_fwd_params &a = *p;
+  if (a.B < 0 || a.Nq < 0 || a.Nk < 0 || a.Hq <= 0 || a.Hkv <= 0 || a.Hq % a.Hkv != 0)
+    return FA_ERR_INVALID_ARG;
+  if (a.dtype != FA_E4M3) return FA_ERR_UNSUPPORTED;
+  if (a.d < 16 || a.d > 128 || a.d % 16 != 0) return FA_ERR_UNSUPPORTED;
+  if (!scale_ok(a.scale)) return FA_ERR_INVALID_ARG;
+  if (a.Nq > (1 << 30) || a.Nk > (1 << 30)) return FA_ERR_INVALID_ARG;
+  if (a.B == 0 || a.Nq == 0) return FA_OK;
+  if (a.q == nullptr || a.o == nullptr || a.lse == nullptr) return FA_ERR_INVALID_ARG;
+  if (!aligned(a.q, 16) || !aligned(a.o, 16) || !aligned(a.lse, 4)) return FA_ERR_INVALID_ARG;
+  for (const float *ds : {q_descale, k_descale, v_descale})
+    if (ds != nullptr && !aligned(ds, 4)) return FA_ERR_INVALID_ARG;
+  if (!stride_ok_16b(a.q_strides[0], a.B) || !stride_ok_16b(a.q_strides[1], a.Nq) ||
+      !stride_ok_16b(a.q_strides[2], a.Hq) || !stride_ok(a.o_strides[0], a.B) ||
+      !stride_ok(a.o_strides[1], a.Nq) || !stride_ok(a.o_strides[2], a.Hq))
+    return FA_ERR_INVALID_ARG;
+  if (a.Nk > 0) {
+    if (a.k == nullptr || a.v == nullptr) return FA_ERR_INVALID_ARG;
+    if (!aligned(a.k, 16) || !aligned(a.v, 16)) return FA_ERR_INVALID_ARG;
+    if (!stride_ok_16b(a.k_strides[0], a.B) || !stride_ok_16b(a.k_strides[1], a.Nk) ||
+        !stride_ok_16b(a.k_strides[2], a.Hkv) || !stride_ok_16b(a.v_strides[0], a.B) ||
+        !stride_ok_16b(a.v_strides[1], a.Nk) || !stride_ok_16b(a.v_strides[2], a.Hkv))
+      return FA_ERR_INVALID_ARG;
+    const size_t need = fa_fwd_fp8_workspace_size(a.B, a.Nk, a.Hkv, a.d);
+    if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256))
+      return FA_ERR_WORKSPACE;
+  }
+  const int mblocks = ceil_div(a.Nq, fa::prefill_tile_rows(128));
+  const int64_t tiles = static_cast<int64_t>(a.B) * a.Hq * mblocks;
+  if (tiles > INT32_MAX) return FA_ERR_INVALID_ARG;
+  ModPlan mod;
+  fa_status st = plan_mod(&a.mod, a.causal, &mod);
+  if (st != FA_OK) return st;
+
+  DeviceInfo *dev = nullptr;
+  st = current_device(&dev);
+  if (st != FA_OK) return st;
+  if (a.Nk == 0) {
+    cudaError_t e = fa::launch_fill_empty(a.o, a.lse, a.B, a.Nq, a.Hq, a.d, a.o_strides[0],
+                                          a.o_strides[1], a.o_strides[2],
+                                          static_cast<int64_t>(a.Hq) * a.Nq, a.Nq, stream);
+    return e == cudaSuccess ? FA_OK : cuda_fail("fill kernel launch", e);
+  }
+  const int nk_pad = static_cast<int>(nk_pad16(a.Nk));
+  CUtensorMap tq, tk, tvt;
+  if ((st = make_map(&tq, a.q, a.d, a.Nq, a.Hq, a.B, a.q_strides[1], a.q_strides[2],
+                     a.q_strides[0], FA_E4M3)) != FA_OK)
+    return st;
+  if ((st = make_map(&tk, a.k, a.d, a.Nk, a.Hkv, a.B, a.k_strides[1], a.k_strides[2],
+                     a.k_strides[0], FA_E4M3)) != FA_OK)
+    return st;
+  if ((st = make_map_vt(&tvt, workspace, nk_pad, a.d, a.Hkv, a.B)) != FA_OK) return st;
+  cudaError_t e = fa::launch_transpose_v(a.v, a.v_strides[0], a.v_strides[1], a.v_strides[2],
+                                         workspace, a.B, a.Nk, a.Hkv, a.d, nk_pad, stream);
+  if (e != cudaSuccess) return cuda_fail("V transpose launch", e);
+  fa::PrefillArgs pa = dense_args(a, mblocks, tiles, dev, mod);
+  pa.q_descale = q_descale;
+  pa.k_descale = k_descale;
+  pa.v_descale = v_descale;
+  const int grid = static_cast<int>(tiles < dev->sm_count ? tiles : dev->sm_count);
+  e = fa::launch_prefill_fp8(mod.mask, tq, tk, tvt, pa, grid, stream);
   return e == cudaSuccess ? FA_OK : cuda_fail("prefill kernel launch", e);
 }
 

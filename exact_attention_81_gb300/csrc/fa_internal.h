@@ -46,6 +46,8 @@ struct PrefillArgs {
   const float *alibi;         // slopes of (b, h) at alibi[b * alibi_sb + h], or null
   int64_t alibi_sb;
   int desc;                   // hand out query blocks last-first (right-bounded windows)
+  // FP8 launches: descale factors per (batch, kv head) at [b * Hkv + hk], or null (= 1).
+  const float *q_descale, *k_descale, *v_descale;
 };
 
 // Masking mode of a prefill launch.
@@ -62,6 +64,17 @@ int next_prefill_sched_slot();
 cudaError_t launch_prefill(int d, int mask, bool f16, const CUtensorMap &tq,
                            const CUtensorMap &tk, const CUtensorMap &tv, const PrefillArgs &a,
                            int grid, cudaStream_t stream);
+
+// FP8 (E4M3) prefill, d <= 128 at kernel width 128: tq, tk over E4M3 Q and K, tvt over the
+// transposed V written by launch_transpose_v (dims {keys, d, kv head, batch}).
+cudaError_t launch_prefill_fp8(int mask, const CUtensorMap &tq, const CUtensorMap &tk,
+                               const CUtensorMap &tvt, const PrefillArgs &a, int grid,
+                               cudaStream_t stream);
+
+// V [B, Nk, Hkv, d] E4M3 (byte strides v_sb, v_sn, v_sh) -> V^T [B, Hkv, d, nk_pad], keys
+// contiguous, zeros in the columns [Nk, nk_pad).
+cudaError_t launch_transpose_v(const void *v, int64_t v_sb, int64_t v_sn, int64_t v_sh, void *vt,
+                               int B, int Nk, int Hkv, int d, int nk_pad, cudaStream_t stream);
 
 // O = 0 and LSE = -inf for every row (no visible keys anywhere).
 cudaError_t launch_fill_empty(void *o, float *lse, int B, int N, int H, int d, int64_t o_sb,

@@ -71,21 +71,30 @@ __host__ __device__ constexpr uint32_t o_col(int t) {
 // D <= 128: two query sub-tiles per work tile, ring slots of one [128 x D] K or V tile.
 // D = 256 ("wide"): one sub-tile with S double-buffered in TMEM (S_0, S_1, O = 512
 // columns), ring slots of half a tile (the d halves), PV as two N = 128 products.
-template <int D, bool F16 = false>
+// F8 (E4M3 inputs, D = 128): one 128-byte box per row; V arrives transposed ([d, keys],
+// K-major like K), P goes through shared memory as E4M3 (both PV operands K-major).
+template <int D, bool F16 = false, bool F8 = false>
 struct Cfg {
   static constexpr bool WIDE = D > 128;
   static constexpr int NSUB = WIDE ? 1 : 2;              // query sub-tiles per work tile
-  static constexpr int KCH = D / 64;                     // 64-wide boxes per row
-  static constexpr int TILE_BYTES = KCH * BOX_BYTES;     // one [128 x D] bf16 tile
+  static constexpr int EB = F8 ? 1 : 2;                  // bytes per element
+  static constexpr int KCH = D * EB / 128;               // 128-byte boxes per row
+  static constexpr int BOX_ELEMS = 128 / EB;             // elements of a row per box
+  static constexpr int TILE_BYTES = KCH * BOX_BYTES;     // one [128 x D] tile
   static constexpr int SLOT_BYTES = WIDE ? TILE_BYTES / 2 : TILE_BYTES;
-  static constexpr int NSLOTS = WIDE ? 5 : (D == 128 ? 4 : 8);  // K/V ring depth
+  static constexpr int NSLOTS = WIDE ? 5 : (F8 ? 8 : (D == 128 ? 4 : 8));  // K/V ring depth
   static constexpr int Q_OFF = 0;
   static constexpr int RING_OFF = NSUB * TILE_BYTES;
-  static constexpr int BAR_OFF = RING_OFF + NSLOTS * SLOT_BYTES;
+  static constexpr int P_OFF = RING_OFF + NSLOTS * SLOT_BYTES;  // F8: E4M3 P per sub-tile
+  static constexpr int P_BYTES = F8 ? NSUB * BR * BC : 0;
+  static constexpr int BAR_OFF = P_OFF + P_BYTES;
   static constexpr int SMEM_BYTES = BAR_OFF + 512 + 1024;  // barriers + alignment slack
-  static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BC, false, false, F16);
-  static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, WIDE ? 128 : D, false, true, F16);
+  static constexpr uint32_t IDESC_S =
+      F8 ? idesc_e4m3_f32(128, BC) : idesc_bf16_f32(128, BC, false, false, F16);
+  static constexpr uint32_t IDESC_PV =
+      F8 ? idesc_e4m3_f32(128, D) : idesc_bf16_f32(128, WIDE ? 128 : D, false, true, F16);
 };
+static_assert(Cfg<128, false, true>::SMEM_BYTES <= 227 * 1024, "fp8 prefill exceeds smem");
 static_assert(Cfg<256>::SMEM_BYTES <= 227 * 1024, "wide prefill exceeds shared memory");
 
 // Per-launch tile-ticket counters: [slot][0] = next ticket, [slot][1] = CTAs finished.
@@ -196,8 +205,19 @@ __device__ __forceinline__ bool varlen_bad(const PrefillArgs &a, int b) {
 // Both issue helpers are warp-collective (the whole MMA warp runs them, one lane issues).
 // S_t = Q_t K^T: D/16 MMAs of 128 x 128 x 16.  Both operands K-major, 128B-swizzled:
 // k-step kk lives in box kk/4 at byte offset 32*(kk%4) inside each 128-byte row.
-template <int D, bool F16>
+template <int D, bool F16, bool F8 = false>
 __device__ __forceinline__ void issue_s(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+  if constexpr (F8) {
+    // E4M3: K = 32 per MMA, so D / 32 MMAs, 32 bytes of each 128-byte row apiece.
+#pragma unroll
+    for (int kk = 0; kk < D / 32; ++kk) {
+      const uint32_t off = static_cast<uint32_t>((kk >> 2) * BOX_BYTES + (kk & 3) * 32);
+      mma_f8_ss_w(d_tmem, sw128_desc(q_smem + off, 16, 1024),
+                  sw128_desc(k_smem + off, 16, 1024), Cfg<D, F16, true>::IDESC_S,
+                  kk > 0 ? 1u : 0u);
+    }
+    return;
+  }
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint32_t off = static_cast<uint32_t>((kk >> 2) * BOX_BYTES + (kk & 3) * 32);
@@ -219,16 +239,29 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint3
   }
 }
 
+// FP8: O_t (+)= P_t V with P_t [128 queries x 128 keys] E4M3 in shared memory and V^T
+// [D x 128 keys] E4M3 from the ring, both K-major; 4 MMAs of 128 x D x 32.
+template <int D>
+__device__ __forceinline__ void issue_pv_f8(uint32_t o_tmem, uint32_t p_smem, uint32_t vt_smem,
+                                            bool accumulate) {
+#pragma unroll
+  for (int kk = 0; kk < BC / 32; ++kk) {
+    const uint32_t off = static_cast<uint32_t>(kk * 32);
+    mma_f8_ss_w(o_tmem, sw128_desc(p_smem + off, 16, 1024), sw128_desc(vt_smem + off, 16, 1024),
+                Cfg<D, false, true>::IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
 // ------------------------------------------------------------------------------------
 // Scheduler + producer (one lane).  Takes tickets from the launch's counter, publishes each
 // tile to the scheduler ring, then issues its Q tile and its K/V ring loads (ring order
 // K_0, V_0, K_1, V_1, ...).  A ticket past the last tile is published as -1 (end).
 
-template <int D, int MASK>
+template <int D, int MASK, bool F8 = false>
 __device__ void producer_role(const PrefillArgs &a, const CUtensorMap *tmq,
                               const CUtensorMap *tmk, const CUtensorMap *tmv, uint8_t *smem,
                               Bars *bars, const WaitCtl &wc) {
-  using C = Cfg<D>;
+  using C = Cfg<D, false, F8>;
   uint32_t kv_iter = 0, q_iter = 0;
   unsigned int *ctr = g_sched[a.sched_slot];
   // One ring slot: `boxes` 64-column boxes of rows [row0, row0 + 128) from map m, the first
@@ -240,7 +273,18 @@ __device__ void producer_role(const PrefillArgs &a, const CUtensorMap *tmq,
     mbar_arrive_expect_tx(&bars->kv_full[slot], C::SLOT_BYTES);
     for (int c = 0; c < boxes; ++c)
       tma_load_4d(smem + C::RING_OFF + slot * C::SLOT_BYTES + c * BOX_BYTES, m,
-                  &bars->kv_full[slot], (c0 + c) * 64, hk, row0, b);
+                  &bars->kv_full[slot], (c0 + c) * C::BOX_ELEMS, hk, row0, b);
+    ++kv_iter;
+    return true;
+  };
+  // FP8: one [D rows x 128 keys] tile of V^T, map dims {keys, d, kv head, batch}.
+  auto load_vt = [&](int hk, int key0, int b) {
+    const int slot = static_cast<int>(kv_iter % C::NSLOTS);
+    const uint32_t use = kv_iter / C::NSLOTS;
+    if (!mbar_wait(&bars->kv_empty[slot], (use & 1u) ^ 1u, wc)) return false;
+    mbar_arrive_expect_tx(&bars->kv_full[slot], C::SLOT_BYTES);
+    tma_load_4d(smem + C::RING_OFF + slot * C::SLOT_BYTES, tmv, &bars->kv_full[slot], key0, 0,
+                hk, b);
     ++kv_iter;
     return true;
   };
@@ -266,7 +310,7 @@ __device__ void producer_role(const PrefillArgs &a, const CUtensorMap *tmq,
 #pragma unroll
       for (int c = 0; c < C::KCH; ++c)
         tma_load_4d(smem + C::Q_OFF + t * C::TILE_BYTES + c * BOX_BYTES, tmq, &bars->q_full,
-                    c * 64, ti.h, ti.q_tok + ti.q_row0 + t * BR, ti.tma_b);
+                    c * C::BOX_ELEMS, ti.h, ti.q_tok + ti.q_row0 + t * BR, ti.tma_b);
     ++q_iter;
     const int krow = ti.k_tok + ti.kv0 * BC;
     if constexpr (C::WIDE) {
@@ -282,6 +326,12 @@ __device__ void producer_role(const PrefillArgs &a, const CUtensorMap *tmq,
       ok = ok && load_slot(tmv, 0, 2, ti.hk, krow + (n - 1) * BC, ti.tma_b) &&
            load_slot(tmv, 2, 2, ti.hk, krow + (n - 1) * BC, ti.tma_b);
       if (!ok) goto out;
+    } else if constexpr (F8) {
+      // V^T rows start at the sequence's first key (dense only: k_tok = 0).
+      for (int j = 0; j < n; ++j)
+        if (!load_slot(tmk, 0, C::KCH, ti.hk, krow + j * BC, ti.tma_b) ||
+            !load_vt(ti.hk, krow + j * BC, ti.tma_b))
+          goto out;
     } else {
       for (int j = 0; j < n; ++j)
         if (!load_slot(tmk, 0, C::KCH, ti.hk, krow + j * BC, ti.tma_b) ||
@@ -346,10 +396,11 @@ __device__ __forceinline__ bool next_tile(Bars *bars, uint32_t k, int &tile, con
 // TMEM columns that PV_t(j) reads P_t(j) from.  Sub-tile t takes part only in the steps
 // [js[t], je[t]) of the block's K/V stream.
 
-template <int D, int MASK, bool F16>
+template <int D, int MASK, bool F16, bool F8 = false>
 __device__ void mma_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, uint32_t tmem,
                          const WaitCtl &wc, int lane) {
-  using C = Cfg<D>;
+  using C = Cfg<D, F16, F8>;
+  const uint32_t p_smem[2] = {smem_u32(smem + C::P_OFF), smem_u32(smem + C::P_OFF + BR * BC)};
   uint32_t kv_iter = 0, q_iter = 0;
   uint32_t p_phase[2] = {0u, 0u}, oe_phase[2] = {0u, 0u};
   bool o_pending[2] = {false, false};
@@ -372,7 +423,7 @@ __device__ void mma_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, uint32
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         if (ti.js[t] == 0 && ti.je[t] > 0) {
-          issue_s<D, F16>(tmem + s_col(t), q_smem[t], ring + slot_k * C::TILE_BYTES);
+          issue_s<D, F16, F8>(tmem + s_col(t), q_smem[t], ring + slot_k * C::TILE_BYTES);
           mma_commit_w(&bars->s_full[t]);
         }
       }
@@ -400,8 +451,12 @@ __device__ void mma_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, uint32
             if (!warp_wait(&bars->p_ready[t], p_phase[t], wc)) goto out;
             p_phase[t] ^= 1u;
             tc_fence_after();
-            issue_pv<D, F16>(tmem + o_col(t), tmem + s_col(t), ring + slot_v * C::TILE_BYTES,
+            if constexpr (F8)
+              issue_pv_f8<D>(tmem + o_col(t), p_smem[t], ring + slot_v * C::TILE_BYTES,
                              j > ti.js[t]);
+            else
+              issue_pv<D, F16>(tmem + o_col(t), tmem + s_col(t), ring + slot_v * C::TILE_BYTES,
+                               j > ti.js[t]);
             if (j == ti.je[t] - 1) {
               mma_commit_w(&bars->o_full[t]);
               o_pending[t] = true;
@@ -409,7 +464,7 @@ __device__ void mma_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, uint32
           }
           if (t == 1) mma_commit_w(&bars->kv_empty[slot_v]);
           if (j + 1 >= ti.js[t] && j + 1 < ti.je[t]) {
-            issue_s<D, F16>(tmem + s_col(t), q_smem[t], ring + slot_k * C::TILE_BYTES);
+            issue_s<D, F16, F8>(tmem + s_col(t), q_smem[t], ring + slot_k * C::TILE_BYTES);
             mma_commit_w(&bars->s_full[t]);
           }
         }
@@ -519,10 +574,14 @@ out:
 // ------------------------------------------------------------------------------------
 // Softmax / correction / epilogue: one thread per query row of its sub-tile.
 
-template <int D, int MASK, bool F16>
-__device__ void softmax_role(const PrefillArgs &a, Bars *bars, uint32_t tmem, const WaitCtl &wc,
-                             int warp, int lane) {
-  using C = Cfg<D, F16>;
+template <int D, int MASK, bool F16, bool F8 = false>
+__device__ void softmax_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, uint32_t tmem,
+                             const WaitCtl &wc, int warp, int lane) {
+  using C = Cfg<D, F16, F8>;
+  // FP8: P is rounded to E4M3 as 2^8 P (values up to 256 of the format's 448, so that small
+  // probabilities keep their significant bits); O = sum(P' V) / sum(P') is unchanged and
+  // the LSE takes the 8 back out.
+  constexpr float POFF = F8 ? 8.f : 0.f;
   constexpr bool CAUSAL = MASK == MASK_CAUSAL;
   constexpr bool MOD = MASK == MASK_MOD;
   const int t = warp >> 2;
@@ -566,9 +625,18 @@ __device__ void softmax_role(const PrefillArgs &a, Bars *bars, uint32_t tmem, co
     }
     float slope2 = 0.f;  // ALiBi slope in log2 units
     if (alibi) slope2 = a.alibi[ti.b * a.alibi_sb + ti.h] * 1.4426950408889634f;
+    // FP8: the Q and K descale factors of (batch, kv head) multiply every score.
+    float qks = 1.f, vds = 1.f;
+    if constexpr (F8) {
+      const int64_t di = static_cast<int64_t>(ti.b) * a.Hkv + ti.hk;
+      if (a.q_descale != nullptr) qks *= a.q_descale[di];
+      if (a.k_descale != nullptr) qks *= a.k_descale[di];
+      if (a.v_descale != nullptr) vds = a.v_descale[di];
+    }
+    const float ct = F8 && !(softcap || alibi) ? c * qks : c;
 
     float m = -INFINITY, l = 0.f;
-    const uint64_t c2 = f2_pack(c, c);
+    const uint64_t c2 = f2_pack(ct, ct);
     for (int j = 0; j < nkv; ++j) {
       const int sb = C::WIDE ? (j & 1) : t;  // S buffer, and its s_full / p_ready barriers
       const uint32_t tS = tmem + lane_off + s_col(sb);
@@ -589,12 +657,13 @@ __device__ void softmax_role(const PrefillArgs &a, Bars *bars, uint32_t tmem, co
       if constexpr (MOD) {
         if (softcap) {
           // softcap * tanh(scale * q.k / softcap), in log2 units
+          const float sci = F8 ? a.sc_in * qks : a.sc_in;
 #pragma unroll
-          for (int i = 0; i < BC; ++i) s[i] = tanh_ex2(s[i] * a.sc_in) * a.sc_out;
+          for (int i = 0; i < BC; ++i) s[i] = tanh_ex2(s[i] * sci) * a.sc_out;
         }
         if (alibi) {
           // - slope * |pos - key|, pos = row + off; the key of column i is kbase + i
-          const float cs = softcap ? 1.f : a.scale_log2;
+          const float cs = softcap ? 1.f : (F8 ? a.scale_log2 * qks : a.scale_log2);
           const float dist0 = static_cast<float>(row + off - kbase);
 #pragma unroll
           for (int i = 0; i < BC; ++i)
@@ -623,12 +692,12 @@ __device__ void softmax_role(const PrefillArgs &a, Bars *bars, uint32_t tmem, co
       }
       const float mx = fmaxf(fmax3(mx0, mx1, s[BC - 4]),
                              fmax3(mx2, mx3, fmax3(s[BC - 3], s[BC - 2], s[BC - 1])));
-      const float m_new = fmaxf(m, mx * c);
+      const float m_new = fmaxf(m, mx * ct);
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
       const bool grow = j > 0 && m_new > m;
       const float alpha = grow ? ex2_approx(m - m_use) : 1.f;
       // P = 2^(S c - m_new) with the FMA and the row sum on packed fp32 pairs.
-      const uint64_t neg2 = f2_pack(-m_use, -m_use);
+      const uint64_t neg2 = f2_pack(POFF - m_use, POFF - m_use);
       uint64_t l2a = f2_pack(0.f, 0.f), l2b = l2a;
       uint32_t p[64];
 #pragma unroll
@@ -640,8 +709,12 @@ __device__ void softmax_role(const PrefillArgs &a, Bars *bars, uint32_t tmem, co
         const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
         l2a = f2_add(l2a, f2_pack(p0, p1));
         l2b = f2_add(l2b, f2_pack(p2, p3));
-        p[i] = pack2<F16>(p0, p1);
-        p[i + 1] = pack2<F16>(p2, p3);
+        if constexpr (F8) {
+          p[i >> 1] = pack_e4m3x4(p0, p1, p2, p3);
+        } else {
+          p[i] = pack2<F16>(p0, p1);
+          p[i + 1] = pack2<F16>(p2, p3);
+        }
       }
       {
         float la, lb, lc, ld;
@@ -649,7 +722,16 @@ __device__ void softmax_role(const PrefillArgs &a, Bars *bars, uint32_t tmem, co
         f2_unpack(l2b, lc, ld);
         l = l * alpha + ((la + lb) + (lc + ld));
       }
-      {
+      if constexpr (F8) {
+        // E4M3 row of 128 keys = 128 bytes, stored in the 128-byte-swizzled K-major layout
+        // of the PV A operand: 16-byte chunk q of row r at chunk q ^ (r mod 8).
+        uint8_t *prow = smem + C::P_OFF + t * (BR * BC) + rit * BC;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          *reinterpret_cast<uint4 *>(prow + ((q ^ (rit & 7)) << 4)) = make_uint4(p[4 * q],
+              p[4 * q + 1], p[4 * q + 2], p[4 * q + 3]);
+        fence_proxy_async_smem();
+      } else {
         uint32_t (&p0)[32] = *reinterpret_cast<uint32_t (*)[32]>(&p[0]);
         uint32_t (&p1)[32] = *reinterpret_cast<uint32_t (*)[32]>(&p[32]);
         tmem_st_x32(tS, p0);
@@ -707,7 +789,7 @@ __device__ void softmax_role(const PrefillArgs &a, Bars *bars, uint32_t tmem, co
       if (!warp_wait(&bars->o_full[t], o_phase, wc)) return;
       o_phase ^= 1u;
       tc_fence_after();
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      const float inv_l = l > 0.f ? vds / l : 0.f;  // vds: FP8 V descale, else 1
 #pragma unroll
       for (int cc = 0; cc < D; cc += 32) {
         uint32_t r[32];
@@ -735,17 +817,17 @@ __device__ void softmax_role(const PrefillArgs &a, Bars *bars, uint32_t tmem, co
         if (8 * v < a.d) dst[v] = make_uint4(0u, 0u, 0u, 0u);
     }
     if (row_ok) {
-      const float lse = l > 0.f ? (m + log2f(l)) * LN2 : -INFINITY;
+      const float lse = l > 0.f ? (m + log2f(l) - POFF) * LN2 : -INFINITY;
       a.lse[static_cast<int64_t>(ti.b) * a.lse_sb + static_cast<int64_t>(ti.h) * a.lse_sh + tok] = lse;
     }
   }
 }
 
-template <int D, int MASK, bool F16>
+template <int D, int MASK, bool F16, bool F8 = false>
 __global__ void __launch_bounds__(NTHREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv, const PrefillArgs a) {
-  using C = Cfg<D>;
+  using C = Cfg<D, F16, F8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -800,7 +882,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(IDLE_REGS));
     } else {
       asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(SOFTMAX_REGS));
-      softmax_role<D, MASK, F16>(a, bars, tmem, wc, warp, lane);
+      softmax_role<D, MASK, F16, F8>(a, smem, bars, tmem, wc, warp, lane);
     }
     __syncwarp();
     tc_fence_before();
@@ -808,12 +890,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   } else {
     if constexpr (!C::WIDE) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(OTHER_REGS));
     if (warp == PRODUCER_WARP) {
-      if (lane == 0) producer_role<D, MASK>(a, &tmq, &tmk, &tmv, smem, bars, wc);
+      if (lane == 0) producer_role<D, MASK, F8>(a, &tmq, &tmk, &tmv, smem, bars, wc);
     } else if (warp == MMA_WARP) {
       if constexpr (C::WIDE)
         mma_role_wide<D, MASK, F16>(a, smem, bars, tmem, wc, lane);
       else
-        mma_role<D, MASK, F16>(a, smem, bars, tmem, wc, lane);
+        mma_role<D, MASK, F16, F8>(a, smem, bars, tmem, wc, lane);
     }
     __syncwarp();
     tc_fence_before();
@@ -825,14 +907,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
 }
 
-template <int D, int MASK, bool F16>
+template <int D, int MASK, bool F16, bool F8 = false>
 cudaError_t launch_impl(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                         const PrefillArgs &a, int grid, cudaStream_t stream) {
-  constexpr int smem = Cfg<D>::SMEM_BYTES;
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, MASK, F16>,
+  constexpr int smem = Cfg<D, F16, F8>::SMEM_BYTES;
+  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, MASK, F16, F8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  prefill_kernel<D, MASK, F16><<<grid, NTHREADS, smem, stream>>>(tq, tk, tv, a);
+  prefill_kernel<D, MASK, F16, F8><<<grid, NTHREADS, smem, stream>>>(tq, tk, tv, a);
   return cudaGetLastError();
 }
 
@@ -864,15 +946,66 @@ int prefill_smem_bytes(int d) {
   return d == 64 ? Cfg<64>::SMEM_BYTES : (d == 128 ? Cfg<128>::SMEM_BYTES : Cfg<256>::SMEM_BYTES);
 }
 
-template <int D, bool F16>
+template <int D, bool F16, bool F8 = false>
 cudaError_t launch_mask(int mask, const CUtensorMap &tq, const CUtensorMap &tk,
                         const CUtensorMap &tv, const PrefillArgs &a, int grid,
                         cudaStream_t stream) {
   switch (mask) {
-    case MASK_NONE: return launch_impl<D, MASK_NONE, F16>(tq, tk, tv, a, grid, stream);
-    case MASK_CAUSAL: return launch_impl<D, MASK_CAUSAL, F16>(tq, tk, tv, a, grid, stream);
-    default: return launch_impl<D, MASK_MOD, F16>(tq, tk, tv, a, grid, stream);
+    case MASK_NONE: return launch_impl<D, MASK_NONE, F16, F8>(tq, tk, tv, a, grid, stream);
+    case MASK_CAUSAL: return launch_impl<D, MASK_CAUSAL, F16, F8>(tq, tk, tv, a, grid, stream);
+    default: return launch_impl<D, MASK_MOD, F16, F8>(tq, tk, tv, a, grid, stream);
   }
+}
+
+cudaError_t launch_prefill_fp8(int mask, const CUtensorMap &tq, const CUtensorMap &tk,
+                               const CUtensorMap &tvt, const PrefillArgs &a, int grid,
+                               cudaStream_t stream) {
+  return launch_mask<128, false, true>(mask, tq, tk, tvt, a, grid, stream);
+}
+
+// V [B, Nk, Hkv, d] E4M3 -> V^T [B, Hkv, d, nk_pad] (keys contiguous, zero past Nk), the
+// K-major layout the FP8 PV product takes.  One block per (64-key tile, kv head, batch).
+__global__ void transpose_v_kernel(const uint8_t *v, int64_t v_sb, int64_t v_sn, int64_t v_sh,
+                                   uint8_t *vt, int Nk, int Hkv, int d, int nk_pad) {
+  __shared__ uint8_t tile[64][128 + 4];
+  const int k0 = blockIdx.x * 64, hk = blockIdx.y, b = blockIdx.z;
+  const int chunks = d / 16;  // 16-byte chunks per key row
+  for (int i = threadIdx.x; i < 64 * chunks; i += blockDim.x) {
+    const int key = i / chunks, c = i - key * chunks;
+    uint4 w = make_uint4(0u, 0u, 0u, 0u);
+    if (k0 + key < Nk)
+      w = *reinterpret_cast<const uint4 *>(v + b * v_sb + static_cast<int64_t>(k0 + key) * v_sn +
+                                           hk * v_sh + c * 16);
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) tile[key][c * 16 + q * 4 + e] = static_cast<uint8_t>(ws[q] >> (8 * e));
+  }
+  __syncthreads();
+  uint8_t *out = vt + (static_cast<int64_t>(b) * Hkv + hk) * d * nk_pad;
+  const int kcols = min(64, nk_pad - k0);  // multiple of 16
+  for (int i = threadIdx.x; i < d * (kcols / 16); i += blockDim.x) {
+    const int row = i / (kcols / 16), c = i - row * (kcols / 16);
+    uint32_t ws[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      ws[q] = static_cast<uint32_t>(tile[c * 16 + q * 4][row]) |
+              (static_cast<uint32_t>(tile[c * 16 + q * 4 + 1][row]) << 8) |
+              (static_cast<uint32_t>(tile[c * 16 + q * 4 + 2][row]) << 16) |
+              (static_cast<uint32_t>(tile[c * 16 + q * 4 + 3][row]) << 24);
+    *reinterpret_cast<uint4 *>(out + static_cast<int64_t>(row) * nk_pad + k0 + c * 16) =
+        make_uint4(ws[0], ws[1], ws[2], ws[3]);
+  }
+}
+
+cudaError_t launch_transpose_v(const void *v, int64_t v_sb, int64_t v_sn, int64_t v_sh, void *vt,
+                               int B, int Nk, int Hkv, int d, int nk_pad, cudaStream_t stream) {
+  if (B == 0 || nk_pad == 0) return cudaSuccess;
+  const dim3 grid((nk_pad + 63) / 64, Hkv, B);
+  transpose_v_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint8_t *>(v), v_sb, v_sn, v_sh,
+                                              static_cast<uint8_t *>(vt), Nk, Hkv, d, nk_pad);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_prefill(int d, int mask, bool f16, const CUtensorMap &tq,

@@ -134,3 +134,17 @@ def kvcache_workload_entry(w: Workload, b: int, device="cpu", seed=None):
     kc[0, n:] = float("nan")
     vc[0, n:] = float("nan")
     return q, kc, vc, int(lens[b])
+
+
+def fp8_inputs(B, Nq, Nk, Hq, Hkv, d, seed, device="cpu", descale=0.25):
+    """E4M3 Q, K, V [B, N, H, d] and their descale factors [B, Hkv]: iid N(0, 1) values
+    divided by a per-(batch, kv head) factor (``descale`` times 1.0 .. 1.5) and rounded to
+    torch.float8_e4m3fn, so that factor * code ~ N(0, 1).  Returns (q, k, v, dq, dk, dv)."""
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    fs = [descale * (1.0 + 0.5 * torch.rand((B, Hkv), generator=g)) for _ in range(3)]
+    out = []
+    for n, h, f in ((Nq, Hq, fs[0]), (Nk, Hkv, fs[1]), (Nk, Hkv, fs[2])):
+        x = torch.randn((B, n, h, d), generator=g)
+        per_head = f.repeat_interleave(h // Hkv, dim=1) if h != Hkv else f
+        out.append((x / per_head[:, None, :, None]).to(torch.float8_e4m3fn).to(device))
+    return (*out, *(f.to(torch.float32).to(device) for f in fs))

@@ -50,7 +50,8 @@ extern "C" {
 /* Element type of Q, K, V and O. */
 typedef enum fa_dtype {
     FA_BF16 = 0, /* bfloat16 */
-    FA_FP16 = 1  /* IEEE binary16 */
+    FA_FP16 = 1, /* IEEE binary16 */
+    FA_E4M3 = 2  /* 8-bit float E4M3 (torch.float8_e4m3fn): inputs of fa_fwd_fp8 only */
 } fa_dtype;
 
 typedef enum fa_status {
@@ -333,6 +334,25 @@ fa_status fa_get_last_device_error(cudaStream_t stream);
 
 /* sizeof(fa_fwd_params), so that foreign-language bindings can check their struct layout. */
 size_t fa_fwd_params_size(void);
+
+/*
+ * FP8 forward ("FlashAttention 1-4 详解", FlashAttention 3 engineering notes: FP8 tensor
+ * cores in the forward pass).  p is read as for fa_fwd, with p->dtype = FA_E4M3: q, k, v
+ * hold E4M3 bytes (strides in elements = bytes, multiples of 16 except where the extent is
+ * 1), o is bf16 (o_strides in bf16 elements), lse fp32.  The attended values are
+ * q_descale * Q, k_descale * K and v_descale * V with one factor per (batch, kv head):
+ * fp32 device arrays [B, Hkv] (contiguous), each may be NULL (= 1).  So S = scale *
+ * (dq dk) Q K^T and O = dv softmax(S) V.  P is rounded to E4M3 for the P V product; the
+ * row sums and the LSE use the unrounded fp32 P.  The score modifiers (p->mod) and causal
+ * apply as in fa_fwd.  d: a multiple of 16 up to 128.  Dense inputs only.
+ * workspace: device memory of at least fa_fwd_fp8_workspace_size(B, Nk, Hkv, d) bytes,
+ * 256-byte aligned, for the transposed V (written by the call, no content needed).
+ * Errors as fa_fwd; FA_ERR_WORKSPACE when the workspace is missing or too small.
+ */
+size_t fa_fwd_fp8_workspace_size(int B, int Nk, int Hkv, int d);
+fa_status fa_fwd_fp8(const fa_fwd_params *p, const float *q_descale, const float *k_descale,
+                     const float *v_descale, void *workspace, size_t workspace_bytes,
+                     cudaStream_t stream);
 
 /* Static text for a status code. */
 const char *fa_status_string(fa_status s);

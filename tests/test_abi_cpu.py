@@ -210,3 +210,38 @@ def test_status_strings(lib):
     lib.fa_status_string.restype = ctypes.c_char_p
     for s in range(6):
         assert lib.fa_status_string(s).decode().startswith("FA_")
+
+
+def test_fp8_rejects_bad_arguments(lib):
+    """fa_fwd_fp8 validates before any CUDA call: dtype must be E4M3, d a multiple of 16 up
+    to 128, 8-bit strides multiples of 16, a large enough 256-byte-aligned workspace."""
+    from exact_attention_81_gb300._binding import FwdParams
+    B, Nq, Nk, Hq, Hkv, d = 2, 100, 300, 4, 2, 128
+
+    def call(ws=4096, wsb=1 << 30, **kw):
+        p = FwdParams()
+        for name in ("q", "k", "v", "o", "lse"):
+            setattr(p, name, 4096)
+        p.B, p.Nq, p.Nk, p.Hq, p.Hkv, p.d = B, Nq, Nk, Hq, Hkv, d
+        p.q_strides[:] = [Nq * Hq * d, Hq * d, d]
+        p.k_strides[:] = p.v_strides[:] = [Nk * Hkv * d, Hkv * d, d]
+        p.o_strides[:] = [Nq * Hq * d, Hq * d, d]
+        p.scale, p.causal, p.dtype = 0.088, 1, 2
+        for key, val in kw.items():
+            if key.endswith("_strides"):
+                getattr(p, key)[:] = val
+            else:
+                setattr(p, key, val)
+        return lib.fa_fwd_fp8(ctypes.byref(p), None, None, None, ws, wsb, None)
+
+    assert call(dtype=0) == 2                      # bf16 inputs: use fa_fwd
+    assert call(d=120) == 2 and call(d=144) == 2 and call(d=8) == 2
+    assert call(q_strides=[Nq * Hq * d, Hq * d + 8, d]) == 1   # 8-bit stride not % 16
+    assert call(k=4104) == 1                       # misaligned pointer
+    assert call(ws=None) == 4
+    need = lib.fa_fwd_fp8_workspace_size(B, Nk, Hkv, d)
+    assert need == ((B * Hkv * d * 304 + 255) // 256) * 256   # keys padded to 304
+    assert call(wsb=need - 1) == 4
+    assert call(ws=4096 + 128) == 4                # workspace not 256-byte aligned
+    assert call(B=0) == 0 and call(Nq=0) == 0      # nothing to do
+    assert lib.fa_fwd_fp8_workspace_size(0, 10, 2, 128) == 0

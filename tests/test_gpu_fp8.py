@@ -1,0 +1,133 @@
+"""GPU parity of the FP8 forward (fa_fwd_fp8: E4M3 Q, K, V with per-(batch, kv head)
+descale factors, bf16 O) against the fp64 oracle.
+
+The pages fix no tolerance for FP8.  The bar is their own test criterion ("flash-attention",
+section 5, tests): the kernel's O error is at most twice that of a PyTorch baseline in the
+input precision (+1e-4) -- fp32 scores and softmax of the decoded inputs, P rounded to E4M3
+for the P V product (the kernel's only 8-bit rounding besides the inputs), normalised by the
+fp32 row sum -- both in the maximum and in the mean; the LSE, computed from unrounded scores
+on both sides, within 1e-3."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.oracle as ORACLE
+from exact_attention_81_gb300 import FA_OK, fa_fwd_fp8, get_last_device_error
+from exact_attention_81_gb300.inputs import fp8_inputs
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _baseline(q, k, v, dq, dk, dv, scale, causal, window=(-1, -1), softcap=0.0):
+    B, Nq, Hq, d = q.shape
+    Nk, Hkv = k.shape[1], k.shape[2]
+    G = Hq // Hkv
+    qf = q.cpu().float() * dq.cpu().repeat_interleave(G, 1)[:, None, :, None]
+    kf = (k.cpu().float() * dk.cpu()[:, None, :, None]).repeat_interleave(G, 2)
+    vf = (v.cpu().float() * dv.cpu()[:, None, :, None]).repeat_interleave(G, 2)
+    s = torch.einsum("bihc,bjhc->bhij", qf, kf) * scale
+    if softcap > 0:
+        s = softcap * torch.tanh(s / softcap)
+    pos = torch.arange(Nq)[:, None] + (Nk - Nq)
+    j = torch.arange(Nk)[None, :]
+    vis = torch.ones(Nq, Nk, dtype=torch.bool)
+    wl, wr = window
+    if causal:
+        wr = 0
+    if wl >= 0:
+        vis &= j >= pos - wl
+    if wr >= 0:
+        vis &= j <= pos + wr
+    s = s.masked_fill(~vis, float("-inf"))
+    m = s.amax(dim=-1, keepdim=True).clamp_min(-1e30)
+    p = torch.exp(s - m)
+    l = p.sum(dim=-1, keepdim=True)
+    p8 = p.to(torch.float8_e4m3fn).float()
+    o = torch.einsum("bhij,bjhc->bihc", p8, vf) / l.permute(0, 2, 1, 3).clamp_min(1e-30)
+    return o.double().numpy()
+
+
+def _check(B, Nq, Nk, Hq, Hkv, d, causal, seed, what, descales=True, **mod):
+    q, k, v, dq, dk, dv = fp8_inputs(B, Nq, Nk, Hq, Hkv, d, seed, device=DEV)
+    if not descales:
+        dq = dk = dv = torch.ones((B, Hkv), dtype=torch.float32, device=DEV)
+    scale = float(np.float32(1 / math.sqrt(d)))
+    o, lse = fa_fwd_fp8(q, k, v, causal=causal, scale=scale,
+                        q_descale=dq if descales else None, k_descale=dk if descales else None,
+                        v_descale=dv if descales else None, **mod)
+    assert get_last_device_error() == FA_OK
+    window = mod.get("window_size", (-1, -1))
+    softcap = mod.get("softcap", 0.0)
+    o_ref, lse_ref = ORACLE.attention_fp8(q.cpu(), k.cpu(), v.cpu(), scale, causal, dq.cpu(),
+                                          dk.cpu(), dv.cpu(), window=window, softcap=softcap)
+    base = _baseline(q, k, v, dq, dk, dv, scale, causal, window, softcap)
+    g = o.double().cpu().numpy()
+    assert np.all(np.isfinite(g)), f"{what}: non-finite O"
+    e_gpu, e_base = np.abs(g - o_ref), np.abs(base - o_ref)
+    assert e_gpu.max() <= 2 * e_base.max() + 1e-4, \
+        f"{what}: max |dO| {e_gpu.max():.3e} > 2 x baseline {e_base.max():.3e}"
+    assert e_gpu.mean() <= 2 * e_base.mean() + 1e-4, \
+        f"{what}: mean |dO| {e_gpu.mean():.3e} > 2 x baseline {e_base.mean():.3e}"
+    l = lse.double().cpu().numpy()
+    fin = np.isfinite(lse_ref)
+    assert np.array_equal(np.isfinite(l), fin), f"{what}: LSE finiteness"
+    assert np.abs(l[fin] - lse_ref[fin]).max(initial=0.0) <= 1e-3, f"{what}: LSE"
+    return e_gpu.max(), e_base.max()
+
+
+@pytest.mark.parametrize("case", [
+    # B, Nq, Nk, Hq, Hkv, d, causal
+    (1, 128, 128, 1, 1, 128, False),
+    (2, 512, 512, 8, 2, 128, True),
+    (2, 700, 700, 4, 4, 128, False),
+    (1, 300, 900, 4, 1, 128, True),
+    (1, 900, 300, 2, 2, 128, True),
+    (2, 333, 517, 4, 2, 64, False),
+    (1, 256, 256, 2, 1, 32, True),
+])
+def test_fp8(case):
+    _check(*case, seed=sum(case[:6]) + 17, what=f"fp8 {case}")
+
+
+def test_fp8_no_descales():
+    _check(1, 400, 400, 4, 2, 128, True, seed=5, what="fp8 without descales", descales=False)
+
+
+@pytest.mark.parametrize("mod", [dict(window_size=(256, 0)), dict(softcap=10.0),
+                                 dict(window_size=(100, 30), softcap=5.0)])
+def test_fp8_modifiers(mod):
+    _check(2, 600, 600, 4, 2, 128, False, seed=23, what=f"fp8 {mod}", **mod)
+
+
+def test_fp8_empty_keys_and_rows_without_keys():
+    """Nk = 0: O = 0, LSE = -inf.  Causal with Nq > Nk: the first rows see no key."""
+    q, k, v, dq, dk, dv = fp8_inputs(1, 64, 1, 2, 2, 128, 31, device=DEV)
+    o, lse = fa_fwd_fp8(q, k[:, :0].contiguous(), v[:, :0].contiguous(), q_descale=dq,
+                        k_descale=dk, v_descale=dv)
+    assert get_last_device_error() == FA_OK
+    assert torch.all(o == 0) and torch.all(torch.isneginf(lse))
+    _check(1, 500, 200, 2, 2, 128, True, seed=32, what="fp8 Nq > Nk causal")
+
+
+def test_fp8_full_size_head():
+    """The causal 8k shape (B=2, H=32, N=8192): every head computed; head (0, 0) against
+    the oracle and the baseline."""
+    B, N, H, d = 2, 8192, 32, 128
+    q, k, v, dq, dk, dv = fp8_inputs(B, N, N, H, H, d, 41, device=DEV)
+    scale = float(np.float32(1 / math.sqrt(d)))
+    o, lse = fa_fwd_fp8(q, k, v, causal=True, scale=scale, q_descale=dq, k_descale=dk,
+                        v_descale=dv)
+    assert get_last_device_error() == FA_OK
+    sl = (slice(0, 1), slice(None), slice(0, 1))
+    q1, k1, v1 = (t[sl].contiguous() for t in (q, k, v))
+    d1 = [x[0:1, 0:1].contiguous() for x in (dq, dk, dv)]
+    o_ref, lse_ref = ORACLE.attention_fp8(q1.cpu(), k1.cpu(), v1.cpu(), scale, True,
+                                          *(x.cpu() for x in d1))
+    base = _baseline(q1, k1, v1, *d1, scale, True)
+    g = o[sl].double().cpu().numpy()
+    e_gpu, e_base = np.abs(g - o_ref), np.abs(base - o_ref)
+    assert e_gpu.max() <= 2 * e_base.max() + 1e-4 and e_gpu.mean() <= 2 * e_base.mean() + 1e-4
+    assert np.abs(lse[0:1, 0:1].double().cpu().numpy() - lse_ref).max() <= 1e-3
