@@ -11,10 +11,11 @@
 //     dV  += P^T dO,  dK += dS^T Q,  dQ += dS K
 // and finally dK *= scale, dQ *= scale (a postprocessing kernel converts dQ).
 //
-// Work unit = (batch b, kv head g, 128-key block j), persistent CTAs in key-block order
-// (with causal masking the first key blocks see the most queries, so the longest units are
-// handed out first; measured against head-major order, which keeps the dQ accumulator
-// tiles of the running CTAs in L2 but balances causal work worse: 705 vs 663 TFLOPS).  A unit visits every
+// Work unit = (batch b, kv head g, 128-key block j), persistent CTAs taking units in order:
+// groups of 8 (b, g) pairs one after the other, key-block-major inside a group (with
+// causal masking the first key blocks see the most queries, so the longest units of a
+// group come first, and the group's dQ accumulators stay in L2; all heads key-block-major:
+// 706 TFLOPS, head-major: 663, groups of 8: 737).  A unit visits every
 // 128-query block i of every query head of group g whose rows can see a key of block j.
 // Keys are the MMA rows (TMEM lanes) of S^T, dP^T, dV and dK, so the dK and dV
 // accumulators stay in TMEM across the unit.
@@ -24,7 +25,7 @@
 //              warps 4-7 queries 64-127), the dQ epilogue (thread = query row, half of the
 //              d columns each) and the dK / dV epilogue at the end of a unit
 //   warp  8    producer: K, V (once per unit), Q, dO (per step) by TMA; LSE and D vectors
-//   warp  9    TMEM allocator and MMA issuer (one lane)
+//   warp  9    TMEM allocator and MMA issuer (the whole warp, one elected lane issues)
 //   warps 10-11 idle: the third warpgroup gives registers back (setmaxnreg) so that the
 //              compute warps hold a 64-query row of P and its dS without spilling
 // TMEM: S^T [0,128), dP^T [128,256) (then dS^T, then dQ), dV [256,256+d), dK [384,384+d).
@@ -53,6 +54,7 @@ constexpr int COMPUTE_REGS = 200;  // 2 x 128 threads x 200
 constexpr int OTHER_REGS = 96;     //   + 128 threads x 96 <= 384 threads x 168 at launch
 constexpr int PRODUCER_WARP = 8;
 constexpr int MMA_WARP = 9;
+constexpr int HEAD_GROUP = 8;     // (batch, kv head) pairs per unit group
 constexpr int BOX = 128 * 128;    // one 128-byte-swizzled box: 128 rows x 128 bytes
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t T_ST = 0, T_DP = 128, T_DV = 256, T_DK = 384;
@@ -99,9 +101,18 @@ struct BUnit {
 template <int MASK>
 __device__ __forceinline__ BUnit bunit_of(const BwdArgs &a, int u) {
   BUnit w;
+  // Units run in groups of HEAD_GROUP (batch, kv head) pairs, key-block-major inside a
+  // group: the CTAs running together then add dQ into a few heads' accumulators (4 MB
+  // each at N = 8192, d = 128), which stay in L2, and causal work still mixes short and
+  // long key blocks (measured: 737 against 706 TFLOPS with all heads key-block-major).
   const int bg = a.B * a.Hkv;
-  w.j = u / bg;
-  const int r = u - w.j * bg;
+  const int S = HEAD_GROUP < bg ? HEAD_GROUP : bg;
+  const int per = a.kblocks * S;
+  const int grp = u / per;
+  const int rem = u - grp * per;
+  const int gs = min(S, bg - grp * S);  // the last group may be smaller
+  w.j = rem / gs;
+  const int r = grp * S + (rem - w.j * gs);
   w.b = r / a.Hkv;
   w.g = r - w.b * a.Hkv;
   if (a.varlen) {
