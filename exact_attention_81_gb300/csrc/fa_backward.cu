@@ -370,7 +370,7 @@ template <int D, int MASK, bool F16>
 __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *smem, BBars *bars,
                             uint32_t tmem, const WaitCtl &wc, int tid) {
   using C = BCfg<D, F16>;
-  const int warp = tid >> 5;
+  const int warp = tid >> 5, lane = tid & 31;
   const int half = warp >> 2;                 // query half (P, dS) / d half (dQ, dK, dV)
   const int r = (warp & 3) * 32 + (tid & 31); // TMEM lane: key row, or query row for dQ
   const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -432,6 +432,34 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
         uint32_t sr[32], dr[32];
         tmem_ld_2x32(tmem + lane_off + T_ST + qc, tmem + lane_off + T_DP + qc, sr, dr);
         uint32_t pp[16], dd[16];
+        if (MASK != MASK_MOD && full) {
+          // No masked pair and no modifier: P = 2^(S c - LSE2), dS = P (dP - D) on packed
+          // fp32 pairs.
+          const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
+#pragma unroll
+          for (int e4 = 0; e4 < 32; e4 += 4) {
+            const float4 l4 = *reinterpret_cast<const float4 *>(lse2 + qc + e4);
+            const float4 d4 = *reinterpret_cast<const float4 *>(dvec + qc + e4);
+            float z0, z1, z2, z3, e0, e1, e2, e3;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e4]), __uint_as_float(sr[e4 + 1])), sc2,
+                             f2_pack(-l4.x, -l4.y)), z0, z1);
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e4 + 2]), __uint_as_float(sr[e4 + 3])),
+                             sc2, f2_pack(-l4.z, -l4.w)), z2, z3);
+            const float p0 = ex2_approx(z0), p1 = ex2_approx(z1);
+            const float p2 = ex2_approx(z2), p3 = ex2_approx(z3);
+            f2_unpack(f2_mul(f2_pack(p0, p1),
+                             f2_add(f2_pack(__uint_as_float(dr[e4]), __uint_as_float(dr[e4 + 1])),
+                                    f2_pack(-d4.x, -d4.y))), e0, e1);
+            f2_unpack(f2_mul(f2_pack(p2, p3),
+                             f2_add(f2_pack(__uint_as_float(dr[e4 + 2]),
+                                            __uint_as_float(dr[e4 + 3])),
+                                    f2_pack(-d4.z, -d4.w))), e2, e3);
+            pp[e4 / 2] = pack2<F16>(p0, p1);
+            pp[e4 / 2 + 1] = pack2<F16>(p2, p3);
+            dd[e4 / 2] = pack2<F16>(e0, e1);
+            dd[e4 / 2 + 1] = pack2<F16>(e2, e3);
+          }
+        } else {
 #pragma unroll
         for (int e4 = 0; e4 < 32; e4 += 4) {
           const float4 l4 = *reinterpret_cast<const float4 *>(lse2 + qc + e4);
@@ -469,6 +497,7 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
           dd[e4 / 2] = pack2<F16>(ds[0], ds[1]);
           dd[e4 / 2 + 1] = pack2<F16>(ds[2], ds[3]);
         }
+        }
         tmem_st_x16(tmem + lane_off + T_ST + packed_col(qc), pp);
         tmem_st_x16(tmem + lane_off + T_DP + packed_col(qc), dd);
         uint8_t *box = ds_s + half * BOX + r * 128;  // box = query half
@@ -485,10 +514,19 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
       tc_fence_before();
       mbar_arrive(&bars->p_ready);
       // dQ epilogue: TMEM -> shared memory (fp32, 128-byte swizzle) -> TMA reduce-add.
+      // Default order: every warp stages its own 32 rows x 64 columns and its lane 0 adds
+      // them (two 32 x 32 boxes), so only warp-level ordering is needed.  Deterministic
+      // order: thread 0 adds the whole tile once the key-block counter allows it.
+      const bool det = a.sem != nullptr;
       if (!warp_wait(&bars->dq_full, it & 1u, wc)) return;
       tc_fence_after();
-      if (tid == 0) bulk_wait_read();  // the previous reduction has read the staging tile
-      if (!group_sync(&bars->cgrp, grp, wc)) return;
+      if (det) {
+        if (tid == 0) bulk_wait_read();  // the previous reduction has read the staging tile
+        if (!group_sync(&bars->cgrp, grp, wc)) return;
+      } else {
+        if (lane == 0) bulk_wait_read();  // this warp's previous reduction read its rows
+        __syncwarp();
+      }
 #pragma unroll
       for (int c2 = 0; c2 < D / 64; ++c2) {
         const int cc = half * (D / 64) + c2;  // 32-column box of dQ
@@ -503,6 +541,21 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
       tc_fence_before();
       mbar_arrive(&bars->dq_empty);
       fence_proxy_async_smem();
+      if (!det) {
+        __syncwarp();
+        if (lane == 0) {
+          const int rq = warp & 3;  // this warp's 32 rows of the tile
+#pragma unroll
+          for (int c2 = 0; c2 < D / 64; ++c2) {
+            const int cc = half * (D / 64) + c2;
+            tma_reduce_add_4d(tdq, dq_s + cc * BOX + rq * 32 * 128, cc * 32, h,
+                              w.q_tok + q0 + rq * 32, w.tma_b);
+          }
+          bulk_commit_group();
+        }
+        ++it;
+        continue;
+      }
       if (!group_sync(&bars->cgrp, grp, wc)) return;
       if (tid == 0) {
         int *sem = a.sem ? a.sem + (static_cast<int64_t>(w.b) * a.Hq + h) * a.qblocks + i : nullptr;
@@ -514,7 +567,10 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
         if (sem != nullptr && !wait_counter(sem, w.j - jmin, wc)) return;
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc)
-          tma_reduce_add_4d(tdq, dq_s + cc * BOX, cc * 32, h, w.q_tok + q0, w.tma_b);
+#pragma unroll
+          for (int rq = 0; rq < 4; ++rq)
+            tma_reduce_add_4d(tdq, dq_s + cc * BOX + rq * 32 * 128, cc * 32, h,
+                              w.q_tok + q0 + rq * 32, w.tma_b);
         bulk_commit_group();
         if (sem != nullptr) {
           bulk_wait_all();             // the additions have been performed
@@ -612,7 +668,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (warp < PRODUCER_WARP) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(COMPUTE_REGS));
     bwd_compute<D, MASK, F16>(a, &tdq, smem, bars, tmem, wc, tid);
-    if (tid == 0) bulk_wait_all();  // every dQ reduction has landed
+    if ((tid & 31) == 0) bulk_wait_all();  // every dQ reduction this lane issued has landed
     __syncwarp();
     tc_fence_before();
     named_barrier(1, NTHREADS);
