@@ -26,7 +26,9 @@
 //              d columns each) and the dK / dV epilogue at the end of a unit
 //   warp  8    producer: K, V (once per unit), Q, dO (per step) by TMA; LSE and D vectors
 //   warp  9    TMEM allocator and MMA issuer (the whole warp, one elected lane issues)
-//   warps 10-11 idle: the third warpgroup gives registers back (setmaxnreg) so that the
+//   warp  10   dQ issuer: TMA reduce-adds of the staged dQ tiles (and the deterministic
+//              order), off the compute warps' critical path
+//   warp  11   idle; the third warpgroup gives registers back (setmaxnreg) so that the
 //              compute warps hold a 64-query row of P and its dS without spilling
 // TMEM: S^T [0,128), dP^T [128,256) (then dS^T, then dQ), dV [256,256+d), dK [384,384+d).
 // P^T and dS^T are written back as packed 16-bit pairs, each query half over the first
@@ -53,6 +55,7 @@ constexpr int NCOMPUTE = 256;
 constexpr int COMPUTE_REGS = 200;  // 2 x 128 threads x 200
 constexpr int OTHER_REGS = 96;     //   + 128 threads x 96 <= 384 threads x 168 at launch
 constexpr int PRODUCER_WARP = 8;
+constexpr int DQ_WARP = 10;       // issues the dQ reduce-adds
 constexpr int MMA_WARP = 9;
 constexpr int HEAD_GROUP = 8;     // (batch, kv head) pairs per unit group
 constexpr int BOX = 128 * 128;    // one 128-byte-swizzled box: 128 rows x 128 bytes
@@ -81,7 +84,7 @@ struct BCfg {
 struct BBars {
   uint64_t kv_full, kv_empty, q_full, q_empty, do_full, do_empty, vec_full, vec_empty;
   uint64_t st_full, dp_full, p_ready, dq_full, dq_empty, acc_full, acc_empty, mma_done;
-  uint64_t cgrp;  // group barrier of the compute threads (bounded wait)
+  uint64_t dq_staged, dq_free;  // dQ staging tile written (compute) / read by the TMA (issuer)
   uint32_t tmem_base;
   int abort;
 };
@@ -188,14 +191,6 @@ __device__ __forceinline__ bool wait_counter(int *ctr, int target, const WaitCtl
   return true;
 }
 
-// Barrier among the compute threads, built on an mbarrier so that the wait is bounded:
-// a warp that has given up never leaves the others blocked.
-__device__ __forceinline__ bool group_sync(uint64_t *bar, uint32_t &phase, const WaitCtl &wc) {
-  mbar_arrive(bar);
-  const bool ok = warp_wait(bar, phase, wc);
-  phase ^= 1u;
-  return ok;
-}
 
 // The issue helpers are warp-collective (the whole MMA warp runs them, one lane issues).
 // M=128 x N=128 x K=D product of two K-major 128-byte-swizzled tiles (S^T and dP^T).
@@ -316,6 +311,62 @@ out:
 }
 
 // ------------------------------------------------------------------------------------
+// dQ issuer: once the compute warps have staged a step's dQ tile, adds it into the fp32
+// accumulator with TMA reduce-adds (32 x 32 boxes), then frees the staging tile as soon as
+// the TMA has read it.  The whole warp runs the loop, lane 0 issues.  Deterministic
+// order: before adding, lane 0 waits until the (batch, head, query block) counter shows
+// that the key blocks before this one have added, and after its own addition has landed
+// it increments the counter.
+
+template <int D, int MASK, bool F16>
+__device__ void bwd_dq_issuer(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *smem,
+                              BBars *bars, const WaitCtl &wc, int lane) {
+  using C = BCfg<D, F16>;
+  uint8_t *dq_s = smem + C::DQ_OFF;
+  uint32_t it = 0;
+  for (int u = blockIdx.x; u < a.num_units; u += gridDim.x) {
+    const BUnit w = bunit_of<MASK>(a, u);
+    if (w.skip || w.nit == 0) continue;
+    const int off = w.nk - w.nq;
+    for (int t = 0; t < w.nit; ++t) {
+      int h, i;
+      bstep(a, w, t, h, i);
+      const int q0 = i * BQ;
+      if (!warp_wait(&bars->dq_staged, it & 1u, wc)) return;
+      bool ok = true;
+      if (lane == 0) {
+        int *sem = a.sem ? a.sem + (static_cast<int64_t>(w.b) * a.Hq + h) * a.qblocks + i : nullptr;
+        // Deterministic order: the key blocks that reach query block i are an interval
+        // jmin .. jmax (jmin = 0 unless a left window bound cuts the first keys); block j
+        // adds after jmin .. j-1.
+        int jmin = 0;
+        if (MASK == MASK_MOD && a.wl >= 0) jmin = max(q0 + off - a.wl, 0) / BKEY;
+        ok = sem == nullptr || wait_counter(sem, w.j - jmin, wc);
+        if (ok) {
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc)
+#pragma unroll
+            for (int rq = 0; rq < 4; ++rq)
+              tma_reduce_add_4d(tdq, dq_s + cc * BOX + rq * 32 * 128, cc * 32, h,
+                                w.q_tok + q0 + rq * 32, w.tma_b);
+          bulk_commit_group();
+          if (sem != nullptr) {
+            bulk_wait_all();             // the additions have been performed
+            fence_proxy_async_global();
+            __threadfence();
+            atomicAdd(sem, 1);
+          }
+          bulk_wait_read();              // the staging tile may be written again
+          mbar_arrive(&bars->dq_free);
+        }
+      }
+      if (!__all_sync(0xffffffffu, ok)) return;
+      ++it;
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------
 // MMA issuer: the whole warp runs the loop, one elected lane issues (an issuing loop
 // confined to one lane is starved by the compute warps of its sub-partition).
 
@@ -370,7 +421,7 @@ template <int D, int MASK, bool F16>
 __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *smem, BBars *bars,
                             uint32_t tmem, const WaitCtl &wc, int tid) {
   using C = BCfg<D, F16>;
-  const int warp = tid >> 5, lane = tid & 31;
+  const int warp = tid >> 5;
   const int half = warp >> 2;                 // query half (P, dS) / d half (dQ, dK, dV)
   const int r = (warp & 3) * 32 + (tid & 31); // TMEM lane: key row, or query row for dQ
   const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -378,7 +429,7 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
   const float *dvec = lse2 + BQ;
   uint8_t *ds_s = smem + C::DS_OFF;
   uint8_t *dq_s = smem + C::DQ_OFF;
-  uint32_t it = 0, acc_n = 0, grp = 0;
+  uint32_t it = 0, acc_n = 0;
   for (int u = blockIdx.x; u < a.num_units; u += gridDim.x) {
     const BUnit w = bunit_of<MASK>(a, u);
     if (w.skip) continue;
@@ -513,20 +564,12 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&bars->p_ready);
-      // dQ epilogue: TMEM -> shared memory (fp32, 128-byte swizzle) -> TMA reduce-add.
-      // Default order: every warp stages its own 32 rows x 64 columns and its lane 0 adds
-      // them (two 32 x 32 boxes), so only warp-level ordering is needed.  Deterministic
-      // order: thread 0 adds the whole tile once the key-block counter allows it.
-      const bool det = a.sem != nullptr;
+      // dQ epilogue: TMEM -> shared memory (fp32, 128-byte swizzle); the reduce-add into
+      // the accumulator is issued by the dQ issuer warp, off this critical path.
       if (!warp_wait(&bars->dq_full, it & 1u, wc)) return;
       tc_fence_after();
-      if (det) {
-        if (tid == 0) bulk_wait_read();  // the previous reduction has read the staging tile
-        if (!group_sync(&bars->cgrp, grp, wc)) return;
-      } else {
-        if (lane == 0) bulk_wait_read();  // this warp's previous reduction read its rows
-        __syncwarp();
-      }
+      // The issuer's previous reduction has read the staging tile.
+      if (it > 0 && !warp_wait(&bars->dq_free, (it - 1) & 1u, wc)) return;
 #pragma unroll
       for (int c2 = 0; c2 < D / 64; ++c2) {
         const int cc = half * (D / 64) + c2;  // 32-column box of dQ
@@ -541,44 +584,7 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
       tc_fence_before();
       mbar_arrive(&bars->dq_empty);
       fence_proxy_async_smem();
-      if (!det) {
-        __syncwarp();
-        if (lane == 0) {
-          const int rq = warp & 3;  // this warp's 32 rows of the tile
-#pragma unroll
-          for (int c2 = 0; c2 < D / 64; ++c2) {
-            const int cc = half * (D / 64) + c2;
-            tma_reduce_add_4d(tdq, dq_s + cc * BOX + rq * 32 * 128, cc * 32, h,
-                              w.q_tok + q0 + rq * 32, w.tma_b);
-          }
-          bulk_commit_group();
-        }
-        ++it;
-        continue;
-      }
-      if (!group_sync(&bars->cgrp, grp, wc)) return;
-      if (tid == 0) {
-        int *sem = a.sem ? a.sem + (static_cast<int64_t>(w.b) * a.Hq + h) * a.qblocks + i : nullptr;
-        // Deterministic order: the key blocks that reach query block i are an interval
-        // jmin .. jmax (jmin = 0 unless a left window bound cuts the first keys); block j
-        // adds after jmin .. j-1.
-        int jmin = 0;
-        if (MASK == MASK_MOD && a.wl >= 0) jmin = max(q0 + off - a.wl, 0) / BKEY;
-        if (sem != nullptr && !wait_counter(sem, w.j - jmin, wc)) return;
-#pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc)
-#pragma unroll
-          for (int rq = 0; rq < 4; ++rq)
-            tma_reduce_add_4d(tdq, dq_s + cc * BOX + rq * 32 * 128, cc * 32, h,
-                              w.q_tok + q0 + rq * 32, w.tma_b);
-        bulk_commit_group();
-        if (sem != nullptr) {
-          bulk_wait_all();             // the additions have been performed
-          fence_proxy_async_global();
-          __threadfence();
-          atomicAdd(sem, 1);
-        }
-      }
+      mbar_arrive(&bars->dq_staged);
       ++it;
     }
     // Unit end: dV and scale * dK of this key row (this warp's half of d) -> global memory.
@@ -643,7 +649,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->acc_empty, NCOMPUTE);
     mbar_init(&bars->mma_done, 1);
-    mbar_init(&bars->cgrp, NCOMPUTE);
+    mbar_init(&bars->dq_staged, NCOMPUTE);
+    mbar_init(&bars->dq_free, 1);
     bars->abort = 0;
     fence_barrier_init();
   }
@@ -668,7 +675,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (warp < PRODUCER_WARP) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(COMPUTE_REGS));
     bwd_compute<D, MASK, F16>(a, &tdq, smem, bars, tmem, wc, tid);
-    if ((tid & 31) == 0) bulk_wait_all();  // every dQ reduction this lane issued has landed
+
     __syncwarp();
     tc_fence_before();
     named_barrier(1, NTHREADS);
@@ -678,6 +685,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       bwd_producer<D, MASK, F16>(a, &tq, &tk, &tv, &tdo, smem, bars, wc, lane);
     } else if (warp == MMA_WARP) {
       bwd_mma<D, MASK, F16>(a, smem, bars, tmem, wc);
+    } else if (warp == DQ_WARP) {
+      bwd_dq_issuer<D, MASK, F16>(a, &tdq, smem, bars, wc, lane);
+      if (lane == 0) bulk_wait_all();  // every dQ reduction has landed
     }
     __syncwarp();
     tc_fence_before();
