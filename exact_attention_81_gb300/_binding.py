@@ -159,6 +159,8 @@ def load_library(path: str | None = None):
         lib.fa_set_wait_timeout_ns.restype = None
         lib.fa_set_fault_injection.argtypes = [ctypes.c_int]
         lib.fa_set_fault_injection.restype = None
+        lib.fa_fwd_host.argtypes = [ctypes.POINTER(FwdParams), vp, vp, vp, vp, vp, i, vp]
+        lib.fa_fwd_host.restype = i
         lib.fa_fwd_fp8_workspace_size.argtypes = [i, i, i, i]
         lib.fa_fwd_fp8_workspace_size.restype = sz
         lib.fa_fwd_fp8.argtypes = [ctypes.POINTER(FwdParams), vp, vp, vp, vp, sz, vp]
@@ -280,6 +282,49 @@ def fa_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, 
     p.dtype = _DTYPE[q.dtype]
     p.mod = _score_mod(B, Hq, q.device, window_size, softcap, alibi_slopes)
     _check(load_library().fa_fwd(ctypes.byref(p), _stream_handle(stream)), "fa_fwd")
+    return out, lse
+
+
+def fa_fwd_host(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
+                device_buffers=None, chunks: int = 8, stream=None, window_size=None,
+                softcap: float = 0.0, alibi_slopes=None, device=None):
+    """fa_fwd on host tensors: q [B,Nq,Hq,d], k/v [B,Nk,Hkv,d] contiguous, pinned CPU bf16 /
+    fp16.  Copies in, computes and copies O and LSE out with the copies overlapping the
+    computation (see fa_fwd_host in fa.h).  device_buffers: (q, k, v, o, lse) CUDA tensors
+    of the same shapes (allocated if None).  Returns (out, lse) pinned CPU tensors; they hold
+    the results once `stream` (default: the current stream) has reached the call."""
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype not in _DTYPE or t.is_cuda or t.dim() != 4 or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous 4-D bf16 / fp16 CPU tensor")
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    if dev.index is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
+    B, Nq, Hq, d = q.shape
+    Nk, Hkv = k.shape[1], k.shape[2]
+    if tuple(k.shape) != (B, Nk, Hkv, d) or tuple(v.shape) != (B, Nk, Hkv, d):
+        raise ValueError("k and v must be [B, Nk, Hkv, d] matching q")
+    if out is None:
+        out = torch.empty((B, Nq, Hq, d), dtype=q.dtype, pin_memory=True)
+    if lse is None:
+        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, pin_memory=True)
+    if device_buffers is None:
+        device_buffers = (torch.empty(q.shape, dtype=q.dtype, device=dev),
+                          torch.empty(k.shape, dtype=q.dtype, device=dev),
+                          torch.empty(v.shape, dtype=q.dtype, device=dev),
+                          torch.empty(out.shape, dtype=q.dtype, device=dev),
+                          torch.empty(lse.shape, dtype=torch.float32, device=dev))
+    p = FwdParams()
+    p.q, p.k, p.v, p.o, p.lse = _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse)
+    p.B, p.Nq, p.Nk, p.Hq, p.Hkv, p.d = B, Nq, Nk, Hq, Hkv, d
+    for name, t in (("q_strides", q), ("k_strides", k), ("v_strides", v), ("o_strides", out)):
+        getattr(p, name)[:] = list(t.stride()[:3])
+    p.scale = default_scale(d) if scale is None else float(scale)
+    p.causal = int(bool(causal))
+    p.dtype = _DTYPE[q.dtype]
+    p.mod = _score_mod(B, Hq, dev, window_size, softcap, alibi_slopes)
+    st = load_library().fa_fwd_host(ctypes.byref(p), *[_ptr(t) for t in device_buffers],
+                                    int(chunks), _stream_handle(stream))
+    _check(st, "fa_fwd_host")
     return out, lse
 
 

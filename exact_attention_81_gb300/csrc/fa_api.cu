@@ -23,11 +23,20 @@ __device__ unsigned int g_device_error;
 constexpr int kMaxDevices = 64;
 constexpr unsigned long long kDefaultTimeoutNs = 10ull * 1000 * 1000 * 1000;
 
+constexpr int kMaxHostRanges = 128;  // (batch, query range) pieces of one fa_fwd_host call
+
 struct DeviceInfo {
   bool ready = false;
   bool supported = false;
   int sm_count = 0;
   unsigned int *err = nullptr;  // device address of g_device_error on this device
+  // fa_fwd_host: two copy streams and the events that order them against the caller's
+  // stream, created on first use; host_mutex serialises the calls that reuse them.
+  bool host_ready = false;
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t ev_start = nullptr, ev_end = nullptr;
+  cudaEvent_t ev_in[kMaxHostRanges] = {}, ev_out[kMaxHostRanges] = {};
+  std::mutex host_mutex;
 };
 
 std::mutex g_mutex;
@@ -304,17 +313,21 @@ bool stride_ok_16b(int64_t s, int64_t extent) {
   return s > 0 && (s % 16) == 0 && s < (int64_t(1) << 38);
 }
 
+fa_status launch_dense(const fa_fwd_params &a, DeviceInfo *dev, const ModPlan &mod,
+                       int64_t lse_sb, int64_t lse_sh, cudaStream_t stream);
+
 // Prefill arguments of a dense call (fa_fwd, fa_fwd_fp8).
 fa::PrefillArgs dense_args(const fa_fwd_params &a, int mblocks, int64_t tiles,
-                           const DeviceInfo *dev, const ModPlan &mod) {
+                           const DeviceInfo *dev, const ModPlan &mod, int64_t lse_sb,
+                           int64_t lse_sh) {
   fa::PrefillArgs pa{};
   pa.o = a.o;
   pa.lse = a.lse;
   pa.o_sb = a.o_strides[0];
   pa.o_sn = a.o_strides[1];
   pa.o_sh = a.o_strides[2];
-  pa.lse_sb = static_cast<int64_t>(a.Hq) * a.Nq;
-  pa.lse_sh = a.Nq;
+  pa.lse_sb = lse_sb;
+  pa.lse_sh = lse_sh;
   pa.B = a.B;
   pa.Hq = a.Hq;
   pa.Hkv = a.Hkv;
@@ -368,7 +381,16 @@ fa_status fa_fwd(const fa_fwd_params *p, cudaStream_t stream) {
   DeviceInfo *dev = nullptr;
   st = current_device(&dev);
   if (st != FA_OK) return st;
-  const int64_t lse_sb = static_cast<int64_t>(a.Hq) * a.Nq, lse_sh = a.Nq;
+  return launch_dense(a, dev, mod, static_cast<int64_t>(a.Hq) * a.Nq, a.Nq, stream);
+}
+
+// The launch part of fa_fwd for validated arguments; lse_sb / lse_sh: LSE strides (the host
+// path computes row ranges of a larger LSE array).
+fa_status launch_dense(const fa_fwd_params &a, DeviceInfo *dev, const ModPlan &mod,
+                       int64_t lse_sb, int64_t lse_sh, cudaStream_t stream) {
+  fa_status st;
+  const int mblocks = ceil_div(a.Nq, fa::prefill_tile_rows(fa::kernel_d(a.d)));
+  const int64_t tiles = static_cast<int64_t>(a.B) * a.Hq * mblocks;
   if (a.Nk == 0) {
     cudaError_t e = fa::launch_fill_empty(a.o, a.lse, a.B, a.Nq, a.Hq, a.d, a.o_strides[0],
                                           a.o_strides[1], a.o_strides[2], lse_sb, lse_sh, stream);
@@ -384,7 +406,7 @@ fa_status fa_fwd(const fa_fwd_params *p, cudaStream_t stream) {
   if ((st = make_map(&tv, a.v, a.d, a.Nk, a.Hkv, a.B, a.v_strides[1], a.v_strides[2],
                      a.v_strides[0], a.dtype)) != FA_OK)
     return st;
-  const fa::PrefillArgs pa = dense_args(a, mblocks, tiles, dev, mod);
+  const fa::PrefillArgs pa = dense_args(a, mblocks, tiles, dev, mod, lse_sb, lse_sh);
   const int grid = static_cast<int>(tiles < dev->sm_count ? tiles : dev->sm_count);
   cudaError_t e =
       fa::launch_prefill(fa::kernel_d(a.d), mod.mask, a.dtype == FA_FP16, tq, tk, tv, pa, grid,
@@ -457,13 +479,160 @@ fa_status fa_fwd_fp8(const fa_fwd_params *p, const float *q_descale, const float
   cudaError_t e = fa::launch_transpose_v(a.v, a.v_strides[0], a.v_strides[1], a.v_strides[2],
                                          workspace, a.B, a.Nk, a.Hkv, a.d, nk_pad, stream);
   if (e != cudaSuccess) return cuda_fail("V transpose launch", e);
-  fa::PrefillArgs pa = dense_args(a, mblocks, tiles, dev, mod);
+  fa::PrefillArgs pa = dense_args(a, mblocks, tiles, dev, mod, static_cast<int64_t>(a.Hq) * a.Nq,
+                                  a.Nq);
   pa.q_descale = q_descale;
   pa.k_descale = k_descale;
   pa.v_descale = v_descale;
   const int grid = static_cast<int>(tiles < dev->sm_count ? tiles : dev->sm_count);
   e = fa::launch_prefill_fp8(mod.mask, tq, tk, tvt, pa, grid, stream);
   return e == cudaSuccess ? FA_OK : cuda_fail("prefill kernel launch", e);
+}
+
+// Copy streams and events of fa_fwd_host on this device (created once).
+fa_status host_resources(DeviceInfo *dev) {
+  if (dev->host_ready) return FA_OK;
+  cudaError_t e;
+  if ((e = cudaStreamCreateWithFlags(&dev->h2d, cudaStreamNonBlocking)) != cudaSuccess ||
+      (e = cudaStreamCreateWithFlags(&dev->d2h, cudaStreamNonBlocking)) != cudaSuccess ||
+      (e = cudaEventCreateWithFlags(&dev->ev_start, cudaEventDisableTiming)) != cudaSuccess ||
+      (e = cudaEventCreateWithFlags(&dev->ev_end, cudaEventDisableTiming)) != cudaSuccess)
+    return cuda_fail("fa_fwd_host stream / event creation", e);
+  for (int i = 0; i < kMaxHostRanges; ++i)
+    if ((e = cudaEventCreateWithFlags(&dev->ev_in[i], cudaEventDisableTiming)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&dev->ev_out[i], cudaEventDisableTiming)) != cudaSuccess)
+      return cuda_fail("fa_fwd_host event creation", e);
+  dev->host_ready = true;
+  return FA_OK;
+}
+
+bool contiguous4(const int64_t s[3], int64_t n, int64_t h, int64_t d) {
+  return s[2] == d && s[1] == h * d && s[0] == n * h * d;
+}
+
+fa_status fa_fwd_host(const fa_fwd_params *p, void *dev_q, void *dev_k, void *dev_v,
+                      void *dev_o, float *dev_lse, int chunks, cudaStream_t stream) {
+  if (p == nullptr) return FA_ERR_INVALID_ARG;
+  const fa_fwd_params &a = *p;
+  if (a.B < 0 || a.Nq < 0 || a.Nk < 0 || a.Hq <= 0 || a.Hkv <= 0 || a.Hq % a.Hkv != 0)
+    return FA_ERR_INVALID_ARG;
+  if (!head_dim_ok(a.d, kMaxPrefillD)) return FA_ERR_UNSUPPORTED;
+  if (!dtype_ok(a.dtype)) return FA_ERR_UNSUPPORTED;
+  if (!scale_ok(a.scale)) return FA_ERR_INVALID_ARG;
+  if (a.Nq > (1 << 30) || a.Nk > (1 << 30)) return FA_ERR_INVALID_ARG;
+  if (chunks < 1 || chunks > 64) return FA_ERR_INVALID_ARG;
+  if (a.B == 0 || a.Nq == 0) return FA_OK;
+  if (a.q == nullptr || a.o == nullptr || a.lse == nullptr || dev_q == nullptr ||
+      dev_o == nullptr || dev_lse == nullptr)
+    return FA_ERR_INVALID_ARG;
+  if (a.Nk > 0 && (a.k == nullptr || a.v == nullptr || dev_k == nullptr || dev_v == nullptr))
+    return FA_ERR_INVALID_ARG;
+  if (!aligned(dev_q, 16) || !aligned(dev_o, 16) || !aligned(dev_lse, 4) ||
+      (a.Nk > 0 && (!aligned(dev_k, 16) || !aligned(dev_v, 16))))
+    return FA_ERR_INVALID_ARG;
+  // Host and device tensors share the contiguous layout, so that a (batch, row range)
+  // piece is one contiguous byte range.
+  if (!contiguous4(a.q_strides, a.Nq, a.Hq, a.d) || !contiguous4(a.o_strides, a.Nq, a.Hq, a.d) ||
+      !contiguous4(a.k_strides, a.Nk, a.Hkv, a.d) || !contiguous4(a.v_strides, a.Nk, a.Hkv, a.d))
+    return FA_ERR_INVALID_ARG;
+  ModPlan mod;
+  fa_status st = plan_mod(&a.mod, a.causal, &mod);
+  if (st != FA_OK) return st;
+  // Row ranges need a key prefix that ends at their last row's position: only when no row
+  // sees keys past its own position (causal, or a right window bound of 0).  Otherwise the
+  // pieces are whole batch entries.
+  const bool prefix = mod.wr == 0;
+  const int per_b = prefix ? std::min<int64_t>(chunks, ceil_div(a.Nq, 128)) : 1;
+  if (static_cast<int64_t>(a.B) * per_b > kMaxHostRanges) return FA_ERR_INVALID_ARG;
+
+  DeviceInfo *dev = nullptr;
+  st = current_device(&dev);
+  if (st != FA_OK) return st;
+  std::lock_guard<std::mutex> lock(dev->host_mutex);
+  if ((st = host_resources(dev)) != FA_OK) return st;
+  const int64_t es = 2;
+  const int64_t qrow = static_cast<int64_t>(a.Hq) * a.d * es;   // bytes per token row
+  const int64_t krow = static_cast<int64_t>(a.Hkv) * a.d * es;
+  cudaError_t e;
+  // The copies start after earlier work on the caller's stream (it may still use the
+  // device buffers).
+  if ((e = cudaEventRecord(dev->ev_start, stream)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(dev->h2d, dev->ev_start, 0)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(dev->d2h, dev->ev_start, 0)) != cudaSuccess)
+    return cuda_fail("fa_fwd_host ordering", e);
+  int piece = 0;
+  for (int b = 0; b < a.B; ++b) {
+    int64_t k_done = 0;  // keys of batch entry b already copied
+    for (int c = 0; c < per_b; ++c, ++piece) {
+      // rows [r0, r1): query blocks split evenly (128-row granularity)
+      const int64_t nblk = ceil_div(a.Nq, 128);
+      const int64_t r0 = std::min<int64_t>(a.Nq, (nblk * c / per_b) * 128);
+      const int64_t r1 = std::min<int64_t>(a.Nq, (nblk * (c + 1) / per_b) * 128);
+      if (r1 <= r0) {
+        // empty range: keep the piece's events in order
+        if ((e = cudaEventRecord(dev->ev_in[piece], dev->h2d)) != cudaSuccess ||
+            (e = cudaEventRecord(dev->ev_out[piece], stream)) != cudaSuccess)
+          return cuda_fail("fa_fwd_host events", e);
+        continue;
+      }
+      // key prefix of the range: positions up to the last row's (bottom-right alignment)
+      const int64_t k_end = prefix ? std::max<int64_t>(0, std::min<int64_t>(a.Nk, r1 + a.Nk - a.Nq))
+                                   : a.Nk;
+      const int64_t qoff = (static_cast<int64_t>(b) * a.Nq + r0) * qrow;
+      const int64_t koff = (static_cast<int64_t>(b) * a.Nk + k_done) * krow;
+      if ((e = cudaMemcpyAsync(static_cast<char *>(dev_q) + qoff,
+                               static_cast<const char *>(a.q) + qoff, (r1 - r0) * qrow,
+                               cudaMemcpyHostToDevice, dev->h2d)) != cudaSuccess)
+        return cuda_fail("fa_fwd_host Q copy", e);
+      if (k_end > k_done) {
+        if ((e = cudaMemcpyAsync(static_cast<char *>(dev_k) + koff,
+                                 static_cast<const char *>(a.k) + koff, (k_end - k_done) * krow,
+                                 cudaMemcpyHostToDevice, dev->h2d)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(static_cast<char *>(dev_v) + koff,
+                                 static_cast<const char *>(a.v) + koff, (k_end - k_done) * krow,
+                                 cudaMemcpyHostToDevice, dev->h2d)) != cudaSuccess)
+          return cuda_fail("fa_fwd_host K/V copy", e);
+        k_done = k_end;
+      }
+      if ((e = cudaEventRecord(dev->ev_in[piece], dev->h2d)) != cudaSuccess ||
+          (e = cudaStreamWaitEvent(stream, dev->ev_in[piece], 0)) != cudaSuccess)
+        return cuda_fail("fa_fwd_host ordering", e);
+      // the range as its own problem: rows [r0, r1) of batch entry b over keys [0, k_end)
+      fa_fwd_params r = a;
+      r.B = 1;
+      r.Nq = static_cast<int>(r1 - r0);
+      r.Nk = static_cast<int>(k_end);
+      r.q = static_cast<const char *>(dev_q) + qoff;
+      r.o = static_cast<char *>(dev_o) + qoff;
+      r.k = static_cast<const char *>(dev_k) + static_cast<int64_t>(b) * a.Nk * krow;
+      r.v = static_cast<const char *>(dev_v) + static_cast<int64_t>(b) * a.Nk * krow;
+      r.lse = dev_lse + static_cast<int64_t>(b) * a.Hq * a.Nq + r0;
+      ModPlan rmod = mod;
+      if (rmod.alibi != nullptr) rmod.alibi += static_cast<int64_t>(b) * rmod.alibi_sb;
+      if ((st = launch_dense(r, dev, rmod, static_cast<int64_t>(a.Hq) * a.Nq, a.Nq, stream)) !=
+          FA_OK)
+        return st;
+      if ((e = cudaEventRecord(dev->ev_out[piece], stream)) != cudaSuccess ||
+          (e = cudaStreamWaitEvent(dev->d2h, dev->ev_out[piece], 0)) != cudaSuccess)
+        return cuda_fail("fa_fwd_host ordering", e);
+      if ((e = cudaMemcpyAsync(static_cast<char *>(a.o) + qoff,
+                               static_cast<const char *>(dev_o) + qoff, (r1 - r0) * qrow,
+                               cudaMemcpyDeviceToHost, dev->d2h)) != cudaSuccess)
+        return cuda_fail("fa_fwd_host O copy", e);
+      // LSE rows [r0, r1) of every head: Hq rows of (r1 - r0) floats, pitch Nq floats
+      const size_t pitch = static_cast<size_t>(a.Nq) * sizeof(float);
+      const int64_t loff = static_cast<int64_t>(b) * a.Hq * a.Nq + r0;
+      if ((e = cudaMemcpy2DAsync(a.lse + loff, pitch, dev_lse + loff, pitch,
+                                 static_cast<size_t>(r1 - r0) * sizeof(float), a.Hq,
+                                 cudaMemcpyDeviceToHost, dev->d2h)) != cudaSuccess)
+        return cuda_fail("fa_fwd_host LSE copy", e);
+    }
+  }
+  // Later work on the caller's stream sees the outputs in host memory.
+  if ((e = cudaEventRecord(dev->ev_end, dev->d2h)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(stream, dev->ev_end, 0)) != cudaSuccess)
+    return cuda_fail("fa_fwd_host ordering", e);
+  return FA_OK;
 }
 
 fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,

@@ -125,6 +125,25 @@ typedef struct fa_fwd_params {
 fa_status fa_fwd(const fa_fwd_params *p, cudaStream_t stream);
 
 /*
+ * fa_fwd with the tensors in host memory: p->q, k, v, o and lse are HOST pointers (page-
+ * locked, so that the copies run asynchronously), in the contiguous layouts [B, Nq, Hq, d],
+ * [B, Nk, Hkv, d] and [B, Hq, Nq] (the strides in p must be those); dev_q, dev_k, dev_v,
+ * dev_o, dev_lse are caller-owned DEVICE buffers of the same shapes, overwritten by the
+ * call.  Enqueues the copies in, the computation and the copies out, ordered after earlier
+ * work on `stream`; later work on `stream` sees O and LSE in host memory.  The query rows
+ * of each batch entry are split into up to `chunks` ranges (1..64) so that copying one
+ * range overlaps computing the previous one: when no row sees keys past its own position
+ * (causal, or a right window bound of 0) a range needs only the key prefix up to its last
+ * row, so K and V travel range by range too, and each range is computed as its own
+ * bottom-right-aligned problem over that prefix (the same rows and LSE as the whole call);
+ * otherwise the ranges are whole batch entries.  B x ranges <= 128.  The library keeps two
+ * copy streams and their events per device for these calls (created on first use).
+ * Errors as fa_fwd; FA_ERR_INVALID_ARG also for other strides or too many ranges.
+ */
+fa_status fa_fwd_host(const fa_fwd_params *p, void *dev_q, void *dev_k, void *dev_v,
+                      void *dev_o, float *dev_lse, int chunks, cudaStream_t stream);
+
+/*
  * Packed variable-length batch, the flash_attn_varlen_func call of "flash-attention"
  * section 1 (capabilities table, varlen row: sequences packed by cu_seqlens).
  *   q   : [total_q, Hq,  d] bf16, contiguous

@@ -245,3 +245,33 @@ def test_fp8_rejects_bad_arguments(lib):
     assert call(ws=4096 + 128) == 4                # workspace not 256-byte aligned
     assert call(B=0) == 0 and call(Nq=0) == 0      # nothing to do
     assert lib.fa_fwd_fp8_workspace_size(0, 10, 2, 128) == 0
+
+
+def test_host_call_rejects_bad_arguments(lib):
+    """fa_fwd_host validates before any CUDA call: 1..64 ranges, contiguous layouts, device
+    buffers present and aligned."""
+    from exact_attention_81_gb300._binding import FwdParams
+    B, Nq, Nk, Hq, Hkv, d = 2, 300, 300, 4, 2, 64
+
+    def call(chunks=4, bufs=(4096, 4096, 4096, 4096, 4096), **kw):
+        p = FwdParams()
+        for name in ("q", "k", "v", "o", "lse"):
+            setattr(p, name, 8192)
+        p.B, p.Nq, p.Nk, p.Hq, p.Hkv, p.d = B, Nq, Nk, Hq, Hkv, d
+        p.q_strides[:] = p.o_strides[:] = [Nq * Hq * d, Hq * d, d]
+        p.k_strides[:] = p.v_strides[:] = [Nk * Hkv * d, Hkv * d, d]
+        p.scale, p.causal, p.dtype = 0.1, 1, 0
+        for key, val in kw.items():
+            if key.endswith("_strides"):
+                getattr(p, key)[:] = val
+            else:
+                setattr(p, key, val)
+        return lib.fa_fwd_host(ctypes.byref(p), *bufs, chunks, None)
+
+    assert call(chunks=0) == 1 and call(chunks=65) == 1
+    assert call(q_strides=[Nq * Hq * d, Hq * d + 8, d]) == 1      # not contiguous
+    assert call(k_strides=[Nk * Hkv * d * 2, Hkv * d, d]) == 1    # batch stride padded
+    assert call(bufs=(None, 4096, 4096, 4096, 4096)) == 1
+    assert call(bufs=(4096, 4096, 4096, 4104, 4096)) == 1         # device O misaligned
+    assert call(d=100) == 2 and call(dtype=2) == 2
+    assert call(B=0) == 0
