@@ -241,10 +241,12 @@ fa_status plan_mod(const fa_score_mod *m, int causal, ModPlan *out) {
     p.alibi_sb = m->alibi_batch_stride;
   }
   if (causal) p.wr = 0;
-  if (p.softcap == 0.f && p.alibi == nullptr && p.wl < 0)
-    p.mask = p.wr < 0 ? fa::MASK_NONE : (p.wr == 0 ? fa::MASK_CAUSAL : fa::MASK_MOD);
-  else
+  if (p.softcap != 0.f || p.alibi != nullptr)
     p.mask = fa::MASK_MOD;
+  else if (p.wl >= 0 || p.wr > 0)
+    p.mask = fa::MASK_WINDOW;
+  else
+    p.mask = p.wr < 0 ? fa::MASK_NONE : fa::MASK_CAUSAL;
   *out = p;
   return FA_OK;
 }

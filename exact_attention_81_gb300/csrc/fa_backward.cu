@@ -142,8 +142,9 @@ __device__ __forceinline__ BUnit bunit_of(const BwdArgs &a, int u) {
   w.ilo = 0;
   w.ihi = w.nqb;
   const long long off = static_cast<long long>(w.nk) - w.nq;
-  const int wr = MASK == MASK_CAUSAL ? 0 : (MASK == MASK_MOD ? a.wr : -1);
-  const int wl = MASK == MASK_MOD ? a.wl : -1;
+  constexpr bool WIN = MASK == MASK_MOD || MASK == MASK_WINDOW;
+  const int wr = MASK == MASK_CAUSAL ? 0 : (WIN ? a.wr : -1);
+  const int wl = WIN ? a.wl : -1;
   if (wr >= 0) {
     // first query block holding a row that sees a key of the block:
     // i*128 + 127 + off + wr >= j*128
@@ -340,7 +341,8 @@ __device__ void bwd_dq_issuer(const BwdArgs &a, const CUtensorMap *tdq, uint8_t 
         // jmin .. jmax (jmin = 0 unless a left window bound cuts the first keys); block j
         // adds after jmin .. j-1.
         int jmin = 0;
-        if (MASK == MASK_MOD && a.wl >= 0) jmin = max(q0 + off - a.wl, 0) / BKEY;
+        if ((MASK == MASK_MOD || MASK == MASK_WINDOW) && a.wl >= 0)
+          jmin = max(q0 + off - a.wl, 0) / BKEY;
         ok = sem == nullptr || wait_counter(sem, w.j - jmin, wc);
         if (ok) {
 #pragma unroll
@@ -465,8 +467,9 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
                (a.wl < 0 || kb >= q0 + BQ - 1 + off - a.wl);
       }
       // this key row's visible query positions (modifiers): key - wr - off <= q <= key + wl - off
-      const int qv_lo = MASK == MASK_MOD && a.wr >= 0 ? key - a.wr - off : INT_MIN;
-      const int qv_hi = MASK == MASK_MOD && a.wl >= 0 ? key + a.wl - off : INT_MAX;
+      constexpr bool WIN = MASK == MASK_MOD || MASK == MASK_WINDOW;
+      const int qv_lo = WIN && a.wr >= 0 ? key - a.wr - off : INT_MIN;
+      const int qv_hi = WIN && a.wl >= 0 ? key + a.wl - off : INT_MAX;
       const bool softcap = MASK == MASK_MOD && a.sc_out != 0.f;
       const bool alibi = MASK == MASK_MOD && a.alibi != nullptr;
       const float slope2 = alibi ? a.alibi[w.b * a.alibi_sb + h] * LOG2E : 0.f;
@@ -535,7 +538,7 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
               z2 = sv * a.scale_log2;
             }
             bool vis;
-            if constexpr (MASK == MASK_MOD)
+            if constexpr (WIN)
               vis = full || (key < w.nk && q0 + qi >= qv_lo && q0 + qi <= qv_hi);
             else
               vis = full || (key < w.nk && (MASK == MASK_NONE || key <= q0 + qi + off));
@@ -802,6 +805,8 @@ cudaError_t launch_bwd_d(int mask, const CUtensorMap &tq, const CUtensorMap &tk,
     case MASK_NONE: return launch_bwd_impl<D, MASK_NONE, F16>(tq, tk, tv, tdo, tdq, a, grid, stream);
     case MASK_CAUSAL:
       return launch_bwd_impl<D, MASK_CAUSAL, F16>(tq, tk, tv, tdo, tdq, a, grid, stream);
+    case MASK_WINDOW:
+      return launch_bwd_impl<D, MASK_WINDOW, F16>(tq, tk, tv, tdo, tdq, a, grid, stream);
     default: return launch_bwd_impl<D, MASK_MOD, F16>(tq, tk, tv, tdo, tdq, a, grid, stream);
   }
 }

@@ -132,7 +132,8 @@ __device__ __forceinline__ TileInfo tile_info(const PrefillArgs &a, int tile) {
   TileInfo ti;
   const int bh = tile / a.mblocks;
   const int r = tile - bh * a.mblocks;
-  const bool desc = MASK == MASK_CAUSAL || (MASK == MASK_MOD && a.desc);
+  const bool desc =
+      MASK == MASK_CAUSAL || ((MASK == MASK_MOD || MASK == MASK_WINDOW) && a.desc);
   const int mb = desc ? (a.mblocks - 1 - r) : r;
   ti.b = bh / a.Hq;
   ti.h = bh - ti.b * a.Hq;
@@ -583,7 +584,8 @@ __device__ void softmax_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, ui
   // the LSE takes the 8 back out.
   constexpr float POFF = F8 ? 8.f : 0.f;
   constexpr bool CAUSAL = MASK == MASK_CAUSAL;
-  constexpr bool MOD = MASK == MASK_MOD;
+  constexpr bool MOD = MASK == MASK_MOD || MASK == MASK_WINDOW;  // window masking
+  constexpr bool SCORE_MOD = MASK == MASK_MOD;                    // softcap / ALiBi code
   const int t = warp >> 2;
   const int wq = warp & 3;
   const int rit = wq * 32 + lane;  // row inside the sub-tile = TMEM lane
@@ -591,8 +593,8 @@ __device__ void softmax_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, ui
   const uint32_t tO = tmem + lane_off + o_col(t);
   // With a softcap or ALiBi the scores are moved to the log2 domain before the max, and
   // the exp2 argument needs no further scaling.
-  const bool softcap = MOD && a.sc_out != 0.f;
-  const bool alibi = MOD && a.alibi != nullptr;
+  const bool softcap = SCORE_MOD && a.sc_out != 0.f;
+  const bool alibi = SCORE_MOD && a.alibi != nullptr;
   const float c = (softcap || alibi) ? 1.f : a.scale_log2;
   // S buffer phases, bit b for buffer b (one buffer per sub-tile; the wide kernel's single
   // sub-tile alternates between two).
@@ -953,6 +955,7 @@ cudaError_t launch_mask(int mask, const CUtensorMap &tq, const CUtensorMap &tk,
   switch (mask) {
     case MASK_NONE: return launch_impl<D, MASK_NONE, F16, F8>(tq, tk, tv, a, grid, stream);
     case MASK_CAUSAL: return launch_impl<D, MASK_CAUSAL, F16, F8>(tq, tk, tv, a, grid, stream);
+    case MASK_WINDOW: return launch_impl<D, MASK_WINDOW, F16, F8>(tq, tk, tv, a, grid, stream);
     default: return launch_impl<D, MASK_MOD, F16, F8>(tq, tk, tv, a, grid, stream);
   }
 }
