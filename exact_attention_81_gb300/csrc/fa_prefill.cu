@@ -1,7 +1,8 @@
 // fa_prefill.cu -- fused exact-attention forward ("prefill") kernel for sm_103a.
 //
 // One persistent CTA per SM walks a list of work tiles.  A work tile is one (batch, query
-// head, 256-row query block): two 128-row query sub-tiles that share one K/V stream, the
+// head, 256-row query block; 128 rows at d > 128): two 128-row query sub-tiles that share
+// one K/V stream, the
 // larger-tile / two-tile ping-pong of "FlashAttention 1-4 详解", FlashAttention 4 section
 // (tile (Br, Bc) -> (Br', Bc') with Br' ~ 2 Br).  For every 128-key K/V tile j the CTA
 // computes, for each sub-tile t,
@@ -19,7 +20,8 @@
 //   warps 0-3  softmax + correction + epilogue for sub-tile 0 (thread = query row)
 //   warps 4-7  the same for sub-tile 1
 //   warp  8    tile scheduler and TMA producer: Q tiles and the K/V ring (one lane)
-//   warp  9    TMEM allocator and MMA issuer (one lane)
+//   warp  9    TMEM allocator and MMA issuer (the whole warp runs the issuing loop, one
+//              elected lane executes each MMA)
 //   warps 10-11 idle
 // The third warpgroup gives registers back (setmaxnreg) so that the two softmax
 // warpgroups can hold a full 128-score row per thread without spilling.
@@ -31,7 +33,8 @@
 // tiles above the diagonal, ~N^2/2 work) limits each sub-tile to the K/V tiles that hold a
 // visible key and masks only the tiles that straddle the diagonal or the sequence end.
 // The score modifiers of the capabilities table of "flash-attention" (sliding window,
-// softcap, ALiBi) run in a third mask mode, MASK_MOD: a 256-row block streams only the K/V
+// softcap, ALiBi) run in the mask modes MASK_WINDOW (a window alone) and MASK_MOD (a
+// softcap or ALiBi, with or without a window): a 256-row block streams only the K/V
 // tiles between its first row's window start and its last row's window end, each
 // sub-tile joins the stream steps its rows can see, and the scores are softcapped and
 // biased in the log2 domain before the row max.
