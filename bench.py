@@ -665,6 +665,23 @@ def extra_workloads(args, dev, pk, world, dist):
                                          "algorithmic_bytes": kv_bytes + io_bytes + new_bytes,
                                          "frac_of_hbm": round(gbs / pk["hbm"], 4),
                                          "gpu_launches_per_call": 3}
+    del q, kc, vc, lens, ws, o, l, kp, vp, kn, vn
+    # decode at head dimension 256 (width-256 instance, 3 ring slots)
+    w = WORKLOADS["decode_d256"]
+    q, kc, vc, lens = kvcache_workload_inputs(w, device=dev)
+    ws = torch.empty(fa.fa_fwd_kvcache_workspace_size(w.B, w.Hq, w.Nk, w.d, 0), dtype=torch.uint8,
+                     device=dev)
+    o = torch.empty_like(q)
+    l = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
+    ms = time_calls(lambda: fa.fa_fwd_kvcache(q, kc, vc, lens, workspace=ws, out=o, lse=l),
+                    max(20, args.steps // 2), stream)
+    kv_bytes = int(lens.long().sum().item()) * w.Hkv * w.d * 2 * 2
+    io_bytes = q.numel() * 2 * 2 + l.numel() * 4
+    gbs = (kv_bytes + io_bytes) / (ms * 1e-3) / 1e9
+    res["decode_d256"] = {"ms": round(ms, 4), "GB/s": round(gbs, 1),
+                          "algorithmic_bytes": kv_bytes + io_bytes,
+                          "frac_of_hbm": round(gbs / pk["hbm"], 4)}
+    del q, kc, vc, lens, ws, o, l
     st = fa.get_last_device_error()
     if st != fa.FA_OK:
         raise RuntimeError(f"device error in extra workloads: {fa.status_string(st)}")

@@ -193,10 +193,11 @@ bool scale_ok(float s) { return std::isfinite(s) && s > 0.f; }
 bool dtype_ok(int t) { return t == FA_BF16 || t == FA_FP16; }
 
 // Head dimensions served: multiples of 8 up to max_d (the kernels run at width 64, 128 or
-// 256; the tensor maps give the columns past d as zeros).  The forward calls take up to
-// 256, decode and backward up to 128.
+// 256; the tensor maps give the columns past d as zeros).  The forward and decode calls
+// take up to 256, the backward up to 128.
 bool head_dim_ok(int d, int max_d = 128) { return d >= 8 && d <= max_d && d % 8 == 0; }
 constexpr int kMaxPrefillD = 256;
+constexpr int kMaxDecodeD = 256;
 
 int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 
@@ -736,9 +737,12 @@ fa_status fa_fwd_kvcache(const void *q, const void *k_cache, const void *v_cache
                          cudaStream_t stream) {
   if (B < 0 || Lmax < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || num_splits < 0)
     return FA_ERR_INVALID_ARG;
-  if (!head_dim_ok(d)) return FA_ERR_UNSUPPORTED;
+  if (!head_dim_ok(d, kMaxDecodeD)) return FA_ERR_UNSUPPORTED;
   const int group = Hq / Hkv;
   if (group != 1 && group != 2 && group != 4 && group != 8) return FA_ERR_UNSUPPORTED;
+  // At width 256 a group of 8 query heads runs as two work items of 4 heads that stream the
+  // same K/V rows (the second read is mostly served by L2): 8 heads' state would spill.
+  const int gshift = fa::kernel_d(d) == 256 && group == 8 ? 1 : 0;
   if (!dtype_ok(dtype)) return FA_ERR_UNSUPPORTED;
   if (!scale_ok(scale)) return FA_ERR_INVALID_ARG;
   if (Lmax > (1 << 30)) return FA_ERR_INVALID_ARG;
@@ -801,12 +805,12 @@ fa_status fa_fwd_kvcache(const void *q, const void *k_cache, const void *v_cache
     const int Leff = mod.wl >= 0 ? std::min<int64_t>(Lmax, static_cast<int64_t>(mod.wl) + kalign)
                                  : Lmax;
     if (num_splits == 0)
-      chunk = auto_chunk(Leff, static_cast<int64_t>(B) * Hkv, dev->sm_count, maxch);
+      chunk = auto_chunk(Leff, static_cast<int64_t>(B) * (Hkv << gshift), dev->sm_count, maxch);
     maxch = ceil_div(Leff, chunk);
     o_part = static_cast<float *>(workspace);
     lse_part = o_part + static_cast<int64_t>(B) * Hq * maxch * fa::kernel_d(d);
   }
-  const int64_t units = static_cast<int64_t>(maxch) * B * Hkv;
+  const int64_t units = static_cast<int64_t>(maxch) * B * (Hkv << gshift);
   if (units > INT32_MAX) return FA_ERR_INVALID_ARG;
   if (Lmax > 0) {
     CUtensorMap tk, tv;
@@ -855,7 +859,8 @@ fa_status fa_fwd_kvcache(const void *q, const void *k_cache, const void *v_cache
     da.lse_part = lse_part;
     da.B = B;
     da.Hq = Hq;
-    da.Hkv = Hkv;
+    da.Hkv = Hkv << gshift;
+    da.gshift = gshift;
     da.Lmax = Lmax;
     da.chunk = chunk;
     da.maxch = maxch;
@@ -881,7 +886,8 @@ fa_status fa_fwd_kvcache(const void *q, const void *k_cache, const void *v_cache
     da.kalign = paged ? 128 : 1;
     const int grid = static_cast<int>(units < dev->sm_count ? units : dev->sm_count);
     cudaError_t e =
-        fa::launch_decode(fa::kernel_d(d), group, dtype == FA_FP16, tk, tv, da, grid, stream);
+        fa::launch_decode(fa::kernel_d(d), group >> gshift, dtype == FA_FP16, tk, tv, da, grid,
+                          stream);
     if (e != cudaSuccess) return cuda_fail("decode kernel launch", e);
   }
   cudaError_t e = fa::launch_combine(fa::kernel_d(d), d, dtype == FA_FP16, o_part, lse_part,

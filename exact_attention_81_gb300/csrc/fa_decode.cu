@@ -63,9 +63,11 @@ struct DCfg {
   static constexpr int NPASS = KPW / KPASS;                    // passes per block
   static constexpr int HPL = (G + TPK - 1) / TPK;              // heads whose p a lane makes
   static constexpr int DQ = D / 4;                             // d quads (P V lanes)
-  static constexpr int KSPLIT = 32 / DQ;                       // key interleave in P V
+  static constexpr int QPL = DQ > 32 ? DQ / 32 : 1;            // quads per lane (d = 256: 2)
+  static constexpr int KSPLIT = DQ >= 32 ? 1 : 32 / DQ;        // key interleave in P V
   static constexpr int PW_BYTES = NWARP * KPW * G * 4;         // per-warp probabilities
-  static constexpr int RED_BYTES = NWARP * G * D * 4;          // per-warp outputs at unit end
+  static constexpr int DS = D / QPL;                           // d columns merged per round
+  static constexpr int RED_BYTES = NWARP * G * DS * 4;         // per-warp outputs at unit end
   static constexpr int MISC_BYTES = 1024;                      // (m, l) per warp, barriers
   static constexpr int BUDGET = 227 * 1024 - 1024;             // minus alignment slack
   static constexpr int NSLOTS =
@@ -79,7 +81,7 @@ struct DCfg {
   static_assert(KPW % KPASS == 0, "passes must cover a warp's keys");
   static_assert(TPK <= 32 && (32 % TPK) == 0, "lanes per key must tile a warp");
   static_assert(DP % 8 == 0, "each lane reads whole 16-byte chunks");
-  static_assert(DQ <= 32 && (32 % DQ) == 0, "d quads must tile a warp");
+  static_assert((DQ <= 32 && (32 % DQ) == 0) || DQ % 32 == 0, "d quads must tile a warp");
 };
 
 struct DBars {
@@ -157,8 +159,8 @@ __device__ void producer(const DecodeArgs &a, const CUtensorMap *tmk, const CUte
 #pragma unroll
           for (int cc = 0; cc < C::KCH; ++cc)
             tma_load_4d_hint(smem + C::RING_OFF + slot * C::BLOCK_BYTES + cc * BOX_BYTES,
-                             which ? tmv : tmk, &bars->full[slot], cc * 64, w.g, row, outer,
-                             policy);
+                             which ? tmv : tmk, &bars->full[slot], cc * 64, w.g >> a.gshift,
+                             row, outer, policy);
         }
         __syncwarp();
         ++it;
@@ -184,8 +186,13 @@ __device__ __forceinline__ bool group_sync(uint64_t *bar, uint32_t &phase, const
   return ok;
 }
 
-// Releases a ring slot: one arrival per compute warp (count 8).
+// Releases a ring slot: one arrival per compute warp (count 8).  The slot was read with
+// generic loads and its next contents arrive through TMA (the async proxy), so each lane
+// orders its reads before the arrival with a proxy fence: without it a TMA write into the
+// released slot could overtake reads still in flight (seen at d = 256 with one query head
+// per group, where the last reads come right before the release).
 __device__ __forceinline__ void release(uint64_t *bar, int lane) {
+  fence_proxy_async_smem();
   __syncwarp();
   if (lane == 0) mbar_arrive(bar);
 }
@@ -203,11 +210,8 @@ __device__ void compute(const DecodeArgs &a, uint8_t *smem, DBars *bars, const W
   const int d0 = part * C::DP;
   const int sbox = d0 / 64;
   const int schunk0 = (d0 % 64) / 8;
-  // P V mapping: lane = (d quad dq, key interleave kpar)
+  // P V mapping: lane = (d quads dq + 32 i for i < QPL, key interleave kpar)
   const int dq = lane % C::DQ, kpar = lane / C::DQ;
-  const int vbox = (4 * dq) / 64;
-  const int vbyte = ((4 * dq) % 64) * 2;
-  const int vchunk = vbyte / 16, vhalf = (vbyte % 16) / 8;
 
   float *pw = reinterpret_cast<float *>(smem + C::PW_OFF) + warp * (C::KPW * G);
   float *red = reinterpret_cast<float *>(smem + C::RED_OFF);
@@ -237,11 +241,12 @@ __device__ void compute(const DecodeArgs &a, uint8_t *smem, DBars *bars, const W
                                       hi_to_f32<F16>(xs[e]) * a.scale_log2);
       }
     }
-    uint64_t acc[G][2];
+    uint64_t acc[G][2 * C::QPL];
     float m[G], l[G];
 #pragma unroll
     for (int gg = 0; gg < G; ++gg) {
-      acc[gg][0] = acc[gg][1] = f2_pack(0.f, 0.f);
+#pragma unroll
+      for (int i = 0; i < 2 * C::QPL; ++i) acc[gg][i] = f2_pack(0.f, 0.f);
       m[gg] = -INFINITY;
       l[gg] = 0.f;
     }
@@ -345,18 +350,26 @@ __device__ void compute(const DecodeArgs &a, uint8_t *smem, DBars *bars, const W
 #pragma unroll
         for (int gg = 0; gg < G; ++gg) {
           const uint64_t al2 = f2_pack(alpha[gg], alpha[gg]);
-          acc[gg][0] = f2_mul(acc[gg][0], al2);
-          acc[gg][1] = f2_mul(acc[gg][1], al2);
+#pragma unroll
+          for (int i = 0; i < 2 * C::QPL; ++i) acc[gg][i] = f2_mul(acc[gg][i], al2);
         }
-        const uint8_t *vblk = smem + C::RING_OFF + slot * C::BLOCK_BYTES + vbox * BOX_BYTES;
+        const uint8_t *vblk0 = smem + C::RING_OFF + slot * C::BLOCK_BYTES;
         const int kend = min(C::KPW, nvalid - kw0);
 #pragma unroll 4
         for (int kk = kpar; kk < kend; kk += C::KSPLIT) {
           const int key = kw0 + kk;
-          const int phys = vchunk ^ (key & 7);
-          const uint2 x = *reinterpret_cast<const uint2 *>(vblk + key * 128 + phys * 16 + vhalf * 8);
-          const uint64_t v01 = f2_pack(lo_to_f32<F16>(x.x), hi_to_f32<F16>(x.x));
-          const uint64_t v23 = f2_pack(lo_to_f32<F16>(x.y), hi_to_f32<F16>(x.y));
+          uint64_t v01[C::QPL], v23[C::QPL];
+#pragma unroll
+          for (int i = 0; i < C::QPL; ++i) {
+            // quad dq + 32 i: box (4 q) / 64, 8-byte half of a swizzled 16-byte chunk
+            const int q4 = 4 * (dq + 32 * i);
+            const int vbyte = (q4 % 64) * 2;
+            const int phys = (vbyte / 16) ^ (key & 7);
+            const uint2 x = *reinterpret_cast<const uint2 *>(
+                vblk0 + (q4 / 64) * BOX_BYTES + key * 128 + phys * 16 + ((vbyte % 16) / 8) * 8);
+            v01[i] = f2_pack(lo_to_f32<F16>(x.x), hi_to_f32<F16>(x.x));
+            v23[i] = f2_pack(lo_to_f32<F16>(x.y), hi_to_f32<F16>(x.y));
+          }
           float p[G];
           if constexpr (G % 4 == 0) {
 #pragma unroll
@@ -374,8 +387,11 @@ __device__ void compute(const DecodeArgs &a, uint8_t *smem, DBars *bars, const W
 #pragma unroll
           for (int gg = 0; gg < G; ++gg) {
             const uint64_t p2 = f2_pack(p[gg], p[gg]);
-            acc[gg][0] = f2_fma(v01, p2, acc[gg][0]);
-            acc[gg][1] = f2_fma(v23, p2, acc[gg][1]);
+#pragma unroll
+            for (int i = 0; i < C::QPL; ++i) {
+              acc[gg][2 * i] = f2_fma(v01[i], p2, acc[gg][2 * i]);
+              acc[gg][2 * i + 1] = f2_fma(v23[i], p2, acc[gg][2 * i + 1]);
+            }
           }
         }
         release(&bars->empty[slot], lane);
@@ -383,11 +399,14 @@ __device__ void compute(const DecodeArgs &a, uint8_t *smem, DBars *bars, const W
     }
 
     // ---- unit end: merge the warps' (m, l, O) and write the normalised partial.
-    float o4[G][4];
+    float o4[G][4 * C::QPL];
 #pragma unroll
     for (int gg = 0; gg < G; ++gg) {
-      f2_unpack(acc[gg][0], o4[gg][0], o4[gg][1]);
-      f2_unpack(acc[gg][1], o4[gg][2], o4[gg][3]);
+#pragma unroll
+      for (int i = 0; i < C::QPL; ++i) {
+        f2_unpack(acc[gg][2 * i], o4[gg][4 * i], o4[gg][4 * i + 1]);
+        f2_unpack(acc[gg][2 * i + 1], o4[gg][4 * i + 2], o4[gg][4 * i + 3]);
+      }
       if constexpr (C::KSPLIT > 1) {
 #pragma unroll
         for (int i = 0; i < 4; ++i)
@@ -396,12 +415,6 @@ __device__ void compute(const DecodeArgs &a, uint8_t *smem, DBars *bars, const W
             o4[gg][i] += __shfl_xor_sync(0xffffffffu, o4[gg][i], off);
       }
     }
-    if (kpar == 0) {
-#pragma unroll
-      for (int gg = 0; gg < G; ++gg)
-        *reinterpret_cast<float4 *>(red + (warp * G + gg) * D + 4 * dq) =
-            make_float4(o4[gg][0], o4[gg][1], o4[gg][2], o4[gg][3]);
-    }
     if (lane == 0) {
 #pragma unroll
       for (int gg = 0; gg < G; ++gg) {
@@ -409,26 +422,38 @@ __device__ void compute(const DecodeArgs &a, uint8_t *smem, DBars *bars, const W
         bars->l[warp][gg] = l[gg];
       }
     }
-    if (!group_sync(&bars->sync, sync_phase, wc)) return;
     const int64_t row0 = (static_cast<int64_t>(w.b) * a.Hq + w.g * G) * a.maxch + w.c;
-    for (int idx = tid; idx < G * D; idx += NCOMPUTE) {
-      const int gg = idx / D, dd = idx - gg * D;
-      float M = -INFINITY;
+    // One round per slice of DS columns (d = 256: two rounds, so the staging buffer holds
+    // half of d and the ring keeps a third slot).
 #pragma unroll
-      for (int ww = 0; ww < C::NWARP; ++ww) M = fmaxf(M, bars->m[ww][gg]);
-      float L = 0.f, O = 0.f;
+    for (int i = 0; i < C::QPL; ++i) {
+      if (kpar == 0) {
 #pragma unroll
-      for (int ww = 0; ww < C::NWARP; ++ww) {
-        const float mw = bars->m[ww][gg];
-        const float wgt = mw == -INFINITY ? 0.f : ex2_approx(mw - M);
-        L = fmaf(bars->l[ww][gg], wgt, L);
-        O = fmaf(red[(ww * G + gg) * D + dd], wgt, O);
+        for (int gg = 0; gg < G; ++gg)
+          *reinterpret_cast<float4 *>(red + (warp * G + gg) * C::DS + 4 * dq) =
+              make_float4(o4[gg][4 * i], o4[gg][4 * i + 1], o4[gg][4 * i + 2],
+                          o4[gg][4 * i + 3]);
       }
-      const int64_t row = row0 + static_cast<int64_t>(gg) * a.maxch;
-      a.o_part[row * D + dd] = O / L;
-      if (dd == 0) a.lse_part[row] = (M + log2f(L)) * LN2;
+      if (!group_sync(&bars->sync, sync_phase, wc)) return;
+      for (int idx = tid; idx < G * C::DS; idx += NCOMPUTE) {
+        const int gg = idx / C::DS, dd = idx - gg * C::DS;
+        float M = -INFINITY;
+#pragma unroll
+        for (int ww = 0; ww < C::NWARP; ++ww) M = fmaxf(M, bars->m[ww][gg]);
+        float L = 0.f, O = 0.f;
+#pragma unroll
+        for (int ww = 0; ww < C::NWARP; ++ww) {
+          const float mw = bars->m[ww][gg];
+          const float wgt = mw == -INFINITY ? 0.f : ex2_approx(mw - M);
+          L = fmaf(bars->l[ww][gg], wgt, L);
+          O = fmaf(red[(ww * G + gg) * C::DS + dd], wgt, O);
+        }
+        const int64_t row = row0 + static_cast<int64_t>(gg) * a.maxch;
+        a.o_part[row * D + i * C::DS + dd] = O / L;
+        if (i == 0 && dd == 0) a.lse_part[row] = (M + log2f(L)) * LN2;
+      }
+      if (!group_sync(&bars->sync, sync_phase, wc)) return;
     }
-    if (!group_sync(&bars->sync, sync_phase, wc)) return;
   }
 }
 
@@ -598,6 +623,13 @@ cudaError_t launch_append(bool f16, const AppendArgs &a, cudaStream_t stream) {
 }
 
 int decode_smem_bytes(int d, int group) {
+  if (d == 256) {  // groups of 8 run as two work items of 4 heads (DecodeArgs::gshift)
+    switch (group) {
+      case 1: return DCfg<256, 1>::SMEM_BYTES;
+      case 2: return DCfg<256, 2>::SMEM_BYTES;
+      default: return DCfg<256, 4>::SMEM_BYTES;
+    }
+  }
   if (d == 64) {
     switch (group) {
       case 1: return DCfg<64, 1>::SMEM_BYTES;
@@ -617,6 +649,13 @@ int decode_smem_bytes(int d, int group) {
 template <bool F16>
 cudaError_t launch_decode_typed(int d, int group, const CUtensorMap &tk, const CUtensorMap &tv,
                                 const DecodeArgs &a, int grid, cudaStream_t stream) {
+  if (d == 256) {  // groups of 8 run as two work items of 4 heads (DecodeArgs::gshift)
+    switch (group) {
+      case 1: return launch_decode_impl<256, 1, F16>(tk, tv, a, grid, stream);
+      case 2: return launch_decode_impl<256, 2, F16>(tk, tv, a, grid, stream);
+      default: return launch_decode_impl<256, 4, F16>(tk, tv, a, grid, stream);
+    }
+  }
   if (d == 64) {
     switch (group) {
       case 1: return launch_decode_impl<64, 1, F16>(tk, tv, a, grid, stream);
@@ -647,8 +686,9 @@ cudaError_t launch_combine(int d, int d_out, bool f16, const float *o_part, cons
   const int blocks = B * Hq;
   if (blocks == 0) return cudaSuccess;
   uint16_t *ob = reinterpret_cast<uint16_t *>(o);
-  auto kern = d == 64 ? (f16 ? combine_kernel<64, true> : combine_kernel<64, false>)
-                      : (f16 ? combine_kernel<128, true> : combine_kernel<128, false>);
+  auto kern = d == 64    ? (f16 ? combine_kernel<64, true> : combine_kernel<64, false>)
+              : d == 256 ? (f16 ? combine_kernel<256, true> : combine_kernel<256, false>)
+                         : (f16 ? combine_kernel<128, true> : combine_kernel<128, false>);
   kern<<<blocks, d, 0, stream>>>(o_part, lse_part, cache_len, len_add, Hq, Lmax, chunk, maxch,
                                  wl, kalign, d_out, ob, lse);
   return cudaGetLastError();

@@ -89,11 +89,15 @@ struct DecodeArgs {
   const int *cache_len;       // [B] device
   float *o_part;              // [B*Hq, maxch, d] fp32 partial outputs (normalised per chunk)
   float *lse_part;            // [B*Hq, maxch] fp32 partial LSE (natural log)
-  int B, Hq, Hkv, Lmax;
+  int B, Hq, Lmax;
+  int Hkv;                    // work-item heads: kv heads << gshift
+  int gshift;                 // each kv head's query group is split into 1 << gshift work
+                              // items of G = group >> gshift heads (d = 256, group 8: G = 4,
+                              // whose q, scores and accumulators fit in registers)
   int chunk;                  // keys per split (multiple of 128)
   int maxch;                  // chunks of the longest visible range: ceil(Leff / chunk)
   int d;                      // head dimension of q and the caches (<= the kernel's D)
-  int num_units;              // maxch * B * Hkv
+  int num_units;              // maxch * B * Hkv (work-item heads)
   float scale_log2;
   unsigned int *err;
   unsigned long long timeout_ns;

@@ -48,6 +48,8 @@ WORKLOADS = {
     "decode16": Workload("decode16", "kvcache", 16, 32, 8, 1, 8192, 128, False, 1006),
     # the causal 8k shape at head dimension 256 (half the heads: the same bytes per token)
     "causal8k_d256": Workload("causal8k_d256", "dense", 2, 16, 16, 8192, 8192, 256, True, 1007),
+    # the decode shape at head dimension 256 (half the batch: the same cache bytes)
+    "decode_d256": Workload("decode_d256", "kvcache", 32, 32, 8, 1, 32768, 256, False, 1008),
 }
 
 

@@ -16,9 +16,10 @@
  * Conventions shared by every call
  *   - Element type: Q, K, V and O are all bf16 or all fp16 (fa_dtype, "flash-attention"
  *     section 5: fp16 / bf16 only); LSE is fp32.  S, l and O accumulate in fp32.
- *   - Head dimension d: a multiple of 8 from 8 to 128 (the upstream limit is "d <= 256
- *     and a multiple of 8" -- "flash-attention", section 5).  The kernels run at width 64
- *     (d <= 64) or 128; the columns past d are read as zeros and never written.
+ *   - Head dimension d: a multiple of 8 from 8 to 256 for the forward and decode calls, to
+ *     128 for the backward (the upstream limit is "d <= 256 and a multiple of 8" --
+ *     "flash-attention", section 5).  The kernels run at width 64 (d <= 64), 128 or 256;
+ *     the columns past d are read as zeros and never written.
  *   - Grouped-query attention: Hkv must divide Hq; query head h reads key/value head
  *     h / (Hq / Hkv) ("flash-attention", capabilities table, MQA / GQA row).
  *   - Causal masking is aligned bottom-right: query i of Nq sees key j of Nk when
@@ -57,8 +58,8 @@ typedef enum fa_dtype {
 typedef enum fa_status {
     FA_OK = 0,
     FA_ERR_INVALID_ARG = 1, /* null pointer, bad size, Hq % Hkv != 0, misaligned pointer/stride */
-    FA_ERR_UNSUPPORTED = 2, /* d not a multiple of 8 in [8, 256] (fa_fwd, fa_fwd_varlen) or
-                               [8, 128] (decode, backward), dtype not a fa_dtype,
+    FA_ERR_UNSUPPORTED = 2, /* d not a multiple of 8 in [8, 256] (forward and decode calls)
+                               or [8, 128] (backward), dtype not a fa_dtype,
                                decode group size not in {1,2,4,8}, or the current device is
                                not an sm_103 GPU */
     FA_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed: see fa_last_cuda_error() */

@@ -165,7 +165,7 @@ def test_kvcache_rejects_bad_arguments(lib):
     assert call(Hq=32, Hkv=2) == 2          # group of 16 not supported by decode
     assert call(dtype=5) == 2
     assert call(d=36) == 2
-    assert call(d=160) == 2
+    assert call(d=264) == 2                 # decode serves d up to 256
     assert call(Hkv=5) == 1
     assert call(ns=-1) == 1
     assert call(lens=None) == 1

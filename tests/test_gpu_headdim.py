@@ -187,14 +187,37 @@ def test_varlen_wide_head_dims(causal):
     compare(*varlen_rows(o, lse), *varlen_rows(o_ref, lse_ref), f"varlen wide causal={causal}")
 
 
-def test_wide_head_dims_not_served_by_decode_and_backward():
+def test_wide_head_dims_not_served_by_backward():
     from exact_attention_81_gb300 import FAError
     d = 256
     q, k, v = dense_inputs(1, 128, 128, 2, 2, d, seed=894, device=DEV)
     o, lse = fa_fwd(q, k, v)
     with pytest.raises(FAError):
         fa_bwd(q, k, v, o, lse, torch.ones_like(q))
-    lens = torch.tensor([100], dtype=torch.int32)
-    qd, kc, vc, lens = kvcache_inputs(1, 256, 2, 2, d, seed=895, lengths=lens, device=DEV)
-    with pytest.raises(FAError):
-        fa_fwd_kvcache(qd, kc, vc, lens)
+
+
+@pytest.mark.parametrize("d,group,dtype", [
+    (256, 8, torch.bfloat16), (256, 4, torch.bfloat16), (256, 2, torch.float16),
+    (192, 8, torch.bfloat16), (136, 1, torch.bfloat16), (248, 4, torch.float16)])
+def test_decode_wide_head_dims(d, group, dtype):
+    """Width-256 decode; a group of 8 runs as two work items of 4 heads on the same rows."""
+    lens = torch.tensor([1, 127, 128, 1000, 3071, 0, 513, 3072], dtype=torch.int32)
+    q, kc, vc, lens = kvcache_inputs(len(lens), 3072, 2 * group, 2, d, seed=900 + d + group,
+                                     lengths=lens, device=DEV, dtype=dtype)
+    o, lse = fa_fwd_kvcache(q, kc, vc, lens)
+    assert get_last_device_error() == FA_OK
+    assert o.shape[-1] == d
+    o_ref, lse_ref = ORACLE.attention_kvcache(q.cpu(), kc.cpu(), vc.cpu(), lens.cpu(), _scale(d))
+    compare(o[:, 0], lse, o_ref, lse_ref, f"decode d={d} G={group} {dtype}")
+
+
+@pytest.mark.parametrize("num_splits", [1, 3, 7])
+def test_decode_wide_explicit_splits(num_splits):
+    lens = torch.tensor([2000, 1, 129, 1024], dtype=torch.int32)
+    q, kc, vc, lens = kvcache_inputs(len(lens), 2048, 16, 2, 256, seed=910 + num_splits,
+                                     lengths=lens, device=DEV)
+    o, lse = fa_fwd_kvcache(q, kc, vc, lens, num_splits=num_splits)
+    assert get_last_device_error() == FA_OK
+    o_ref, lse_ref = ORACLE.attention_kvcache(q.cpu(), kc.cpu(), vc.cpu(), lens.cpu(),
+                                              _scale(256))
+    compare(o[:, 0], lse, o_ref, lse_ref, f"decode d=256 splits={num_splits}")

@@ -123,6 +123,24 @@ def test_paged(page, extra):
     compare(o[:, 0], lse, o_ref, l_ref, f"paged {page} {extra}")
 
 
+@pytest.mark.parametrize("group,extra", [(8, "append_rotary"), (8, "window_softcap"),
+                                         (4, "append"), (2, "none")])
+def test_paged_wide(group, extra):
+    """Width-256 decode through a shuffled block table with the step's extras."""
+    B, Lmax, Hkv, d = 4, 1024, 2, 256
+    q, kc, vc, kn, vn = _case(B, Lmax, Hkv * group, Hkv, d, 630 + group)
+    kp, vp, table = _paged(kc, vc, 128, 631 + group)
+    lens = torch.tensor([1, 300, 1023, 640], dtype=torch.int32, device=DEV)
+    cos, sin = (torch.from_numpy(t).to(DEV) for t in _rope(1100, 128))
+    kw = {"none": {}, "append": dict(k_new=kn, v_new=vn),
+          "append_rotary": dict(k_new=kn, v_new=vn, rotary_cos=cos, rotary_sin=sin),
+          "window_softcap": dict(k_new=kn, v_new=vn, window_size=(333, -1), softcap=12.0)}[extra]
+    st, o, lse, (o_ref, l_ref, k_ref, v_ref) = _step(q, kp, vp, lens, block_table=table, **kw)
+    assert st == FA_OK
+    assert np.array_equal(_bits(kp), k_ref) and np.array_equal(_bits(vp), v_ref)
+    compare(o[:, 0], lse, o_ref, l_ref, f"paged d=256 G={group} {extra}")
+
+
 def test_refused_append_is_flagged_and_writes_nothing():
     """A sequence already at Lmax has no room: flagged, its rows untouched; the others are
     appended and attended as usual in the same call."""

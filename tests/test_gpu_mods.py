@@ -104,7 +104,7 @@ def test_modifiers_varlen():
         compare(*varlen_rows(o, lse), *varlen_rows(o_ref, lse_ref), f"varlen {causal} {mod}")
 
 
-@pytest.mark.parametrize("d,group", [(128, 4), (128, 8), (64, 1), (128, 1)])
+@pytest.mark.parametrize("d,group", [(128, 4), (128, 8), (64, 1), (128, 1), (256, 8), (192, 4)])
 @pytest.mark.parametrize("mod", ["window", "softcap", "alibi", "all"])
 def test_modifiers_decode(d, group, mod):
     lens = torch.tensor([1, 127, 128, 129, 1000, 3000, 0, 4096], dtype=torch.int32)
