@@ -665,7 +665,32 @@ def extra_workloads(args, dev, pk, world, dist):
                                          "algorithmic_bytes": kv_bytes + io_bytes + new_bytes,
                                          "frac_of_hbm": round(gbs / pk["hbm"], 4),
                                          "gpu_launches_per_call": 3}
-    del q, kc, vc, lens, ws, o, l, kp, vp, kn, vn
+    # the decode workload over E4M3 caches: the bf16 caches divided by a per-(batch, kv head)
+    # factor and rounded to float8_e4m3fn on the device (input preparation, untimed)
+    g8 = torch.Generator(device="cpu").manual_seed(w.seed + 100)
+    fk, fv = (0.25 * (1.0 + 0.5 * torch.rand((w.B, w.Hkv), generator=g8)) for _ in range(2))
+    kc8 = torch.empty(kc.shape, dtype=torch.float8_e4m3fn, device=dev)
+    vc8 = torch.empty(vc.shape, dtype=torch.float8_e4m3fn, device=dev)
+    for b in range(w.B):
+        n = int(lens[b].item())
+        kc8[b].view(torch.uint8).fill_(0)
+        vc8[b].view(torch.uint8).fill_(0)
+        kc8[b, :n] = (kc[b, :n].float() / fk[b].to(dev)[None, :, None]).to(torch.float8_e4m3fn)
+        vc8[b, :n] = (vc[b, :n].float() / fv[b].to(dev)[None, :, None]).to(torch.float8_e4m3fn)
+    dk8, dv8 = fk.float().to(dev), fv.float().to(dev)
+    del kp, vp
+    ms_bf16 = res["decode"]["ms"]
+    ms = time_calls(lambda: fa.fa_fwd_kvcache_fp8(q, kc8, vc8, lens, k_descale=dk8, v_descale=dv8,
+                                                  workspace=ws, out=o, lse=l),
+                    max(20, args.steps // 2), stream)
+    kv_bytes = int(lens.long().sum().item()) * w.Hkv * w.d * 1 * 2
+    gbs = (kv_bytes + io_bytes) / (ms * 1e-3) / 1e9
+    res["decode_fp8"] = {"ms": round(ms, 4), "GB/s": round(gbs, 1),
+                         "algorithmic_bytes": kv_bytes + io_bytes,
+                         "frac_of_hbm": round(gbs / pk["hbm"], 4),
+                         "speedup_vs_bf16_cache": round(ms_bf16 / ms, 3),
+                         "gpu_launches_per_call": 2}
+    del q, kc, vc, kc8, vc8, lens, ws, o, l, kn, vn
     # decode at head dimension 256 (width-256 instance, 3 ring slots)
     w = WORKLOADS["decode_d256"]
     q, kc, vc, lens = kvcache_workload_inputs(w, device=dev)

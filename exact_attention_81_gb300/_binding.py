@@ -149,6 +149,10 @@ def load_library(path: str | None = None):
                                        vp, sz, vp, vp, i, pmod, ctypes.POINTER(KvCacheExtras),
                                        vp]
         lib.fa_fwd_kvcache.restype = i
+        lib.fa_fwd_kvcache_fp8.argtypes = [vp, vp, vp, vp, i, i, i, i, i, ctypes.POINTER(i64), f,
+                                           i, vp, vp, vp, sz, vp, vp, pmod,
+                                           ctypes.POINTER(KvCacheExtras), vp]
+        lib.fa_fwd_kvcache_fp8.restype = i
         lib.fa_get_last_device_error.argtypes = [vp]
         lib.fa_get_last_device_error.restype = i
         lib.fa_status_string.argtypes = [i]
@@ -509,6 +513,59 @@ def fa_fwd_kvcache(q, k_cache, v_cache, cache_seqlens, scale: float | None = Non
                                        None if ex is None else ctypes.byref(ex),
                                        _stream_handle(stream))
     _check(st, "fa_fwd_kvcache")
+    return out, lse
+
+
+def fa_fwd_kvcache_fp8(q, k_cache, v_cache, cache_seqlens, k_descale=None, v_descale=None,
+                       scale: float | None = None, num_splits: int = 0, workspace=None,
+                       out=None, lse=None, stream=None, window_size=None, softcap: float = 0.0,
+                       alibi_slopes=None, block_table=None):
+    """Single-query decode over an E4M3 KV cache.  q [B,1,Hq,d] bf16; caches [B,Lmax,Hkv,d]
+    torch.float8_e4m3fn (paged: [num_pages, page_size, Hkv, d] with block_table);
+    k_descale / v_descale fp32 [B, Hkv] CUDA tensors or None (= 1).  d a multiple of 16 up
+    to 256.  Returns (out [B,1,Hq,d] bf16, lse [B,Hq] fp32)."""
+    _require_bf16_cuda("q", q, 4)
+    if q.dtype != torch.bfloat16:
+        raise TypeError("q must be bf16 for an E4M3 cache")
+    for name, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+        if t.dtype != torch.float8_e4m3fn or not t.is_cuda or t.dim() != 4:
+            raise TypeError(f"{name} must be a 4-D torch.float8_e4m3fn CUDA tensor")
+    if k_cache.stride() != v_cache.stride() or k_cache.shape != v_cache.shape:
+        raise ValueError("k_cache and v_cache must share shape and strides")
+    if cache_seqlens.dtype != torch.int32 or not cache_seqlens.is_cuda:
+        raise TypeError("cache_seqlens must be an int32 CUDA tensor")
+    if not q.is_contiguous():
+        raise ValueError("q must be contiguous")
+    B, _, Hq, d = q.shape
+    Hkv = k_cache.shape[2]
+    Lmax = k_cache.shape[1] if block_table is None else block_table.shape[1] * k_cache.shape[1]
+    ex = _kv_extras(q, k_cache, B, Hkv, d, None, None, None, None, False, block_table)
+    keep, ptrs = [], []
+    for name, t in (("k_descale", k_descale), ("v_descale", v_descale)):
+        if t is None:
+            ptrs.append(None)
+            continue
+        if t.dtype != torch.float32 or not t.is_cuda or t.numel() != B * Hkv:
+            raise TypeError(f"{name} must be an fp32 CUDA tensor of B * Hkv elements")
+        t = t.contiguous()
+        keep.append(t)
+        ptrs.append(_ptr(t))
+    if out is None:
+        out = torch.empty((B, 1, Hq, d), dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    need = fa_fwd_kvcache_workspace_size(B, Hq, Lmax, d, num_splits)
+    if workspace is None:
+        workspace = torch.empty((max(need, 256),), dtype=torch.uint8, device=q.device)
+    strides = (ctypes.c_int64 * 3)(*k_cache.stride()[:3])
+    sc = default_scale(d) if scale is None else float(scale)
+    mod = _score_mod(B, Hq, q.device, window_size, softcap, alibi_slopes)
+    st = load_library().fa_fwd_kvcache_fp8(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cache_seqlens), B, Lmax, Hq, Hkv, d,
+        strides, sc, int(num_splits), ptrs[0], ptrs[1], _ptr(workspace), workspace.numel(),
+        _ptr(out), _ptr(lse), ctypes.byref(mod), None if ex is None else ctypes.byref(ex),
+        _stream_handle(stream))
+    _check(st, "fa_fwd_kvcache_fp8")
     return out, lse
 
 

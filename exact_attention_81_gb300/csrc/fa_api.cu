@@ -729,21 +729,30 @@ size_t fa_fwd_kvcache_workspace_size(int B, int Hq, int Lmax, int d, int num_spl
   return static_cast<size_t>((bytes + 255) / 256 * 256);
 }
 
-fa_status fa_fwd_kvcache(const void *q, const void *k_cache, const void *v_cache,
-                         const int *cache_seqlens, int B, int Lmax, int Hq, int Hkv, int d,
-                         const int64_t cache_strides[3], float scale, int num_splits,
-                         void *workspace, size_t workspace_bytes, void *o, float *lse,
-                         int dtype, const fa_score_mod *mod_in, const fa_kvcache_extras *ex,
-                         cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Decode over 16-bit caches (kv_e4m3 false) or E4M3 caches with descale factors per
+// (batch, kv head) and a bf16 query (kv_e4m3 true; no append or rotary).
+fa_status kvcache_call(const void *q, const void *k_cache, const void *v_cache,
+                       const int *cache_seqlens, int B, int Lmax, int Hq, int Hkv, int d,
+                       const int64_t cache_strides[3], float scale, int num_splits,
+                       void *workspace, size_t workspace_bytes, void *o, float *lse, int dtype,
+                       const fa_score_mod *mod_in, const fa_kvcache_extras *ex, bool kv_e4m3,
+                       const float *k_descale, const float *v_descale, cudaStream_t stream) {
   if (B < 0 || Lmax < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || num_splits < 0)
     return FA_ERR_INVALID_ARG;
   if (!head_dim_ok(d, kMaxDecodeD)) return FA_ERR_UNSUPPORTED;
+  if (kv_e4m3 && (d < 16 || d % 16 != 0)) return FA_ERR_UNSUPPORTED;
   const int group = Hq / Hkv;
   if (group != 1 && group != 2 && group != 4 && group != 8) return FA_ERR_UNSUPPORTED;
   // At width 256 a group of 8 query heads runs as two work items of 4 heads that stream the
   // same K/V rows (the second read is mostly served by L2): 8 heads' state would spill.
-  const int gshift = fa::kernel_d(d) == 256 && group == 8 ? 1 : 0;
-  if (!dtype_ok(dtype)) return FA_ERR_UNSUPPORTED;
+  const int kd = kv_e4m3 ? fa::kernel_d_e4m3(d) : fa::kernel_d(d);
+  const int gshift = kd == 256 && group == 8 ? 1 : 0;
+  if (!dtype_ok(dtype) || (kv_e4m3 && dtype != FA_BF16)) return FA_ERR_UNSUPPORTED;
+  if (!aligned(k_descale, 4) || !aligned(v_descale, 4)) return FA_ERR_INVALID_ARG;
   if (!scale_ok(scale)) return FA_ERR_INVALID_ARG;
   if (Lmax > (1 << 30)) return FA_ERR_INVALID_ARG;
   if (B == 0) return FA_OK;
@@ -759,6 +768,7 @@ fa_status fa_fwd_kvcache(const void *q, const void *k_cache, const void *v_cache
   const bool append = ex != nullptr && (ex->k_new != nullptr || ex->v_new != nullptr);
   const bool rotary = ex != nullptr && (ex->rotary_cos != nullptr || ex->rotary_sin != nullptr);
   const bool paged = ex != nullptr && ex->block_table != nullptr;
+  if (kv_e4m3 && (append || rotary)) return FA_ERR_UNSUPPORTED;
   if (append) {
     if (ex->k_new == nullptr || ex->v_new == nullptr || Lmax == 0) return FA_ERR_INVALID_ARG;
     if (!aligned(ex->k_new, 2) || !aligned(ex->v_new, 2)) return FA_ERR_INVALID_ARG;
@@ -814,11 +824,12 @@ fa_status fa_fwd_kvcache(const void *q, const void *k_cache, const void *v_cache
   if (units > INT32_MAX) return FA_ERR_INVALID_ARG;
   if (Lmax > 0) {
     CUtensorMap tk, tv;
+    const int kv_type = kv_e4m3 ? FA_E4M3 : dtype;
     if ((st = make_map(&tk, k_cache, d, num_rows, Hkv, num_outer, cache_strides[1],
-                       cache_strides[2], cache_strides[0], dtype)) != FA_OK)
+                       cache_strides[2], cache_strides[0], kv_type)) != FA_OK)
       return st;
     if ((st = make_map(&tv, v_cache, d, num_rows, Hkv, num_outer, cache_strides[1],
-                       cache_strides[2], cache_strides[0], dtype)) != FA_OK)
+                       cache_strides[2], cache_strides[0], kv_type)) != FA_OK)
       return st;
     if (append) {
       fa::AppendArgs ap{};
@@ -884,10 +895,12 @@ fa_status fa_fwd_kvcache(const void *q, const void *k_cache, const void *v_cache
     da.page_size = paged ? ex->page_size : 1;
     da.num_pages = paged ? ex->num_pages : 0;
     da.kalign = paged ? 128 : 1;
+    da.k_descale = kv_e4m3 ? k_descale : nullptr;
+    da.v_descale = kv_e4m3 ? v_descale : nullptr;
+    da.ostride = fa::kernel_d(d);
     const int grid = static_cast<int>(units < dev->sm_count ? units : dev->sm_count);
-    cudaError_t e =
-        fa::launch_decode(fa::kernel_d(d), group >> gshift, dtype == FA_FP16, tk, tv, da, grid,
-                          stream);
+    cudaError_t e = fa::launch_decode(kd, group >> gshift, dtype == FA_FP16, kv_e4m3, tk, tv,
+                                      da, grid, stream);
     if (e != cudaSuccess) return cuda_fail("decode kernel launch", e);
   }
   cudaError_t e = fa::launch_combine(fa::kernel_d(d), d, dtype == FA_FP16, o_part, lse_part,
@@ -895,6 +908,33 @@ fa_status fa_fwd_kvcache(const void *q, const void *k_cache, const void *v_cache
                                      append ? 1 : 0, B, Hq, Lmax, chunk, maxch, mod.wl,
                                      paged ? 128 : 1, o, lse, dev->err, stream);
   return e == cudaSuccess ? FA_OK : cuda_fail("combine kernel launch", e);
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_fwd_kvcache(const void *q, const void *k_cache, const void *v_cache,
+                         const int *cache_seqlens, int B, int Lmax, int Hq, int Hkv, int d,
+                         const int64_t cache_strides[3], float scale, int num_splits,
+                         void *workspace, size_t workspace_bytes, void *o, float *lse,
+                         int dtype, const fa_score_mod *mod_in, const fa_kvcache_extras *ex,
+                         cudaStream_t stream) {
+  return kvcache_call(q, k_cache, v_cache, cache_seqlens, B, Lmax, Hq, Hkv, d, cache_strides,
+                      scale, num_splits, workspace, workspace_bytes, o, lse, dtype, mod_in, ex,
+                      false, nullptr, nullptr, stream);
+}
+
+fa_status fa_fwd_kvcache_fp8(const void *q, const void *k_cache, const void *v_cache,
+                             const int *cache_seqlens, int B, int Lmax, int Hq, int Hkv, int d,
+                             const int64_t cache_strides[3], float scale, int num_splits,
+                             const float *k_descale, const float *v_descale, void *workspace,
+                             size_t workspace_bytes, void *o, float *lse,
+                             const fa_score_mod *mod_in, const fa_kvcache_extras *ex,
+                             cudaStream_t stream) {
+  return kvcache_call(q, k_cache, v_cache, cache_seqlens, B, Lmax, Hq, Hkv, d, cache_strides,
+                      scale, num_splits, workspace, workspace_bytes, o, lse, FA_BF16, mod_in, ex,
+                      true, k_descale, v_descale, stream);
 }
 
 size_t fa_bwd_params_size(void) { return sizeof(fa_bwd_params); }

@@ -51,9 +51,12 @@ constexpr float LN2 = 0.6931471805599453f;
 __host__ __device__ constexpr int cmax(int a, int b) { return a > b ? a : b; }
 __host__ __device__ constexpr int cmin(int a, int b) { return a < b ? a : b; }
 
-template <int D, int G>
+// F8: K and V are E4M3 (one byte per element, 128 elements per 128-byte box row).
+template <int D, int G, bool F8 = false>
 struct DCfg {
-  static constexpr int KCH = D / 64;
+  static constexpr int EB = F8 ? 1 : 2;                        // bytes per K/V element
+  static constexpr int BOX_ELEMS = 128 / EB;                   // elements of a row per box
+  static constexpr int KCH = D * EB / 128;                     // boxes per row
   static constexpr int BLOCK_BYTES = KCH * BOX_BYTES;         // one K or V block
   static constexpr int NWARP = NCOMPUTE / 32;                  // compute warps
   static constexpr int KPW = KB / NWARP;                       // keys of a block per warp
@@ -62,6 +65,8 @@ struct DCfg {
   static constexpr int KPASS = 32 / TPK;                       // keys per pass of a warp
   static constexpr int NPASS = KPW / KPASS;                    // passes per block
   static constexpr int HPL = (G + TPK - 1) / TPK;              // heads whose p a lane makes
+  static constexpr int CPL = DP * EB / 16;                     // 16-byte chunks per lane
+  static constexpr int PPC = 8 / EB;                           // element pairs per chunk
   static constexpr int DQ = D / 4;                             // d quads (P V lanes)
   static constexpr int QPL = DQ > 32 ? DQ / 32 : 1;            // quads per lane (d = 256: 2)
   static constexpr int KSPLIT = DQ >= 32 ? 1 : 32 / DQ;        // key interleave in P V
@@ -80,7 +85,7 @@ struct DCfg {
   static_assert(NSLOTS >= 2, "ring too small");
   static_assert(KPW % KPASS == 0, "passes must cover a warp's keys");
   static_assert(TPK <= 32 && (32 % TPK) == 0, "lanes per key must tile a warp");
-  static_assert(DP % 8 == 0, "each lane reads whole 16-byte chunks");
+  static_assert((DP * EB) % 16 == 0 && KCH >= 1, "each lane reads whole 16-byte chunks");
   static_assert((DQ <= 32 && (32 % DQ) == 0) || DQ % 32 == 0, "d quads must tile a warp");
 };
 
@@ -94,6 +99,19 @@ struct DBars {
 struct Unit {
   int b, g, c, len, key0, nkeys;
 };
+
+// Element pair e (elements 2e, 2e + 1) of a 16-byte chunk of a K row as packed fp32: bf16
+// or fp16 halves, or E4M3 bytes as values times 2^-120 (the callers scale q by 2^120).
+template <bool F16, bool F8>
+__device__ __forceinline__ uint64_t kv_pair(const uint32_t (&xs)[4], int e) {
+  if constexpr (F8) {
+    const uint32_t w = xs[e >> 1];
+    return (e & 1) ? f2_pack(e4m3_raw<2>(w), e4m3_raw<3>(w))
+                   : f2_pack(e4m3_raw<0>(w), e4m3_raw<1>(w));
+  } else {
+    return f2_pack(lo_to_f32<F16>(xs[e]), hi_to_f32<F16>(xs[e]));
+  }
+}
 
 // First key visible to the decode query of a sequence of len keys (position len - 1).
 __device__ __forceinline__ int first_visible(int len, int wl) {
@@ -124,10 +142,10 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const 
 
 // TMA producer: the whole warp runs the loop and its waits, lane 0 issues the loads (a
 // loop confined to one lane issues late next to the compute warps: 1.7 % of bandwidth).
-template <int D, int G, bool MOD>
+template <int D, int G, bool F8, bool MOD>
 __device__ void producer(const DecodeArgs &a, const CUtensorMap *tmk, const CUtensorMap *tmv,
                          uint8_t *smem, DBars *bars, const WaitCtl &wc, int lane) {
-  using C = DCfg<D, G>;
+  using C = DCfg<D, G, F8>;
   uint32_t it = 0;
   const uint64_t policy = policy_evict_first();  // every cache byte is read once
   if (a.inject) goto out;  // failure injection: load nothing, the consumers' waits run out
@@ -159,7 +177,8 @@ __device__ void producer(const DecodeArgs &a, const CUtensorMap *tmk, const CUte
 #pragma unroll
           for (int cc = 0; cc < C::KCH; ++cc)
             tma_load_4d_hint(smem + C::RING_OFF + slot * C::BLOCK_BYTES + cc * BOX_BYTES,
-                             which ? tmv : tmk, &bars->full[slot], cc * 64, w.g >> a.gshift,
+                             which ? tmv : tmk, &bars->full[slot], cc * C::BOX_ELEMS,
+                             w.g >> a.gshift,
                              row, outer, policy);
         }
         __syncwarp();
@@ -200,16 +219,16 @@ __device__ __forceinline__ void release(uint64_t *bar, int lane) {
 // MOD: the launch has a softcap, ALiBi slopes, or a window over a paged cache (whose unit
 // starts are page-aligned, so keys before the window are masked); uniform runtime branches
 // inside, and the plain instances carry none of that state.
-template <int D, int G, bool F16, bool MOD>
+template <int D, int G, bool F16, bool F8, bool MOD>
 __device__ void compute(const DecodeArgs &a, uint8_t *smem, DBars *bars, const WaitCtl &wc,
                         int tid) {
-  using C = DCfg<D, G>;
+  using C = DCfg<D, G, F8>;
   const int warp = tid >> 5, lane = tid & 31;
   // scores mapping: lane = (key kl of the pass, slice `part` of d)
   const int kl = lane / C::TPK, part = lane % C::TPK;
   const int d0 = part * C::DP;
-  const int sbox = d0 / 64;
-  const int schunk0 = (d0 % 64) / 8;
+  const int sbox = d0 * C::EB / 128;
+  const int schunk0 = (d0 * C::EB % 128) / 16;
   // P V mapping: lane = (d quads dq + 32 i for i < QPL, key interleave kpar)
   const int dq = lane % C::DQ, kpar = lane / C::DQ;
 
@@ -225,6 +244,14 @@ __device__ void compute(const DecodeArgs &a, uint8_t *smem, DBars *bars, const W
     if (w.nkeys <= 0) continue;
     const int nblk = (w.nkeys + KB - 1) / KB;
 
+    // E4M3 caches: descale factors of (b, kv head); K's and 2^120 (the raw-byte decode)
+    // go into q, V's into the partial output.
+    float qscale = a.scale_log2, vds = 1.f;
+    if constexpr (F8) {
+      const int64_t kh = static_cast<int64_t>(w.b) * (a.Hkv >> a.gshift) + (w.g >> a.gshift);
+      qscale *= (a.k_descale ? a.k_descale[kh] : 1.f) * 0x1p120f;
+      vds = a.v_descale ? a.v_descale[kh] : 1.f;
+    }
     // q slice of the G heads of group g in the log2 domain, as pairs (q[d], q[d+1]).
     uint64_t q2[G][C::DP / 2];
 #pragma unroll
@@ -237,8 +264,8 @@ __device__ void compute(const DecodeArgs &a, uint8_t *smem, DBars *bars, const W
         const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          q2[gg][4 * v + e] = f2_pack(lo_to_f32<F16>(xs[e]) * a.scale_log2,
-                                      hi_to_f32<F16>(xs[e]) * a.scale_log2);
+          q2[gg][4 * v + e] = f2_pack(lo_to_f32<F16>(xs[e]) * qscale,
+                                      hi_to_f32<F16>(xs[e]) * qscale);
       }
     }
     uint64_t acc[G][2 * C::QPL];
@@ -274,15 +301,16 @@ __device__ void compute(const DecodeArgs &a, uint8_t *smem, DBars *bars, const W
 #pragma unroll
           for (int gg = 0; gg < G; ++gg) s2[gg] = f2_pack(0.f, 0.f);
 #pragma unroll
-          for (int v = 0; v < C::DP / 8; ++v) {
+          for (int v = 0; v < C::CPL; ++v) {
             const int phys = (schunk0 + v) ^ (key & 7);
             const uint4 x = *reinterpret_cast<const uint4 *>(krow + phys * 16);
             const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const uint64_t k2 = f2_pack(lo_to_f32<F16>(xs[e]), hi_to_f32<F16>(xs[e]));
+            for (int e = 0; e < C::PPC; ++e) {
+              const uint64_t k2 = kv_pair<F16, F8>(xs, e);
 #pragma unroll
-              for (int gg = 0; gg < G; ++gg) s2[gg] = f2_fma(q2[gg][4 * v + e], k2, s2[gg]);
+              for (int gg = 0; gg < G; ++gg)
+                s2[gg] = f2_fma(q2[gg][C::PPC * v + e], k2, s2[gg]);
             }
           }
 #pragma unroll
@@ -329,7 +357,7 @@ __device__ void compute(const DecodeArgs &a, uint8_t *smem, DBars *bars, const W
 #pragma unroll
           for (int pass = 0; pass < C::NPASS; ++pass) {
             const float p = ex2_approx(sc[pass][gg] - m_use);
-            pw[(pass * C::KPASS + kl) * G + gg] = p;
+            pw[(pass * C::KPASS + kl) * G + gg] = F8 ? p * 0x1p120f : p;  // V raw: 2^-120
             psum[i] += p;
           }
         }
@@ -361,14 +389,21 @@ __device__ void compute(const DecodeArgs &a, uint8_t *smem, DBars *bars, const W
           uint64_t v01[C::QPL], v23[C::QPL];
 #pragma unroll
           for (int i = 0; i < C::QPL; ++i) {
-            // quad dq + 32 i: box (4 q) / 64, 8-byte half of a swizzled 16-byte chunk
+            // quad dq + 32 i: its box, then its bytes inside a swizzled 16-byte chunk
             const int q4 = 4 * (dq + 32 * i);
-            const int vbyte = (q4 % 64) * 2;
+            const int vbyte = (q4 % C::BOX_ELEMS) * C::EB;
             const int phys = (vbyte / 16) ^ (key & 7);
-            const uint2 x = *reinterpret_cast<const uint2 *>(
-                vblk0 + (q4 / 64) * BOX_BYTES + key * 128 + phys * 16 + ((vbyte % 16) / 8) * 8);
-            v01[i] = f2_pack(lo_to_f32<F16>(x.x), hi_to_f32<F16>(x.x));
-            v23[i] = f2_pack(lo_to_f32<F16>(x.y), hi_to_f32<F16>(x.y));
+            const uint8_t *src =
+                vblk0 + (q4 / C::BOX_ELEMS) * BOX_BYTES + key * 128 + phys * 16 + vbyte % 16;
+            if constexpr (F8) {
+              const uint32_t x = *reinterpret_cast<const uint32_t *>(src);
+              v01[i] = f2_pack(e4m3_raw<0>(x), e4m3_raw<1>(x));
+              v23[i] = f2_pack(e4m3_raw<2>(x), e4m3_raw<3>(x));
+            } else {
+              const uint2 x = *reinterpret_cast<const uint2 *>(src);
+              v01[i] = f2_pack(lo_to_f32<F16>(x.x), hi_to_f32<F16>(x.x));
+              v23[i] = f2_pack(lo_to_f32<F16>(x.y), hi_to_f32<F16>(x.y));
+            }
           }
           float p[G];
           if constexpr (G % 4 == 0) {
@@ -449,7 +484,8 @@ __device__ void compute(const DecodeArgs &a, uint8_t *smem, DBars *bars, const W
           O = fmaf(red[(ww * G + gg) * C::DS + dd], wgt, O);
         }
         const int64_t row = row0 + static_cast<int64_t>(gg) * a.maxch;
-        a.o_part[row * D + i * C::DS + dd] = O / L;
+        const int col = i * C::DS + dd;  // rows of the partials are ostride (<= D) wide
+        if (col < a.ostride) a.o_part[row * a.ostride + col] = O / L * vds;
         if (i == 0 && dd == 0) a.lse_part[row] = (M + log2f(L)) * LN2;
       }
       if (!group_sync(&bars->sync, sync_phase, wc)) return;
@@ -457,11 +493,11 @@ __device__ void compute(const DecodeArgs &a, uint8_t *smem, DBars *bars, const W
   }
 }
 
-template <int D, int G, bool F16, bool MOD>
+template <int D, int G, bool F16, bool F8, bool MOD>
 __global__ void __launch_bounds__(NTHREADS, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   const DecodeArgs a) {
-  using C = DCfg<D, G>;
+  using C = DCfg<D, G, F8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -486,23 +522,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // Each register-split branch ends on its own named barrier.
   if (warp < PRODUCER_WARP) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(COMPUTE_REGS));
-    compute<D, G, F16, MOD>(a, smem, bars, wc, tid);
+    compute<D, G, F16, F8, MOD>(a, smem, bars, wc, tid);
     __syncwarp();
     named_barrier(1, NTHREADS);
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(PRODUCER_REGS));
-    if (warp == PRODUCER_WARP) producer<D, G, MOD>(a, &tmk, &tmv, smem, bars, wc, lane);
+    if (warp == PRODUCER_WARP) producer<D, G, F8, MOD>(a, &tmk, &tmv, smem, bars, wc, lane);
     __syncwarp();
     named_barrier(1, NTHREADS);
   }
 }
 
-template <int D, int G, bool F16>
+template <int D, int G, bool F16, bool F8 = false>
 cudaError_t launch_decode_impl(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeArgs &a,
                                int grid, cudaStream_t stream) {
-  constexpr int smem = DCfg<D, G>::SMEM_BYTES;
+  constexpr int smem = DCfg<D, G, F8>::SMEM_BYTES;
   const bool mod = a.sc_out != 0.f || a.alibi != nullptr || (a.wl >= 0 && a.kalign > 1);
-  auto kern = mod ? decode_kernel<D, G, F16, true> : decode_kernel<D, G, F16, false>;
+  auto kern = mod ? decode_kernel<D, G, F16, F8, true> : decode_kernel<D, G, F16, F8, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   kern<<<grid, NTHREADS, smem, stream>>>(tk, tv, a);
@@ -672,9 +708,28 @@ cudaError_t launch_decode_typed(int d, int group, const CUtensorMap &tk, const C
   }
 }
 
-cudaError_t launch_decode(int d, int group, bool f16, const CUtensorMap &tk,
+// E4M3 caches with a bf16 query: widths 128 and 256 (a 128-byte box row holds 128 elements).
+cudaError_t launch_decode_e4m3(int d, int group, const CUtensorMap &tk, const CUtensorMap &tv,
+                               const DecodeArgs &a, int grid, cudaStream_t stream) {
+  if (d == 256) {  // groups of 8 run as two work items of 4 heads (DecodeArgs::gshift)
+    switch (group) {
+      case 1: return launch_decode_impl<256, 1, false, true>(tk, tv, a, grid, stream);
+      case 2: return launch_decode_impl<256, 2, false, true>(tk, tv, a, grid, stream);
+      default: return launch_decode_impl<256, 4, false, true>(tk, tv, a, grid, stream);
+    }
+  }
+  switch (group) {
+    case 1: return launch_decode_impl<128, 1, false, true>(tk, tv, a, grid, stream);
+    case 2: return launch_decode_impl<128, 2, false, true>(tk, tv, a, grid, stream);
+    case 4: return launch_decode_impl<128, 4, false, true>(tk, tv, a, grid, stream);
+    default: return launch_decode_impl<128, 8, false, true>(tk, tv, a, grid, stream);
+  }
+}
+
+cudaError_t launch_decode(int d, int group, bool f16, bool kv_e4m3, const CUtensorMap &tk,
                           const CUtensorMap &tv, const DecodeArgs &a, int grid,
                           cudaStream_t stream) {
+  if (kv_e4m3) return launch_decode_e4m3(d, group, tk, tv, a, grid, stream);
   return f16 ? launch_decode_typed<true>(d, group, tk, tv, a, grid, stream)
              : launch_decode_typed<false>(d, group, tk, tv, a, grid, stream);
 }

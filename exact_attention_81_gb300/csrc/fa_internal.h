@@ -112,6 +112,9 @@ struct DecodeArgs {
   const int *block_table;     // paged cache: page of logical block j of b at [b*bt_stride + j]
   int bt_stride, page_size, num_pages;
   int kalign;                 // unit starts rounded down to a multiple of this (128 if paged)
+  // E4M3 caches: descale factors per (batch, kv head) [B, kv heads], null = 1.
+  const float *k_descale, *v_descale;
+  int ostride;                // width of a partial-output row (<= the kernel's D)
 };
 
 // First key a decode unit streams: the first visible key, rounded down to `align` so that a
@@ -141,21 +144,25 @@ struct AppendArgs {
 
 cudaError_t launch_append(bool f16, const AppendArgs &a, cudaStream_t stream);
 
-cudaError_t launch_decode(int d, int group, bool f16, const CUtensorMap &tk,
+// d: the kernel width (64, 128 or 256; 128 or 256 when kv_e4m3, with a bf16 query).
+cudaError_t launch_decode(int d, int group, bool f16, bool kv_e4m3, const CUtensorMap &tk,
                           const CUtensorMap &tv, const DecodeArgs &a, int grid,
                           cudaStream_t stream);
 
 // wl, kalign, len_add: as in DecodeArgs; chunks tile the keys [decode_first_key, len) of
 // each sequence, len = cache_len + len_add.
-// d: the kernel width of the partials (64 or 128); d_out: the head dimension of o.
+// d: the width of the partial rows (64, 128 or 256); d_out: the head dimension of o.
 cudaError_t launch_combine(int d, int d_out, bool f16, const float *o_part, const float *lse_part,
                            const int *cache_len, int len_add, int B, int Hq, int Lmax, int chunk,
                            int maxch, int wl, int kalign, void *o, float *lse, unsigned int *err,
                            cudaStream_t stream);
 
 // Width of the kernel instance that serves head dimension d (8 <= d <= 256, d % 8 == 0;
-// widths above 128 exist for the prefill kernel only).
+// the backward serves widths up to 128).
 inline int kernel_d(int d) { return d <= 64 ? 64 : (d <= 128 ? 128 : 256); }
+
+// Width of the decode instance over E4M3 caches (a 128-byte box row is 128 elements).
+inline int kernel_d_e4m3(int d) { return d <= 128 ? 128 : 256; }
 
 // Query rows of one prefill work tile for kernel width kd: two 128-row sub-tiles, one
 // when the head dimension is above 128 (TMEM holds a single D-wide accumulator then).

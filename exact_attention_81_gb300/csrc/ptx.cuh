@@ -456,6 +456,18 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_addr, uint32_t lbo_
 // ---------------------------------------------------------------------------------------
 // Numeric helpers.
 
+// E4M3 byte K (0..3) of a word -> fp32 with the same sign, exponent and mantissa fields
+// moved into place: the value times 2^-120 (bias 7 -> 127), exact.  E4M3 subnormals
+// become fp32 subnormals, so the products that use these values must not flush them
+// (the callers fold 2^120 into the other factor).  The E4M3 NaN codes (S.1111.111) read
+// as 480 * 2^-120.  An arithmetic shift copies the sign down; the mask keeps the sign and
+// the seven exponent-mantissa bits.
+template <int K>
+__device__ __forceinline__ float e4m3_raw(uint32_t w) {
+  const int32_t t = static_cast<int32_t>(w << (24 - 8 * K));
+  return __uint_as_float(static_cast<uint32_t>(t >> 4) & 0x87F00000u);
+}
+
 // Four fp32 values -> four E4M3 bytes (a in the lowest byte), round to nearest even,
 // saturating at the largest finite value.
 __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {

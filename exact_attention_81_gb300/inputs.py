@@ -150,3 +150,27 @@ def fp8_inputs(B, Nq, Nk, Hq, Hkv, d, seed, device="cpu", descale=0.25):
         per_head = f.repeat_interleave(h // Hkv, dim=1) if h != Hkv else f
         out.append((x / per_head[:, None, :, None]).to(torch.float8_e4m3fn).to(device))
     return (*out, *(f.to(torch.float32).to(device) for f in fs))
+
+
+def kvcache_fp8_inputs(B, Lmax, Hq, Hkv, d, seed, lengths, device="cpu", poison=True,
+                       descale=0.25):
+    """A bf16 query [B,1,Hq,d] and E4M3 caches [B,Lmax,Hkv,d] with descale factors [B, Hkv]:
+    iid N(0, 1) values divided by a per-(batch, kv head) factor (``descale`` times
+    1.0 .. 1.5) and rounded to torch.float8_e4m3fn.  Rows at or past lengths[b] hold the
+    E4M3 NaN code when ``poison`` is set.  Returns (q, k_cache, v_cache, lengths int32,
+    k_descale, v_descale)."""
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    lengths = torch.as_tensor(lengths, dtype=torch.int32).cpu()
+    q = torch.randn((B, 1, Hq, d), generator=g).to(torch.bfloat16)
+    fs = [descale * (1.0 + 0.5 * torch.rand((B, Hkv), generator=g)) for _ in range(2)]
+    caches = []
+    for f in fs:
+        c = torch.empty((B, Lmax, Hkv, d), dtype=torch.uint8)
+        for b in range(B):  # one batch entry at a time bounds the float32 temporary
+            x = torch.randn((Lmax, Hkv, d), generator=g) / f[b][None, :, None]
+            c[b] = x.to(torch.float8_e4m3fn).view(torch.uint8)
+            if poison:
+                c[b, int(lengths[b]):] = 0x7F
+        caches.append(c.view(torch.float8_e4m3fn).to(device))
+    return (q.to(device), caches[0], caches[1], lengths.to(device),
+            fs[0].to(torch.float32).to(device), fs[1].to(torch.float32).to(device))

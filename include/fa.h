@@ -248,6 +248,27 @@ fa_status fa_fwd_kvcache(const void *q, const void *k_cache, const void *v_cache
                          cudaStream_t stream);
 
 /*
+ * Single-query decode over an FP8 KV cache: fa_fwd_kvcache with k_cache / v_cache in E4M3
+ * (torch.float8_e4m3fn bytes, the FP8 format of the FP8 forward pass the capabilities table
+ * of "flash-attention" names) and a bf16 query and output.  Attended values are
+ * k_descale[b * Hkv + g] * K and v_descale[b * Hkv + g] * V for kv head g of sequence b
+ * (DEVICE fp32 [B, Hkv], 4-byte aligned; NULL means 1).  Scores, softmax and O accumulate in
+ * fp32, as in fa_fwd_kvcache; E4M3 values are decoded exactly (NaN codes read as +-480).
+ * d: a multiple of 16 from 16 to 256; cache strides (elements = bytes) multiples of 16.
+ * Windows, softcap, ALiBi and paged caches (ex->block_table) apply as in fa_fwd_kvcache;
+ * an append (ex->k_new) or rotary is FA_ERR_UNSUPPORTED.  Workspace: as fa_fwd_kvcache,
+ * fa_fwd_kvcache_workspace_size(B, Hq, Lmax, d, num_splits) bytes.  Errors as
+ * fa_fwd_kvcache.
+ */
+fa_status fa_fwd_kvcache_fp8(const void *q, const void *k_cache, const void *v_cache,
+                             const int *cache_seqlens, int B, int Lmax, int Hq, int Hkv, int d,
+                             const int64_t cache_strides[3], float scale, int num_splits,
+                             const float *k_descale, const float *v_descale, void *workspace,
+                             size_t workspace_bytes, void *o, float *lse,
+                             const fa_score_mod *mod, const fa_kvcache_extras *ex,
+                             cudaStream_t stream);
+
+/*
  * Split-KV decode that allocates nothing.  Same computation, arguments and outputs as
  * fa_fwd_kvcache with bf16 inputs, minus the workspace.  (The paper has no counterpart: this entry point
  * exists for callers of this library, not for the method.)

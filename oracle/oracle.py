@@ -494,6 +494,52 @@ def e4m3_to_bf16_bits(codes) -> np.ndarray:
     return (bits >> 16).astype(np.uint16)
 
 
+def attention_kvcache_fp8(q, k_cache, v_cache, cache_seqlens, scale: float, k_descale=None,
+                          v_descale=None, nthreads: int | None = None, window=(-1, -1),
+                          softcap=0.0, alibi_slopes=None):
+    """Single-query decode of a bf16 query q [B,1,Hq,d] against E4M3 caches [B,Lmax,Hkv,d]
+    with descale factors per (batch, kv head) ([B, Hkv] fp32, None = 1): the attended keys
+    and values are dk * K and dv * V.  The plain decode definition with the score scale
+    scale * dk on the decoded cache, and O times dv (O is linear in V).  Returns
+    (O [B,Hq,d], LSE [B,Hq]) in float64."""
+    qb = _bits(q)
+    kb, vb = e4m3_to_bf16_bits(k_cache), e4m3_to_bf16_bits(v_cache)
+    lens = np.asarray(cache_seqlens, dtype=np.int32).reshape(-1)
+    B, _, Hq, d = qb.shape
+    Hkv = kb.shape[2]
+    G = Hq // Hkv
+
+    def desc(x):
+        if x is None:
+            return np.ones((B, Hkv), dtype=np.float64)
+        if hasattr(x, "detach"):
+            x = x.detach().cpu().numpy()
+        return np.asarray(x, dtype=np.float32).astype(np.float64).reshape(B, Hkv)
+
+    dk, dv = desc(k_descale), desc(v_descale)
+    slopes = None
+    if alibi_slopes is not None:
+        s_ = alibi_slopes.detach().cpu().numpy() if hasattr(alibi_slopes, "detach") \
+            else np.asarray(alibi_slopes)
+        slopes = np.broadcast_to(s_.astype(np.float32), (B, Hq))
+    o_all = np.empty((B, Hq, d))
+    lse_all = np.empty((B, Hq))
+    for b in range(B):
+        for g in range(Hkv):
+            h0, h1 = g * G, (g + 1) * G  # the query heads of kv head g
+            sigma = float(np.float32(scale)) * dk[b, g]
+            o, lse = attention_kvcache(np.ascontiguousarray(qb[b:b + 1, :, h0:h1]),
+                                       np.ascontiguousarray(kb[b:b + 1, :, g:g + 1]),
+                                       np.ascontiguousarray(vb[b:b + 1, :, g:g + 1]),
+                                       lens[b:b + 1], sigma, nthreads, elem=0, window=window,
+                                       softcap=softcap,
+                                       alibi_slopes=None if slopes is None else
+                                       np.ascontiguousarray(slopes[b, h0:h1]))
+            o_all[b, h0:h1] = o[0] * dv[b, g]
+            lse_all[b, h0:h1] = lse[0]
+    return o_all, lse_all
+
+
 def attention_fp8(q, k, v, scale: float, causal: bool = False, q_descale=None,
                   k_descale=None, v_descale=None, nthreads: int | None = None,
                   window=(-1, -1), softcap=0.0, alibi_slopes=None):

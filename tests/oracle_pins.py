@@ -971,10 +971,45 @@ def pin_fp8_bruteforce(O):
         _close(lse[fin], ref_lse.numpy()[fin], 1e-12, f"fp8 case {n} LSE")
 
 
+def pin_fp8_kvcache_bruteforce(O):
+    """Decode over E4M3 caches against the definition written out in torch float64 on
+    values decoded by torch: for each sequence and query head, scores scale * q.(dk k) over
+    the first cache_seqlens[b] rows of its kv head, softmax, P (dv V); the empty sequence
+    gives O = 0 and LSE = -inf."""
+    for n, (B, Lmax, Hq, Hkv, d, lens) in enumerate(
+            [(3, 9, 4, 2, 16, [5, 9, 0]), (2, 12, 3, 3, 32, [1, 12]), (1, 7, 8, 1, 16, [7])]):
+        k, v = (_e4m3_codes((B, Lmax, Hkv, d), 640 + 2 * n + i) for i in range(2))
+        g = np.random.default_rng(650 + n)
+        q = g.standard_normal((B, 1, Hq, d)).astype(np.float32)
+        qbits = (q.view(np.uint32) >> 16).astype(np.uint16)  # truncated to bf16 bits
+        dk, dv = (g.uniform(0.02, 0.5, size=(B, Hkv)).astype(np.float32) for _ in range(2))
+        scale = 0.4
+        o, lse = O.attention_kvcache_fp8(qbits, k, v, np.array(lens, np.int32), scale, dk, dv)
+        val = lambda c: torch.from_numpy(c).view(torch.float8_e4m3fn).to(torch.float64)
+        qq = torch.from_numpy((qbits.astype(np.uint32) << 16).view(np.float32).astype(np.float64))
+        G = Hq // Hkv
+        for b in range(B):
+            for h in range(Hq):
+                kv = h // G
+                L = lens[b]
+                if L == 0:
+                    assert np.all(o[b, h] == 0.0) and lse[b, h] == -np.inf, "empty sequence"
+                    continue
+                kk = val(k)[b, :L, kv] * float(dk[b, kv])
+                vv = val(v)[b, :L, kv] * float(dv[b, kv])
+                z = (kk @ qq[b, 0, h]) * float(np.float32(scale))
+                ref_lse = torch.logsumexp(z, 0)
+                ref_o = torch.softmax(z, 0) @ vv
+                _close(o[b, h], ref_o.numpy(), 1e-12, f"fp8 decode case {n} O b{b} h{h}")
+                _close(np.array([lse[b, h]]), np.array([float(ref_lse)]), 1e-12,
+                       f"fp8 decode case {n} LSE b{b} h{h}")
+
+
 ALL_PINS = [pin_library, pin_library_fp16, pin_fp16_values, pin_uniform_scores, pin_single_key, pin_constant_v, pin_two_keys,
             pin_empty_rows, pin_hard_max, pin_probs, pin_shift, pin_permutation, pin_gqa,
             pin_varlen, pin_kvcache, pin_rows, pin_recurrence, pin_lse_recompute,
             pin_window_uniform, pin_window_diagonal, pin_window_library, pin_softcap_limits,
             pin_alibi_geometric, pin_alibi_library, pin_mod_bruteforce, pin_mod_paths,
             pin_round16_library, pin_rotary, pin_kv_append, pin_kv_paged, pin_bwd_library,
-            pin_bwd_closed_forms, pin_bwd_modifiers, pin_e4m3_decode, pin_fp8_bruteforce]
+            pin_bwd_closed_forms, pin_bwd_modifiers, pin_e4m3_decode, pin_fp8_bruteforce,
+            pin_fp8_kvcache_bruteforce]

@@ -196,6 +196,33 @@ def test_kvcache_rejects_bad_arguments(lib):
     assert call(mod=ctypes.byref(_mod(alibi_slopes=4096, alibi_batch_stride=-32))) == 1
 
 
+def test_kvcache_fp8_rejects_bad_arguments(lib):
+    strides = (ctypes.c_int64 * 3)(1024 * 8 * 128, 8 * 128, 128)
+
+    def call(**kw):
+        a = dict(q=4096, kc=4096, vc=4096, lens=4096, B=2, L=1024, Hq=32, Hkv=8, d=128,
+                 scale=0.1, ns=0, kd=None, vd=None, ws=4096, wsb=1 << 30, o=4096, lse=4096)
+        a.update(kw)
+        return lib.fa_fwd_kvcache_fp8(a["q"], a["kc"], a["vc"], a["lens"], a["B"], a["L"],
+                                      a["Hq"], a["Hkv"], a["d"], strides, a["scale"], a["ns"],
+                                      a["kd"], a["vd"], a["ws"], a["wsb"], a["o"], a["lse"],
+                                      a.get("mod"), a.get("ex"), None)
+
+    assert call(d=8) == 2                   # E4M3 rows: d a multiple of 16
+    assert call(d=24) == 2
+    assert call(d=272) == 2
+    assert call(Hq=32, Hkv=2) == 2          # group of 16
+    assert call(kd=4098) == 1               # descale pointers 4-byte aligned
+    assert call(vd=4097) == 1
+    assert call(lens=None) == 1
+    assert call(ws=None) == 4
+    assert call(B=0) == 0
+    from exact_attention_81_gb300._binding import KvCacheExtras
+    e = KvCacheExtras()
+    e.k_new, e.v_new = 4096, 4096
+    assert call(ex=ctypes.byref(e)) == 2    # no append into an E4M3 cache
+
+
 def test_workspace_size(lib):
     ws = lib.fa_fwd_kvcache_workspace_size
     # automatic chunking: ~16 splits of a full-length cache, chunk >= 256, multiple of 128

@@ -131,3 +131,76 @@ def test_fp8_full_size_head():
     e_gpu, e_base = np.abs(g - o_ref), np.abs(base - o_ref)
     assert e_gpu.max() <= 2 * e_base.max() + 1e-4 and e_gpu.mean() <= 2 * e_base.mean() + 1e-4
     assert np.abs(lse[0:1, 0:1].double().cpu().numpy() - lse_ref).max() <= 1e-3
+
+
+# ---- decode over E4M3 caches (fa_fwd_kvcache_fp8): the cache is decoded exactly and every
+# product is in fp32, as in the 16-bit decode, so the 16-bit decode bar applies.
+
+def _decode_fp8(d, group, lens, seed, Lmax=3072, Hkv=2, descales=True, num_splits=0, **mod):
+    from exact_attention_81_gb300 import fa_fwd_kvcache_fp8
+    from exact_attention_81_gb300.inputs import kvcache_fp8_inputs
+    from tests.parity_util import compare
+    q, kc, vc, lens, dk, dv = kvcache_fp8_inputs(len(lens), Lmax, Hkv * group, Hkv, d, seed,
+                                                 lens, device=DEV)
+    if not descales:
+        dk = dv = None
+    scale = float(np.float32(1 / math.sqrt(d)))
+    sl = mod.get("alibi_slopes")
+    kw = dict(mod, alibi_slopes=None if sl is None else sl.to(DEV))
+    o, lse = fa_fwd_kvcache_fp8(q, kc, vc, lens, k_descale=dk, v_descale=dv, scale=scale,
+                                num_splits=num_splits, **kw)
+    assert get_last_device_error() == FA_OK
+    o_ref, lse_ref = ORACLE.attention_kvcache_fp8(
+        q.cpu(), kc.cpu(), vc.cpu(), lens.cpu().numpy(), scale,
+        None if dk is None else dk.cpu(), None if dv is None else dv.cpu(),
+        window=mod.get("window_size", (-1, -1)), softcap=mod.get("softcap", 0.0),
+        alibi_slopes=sl)
+    compare(o[:, 0], lse, o_ref, lse_ref, f"fp8 decode d={d} G={group} {mod}")
+    return q, kc, vc, lens, dk, dv, o, lse
+
+
+@pytest.mark.parametrize("d,group", [(128, 4), (128, 8), (128, 1), (64, 2), (96, 4),
+                                     (256, 2), (256, 8), (192, 4), (16, 1)])
+def test_decode_fp8(d, group):
+    _decode_fp8(d, group, [1, 127, 128, 1000, 3071, 0, 513, 3072], 700 + d + group)
+
+
+def test_decode_fp8_without_descales_and_explicit_splits():
+    _decode_fp8(128, 4, [2000, 1, 129, 1024], 760, Lmax=2048, descales=False)
+    _decode_fp8(128, 4, [2000, 1, 129, 1024], 761, Lmax=2048, num_splits=5)
+
+
+@pytest.mark.parametrize("mod", ["window", "softcap", "alibi", "all"])
+def test_decode_fp8_modifiers(mod):
+    slopes = torch.tensor(2.0 ** (-8.0 * np.arange(1, 9) / 8), dtype=torch.float32)
+    kw = {"window": dict(window_size=(700, -1)), "softcap": dict(softcap=15.0),
+          "alibi": dict(alibi_slopes=slopes),
+          "all": dict(window_size=(1500, 0), softcap=4.0, alibi_slopes=slopes)}[mod]
+    _decode_fp8(128, 4, [1, 127, 128, 129, 1000, 3000, 0, 3072], 770, **kw)
+
+
+@pytest.mark.parametrize("d", [128, 256])
+def test_decode_fp8_paged(d):
+    """The same E4M3 caches as shuffled pages of 128 rows through a block table."""
+    from exact_attention_81_gb300 import fa_fwd_kvcache_fp8
+    from exact_attention_81_gb300.inputs import kvcache_fp8_inputs
+    from tests.parity_util import compare
+    B, Lmax, Hq, Hkv, page = 4, 1024, 8, 2, 128
+    lens = [1, 300, 1024, 640]
+    q, kc, vc, lens_t, dk, dv = kvcache_fp8_inputs(B, Lmax, Hq, Hkv, d, 780 + d, lens,
+                                                   device=DEV)
+    nblk = Lmax // page
+    perm = np.random.default_rng(781).permutation(B * nblk + 3)[:B * nblk]
+    table = torch.from_numpy(perm.reshape(B, nblk).astype(np.int32)).to(DEV)
+    pages = []
+    for c in (kc, vc):
+        p8 = torch.zeros((B * nblk + 3, page, Hkv, d), dtype=torch.uint8, device=DEV)
+        p8[table.reshape(-1).long()] = c.view(torch.uint8).reshape(B * nblk, page, Hkv, d)
+        pages.append(p8.view(torch.float8_e4m3fn))
+    scale = float(np.float32(1 / math.sqrt(d)))
+    o, lse = fa_fwd_kvcache_fp8(q, pages[0], pages[1], lens_t, k_descale=dk, v_descale=dv,
+                                scale=scale, block_table=table, window_size=(400, -1))
+    assert get_last_device_error() == FA_OK
+    o_ref, lse_ref = ORACLE.attention_kvcache_fp8(q.cpu(), kc.cpu(), vc.cpu(), np.array(lens),
+                                                  scale, dk.cpu(), dv.cpu(), window=(400, -1))
+    compare(o[:, 0], lse, o_ref, lse_ref, f"fp8 decode paged d={d}")

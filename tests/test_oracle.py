@@ -113,6 +113,14 @@ MUTATIONS = [
      "o_all[b, :, hs] = o[0] * dv[b, 0]", "py"),
     ("FP8 query heads of the wrong group", "hs = slice(g * G, (g + 1) * G)",
      "hs = slice(g, g + G)", "py"),
+    ("FP8 decode K descale ignored", "sigma = float(np.float32(scale)) * dk[b, g]",
+     "sigma = float(np.float32(scale))", "py"),
+    ("FP8 decode V descale dropped", "o_all[b, h0:h1] = o[0] * dv[b, g]",
+     "o_all[b, h0:h1] = o[0]", "py"),
+    ("FP8 decode query heads of the first group", "qb[b:b + 1, :, h0:h1]",
+     "qb[b:b + 1, :, 0:G]", "py"),
+    ("FP8 decode length of the first sequence", "lens[b:b + 1], sigma",
+     "lens[0:1], sigma", "py"),
 ]
 
 
