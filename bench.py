@@ -314,24 +314,48 @@ class DecodeCase:
     """One fa_fwd_kvcache call (split-KV decode + combine); work = bytes of the visible
     K/V prefix, Q, O and LSE (the split partials are overhead, not counted)."""
 
-    def __init__(self, w, dev):
+    def __init__(self, w, dev, e4m3=False):
         import torch
         import exact_attention_81_gb300 as fa
         from exact_attention_81_gb300.inputs import kvcache_workload_inputs
         self.w = w
+        self.e4m3 = e4m3
         self.q, self.kc, self.vc, self.lens = kvcache_workload_inputs(w, device=dev)
+        self.dk = self.dv = None
+        if e4m3:  # the caches divided by a per-(batch, kv head) factor, rounded to E4M3
+            g8 = torch.Generator(device="cpu").manual_seed(w.seed + 100)
+            fk, fv = (0.25 * (1.0 + 0.5 * torch.rand((w.B, w.Hkv), generator=g8))
+                      for _ in range(2))
+            caches = []
+            for c, f in ((self.kc, fk), (self.vc, fv)):
+                c8 = torch.zeros(c.shape, dtype=torch.uint8, device=dev)
+                for b in range(w.B):
+                    n = int(self.lens[b].item())
+                    c8[b, :n] = (c[b, :n].float() / f[b].to(dev)[None, :, None]).to(
+                        torch.float8_e4m3fn).view(torch.uint8)
+                caches.append(c8.view(torch.float8_e4m3fn))
+            self.kc, self.vc = caches
+            self.dk, self.dv = fk.float().to(dev), fv.float().to(dev)
         self.ws = torch.empty(fa.fa_fwd_kvcache_workspace_size(w.B, w.Hq, w.Nk, w.d, 0),
                               dtype=torch.uint8, device=dev)
         self.out = torch.empty_like(self.q)
         self.lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
-        kv = int(self.lens.long().sum().item()) * w.Hkv * w.d * 2 * 2
+        kv = int(self.lens.long().sum().item()) * w.Hkv * w.d * (1 if e4m3 else 2) * 2
         self.work = kv + self.q.numel() * 2 * 2 + self.lse.numel() * 4
         self.launches = 2
 
-    def step(self):
+    def _call(self, q):
         import exact_attention_81_gb300 as fa
-        fa.fa_fwd_kvcache(self.q, self.kc, self.vc, self.lens, workspace=self.ws, out=self.out,
-                          lse=self.lse)
+        if self.e4m3:
+            fa.fa_fwd_kvcache_fp8(q, self.kc, self.vc, self.lens, k_descale=self.dk,
+                                  v_descale=self.dv, workspace=self.ws, out=self.out,
+                                  lse=self.lse)
+        else:
+            fa.fa_fwd_kvcache(q, self.kc, self.vc, self.lens, workspace=self.ws, out=self.out,
+                              lse=self.lse)
+
+    def step(self):
+        self._call(self.q)
 
     def e2e(self):
         """The cache is resident state; each step copies the new queries in and the
@@ -345,8 +369,7 @@ class DecodeCase:
 
         def run():
             dq.copy_(hq, non_blocking=True)
-            fa.fa_fwd_kvcache(dq, self.kc, self.vc, self.lens, workspace=self.ws,
-                              out=self.out, lse=self.lse)
+            self._call(dq)
             ho.copy_(self.out, non_blocking=True)
             hl.copy_(self.lse, non_blocking=True)
         return run, self.q.numel() * 2, self.out.numel() * 2 + self.lse.numel() * 4
@@ -358,16 +381,18 @@ class DecodeCase:
             "metric": DECODE_METRIC, "unit": "GB/s",
             "value": round(job_value(self.work, ms_step, world, 1e9), 1),
             "config": {"workload": f"{w.name}: B={w.B} Hq={w.Hq} Hkv={w.Hkv} cache={w.Nk} "
-                                   f"d={w.d} lengths U[{w.Nk // 32},{w.Nk}] bf16",
+                                   f"d={w.d} lengths U[{w.Nk // 32},{w.Nk}] "
+                                   + ("bf16 query, E4M3 cache" if self.e4m3 else "bf16"),
                        "batch": w.B, "heads": w.Hq, "kv_heads": w.Hkv, "cache_len": w.Nk,
                        "head_dim": w.d, "parallelism": f"replicas x{world}",
                        "l2": f"K/V read {self.work / 1e9:.2f} GB > L2, no flush"},
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"],
                          "unit": "GB/s", "frac": round(gbs / pk["hbm"], 4),
-                         "traffic": profiled_traffic(f"decode_kernel<{w.d},{w.Hq // w.Hkv}>",
-                                                     DECODE_SRC, w.name),
+                         "traffic": None if self.e4m3 else profiled_traffic(
+                             f"decode_kernel<{w.d},{w.Hq // w.Hkv}>", DECODE_SRC, w.name),
                          "peak_basis": f"{pk['basis']} copy bandwidth",
-                         "kernel": f"decode_kernel<{w.d},{w.Hq // w.Hkv}> + combine_kernel"},
+                         "kernel": f"decode_kernel<{w.d},{w.Hq // w.Hkv}"
+                                   + (",e4m3" if self.e4m3 else "") + "> + combine_kernel"},
         }
 
     def e2e_value(self, ms, world):
@@ -385,7 +410,7 @@ def run_ours(args, rank, world, dist):
     pk = peaks()
     w = WORKLOADS[args.workload]
     if w.kind == "kvcache":
-        case = DecodeCase(w, dev)
+        case = DecodeCase(w, dev, e4m3=args.kv_e4m3)
     else:
         case = BwdCase(w, dev) if args.backward else DenseCase(w, dev)
     stream = torch.cuda.current_stream()
@@ -451,7 +476,7 @@ def run_ours(args, rank, world, dist):
     }
     if not args.no_extra:
         result["extra"] = extra_workloads(args, dev, pk, world, dist)
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and not args.kv_e4m3:
         if w.kind == "kvcache":
             result["cpu_baseline"] = cpu_baseline_decode(case, args.cpu_seconds)
         elif args.backward:
@@ -848,6 +873,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--backward", action="store_true",
                     help="time the backward pass (fa_bwd) of the dense workload instead")
+    ap.add_argument("--kv-e4m3", action="store_true",
+                    help="decode workloads: E4M3 caches (fa_fwd_kvcache_fp8) instead of bf16")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -101,13 +101,12 @@ struct Unit {
 };
 
 // Element pair e (elements 2e, 2e + 1) of a 16-byte chunk of a K row as packed fp32: bf16
-// or fp16 halves, or E4M3 bytes as values times 2^-120 (the callers scale q by 2^120).
+// or fp16 halves, or E4M3 bytes.
 template <bool F16, bool F8>
 __device__ __forceinline__ uint64_t kv_pair(const uint32_t (&xs)[4], int e) {
   if constexpr (F8) {
     const uint32_t w = xs[e >> 1];
-    return (e & 1) ? f2_pack(e4m3_raw<2>(w), e4m3_raw<3>(w))
-                   : f2_pack(e4m3_raw<0>(w), e4m3_raw<1>(w));
+    return (e & 1) ? e4m3x2_to_f32x2(w >> 16) : e4m3x2_to_f32x2(w & 0xFFFFu);
   } else {
     return f2_pack(lo_to_f32<F16>(xs[e]), hi_to_f32<F16>(xs[e]));
   }
@@ -244,12 +243,12 @@ __device__ void compute(const DecodeArgs &a, uint8_t *smem, DBars *bars, const W
     if (w.nkeys <= 0) continue;
     const int nblk = (w.nkeys + KB - 1) / KB;
 
-    // E4M3 caches: descale factors of (b, kv head); K's and 2^120 (the raw-byte decode)
-    // go into q, V's into the partial output.
+    // E4M3 caches: descale factors of (b, kv head); K's goes into q, V's into the partial
+    // output.
     float qscale = a.scale_log2, vds = 1.f;
     if constexpr (F8) {
       const int64_t kh = static_cast<int64_t>(w.b) * (a.Hkv >> a.gshift) + (w.g >> a.gshift);
-      qscale *= (a.k_descale ? a.k_descale[kh] : 1.f) * 0x1p120f;
+      qscale *= a.k_descale ? a.k_descale[kh] : 1.f;
       vds = a.v_descale ? a.v_descale[kh] : 1.f;
     }
     // q slice of the G heads of group g in the log2 domain, as pairs (q[d], q[d+1]).
@@ -357,7 +356,7 @@ __device__ void compute(const DecodeArgs &a, uint8_t *smem, DBars *bars, const W
 #pragma unroll
           for (int pass = 0; pass < C::NPASS; ++pass) {
             const float p = ex2_approx(sc[pass][gg] - m_use);
-            pw[(pass * C::KPASS + kl) * G + gg] = F8 ? p * 0x1p120f : p;  // V raw: 2^-120
+            pw[(pass * C::KPASS + kl) * G + gg] = p;
             psum[i] += p;
           }
         }
@@ -397,8 +396,8 @@ __device__ void compute(const DecodeArgs &a, uint8_t *smem, DBars *bars, const W
                 vblk0 + (q4 / C::BOX_ELEMS) * BOX_BYTES + key * 128 + phys * 16 + vbyte % 16;
             if constexpr (F8) {
               const uint32_t x = *reinterpret_cast<const uint32_t *>(src);
-              v01[i] = f2_pack(e4m3_raw<0>(x), e4m3_raw<1>(x));
-              v23[i] = f2_pack(e4m3_raw<2>(x), e4m3_raw<3>(x));
+              v01[i] = e4m3x2_to_f32x2(x & 0xFFFFu);
+              v23[i] = e4m3x2_to_f32x2(x >> 16);
             } else {
               const uint2 x = *reinterpret_cast<const uint2 *>(src);
               v01[i] = f2_pack(lo_to_f32<F16>(x.x), hi_to_f32<F16>(x.x));

@@ -164,8 +164,9 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-// Orders this thread's generic-proxy shared-memory writes before later async-proxy reads
-// (TMA stores / reductions, tcgen05.mma operands).
+// Orders this thread's generic-proxy shared-memory accesses before later async-proxy ones:
+// writes before TMA stores / reductions and tcgen05.mma operand reads, reads before the TMA
+// writes that refill a released buffer.
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -456,18 +457,6 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_addr, uint32_t lbo_
 // ---------------------------------------------------------------------------------------
 // Numeric helpers.
 
-// E4M3 byte K (0..3) of a word -> fp32 with the same sign, exponent and mantissa fields
-// moved into place: the value times 2^-120 (bias 7 -> 127), exact.  E4M3 subnormals
-// become fp32 subnormals, so the products that use these values must not flush them
-// (the callers fold 2^120 into the other factor).  The E4M3 NaN codes (S.1111.111) read
-// as 480 * 2^-120.  An arithmetic shift copies the sign down; the mask keeps the sign and
-// the seven exponent-mantissa bits.
-template <int K>
-__device__ __forceinline__ float e4m3_raw(uint32_t w) {
-  const int32_t t = static_cast<int32_t>(w << (24 - 8 * K));
-  return __uint_as_float(static_cast<uint32_t>(t >> 4) & 0x87F00000u);
-}
-
 // Four fp32 values -> four E4M3 bytes (a in the lowest byte), round to nearest even,
 // saturating at the largest finite value.
 __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
@@ -530,6 +519,21 @@ __device__ __forceinline__ float f16hi_to_f32(uint32_t x) {
   float f;
   asm("{\n.reg .b16 lo, hi;\nmov.b32 {lo, hi}, %1;\ncvt.f32.f16 %0, hi;\n}" : "=f"(f) : "r"(x));
   return f;
+}
+
+// Two E4M3 values (the low 16 bits of w16, element 0 in the low byte) -> packed fp32, exact:
+// E4M3 -> f16x2 (every E4M3 value, subnormals included, is an f16 value), then each half
+// widened to fp32.
+__device__ __forceinline__ uint64_t e4m3x2_to_f32x2(uint32_t w16) {
+  uint32_t h2;
+  asm("{\n"
+      ".reg .b16 l;\n"
+      "cvt.u16.u32 l, %1;\n"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n"
+      "}\n"
+      : "=r"(h2)
+      : "r"(w16));
+  return f2_pack(f16lo_to_f32(h2), f16hi_to_f32(h2));
 }
 
 // The two 16-bit element types of the kernels: bf16 (F16 = false) or fp16 (F16 = true).

@@ -52,7 +52,8 @@ extern "C" {
 typedef enum fa_dtype {
     FA_BF16 = 0, /* bfloat16 */
     FA_FP16 = 1, /* IEEE binary16 */
-    FA_E4M3 = 2  /* 8-bit float E4M3 (torch.float8_e4m3fn): inputs of fa_fwd_fp8 only */
+    FA_E4M3 = 2  /* 8-bit float E4M3 (torch.float8_e4m3fn): the inputs of fa_fwd_fp8, the
+                    caches of fa_fwd_kvcache_fp8 */
 } fa_dtype;
 
 typedef enum fa_status {
@@ -253,7 +254,7 @@ fa_status fa_fwd_kvcache(const void *q, const void *k_cache, const void *v_cache
  * of "flash-attention" names) and a bf16 query and output.  Attended values are
  * k_descale[b * Hkv + g] * K and v_descale[b * Hkv + g] * V for kv head g of sequence b
  * (DEVICE fp32 [B, Hkv], 4-byte aligned; NULL means 1).  Scores, softmax and O accumulate in
- * fp32, as in fa_fwd_kvcache; E4M3 values are decoded exactly (NaN codes read as +-480).
+ * fp32, as in fa_fwd_kvcache; E4M3 values are decoded exactly (a NaN code decodes to NaN).
  * d: a multiple of 16 from 16 to 256; cache strides (elements = bytes) multiples of 16.
  * Windows, softcap, ALiBi and paged caches (ex->block_table) apply as in fa_fwd_kvcache;
  * an append (ex->k_new) or rotary is FA_ERR_UNSUPPORTED.  Workspace: as fa_fwd_kvcache,
