@@ -657,30 +657,6 @@ cudaError_t launch_append(bool f16, const AppendArgs &a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-int decode_smem_bytes(int d, int group) {
-  if (d == 256) {  // groups of 8 run as two work items of 4 heads (DecodeArgs::gshift)
-    switch (group) {
-      case 1: return DCfg<256, 1>::SMEM_BYTES;
-      case 2: return DCfg<256, 2>::SMEM_BYTES;
-      default: return DCfg<256, 4>::SMEM_BYTES;
-    }
-  }
-  if (d == 64) {
-    switch (group) {
-      case 1: return DCfg<64, 1>::SMEM_BYTES;
-      case 2: return DCfg<64, 2>::SMEM_BYTES;
-      case 4: return DCfg<64, 4>::SMEM_BYTES;
-      default: return DCfg<64, 8>::SMEM_BYTES;
-    }
-  }
-  switch (group) {
-    case 1: return DCfg<128, 1>::SMEM_BYTES;
-    case 2: return DCfg<128, 2>::SMEM_BYTES;
-    case 4: return DCfg<128, 4>::SMEM_BYTES;
-    default: return DCfg<128, 8>::SMEM_BYTES;
-  }
-}
-
 template <bool F16>
 cudaError_t launch_decode_typed(int d, int group, const CUtensorMap &tk, const CUtensorMap &tv,
                                 const DecodeArgs &a, int grid, cudaStream_t stream) {

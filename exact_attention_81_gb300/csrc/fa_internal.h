@@ -214,8 +214,7 @@ cudaError_t launch_bwd_post(int d, bool f16, const float *dq_acc, float scale, v
 cudaError_t launch_zero16(void *x, int B, int N, int H, int d, const int64_t st[3],
                           cudaStream_t stream);
 
-// Shared-memory bytes the kernels request (for host-side checks).
+// Shared-memory bytes the prefill kernel requests (for host-side checks).
 int prefill_smem_bytes(int d);
-int decode_smem_bytes(int d, int group);
 
 }  // namespace fa

@@ -1,12 +1,14 @@
 """GPU parity of the FP8 forward (fa_fwd_fp8: E4M3 Q, K, V with per-(batch, kv head)
-descale factors, bf16 O) against the fp64 oracle.
+descale factors, bf16 O) and of the decode call over E4M3 caches (fa_fwd_kvcache_fp8)
+against the fp64 oracle.
 
 The pages fix no tolerance for FP8.  The bar is their own test criterion ("flash-attention",
 section 5, tests): the kernel's O error is at most twice that of a PyTorch baseline in the
 input precision (+1e-4) -- fp32 scores and softmax of the decoded inputs, P rounded to E4M3
 for the P V product (the kernel's only 8-bit rounding besides the inputs), normalised by the
 fp32 row sum -- both in the maximum and in the mean; the LSE, computed from unrounded scores
-on both sides, within 1e-3."""
+on both sides, within 1e-3.  The decode over E4M3 caches rounds nothing beyond its inputs,
+so it takes the 16-bit decode bar (tests.parity_util)."""
 import math
 
 import numpy as np
