@@ -100,9 +100,61 @@ def profiled_traffic(kernel: str, src_files, workload: str):
     return None
 
 
+class _Nvml:
+    """Read-only NVML queries through ctypes (SM clock, its maximum, power, clock-event
+    reasons), or None attributes when the library is missing."""
+
+    # clock-event reason bits (nvml.h: nvmlClocksEventReason*)
+    REASONS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+               "hw_thermal_slowdown": 0x40}
+
+    def __init__(self, index: int, pci_bus_id: str | None = None):
+        import ctypes
+        self.ok = False
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            # the CUDA device by its PCI address (NVML numbers GPUs its own way), else by index
+            if not pci_bus_id or lib.nvmlDeviceGetHandleByPciBusId_v2(
+                    pci_bus_id.encode(), ctypes.byref(h)) != 0:
+                if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(h)) != 0:
+                    return
+            self.lib, self.h, self.ct = lib, h, ctypes
+            reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+            self.reasons_fn = reasons or lib.nvmlDeviceGetCurrentClocksThrottleReasons
+            v = ctypes.c_uint()
+            self.max_mhz = (float(v.value) if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(v))
+                            == 0 else None)
+            self.ok = True
+        except Exception:
+            self.ok = False
+
+    def sample(self):
+        """(sm MHz, power W, reason bits) now."""
+        ct = self.ct
+        mhz, mw, bits = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        self.lib.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(mhz))  # NVML_CLOCK_SM
+        self.lib.nvmlDeviceGetPowerUsage(self.h, ct.byref(mw))
+        self.reasons_fn(self.h, ct.byref(bits))
+        return float(mhz.value), mw.value / 1000.0, int(bits.value)
+
+
+def _pci_bus_id(index: int):
+    """PCI address of CUDA device `index` in NVML's form, or None."""
+    try:
+        import torch
+        p = torch.cuda.get_device_properties(index)
+        return f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
+    except Exception:
+        return None
+
+
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason sampling in the background (25 ms period: the
-    timed region of a default run lasts well under a second)."""
+    """SM clock and clock-event reasons sampled in the background while the timed region
+    runs: NVML every millisecond (so that a timed region of a few tens of milliseconds
+    still gets tens of samples), else nvidia-smi every 25 ms."""
 
     QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -110,11 +162,18 @@ class ClockSampler:
 
     def __init__(self, index: int):
         self.index = index
-        self.samples = []
+        self.samples = []  # (time, sm MHz, max MHz, set of reasons)
         self.proc = None
         self.thread = None
+        self.stop_flag = threading.Event()
+        self.nvml = _Nvml(index, _pci_bus_id(index))
+        self.source = "nvml 1 ms" if self.nvml.ok else "nvidia-smi 25 ms"
 
     def start(self):
+        if self.nvml.ok:
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
+            return
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
@@ -126,31 +185,48 @@ class ClockSampler:
         self.thread = threading.Thread(target=self._read, daemon=True)
         self.thread.start()
 
+    def _poll(self):
+        names = _Nvml.REASONS
+        while not self.stop_flag.is_set():
+            try:
+                mhz, _, bits = self.nvml.sample()
+            except Exception:
+                break
+            self.samples.append((time.time(), mhz, self.nvml.max_mhz or mhz,
+                                 {n for n, b in names.items() if bits & b}))
+            time.sleep(0.001)
+
     def _read(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in self.proc.stdout:
-            self.samples.append((time.time(), line.strip()))
+            parts = [p.strip() for p in line.strip().split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                mhz, mx = float(parts[2]), float(parts[3])
+            except ValueError:
+                continue
+            self.samples.append((time.time(), mhz, mx,
+                                 {n for n, v in zip(names, parts[6:10])
+                                  if v.lower().startswith("active")}))
 
     def stop(self):
+        self.stop_flag.set()
         if self.proc is not None:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except Exception:
                 self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
 
     def summary(self, t0: float, t1: float):
-        rows = []
-        for ts, line in self.samples:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 10:
-                continue
-            try:
-                rows.append((ts, float(parts[2]), float(parts[3]), parts))
-            except ValueError:
-                continue
+        rows = list(self.samples)
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "window": "none"}
-        inside = [r for r in rows if t0 <= r[0] <= t1 + 0.03]
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"],
+                    "window": "none", "source": self.source}
+        inside = [r for r in rows if t0 <= r[0] <= t1]
         window = "timed"
         if not inside:
             after = [r for r in rows if r[0] >= t0]
@@ -158,13 +234,11 @@ class ClockSampler:
             window = "nearest"
         mhz = sorted(r[1] for r in inside)
         reasons = set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in inside:
-            for name, val in zip(names, r[3][6:10]):
-                if val.lower().startswith("active"):
-                    reasons.add(name)
+            reasons |= r[3]
         return {"sm_mhz": mhz[len(mhz) // 2], "sm_max_mhz": max(r[2] for r in inside),
-                "reasons": sorted(reasons), "samples": len(inside), "window": window}
+                "sm_min_mhz": mhz[0], "reasons": sorted(reasons), "samples": len(inside),
+                "window": window, "source": self.source}
 
 
 # ----------------------------------------------------------------------------- GPU arm

@@ -15,6 +15,7 @@ from ._binding import (  # noqa: F401
     FA_ERR_CUDA,
     FA_ERR_INVALID_ARG,
     FA_ERR_TIMEOUT,
+    FA_ERR_CONCURRENT,
     FA_ERR_UNSUPPORTED,
     FA_ERR_WORKSPACE,
     FA_OK,

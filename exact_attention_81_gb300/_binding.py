@@ -24,6 +24,7 @@ FA_ERR_UNSUPPORTED = 2
 FA_ERR_CUDA = 3
 FA_ERR_WORKSPACE = 4
 FA_ERR_TIMEOUT = 5
+FA_ERR_CONCURRENT = 6
 
 FA_BF16 = 0
 FA_FP16 = 1

@@ -293,6 +293,9 @@ const char *fa_status_string(fa_status s) {
     case FA_ERR_CUDA: return "FA_ERR_CUDA: CUDA call failed";
     case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE: workspace missing or too small";
     case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a device-side wait gave up";
+    case FA_ERR_CONCURRENT:
+      return "FA_ERR_CONCURRENT: a launch shared its tile-ticket counter with another launch "
+             "running at the same time";
   }
   return "unknown fa_status";
 }
@@ -745,12 +748,15 @@ fa_status kvcache_call(const void *q, const void *k_cache, const void *v_cache,
     return FA_ERR_INVALID_ARG;
   if (!head_dim_ok(d, kMaxDecodeD)) return FA_ERR_UNSUPPORTED;
   if (kv_e4m3 && (d < 16 || d % 16 != 0)) return FA_ERR_UNSUPPORTED;
+  // The query heads of one kv head (any group size) run as nsplit work items of G heads,
+  // G the largest of 8, 4, 2, 1 that divides the group (at most 4 at width 256, where more
+  // heads' state would spill).  The items of one kv head stream the same K/V rows at about
+  // the same time, so the repeated reads are mostly served by L2.
   const int group = Hq / Hkv;
-  if (group != 1 && group != 2 && group != 4 && group != 8) return FA_ERR_UNSUPPORTED;
-  // At width 256 a group of 8 query heads runs as two work items of 4 heads that stream the
-  // same K/V rows (the second read is mostly served by L2): 8 heads' state would spill.
   const int kd = kv_e4m3 ? fa::kernel_d_e4m3(d) : fa::kernel_d(d);
-  const int gshift = kd == 256 && group == 8 ? 1 : 0;
+  int G = kd == 256 ? 4 : 8;
+  while (group % G != 0) G /= 2;
+  const int nsplit = group / G;
   if (!dtype_ok(dtype) || (kv_e4m3 && dtype != FA_BF16)) return FA_ERR_UNSUPPORTED;
   if (!aligned(k_descale, 4) || !aligned(v_descale, 4)) return FA_ERR_INVALID_ARG;
   if (!scale_ok(scale)) return FA_ERR_INVALID_ARG;
@@ -815,12 +821,12 @@ fa_status kvcache_call(const void *q, const void *k_cache, const void *v_cache,
     const int Leff = mod.wl >= 0 ? std::min<int64_t>(Lmax, static_cast<int64_t>(mod.wl) + kalign)
                                  : Lmax;
     if (num_splits == 0)
-      chunk = auto_chunk(Leff, static_cast<int64_t>(B) * (Hkv << gshift), dev->sm_count, maxch);
+      chunk = auto_chunk(Leff, static_cast<int64_t>(B) * Hkv * nsplit, dev->sm_count, maxch);
     maxch = ceil_div(Leff, chunk);
     o_part = static_cast<float *>(workspace);
     lse_part = o_part + static_cast<int64_t>(B) * Hq * maxch * fa::kernel_d(d);
   }
-  const int64_t units = static_cast<int64_t>(maxch) * B * (Hkv << gshift);
+  const int64_t units = static_cast<int64_t>(maxch) * B * Hkv * nsplit;
   if (units > INT32_MAX) return FA_ERR_INVALID_ARG;
   if (Lmax > 0) {
     CUtensorMap tk, tv;
@@ -870,13 +876,14 @@ fa_status kvcache_call(const void *q, const void *k_cache, const void *v_cache,
     da.lse_part = lse_part;
     da.B = B;
     da.Hq = Hq;
-    da.Hkv = Hkv << gshift;
-    da.gshift = gshift;
+    da.Hkv = Hkv * nsplit;
+    da.nsplit = nsplit;
     da.Lmax = Lmax;
     da.chunk = chunk;
     da.maxch = maxch;
     da.d = d;
     da.num_units = static_cast<int>(units);
+    da.sched_slot = fa::next_decode_sched_slot();
     da.scale_log2 = scale_log2(scale);
     da.err = dev->err;
     da.timeout_ns = g_timeout_ns;
@@ -899,7 +906,7 @@ fa_status kvcache_call(const void *q, const void *k_cache, const void *v_cache,
     da.v_descale = kv_e4m3 ? v_descale : nullptr;
     da.ostride = fa::kernel_d(d);
     const int grid = static_cast<int>(units < dev->sm_count ? units : dev->sm_count);
-    cudaError_t e = fa::launch_decode(kd, group >> gshift, dtype == FA_FP16, kv_e4m3, tk, tv,
+    cudaError_t e = fa::launch_decode(kd, G, dtype == FA_FP16, kv_e4m3, tk, tv,
                                       da, grid, stream);
     if (e != cudaSuccess) return cuda_fail("decode kernel launch", e);
   }
@@ -1193,6 +1200,7 @@ fa_status fa_get_last_device_error(cudaStream_t stream) {
   if (word & (fa::DEVERR_BAD_CU_SEQLENS | fa::DEVERR_BAD_CACHE_LEN | fa::DEVERR_BAD_APPEND |
               fa::DEVERR_BAD_BLOCK_TABLE))
     return FA_ERR_INVALID_ARG;
+  if (word & fa::DEVERR_SCHED_OVERLAP) return FA_ERR_CONCURRENT;
   return FA_OK;
 }
 

@@ -29,6 +29,7 @@
 //
 // The combine kernel merges the partials of each (b, query head):
 //   LSE = log sum_s exp(LSE_s),  O = sum_s exp(LSE_s - LSE) O_s.
+#include <atomic>
 #include <cmath>
 
 #include "fa_internal.h"
@@ -89,12 +90,24 @@ struct DCfg {
   static_assert((DQ <= 32 && (32 % DQ) == 0) || DQ % 32 == 0, "d quads must tile a warp");
 };
 
+constexpr int SCHED_DEPTH = 4;     // units in flight between the scheduler and the compute warps
+constexpr int NUM_SCHED_SLOTS = 256;
+
+// Per-launch unit-ticket counters: [slot][0] = next ticket, [slot][1] = CTAs finished.  The
+// host gives each launch its own slot (round robin); the last CTA of a launch to finish
+// checks that the launch took exactly its own tickets and resets the slot for its next user.
+__device__ unsigned int g_dsched[NUM_SCHED_SLOTS][2];
+
 struct DBars {
   uint64_t full[12], empty[12];
+  uint64_t sched_full[SCHED_DEPTH], sched_empty[SCHED_DEPTH];
+  int sched_unit[SCHED_DEPTH];
   uint64_t sync;  // group barrier of the 256 compute threads (bounded wait)
   float m[8][8], l[8][8];  // [warp][head] running max / sum at the end of a unit
   int abort;
 };
+
+static_assert(sizeof(DBars) <= 1024, "decode barriers exceed their shared-memory region");
 
 struct Unit {
   int b, g, c, len, key0, nkeys;
@@ -117,7 +130,8 @@ __device__ __forceinline__ int first_visible(int len, int wl) {
   return wl >= 0 ? max(len - 1 - wl, 0) : 0;
 }
 
-// Unit u = (chunk c, batch b, kv head g).  Chunks tile the keys [first, len) from the
+// Unit u = (chunk c, batch b, work item g); work item g serves query heads
+// [g G, g G + G) of kv head g / nsplit.  Chunks tile the keys [first, len) from the
 // first visible key on (rounded down to a page-safe multiple of 128 for paged caches), so
 // a window only moves the start.  len counts an appended row.
 __device__ __forceinline__ Unit unit_of(const DecodeArgs &a, int u) {
@@ -139,22 +153,46 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const 
   return __all_sync(0xffffffffu, ok);
 }
 
-// TMA producer: the whole warp runs the loop and its waits, lane 0 issues the loads (a
-// loop confined to one lane issues late next to the compute warps: 1.7 % of bandwidth).
+// Scheduler and TMA producer: the whole warp runs the loop and its waits, lane 0 takes the
+// tickets and issues the loads (a loop confined to one lane issues late next to the compute
+// warps: 1.7 % of bandwidth).  Units are claimed from the launch's ticket counter, so a CTA
+// that drew short units takes more of them; units without keys are skipped here and never
+// reach the compute warps.  Each claimed unit goes to the compute warps through the
+// scheduler ring (-1 = no more), then its K and V blocks through the load ring.
 template <int D, int G, bool F8, bool MOD>
 __device__ void producer(const DecodeArgs &a, const CUtensorMap *tmk, const CUtensorMap *tmv,
                          uint8_t *smem, DBars *bars, const WaitCtl &wc, int lane) {
   using C = DCfg<D, G, F8>;
   uint32_t it = 0;
+  unsigned int *ctr = g_dsched[a.sched_slot];
   const uint64_t policy = policy_evict_first();  // every cache byte is read once
   if (a.inject) goto out;  // failure injection: load nothing, the consumers' waits run out
-  for (int u = blockIdx.x; u < a.num_units; u += gridDim.x) {
-    const Unit w = unit_of(a, u);
-    if (w.c == 0 && w.g == 0) {
-      const int len_raw = a.cache_len[w.b] + a.len_add;
-      if (lane == 0 && (len_raw < 0 || len_raw > a.Lmax)) atomicOr(a.err, DEVERR_BAD_CACHE_LEN);
+  for (uint32_t k = 0;; ++k) {
+    int unit = -1;
+    while (true) {
+      unsigned int t = 0;
+      if (lane == 0) t = atomicAdd(&ctr[0], 1u);
+      t = __shfl_sync(0xffffffffu, t, 0);
+      if (t >= static_cast<unsigned int>(a.num_units)) break;
+      const Unit w = unit_of(a, static_cast<int>(t));
+      if (w.c == 0 && w.g == 0) {
+        const int len_raw = a.cache_len[w.b] + a.len_add;
+        if (lane == 0 && (len_raw < 0 || len_raw > a.Lmax)) atomicOr(a.err, DEVERR_BAD_CACHE_LEN);
+      }
+      if (w.nkeys > 0) {
+        unit = static_cast<int>(t);
+        break;
+      }
     }
-    if (w.nkeys <= 0) continue;
+    const int rs = static_cast<int>(k % SCHED_DEPTH);
+    if (!warp_wait(&bars->sched_empty[rs], ((k / SCHED_DEPTH) & 1u) ^ 1u, wc)) goto out;
+    if (lane == 0) {
+      bars->sched_unit[rs] = unit;
+      mbar_arrive(&bars->sched_full[rs]);
+    }
+    __syncwarp();
+    if (unit < 0) break;
+    const Unit w = unit_of(a, unit);
     const int nblk = (w.nkeys + KB - 1) / KB;
     for (int blk = 0; blk < nblk; ++blk) {
 #pragma unroll
@@ -177,8 +215,7 @@ __device__ void producer(const DecodeArgs &a, const CUtensorMap *tmk, const CUte
           for (int cc = 0; cc < C::KCH; ++cc)
             tma_load_4d_hint(smem + C::RING_OFF + slot * C::BLOCK_BYTES + cc * BOX_BYTES,
                              which ? tmv : tmk, &bars->full[slot], cc * C::BOX_ELEMS,
-                             w.g >> a.gshift,
-                             row, outer, policy);
+                             w.g / a.nsplit, row, outer, policy);
         }
         __syncwarp();
         ++it;
@@ -186,6 +223,21 @@ __device__ void producer(const DecodeArgs &a, const CUtensorMap *tmk, const CUte
     }
   }
 out:
+  // This CTA takes no more tickets (it reached the end, or gave up): count it as finished.
+  // Every CTA takes exactly one ticket past the last unit, so the launch took num_units +
+  // gridDim.x tickets in all; another count means that another launch ran on the same slot
+  // at the same time (or a CTA gave up, which sets its own error bit).  The last CTA to
+  // finish resets the slot for its next launch.
+  if (lane == 0) {
+    __threadfence();
+    if (atomicAdd(&ctr[1], 1u) == gridDim.x - 1) {
+      const unsigned int taken = atomicAdd(&ctr[0], 0u);
+      if (!a.inject && taken != static_cast<unsigned int>(a.num_units) + gridDim.x)
+        atomicOr(a.err, DEVERR_SCHED_OVERLAP);
+      atomicExch(&ctr[0], 0u);
+      atomicExch(&ctr[1], 0u);
+    }
+  }
   for (int s = 0; s < C::NSLOTS; ++s) {
     if (it > static_cast<uint32_t>(s)) {
       const uint32_t uses = (it - 1 - s) / C::NSLOTS + 1;
@@ -238,16 +290,22 @@ __device__ void compute(const DecodeArgs &a, uint8_t *smem, DBars *bars, const W
   const bool alibi = MOD && a.alibi != nullptr;
   uint32_t it = 0, sync_phase = 0;
 
-  for (int u = blockIdx.x; u < a.num_units; u += gridDim.x) {
+  for (uint32_t k = 0;; ++k) {
+    // Next unit from the scheduler ring (one arrival per warp frees the entry).
+    const int rs = static_cast<int>(k % SCHED_DEPTH);
+    if (!warp_wait(&bars->sched_full[rs], (k / SCHED_DEPTH) & 1u, wc)) return;
+    const int u = bars->sched_unit[rs];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars->sched_empty[rs]);
+    if (u < 0) break;
     const Unit w = unit_of(a, u);
-    if (w.nkeys <= 0) continue;
     const int nblk = (w.nkeys + KB - 1) / KB;
 
     // E4M3 caches: descale factors of (b, kv head); K's goes into q, V's into the partial
     // output.
     float qscale = a.scale_log2, vds = 1.f;
     if constexpr (F8) {
-      const int64_t kh = static_cast<int64_t>(w.b) * (a.Hkv >> a.gshift) + (w.g >> a.gshift);
+      const int64_t kh = static_cast<int64_t>(w.b) * (a.Hkv / a.nsplit) + w.g / a.nsplit;
       qscale *= a.k_descale ? a.k_descale[kh] : 1.f;
       vds = a.v_descale ? a.v_descale[kh] : 1.f;
     }
@@ -508,6 +566,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(&bars->full[s], 1);
       mbar_init(&bars->empty[s], NCOMPUTE / 32);
     }
+    for (int i = 0; i < SCHED_DEPTH; ++i) {
+      mbar_init(&bars->sched_full[i], 1);
+      mbar_init(&bars->sched_empty[i], NCOMPUTE / 32);  // one arrival per compute warp
+    }
     mbar_init(&bars->sync, NCOMPUTE);
     bars->abort = 0;
     fence_barrier_init();
@@ -648,6 +710,11 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
 
 }  // namespace
 
+int next_decode_sched_slot() {
+  static std::atomic<unsigned int> seq{0};
+  return static_cast<int>(seq.fetch_add(1u) % NUM_SCHED_SLOTS);
+}
+
 cudaError_t launch_append(bool f16, const AppendArgs &a, cudaStream_t stream) {
   if (a.B == 0) return cudaSuccess;
   if (f16)
@@ -660,7 +727,9 @@ cudaError_t launch_append(bool f16, const AppendArgs &a, cudaStream_t stream) {
 template <bool F16>
 cudaError_t launch_decode_typed(int d, int group, const CUtensorMap &tk, const CUtensorMap &tv,
                                 const DecodeArgs &a, int grid, cudaStream_t stream) {
-  if (d == 256) {  // groups of 8 run as two work items of 4 heads (DecodeArgs::gshift)
+  // group: the heads of one work item (DecodeArgs::nsplit items per kv head); at d = 256
+  // at most 4.
+  if (d == 256) {
     switch (group) {
       case 1: return launch_decode_impl<256, 1, F16>(tk, tv, a, grid, stream);
       case 2: return launch_decode_impl<256, 2, F16>(tk, tv, a, grid, stream);
@@ -686,7 +755,7 @@ cudaError_t launch_decode_typed(int d, int group, const CUtensorMap &tk, const C
 // E4M3 caches with a bf16 query: widths 128 and 256 (a 128-byte box row holds 128 elements).
 cudaError_t launch_decode_e4m3(int d, int group, const CUtensorMap &tk, const CUtensorMap &tv,
                                const DecodeArgs &a, int grid, cudaStream_t stream) {
-  if (d == 256) {  // groups of 8 run as two work items of 4 heads (DecodeArgs::gshift)
+  if (d == 256) {  // at most 4 heads per work item (DecodeArgs::nsplit)
     switch (group) {
       case 1: return launch_decode_impl<256, 1, false, true>(tk, tv, a, grid, stream);
       case 2: return launch_decode_impl<256, 2, false, true>(tk, tv, a, grid, stream);

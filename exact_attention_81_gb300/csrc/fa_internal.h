@@ -18,6 +18,8 @@ enum : unsigned int {
   DEVERR_BAD_APPEND = 16u,      // no room for an appended row / position past the tables
   DEVERR_BAD_BLOCK_TABLE = 32u, // a block-table entry outside [0, num_pages)
   DEVERR_BWD_TIMEOUT = 64u,     // a bounded wait in the backward kernel gave up
+  DEVERR_SCHED_OVERLAP = 128u,  // a launch's ticket counter was shared with another launch
+                                // running at the same time (tickets taken != expected)
 };
 
 // Arguments of the fused prefill kernel (dense and varlen share it).
@@ -62,6 +64,9 @@ enum PrefillMask : int {
 // Tile-ticket counter slot for the next prefill launch (round robin over the slots).
 int next_prefill_sched_slot();
 
+// Unit-ticket counter slot for the next decode launch (round robin over the slots).
+int next_decode_sched_slot();
+
 // f16: inputs and output are fp16 instead of bf16.
 cudaError_t launch_prefill(int d, int mask, bool f16, const CUtensorMap &tq,
                            const CUtensorMap &tk, const CUtensorMap &tv, const PrefillArgs &a,
@@ -90,14 +95,16 @@ struct DecodeArgs {
   float *o_part;              // [B*Hq, maxch, d] fp32 partial outputs (normalised per chunk)
   float *lse_part;            // [B*Hq, maxch] fp32 partial LSE (natural log)
   int B, Hq, Lmax;
-  int Hkv;                    // work-item heads: kv heads << gshift
-  int gshift;                 // each kv head's query group is split into 1 << gshift work
-                              // items of G = group >> gshift heads (d = 256, group 8: G = 4,
-                              // whose q, scores and accumulators fit in registers)
+  int Hkv;                    // work items per batch entry: kv heads * nsplit
+  int nsplit;                 // each kv head's query group runs as nsplit work items of the
+                              // kernel's G heads (group = nsplit * G; G <= 8, and <= 4 at
+                              // d = 256, whose q, scores and accumulators must fit in
+                              // registers); the items of one kv head stream the same K/V rows
   int chunk;                  // keys per split (multiple of 128)
   int maxch;                  // chunks of the longest visible range: ceil(Leff / chunk)
   int d;                      // head dimension of q and the caches (<= the kernel's D)
-  int num_units;              // maxch * B * Hkv (work-item heads)
+  int num_units;              // maxch * B * Hkv (work items)
+  int sched_slot;             // this launch's unit-ticket counter slot
   float scale_log2;
   unsigned int *err;
   unsigned long long timeout_ns;

@@ -52,8 +52,9 @@ extern "C" fa_status fa_fwd_kvcache_noalloc(const void *q, const void *k_cache,
                                             const int64_t cache_strides[3], float scale,
                                             int num_splits, void *o, float *lse,
                                             cudaStream_t stream) {
+  // Sizes, head dimension and pointers are validated by fa_fwd_kvcache; only the scratch
+  // bound is checked here, before the array's address is looked up.
   if (B < 0 || Lmax < 0 || Hq <= 0 || Hkv <= 0 || num_splits < 0) return FA_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   if (B == 0) return FA_OK;
   const size_t need = Lmax > 0 ? fa_fwd_kvcache_workspace_size(B, Hq, Lmax, d, num_splits) : 0;
   if (need > static_cast<size_t>(FA_NOALLOC_SCRATCH_BYTES)) return FA_ERR_WORKSPACE;

@@ -345,9 +345,15 @@ __device__ void producer_role(const PrefillArgs &a, const CUtensorMap *tmq,
   }
 out:
   // This CTA takes no more tickets (it reached the end, or gave up): count it as finished.
-  // The last CTA of the launch to finish resets the counters for the slot's next launch.
+  // Every CTA takes exactly one ticket past the last tile, so the launch took num_tiles +
+  // gridDim.x tickets in all; another count means that another launch ran on the same slot
+  // at the same time (or a CTA gave up, which sets its own error bit).  The last CTA of the
+  // launch to finish resets the counters for the slot's next launch.
   __threadfence();
   if (atomicAdd(&ctr[1], 1u) == gridDim.x - 1) {
+    const unsigned int taken = atomicAdd(&ctr[0], 0u);
+    if (!a.inject && taken != static_cast<unsigned int>(a.num_tiles) + gridDim.x)
+      atomicOr(a.err, DEVERR_SCHED_OVERLAP);
     atomicExch(&ctr[0], 0u);
     atomicExch(&ctr[1], 0u);
   }

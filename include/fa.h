@@ -60,13 +60,30 @@ typedef enum fa_status {
     FA_OK = 0,
     FA_ERR_INVALID_ARG = 1, /* null pointer, bad size, Hq % Hkv != 0, misaligned pointer/stride */
     FA_ERR_UNSUPPORTED = 2, /* d not a multiple of 8 in [8, 256] (forward and decode calls)
-                               or [8, 128] (backward), dtype not a fa_dtype,
-                               decode group size not in {1,2,4,8}, or the current device is
-                               not an sm_103 GPU */
+                               or [8, 128] (backward), dtype not a fa_dtype, or the current
+                               device is not an sm_103 GPU */
     FA_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed: see fa_last_cuda_error() */
     FA_ERR_WORKSPACE = 4,   /* workspace pointer null or smaller than required */
-    FA_ERR_TIMEOUT = 5      /* a device-side wait gave up (reported by fa_get_last_device_error) */
+    FA_ERR_TIMEOUT = 5,     /* a device-side wait gave up (reported by fa_get_last_device_error) */
+    FA_ERR_CONCURRENT = 6   /* reported by fa_get_last_device_error: a forward or decode launch
+                               found its work-ticket counter shared with another launch running
+                               at the same time (see "Work tickets" below); its outputs are not
+                               valid */
 } fa_status;
+
+/*
+ * Work tickets.  The forward (fa_fwd, fa_fwd_varlen, fa_fwd_fp8, fa_fwd_host) and decode
+ * (fa_fwd_kvcache*, fa_fwd_kvcache_noalloc) kernels hand out their work tiles dynamically:
+ * the CTAs of a launch take tickets from a counter in a 256-entry table compiled into the
+ * library, one table per call kind, and the host gives each launch the next entry in turn
+ * (the entry is fixed when the call is made, so a captured CUDA graph replays with the
+ * entry it was captured with).  Two launches that use the same entry must not run at the
+ * same time: do not replay one captured call concurrently with itself (on two streams, or
+ * from two graphs running at once), and keep fewer than 256 forward (or decode) launches in
+ * flight at once.  Launches on one stream never overlap.  A launch that finds its counter
+ * disturbed by another sets FA_ERR_CONCURRENT in the device error word (a check made when
+ * its last CTA finishes; it catches a shared entry in most cases, not in every case).
+ */
 
 /*
  * Score modifiers: the sliding window, softcap and ALiBi variants named in the
@@ -187,7 +204,9 @@ fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, fl
  *                  256-byte aligned; owned by the caller, overwritten by the call.
  *   o            : [B, 1, Hq, d] bf16 output, contiguous
  *   lse          : [B, Hq] fp32 output, contiguous
- * Hq / Hkv must be 1, 2, 4 or 8.  dtype is the fa_dtype of q, the caches and o.
+ * Hkv must divide Hq (any group size: the query heads of one kv head are evaluated
+ * together in work items of up to 8 heads, 4 at d > 128, that share the K/V stream).
+ * dtype is the fa_dtype of q, the caches and o.
  * mod: score modifiers (NULL = none; host memory, read during the call).  Only the left
  * window bound can hide a cached key (the query is the last position); cache rows before
  * the window start take no part in the result.  ex: append / rotary / paged cache
@@ -270,9 +289,11 @@ fa_status fa_fwd_kvcache_fp8(const void *q, const void *k_cache, const void *v_c
                              cudaStream_t stream);
 
 /*
- * Split-KV decode that allocates nothing.  Same computation, arguments and outputs as
- * fa_fwd_kvcache with bf16 inputs, minus the workspace.  (The paper has no counterpart: this entry point
- * exists for callers of this library, not for the method.)
+ * Split-KV decode that allocates nothing.  Same computation, arguments, outputs and limits
+ * (head dimensions 8..256, every group size fa_fwd_kvcache takes) as fa_fwd_kvcache with
+ * bf16 inputs and no score modifiers or extras, minus the workspace; with the same
+ * num_splits the two calls return the same bits.  (The paper has no counterpart: this
+ * entry point exists for callers of this library, not for the method.)
  *
  * Some callers cannot allocate device memory at call time and have no buffer set aside
  * to pass as a workspace -- for example code running as a plugin inside another runtime

@@ -5,16 +5,21 @@ pass is held to: max|O - O_ref| <= 1e-2, mean|O - O_ref| <= 1e-3 and
 max|LSE - LSE_ref| <= 1e-3, with O_ref and LSE_ref from the fp64 oracle on the same
 bf16 inputs.  Rows that see no key must give O = 0 exactly and LSE = -inf.
 
-The O bounds are charged with the error of the computation, not with the rounding of the
-exact result to the 16-bit output: per element, half an ulp of the output type at
-max(|O|, |O_ref|) is taken off |O - O_ref| before the bounds apply.  No bf16 output can come
-closer to O_ref than that (an exact O of 3 is already 0.0078 from its nearest bf16), and the
-flash-attention page (section 5, tests) judges an implementation against a PyTorch
-baseline that rounds its output the same way.  Plain attention outputs are small averages,
-where the allowance is below 2^-9; it matters where the probabilities concentrate on a few
-keys (steep ALiBi slopes, narrow windows) and O is close to one value row.
+By default the bounds apply to the raw differences.  A test may pass allowance=True when
+its outputs are dominated by a few keys (steep ALiBi slopes, narrow windows, softcaps that
+saturate): O is then close to one value row, and a 16-bit output cannot come closer to
+O_ref than half an ulp of the output type (an exact O of 3 is already 0.0078 from its
+nearest bf16).  With the allowance, half an ulp at max(|O|, |O_ref|) is taken off each
+element's difference before the bounds apply.  The flash-attention page (section 5, tests)
+judges an implementation against a PyTorch baseline that rounds its output the same way.
+
+With FA_PARITY_LOG set to a file path, every comparison appends one JSON line with the
+raw and the allowance-adjusted errors and the test it came from.
 """
 from __future__ import annotations
+
+import json
+import os
 
 import numpy as np
 import torch
@@ -44,8 +49,20 @@ def half_ulp(x: np.ndarray, dtype) -> np.ndarray:
     return np.exp2(e - bits)
 
 
-def compare(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
-    """o_* [..., d] and lse_* [...] with the same row order (o.shape[:-1] == lse.shape)."""
+def _log(rec):
+    path = os.environ.get("FA_PARITY_LOG")
+    if not path:
+        return
+    rec = dict(rec, test=os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0])
+    with open(path, "a") as f:
+        f.write(json.dumps(rec) + "\n")
+
+
+def compare(o_gpu, lse_gpu, o_ref, lse_ref, what="", allowance=False):
+    """o_* [..., d] and lse_* [...] with the same row order (o.shape[:-1] == lse.shape).
+
+    Asserts the bounds on the raw differences, or on the differences beyond half an ulp
+    of the output type when allowance=True.  Returns the errors it measured."""
     out_dtype = o_gpu.dtype if isinstance(o_gpu, torch.Tensor) else None
     o = to_np(o_gpu) if isinstance(o_gpu, torch.Tensor) else np.asarray(o_gpu, np.float64)
     lse = to_np(lse_gpu) if isinstance(lse_gpu, torch.Tensor) else np.asarray(lse_gpu, np.float64)
@@ -60,15 +77,27 @@ def compare(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
     assert np.all(lse[empty] == -np.inf), f"{what}: empty rows must have LSE = -inf"
     if empty.any():
         assert np.all(o[empty] == 0.0), f"{what}: empty rows must have O = 0"
+    raw = np.abs(o - o_ref)
+    raw_max = float(raw.max(initial=0.0))
+    raw_mean = float(raw.mean()) if raw.size else 0.0
     rep = np.maximum(half_ulp(o, out_dtype), half_ulp(o_ref, out_dtype))
-    err = np.maximum(np.abs(o - o_ref) - rep, 0.0)
-    max_o, mean_o = float(err.max(initial=0.0)), float(err.mean()) if err.size else 0.0
+    adj = np.maximum(raw - rep, 0.0)
+    del rep
+    adj_max = float(adj.max(initial=0.0))
+    adj_mean = float(adj.mean()) if adj.size else 0.0
+    del adj
     fin = ~empty
     max_l = float(np.abs(lse[fin] - lse_ref[fin]).max(initial=0.0))
-    assert max_o <= O_MAX_TOL, f"{what}: max|dO| = {max_o:.3e} > {O_MAX_TOL}"
-    assert mean_o <= O_MEAN_TOL, f"{what}: mean|dO| = {mean_o:.3e} > {O_MEAN_TOL}"
+    _log({"what": what, "allowance": bool(allowance), "elements": int(raw.size),
+          "raw_max_abs_o": raw_max, "raw_mean_abs_o": raw_mean, "adj_max_abs_o": adj_max,
+          "adj_mean_abs_o": adj_mean, "max_abs_lse": max_l})
+    max_o, mean_o = (adj_max, adj_mean) if allowance else (raw_max, raw_mean)
+    tag = " (beyond half an ulp)" if allowance else ""
+    assert max_o <= O_MAX_TOL, f"{what}: max|dO|{tag} = {max_o:.3e} > {O_MAX_TOL}"
+    assert mean_o <= O_MEAN_TOL, f"{what}: mean|dO|{tag} = {mean_o:.3e} > {O_MEAN_TOL}"
     assert max_l <= LSE_TOL, f"{what}: max|dLSE| = {max_l:.3e} > {LSE_TOL}"
-    return {"max_abs_o": max_o, "mean_abs_o": mean_o, "max_abs_lse": max_l}
+    return {"max_abs_o": max_o, "mean_abs_o": mean_o, "max_abs_lse": max_l,
+            "raw_max_abs_o": raw_max, "raw_mean_abs_o": raw_mean}
 
 
 def sample_rows(B, H, N, n, seed, must=()):

@@ -162,7 +162,10 @@ def test_kvcache_rejects_bad_arguments(lib):
                                   a["wsb"], a["o"], a["lse"], a["dtype"], a.get("mod"),
                                   a.get("ex"), None)
 
-    assert call(Hq=32, Hkv=2) == 2          # group of 16 not supported by decode
+    # any group size passes host validation (without a GPU the call then stops at the
+    # device lookup, never at an argument check)
+    for hq, hkv in ((32, 2), (32, 1), (24, 8), (12, 2)):
+        assert call(Hq=hq, Hkv=hkv) not in (1, 2, 4)
     assert call(dtype=5) == 2
     assert call(d=36) == 2
     assert call(d=264) == 2                 # decode serves d up to 256
@@ -211,7 +214,7 @@ def test_kvcache_fp8_rejects_bad_arguments(lib):
     assert call(d=8) == 2                   # E4M3 rows: d a multiple of 16
     assert call(d=24) == 2
     assert call(d=272) == 2
-    assert call(Hq=32, Hkv=2) == 2          # group of 16
+    assert call(Hq=32, Hkv=1) not in (1, 2, 4)   # MQA 32:1 passes host validation
     assert call(kd=4098) == 1               # descale pointers 4-byte aligned
     assert call(vd=4097) == 1
     assert call(lens=None) == 1
@@ -235,7 +238,7 @@ def test_workspace_size(lib):
 
 def test_status_strings(lib):
     lib.fa_status_string.restype = ctypes.c_char_p
-    for s in range(6):
+    for s in range(7):
         assert lib.fa_status_string(s).decode().startswith("FA_")
 
 

@@ -162,7 +162,8 @@ def _decode_fp8(d, group, lens, seed, Lmax=3072, Hkv=2, descales=True, num_split
 
 
 @pytest.mark.parametrize("d,group", [(128, 4), (128, 8), (128, 1), (64, 2), (96, 4),
-                                     (256, 2), (256, 8), (192, 4), (16, 1)])
+                                     (256, 2), (256, 8), (192, 4), (16, 1), (128, 16),
+                                     (128, 6), (256, 32)])
 def test_decode_fp8(d, group):
     _decode_fp8(d, group, [1, 127, 128, 1000, 3071, 0, 513, 3072], 700 + d + group)
 

@@ -1,6 +1,6 @@
 """GPU parity of the dense and varlen prefill path (libfa.so through its C ABI) against the
-fp64 oracle, on seeded inputs: small cases compared element by element, the full-size
-workloads on sampled rows plus whole-output properties."""
+fp64 oracle, on seeded inputs, element by element: small cases with ragged tails and
+degenerate shapes, and the full-size workloads in the benchmark's launch configuration."""
 import math
 
 import numpy as np
@@ -11,7 +11,7 @@ import oracle.oracle as ORACLE
 from exact_attention_81_gb300 import (FA_OK, fa_fwd, fa_fwd_varlen, get_last_device_error)
 from exact_attention_81_gb300.inputs import (WORKLOADS, dense_inputs, varlen_inputs,
                                              workload_inputs)
-from tests.parity_util import compare, dense_rows, sample_rows, varlen_rows
+from tests.parity_util import compare, dense_rows, varlen_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -166,30 +166,17 @@ def test_varlen_bad_cu_seqlens_flagged():
 
 @pytest.mark.parametrize("name", ["dense2k", "causal8k", "gqa16k"])
 def test_full_size_workload(name):
-    """The benchmark workloads at full size, in the benchmark's launch configuration:
-    sampled rows against the oracle, plus properties of the whole output (finite, each O
-    a convex combination of V rows, LSE >= the largest visible score)."""
+    """The benchmark workloads at full size, in the benchmark's launch configuration, every
+    output element against the oracle (threaded over all host cores): raw max and mean
+    |O - O_ref| over the whole workload and max |LSE - LSE_ref| over all of its rows."""
     w = WORKLOADS[name]
     q, k, v = workload_inputs(w, device=DEV)
     o, lse = _run_dense(q, k, v, w.causal)
-    rows = sample_rows(w.B, w.Hq, w.Nq, 160, seed=w.seed)
-    o_ref, lse_ref = ORACLE.attention_rows(q.cpu(), k.cpu(), v.cpu(), rows, w.scale, w.causal)
-    r = torch.as_tensor(rows, dtype=torch.long)
-    o_s = o[r[:, 0], r[:, 2], r[:, 1]]
-    l_s = lse[r[:, 0], r[:, 1], r[:, 2]]
-    compare(o_s, l_s, o_ref, lse_ref, name)
-    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
-    G = w.Hq // w.Hkv
-    vmax = v.float().amax(dim=1).repeat_interleave(G, dim=1)  # [B, Hq, d]
-    vmin = v.float().amin(dim=1).repeat_interleave(G, dim=1)
-    of = o.float()
-    assert (of <= vmax[:, None] + 1e-2).all() and (of >= vmin[:, None] - 1e-2).all()
-    # LSE >= scale * q_i . k_j for the diagonal key (always visible in the causal case)
-    if w.causal:
-        G = w.Hq // w.Hkv
-        kk = k.float().repeat_interleave(G, dim=2)
-        diag = (q.float() * kk).sum(-1) * w.scale  # [B, N, Hq]
-        assert (lse >= diag.transpose(1, 2) - 1e-3).all()
+    o_ref, lse_ref = _oracle_dense(q, k, v, w.causal, w.scale)
+    stats = compare(*dense_rows(o, lse), *dense_rows(o_ref, lse_ref), name)
+    print(f"{name}: raw max|dO| {stats['raw_max_abs_o']:.3e}, mean|dO| "
+          f"{stats['raw_mean_abs_o']:.3e}, max|dLSE| {stats['max_abs_lse']:.3e} over "
+          f"{o.numel()} elements")
 
 
 @pytest.mark.parametrize("causal", [False, True])

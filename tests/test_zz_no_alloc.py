@@ -1,8 +1,9 @@
 """fa_fwd_kvcache_noalloc: the split-KV decode entry point for callers that cannot allocate
 device memory (it keeps its partials in a scratch array compiled into libfa.so instead of a
-caller workspace).  Called here through the C ABI and checked against fa_fwd_kvcache, the
-entry point that takes a workspace, on two calls in a row.  Kept in a file of its own that
-pytest collects last."""
+caller workspace).  Called here through the C ABI and checked bit for bit against
+fa_fwd_kvcache, the entry point that takes a workspace (same kernels, same splits), on calls
+in a row that reuse the scratch with different layouts, and against the fp64 oracle at head
+dimensions 96 and 256.  Kept in a file of its own that pytest collects last."""
 import ctypes
 import math
 
@@ -10,11 +11,12 @@ import numpy as np
 import pytest
 import torch
 
+import oracle.oracle as ORACLE
 from exact_attention_81_gb300 import (FA_ERR_WORKSPACE, FA_OK, fa_fwd_kvcache,
                                       fa_fwd_kvcache_workspace_size, get_last_device_error,
                                       load_library)
 from exact_attention_81_gb300.inputs import kvcache_inputs
-from tests.parity_util import LSE_TOL, O_MAX_TOL, O_MEAN_TOL
+from tests.parity_util import compare
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -43,29 +45,48 @@ def _call_noalloc(f, q, kc, vc, lens, num_splits=0):
     return st, o, lse
 
 
-def _close(o, lse, o_ref, lse_ref):
-    err = (o.float() - o_ref.float()).abs()
-    assert err.max().item() <= O_MAX_TOL and err.mean().item() <= O_MEAN_TOL
-    fin = torch.isfinite(lse_ref)
-    assert torch.equal(torch.isfinite(lse), fin)
-    assert (lse[fin] - lse_ref[fin]).abs().max().item() <= LSE_TOL
+CASES = {
+    "wide": dict(lens=[4096, 1, 3000, 128, 129, 2047, 0, 4000], Lmax=4096, Hq=32, Hkv=8,
+                 d=128, seed=901, splits=0),
+    "small": dict(lens=[17, 900, 4096, 2], Lmax=4096, Hq=16, Hkv=8, d=64, seed=902, splits=0),
+    "d96_splits3": dict(lens=[1000, 3, 2500, 513], Lmax=2560, Hq=8, Hkv=2, d=96, seed=903,
+                        splits=3),
+    "d256": dict(lens=[2048, 77, 1500], Lmax=2048, Hq=16, Hkv=2, d=256, seed=904, splits=0),
+}
 
 
-def test_noalloc_matches_workspace_entry_point_twice():
+def _inputs(c):
+    return kvcache_inputs(len(c["lens"]), c["Lmax"], c["Hq"], c["Hkv"], c["d"], seed=c["seed"],
+                          lengths=torch.tensor(c["lens"]), device=DEV)
+
+
+def test_noalloc_matches_workspace_entry_point_bit_for_bit():
+    """Calls in a row on the one scratch array: a large layout, a small one, the large one
+    again (it finds the small call's partials in the scratch), an explicit split count, and
+    the width-256 instance.  Each output equals fa_fwd_kvcache's with the same num_splits."""
     f = _noalloc_fn()
-    cases = [
-        dict(lens=[4096, 1, 3000, 128, 129, 2047, 0, 4000], Hq=32, Hkv=8, d=128, seed=901),
-        dict(lens=[17, 900, 4096, 2], Hq=16, Hkv=8, d=64, seed=902),
-    ]
-    for c in cases:  # two calls in a row; the second finds the first one's partials
-        q, kc, vc, lens = kvcache_inputs(len(c["lens"]), 4096, c["Hq"], c["Hkv"], c["d"],
-                                         seed=c["seed"], lengths=torch.tensor(c["lens"]),
-                                         device=DEV)
-        o_ref, lse_ref = fa_fwd_kvcache(q, kc, vc, lens)
-        st, o, lse = _call_noalloc(f, q, kc, vc, lens)
-        assert st == FA_OK
+    for name in ["wide", "small", "wide", "d96_splits3", "d256", "wide"]:
+        c = CASES[name]
+        q, kc, vc, lens = _inputs(c)
+        o_ref, lse_ref = fa_fwd_kvcache(q, kc, vc, lens, num_splits=c["splits"])
+        st, o, lse = _call_noalloc(f, q, kc, vc, lens, num_splits=c["splits"])
+        assert st == FA_OK, name
         assert get_last_device_error() == FA_OK
-        _close(o, lse, o_ref, lse_ref)
+        assert torch.equal(o, o_ref), name
+        assert torch.equal(lse, lse_ref), name
+
+
+@pytest.mark.parametrize("name", ["d96_splits3", "d256"])
+def test_noalloc_matches_oracle(name):
+    f = _noalloc_fn()
+    c = CASES[name]
+    q, kc, vc, lens = _inputs(c)
+    st, o, lse = _call_noalloc(f, q, kc, vc, lens, num_splits=c["splits"])
+    assert st == FA_OK
+    assert get_last_device_error() == FA_OK
+    o_ref, lse_ref = ORACLE.attention_kvcache(q.cpu(), kc.cpu(), vc.cpu(), lens.cpu(),
+                                              float(np.float32(1 / math.sqrt(c["d"]))))
+    compare(o[:, 0], lse, o_ref, lse_ref, f"noalloc {name}")
 
 
 def test_noalloc_rejects_calls_beyond_its_scratch():
