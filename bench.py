@@ -650,6 +650,8 @@ def extra_workloads(args, dev, pk, world, dist):
             ("causal8k_fp16", torch.float16, {}, flops(w)),
             ("causal8k_window4096", torch.bfloat16, {"window_size": (4096, 0)},
              4.0 * w.d * w.B * w.Hq * window_pairs(w.Nq, w.Nk, 4096, 0)),
+            ("causal8k_alibi", torch.bfloat16, {"alibi_slopes": slopes}, flops(w)),
+            ("causal8k_softcap", torch.bfloat16, {"softcap": 30.0}, flops(w)),
             ("causal8k_softcap_alibi", torch.bfloat16,
              {"softcap": 30.0, "alibi_slopes": slopes}, flops(w))]:
         q, k, v = workload_inputs(w, device=dev, dtype=dtype)
@@ -703,6 +705,7 @@ def extra_workloads(args, dev, pk, world, dist):
     for name, kw, work in [
             ("causal8k_backward_window4096", {"window_size": (4096, 0)},
              10.0 * w.d * w.B * w.Hq * window_pairs(w.Nq, w.Nk, 4096, 0)),
+            ("causal8k_backward_alibi", {"alibi_slopes": slopes}, 2.5 * flops(w)),
             ("causal8k_backward_softcap_alibi", {"softcap": 30.0, "alibi_slopes": slopes},
              2.5 * flops(w))]:
         o, l = fa.fa_fwd(q, k, v, causal=True, **kw)

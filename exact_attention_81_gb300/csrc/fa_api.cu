@@ -242,8 +242,10 @@ fa_status plan_mod(const fa_score_mod *m, int causal, ModPlan *out) {
     p.alibi_sb = m->alibi_batch_stride;
   }
   if (causal) p.wr = 0;
-  if (p.softcap != 0.f || p.alibi != nullptr)
+  if (p.softcap != 0.f)
     p.mask = fa::MASK_MOD;
+  else if (p.alibi != nullptr)
+    p.mask = fa::MASK_ALIBI;
   else if (p.wl >= 0 || p.wr > 0)
     p.mask = fa::MASK_WINDOW;
   else

@@ -142,7 +142,7 @@ __device__ __forceinline__ BUnit bunit_of(const BwdArgs &a, int u) {
   w.ilo = 0;
   w.ihi = w.nqb;
   const long long off = static_cast<long long>(w.nk) - w.nq;
-  constexpr bool WIN = MASK == MASK_MOD || MASK == MASK_WINDOW;
+  constexpr bool WIN = mask_has_window(MASK);
   const int wr = MASK == MASK_CAUSAL ? 0 : (WIN ? a.wr : -1);
   const int wl = WIN ? a.wl : -1;
   if (wr >= 0) {
@@ -341,7 +341,7 @@ __device__ void bwd_dq_issuer(const BwdArgs &a, const CUtensorMap *tdq, uint8_t 
         // jmin .. jmax (jmin = 0 unless a left window bound cuts the first keys); block j
         // adds after jmin .. j-1.
         int jmin = 0;
-        if ((MASK == MASK_MOD || MASK == MASK_WINDOW) && a.wl >= 0)
+        if (mask_has_window(MASK) && a.wl >= 0)
           jmin = max(q0 + off - a.wl, 0) / BKEY;
         ok = sem == nullptr || wait_counter(sem, w.j - jmin, wc);
         if (ok) {
@@ -467,11 +467,15 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
                (a.wl < 0 || kb >= q0 + BQ - 1 + off - a.wl);
       }
       // this key row's visible query positions (modifiers): key - wr - off <= q <= key + wl - off
-      constexpr bool WIN = MASK == MASK_MOD || MASK == MASK_WINDOW;
+      constexpr bool WIN = mask_has_window(MASK);
+      constexpr bool SCORE_MOD = MASK == MASK_MOD || MASK == MASK_ALIBI;
       const int qv_lo = WIN && a.wr >= 0 ? key - a.wr - off : INT_MIN;
       const int qv_hi = WIN && a.wl >= 0 ? key + a.wl - off : INT_MAX;
       const bool softcap = MASK == MASK_MOD && a.sc_out != 0.f;
-      const bool alibi = MASK == MASK_MOD && a.alibi != nullptr;
+      const bool alibi = SCORE_MOD && a.alibi != nullptr;
+      // ALiBi without a softcap on a block with no masked pair whose queries all sit at or
+      // after its keys: the bias -slope2 (q + off - key) is linear in the query.
+      const bool alibi_lin = MASK == MASK_ALIBI && full && kb + BKEY - 1 <= q0 + off;
       const float slope2 = alibi ? a.alibi[w.b * a.alibi_sb + h] * LOG2E : 0.f;
       // P^T and dS^T = P^T (dP^T - D) of this key row for the 64 queries of this half,
       // 32 at a time: P^T and dS^T to TMEM (dV, dK), dS to shared memory with queries
@@ -486,7 +490,41 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
         uint32_t sr[32], dr[32];
         tmem_ld_2x32(tmem + lane_off + T_ST + qc, tmem + lane_off + T_DP + qc, sr, dr);
         uint32_t pp[16], dd[16];
-        if (MASK != MASK_MOD && full) {
+        if (MASK == MASK_ALIBI && alibi_lin) {
+          // P = 2^(S c - slope2 (q + off - key) - LSE2): the bias pairs of queries (e, e+1)
+          // and (e+2, e+3) step by -4 slope2 along two chains that start from exact
+          // products; then dS = P (dP - D), all on packed fp32 pairs.
+          const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
+          const float base = -slope2 * static_cast<float>(q0 + qc + off - key);
+          uint64_t w01 = f2_pack(base, base - slope2);
+          uint64_t w23 = f2_pack(base - 2.f * slope2, base - 3.f * slope2);
+          const uint64_t step = f2_pack(-4.f * slope2, -4.f * slope2);
+#pragma unroll
+          for (int e4 = 0; e4 < 32; e4 += 4) {
+            const float4 l4 = *reinterpret_cast<const float4 *>(lse2 + qc + e4);
+            const float4 d4 = *reinterpret_cast<const float4 *>(dvec + qc + e4);
+            float z0, z1, z2, z3, e0, e1, e2, e3;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e4]), __uint_as_float(sr[e4 + 1])), sc2,
+                             f2_add(w01, f2_pack(-l4.x, -l4.y))), z0, z1);
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e4 + 2]), __uint_as_float(sr[e4 + 3])),
+                             sc2, f2_add(w23, f2_pack(-l4.z, -l4.w))), z2, z3);
+            w01 = f2_add(w01, step);
+            w23 = f2_add(w23, step);
+            const float p0 = ex2_approx(z0), p1 = ex2_approx(z1);
+            const float p2 = ex2_approx(z2), p3 = ex2_approx(z3);
+            f2_unpack(f2_mul(f2_pack(p0, p1),
+                             f2_add(f2_pack(__uint_as_float(dr[e4]), __uint_as_float(dr[e4 + 1])),
+                                    f2_pack(-d4.x, -d4.y))), e0, e1);
+            f2_unpack(f2_mul(f2_pack(p2, p3),
+                             f2_add(f2_pack(__uint_as_float(dr[e4 + 2]),
+                                            __uint_as_float(dr[e4 + 3])),
+                                    f2_pack(-d4.z, -d4.w))), e2, e3);
+            pp[e4 / 2] = pack2<F16>(p0, p1);
+            pp[e4 / 2 + 1] = pack2<F16>(p2, p3);
+            dd[e4 / 2] = pack2<F16>(e0, e1);
+            dd[e4 / 2 + 1] = pack2<F16>(e2, e3);
+          }
+        } else if (!SCORE_MOD && full) {
           // No masked pair and no modifier: P = 2^(S c - LSE2), dS = P (dP - D) on packed
           // fp32 pairs.
           const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
@@ -525,7 +563,7 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
             const int qi = qc + e4 + x;
             const float sv = __uint_as_float(sr[e4 + x]);
             float z2, dz = 1.f;  // score in log2 units and dz/ds
-            if constexpr (MASK == MASK_MOD) {
+            if constexpr (SCORE_MOD) {
               if (softcap) {
                 const float t = tanh_ex2(sv * a.sc_in);
                 z2 = t * a.sc_out;
@@ -807,6 +845,8 @@ cudaError_t launch_bwd_d(int mask, const CUtensorMap &tq, const CUtensorMap &tk,
       return launch_bwd_impl<D, MASK_CAUSAL, F16>(tq, tk, tv, tdo, tdq, a, grid, stream);
     case MASK_WINDOW:
       return launch_bwd_impl<D, MASK_WINDOW, F16>(tq, tk, tv, tdo, tdq, a, grid, stream);
+    case MASK_ALIBI:
+      return launch_bwd_impl<D, MASK_ALIBI, F16>(tq, tk, tv, tdo, tdq, a, grid, stream);
     default: return launch_bwd_impl<D, MASK_MOD, F16>(tq, tk, tv, tdo, tdq, a, grid, stream);
   }
 }

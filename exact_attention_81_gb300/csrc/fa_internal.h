@@ -42,7 +42,7 @@ struct PrefillArgs {
   unsigned int *err;          // device error word
   unsigned long long timeout_ns;
   int inject;                 // failure injection: the producer issues no load at all
-  // Score modifiers (read by the MASK_MOD kernel only).
+  // Score modifiers (read by the MASK_MOD / MASK_ALIBI / MASK_WINDOW kernels only).
   int wl, wr;                 // window bounds in keys, -1 = unbounded (causal folded: wr = 0)
   float sc_in, sc_out;        // softcap: s -> tanh(s * sc_in) * sc_out (log2 units); 0 = off
   const float *alibi;         // slopes of (b, h) at alibi[b * alibi_sb + h], or null
@@ -56,10 +56,16 @@ struct PrefillArgs {
 enum PrefillMask : int {
   MASK_NONE = 0,    // every key visible (tail of the key range masked)
   MASK_CAUSAL = 1,  // bottom-right causal
-  MASK_MOD = 2,     // softcap and/or ALiBi (and any window)
+  MASK_MOD = 2,     // softcap, with or without ALiBi (and any window)
   MASK_WINDOW = 3,  // sliding window only: the MASK_MOD masking without the softcap / ALiBi
                     // code, which made every window call 27 % slower
+  MASK_ALIBI = 4,   // ALiBi without a softcap (and any window): no tanh code
 };
+
+// Mask modes whose kernels apply a general window (left and right bounds).
+__host__ __device__ constexpr bool mask_has_window(int m) {
+  return m == MASK_MOD || m == MASK_WINDOW || m == MASK_ALIBI;
+}
 
 // Tile-ticket counter slot for the next prefill launch (round robin over the slots).
 int next_prefill_sched_slot();
@@ -190,7 +196,7 @@ struct BwdArgs {
   int kblocks;                // ceil(Nk / 128)
   int d;                      // head dimension of the tensors (<= the kernel's D)
   int *sem;                   // deterministic dQ: additions done per (b, h, query block), or null
-  // Score modifiers (read by the MASK_MOD kernel only), as in PrefillArgs.
+  // Score modifiers (read by the windowed / modifier kernels only), as in PrefillArgs.
   int wl, wr;
   float sc_in, sc_out;        // softcap: z2 = tanh(s * sc_in) * sc_out, dz/ds = 1 - tanh^2
   const float *alibi;

@@ -135,8 +135,7 @@ __device__ __forceinline__ TileInfo tile_info(const PrefillArgs &a, int tile) {
   TileInfo ti;
   const int bh = tile / a.mblocks;
   const int r = tile - bh * a.mblocks;
-  const bool desc =
-      MASK == MASK_CAUSAL || ((MASK == MASK_MOD || MASK == MASK_WINDOW) && a.desc);
+  const bool desc = MASK == MASK_CAUSAL || (mask_has_window(MASK) && a.desc);
   const int mb = desc ? (a.mblocks - 1 - r) : r;
   ti.b = bh / a.Hq;
   ti.h = bh - ti.b * a.Hq;
@@ -593,8 +592,9 @@ __device__ void softmax_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, ui
   // the LSE takes the 8 back out.
   constexpr float POFF = F8 ? 8.f : 0.f;
   constexpr bool CAUSAL = MASK == MASK_CAUSAL;
-  constexpr bool MOD = MASK == MASK_MOD || MASK == MASK_WINDOW;  // window masking
-  constexpr bool SCORE_MOD = MASK == MASK_MOD;                    // softcap / ALiBi code
+  constexpr bool MOD = mask_has_window(MASK);   // window masking
+  constexpr bool SCORE_MOD = MASK == MASK_MOD;    // softcap (+ ALiBi) code
+  constexpr bool ALIBI = MASK == MASK_ALIBI;      // ALiBi without a softcap
   const int t = warp >> 2;
   const int wq = warp & 3;
   const int rit = wq * 32 + lane;  // row inside the sub-tile = TMEM lane
@@ -604,7 +604,7 @@ __device__ void softmax_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, ui
   // the exp2 argument needs no further scaling.
   const bool softcap = SCORE_MOD && a.sc_out != 0.f;
   const bool alibi = SCORE_MOD && a.alibi != nullptr;
-  const float c = (softcap || alibi) ? 1.f : a.scale_log2;
+  const float c = (softcap || alibi || ALIBI) ? 1.f : a.scale_log2;
   // S buffer phases, bit b for buffer b (one buffer per sub-tile; the wide kernel's single
   // sub-tile alternates between two).
   uint32_t s_phase = 0, o_phase = 0, pv_phase = 0;
@@ -635,7 +635,7 @@ __device__ void softmax_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, ui
       min_limit = CAUSAL ? min(first_row + off, ti.nk - 1) : ti.nk - 1;
     }
     float slope2 = 0.f;  // ALiBi slope in log2 units
-    if (alibi) slope2 = a.alibi[ti.b * a.alibi_sb + ti.h] * 1.4426950408889634f;
+    if (alibi || ALIBI) slope2 = a.alibi[ti.b * a.alibi_sb + ti.h] * 1.4426950408889634f;
     // FP8: the Q and K descale factors of (batch, kv head) multiply every score.
     float qks = 1.f, vds = 1.f;
     if constexpr (F8) {
@@ -644,7 +644,7 @@ __device__ void softmax_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, ui
       if (a.k_descale != nullptr) qks *= a.k_descale[di];
       if (a.v_descale != nullptr) vds = a.v_descale[di];
     }
-    const float ct = F8 && !(softcap || alibi) ? c * qks : c;
+    const float ct = F8 && !(softcap || alibi || ALIBI) ? c * qks : c;
 
     float m = -INFINITY, l = 0.f;
     const uint64_t c2 = f2_pack(ct, ct);
@@ -665,7 +665,48 @@ __device__ void softmax_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, ui
         }
       }
       const int kbase = (kt0 + j) * BC;
-      if constexpr (MOD) {
+      // ALiBi without a softcap: the stored scores are y = s scale log2e - slope2 |pos - key|
+      // - toff, in log2 units, and toff (a per-row constant of the tile) goes into the max
+      // and the exp2 offset.  When every key of the tile lies at or before pos (all of a
+      // causal row's tiles but the diagonal one) the bias is linear in the column:
+      // -slope2 (dist0 - i) = slope2 i + toff with toff = -slope2 dist0, and y = s c +
+      // slope2 i is one packed FMA per pair, the slope2 i pairs stepping by 8 slope2 along
+      // four independent chains that start from exact products.
+      float toff = 0.f;
+      if constexpr (ALIBI) {
+        const float cs = F8 ? a.scale_log2 * qks : a.scale_log2;
+        const int dist0 = row + off - kbase;  // pos - the tile's first key
+        if (dist0 >= BC - 1) {
+          toff = -slope2 * static_cast<float>(dist0);
+          const uint64_t cs2 = f2_pack(cs, cs);
+          const uint64_t step = f2_pack(8.f * slope2, 8.f * slope2);
+          uint64_t w[4];
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4)
+            w[q4] = f2_pack(slope2 * static_cast<float>(2 * q4),
+                            slope2 * static_cast<float>(2 * q4 + 1));
+#pragma unroll
+          for (int i = 0; i < BC; i += 8) {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              const int e = i + 2 * q4;
+              f2_unpack(f2_fma(f2_pack(s[e], s[e + 1]), cs2, w[q4]), s[e], s[e + 1]);
+              w[q4] = f2_add(w[q4], step);
+            }
+          }
+        } else {
+          const float fd = static_cast<float>(dist0);
+#pragma unroll
+          for (int i = 0; i < BC; ++i)
+            s[i] = fmaf(s[i], cs, -slope2 * fabsf(fd - static_cast<float>(i)));
+        }
+        if (kbase < all_lo || kbase + BC - 1 > min_limit) {
+          const int l0 = lo - kbase, lim = limit - kbase;
+#pragma unroll
+          for (int i = 0; i < BC; ++i)
+            if (i < l0 || i > lim) s[i] = -INFINITY;
+        }
+      } else if constexpr (MOD) {
         if (softcap) {
           // softcap * tanh(scale * q.k / softcap), in log2 units
           const float sci = F8 ? a.sc_in * qks : a.sc_in;
@@ -703,12 +744,12 @@ __device__ void softmax_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, ui
       }
       const float mx = fmaxf(fmax3(mx0, mx1, s[BC - 4]),
                              fmax3(mx2, mx3, fmax3(s[BC - 3], s[BC - 2], s[BC - 1])));
-      const float m_new = fmaxf(m, mx * ct);
+      const float m_new = fmaxf(m, mx * ct + toff);
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
       const bool grow = j > 0 && m_new > m;
       const float alpha = grow ? ex2_approx(m - m_use) : 1.f;
-      // P = 2^(S c - m_new) with the FMA and the row sum on packed fp32 pairs.
-      const uint64_t neg2 = f2_pack(POFF - m_use, POFF - m_use);
+      // P = 2^(S c + toff - m_new) with the FMA and the row sum on packed fp32 pairs.
+      const uint64_t neg2 = f2_pack(POFF + toff - m_use, POFF + toff - m_use);
       uint64_t l2a = f2_pack(0.f, 0.f), l2b = l2a;
       uint32_t p[64];
 #pragma unroll
@@ -965,6 +1006,7 @@ cudaError_t launch_mask(int mask, const CUtensorMap &tq, const CUtensorMap &tk,
     case MASK_NONE: return launch_impl<D, MASK_NONE, F16, F8>(tq, tk, tv, a, grid, stream);
     case MASK_CAUSAL: return launch_impl<D, MASK_CAUSAL, F16, F8>(tq, tk, tv, a, grid, stream);
     case MASK_WINDOW: return launch_impl<D, MASK_WINDOW, F16, F8>(tq, tk, tv, a, grid, stream);
+    case MASK_ALIBI: return launch_impl<D, MASK_ALIBI, F16, F8>(tq, tk, tv, a, grid, stream);
     default: return launch_impl<D, MASK_MOD, F16, F8>(tq, tk, tv, a, grid, stream);
   }
 }

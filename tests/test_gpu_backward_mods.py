@@ -182,3 +182,12 @@ def test_varlen_backward_modifiers():
                       do[a:e].unsqueeze(0), sc, window[0], window[1], softcap, slopes[b])
         base[0][a:e], base[1][ka:ke], base[2][ka:ke] = g[0][0], g[1][0], g[2][0]
     _bar("varlen with modifiers", grads, ref, base)
+
+
+@pytest.mark.parametrize("deterministic,Nq,Nk", [(False, 1024, 1024), (True, 700, 1100)])
+def test_alibi_only_backward_long_rows(deterministic, Nq, Nk):
+    """ALiBi without a softcap: blocks whose queries all sit at or after their keys build the
+    bias as a linear function of the query (the ALiBi instance's packed path)."""
+    slopes = torch.tensor([1.0, 0.5, 0.25, 0.125], dtype=torch.float32)
+    _dense(1, Nq, Nk, 4, 2, 128, True, seed=970 + Nq, deterministic=deterministic,
+           slopes=slopes)

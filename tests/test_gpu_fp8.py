@@ -157,7 +157,11 @@ def _decode_fp8(d, group, lens, seed, Lmax=3072, Hkv=2, descales=True, num_split
         None if dk is None else dk.cpu(), None if dv is None else dv.cpu(),
         window=mod.get("window_size", (-1, -1)), softcap=mod.get("softcap", 0.0),
         alibi_slopes=sl)
-    compare(o[:, 0], lse, o_ref, lse_ref, f"fp8 decode d={d} G={group} {mod}")
+    # allowance without descales: the codes were drawn as N(0,1) / (0.25..0.375), so the
+    # undescaled values and O are several times larger (|O| up to ~4, where half a bf16
+    # ulp is 0.0156); measured 4e-7 beyond half an ulp, 1.5e-2 raw
+    compare(o[:, 0], lse, o_ref, lse_ref, f"fp8 decode d={d} G={group} {mod}",
+            allowance=not descales)
     return q, kc, vc, lens, dk, dv, o, lse
 
 
