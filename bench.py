@@ -630,6 +630,22 @@ def extra_workloads(args, dev, pk, world, dist):
     from exact_attention_81_gb300.inputs import WORKLOADS, kvcache_workload_inputs, workload_inputs
     stream = torch.cuda.current_stream()
     res = {}
+    # the width-128 forward on CTA pairs (cta_group::2), next to the default single-CTA kernel
+    for name in ("causal8k", "dense2k", "gqa16k"):
+        w = WORKLOADS[name]
+        q, k, v = workload_inputs(w, device=dev)
+        o = torch.empty_like(q)
+        l = torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device=dev)
+        fa.set_cta_pairs(True)
+        try:
+            ms = time_calls(lambda: fa.fa_fwd(q, k, v, causal=w.causal, out=o, lse=l),
+                            max(10, args.steps // 4), stream)
+        finally:
+            fa.set_cta_pairs(False)
+        tf = flops(w) / (ms * 1e-3) / 1e12
+        res[name + "_cta_pairs"] = {"ms": round(ms, 4), "TFLOPS": round(tf, 2),
+                                    "frac_of_bf16_peak": round(tf / pk["bf16"], 4)}
+        del q, k, v, o, l
     for name in ("dense2k", "gqa16k", "causal8k_d256"):
         w = WORKLOADS[name]
         q, k, v = workload_inputs(w, device=dev)

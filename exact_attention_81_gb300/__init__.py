@@ -36,6 +36,7 @@ from ._binding import (  # noqa: F401
     flash_attn_with_kvcache,
     get_last_device_error,
     load_library,
+    set_cta_pairs,
     set_fault_injection,
     set_wait_timeout_ns,
     status_string,

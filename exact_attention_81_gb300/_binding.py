@@ -164,6 +164,8 @@ def load_library(path: str | None = None):
         lib.fa_set_wait_timeout_ns.restype = None
         lib.fa_set_fault_injection.argtypes = [ctypes.c_int]
         lib.fa_set_fault_injection.restype = None
+        lib.fa_set_cta_pairs.argtypes = [ctypes.c_int]
+        lib.fa_set_cta_pairs.restype = None
         lib.fa_fwd_host.argtypes = [ctypes.POINTER(FwdParams), vp, vp, vp, vp, vp, i, vp]
         lib.fa_fwd_host.restype = i
         lib.fa_fwd_fp8_workspace_size.argtypes = [i, i, i, i]
@@ -666,6 +668,12 @@ def set_wait_timeout_ns(ns: int):
 def set_fault_injection(withhold_loads: bool):
     """Testing aid: later kernels issue no loads, so their waits run into the limit."""
     load_library().fa_set_fault_injection(int(bool(withhold_loads)))
+
+
+def set_cta_pairs(enable: bool):
+    """Run the 16-bit forward at head dimensions 72..128 on CTA pairs, or on the single-CTA
+    kernel (the default) (process-wide, for later calls)."""
+    load_library().fa_set_cta_pairs(int(bool(enable)))
 
 
 # Names of the upstream Python API ("flash-attention", section 1), mapped onto the C calls.

@@ -43,6 +43,7 @@ std::mutex g_mutex;
 DeviceInfo g_dev[kMaxDevices];
 unsigned long long g_timeout_ns = kDefaultTimeoutNs;
 int g_inject = 0;  // fa_set_fault_injection
+int g_cta_pairs = 0;  // fa_set_cta_pairs
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                    const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -103,10 +104,11 @@ fa_status current_device(DeviceInfo **out) {
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // 4-D 16-bit tensor map over a (batch, seq, head, d) tensor, dimensions ordered
-// {d, head, seq, batch}, box {64, 1, 128, 1} (64 columns x 128 rows of one head), 128-byte
-// swizzle, zero fill past the tensor edges.  sn/sh/sb are element strides.
+// {d, head, seq, batch}, box {64, 1, box_rows, 1} (64 columns x 128 rows of one head, or 64
+// rows for the K halves of a CTA pair), 128-byte swizzle, zero fill past the tensor edges.
+// sn/sh/sb are element strides.
 fa_status make_map(CUtensorMap *map, const void *base, int d, int64_t n, int64_t h, int64_t b,
-                   int64_t sn, int64_t sh, int64_t sb, int dtype) {
+                   int64_t sn, int64_t sh, int64_t sb, int dtype, int box_rows = 128) {
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(h),
                         static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(b)};
   // The stride of a dimension of extent 1 is never used; give it a legal value.
@@ -120,7 +122,7 @@ fa_status make_map(CUtensorMap *map, const void *base, int d, int64_t n, int64_t
     if (strides[i] == 0 || (strides[i] % 16) != 0 || strides[i] >= (cuuint64_t(1) << 40))
       return FA_ERR_INVALID_ARG;
   // 128-byte box rows: 64 16-bit or 128 8-bit elements
-  cuuint32_t box[4] = {dtype == FA_E4M3 ? 128u : 64u, 1, 128, 1};
+  cuuint32_t box[4] = {dtype == FA_E4M3 ? 128u : 64u, 1, static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUtensorMapDataType ty =
       dtype == FA_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
@@ -200,6 +202,12 @@ constexpr int kMaxPrefillD = 256;
 constexpr int kMaxDecodeD = 256;
 
 int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
+
+// The 16-bit forward at width 128 runs on CTA pairs (cta_group::2) after fa_set_cta_pairs(1).
+bool use_pairs(int d) { return g_cta_pairs != 0 && fa::kernel_d(d) == 128; }
+
+// Query rows of a prefill work tile: 512 for CTA pairs (two 256-row sub-tiles).
+int tile_rows(int d, bool pairs) { return pairs ? 512 : fa::prefill_tile_rows(fa::kernel_d(d)); }
 
 // Keys per split for the decode path (a multiple of the 128-key block).
 int decode_chunk(int Lmax, int num_splits) {
@@ -312,6 +320,8 @@ void fa_set_wait_timeout_ns(unsigned long long ns) {
 
 void fa_set_fault_injection(int withhold_loads) { g_inject = withhold_loads != 0; }
 
+void fa_set_cta_pairs(int enable) { g_cta_pairs = enable != 0; }
+
 // Keys padded to a multiple of 16 (the byte stride of a transposed V row).
 int64_t nk_pad16(int64_t nk) { return (nk + 15) / 16 * 16; }
 
@@ -379,7 +389,7 @@ fa_status fa_fwd(const fa_fwd_params *p, cudaStream_t stream) {
         !stride_ok(a.v_strides[1], a.Nk) || !stride_ok(a.v_strides[2], a.Hkv))
       return FA_ERR_INVALID_ARG;
   }
-  const int mblocks = ceil_div(a.Nq, fa::prefill_tile_rows(fa::kernel_d(a.d)));
+  const int mblocks = ceil_div(a.Nq, tile_rows(a.d, false));
   const int64_t tiles = static_cast<int64_t>(a.B) * a.Hq * mblocks;
   if (tiles > INT32_MAX) return FA_ERR_INVALID_ARG;
   ModPlan mod;
@@ -397,7 +407,8 @@ fa_status fa_fwd(const fa_fwd_params *p, cudaStream_t stream) {
 fa_status launch_dense(const fa_fwd_params &a, DeviceInfo *dev, const ModPlan &mod,
                        int64_t lse_sb, int64_t lse_sh, cudaStream_t stream) {
   fa_status st;
-  const int mblocks = ceil_div(a.Nq, fa::prefill_tile_rows(fa::kernel_d(a.d)));
+  const bool pairs = use_pairs(a.d);
+  const int mblocks = ceil_div(a.Nq, tile_rows(a.d, pairs));
   const int64_t tiles = static_cast<int64_t>(a.B) * a.Hq * mblocks;
   if (a.Nk == 0) {
     cudaError_t e = fa::launch_fill_empty(a.o, a.lse, a.B, a.Nq, a.Hq, a.d, a.o_strides[0],
@@ -409,16 +420,21 @@ fa_status launch_dense(const fa_fwd_params &a, DeviceInfo *dev, const ModPlan &m
                      a.q_strides[0], a.dtype)) != FA_OK)
     return st;
   if ((st = make_map(&tk, a.k, a.d, a.Nk, a.Hkv, a.B, a.k_strides[1], a.k_strides[2],
-                     a.k_strides[0], a.dtype)) != FA_OK)
+                     a.k_strides[0], a.dtype, pairs ? 64 : 128)) != FA_OK)
     return st;
   if ((st = make_map(&tv, a.v, a.d, a.Nk, a.Hkv, a.B, a.v_strides[1], a.v_strides[2],
                      a.v_strides[0], a.dtype)) != FA_OK)
     return st;
   const fa::PrefillArgs pa = dense_args(a, mblocks, tiles, dev, mod, lse_sb, lse_sh);
-  const int grid = static_cast<int>(tiles < dev->sm_count ? tiles : dev->sm_count);
-  cudaError_t e =
-      fa::launch_prefill(fa::kernel_d(a.d), mod.mask, a.dtype == FA_FP16, tq, tk, tv, pa, grid,
-                         stream);
+  cudaError_t e;
+  if (pairs) {
+    e = fa::launch_prefill_pair(mod.mask, a.dtype == FA_FP16, tq, tk, tv, pa,
+                                static_cast<int>(tiles), stream);
+  } else {
+    const int grid = static_cast<int>(tiles < dev->sm_count ? tiles : dev->sm_count);
+    e = fa::launch_prefill(fa::kernel_d(a.d), mod.mask, a.dtype == FA_FP16, tq, tk, tv, pa, grid,
+                           stream);
+  }
   return e == cudaSuccess ? FA_OK : cuda_fail("prefill kernel launch", e);
 }
 
@@ -665,7 +681,8 @@ fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, fl
     return FA_ERR_INVALID_ARG;
   if (total_k > 0 && (k == nullptr || v == nullptr || !aligned(k, 16) || !aligned(v, 16)))
     return FA_ERR_INVALID_ARG;
-  const int mblocks = ceil_div(max_seqlen_q, fa::prefill_tile_rows(fa::kernel_d(d)));
+  const bool pairs = use_pairs(d);
+  const int mblocks = ceil_div(max_seqlen_q, tile_rows(d, pairs));
   const int64_t tiles = static_cast<int64_t>(B) * Hq * mblocks;
   if (tiles > INT32_MAX) return FA_ERR_INVALID_ARG;
   ModPlan mod;
@@ -685,8 +702,8 @@ fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, fl
   if ((st = make_map(&tq, q, d, total_q, Hq, 1, static_cast<int64_t>(Hq) * d, d, 0, dtype)) !=
       FA_OK)
     return st;
-  if ((st = make_map(&tk, k, d, total_k, Hkv, 1, static_cast<int64_t>(Hkv) * d, d, 0, dtype)) !=
-      FA_OK)
+  if ((st = make_map(&tk, k, d, total_k, Hkv, 1, static_cast<int64_t>(Hkv) * d, d, 0, dtype,
+                     pairs ? 64 : 128)) != FA_OK)
     return st;
   if ((st = make_map(&tv, v, d, total_k, Hkv, 1, static_cast<int64_t>(Hkv) * d, d, 0, dtype)) !=
       FA_OK)
@@ -719,10 +736,15 @@ fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, fl
   pa.sched_slot = fa::next_prefill_sched_slot();
   pa.d = d;
   apply_mod(mod, scale, &pa);
-  const int grid = static_cast<int>(tiles < dev->sm_count ? tiles : dev->sm_count);
-  cudaError_t e =
-      fa::launch_prefill(fa::kernel_d(d), mod.mask, dtype == FA_FP16, tq, tk, tv, pa, grid,
-                         stream);
+  cudaError_t e;
+  if (pairs) {
+    e = fa::launch_prefill_pair(mod.mask, dtype == FA_FP16, tq, tk, tv, pa,
+                                static_cast<int>(tiles), stream);
+  } else {
+    const int grid = static_cast<int>(tiles < dev->sm_count ? tiles : dev->sm_count);
+    e = fa::launch_prefill(fa::kernel_d(d), mod.mask, dtype == FA_FP16, tq, tk, tv, pa, grid,
+                           stream);
+  }
   return e == cudaSuccess ? FA_OK : cuda_fail("prefill kernel launch", e);
 }
 

@@ -78,6 +78,13 @@ cudaError_t launch_prefill(int d, int mask, bool f16, const CUtensorMap &tq,
                            const CUtensorMap &tk, const CUtensorMap &tv, const PrefillArgs &a,
                            int grid, cudaStream_t stream);
 
+// The width-128 16-bit prefill on CTA pairs (clusters of two computing each 256-row sub-tile
+// as one cta_group::2 product; work tiles of 512 query rows): tk is a K map with 64-row boxes,
+// tq and tv maps with 128-row boxes.  The grid is sized inside from `tiles`.
+cudaError_t launch_prefill_pair(int mask, bool f16, const CUtensorMap &tq, const CUtensorMap &tk,
+                                const CUtensorMap &tv, const PrefillArgs &a, int tiles,
+                                cudaStream_t stream);
+
 // FP8 (E4M3) prefill, d <= 128 at kernel width 128: tq, tk over E4M3 Q and K, tvt over the
 // transposed V written by launch_transpose_v (dims {keys, d, kv head, batch}).
 cudaError_t launch_prefill_fp8(int mask, const CUtensorMap &tq, const CUtensorMap &tk,

@@ -76,16 +76,22 @@ __host__ __device__ constexpr uint32_t o_col(int t) {
 // columns), ring slots of half a tile (the d halves), PV as two N = 128 products.
 // F8 (E4M3 inputs, D = 128): one 128-byte box per row; V arrives transposed ([d, keys],
 // K-major like K), P goes through shared memory as E4M3 (both PV operands K-major).
-template <int D, bool F16 = false, bool F8 = false>
+// PAIR (D = 128, 16-bit): a CTA pair computes each sub-tile as one M = 256 product
+// (cta_group::2): each CTA holds 128 of its query rows; a ring slot holds this CTA's half of
+// a K tile (64 keys x D) or of a V tile (128 keys x D / 2 columns), so the pair reads each
+// K/V tile once and each CTA half of it.
+template <int D, bool F16 = false, bool F8 = false, bool PAIR = false>
 struct Cfg {
   static constexpr bool WIDE = D > 128;
   static constexpr int NSUB = WIDE ? 1 : 2;              // query sub-tiles per work tile
+  static constexpr int SUB_ROWS = PAIR ? 256 : BR;       // query rows of a sub-tile (MMA M)
   static constexpr int EB = F8 ? 1 : 2;                  // bytes per element
   static constexpr int KCH = D * EB / 128;               // 128-byte boxes per row
   static constexpr int BOX_ELEMS = 128 / EB;             // elements of a row per box
   static constexpr int TILE_BYTES = KCH * BOX_BYTES;     // one [128 x D] tile
-  static constexpr int SLOT_BYTES = WIDE ? TILE_BYTES / 2 : TILE_BYTES;
-  static constexpr int NSLOTS = WIDE ? 5 : (F8 ? 8 : (D == 128 ? 4 : 8));  // K/V ring depth
+  static constexpr int SLOT_BYTES = (WIDE || PAIR) ? TILE_BYTES / 2 : TILE_BYTES;
+  static constexpr int NSLOTS =
+      PAIR ? 10 : (WIDE ? 5 : (F8 ? 8 : (D == 128 ? 4 : 8)));  // K/V ring depth
   static constexpr int Q_OFF = 0;
   static constexpr int RING_OFF = NSUB * TILE_BYTES;
   static constexpr int P_OFF = RING_OFF + NSLOTS * SLOT_BYTES;  // F8: E4M3 P per sub-tile
@@ -93,12 +99,14 @@ struct Cfg {
   static constexpr int BAR_OFF = P_OFF + P_BYTES;
   static constexpr int SMEM_BYTES = BAR_OFF + 512 + 1024;  // barriers + alignment slack
   static constexpr uint32_t IDESC_S =
-      F8 ? idesc_e4m3_f32(128, BC) : idesc_bf16_f32(128, BC, false, false, F16);
+      F8 ? idesc_e4m3_f32(128, BC) : idesc_bf16_f32(SUB_ROWS, BC, false, false, F16);
   static constexpr uint32_t IDESC_PV =
-      F8 ? idesc_e4m3_f32(128, D) : idesc_bf16_f32(128, WIDE ? 128 : D, false, true, F16);
+      F8 ? idesc_e4m3_f32(128, D) : idesc_bf16_f32(SUB_ROWS, WIDE ? 128 : D, false, true, F16);
+  static_assert(!PAIR || (D == 128 && !F8), "CTA pairs: 16-bit inputs at width 128");
 };
 static_assert(Cfg<128, false, true>::SMEM_BYTES <= 227 * 1024, "fp8 prefill exceeds smem");
 static_assert(Cfg<256>::SMEM_BYTES <= 227 * 1024, "wide prefill exceeds shared memory");
+static_assert(Cfg<128, false, false, true>::SMEM_BYTES <= 227 * 1024, "pair prefill exceeds smem");
 
 // Per-launch tile-ticket counters: [slot][0] = next ticket, [slot][1] = CTAs finished.
 // The host gives each launch its own slot (round robin); the last CTA of a launch to
@@ -109,13 +117,15 @@ struct Bars {
   uint64_t sched_full[SCHED_DEPTH], sched_empty[SCHED_DEPTH];
   int sched_tile[SCHED_DEPTH];
   uint64_t q_full, q_empty;
-  uint64_t kv_full[8], kv_empty[8];
+  uint64_t kv_full[10], kv_empty[10];
   uint64_t s_full[2], p_ready[2], o_full[2], o_empty[2];  // per sub-tile (wide: per S buffer)
   uint64_t pv_done;  // wide: PV(j) complete, before the softmax of j + 1 rescales O
   uint64_t mma_done;
+  uint64_t exit_bar;  // CTA pairs: both CTAs are done with each other's shared memory
   uint32_t tmem_base;
   int abort;
 };
+static_assert(sizeof(Bars) <= 512, "prefill barriers exceed their shared-memory region");
 
 struct TileInfo {
   int b, h, hk;
@@ -130,7 +140,8 @@ struct TileInfo {
   int js[2], je[2], nkv[2];
 };
 
-template <int MASK, int NSUB>
+// SUB: query rows of a sub-tile (128; 256 for a CTA pair, whose CTAs hold 128 rows each).
+template <int MASK, int NSUB, int SUB = BR>
 __device__ __forceinline__ TileInfo tile_info(const PrefillArgs &a, int tile) {
   TileInfo ti;
   const int bh = tile / a.mblocks;
@@ -140,7 +151,7 @@ __device__ __forceinline__ TileInfo tile_info(const PrefillArgs &a, int tile) {
   ti.b = bh / a.Hq;
   ti.h = bh - ti.b * a.Hq;
   ti.hk = ti.h / a.group;
-  ti.q_row0 = mb * NSUB * BR;
+  ti.q_row0 = mb * NSUB * SUB;
   if (a.varlen) {
     const int q0 = a.cu_q[ti.b], q1 = a.cu_q[ti.b + 1];
     const int k0 = a.cu_k[ti.b], k1 = a.cu_k[ti.b + 1];
@@ -162,8 +173,8 @@ __device__ __forceinline__ TileInfo tile_info(const PrefillArgs &a, int tile) {
   int lo[2], hi[2];  // K/V tile range [lo, hi) of each sub-tile
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
-    const int first = ti.q_row0 + t * BR;
-    const int nr = t < NSUB ? min(max(ti.nq - first, 0), BR) : 0;
+    const int first = ti.q_row0 + t * SUB;
+    const int nr = t < NSUB ? min(max(ti.nq - first, 0), SUB) : 0;
     ti.nrows[t] = nr;
     lo[t] = 0;
     hi[t] = 0;
@@ -239,6 +250,36 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint3
     mma_bf16_ts_w(o_tmem, p_tmem + static_cast<uint32_t>(kk * 8),
                   sw128_desc(v_smem + static_cast<uint32_t>(kk * 16 * 128), BOX_BYTES, 1024),
                   Cfg<D, F16>::IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+// CTA pairs (issued by the even CTA; both CTAs' operands at the same addresses).
+// S_t = Q_t K^T as M = 256: each CTA's Q sub-tile holds its 128 rows (128-row boxes), its
+// K half holds 64 keys (64-row boxes, 8 KB apart); D/16 MMAs of 256 x 128 x 16.
+template <int D, bool F16>
+__device__ __forceinline__ void issue_s_pair(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t in_row = static_cast<uint32_t>((kk & 3) * 32);
+    mma_bf16_ss_pair_w(d_tmem,
+                       sw128_desc(q_smem + static_cast<uint32_t>((kk >> 2) * BOX_BYTES) + in_row,
+                                  16, 1024),
+                       sw128_desc(k_smem + static_cast<uint32_t>((kk >> 2) * (BOX_BYTES / 2)) +
+                                      in_row, 16, 1024),
+                       Cfg<D, F16, false, true>::IDESC_S, kk > 0 ? 1u : 0u);
+  }
+}
+
+// O_t (+)= P_t V as M = 256, N = D: P from each CTA's TMEM, each CTA's V half one MN-major box
+// of D / 2 = 64 columns for the 128 keys (16 keys = 2048 bytes per k-step).
+template <int D, bool F16>
+__device__ __forceinline__ void issue_pv_pair(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_smem,
+                                              bool accumulate) {
+#pragma unroll
+  for (int kk = 0; kk < BC / 16; ++kk) {
+    mma_bf16_ts_pair_w(o_tmem, p_tmem + static_cast<uint32_t>(kk * 8),
+                       sw128_desc(v_smem + static_cast<uint32_t>(kk * 16 * 128), BOX_BYTES, 1024),
+                       Cfg<D, F16, false, true>::IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
@@ -366,6 +407,106 @@ out:
   if (q_iter > 0) mbar_wait_teardown(&bars->q_full, (q_iter - 1) & 1u, 1000000000ull);
 }
 
+// Scheduler + producer of a CTA pair (one lane in each CTA).  The even CTA takes the tickets
+// and publishes each tile to both CTAs' scheduler rings (its own, and the odd CTA's through a
+// shared::cluster store and a remote arrival); every consumer of both CTAs frees the entry on
+// the even CTA's ring.  Each CTA loads its own 128 rows of both query sub-tiles, and its half
+// of every K tile (keys [64 rank, 64 rank + 64)) and V tile (columns [64 rank, 64 rank + 64)),
+// counted on the even CTA's barriers, where the even CTA posts the bytes of both halves.  The
+// ring order and slot sequence are the same in both CTAs.
+template <int D, int MASK>
+__device__ void producer_role_pair(const PrefillArgs &a, const CUtensorMap *tmq,
+                                   const CUtensorMap *tmk, const CUtensorMap *tmv, uint8_t *smem,
+                                   Bars *bars, const WaitCtl &wc, uint32_t rank) {
+  using C = Cfg<D, false, false, true>;
+  uint32_t kv_iter = 0, q_iter = 0;
+  unsigned int *ctr = g_sched[a.sched_slot];
+  const uint32_t peer = rank ^ 1u;
+  auto load_half = [&](bool is_v, int hk, int row0, int b) {
+    const int slot = static_cast<int>(kv_iter % C::NSLOTS);
+    const uint32_t use = kv_iter / C::NSLOTS;
+    if (!mbar_wait(&bars->kv_empty[slot], (use & 1u) ^ 1u, wc)) return false;
+    if (*wc.abort) return false;
+    if (rank == 0) mbar_arrive_expect_tx(&bars->kv_full[slot], 2 * C::SLOT_BYTES);
+    const uint32_t fb = mapa_shared(&bars->kv_full[slot], 0);
+    uint8_t *dst = smem + C::RING_OFF + slot * C::SLOT_BYTES;
+    if (is_v) {
+      tma_load_4d_pair(dst, tmv, fb, static_cast<int>(rank) * 64, hk, row0, b);
+    } else {
+#pragma unroll
+      for (int c = 0; c < C::KCH; ++c)
+        tma_load_4d_pair(dst + c * (BOX_BYTES / 2), tmk, fb, c * 64, hk,
+                         row0 + static_cast<int>(rank) * 64, b);
+    }
+    ++kv_iter;
+    return true;
+  };
+  for (uint32_t k = 0;; ++k) {
+    if (a.inject) break;  // failure injection: no ticket, no load
+    const int rs = static_cast<int>(k % SCHED_DEPTH);
+    int tile;
+    if (rank == 0) {
+      const int ticket = static_cast<int>(atomicAdd(&ctr[0], 1u));
+      tile = ticket < a.num_tiles ? ticket : -1;
+      if (!mbar_wait_cluster(&bars->sched_empty[rs], ((k / SCHED_DEPTH) & 1u) ^ 1u, wc)) goto out;
+      bars->sched_tile[rs] = tile;
+      st_cluster_u32(mapa_shared(&bars->sched_tile[rs], peer), static_cast<uint32_t>(tile));
+      mbar_arrive(&bars->sched_full[rs]);
+      mbar_arrive_cluster(mapa_shared(&bars->sched_full[rs], peer));
+    } else {
+      if (!mbar_wait_cluster(&bars->sched_full[rs], (k / SCHED_DEPTH) & 1u, wc)) goto out;
+      tile = bars->sched_tile[rs];
+      mbar_arrive_cluster(mapa_shared(&bars->sched_empty[rs], 0));
+    }
+    if (tile < 0) break;
+    const TileInfo ti = tile_info<MASK, 2, C::SUB_ROWS>(a, tile);
+    if (rank == 0 && a.varlen && ti.q_row0 == 0 && varlen_bad(a, ti.b))
+      atomicOr(a.err, DEVERR_BAD_CU_SEQLENS);
+    const int n = max(ti.je[0], ti.je[1]);
+    if (n == 0) continue;
+    if (q_iter > 0 && !mbar_wait(&bars->q_empty, (q_iter - 1) & 1u, wc)) goto out;
+    if (*wc.abort) goto out;
+    if (rank == 0) mbar_arrive_expect_tx(&bars->q_full, 2 * C::NSUB * C::TILE_BYTES);
+    {
+      const uint32_t qb = mapa_shared(&bars->q_full, 0);
+#pragma unroll
+      for (int t = 0; t < C::NSUB; ++t)
+#pragma unroll
+        for (int c = 0; c < C::KCH; ++c)
+          tma_load_4d_pair(smem + C::Q_OFF + t * C::TILE_BYTES + c * BOX_BYTES, tmq, qb, c * 64,
+                           ti.h, ti.q_tok + ti.q_row0 + t * C::SUB_ROWS + static_cast<int>(rank) * BR,
+                           ti.tma_b);
+    }
+    ++q_iter;
+    const int krow = ti.k_tok + ti.kv0 * BC;
+    for (int j = 0; j < n; ++j)
+      if (!load_half(false, ti.hk, krow + j * BC, ti.tma_b) ||
+          !load_half(true, ti.hk, krow + j * BC, ti.tma_b))
+        goto out;
+  }
+out:
+  if (rank == 0) {
+    // As in the single-CTA producer; only even CTAs take tickets.
+    const unsigned int pairs = gridDim.x / 2;
+    __threadfence();
+    if (atomicAdd(&ctr[1], 1u) == pairs - 1) {
+      const unsigned int taken = atomicAdd(&ctr[0], 0u);
+      if (!a.inject && taken != static_cast<unsigned int>(a.num_tiles) + pairs)
+        atomicOr(a.err, DEVERR_SCHED_OVERLAP);
+      atomicExch(&ctr[0], 0u);
+      atomicExch(&ctr[1], 0u);
+    }
+    // Teardown: both CTAs' loads are counted here; let every armed phase complete.
+    for (int s2 = 0; s2 < C::NSLOTS; ++s2) {
+      if (kv_iter > static_cast<uint32_t>(s2)) {
+        const uint32_t uses = (kv_iter - 1 - s2) / C::NSLOTS + 1;
+        mbar_wait_teardown(&bars->kv_full[s2], (uses - 1) & 1u, 1000000000ull);
+      }
+    }
+    if (q_iter > 0) mbar_wait_teardown(&bars->q_full, (q_iter - 1) & 1u, 1000000000ull);
+  }
+}
+
 // Bounded wait by a whole warp; every lane gets the same answer.
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const WaitCtl &wc) {
   const bool ok = mbar_wait(bar, parity, wc);
@@ -488,6 +629,97 @@ out:
   mbar_wait_teardown(&bars->mma_done, 0u, 1000000000ull);
 }
 
+// MMA issuer of a CTA pair (the even CTA's MMA warp): the order of mma_role, every product
+// an M = 256 cta_group::2 MMA over both CTAs' rows, every commit multicast to the barrier at
+// the same offset in both CTAs.  p_ready and o_empty count the softmax warps of both CTAs.
+template <int D, int MASK, bool F16>
+__device__ void mma_role_pair(const PrefillArgs &a, uint8_t *smem, Bars *bars, uint32_t tmem,
+                              const WaitCtl &wc, int lane) {
+  using C = Cfg<D, F16, false, true>;
+  uint32_t kv_iter = 0, q_iter = 0;
+  uint32_t p_phase[2] = {0u, 0u}, oe_phase[2] = {0u, 0u};
+  bool o_pending[2] = {false, false};
+  const uint32_t q_smem[2] = {smem_u32(smem + C::Q_OFF), smem_u32(smem + C::Q_OFF + C::TILE_BYTES)};
+  const uint32_t ring = smem_u32(smem + C::RING_OFF);
+  auto wait_c = [&](uint64_t *bar, uint32_t parity) {
+    const bool ok = mbar_wait_cluster(bar, parity, wc);
+    return __all_sync(0xffffffffu, ok);
+  };
+  for (uint32_t k = 0;; ++k) {
+    int tile;
+    {
+      const int rs = static_cast<int>(k % SCHED_DEPTH);
+      if (!wait_c(&bars->sched_full[rs], (k / SCHED_DEPTH) & 1u)) goto out;
+      tile = bars->sched_tile[rs];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->sched_empty[rs]);
+    }
+    if (tile < 0) break;
+    {
+      const TileInfo ti = tile_info<MASK, 2, C::SUB_ROWS>(a, tile);
+      const int n = max(ti.je[0], ti.je[1]);
+      if (n == 0) continue;
+      if (!wait_c(&bars->q_full, q_iter & 1u)) goto out;
+      ++q_iter;
+      int slot_k = static_cast<int>(kv_iter % C::NSLOTS);
+      if (!wait_c(&bars->kv_full[slot_k], (kv_iter / C::NSLOTS) & 1u)) goto out;
+      ++kv_iter;
+      tc_fence_after();
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        if (ti.js[t] == 0 && ti.je[t] > 0) {
+          issue_s_pair<D, F16>(tmem + s_col(t), q_smem[t], ring + slot_k * C::SLOT_BYTES);
+          mma_commit_pair_w(&bars->s_full[t]);
+        }
+      }
+      mma_commit_pair_w(&bars->kv_empty[slot_k]);
+      for (int j = 0; j < n; ++j) {
+        const int slot_v = static_cast<int>(kv_iter % C::NSLOTS);
+        if (!wait_c(&bars->kv_full[slot_v], (kv_iter / C::NSLOTS) & 1u)) goto out;
+        ++kv_iter;
+        slot_k = -1;
+        if (j + 1 < n) {
+          slot_k = static_cast<int>(kv_iter % C::NSLOTS);
+          if (!wait_c(&bars->kv_full[slot_k], (kv_iter / C::NSLOTS) & 1u)) goto out;
+          ++kv_iter;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (j >= ti.js[t] && j < ti.je[t]) {
+            if (j == ti.js[t] && o_pending[t]) {
+              if (!warp_wait(&bars->o_empty[t], oe_phase[t], wc)) goto out;
+              oe_phase[t] ^= 1u;
+              o_pending[t] = false;
+            }
+            if (!warp_wait(&bars->p_ready[t], p_phase[t], wc)) goto out;
+            p_phase[t] ^= 1u;
+            tc_fence_after();
+            issue_pv_pair<D, F16>(tmem + o_col(t), tmem + s_col(t),
+                                  ring + slot_v * C::SLOT_BYTES, j > ti.js[t]);
+            if (j == ti.je[t] - 1) {
+              mma_commit_pair_w(&bars->o_full[t]);
+              o_pending[t] = true;
+            }
+          }
+          if (t == 1) mma_commit_pair_w(&bars->kv_empty[slot_v]);
+          if (j + 1 >= ti.js[t] && j + 1 < ti.je[t]) {
+            issue_s_pair<D, F16>(tmem + s_col(t), q_smem[t], ring + slot_k * C::SLOT_BYTES);
+            mma_commit_pair_w(&bars->s_full[t]);
+          }
+        }
+        if (slot_k >= 0) mma_commit_pair_w(&bars->kv_empty[slot_k]);
+      }
+      mma_commit_pair_w(&bars->q_empty);
+    }
+  }
+out:
+  // Teardown: every MMA issued so far (into both CTAs) must finish before TMEM is released;
+  // the commit reaches the odd CTA's mma_done too.
+  mma_commit_pair_w(&bars->mma_done);
+  mbar_wait_teardown(&bars->mma_done, 0u, 1000000000ull);
+}
+
 // MMA issuer of the wide kernel (one sub-tile, S double-buffered in TMEM columns
 // [0,128) and [128,256), O in [256,512)).  Order per tile of n K/V steps:
 //   S(0), S(1), PV(0), S(2), PV(1), S(3), ..., PV(n-1)
@@ -583,10 +815,32 @@ out:
 // ------------------------------------------------------------------------------------
 // Softmax / correction / epilogue: one thread per query row of its sub-tile.
 
-template <int D, int MASK, bool F16, bool F8 = false>
+// PAIR: the sub-tile is 256 rows over both CTAs of a pair; this CTA holds rows
+// [128 rank, 128 rank + 128) of it, and takes part in every step of the sub-tile (the MMA
+// covers both CTAs) whether or not its own rows are valid.  p_ready, o_empty and the
+// scheduler ring are the even CTA's: one arrival per warp, with cluster-scope release.
+template <int D, int MASK, bool F16, bool F8 = false, bool PAIR = false>
 __device__ void softmax_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, uint32_t tmem,
                              const WaitCtl &wc, int warp, int lane) {
-  using C = Cfg<D, F16, F8>;
+  using C = Cfg<D, F16, F8, PAIR>;
+  const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
+  // Arrival on a barrier of the even CTA (after this thread's tcgen05 fences): one per warp
+  // for a pair, one per thread otherwise.  TMEM: the handoffs of P (p_ready) and of the read
+  // O (o_empty), whose TMEM stores / loads every lane has completed (tcgen05.wait) before the
+  // warp arrives; the scheduler ring's entry is shared memory and takes cluster scope.
+  auto arrive_leader = [&](uint64_t *bar, bool tmem_data) {
+    if constexpr (PAIR) {
+      __syncwarp();
+      if (lane == 0) {
+        if (tmem_data)
+          mbar_arrive_remote(mapa_shared(bar, 0));
+        else
+          mbar_arrive_cluster(mapa_shared(bar, 0));
+      }
+    } else {
+      mbar_arrive(bar);
+    }
+  };
   // FP8: P is rounded to E4M3 as 2^8 P (values up to 256 of the format's 448, so that small
   // probabilities keep their significant bits); O = sum(P' V) / sum(P') is unchanged and
   // the LSE takes the 8 back out.
@@ -612,14 +866,24 @@ __device__ void softmax_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, ui
 
   for (uint32_t k = 0;; ++k) {
     int tile;
-    if (!next_tile<true>(bars, k, tile, wc)) return;
+    if constexpr (PAIR) {
+      const int rs = static_cast<int>(k % SCHED_DEPTH);
+      const bool ok = __all_sync(0xffffffffu, mbar_wait_cluster(&bars->sched_full[rs],
+                                                                (k / SCHED_DEPTH) & 1u, wc));
+      if (!ok) return;
+      tile = bars->sched_tile[rs];
+      arrive_leader(&bars->sched_empty[rs], false);
+    } else {
+      if (!next_tile<true>(bars, k, tile, wc)) return;
+    }
     if (tile < 0) break;
-    const TileInfo ti = tile_info<MASK, C::NSUB>(a, tile);
-    const int nrows = t == 0 ? ti.nrows[0] : ti.nrows[1];
-    if (nrows == 0) continue;
+    const TileInfo ti = tile_info<MASK, C::NSUB, C::SUB_ROWS>(a, tile);
+    const int sub_rows = t == 0 ? ti.nrows[0] : ti.nrows[1];  // rows of the whole sub-tile
+    if (sub_rows == 0) continue;
     const int nkv = t == 0 ? ti.nkv[0] : ti.nkv[1];
     const int kt0 = ti.kv0 + (t == 0 ? ti.js[0] : ti.js[1]);  // first K/V tile of this sub-tile
-    const int first_row = ti.q_row0 + t * BR;
+    const int first_row = ti.q_row0 + t * C::SUB_ROWS + rank * BR;  // this CTA's first row
+    const int nrows = min(max(sub_rows - rank * BR, 0), BR);       // this CTA's rows
     const int row = first_row + rit;
     const bool row_ok = rit < nrows;
     const int off = ti.nk - ti.nq;  // bottom-right alignment: row i sits at key position i + off
@@ -829,7 +1093,7 @@ __device__ void softmax_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, ui
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&bars->p_ready[sb]);
+      arrive_leader(&bars->p_ready[sb], true);
       m = m_new;
     }
 
@@ -861,7 +1125,7 @@ __device__ void softmax_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, ui
         }
       }
       tc_fence_before();
-      mbar_arrive(&bars->o_empty[t]);
+      arrive_leader(&bars->o_empty[t], true);
     } else if (row_ok) {
       uint4 *dst = reinterpret_cast<uint4 *>(orow);
 #pragma unroll
@@ -875,22 +1139,25 @@ __device__ void softmax_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, ui
   }
 }
 
-template <int D, int MASK, bool F16, bool F8 = false>
+template <int D, int MASK, bool F16, bool F8 = false, bool PAIR = false>
 __global__ void __launch_bounds__(NTHREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv, const PrefillArgs a) {
-  using C = Cfg<D, F16, F8>;
+  using C = Cfg<D, F16, F8, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   Bars *bars = reinterpret_cast<Bars *>(smem + C::BAR_OFF);
   const int warp = static_cast<int>(threadIdx.x) >> 5;
   const int lane = static_cast<int>(threadIdx.x) & 31;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < SCHED_DEPTH; ++i) {
       mbar_init(&bars->sched_full[i], 1);
-      mbar_init(&bars->sched_empty[i], 1 + 128 * C::NSUB);  // MMA lane + every softmax thread
+      // MMA warp + every softmax thread; a pair: the even CTA's MMA warp, one arrival per
+      // softmax warp of both CTAs and the odd CTA's producer
+      mbar_init(&bars->sched_empty[i], PAIR ? 1 + 2 * 4 * C::NSUB + 1 : 1 + 128 * C::NSUB);
     }
     mbar_init(&bars->q_full, 1);
     mbar_init(&bars->q_empty, 1);
@@ -900,12 +1167,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->s_full[t], 1);
-      mbar_init(&bars->p_ready[t], 128);
+      mbar_init(&bars->p_ready[t], PAIR ? 8 : 128);  // pair: 4 warps of each CTA
       mbar_init(&bars->o_full[t], 1);
-      mbar_init(&bars->o_empty[t], 128);
+      mbar_init(&bars->o_empty[t], PAIR ? 8 : 128);
     }
     mbar_init(&bars->pv_done, 1);
     mbar_init(&bars->mma_done, 1);
+    mbar_init(&bars->exit_bar, 2);
     bars->abort = 0;
     fence_barrier_init();
   }
@@ -915,14 +1183,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tma_prefetch_desc(&tmv);
   }
   if (warp == MMA_WARP) {
-    tmem_alloc(&bars->tmem_base, TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(&bars->tmem_base, TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(&bars->tmem_base, TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) {
+    // Both CTAs' barriers are initialised before either CTA signals the other's.  (The two
+    // CTAs of a cluster run together, so this wait always ends.)
+    asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;"
+                 ::: "memory");
+  } else {
+    __syncthreads();
+  }
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
-  const WaitCtl wc{&bars->abort, a.err, a.timeout_ns, DEVERR_PREFILL_TIMEOUT};
+  const WaitCtl wc{&bars->abort, a.err, a.timeout_ns, DEVERR_PREFILL_TIMEOUT,
+                   PAIR ? mapa_shared(&bars->abort, rank ^ 1u) : 0u};
 
   // Each register-split branch ends the kernel on its own; the two meet at a named barrier
   // before TMEM is released.
@@ -934,7 +1215,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(IDLE_REGS));
     } else {
       asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(SOFTMAX_REGS));
-      softmax_role<D, MASK, F16, F8>(a, smem, bars, tmem, wc, warp, lane);
+      softmax_role<D, MASK, F16, F8, PAIR>(a, smem, bars, tmem, wc, warp, lane);
     }
     __syncwarp();
     tc_fence_before();
@@ -942,19 +1223,46 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   } else {
     if constexpr (!C::WIDE) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(OTHER_REGS));
     if (warp == PRODUCER_WARP) {
-      if (lane == 0) producer_role<D, MASK, F8>(a, &tmq, &tmk, &tmv, smem, bars, wc);
+      if constexpr (PAIR) {
+        if (lane == 0) producer_role_pair<D, MASK>(a, &tmq, &tmk, &tmv, smem, bars, wc, rank);
+      } else {
+        if (lane == 0) producer_role<D, MASK, F8>(a, &tmq, &tmk, &tmv, smem, bars, wc);
+      }
     } else if (warp == MMA_WARP) {
-      if constexpr (C::WIDE)
+      if constexpr (PAIR) {
+        if (rank == 0) {
+          mma_role_pair<D, MASK, F16>(a, smem, bars, tmem, wc, lane);
+        } else {
+          // The even CTA's last commit (its teardown) reaches this CTA's mma_done too.
+          mbar_wait_teardown(&bars->mma_done, 0u, 2 * a.timeout_ns + 1000000000ull);
+        }
+      } else if constexpr (C::WIDE) {
         mma_role_wide<D, MASK, F16>(a, smem, bars, tmem, wc, lane);
-      else
+      } else {
         mma_role<D, MASK, F16, F8>(a, smem, bars, tmem, wc, lane);
+      }
     }
     __syncwarp();
     tc_fence_before();
     named_barrier(1, NTHREADS);
     if (warp == MMA_WARP) {
-      tc_fence_after();
-      tmem_dealloc(tmem, TMEM_COLS);
+      if constexpr (PAIR) {
+        // Neither CTA leaves (and frees its shared memory) while the other may still signal
+        // it: each arrives on both exit barriers once all its roles are done, then waits for
+        // the other's arrival (bounded).
+        if (lane == 0) {
+          mbar_arrive_cluster(mapa_shared(&bars->exit_bar, rank ^ 1u));
+          mbar_arrive(&bars->exit_bar);
+        }
+        __syncwarp();
+        mbar_wait_teardown(&bars->exit_bar, 0u, 2 * a.timeout_ns + 1000000000ull);
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, TMEM_COLS);
+      } else {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+      }
     }
   }
 }
@@ -967,6 +1275,48 @@ cudaError_t launch_impl(const CUtensorMap &tq, const CUtensorMap &tk, const CUte
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   prefill_kernel<D, MASK, F16, F8><<<grid, NTHREADS, smem, stream>>>(tq, tk, tv, a);
+  return cudaGetLastError();
+}
+
+// CTA pairs: clusters of two; `clusters` pairs (at most the number that fit on the GPU at
+// once, from the occupancy query, so that every pair of the persistent grid runs together).
+template <int MASK, bool F16>
+cudaError_t launch_pair_impl(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                             const PrefillArgs &a, int tiles, cudaStream_t stream) {
+  constexpr int smem = Cfg<128, F16, false, true>::SMEM_BYTES;
+  auto kern = prefill_kernel<128, MASK, F16, false, true>;
+  static int max_clusters[64] = {};  // per device, found on the first launch there
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(NTHREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (max_clusters[dev] == 0) {
+    int sms = 0;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return e;
+    cfg.gridDim = dim3(static_cast<unsigned>(sms / 2 * 2), 1, 1);
+    int n = 0;
+    if ((e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg)) != cudaSuccess) return e;
+    if (n < 1) return cudaErrorInvalidConfiguration;
+    max_clusters[dev] = n;
+  }
+  const int clusters = tiles < max_clusters[dev] ? tiles : max_clusters[dev];
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
+  e = cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -1060,6 +1410,26 @@ cudaError_t launch_transpose_v(const void *v, int64_t v_sb, int64_t v_sn, int64_
   transpose_v_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint8_t *>(v), v_sb, v_sn, v_sh,
                                               static_cast<uint8_t *>(vt), Nk, Hkv, d, nk_pad);
   return cudaGetLastError();
+}
+
+template <bool F16>
+cudaError_t launch_pair_mask(int mask, const CUtensorMap &tq, const CUtensorMap &tk,
+                             const CUtensorMap &tv, const PrefillArgs &a, int tiles,
+                             cudaStream_t stream) {
+  switch (mask) {
+    case MASK_NONE: return launch_pair_impl<MASK_NONE, F16>(tq, tk, tv, a, tiles, stream);
+    case MASK_CAUSAL: return launch_pair_impl<MASK_CAUSAL, F16>(tq, tk, tv, a, tiles, stream);
+    case MASK_WINDOW: return launch_pair_impl<MASK_WINDOW, F16>(tq, tk, tv, a, tiles, stream);
+    case MASK_ALIBI: return launch_pair_impl<MASK_ALIBI, F16>(tq, tk, tv, a, tiles, stream);
+    default: return launch_pair_impl<MASK_MOD, F16>(tq, tk, tv, a, tiles, stream);
+  }
+}
+
+cudaError_t launch_prefill_pair(int mask, bool f16, const CUtensorMap &tq, const CUtensorMap &tk,
+                                const CUtensorMap &tv, const PrefillArgs &a, int tiles,
+                                cudaStream_t stream) {
+  return f16 ? launch_pair_mask<true>(mask, tq, tk, tv, a, tiles, stream)
+             : launch_pair_mask<false>(mask, tq, tk, tv, a, tiles, stream);
 }
 
 cudaError_t launch_prefill(int d, int mask, bool f16, const CUtensorMap &tq,

@@ -67,15 +67,40 @@ struct WaitCtl {
   unsigned int *err;    // device error word (global memory)
   unsigned long long timeout_ns;
   unsigned int code;
+  uint32_t peer_abort;  // CTA pairs: the peer CTA's abort flag (shared::cluster address), or 0
 };
 
+// Same as mbar_try_wait, with cluster-scope acquire: for phases completed by arrivals of the
+// peer CTA of a pair, whose writes (shared memory, Tensor Memory) the waiter then reads.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// The slow path polls the barrier 32 times between reads of the abort flag and of
+// %globaltimer: a timer read on every poll made a handoff between two CTAs of a pair about
+// 270 cycles later to be seen (measured round trip 1374 cycles against 839 without it).
+template <bool CLUSTER>
 __device__ __forceinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, const WaitCtl &c) {
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
     if (*c.abort) return false;
     if (globaltimer_ns() - t0 > c.timeout_ns) {
       *c.abort = 1;
+      if (c.peer_abort != 0)  // the peer CTA of a pair unwinds too
+        asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(c.peer_abort), "r"(1) : "memory");
       atomicOr(c.err, c.code);
       return false;
     }
@@ -84,7 +109,13 @@ __device__ __forceinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, c
 
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const WaitCtl &c) {
   if (mbar_try_wait(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity, c);
+  return mbar_wait_slow<false>(bar, parity, c);
+}
+
+// Bounded wait with cluster-scope acquire (see mbar_try_wait_cluster).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, const WaitCtl &c) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  return mbar_wait_slow<true>(bar, parity, c);
 }
 
 // Wait used only on the teardown path: ignores the abort flag, bounded by a fixed time.
@@ -95,6 +126,43 @@ __device__ __forceinline__ bool mbar_wait_teardown(uint64_t *bar, uint32_t parit
     if (globaltimer_ns() - t0 > limit_ns) return false;
   }
   return true;
+}
+
+// ---------------------------------------------------------------------------------------
+// CTA pairs (a cluster of two CTAs whose tensor-core work is issued as cta_group::2).
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// shared::cluster address of the variable at the same offset as `p` in CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(const void *p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+
+// Arrive on an mbarrier given by its shared::cluster address (this CTA's or the peer's), with
+// cluster-scope release: orders this thread's earlier memory accesses (a shared::cluster store,
+// say) before the arrival for the peer CTA's threads.  A round trip of two such handoffs
+// measured 839 cycles.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+               : "memory");
+}
+
+// Arrive on a (possibly remote) mbarrier with the default CTA-scope semantics: a round trip
+// measured 200 cycles.  For handoffs whose data is Tensor Memory the arriving thread has
+// already completed (tcgen05.wait::st / wait::ld) before it arrives, so no memory ordering
+// toward the other CTA is needed beyond the arrival itself.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
 // Named barrier among `nthreads` threads (a multiple of 32) of the CTA.
@@ -128,6 +196,19 @@ __device__ __forceinline__ void tma_load_4d_hint(void *dst, const CUtensorMap *m
       ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;"
       ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2),
       "r"(c3), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// CTA pairs: a tiled load into this CTA's shared memory whose completion is counted on an
+// mbarrier of either CTA of the pair (bar_cluster: its shared::cluster address).
+__device__ __forceinline__ void tma_load_4d_pair(void *dst, const CUtensorMap *map,
+                                                 uint32_t bar_cluster, int c0, int c1, int c2,
+                                                 int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2),
+      "r"(c3), "r"(bar_cluster)
       : "memory");
 }
 
@@ -199,6 +280,22 @@ __device__ __forceinline__ void tmem_relinquish() {
 
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+// The cta_group::2 forms: one warp of EACH CTA of the pair executes them, together; the
+// allocation has the same address in both CTAs.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t *dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
                : "memory");
 }
 
@@ -395,6 +492,52 @@ __device__ __forceinline__ void mma_commit_w(uint64_t *bar) {
       "elect.sync _|e, 0xffffffff;\n"
       "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n"
       "}\n" ::"r"(smem_u32(bar))
+      : "memory");
+}
+
+// CTA-pair forms (cta_group::2), issued by the even CTA of the pair: D [M = 256 x N] spans
+// both CTAs' Tensor Memory (128 lanes each), A is split by rows (each CTA's own shared memory
+// or Tensor Memory at the same address), B by columns (each CTA holds N / 2 of them).
+// Warp-collective like the forms above.
+__device__ __forceinline__ void mma_bf16_ss_pair_w(uint32_t d_tmem, uint64_t a_desc,
+                                                   uint64_t b_desc, uint32_t idesc,
+                                                   uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      ".reg .pred e, p;\n"
+      "elect.sync _|e, 0xffffffff;\n"
+      "setp.ne.b32 p, %4, 0;\n"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16_ts_pair_w(uint32_t d_tmem, uint32_t a_tmem,
+                                                   uint64_t b_desc, uint32_t idesc,
+                                                   uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      ".reg .pred e, p;\n"
+      "elect.sync _|e, 0xffffffff;\n"
+      "setp.ne.b32 p, %4, 0;\n"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive (once) on the mbarrier at the same offset as `bar` in BOTH CTAs of the pair when every
+// cta_group::2 MMA issued so far by this thread has completed.
+__device__ __forceinline__ void mma_commit_pair_w(uint64_t *bar) {
+  asm volatile(
+      "{\n"
+      ".reg .pred e;\n"
+      "elect.sync _|e, 0xffffffff;\n"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;\n"
+      "}\n" ::"r"(smem_u32(bar)),
+      "h"(static_cast<unsigned short>(3))
       : "memory");
 }
 

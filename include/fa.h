@@ -441,6 +441,18 @@ void fa_set_wait_timeout_ns(unsigned long long ns);
  */
 void fa_set_fault_injection(int withhold_loads);
 
+/*
+ * Forward kernel selection (process-wide, for calls made after it).  With enable != 0 the
+ * 16-bit forward calls at head dimensions 72..128 (fa_fwd, fa_fwd_varlen, fa_fwd_host) run
+ * on CTA pairs: clusters of two CTAs that compute each 256-row query sub-tile as one product
+ * over both SMs' tensor cores (tcgen05 cta_group::2, the 2-CTA MMA mode of "FlashAttention
+ * 1-4 详解", FlashAttention 4 section), each CTA loading half of every K and V tile.
+ * enable = 0 (the default) selects the single-CTA kernel, which measures faster on the
+ * causal and dense workloads.  Both give the same results (bit for bit in every case
+ * tested; each call is deterministic).
+ */
+void fa_set_cta_pairs(int enable);
+
 #ifdef __cplusplus
 }
 #endif

@@ -196,3 +196,57 @@ def test_row_max_jumps_across_tiles(direction, causal):
     o, lse = _run_dense(q, k, v, causal, scale=scale)
     o_ref, lse_ref = _oracle_dense(q, k, v, causal, float(np.float32(scale)))
     compare(*dense_rows(o, lse), *dense_rows(o_ref, lse_ref), f"max jumps {direction}")
+
+
+# ------------------------------------------------------------------ CTA pairs
+
+PAIR_CASES = [
+    # B, Nq, Nk, Hq, Hkv, d, causal: work tiles of 512 rows, sub-tiles of 256 over two CTAs
+    (1, 256, 256, 1, 1, 128, False),    # one sub-tile
+    (1, 100, 100, 1, 1, 128, True),     # the odd CTA of the pair holds no valid row
+    (2, 700, 700, 4, 2, 128, True),     # 2 work tiles, ragged second (700 = 512 + 188)
+    (1, 1300, 1300, 2, 2, 96, False),   # d = 96, three tiles, ragged
+    (1, 333, 1000, 8, 1, 128, True),    # Nq < Nk (bottom-right), MQA
+    (1, 1000, 333, 2, 2, 80, True),     # Nq > Nk: leading rows see no key
+]
+
+
+@pytest.mark.parametrize("case", PAIR_CASES, ids=lambda c: "B{}_q{}_k{}_h{}x{}_d{}_{}".format(
+    c[0], c[1], c[2], c[3], c[4], c[5], "causal" if c[6] else "full"))
+def test_cta_pairs_and_single_cta_against_oracle(case):
+    """The width-128 forward on CTA pairs and on the single-CTA kernel (the default), each
+    against the oracle; each selection is deterministic and the two agree bit for bit."""
+    from exact_attention_81_gb300 import set_cta_pairs
+    B, Nq, Nk, Hq, Hkv, d, causal = case
+    q, k, v = dense_inputs(B, Nq, Nk, Hq, Hkv, d, seed=3000 + Nq + d, device=DEV)
+    o_ref, lse_ref = _oracle_dense(q, k, v, causal, float(np.float32(1 / math.sqrt(d))))
+    outs = []
+    try:
+        for pairs in (True, False):
+            set_cta_pairs(pairs)
+            o, lse = _run_dense(q, k, v, causal)
+            compare(*dense_rows(o, lse), *dense_rows(o_ref, lse_ref), f"pairs={pairs} {case}")
+            o2, l2 = _run_dense(q, k, v, causal)
+            assert torch.equal(o, o2) and torch.equal(lse, l2)
+            outs.append((o, lse))
+    finally:
+        set_cta_pairs(False)
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_cta_pairs_varlen(causal):
+    from exact_attention_81_gb300 import set_cta_pairs
+    sq = [5, 0, 700, 256, 257, 1100, 1]
+    sk = [9, 4, 700, 300, 257, 1100, 1]
+    q, k, v, cu_q, cu_k = varlen_inputs(sq, sk, 4, 2, 128, seed=77, device=DEV)
+    o_ref, lse_ref = ORACLE.attention_varlen(q.cpu(), k.cpu(), v.cpu(), cu_q.cpu(), cu_k.cpu(),
+                                             float(np.float32(1 / math.sqrt(128))), causal)
+    try:
+        for pairs in (True, False):
+            set_cta_pairs(pairs)
+            o, lse = fa_fwd_varlen(q, k, v, cu_q, cu_k, max(sq), max(sk), causal=causal)
+            assert get_last_device_error() == FA_OK
+            compare(*varlen_rows(o, lse), *varlen_rows(o_ref, lse_ref), f"pairs={pairs} varlen")
+    finally:
+        set_cta_pairs(False)

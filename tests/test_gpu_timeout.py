@@ -28,18 +28,26 @@ def _with_tiny_timeout(fn):
         set_wait_timeout_ns(0)
 
 
+@pytest.mark.parametrize("pairs", [False, True])
 @pytest.mark.parametrize("causal", [False, True])
-def test_prefill_wait_timeout_reports_and_recovers(causal):
+def test_prefill_wait_timeout_reports_and_recovers(causal, pairs):
+    """pairs: the CTA-pair kernel, whose two CTAs both unwind (a CTA that gives up also sets
+    its peer's abort flag) and meet at their bounded exit handshake before TMEM is freed."""
+    from exact_attention_81_gb300 import set_cta_pairs
     q, k, v = dense_inputs(2, 1500, 1500, 4, 2, 128, seed=71, device=DEV)
-    o_ok, l_ok = fa_fwd(q, k, v, causal=causal)
-    assert get_last_device_error() == FA_OK
-    st = _with_tiny_timeout(lambda: fa_fwd(q, k, v, causal=causal))
-    assert st == FA_ERR_TIMEOUT
-    assert get_last_device_error() == FA_OK  # the word was cleared by the read
-    for _ in range(2):
-        o2, l2 = fa_fwd(q, k, v, causal=causal)
+    set_cta_pairs(pairs)
+    try:
+        o_ok, l_ok = fa_fwd(q, k, v, causal=causal)
         assert get_last_device_error() == FA_OK
-        assert torch.equal(o2, o_ok) and torch.equal(l2, l_ok)
+        st = _with_tiny_timeout(lambda: fa_fwd(q, k, v, causal=causal))
+        assert st == FA_ERR_TIMEOUT
+        assert get_last_device_error() == FA_OK  # the word was cleared by the read
+        for _ in range(2):
+            o2, l2 = fa_fwd(q, k, v, causal=causal)
+            assert get_last_device_error() == FA_OK
+            assert torch.equal(o2, o_ok) and torch.equal(l2, l_ok)
+    finally:
+        set_cta_pairs(False)
 
 
 def test_decode_wait_timeout_reports_and_recovers():
