@@ -550,6 +550,230 @@ __device__ void compute(const DecodeArgs &a, uint8_t *smem, DBars *bars, const W
   }
 }
 
+// E4M3 caches at width 128 on the tensor cores: mma.sync m16n8k16 with f16 operands and
+// fp32 accumulation (the E4M3 values convert to f16 exactly, in registers).  Warp w owns keys
+// [16 w, 16 w + 16) of every 128-key block and its own online-softmax state, as in compute();
+// lane = 4 g + t.
+//   S = Q K^T: M = the work item's heads (row g < G; rows g + 8 and g >= G are zero), N = the
+//   warp's 16 keys as two n-tiles (column g of n-tile n = key 8 n + g), K = d in 8 steps.  The
+//   contraction index is permuted on both operands so that lane t reads the 32 bytes
+//   [32 t, 32 t + 32) of a key row: at step ks, columns 2t + {0,1} stand for d = 32 t + 4 ks +
+//   {0,1} and 2t + 8 + {0,1} for d = 32 t + 4 ks + {2,3}, so each 4-byte word of the row is the
+//   two f16 pairs of one step.  The bf16 query is scaled by a power of two (its largest
+//   magnitude below 2^15) and converted to f16 once per unit; values below 2^-38 of the
+//   largest are the only ones f16 does not hold.
+//   S arrives as lane (g, t): head g at keys 2t, 2t + 1 and 8 + 2t, 9 + 2t, which is the A
+//   layout of P in the second product: P goes from the softmax to the MMA in registers.
+//   O += P V: M = heads, N = d in 16 n-tiles (column g of n-tile nd = d 16 g + nd), K = the 16
+//   keys: lane (g, t) reads 16 bytes of key rows 2t, 2t + 1, 2t + 8, 2t + 9 and pairs the bytes
+//   of two rows with byte permutes; its accumulators hold O[head g][32 t + nd] and
+//   O[head g][32 t + 16 + nd].  P enters as f16 (values <= 1, relative rounding 2^-11); the
+//   row sums stay fp32.  Rows of keys that take no part (past the length, before the window
+//   start) are zeroed in the V operand, so 0 x NaN cannot reach O.
+template <int G, bool MOD>
+__device__ void compute_f8_mma(const DecodeArgs &a, uint8_t *smem, DBars *bars, const WaitCtl &wc,
+                               int tid) {
+  constexpr int D = 128;
+  using C = DCfg<D, G, true>;
+  static_assert(C::KPW == 16 && C::BLOCK_BYTES == KB * 128, "one 128-byte box row per key");
+  const int warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t = lane & 3;
+  float *red = reinterpret_cast<float *>(smem + C::RED_OFF);
+  const uint16_t *qg = reinterpret_cast<const uint16_t *>(a.q);  // bf16
+  const bool softcap = MOD && a.sc_out != 0.f;
+  const bool alibi = MOD && a.alibi != nullptr;
+  uint32_t it = 0, sync_phase = 0;
+
+  for (uint32_t k = 0;; ++k) {
+    const int rs = static_cast<int>(k % SCHED_DEPTH);
+    if (!warp_wait(&bars->sched_full[rs], (k / SCHED_DEPTH) & 1u, wc)) return;
+    const int u = bars->sched_unit[rs];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars->sched_empty[rs]);
+    if (u < 0) break;
+    const Unit w = unit_of(a, u);
+    const int nblk = (w.nkeys + KB - 1) / KB;
+    const int64_t kh = static_cast<int64_t>(w.b) * (a.Hkv / a.nsplit) + w.g / a.nsplit;
+    const float kds = a.k_descale ? a.k_descale[kh] : 1.f;
+    const float vds = a.v_descale ? a.v_descale[kh] : 1.f;
+
+    // Query of head g, d [32 t, 32 t + 32), to f16 pairs (scaled by sq = 2^e).
+    float qf[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) qf[i] = 0.f;
+    if (g < G) {
+      const uint4 *src = reinterpret_cast<const uint4 *>(
+          qg + (static_cast<int64_t>(w.b) * a.Hq + w.g * G + g) * a.d + 32 * t);
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        if (32 * t + 8 * v < a.d) {  // columns past d are padding
+          const uint4 x = src[v];
+          const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            qf[8 * v + 2 * e] = bf16lo_to_f32(xs[e]);
+            qf[8 * v + 2 * e + 1] = bf16hi_to_f32(xs[e]);
+          }
+        }
+      }
+    }
+    float qmax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) qmax = fmaxf(qmax, fabsf(qf[i]));
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, off));
+    // qmax < 2^(ex + 1) with ex its exponent, so qmax * 2^(14 - ex) < 2^15
+    const int ex = static_cast<int>((__float_as_uint(qmax) >> 23) & 0xFFu) - 127;
+    const float sq = qmax > 0.f ? __uint_as_float(static_cast<uint32_t>(min(max(141 - ex, 1), 254)) << 23)
+                                : 1.f;
+    uint32_t qa[8][2];
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      qa[ks][0] = pack_f16x2(qf[4 * ks] * sq, qf[4 * ks + 1] * sq);
+      qa[ks][1] = pack_f16x2(qf[4 * ks + 2] * sq, qf[4 * ks + 3] * sq);
+    }
+    const float sc = a.scale_log2 * kds / sq;  // MMA score -> scaled score in log2 units
+    const float slope2 = (alibi && g < G) ? a.alibi[w.b * a.alibi_sb + w.g * G + g] * -1.4426950408889634f
+                                          : 0.f;
+    const int first = MOD ? first_visible(w.len, a.wl) : 0;
+    float o[16][4];
+#pragma unroll
+    for (int nd = 0; nd < 16; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
+    float m = -INFINITY, l = 0.f;
+
+    for (int blk = 0; blk < nblk; ++blk) {
+      const int nvalid = min(KB, w.nkeys - blk * KB);
+      const int kw0 = warp * C::KPW;
+      const int kglob = w.key0 + blk * KB + kw0;  // cache row of the warp's first key
+      // keys of this lane's scores (and of its V rows): kw0 + 2t + {0, 1, 8, 9}
+      const int kl[4] = {2 * t, 2 * t + 1, 8 + 2 * t, 9 + 2 * t};
+      bool valid[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        valid[i] = kw0 + kl[i] < nvalid && (!MOD || kglob + kl[i] >= first);
+      float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      {
+        const int slot = static_cast<int>(it % C::NSLOTS);
+        if (!warp_wait(&bars->full[slot], (it / C::NSLOTS) & 1u, wc)) return;
+        ++it;
+        const uint8_t *kblk = smem + C::RING_OFF + slot * C::BLOCK_BYTES;
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+          const int key = kw0 + 8 * n + g;
+          const uint8_t *krow = kblk + key * 128;
+          const uint4 c0 = *reinterpret_cast<const uint4 *>(krow + (((2 * t) ^ (key & 7)) << 4));
+          const uint4 c1 =
+              *reinterpret_cast<const uint4 *>(krow + (((2 * t + 1) ^ (key & 7)) << 4));
+          const uint32_t wd[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            uint32_t b0, b1;
+            e4m3x4_to_f16x2x2(wd[ks], b0, b1);
+            mma_f16_m16n8k16(sacc[n], qa[ks][0], 0u, qa[ks][1], 0u, b0, b1);
+          }
+        }
+        release(&bars->empty[slot], lane);
+      }
+      // ---- online softmax of head g over the warp's 16 keys (4 per lane, 4 lanes per head)
+      float sv[4] = {sacc[0][0] * sc, sacc[0][1] * sc, sacc[1][0] * sc, sacc[1][1] * sc};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (softcap) sv[i] = tanh_ex2(sv[i] * a.sc_in) * a.sc_out;
+        if (alibi)  // - slope * distance from the query at position len - 1, log2 units
+          sv[i] = fmaf(slope2, static_cast<float>(w.len - 1 - (kglob + kl[i])), sv[i]);
+        if (!valid[i]) sv[i] = -INFINITY;
+      }
+      float bm = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
+      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
+      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
+      const float m_new = fmaxf(m, bm);
+      const float m_use = m_new == -INFINITY ? 0.f : m_new;
+      const float alpha = m_new > m ? ex2_approx(m - m_use) : 1.f;
+      m = m_new;
+      float p[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) p[i] = ex2_approx(sv[i] - m_use);
+      float ps = (p[0] + p[1]) + (p[2] + p[3]);
+      ps += __shfl_xor_sync(0xffffffffu, ps, 1);
+      ps += __shfl_xor_sync(0xffffffffu, ps, 2);
+      l = l * alpha + ps;
+      if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+        for (int nd = 0; nd < 16; ++nd) {
+          o[nd][0] *= alpha;
+          o[nd][1] *= alpha;
+        }
+      }
+      const uint32_t pa0 = pack_f16x2(p[0], p[1]), pa2 = pack_f16x2(p[2], p[3]);
+      // ---- O += P V
+      {
+        const int slot = static_cast<int>(it % C::NSLOTS);
+        if (!warp_wait(&bars->full[slot], (it / C::NSLOTS) & 1u, wc)) return;
+        ++it;
+        const uint8_t *vblk = smem + C::RING_OFF + slot * C::BLOCK_BYTES;
+        uint32_t vr[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int row = kw0 + kl[i];
+          const uint4 x = *reinterpret_cast<const uint4 *>(vblk + row * 128 + ((g ^ (row & 7)) << 4));
+          vr[i][0] = valid[i] ? x.x : 0u;
+          vr[i][1] = valid[i] ? x.y : 0u;
+          vr[i][2] = valid[i] ? x.z : 0u;
+          vr[i][3] = valid[i] ? x.w : 0u;
+        }
+        release(&bars->empty[slot], lane);
+#pragma unroll
+        for (int w4 = 0; w4 < 4; ++w4) {
+          uint32_t b0a, b0b, b0c, b0d, b1a, b1b, b1c, b1d;
+          // (row 2t, row 2t+1) and (row 2t+8, row 2t+9) byte pairs at d = 16 g + 4 w4 + j
+          e4m3x4_to_f16x2x2(byte_perm(vr[0][w4], vr[1][w4], 0x5140u), b0a, b0b);
+          e4m3x4_to_f16x2x2(byte_perm(vr[0][w4], vr[1][w4], 0x7362u), b0c, b0d);
+          e4m3x4_to_f16x2x2(byte_perm(vr[2][w4], vr[3][w4], 0x5140u), b1a, b1b);
+          e4m3x4_to_f16x2x2(byte_perm(vr[2][w4], vr[3][w4], 0x7362u), b1c, b1d);
+          mma_f16_m16n8k16(o[4 * w4 + 0], pa0, 0u, pa2, 0u, b0a, b1a);
+          mma_f16_m16n8k16(o[4 * w4 + 1], pa0, 0u, pa2, 0u, b0b, b1b);
+          mma_f16_m16n8k16(o[4 * w4 + 2], pa0, 0u, pa2, 0u, b0c, b1c);
+          mma_f16_m16n8k16(o[4 * w4 + 3], pa0, 0u, pa2, 0u, b0d, b1d);
+        }
+      }
+    }
+
+    // ---- unit end: merge the warps' (m, l, O) and write the normalised partial
+    if (t == 0 && g < G) {
+      bars->m[warp][g] = m;
+      bars->l[warp][g] = l;
+    }
+    if (g < G) {
+      float4 *dst = reinterpret_cast<float4 *>(red + (warp * G + g) * D + 32 * t);
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        dst[v] = make_float4(o[4 * v][0], o[4 * v + 1][0], o[4 * v + 2][0], o[4 * v + 3][0]);
+        dst[4 + v] = make_float4(o[4 * v][1], o[4 * v + 1][1], o[4 * v + 2][1], o[4 * v + 3][1]);
+      }
+    }
+    if (!group_sync(&bars->sync, sync_phase, wc)) return;
+    const int64_t row0 = (static_cast<int64_t>(w.b) * a.Hq + w.g * G) * a.maxch + w.c;
+    for (int idx = tid; idx < G * D; idx += NCOMPUTE) {
+      const int gg = idx / D, dd = idx - gg * D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int ww = 0; ww < C::NWARP; ++ww) M = fmaxf(M, bars->m[ww][gg]);
+      float L = 0.f, O = 0.f;
+#pragma unroll
+      for (int ww = 0; ww < C::NWARP; ++ww) {
+        const float mw = bars->m[ww][gg];
+        const float wgt = mw == -INFINITY ? 0.f : ex2_approx(mw - M);
+        L = fmaf(bars->l[ww][gg], wgt, L);
+        O = fmaf(red[(ww * G + gg) * D + dd], wgt, O);
+      }
+      const int64_t row = row0 + static_cast<int64_t>(gg) * a.maxch;
+      if (dd < a.ostride) a.o_part[row * a.ostride + dd] = O / L * vds;
+      if (dd == 0) a.lse_part[row] = (M + log2f(L)) * LN2;
+    }
+    if (!group_sync(&bars->sync, sync_phase, wc)) return;
+  }
+}
+
 template <int D, int G, bool F16, bool F8, bool MOD>
 __global__ void __launch_bounds__(NTHREADS, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
@@ -583,7 +807,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // Each register-split branch ends on its own named barrier.
   if (warp < PRODUCER_WARP) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(COMPUTE_REGS));
-    compute<D, G, F16, F8, MOD>(a, smem, bars, wc, tid);
+    if constexpr (F8 && D == 128)
+      compute_f8_mma<G, MOD>(a, smem, bars, wc, tid);
+    else
+      compute<D, G, F16, F8, MOD>(a, smem, bars, wc, tid);
     __syncwarp();
     named_barrier(1, NTHREADS);
   } else {

@@ -679,6 +679,40 @@ __device__ __forceinline__ uint64_t e4m3x2_to_f32x2(uint32_t w16) {
   return f2_pack(f16lo_to_f32(h2), f16hi_to_f32(h2));
 }
 
+// Four E4M3 bytes of w -> two f16x2 (bytes 0-1 -> lo, bytes 2-3 -> hi), exact.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t &lo, uint32_t &hi) {
+  asm("{\n"
+      ".reg .b16 l, h;\n"
+      "mov.b32 {l, h}, %2;\n"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n"
+      "cvt.rn.f16x2.e4m3x2 %1, h;\n"
+      "}\n"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
+// Bytes of {b, a} (a = bytes 0-3, b = bytes 4-7) picked by the four selector nibbles.
+__device__ __forceinline__ uint32_t byte_perm(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// Warp-level D[16 x 8] += A[16 x 16] B[16 x 8], f16 A and B, fp32 accumulation (mma.sync;
+// the register fragments of the PTX ISA's m16n8k16 layout: lane = 4 g + t holds A rows g and
+// g + 8 at columns 2t, 2t + 1 (a0: row g, a1: row g + 8) and 2t + 8, 2t + 9 (a2, a3); B rows
+// 2t, 2t + 1 (b0) and 2t + 8, 2t + 9 (b1) of column g; D rows g (d[0], d[1]) and g + 8 (d[2],
+// d[3]) at columns 2t, 2t + 1).
+__device__ __forceinline__ void mma_f16_m16n8k16(float (&d)[4], uint32_t a0, uint32_t a1,
+                                                 uint32_t a2, uint32_t a3, uint32_t b0,
+                                                 uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7},"
+      " {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 // The two 16-bit element types of the kernels: bf16 (F16 = false) or fp16 (F16 = true).
 template <bool F16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
