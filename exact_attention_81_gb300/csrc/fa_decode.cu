@@ -550,39 +550,61 @@ __device__ void compute(const DecodeArgs &a, uint8_t *smem, DBars *bars, const W
   }
 }
 
-// E4M3 caches at width 128 on the tensor cores: mma.sync m16n8k16 with f16 operands and
-// fp32 accumulation (the E4M3 values convert to f16 exactly, in registers).  Warp w owns keys
+// The decode contractions on the tensor cores: mma.sync m16n8k16 with fp32 accumulation, bf16
+// or fp16 operands for 16-bit caches, f16 operands for E4M3 caches (their values convert to
+// f16 exactly, in registers).  Widths 64 and 128 (E4M3: 128).  Warp w owns keys
 // [16 w, 16 w + 16) of every 128-key block and its own online-softmax state, as in compute();
 // lane = 4 g + t.
 //   S = Q K^T: M = the work item's heads (row g < G; rows g + 8 and g >= G are zero), N = the
-//   warp's 16 keys as two n-tiles (column g of n-tile n = key 8 n + g), K = d in 8 steps.  The
-//   contraction index is permuted on both operands so that lane t reads the 32 bytes
-//   [32 t, 32 t + 32) of a key row: at step ks, columns 2t + {0,1} stand for d = 32 t + 4 ks +
-//   {0,1} and 2t + 8 + {0,1} for d = 32 t + 4 ks + {2,3}, so each 4-byte word of the row is the
-//   two f16 pairs of one step.  The bf16 query is scaled by a power of two (its largest
-//   magnitude below 2^15) and converted to f16 once per unit; values below 2^-38 of the
-//   largest are the only ones f16 does not hold.
+//   warp's 16 keys as two n-tiles (column g of n-tile n = key 8 n + g), K = d in D / 16 steps.
+//   The contraction index is permuted on both operands so that lane t reads the D / 4
+//   contiguous elements [t D / 4, (t + 1) D / 4) of a key row: at step ks, columns 2t + {0,1}
+//   stand for d = t D / 4 + 4 ks + {0,1} and 2t + 8 + {0,1} for d = t D / 4 + 4 ks + {2,3}, so
+//   the operand registers are the row's own element pairs (E4M3: each 4-byte word converts to
+//   the two f16 pairs of one step).  The query enters exactly: as stored for 16-bit caches;
+//   for E4M3 caches as f16 after a power-of-two scaling that puts its largest magnitude below
+//   2^15 (values below 2^-38 of the largest are the only ones f16 does not hold).
 //   S arrives as lane (g, t): head g at keys 2t, 2t + 1 and 8 + 2t, 9 + 2t, which is the A
 //   layout of P in the second product: P goes from the softmax to the MMA in registers.
-//   O += P V: M = heads, N = d in 16 n-tiles (column g of n-tile nd = d 16 g + nd), K = the 16
-//   keys: lane (g, t) reads 16 bytes of key rows 2t, 2t + 1, 2t + 8, 2t + 9 and pairs the bytes
-//   of two rows with byte permutes; its accumulators hold O[head g][32 t + nd] and
-//   O[head g][32 t + 16 + nd].  P enters as f16 (values <= 1, relative rounding 2^-11); the
-//   row sums stay fp32.  Rows of keys that take no part (past the length, before the window
-//   start) are zeroed in the V operand, so 0 x NaN cannot reach O.
-template <int G, bool MOD>
-__device__ void compute_f8_mma(const DecodeArgs &a, uint8_t *smem, DBars *bars, const WaitCtl &wc,
-                               int tid) {
-  constexpr int D = 128;
-  using C = DCfg<D, G, true>;
-  static_assert(C::KPW == 16 && C::BLOCK_BYTES == KB * 128, "one 128-byte box row per key");
+//   O += P V: M = heads, N = d in D / 8 n-tiles (column g of n-tile nd = d g D / 8 + nd),
+//   K = the 16 keys: lane (g, t) reads D / 8 elements of key rows 2t, 2t + 1, 2t + 8, 2t + 9
+//   and pairs the elements of two rows with byte permutes; its accumulators hold
+//   O[head g][t D / 4 + nd] and O[head g][t D / 4 + D / 8 + nd], D / 4 contiguous columns.
+//   P enters the product rounded to f16 (values <= 1: relative rounding 2^-11), or for bf16
+//   operands as bf16(p) plus a second product with the remainder bf16(p - bf16(p)) (about 16
+//   significant bits: a bf16 P alone raised the largest error of short decode rows from
+//   7.7e-3 to 9.8e-3); the row sums stay fp32.  Rows of keys that take no part (past the length, before the window start) are
+//   zeroed in the V operand, so 0 x NaN cannot reach O.
+template <int D, int G, bool F16, bool F8, bool MOD>
+__device__ void compute_mma(const DecodeArgs &a, uint8_t *smem, DBars *bars, const WaitCtl &wc,
+                            int tid) {
+  using C = DCfg<D, G, F8>;
+  constexpr int EB = C::EB;                  // bytes per cache element
+  constexpr int KSTEPS = D / 16;             // k-steps of S
+  constexpr int NT = D / 8;                  // n-tiles of P V
+  constexpr int KWORDS = D / 4 * EB / 4;     // 32-bit words of a key-row slice (lane t)
+  constexpr int VWORDS = D / 8 * EB / 4;     // 32-bit words of a V-row slice (lane g)
+  constexpr bool HALF = F8 || F16;           // f16 MMA (else bf16)
+  static_assert(C::KPW == 16, "16 keys per warp and block");
+  static_assert(!F8 || D == 128, "E4M3 rows are one 128-byte box");
   const int warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
   float *red = reinterpret_cast<float *>(smem + C::RED_OFF);
-  const uint16_t *qg = reinterpret_cast<const uint16_t *>(a.q);  // bf16
+  const uint16_t *qg = reinterpret_cast<const uint16_t *>(a.q);
   const bool softcap = MOD && a.sc_out != 0.f;
   const bool alibi = MOD && a.alibi != nullptr;
+  // Element e of a ring row: box e / BOX_ELEMS, 16-byte chunk ((e % BOX_ELEMS) EB) / 16.
+  const int ke0 = t * (D / 4);      // first element of this lane's key-row slice
+  const int ve0 = g * (D / 8);      // first element of this lane's V-row slice
+  const int kbox = ke0 / C::BOX_ELEMS, kchunk = (ke0 % C::BOX_ELEMS) * EB / 16;
+  const int vbox = ve0 / C::BOX_ELEMS, vchunk = (ve0 % C::BOX_ELEMS) * EB / 16;
   uint32_t it = 0, sync_phase = 0;
+  auto mma = [](float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+    if constexpr (HALF)
+      mma_f16_m16n8k16(d, a0, 0u, a2, 0u, b0, b1);
+    else
+      mma_bf16_m16n8k16(d, a0, 0u, a2, 0u, b0, b1);
+  };
 
   for (uint32_t k = 0;; ++k) {
     const int rs = static_cast<int>(k % SCHED_DEPTH);
@@ -593,59 +615,71 @@ __device__ void compute_f8_mma(const DecodeArgs &a, uint8_t *smem, DBars *bars, 
     if (u < 0) break;
     const Unit w = unit_of(a, u);
     const int nblk = (w.nkeys + KB - 1) / KB;
-    const int64_t kh = static_cast<int64_t>(w.b) * (a.Hkv / a.nsplit) + w.g / a.nsplit;
-    const float kds = a.k_descale ? a.k_descale[kh] : 1.f;
-    const float vds = a.v_descale ? a.v_descale[kh] : 1.f;
+    float sc = a.scale_log2, vds = 1.f;
+    if constexpr (F8) {
+      const int64_t kh = static_cast<int64_t>(w.b) * (a.Hkv / a.nsplit) + w.g / a.nsplit;
+      sc *= a.k_descale ? a.k_descale[kh] : 1.f;
+      vds = a.v_descale ? a.v_descale[kh] : 1.f;
+    }
 
-    // Query of head g, d [32 t, 32 t + 32), to f16 pairs (scaled by sq = 2^e).
-    float qf[32];
+    // Query of head g, elements [ke0, ke0 + D / 4): the A operand pairs of every k-step.
+    uint32_t qa[KSTEPS][2];
+    {
+      uint32_t qw[D / 8];  // the slice as element pairs
 #pragma unroll
-    for (int i = 0; i < 32; ++i) qf[i] = 0.f;
-    if (g < G) {
-      const uint4 *src = reinterpret_cast<const uint4 *>(
-          qg + (static_cast<int64_t>(w.b) * a.Hq + w.g * G + g) * a.d + 32 * t);
+      for (int i = 0; i < D / 8; ++i) qw[i] = 0u;
+      if (g < G) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(
+            qg + (static_cast<int64_t>(w.b) * a.Hq + w.g * G + g) * a.d + ke0);
 #pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        if (32 * t + 8 * v < a.d) {  // columns past d are padding
-          const uint4 x = src[v];
-          const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            qf[8 * v + 2 * e] = bf16lo_to_f32(xs[e]);
-            qf[8 * v + 2 * e + 1] = bf16hi_to_f32(xs[e]);
+        for (int v = 0; v < D / 32; ++v) {
+          if (ke0 + 8 * v < a.d) {  // columns past d are padding
+            const uint4 x = src[v];
+            qw[4 * v] = x.x;
+            qw[4 * v + 1] = x.y;
+            qw[4 * v + 2] = x.z;
+            qw[4 * v + 3] = x.w;
           }
         }
       }
+      if constexpr (F8) {
+        // bf16 query -> f16, scaled by sq = 2^e so that the largest magnitude is below 2^15
+        float qmax = 0.f;
+#pragma unroll
+        for (int i = 0; i < D / 8; ++i)
+          qmax = fmaxf(qmax, fmaxf(fabsf(bf16lo_to_f32(qw[i])), fabsf(bf16hi_to_f32(qw[i]))));
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1)
+          qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, off));
+        const int ex = static_cast<int>((__float_as_uint(qmax) >> 23) & 0xFFu) - 127;
+        const float sq =
+            qmax > 0.f ? __uint_as_float(static_cast<uint32_t>(min(max(141 - ex, 1), 254)) << 23)
+                       : 1.f;
+#pragma unroll
+        for (int i = 0; i < D / 8; ++i)
+          qw[i] = pack_f16x2(bf16lo_to_f32(qw[i]) * sq, bf16hi_to_f32(qw[i]) * sq);
+        sc /= sq;
+      }
+#pragma unroll
+      for (int ks = 0; ks < KSTEPS; ++ks) {
+        qa[ks][0] = qw[2 * ks];
+        qa[ks][1] = qw[2 * ks + 1];
+      }
     }
-    float qmax = 0.f;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) qmax = fmaxf(qmax, fabsf(qf[i]));
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, off));
-    // qmax < 2^(ex + 1) with ex its exponent, so qmax * 2^(14 - ex) < 2^15
-    const int ex = static_cast<int>((__float_as_uint(qmax) >> 23) & 0xFFu) - 127;
-    const float sq = qmax > 0.f ? __uint_as_float(static_cast<uint32_t>(min(max(141 - ex, 1), 254)) << 23)
-                                : 1.f;
-    uint32_t qa[8][2];
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      qa[ks][0] = pack_f16x2(qf[4 * ks] * sq, qf[4 * ks + 1] * sq);
-      qa[ks][1] = pack_f16x2(qf[4 * ks + 2] * sq, qf[4 * ks + 3] * sq);
-    }
-    const float sc = a.scale_log2 * kds / sq;  // MMA score -> scaled score in log2 units
-    const float slope2 = (alibi && g < G) ? a.alibi[w.b * a.alibi_sb + w.g * G + g] * -1.4426950408889634f
-                                          : 0.f;
+    const float slope2 = (alibi && g < G)
+                             ? a.alibi[w.b * a.alibi_sb + w.g * G + g] * -1.4426950408889634f
+                             : 0.f;
     const int first = MOD ? first_visible(w.len, a.wl) : 0;
-    float o[16][4];
+    float o[NT][4];
 #pragma unroll
-    for (int nd = 0; nd < 16; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
+    for (int nd = 0; nd < NT; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
     float m = -INFINITY, l = 0.f;
 
     for (int blk = 0; blk < nblk; ++blk) {
       const int nvalid = min(KB, w.nkeys - blk * KB);
       const int kw0 = warp * C::KPW;
       const int kglob = w.key0 + blk * KB + kw0;  // cache row of the warp's first key
-      // keys of this lane's scores (and of its V rows): kw0 + 2t + {0, 1, 8, 9}
+      // keys of this lane's scores and V rows: kw0 + 2t + {0, 1, 8, 9}
       const int kl[4] = {2 * t, 2 * t + 1, 8 + 2 * t, 9 + 2 * t};
       bool valid[4];
 #pragma unroll
@@ -656,20 +690,30 @@ __device__ void compute_f8_mma(const DecodeArgs &a, uint8_t *smem, DBars *bars, 
         const int slot = static_cast<int>(it % C::NSLOTS);
         if (!warp_wait(&bars->full[slot], (it / C::NSLOTS) & 1u, wc)) return;
         ++it;
-        const uint8_t *kblk = smem + C::RING_OFF + slot * C::BLOCK_BYTES;
+        const uint8_t *kblk = smem + C::RING_OFF + slot * C::BLOCK_BYTES + kbox * BOX_BYTES;
+        // one 16-byte chunk of each key row at a time, then the k-steps it holds (2 for 16-bit
+        // elements, 4 for E4M3), so that the slice never sits in registers as a whole
+        constexpr int KS_PER_CHUNK = 16 / (4 * EB);
 #pragma unroll
-        for (int n = 0; n < 2; ++n) {
-          const int key = kw0 + 8 * n + g;
-          const uint8_t *krow = kblk + key * 128;
-          const uint4 c0 = *reinterpret_cast<const uint4 *>(krow + (((2 * t) ^ (key & 7)) << 4));
-          const uint4 c1 =
-              *reinterpret_cast<const uint4 *>(krow + (((2 * t + 1) ^ (key & 7)) << 4));
-          const uint32_t wd[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+        for (int c = 0; c < KWORDS / 4; ++c) {
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            uint32_t b0, b1;
-            e4m3x4_to_f16x2x2(wd[ks], b0, b1);
-            mma_f16_m16n8k16(sacc[n], qa[ks][0], 0u, qa[ks][1], 0u, b0, b1);
+          for (int n = 0; n < 2; ++n) {
+            const int key = kw0 + 8 * n + g;
+            const uint4 x = *reinterpret_cast<const uint4 *>(
+                kblk + key * 128 + (((kchunk + c) ^ (key & 7)) << 4));
+            const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int j = 0; j < KS_PER_CHUNK; ++j) {
+              const int ks = c * KS_PER_CHUNK + j;
+              uint32_t b0, b1;
+              if constexpr (F8) {
+                e4m3x4_to_f16x2x2(xw[j], b0, b1);
+              } else {
+                b0 = xw[2 * j];
+                b1 = xw[2 * j + 1];
+              }
+              mma(sacc[n], qa[ks][0], qa[ks][1], b0, b1);
+            }
           }
         }
         release(&bars->empty[slot], lane);
@@ -699,41 +743,65 @@ __device__ void compute_f8_mma(const DecodeArgs &a, uint8_t *smem, DBars *bars, 
       l = l * alpha + ps;
       if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-        for (int nd = 0; nd < 16; ++nd) {
+        for (int nd = 0; nd < NT; ++nd) {
           o[nd][0] *= alpha;
           o[nd][1] *= alpha;
         }
       }
-      const uint32_t pa0 = pack_f16x2(p[0], p[1]), pa2 = pack_f16x2(p[2], p[3]);
+      const uint32_t pa0 = HALF ? pack_f16x2(p[0], p[1]) : pack_bf16x2(p[0], p[1]);
+      const uint32_t pa2 = HALF ? pack_f16x2(p[2], p[3]) : pack_bf16x2(p[2], p[3]);
+      // bf16 operands: P also enters as its rounding remainder p - bf16(p) (a second product
+      // on the same V fragments), so P carries about 16 significant bits instead of 8
+      uint32_t pl0 = 0u, pl2 = 0u;
+      if constexpr (!HALF) {
+        pl0 = pack_bf16x2(p[0] - bf16lo_to_f32(pa0), p[1] - bf16hi_to_f32(pa0));
+        pl2 = pack_bf16x2(p[2] - bf16lo_to_f32(pa2), p[3] - bf16hi_to_f32(pa2));
+      }
       // ---- O += P V
       {
         const int slot = static_cast<int>(it % C::NSLOTS);
         if (!warp_wait(&bars->full[slot], (it / C::NSLOTS) & 1u, wc)) return;
         ++it;
-        const uint8_t *vblk = smem + C::RING_OFF + slot * C::BLOCK_BYTES;
-        uint32_t vr[4][4];
+        const uint8_t *vblk = smem + C::RING_OFF + slot * C::BLOCK_BYTES + vbox * BOX_BYTES;
+        uint32_t vr[4][VWORDS];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int row = kw0 + kl[i];
-          const uint4 x = *reinterpret_cast<const uint4 *>(vblk + row * 128 + ((g ^ (row & 7)) << 4));
-          vr[i][0] = valid[i] ? x.x : 0u;
-          vr[i][1] = valid[i] ? x.y : 0u;
-          vr[i][2] = valid[i] ? x.z : 0u;
-          vr[i][3] = valid[i] ? x.w : 0u;
+#pragma unroll
+          for (int c = 0; c < (VWORDS + 3) / 4; ++c) {
+            const uint4 x = *reinterpret_cast<const uint4 *>(
+                vblk + row * 128 + (((vchunk + c) ^ (row & 7)) << 4));
+            const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (4 * c + e < VWORDS) vr[i][4 * c + e] = valid[i] ? xs[e] : 0u;
+          }
         }
         release(&bars->empty[slot], lane);
+        if constexpr (F8) {
 #pragma unroll
-        for (int w4 = 0; w4 < 4; ++w4) {
-          uint32_t b0a, b0b, b0c, b0d, b1a, b1b, b1c, b1d;
-          // (row 2t, row 2t+1) and (row 2t+8, row 2t+9) byte pairs at d = 16 g + 4 w4 + j
-          e4m3x4_to_f16x2x2(byte_perm(vr[0][w4], vr[1][w4], 0x5140u), b0a, b0b);
-          e4m3x4_to_f16x2x2(byte_perm(vr[0][w4], vr[1][w4], 0x7362u), b0c, b0d);
-          e4m3x4_to_f16x2x2(byte_perm(vr[2][w4], vr[3][w4], 0x5140u), b1a, b1b);
-          e4m3x4_to_f16x2x2(byte_perm(vr[2][w4], vr[3][w4], 0x7362u), b1c, b1d);
-          mma_f16_m16n8k16(o[4 * w4 + 0], pa0, 0u, pa2, 0u, b0a, b1a);
-          mma_f16_m16n8k16(o[4 * w4 + 1], pa0, 0u, pa2, 0u, b0b, b1b);
-          mma_f16_m16n8k16(o[4 * w4 + 2], pa0, 0u, pa2, 0u, b0c, b1c);
-          mma_f16_m16n8k16(o[4 * w4 + 3], pa0, 0u, pa2, 0u, b0d, b1d);
+          for (int w4 = 0; w4 < VWORDS; ++w4) {
+            uint32_t b0a, b0b, b0c, b0d, b1a, b1b, b1c, b1d;
+            // (row 2t, row 2t+1) and (row 2t+8, row 2t+9) byte pairs at d = 16 g + 4 w4 + j
+            e4m3x4_to_f16x2x2(byte_perm(vr[0][w4], vr[1][w4], 0x5140u), b0a, b0b);
+            e4m3x4_to_f16x2x2(byte_perm(vr[0][w4], vr[1][w4], 0x7362u), b0c, b0d);
+            e4m3x4_to_f16x2x2(byte_perm(vr[2][w4], vr[3][w4], 0x5140u), b1a, b1b);
+            e4m3x4_to_f16x2x2(byte_perm(vr[2][w4], vr[3][w4], 0x7362u), b1c, b1d);
+            mma(o[4 * w4 + 0], pa0, pa2, b0a, b1a);
+            mma(o[4 * w4 + 1], pa0, pa2, b0b, b1b);
+            mma(o[4 * w4 + 2], pa0, pa2, b0c, b1c);
+            mma(o[4 * w4 + 3], pa0, pa2, b0d, b1d);
+          }
+        } else {
+#pragma unroll
+          for (int nd = 0; nd < NT; ++nd) {
+            // element nd of the slice (word nd / 2, half nd % 2) of rows (2t, 2t+1), (2t+8, 2t+9)
+            const uint32_t sel = (nd & 1) ? 0x7632u : 0x5410u;
+            const uint32_t b0 = byte_perm(vr[0][nd / 2], vr[1][nd / 2], sel);
+            const uint32_t b1 = byte_perm(vr[2][nd / 2], vr[3][nd / 2], sel);
+            mma(o[nd], pa0, pa2, b0, b1);
+            if constexpr (!HALF) mma(o[nd], pl0, pl2, b0, b1);
+          }
         }
       }
     }
@@ -744,11 +812,11 @@ __device__ void compute_f8_mma(const DecodeArgs &a, uint8_t *smem, DBars *bars, 
       bars->l[warp][g] = l;
     }
     if (g < G) {
-      float4 *dst = reinterpret_cast<float4 *>(red + (warp * G + g) * D + 32 * t);
+      float *dst = red + (warp * G + g) * D + ke0;
 #pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        dst[v] = make_float4(o[4 * v][0], o[4 * v + 1][0], o[4 * v + 2][0], o[4 * v + 3][0]);
-        dst[4 + v] = make_float4(o[4 * v][1], o[4 * v + 1][1], o[4 * v + 2][1], o[4 * v + 3][1]);
+      for (int nd = 0; nd < NT; ++nd) {
+        dst[nd] = o[nd][0];
+        dst[NT + nd] = o[nd][1];
       }
     }
     if (!group_sync(&bars->sync, sync_phase, wc)) return;
@@ -807,8 +875,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // Each register-split branch ends on its own named barrier.
   if (warp < PRODUCER_WARP) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(COMPUTE_REGS));
-    if constexpr (F8 && D == 128)
-      compute_f8_mma<G, MOD>(a, smem, bars, wc, tid);
+    if constexpr (D <= 128)
+      compute_mma<D, G, F16, F8, MOD>(a, smem, bars, wc, tid);
     else
       compute<D, G, F16, F8, MOD>(a, smem, bars, wc, tid);
     __syncwarp();
