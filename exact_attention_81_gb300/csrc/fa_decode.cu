@@ -806,39 +806,48 @@ __device__ void compute_mma(const DecodeArgs &a, uint8_t *smem, DBars *bars, con
       }
     }
 
-    // ---- unit end: merge the warps' (m, l, O) and write the normalised partial
+    // ---- unit end: merge the warps' (m, l, O) and write the normalised partial.  The staging
+    // buffer holds DS columns per (warp, head) (DS = D up to width 128, half of it at 256), so
+    // the merge runs in D / DS rounds; in round r the lanes whose slice [ke0, ke0 + D / 4) lies
+    // in columns [r DS, (r + 1) DS) stage it.
+    constexpr int DS = C::DS;
+    static_assert(DS % (D / 4) == 0, "a lane's slice lies in one round");
     if (t == 0 && g < G) {
       bars->m[warp][g] = m;
       bars->l[warp][g] = l;
     }
-    if (g < G) {
-      float *dst = red + (warp * G + g) * D + ke0;
-#pragma unroll
-      for (int nd = 0; nd < NT; ++nd) {
-        dst[nd] = o[nd][0];
-        dst[NT + nd] = o[nd][1];
-      }
-    }
-    if (!group_sync(&bars->sync, sync_phase, wc)) return;
     const int64_t row0 = (static_cast<int64_t>(w.b) * a.Hq + w.g * G) * a.maxch + w.c;
-    for (int idx = tid; idx < G * D; idx += NCOMPUTE) {
-      const int gg = idx / D, dd = idx - gg * D;
-      float M = -INFINITY;
+#pragma unroll 1
+    for (int r = 0; r < D / DS; ++r) {
+      if (g < G && ke0 / DS == r) {
+        float *dst = red + (warp * G + g) * DS + (ke0 - r * DS);
 #pragma unroll
-      for (int ww = 0; ww < C::NWARP; ++ww) M = fmaxf(M, bars->m[ww][gg]);
-      float L = 0.f, O = 0.f;
-#pragma unroll
-      for (int ww = 0; ww < C::NWARP; ++ww) {
-        const float mw = bars->m[ww][gg];
-        const float wgt = mw == -INFINITY ? 0.f : ex2_approx(mw - M);
-        L = fmaf(bars->l[ww][gg], wgt, L);
-        O = fmaf(red[(ww * G + gg) * D + dd], wgt, O);
+        for (int nd = 0; nd < NT; ++nd) {
+          dst[nd] = o[nd][0];
+          dst[NT + nd] = o[nd][1];
+        }
       }
-      const int64_t row = row0 + static_cast<int64_t>(gg) * a.maxch;
-      if (dd < a.ostride) a.o_part[row * a.ostride + dd] = O / L * vds;
-      if (dd == 0) a.lse_part[row] = (M + log2f(L)) * LN2;
+      if (!group_sync(&bars->sync, sync_phase, wc)) return;
+      for (int idx = tid; idx < G * DS; idx += NCOMPUTE) {
+        const int gg = idx / DS, dd = idx - gg * DS;
+        float M = -INFINITY;
+#pragma unroll
+        for (int ww = 0; ww < C::NWARP; ++ww) M = fmaxf(M, bars->m[ww][gg]);
+        float L = 0.f, O = 0.f;
+#pragma unroll
+        for (int ww = 0; ww < C::NWARP; ++ww) {
+          const float mw = bars->m[ww][gg];
+          const float wgt = mw == -INFINITY ? 0.f : ex2_approx(mw - M);
+          L = fmaf(bars->l[ww][gg], wgt, L);
+          O = fmaf(red[(ww * G + gg) * DS + dd], wgt, O);
+        }
+        const int64_t row = row0 + static_cast<int64_t>(gg) * a.maxch;
+        const int col = r * DS + dd;  // rows of the partials are ostride (<= D) wide
+        if (col < a.ostride) a.o_part[row * a.ostride + col] = O / L * vds;
+        if (r == 0 && dd == 0) a.lse_part[row] = (M + log2f(L)) * LN2;
+      }
+      if (!group_sync(&bars->sync, sync_phase, wc)) return;
     }
-    if (!group_sync(&bars->sync, sync_phase, wc)) return;
   }
 }
 
@@ -875,7 +884,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // Each register-split branch ends on its own named barrier.
   if (warp < PRODUCER_WARP) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(COMPUTE_REGS));
-    if constexpr (D <= 128)
+    if constexpr (D <= 256 && !(F8 && D == 256))
       compute_mma<D, G, F16, F8, MOD>(a, smem, bars, wc, tid);
     else
       compute<D, G, F16, F8, MOD>(a, smem, bars, wc, tid);
@@ -1023,7 +1032,7 @@ template <bool F16>
 cudaError_t launch_decode_typed(int d, int group, const CUtensorMap &tk, const CUtensorMap &tv,
                                 const DecodeArgs &a, int grid, cudaStream_t stream) {
   // group: the heads of one work item (DecodeArgs::nsplit items per kv head); at d = 256
-  // at most 4.
+  // at most 4 (more heads' staging would leave the ring two slots).
   if (d == 256) {
     switch (group) {
       case 1: return launch_decode_impl<256, 1, F16>(tk, tv, a, grid, stream);
