@@ -487,6 +487,7 @@ def run_ours(args, rank, world, dist):
         case = DecodeCase(w, dev, e4m3=args.kv_e4m3)
     else:
         case = BwdCase(w, dev) if args.backward else DenseCase(w, dev)
+    fa.set_cta_pairs(args.cta_pairs)
     stream = torch.cuda.current_stream()
 
     def barrier():
@@ -968,6 +969,8 @@ def main():
                     help="time the backward pass (fa_bwd) of the dense workload instead")
     ap.add_argument("--kv-e4m3", action="store_true",
                     help="decode workloads: E4M3 caches (fa_fwd_kvcache_fp8) instead of bf16")
+    ap.add_argument("--cta-pairs", action="store_true",
+                    help="dense forward workloads: run the forward on CTA pairs (cta_group::2)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -50,6 +50,10 @@ WORKLOADS = {
     "causal8k_d256": Workload("causal8k_d256", "dense", 2, 16, 16, 8192, 8192, 256, True, 1007),
     # the decode shape at head dimension 256 (half the batch: the same cache bytes)
     "decode_d256": Workload("decode_d256", "kvcache", 32, 32, 8, 1, 32768, 256, False, 1008),
+    # profiling captures: the causal 8k shape with one batch entry (192 MB of Q/K/V, above
+    # the 129 MB L2) and the decode shape with 16 sequences (2.1 GB of cache)
+    "causal8k_b1": Workload("causal8k_b1", "dense", 1, 32, 32, 8192, 8192, 128, True, 1009),
+    "decode_b16": Workload("decode_b16", "kvcache", 16, 32, 8, 1, 32768, 128, False, 1010),
 }
 
 
