@@ -256,6 +256,21 @@ def max_over_ranks(ms: float, dist, device) -> float:
     return float(t.item())
 
 
+def shard_workload(w, world: int, rank: int):
+    """The rank's part of a workload under head sharding (strong scaling): the kv heads are
+    cut into `world` contiguous ranges, each rank taking its kv heads and the query heads that
+    read them (the (batch, head) units are independent, so no collective is needed and each
+    GPU holds only its own K/V).  The rank draws its inputs with its own seed.  Requires Hkv
+    to be a multiple of world."""
+    import dataclasses
+    if world == 1:
+        return w
+    if w.Hkv % world != 0:
+        raise ValueError(f"{w.name}: {w.Hkv} kv heads do not split over {world} ranks")
+    return dataclasses.replace(w, Hq=w.Hq // world, Hkv=w.Hkv // world,
+                               seed=w.seed + 7919 * rank)
+
+
 def job_value(work_per_rank: float, ms_step: float, world: int, scale: float) -> float:
     """Whole-job throughput under weak scaling: every rank processes `work_per_rank`
     units per step; the job's step takes the slowest rank's time."""
@@ -482,7 +497,8 @@ def run_ours(args, rank, world, dist):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     pk = peaks()
-    w = WORKLOADS[args.workload]
+    w_job = WORKLOADS[args.workload]
+    w = shard_workload(w_job, world, rank) if args.shard else w_job
     if w.kind == "kvcache":
         case = DecodeCase(w, dev, e4m3=args.kv_e4m3)
     else:
@@ -538,10 +554,15 @@ def run_ours(args, rank, world, dist):
     e2e_val, e2e_unit = case.e2e_value(e2e_ms, world)
 
     d = case.describe(pk, ms_step, world)
+    if args.shard:  # every rank computed 1 / world of the one workload
+        d["config"]["parallelism"] = (f"kv heads sharded x{world} (each GPU holds its own "
+                                      "heads' K/V; no collective on the data path)")
+        d["config"]["workload"] += f" (this rank: Hq={w.Hq} Hkv={w.Hkv})"
     result = {
         "metric": d["metric"], "value": d["value"], "unit": d["unit"], "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "strong" if args.shard else "weak",
+        "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded iid N(0,1) bf16)", "config": d["config"],
         "roofline": d["roofline"],
         "e2e": {"value": e2e_val, "unit": e2e_unit, "ms_per_step": round(e2e_ms, 4),
@@ -969,6 +990,9 @@ def main():
                     help="time the backward pass (fa_bwd) of the dense workload instead")
     ap.add_argument("--kv-e4m3", action="store_true",
                     help="decode workloads: E4M3 caches (fa_fwd_kvcache_fp8) instead of bf16")
+    ap.add_argument("--shard", action="store_true",
+                    help="N > 1: split the one workload's kv heads over the ranks (strong "
+                         "scaling) instead of running it whole on every rank (weak scaling)")
     ap.add_argument("--cta-pairs", action="store_true",
                     help="dense forward workloads: run the forward on CTA pairs (cta_group::2)")
     args = ap.parse_args()
