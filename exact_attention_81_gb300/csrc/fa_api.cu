@@ -355,6 +355,8 @@ fa::PrefillArgs dense_args(const fa_fwd_params &a, int mblocks, int64_t tiles,
   pa.varlen = 0;
   pa.mblocks = mblocks;
   pa.num_tiles = static_cast<int>(tiles);
+  pa.half_from = pa.num_tiles;
+  pa.num_tickets = pa.num_tiles;
   pa.scale_log2 = scale_log2(a.scale);
   pa.err = dev->err;
   pa.timeout_ns = g_timeout_ns;
@@ -425,13 +427,21 @@ fa_status launch_dense(const fa_fwd_params &a, DeviceInfo *dev, const ModPlan &m
   if ((st = make_map(&tv, a.v, a.d, a.Nk, a.Hkv, a.B, a.v_strides[1], a.v_strides[2],
                      a.v_strides[0], a.dtype)) != FA_OK)
     return st;
-  const fa::PrefillArgs pa = dense_args(a, mblocks, tiles, dev, mod, lse_sb, lse_sh);
+  fa::PrefillArgs pa = dense_args(a, mblocks, tiles, dev, mod, lse_sb, lse_sh);
   cudaError_t e;
   if (pairs) {
     e = fa::launch_prefill_pair(mod.mask, a.dtype == FA_FP16, tq, tk, tv, pa,
                                 static_cast<int>(tiles), stream);
   } else {
     const int grid = static_cast<int>(tiles < dev->sm_count ? tiles : dev->sm_count);
+    // Without a mask every tile costs the same, and tiles % grid of them would run as a last,
+    // partial wave; they are handed out as two half tiles each instead (S double-buffered:
+    // a half tile takes about half a tile's time).
+    if (mod.mask == fa::MASK_NONE && fa::kernel_d(a.d) <= 128 && tiles > grid &&
+        tiles % grid != 0) {
+      pa.half_from = static_cast<int>(tiles - tiles % grid);
+      pa.num_tickets = pa.half_from + 2 * static_cast<int>(tiles % grid);
+    }
     e = fa::launch_prefill(fa::kernel_d(a.d), mod.mask, a.dtype == FA_FP16, tq, tk, tv, pa, grid,
                            stream);
   }
@@ -729,6 +739,8 @@ fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, fl
   pa.total_k = total_k;
   pa.mblocks = mblocks;
   pa.num_tiles = static_cast<int>(tiles);
+  pa.half_from = pa.num_tiles;
+  pa.num_tickets = pa.num_tiles;
   pa.scale_log2 = scale_log2(scale);
   pa.err = dev->err;
   pa.timeout_ns = g_timeout_ns;

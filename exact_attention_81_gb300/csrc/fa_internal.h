@@ -35,6 +35,9 @@ struct PrefillArgs {
   int total_q, total_k;
   int mblocks;                // query blocks (prefill_tile_rows rows) per (batch, head)
   int num_tiles;              // B * Hq * mblocks
+  int half_from;              // tiles [half_from, num_tiles) are handed out as two half tiles
+                              // (one 128-row sub-tile each); = num_tiles for none
+  int num_tickets;            // half_from + 2 * (num_tiles - half_from)
   float scale_log2;           // scale * log2(e)
   int sched_slot;             // this launch's tile-ticket counter slot
   int d;                      // head dimension of the tensors (the kernel's D may be larger:

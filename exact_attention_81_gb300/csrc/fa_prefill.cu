@@ -11,7 +11,10 @@
 //     O_t = 2^(m - m_new) O_t + P V_j       (P stored to TMEM as bf16, tcgen05.mma again)
 // with c = scale * log2(e) folded into one FMA before the exp2 ("flash-attention",
 // section 4, scale_apply_exp2), the O rescale done only for warps whose row maxima grew
-// ("FlashAttention 1-4 详解", FlashAttention 4, conditional rescale when m_new > m), and
+// ("FlashAttention 1-4 详解", FlashAttention 4, conditional rescale when m_new > m) and,
+// for 16-bit inputs, only when a row max grew past the reference max m by more than 8 (log2
+// units; m stays put otherwise, so P <= 2^8 -- O / l and m + log2 l do not depend on which
+// reference max P and l share), and
 // the division by l deferred to the epilogue ("FlashAttention 1-4 详解", FlashAttention 2,
 // normalise once after the inner loop).  The epilogue writes O (bf16) and the natural-log
 // LSE = ln2 * (m + log2 l).  S and P never leave the SM.
@@ -128,6 +131,7 @@ struct Bars {
 static_assert(sizeof(Bars) <= 512, "prefill barriers exceed their shared-memory region");
 
 struct TileInfo {
+  bool half;        // a half tile: sub-tile 0 only (rows shifted by 128 for the second half)
   int b, h, hk;
   int q_row0;       // first query row of the block (NSUB x 128 rows), within its sequence
   int q_tok, k_tok; // packed-token offset of the sequence (varlen), else 0
@@ -141,9 +145,18 @@ struct TileInfo {
 };
 
 // SUB: query rows of a sub-tile (128; 256 for a CTA pair, whose CTAs hold 128 rows each).
+// `ticket` is a tile number, or at or past a.half_from a half-tile ticket: ticket
+// half_from + 2 i + s stands for half s of tile half_from + i.
 template <int MASK, int NSUB, int SUB = BR>
-__device__ __forceinline__ TileInfo tile_info(const PrefillArgs &a, int tile) {
+__device__ __forceinline__ TileInfo tile_info(const PrefillArgs &a, int ticket) {
   TileInfo ti;
+  int tile = ticket, half = -1;
+  if (NSUB == 2 && ticket >= a.half_from) {
+    const int hh = ticket - a.half_from;
+    half = hh & 1;
+    tile = a.half_from + (hh >> 1);
+  }
+  ti.half = half >= 0;
   const int bh = tile / a.mblocks;
   const int r = tile - bh * a.mblocks;
   const bool desc = MASK == MASK_CAUSAL || (mask_has_window(MASK) && a.desc);
@@ -151,7 +164,7 @@ __device__ __forceinline__ TileInfo tile_info(const PrefillArgs &a, int tile) {
   ti.b = bh / a.Hq;
   ti.h = bh - ti.b * a.Hq;
   ti.hk = ti.h / a.group;
-  ti.q_row0 = mb * NSUB * SUB;
+  ti.q_row0 = mb * NSUB * SUB + (half > 0 ? BR : 0);
   if (a.varlen) {
     const int q0 = a.cu_q[ti.b], q1 = a.cu_q[ti.b + 1];
     const int k0 = a.cu_k[ti.b], k1 = a.cu_k[ti.b + 1];
@@ -174,7 +187,7 @@ __device__ __forceinline__ TileInfo tile_info(const PrefillArgs &a, int tile) {
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     const int first = ti.q_row0 + t * SUB;
-    const int nr = t < NSUB ? min(max(ti.nq - first, 0), SUB) : 0;
+    const int nr = t < (ti.half ? 1 : NSUB) ? min(max(ti.nq - first, 0), SUB) : 0;
     ti.nrows[t] = nr;
     lo[t] = 0;
     hi[t] = 0;
@@ -337,7 +350,7 @@ __device__ void producer_role(const PrefillArgs &a, const CUtensorMap *tmq,
     // runs into the wait limit.
     if (a.inject) break;
     const int ticket = static_cast<int>(atomicAdd(&ctr[0], 1u));
-    const int tile = ticket < a.num_tiles ? ticket : -1;
+    const int tile = ticket < a.num_tickets ? ticket : -1;
     const int rs = static_cast<int>(k % SCHED_DEPTH);
     if (!mbar_wait(&bars->sched_empty[rs], ((k / SCHED_DEPTH) & 1u) ^ 1u, wc)) goto out;
     bars->sched_tile[rs] = tile;
@@ -348,16 +361,27 @@ __device__ void producer_role(const PrefillArgs &a, const CUtensorMap *tmq,
     const int n = max(ti.je[0], ti.je[1]);
     if (n == 0) continue;
     if (q_iter > 0 && !mbar_wait(&bars->q_empty, (q_iter - 1) & 1u, wc)) goto out;
-    mbar_arrive_expect_tx(&bars->q_full, C::NSUB * C::TILE_BYTES);
+    {
+      const int nsub = ti.half ? 1 : C::NSUB;
+      mbar_arrive_expect_tx(&bars->q_full, nsub * C::TILE_BYTES);
+      for (int t = 0; t < nsub; ++t)
 #pragma unroll
-    for (int t = 0; t < C::NSUB; ++t)
-#pragma unroll
-      for (int c = 0; c < C::KCH; ++c)
-        tma_load_4d(smem + C::Q_OFF + t * C::TILE_BYTES + c * BOX_BYTES, tmq, &bars->q_full,
-                    c * C::BOX_ELEMS, ti.h, ti.q_tok + ti.q_row0 + t * BR, ti.tma_b);
+        for (int c = 0; c < C::KCH; ++c)
+          tma_load_4d(smem + C::Q_OFF + t * C::TILE_BYTES + c * BOX_BYTES, tmq, &bars->q_full,
+                      c * C::BOX_ELEMS, ti.h, ti.q_tok + ti.q_row0 + t * BR, ti.tma_b);
+    }
     ++q_iter;
     const int krow = ti.k_tok + ti.kv0 * BC;
-    if constexpr (C::WIDE) {
+    if (!C::WIDE && !F8 && ti.half) {
+      // half tile: S is double-buffered, so K(j + 1) is needed before V(j): ring order
+      // K_0, K_1, V_0, K_2, V_1, ..., V_{n-1}
+      bool ok = load_slot(tmk, 0, C::KCH, ti.hk, krow, ti.tma_b) &&
+                (n < 2 || load_slot(tmk, 0, C::KCH, ti.hk, krow + BC, ti.tma_b));
+      for (int j = 0; ok && j < n; ++j)
+        ok = load_slot(tmv, 0, C::KCH, ti.hk, krow + j * BC, ti.tma_b) &&
+             (j + 2 >= n || load_slot(tmk, 0, C::KCH, ti.hk, krow + (j + 2) * BC, ti.tma_b));
+      if (!ok) goto out;
+    } else if constexpr (C::WIDE) {
       // Ring order K_0, K_1, V_0, K_2, V_1, ..., V_{n-1} (the MMA issues S one step ahead),
       // each tile as two slots: d columns [0, 128) then [128, 256).
       bool ok = load_slot(tmk, 0, 2, ti.hk, krow, ti.tma_b) &&
@@ -392,7 +416,7 @@ out:
   __threadfence();
   if (atomicAdd(&ctr[1], 1u) == gridDim.x - 1) {
     const unsigned int taken = atomicAdd(&ctr[0], 0u);
-    if (!a.inject && taken != static_cast<unsigned int>(a.num_tiles) + gridDim.x)
+    if (!a.inject && taken != static_cast<unsigned int>(a.num_tickets) + gridDim.x)
       atomicOr(a.err, DEVERR_SCHED_OVERLAP);
     atomicExch(&ctr[0], 0u);
     atomicExch(&ctr[1], 0u);
@@ -447,7 +471,7 @@ __device__ void producer_role_pair(const PrefillArgs &a, const CUtensorMap *tmq,
     int tile;
     if (rank == 0) {
       const int ticket = static_cast<int>(atomicAdd(&ctr[0], 1u));
-      tile = ticket < a.num_tiles ? ticket : -1;
+      tile = ticket < a.num_tickets ? ticket : -1;
       if (!mbar_wait_cluster(&bars->sched_empty[rs], ((k / SCHED_DEPTH) & 1u) ^ 1u, wc)) goto out;
       bars->sched_tile[rs] = tile;
       st_cluster_u32(mapa_shared(&bars->sched_tile[rs], peer), static_cast<uint32_t>(tile));
@@ -491,7 +515,7 @@ out:
     __threadfence();
     if (atomicAdd(&ctr[1], 1u) == pairs - 1) {
       const unsigned int taken = atomicAdd(&ctr[0], 0u);
-      if (!a.inject && taken != static_cast<unsigned int>(a.num_tiles) + pairs)
+      if (!a.inject && taken != static_cast<unsigned int>(a.num_tickets) + pairs)
         atomicOr(a.err, DEVERR_SCHED_OVERLAP);
       atomicExch(&ctr[0], 0u);
       atomicExch(&ctr[1], 0u);
@@ -565,6 +589,55 @@ __device__ void mma_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, uint32
     if (n == 0) continue;
     if (!warp_wait(&bars->q_full, q_iter & 1u, wc)) goto out;
     ++q_iter;
+    if (!F8 && ti.half) {
+      // Half tile (sub-tile 0 alone): S double-buffered in the S regions of both sub-tiles,
+      // order S(0), S(1), PV(0), S(2), PV(1), ..., PV(n-1), so that the tensor core computes
+      // S(j+1) while the softmax works on S(j); S(j+2) reuses the buffer of S(j) right after
+      // PV(j) has read P(j) from it (issue order).  Every PV but the last is committed to
+      // pv_done: the softmax of step j+1 waits for it before it rescales O.
+      auto s_half = [&](int buf) -> bool {
+        const int slot = static_cast<int>(kv_iter % C::NSLOTS);
+        if (!warp_wait(&bars->kv_full[slot], (kv_iter / C::NSLOTS) & 1u, wc)) return false;
+        ++kv_iter;
+        tc_fence_after();
+        issue_s<D, F16>(tmem + s_col(buf), q_smem[0], ring + slot * C::TILE_BYTES);
+        mma_commit_w(&bars->s_full[buf]);
+        mma_commit_w(&bars->kv_empty[slot]);
+        return true;
+      };
+      if (!s_half(0)) goto out;
+      if (n > 1 && !s_half(1)) goto out;
+      // p_ready phases as bits (indexed by the runtime buffer number without local memory).
+      uint32_t pb = p_phase[0] | (p_phase[1] << 1);
+      for (int j = 0; j < n; ++j) {
+        const int buf = j & 1;
+        if (j == 0 && o_pending[0]) {
+          if (!warp_wait(&bars->o_empty[0], oe_phase[0], wc)) goto out;
+          oe_phase[0] ^= 1u;
+          o_pending[0] = false;
+        }
+        if (!warp_wait(&bars->p_ready[buf], (pb >> buf) & 1u, wc)) goto out;
+        pb ^= 1u << buf;
+        tc_fence_after();
+        const int slot = static_cast<int>(kv_iter % C::NSLOTS);
+        if (!warp_wait(&bars->kv_full[slot], (kv_iter / C::NSLOTS) & 1u, wc)) goto out;
+        ++kv_iter;
+        tc_fence_after();
+        issue_pv<D, F16>(tmem + o_col(0), tmem + s_col(buf), ring + slot * C::TILE_BYTES, j > 0);
+        mma_commit_w(&bars->kv_empty[slot]);
+        if (j == n - 1) {
+          mma_commit_w(&bars->o_full[0]);
+          o_pending[0] = true;
+        } else {
+          mma_commit_w(&bars->pv_done);
+        }
+        if (j + 2 < n && !s_half(buf)) goto out;
+      }
+      p_phase[0] = pb & 1u;
+      p_phase[1] = (pb >> 1) & 1u;
+      mma_commit_w(&bars->q_empty);
+      continue;
+    }
     {
       int slot_k = static_cast<int>(kv_iter % C::NSLOTS);
       if (!warp_wait(&bars->kv_full[slot_k], (kv_iter / C::NSLOTS) & 1u, wc)) goto out;
@@ -845,6 +918,9 @@ __device__ void softmax_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, ui
   // probabilities keep their significant bits); O = sum(P' V) / sum(P') is unchanged and
   // the LSE takes the 8 back out.
   constexpr float POFF = F8 ? 8.f : 0.f;
+  // Rescale threshold in log2 units: 16-bit P takes values up to 2^8 without loss; FP8 P has
+  // no room above its 2^8 offset, so its reference max follows every increase.
+  constexpr float RTH = F8 ? 0.f : 8.f;
   constexpr bool CAUSAL = MASK == MASK_CAUSAL;
   constexpr bool MOD = mask_has_window(MASK);   // window masking
   constexpr bool SCORE_MOD = MASK == MASK_MOD;    // softcap (+ ALiBi) code
@@ -878,8 +954,18 @@ __device__ void softmax_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, ui
     }
     if (tile < 0) break;
     const TileInfo ti = tile_info<MASK, C::NSUB, C::SUB_ROWS>(a, tile);
+    if constexpr (!C::WIDE && !PAIR) {
+      // Phase bits of S buffer 1, which both groups use: a full tile completes it once per
+      // step of sub-tile 1 (group 1's steps), a half tile once per odd step of its single
+      // sub-tile (group 0's); each group follows the completions it does not wait for.
+      if (t == 0 && !ti.half) s_phase ^= static_cast<uint32_t>(ti.nkv[1] & 1) << 1;
+      if (t == 1 && ti.half) s_phase ^= static_cast<uint32_t>((ti.nkv[0] / 2) & 1) << 1;
+    }
     const int sub_rows = t == 0 ? ti.nrows[0] : ti.nrows[1];  // rows of the whole sub-tile
     if (sub_rows == 0) continue;
+    // S alternates between two buffers (and P(j+1) is computed while PV(j) runs) in the wide
+    // kernel and in half tiles
+    const bool dbuf = C::WIDE || ti.half;
     const int nkv = t == 0 ? ti.nkv[0] : ti.nkv[1];
     const int kt0 = ti.kv0 + (t == 0 ? ti.js[0] : ti.js[1]);  // first K/V tile of this sub-tile
     const int first_row = ti.q_row0 + t * C::SUB_ROWS + rank * BR;  // this CTA's first row
@@ -910,10 +996,12 @@ __device__ void softmax_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, ui
     }
     const float ct = F8 && !(softcap || alibi || ALIBI) ? c * qks : c;
 
-    float m = -INFINITY, l = 0.f;
+    // l: the row sum of P (for the LSE); lq: the rounding error of the tiles' largest P
+    // (l + lq divides O).
+    float m = -INFINITY, l = 0.f, lq = 0.f;
     const uint64_t c2 = f2_pack(ct, ct);
     for (int j = 0; j < nkv; ++j) {
-      const int sb = C::WIDE ? (j & 1) : t;  // S buffer, and its s_full / p_ready barriers
+      const int sb = dbuf ? (j & 1) : t;  // S buffer, and its s_full / p_ready barriers
       const uint32_t tS = tmem + lane_off + s_col(sb);
       if (!warp_wait(&bars->s_full[sb], (s_phase >> sb) & 1u, wc)) return;
       s_phase ^= 1u << sb;
@@ -1008,12 +1096,25 @@ __device__ void softmax_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, ui
       }
       const float mx = fmaxf(fmax3(mx0, mx1, s[BC - 4]),
                              fmax3(mx2, mx3, fmax3(s[BC - 3], s[BC - 2], s[BC - 1])));
-      const float m_new = fmaxf(m, mx * ct + toff);
+      // The reference max m moves only when the tile's row max exceeds it by more than RTH:
+      // O and l are rescaled on those steps alone, and P = 2^(S c - m) stays below 2^RTH.
+      const float mx_s = mx * ct + toff;
+      const float m_new = mx_s > m + RTH ? mx_s : m;
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
       const bool grow = j > 0 && m_new > m;
       const float alpha = grow ? ex2_approx(m - m_use) : 1.f;
       // P = 2^(S c + toff - m_new) with the FMA and the row sum on packed fp32 pairs.
-      const uint64_t neg2 = f2_pack(POFF + toff - m_use, POFF + toff - m_use);
+      const float negs = POFF + toff - m_use;
+      const uint64_t neg2 = f2_pack(negs, negs);
+      // l sums P before its rounding to 16 bits, O the rounded P.  The tile's largest P (up
+      // to 2^RTH, not a power of two) may carry most of the row's weight: its rounding error
+      // goes into the divisor of O as well, so that a row dominated by one key still gets
+      // that key's V.
+      float lcorr = 0.f;
+      if constexpr (!F8) {
+        const float pmx = ex2_approx(fmaf(mx, ct, negs));  // the same FMA and exp2 as below
+        lcorr = lo_to_f32<F16>(pack2<F16>(pmx, 0.f)) - pmx;
+      }
       uint64_t l2a = f2_pack(0.f, 0.f), l2b = l2a;
       uint32_t p[64];
 #pragma unroll
@@ -1037,6 +1138,7 @@ __device__ void softmax_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, ui
         f2_unpack(l2a, la, lb);
         f2_unpack(l2b, lc, ld);
         l = l * alpha + ((la + lb) + (lc + ld));
+        lq = lq * alpha + lcorr;
       }
       if constexpr (F8) {
         // E4M3 row of 128 keys = 128 bytes, stored in the 128-byte-swizzled K-major layout
@@ -1053,13 +1155,11 @@ __device__ void softmax_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, ui
         tmem_st_x32(tS, p0);
         tmem_st_x32(tS + 32, p1);
       }
-      if constexpr (C::WIDE) {
+      if (dbuf && j > 0) {
         // S(j) was issued before PV(j-1): wait for PV(j-1) before touching O.
-        if (j > 0) {
-          if (!warp_wait(&bars->pv_done, pv_phase, wc)) return;
-          pv_phase ^= 1u;
-          tc_fence_after();
-        }
+        if (!warp_wait(&bars->pv_done, pv_phase, wc)) return;
+        pv_phase ^= 1u;
+        tc_fence_after();
       }
       if (__any_sync(0xffffffffu, grow)) {
         // Conditional rescale of the O accumulator held in TMEM, done after P so that the
@@ -1105,7 +1205,7 @@ __device__ void softmax_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, ui
       if (!warp_wait(&bars->o_full[t], o_phase, wc)) return;
       o_phase ^= 1u;
       tc_fence_after();
-      const float inv_l = l > 0.f ? vds / l : 0.f;  // vds: FP8 V descale, else 1
+      const float inv_l = l > 0.f ? vds / (l + lq) : 0.f;  // vds: FP8 V descale, else 1
 #pragma unroll
       for (int cc = 0; cc < D; cc += 32) {
         uint32_t r[32];

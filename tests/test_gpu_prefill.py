@@ -162,6 +162,41 @@ def test_varlen_bad_cu_seqlens_flagged():
     assert get_last_device_error() == FA_OK
 
 
+# ------------------------------------------------------------------ half tiles
+
+def _half_tile_case(which, sm):
+    # (B, Nq, Nk, Hq, Hkv, d): tile count just above the SM count and not a multiple of it,
+    # so the last partial wave runs as half tiles; ragged last query blocks whose second
+    # half is empty, and a ragged last key tile.
+    if which == "ragged_rows":
+        hq = (sm + 10 + 1) // 2  # 2 query blocks (256 rows) per head
+        return 1, 300, 300, hq, hq, 128
+    hq = sm // 6 + 1           # 3 query blocks per head, 2 batch entries
+    return 2, 600, 1000, hq, 1, 64
+
+
+@pytest.mark.parametrize("which", ["ragged_rows", "mqa_ragged_keys"])
+def test_half_tiles_last_wave(which):
+    """Without a mask, the tiles of the last, partial wave are split into two half tiles
+    (one 128-row sub-tile each); every row is computed as in a whole tile, so the output
+    equals the varlen call (which never splits tiles) bit for bit, and the oracle."""
+    sm = torch.cuda.get_device_properties(0).multi_processor_count
+    B, Nq, Nk, Hq, Hkv, d = _half_tile_case(which, sm)
+    tiles = B * Hq * ((Nq + 255) // 256)
+    assert tiles > sm and tiles % sm != 0
+    q, k, v = dense_inputs(B, Nq, Nk, Hq, Hkv, d, seed=4100 + Nq + d, device=DEV)
+    o, lse = _run_dense(q, k, v, False)
+    cu_q = torch.arange(0, (B + 1) * Nq, Nq, dtype=torch.int32, device=DEV)
+    cu_k = torch.arange(0, (B + 1) * Nk, Nk, dtype=torch.int32, device=DEV)
+    o_v, l_v = fa_fwd_varlen(q.reshape(B * Nq, Hq, d), k.reshape(B * Nk, Hkv, d),
+                             v.reshape(B * Nk, Hkv, d), cu_q, cu_k, Nq, Nk, causal=False)
+    assert get_last_device_error() == FA_OK
+    assert torch.equal(o_v.reshape(B, Nq, Hq, d), o)
+    assert torch.equal(l_v.reshape(Hq, B, Nq).permute(1, 0, 2), lse)  # varlen LSE: (Hq, total_q)
+    o_ref, lse_ref = _oracle_dense(q, k, v, False, float(np.float32(1 / math.sqrt(d))))
+    compare(*dense_rows(o, lse), *dense_rows(o_ref, lse_ref), f"half tiles {which}")
+
+
 # ------------------------------------------------------------------ full-size workloads
 
 @pytest.mark.parametrize("name", ["dense2k", "causal8k", "gqa16k"])
