@@ -277,6 +277,11 @@ void set_mod_fields(const ModPlan &m, float scale, Args *a) {
 void apply_mod(const ModPlan &m, float scale, fa::PrefillArgs *pa) {
   set_mod_fields(m, scale, pa);
   pa->desc = m.wr >= 0;
+  // ALiBi with a right-bounded window: the bias grows toward the last visible key, so the
+  // K/V tiles run last-first and the row max is met on the first tile instead of moving
+  // (and rescaling O) on every one.  Not with a softcap: there the reversed order measured
+  // slower (1.5 % on causal 8k), the softcap's tanh and not the rescale bounding the step.
+  pa->kv_rev = m.alibi != nullptr && m.wr >= 0 && m.softcap == 0.f;
 }
 
 // Keys per split when the caller leaves it to the library.  Long chunks amortise the

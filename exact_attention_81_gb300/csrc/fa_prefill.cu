@@ -111,6 +111,27 @@ static_assert(Cfg<128, false, true>::SMEM_BYTES <= 227 * 1024, "fp8 prefill exce
 static_assert(Cfg<256>::SMEM_BYTES <= 227 * 1024, "wide prefill exceeds shared memory");
 static_assert(Cfg<128, false, false, true>::SMEM_BYTES <= 227 * 1024, "pair prefill exceeds smem");
 
+// ALiBi column bias built by the tensor core (ALiBi without a softcap; 16-bit inputs, width
+// <= 128, one CTA).  On a tile whose keys all lie at or before the position of every row of
+// the sub-tile, the bias -slope |pos - key| is slope (key - kbase) plus a per-row constant;
+// its per-column part, divided by the score scale, enters S through one more 128 x 128 x 16
+// MMA ahead of Q K^T: A is a ones matrix (1 in k = 0..2), B holds in row i a three-term bf16
+// split of i slope / scale (k = 0..2).  Both are K-major and 128B-swizzled (only the first
+// 32 bytes of each 128-byte row are read; the second 16 bytes stay zero), 16 KB each,
+// right after the barriers.
+template <int D, int MASK, bool F8, bool PAIR>
+__host__ __device__ constexpr bool abias() {
+  return MASK == MASK_ALIBI && !F8 && !PAIR && D <= 128;
+}
+constexpr int ABIAS_BYTES = 2 * BR * 128;
+template <int D, int MASK, bool F16, bool F8, bool PAIR>
+__host__ __device__ constexpr int prefill_smem() {
+  using C = Cfg<D, F16, F8, PAIR>;
+  return abias<D, MASK, F8, PAIR>() ? C::BAR_OFF + 1024 + ABIAS_BYTES + 1024 : C::SMEM_BYTES;
+}
+static_assert(prefill_smem<128, MASK_ALIBI, false, false, false>() <= 227 * 1024,
+              "ALiBi prefill exceeds shared memory");
+
 // Per-launch tile-ticket counters: [slot][0] = next ticket, [slot][1] = CTAs finished.
 // The host gives each launch its own slot (round robin); the last CTA of a launch to
 // finish resets the slot to zero for its next user.
@@ -142,6 +163,8 @@ struct TileInfo {
   // [js[t], je[t]) and so visits nkv[t] = je[t] - js[t] tiles (0: its rows see no key).
   int kv0;
   int js[2], je[2], nkv[2];
+  // Key tile of stream step j: kt_first + kdir * j (kdir = -1: the tiles run last-first).
+  int kt_first, kdir;
 };
 
 // SUB: query rows of a sub-tile (128; 256 for a CTA pair, whose CTAs hold 128 rows each).
@@ -219,7 +242,30 @@ __device__ __forceinline__ TileInfo tile_info(const PrefillArgs &a, int ticket) 
     ti.je[t] = act ? hi[t] - ti.kv0 : 0;
     ti.nkv[t] = ti.je[t] - ti.js[t];
   }
+  ti.kt_first = ti.kv0;
+  ti.kdir = 1;
+  if ((MASK == MASK_ALIBI || MASK == MASK_MOD) && a.kv_rev) {
+    // Last-first: step j streams tile kv0 + n - 1 - j, so sub-tile t's tiles
+    // [kv0 + js, kv0 + je) are the steps [n - je, n - js).
+    const int n = max(ti.je[0], ti.je[1]);
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      if (ti.nkv[t] > 0) {
+        const int js = ti.js[t];
+        ti.js[t] = n - ti.je[t];
+        ti.je[t] = n - js;
+      }
+    }
+    ti.kt_first = ti.kv0 + n - 1;
+    ti.kdir = -1;
+  }
   return ti;
+}
+
+// Whether every key of the tile at kbase lies at or before the position of every row of
+// sub-tile t (the first row has the smallest position, so it decides for all).
+__device__ __forceinline__ bool alibi_lin(const TileInfo &ti, int t, int kbase) {
+  return ti.q_row0 + t * BR + (ti.nk - ti.nq) - kbase >= BC - 1;
 }
 
 __device__ __forceinline__ bool varlen_bad(const PrefillArgs &a, int b) {
@@ -250,6 +296,22 @@ __device__ __forceinline__ void issue_s(uint32_t d_tmem, uint32_t q_smem, uint32
     const uint32_t off = static_cast<uint32_t>((kk >> 2) * BOX_BYTES + (kk & 3) * 32);
     mma_bf16_ss_w(d_tmem, sw128_desc(q_smem + off, 16, 1024),
                   sw128_desc(k_smem + off, 16, 1024), Cfg<D, F16>::IDESC_S, kk > 0 ? 1u : 0u);
+  }
+}
+
+// S_t = A B^T + Q_t K^T: the ALiBi column bias (bf16 MMA over the two bias operands at
+// bias_smem) and then the D/16 MMAs of issue_s, accumulating onto it.
+template <int D, bool F16>
+__device__ __forceinline__ void issue_s_alibi(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem,
+                                              uint32_t bias_smem) {
+  mma_bf16_ss_w(d_tmem, sw128_desc(bias_smem, 16, 1024),
+                sw128_desc(bias_smem + static_cast<uint32_t>(BR * 128), 16, 1024),
+                idesc_bf16_f32(BR, BC, false, false, false), 0u);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = static_cast<uint32_t>((kk >> 2) * BOX_BYTES + (kk & 3) * 32);
+    mma_bf16_ss_w(d_tmem, sw128_desc(q_smem + off, 16, 1024),
+                  sw128_desc(k_smem + off, 16, 1024), Cfg<D, F16>::IDESC_S, 1u);
   }
 }
 
@@ -371,15 +433,16 @@ __device__ void producer_role(const PrefillArgs &a, const CUtensorMap *tmq,
                       c * C::BOX_ELEMS, ti.h, ti.q_tok + ti.q_row0 + t * BR, ti.tma_b);
     }
     ++q_iter;
-    const int krow = ti.k_tok + ti.kv0 * BC;
+    const int krow = ti.k_tok + ti.kt_first * BC;  // K/V row of stream step j: krow + j kst
+    const int kst = ti.kdir * BC;
     if (!C::WIDE && !F8 && ti.half) {
       // half tile: S is double-buffered, so K(j + 1) is needed before V(j): ring order
       // K_0, K_1, V_0, K_2, V_1, ..., V_{n-1}
       bool ok = load_slot(tmk, 0, C::KCH, ti.hk, krow, ti.tma_b) &&
-                (n < 2 || load_slot(tmk, 0, C::KCH, ti.hk, krow + BC, ti.tma_b));
+                (n < 2 || load_slot(tmk, 0, C::KCH, ti.hk, krow + kst, ti.tma_b));
       for (int j = 0; ok && j < n; ++j)
-        ok = load_slot(tmv, 0, C::KCH, ti.hk, krow + j * BC, ti.tma_b) &&
-             (j + 2 >= n || load_slot(tmk, 0, C::KCH, ti.hk, krow + (j + 2) * BC, ti.tma_b));
+        ok = load_slot(tmv, 0, C::KCH, ti.hk, krow + j * kst, ti.tma_b) &&
+             (j + 2 >= n || load_slot(tmk, 0, C::KCH, ti.hk, krow + (j + 2) * kst, ti.tma_b));
       if (!ok) goto out;
     } else if constexpr (C::WIDE) {
       // Ring order K_0, K_1, V_0, K_2, V_1, ..., V_{n-1} (the MMA issues S one step ahead),
@@ -387,23 +450,23 @@ __device__ void producer_role(const PrefillArgs &a, const CUtensorMap *tmq,
       bool ok = load_slot(tmk, 0, 2, ti.hk, krow, ti.tma_b) &&
                 load_slot(tmk, 2, 2, ti.hk, krow, ti.tma_b);
       for (int j = 1; ok && j < n; ++j)
-        ok = load_slot(tmk, 0, 2, ti.hk, krow + j * BC, ti.tma_b) &&
-             load_slot(tmk, 2, 2, ti.hk, krow + j * BC, ti.tma_b) &&
-             load_slot(tmv, 0, 2, ti.hk, krow + (j - 1) * BC, ti.tma_b) &&
-             load_slot(tmv, 2, 2, ti.hk, krow + (j - 1) * BC, ti.tma_b);
-      ok = ok && load_slot(tmv, 0, 2, ti.hk, krow + (n - 1) * BC, ti.tma_b) &&
-           load_slot(tmv, 2, 2, ti.hk, krow + (n - 1) * BC, ti.tma_b);
+        ok = load_slot(tmk, 0, 2, ti.hk, krow + j * kst, ti.tma_b) &&
+             load_slot(tmk, 2, 2, ti.hk, krow + j * kst, ti.tma_b) &&
+             load_slot(tmv, 0, 2, ti.hk, krow + (j - 1) * kst, ti.tma_b) &&
+             load_slot(tmv, 2, 2, ti.hk, krow + (j - 1) * kst, ti.tma_b);
+      ok = ok && load_slot(tmv, 0, 2, ti.hk, krow + (n - 1) * kst, ti.tma_b) &&
+           load_slot(tmv, 2, 2, ti.hk, krow + (n - 1) * kst, ti.tma_b);
       if (!ok) goto out;
     } else if constexpr (F8) {
       // V^T rows start at the sequence's first key (dense only: k_tok = 0).
       for (int j = 0; j < n; ++j)
-        if (!load_slot(tmk, 0, C::KCH, ti.hk, krow + j * BC, ti.tma_b) ||
-            !load_vt(ti.hk, krow + j * BC, ti.tma_b))
+        if (!load_slot(tmk, 0, C::KCH, ti.hk, krow + j * kst, ti.tma_b) ||
+            !load_vt(ti.hk, krow + j * kst, ti.tma_b))
           goto out;
     } else {
       for (int j = 0; j < n; ++j)
-        if (!load_slot(tmk, 0, C::KCH, ti.hk, krow + j * BC, ti.tma_b) ||
-            !load_slot(tmv, 0, C::KCH, ti.hk, krow + j * BC, ti.tma_b))
+        if (!load_slot(tmk, 0, C::KCH, ti.hk, krow + j * kst, ti.tma_b) ||
+            !load_slot(tmv, 0, C::KCH, ti.hk, krow + j * kst, ti.tma_b))
           goto out;
     }
   }
@@ -502,10 +565,11 @@ __device__ void producer_role_pair(const PrefillArgs &a, const CUtensorMap *tmq,
                            ti.tma_b);
     }
     ++q_iter;
-    const int krow = ti.k_tok + ti.kv0 * BC;
+    const int krow = ti.k_tok + ti.kt_first * BC;
+    const int kst = ti.kdir * BC;
     for (int j = 0; j < n; ++j)
-      if (!load_half(false, ti.hk, krow + j * BC, ti.tma_b) ||
-          !load_half(true, ti.hk, krow + j * BC, ti.tma_b))
+      if (!load_half(false, ti.hk, krow + j * kst, ti.tma_b) ||
+          !load_half(true, ti.hk, krow + j * kst, ti.tma_b))
         goto out;
   }
 out:
@@ -580,6 +644,9 @@ __device__ void mma_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, uint32
   bool o_pending[2] = {false, false};
   const uint32_t q_smem[2] = {smem_u32(smem + C::Q_OFF), smem_u32(smem + C::Q_OFF + C::TILE_BYTES)};
   const uint32_t ring = smem_u32(smem + C::RING_OFF);
+  constexpr bool ABIAS = abias<D, MASK, F8, false>();
+  const uint32_t bias_smem = smem_u32(smem + C::BAR_OFF + 1024);
+  int bias_bh = -1;  // (batch, head) whose slope the B bias operand holds
   for (uint32_t k = 0;; ++k) {
     int tile;
     if (!next_tile_mma(bars, k, tile, lane, wc)) goto out;
@@ -587,6 +654,27 @@ __device__ void mma_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, uint32
     const TileInfo ti = tile_info<MASK, 2>(a, tile);
     const int n = max(ti.je[0], ti.je[1]);
     if (n == 0) continue;
+    if constexpr (ABIAS) {
+      // The previous tile's MMAs have completed (its last P was ready, so the S before it
+      // was), so B may be rewritten: row i = i slope / scale as hi + mid + lo in bf16.
+      const int bh = ti.b * a.Hq + ti.h;
+      if (bh != bias_bh) {
+        bias_bh = bh;
+        const float ratio = a.alibi[ti.b * a.alibi_sb + ti.h] * 1.4426950408889634f / a.scale_log2;
+        uint8_t *bb = smem + C::BAR_OFF + 1024 + BR * 128;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int i = lane * 4 + q;
+          const float v = static_cast<float>(i) * ratio;
+          const float vh = bf16lo_to_f32(pack_bf16x2(v, 0.f));
+          const float vm = bf16lo_to_f32(pack_bf16x2(v - vh, 0.f));
+          *reinterpret_cast<uint4 *>(bb + i * 128 + ((i & 7) << 4)) =
+              make_uint4(pack_bf16x2(vh, vm), pack_bf16x2((v - vh) - vm, 0.f), 0u, 0u);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+    }
     if (!warp_wait(&bars->q_full, q_iter & 1u, wc)) goto out;
     ++q_iter;
     if (!F8 && ti.half) {
@@ -646,7 +734,11 @@ __device__ void mma_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, uint32
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         if (ti.js[t] == 0 && ti.je[t] > 0) {
-          issue_s<D, F16, F8>(tmem + s_col(t), q_smem[t], ring + slot_k * C::TILE_BYTES);
+          if (ABIAS && alibi_lin(ti, t, ti.kt_first * BC))
+            issue_s_alibi<D, F16>(tmem + s_col(t), q_smem[t], ring + slot_k * C::TILE_BYTES,
+                                  bias_smem);
+          else
+            issue_s<D, F16, F8>(tmem + s_col(t), q_smem[t], ring + slot_k * C::TILE_BYTES);
           mma_commit_w(&bars->s_full[t]);
         }
       }
@@ -687,7 +779,11 @@ __device__ void mma_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, uint32
           }
           if (t == 1) mma_commit_w(&bars->kv_empty[slot_v]);
           if (j + 1 >= ti.js[t] && j + 1 < ti.je[t]) {
-            issue_s<D, F16, F8>(tmem + s_col(t), q_smem[t], ring + slot_k * C::TILE_BYTES);
+            if (ABIAS && alibi_lin(ti, t, (ti.kt_first + ti.kdir * (j + 1)) * BC))
+              issue_s_alibi<D, F16>(tmem + s_col(t), q_smem[t], ring + slot_k * C::TILE_BYTES,
+                                    bias_smem);
+            else
+              issue_s<D, F16, F8>(tmem + s_col(t), q_smem[t], ring + slot_k * C::TILE_BYTES);
             mma_commit_w(&bars->s_full[t]);
           }
         }
@@ -967,7 +1063,7 @@ __device__ void softmax_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, ui
     // kernel and in half tiles
     const bool dbuf = C::WIDE || ti.half;
     const int nkv = t == 0 ? ti.nkv[0] : ti.nkv[1];
-    const int kt0 = ti.kv0 + (t == 0 ? ti.js[0] : ti.js[1]);  // first K/V tile of this sub-tile
+    const int jst = t == 0 ? ti.js[0] : ti.js[1];  // this sub-tile's first stream step
     const int first_row = ti.q_row0 + t * C::SUB_ROWS + rank * BR;  // this CTA's first row
     const int nrows = min(max(sub_rows - rank * BR, 0), BR);       // this CTA's rows
     const int row = first_row + rit;
@@ -999,7 +1095,7 @@ __device__ void softmax_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, ui
     // l: the row sum of P (for the LSE); lq: the rounding error of the tiles' largest P
     // (l + lq divides O).
     float m = -INFINITY, l = 0.f, lq = 0.f;
-    const uint64_t c2 = f2_pack(ct, ct);
+    const uint64_t c2t = f2_pack(ct, ct);
     for (int j = 0; j < nkv; ++j) {
       const int sb = dbuf ? (j & 1) : t;  // S buffer, and its s_full / p_ready barriers
       const uint32_t tS = tmem + lane_off + s_col(sb);
@@ -1016,7 +1112,7 @@ __device__ void softmax_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, ui
           s[64 + i] = __uint_as_float(r1[i]);
         }
       }
-      const int kbase = (kt0 + j) * BC;
+      const int kbase = (ti.kt_first + ti.kdir * (jst + j)) * BC;
       // ALiBi without a softcap: the stored scores are y = s scale log2e - slope2 |pos - key|
       // - toff, in log2 units, and toff (a per-row constant of the tile) goes into the max
       // and the exp2 offset.  When every key of the tile lies at or before pos (all of a
@@ -1025,10 +1121,15 @@ __device__ void softmax_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, ui
       // slope2 i is one packed FMA per pair, the slope2 i pairs stepping by 8 slope2 along
       // four independent chains that start from exact products.
       float toff = 0.f;
+      float ctj = ct;  // the factor that takes this tile's scores to log2 units
       if constexpr (ALIBI) {
         const float cs = F8 ? a.scale_log2 * qks : a.scale_log2;
         const int dist0 = row + off - kbase;  // pos - the tile's first key
-        if (dist0 >= BC - 1) {
+        if (abias<D, MASK, F8, PAIR>() && alibi_lin(ti, t, kbase)) {
+          // The tensor core added slope2 i / cs to the scores: only toff is left.
+          toff = -slope2 * static_cast<float>(dist0);
+          ctj = cs;
+        } else if (dist0 >= BC - 1) {
           toff = -slope2 * static_cast<float>(dist0);
           const uint64_t cs2 = f2_pack(cs, cs);
           const uint64_t step = f2_pack(8.f * slope2, 8.f * slope2);
@@ -1098,7 +1199,7 @@ __device__ void softmax_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, ui
                              fmax3(mx2, mx3, fmax3(s[BC - 3], s[BC - 2], s[BC - 1])));
       // The reference max m moves only when the tile's row max exceeds it by more than RTH:
       // O and l are rescaled on those steps alone, and P = 2^(S c - m) stays below 2^RTH.
-      const float mx_s = mx * ct + toff;
+      const float mx_s = mx * ctj + toff;
       const float m_new = mx_s > m + RTH ? mx_s : m;
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
       const bool grow = j > 0 && m_new > m;
@@ -1106,15 +1207,7 @@ __device__ void softmax_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, ui
       // P = 2^(S c + toff - m_new) with the FMA and the row sum on packed fp32 pairs.
       const float negs = POFF + toff - m_use;
       const uint64_t neg2 = f2_pack(negs, negs);
-      // l sums P before its rounding to 16 bits, O the rounded P.  The tile's largest P (up
-      // to 2^RTH, not a power of two) may carry most of the row's weight: its rounding error
-      // goes into the divisor of O as well, so that a row dominated by one key still gets
-      // that key's V.
-      float lcorr = 0.f;
-      if constexpr (!F8) {
-        const float pmx = ex2_approx(fmaf(mx, ct, negs));  // the same FMA and exp2 as below
-        lcorr = lo_to_f32<F16>(pack2<F16>(pmx, 0.f)) - pmx;
-      }
+      const uint64_t c2 = abias<D, MASK, F8, PAIR>() ? f2_pack(ctj, ctj) : c2t;
       uint64_t l2a = f2_pack(0.f, 0.f), l2b = l2a;
       uint32_t p[64];
 #pragma unroll
@@ -1132,6 +1225,15 @@ __device__ void softmax_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, ui
           p[i] = pack2<F16>(p0, p1);
           p[i + 1] = pack2<F16>(p2, p3);
         }
+      }
+      // l sums P before its rounding to 16 bits, O the rounded P.  The tile's largest P (up
+      // to 2^RTH, not a power of two) may carry most of the row's weight: its rounding error
+      // goes into the divisor of O as well, so that a row dominated by one key still gets
+      // that key's V.
+      float lcorr = 0.f;
+      if constexpr (!F8) {
+        const float pmx = ex2_approx(fmaf(mx, ctj, negs));  // the loop's FMA and exp2
+        lcorr = lo_to_f32<F16>(pack2<F16>(pmx, 0.f)) - pmx;
       }
       {
         float la, lb, lc, ld;
@@ -1277,6 +1379,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     bars->abort = 0;
     fence_barrier_init();
   }
+  if constexpr (abias<D, MASK, F8, PAIR>()) {
+    // Ones matrix A (row r: 1 in k = 0..2) and the zero second 16 bytes of every B row.
+    if (threadIdx.x < BR) {
+      const int r = static_cast<int>(threadIdx.x);
+      uint8_t *ab = smem + C::BAR_OFF + 1024;
+      const uint32_t one2 = pack_bf16x2(1.f, 1.f), one1 = pack_bf16x2(1.f, 0.f);
+      *reinterpret_cast<uint4 *>(ab + r * 128 + ((r & 7) << 4)) = make_uint4(one2, one1, 0u, 0u);
+      *reinterpret_cast<uint4 *>(ab + r * 128 + (((r & 7) ^ 1) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4 *>(ab + BR * 128 + r * 128 + (((r & 7) ^ 1) << 4)) =
+          make_uint4(0u, 0u, 0u, 0u);
+      fence_proxy_async_smem();
+    }
+  }
   if (warp == PRODUCER_WARP && lane == 0) {
     tma_prefetch_desc(&tmq);
     tma_prefetch_desc(&tmk);
@@ -1370,7 +1485,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 template <int D, int MASK, bool F16, bool F8 = false>
 cudaError_t launch_impl(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                         const PrefillArgs &a, int grid, cudaStream_t stream) {
-  constexpr int smem = Cfg<D, F16, F8>::SMEM_BYTES;
+  constexpr int smem = prefill_smem<D, MASK, F16, F8, false>();
   cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, MASK, F16, F8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
