@@ -280,7 +280,7 @@ def job_value(work_per_rank: float, ms_step: float, world: int, scale: float) ->
 class DenseCase:
     """One fa_fwd call over a dense workload; work = FLOPs."""
 
-    def __init__(self, w, dev):
+    def __init__(self, w, dev, softcap=0.0, alibi=False):
         import torch
         from exact_attention_81_gb300.inputs import workload_inputs
         self.w = w
@@ -289,10 +289,19 @@ class DenseCase:
         self.lse = torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device=dev)
         self.work = flops(w)
         self.launches = 1
+        # score modifiers (softcap, ALiBi with the geometric slopes 2^(-8 (h + 1) / H))
+        self.mods = {}
+        if softcap > 0.0:
+            self.mods["softcap"] = softcap
+        if alibi:
+            self.mods["alibi_slopes"] = torch.tensor(
+                [2.0 ** (-8.0 * (h + 1) / w.Hq) for h in range(w.Hq)], dtype=torch.float32,
+                device=dev)
 
     def step(self):
         import exact_attention_81_gb300 as fa
-        fa.fa_fwd(self.q, self.k, self.v, causal=self.w.causal, out=self.out, lse=self.lse)
+        fa.fa_fwd(self.q, self.k, self.v, causal=self.w.causal, out=self.out, lse=self.lse,
+                  **self.mods)
 
     def e2e(self):
         """Pinned host Q/K/V copied in, O/LSE copied out, every step, through fa_fwd_host
@@ -315,6 +324,14 @@ class DenseCase:
         w = self.w
         tf = self.work / (ms_step * 1e-3) / 1e12
         io = (self.q.numel() + self.k.numel() + self.v.numel()) * 2
+        kernel = f"prefill_kernel<{w.d},{str(w.causal).lower()}>"
+        mods = []
+        if "softcap" in self.mods:
+            mods.append(f"softcap {self.mods['softcap']:g}")
+        if "alibi_slopes" in self.mods:
+            mods.append("ALiBi 2^(-8(h+1)/H)")
+        if mods:
+            kernel = f"prefill_kernel<{w.d},{str(w.causal).lower()},{'+'.join(mods)}>"
         return {
             "metric": METRIC, "unit": "TFLOPS",
             "value": round(job_value(self.work, ms_step, world, 1e12), 2),
@@ -323,14 +340,13 @@ class DenseCase:
                        "batch": w.B, "heads": w.Hq, "seq_len": w.Nq, "head_dim": w.d,
                        "causal": w.causal,
                        "parallelism": f"replicas x{world} (independent heads)",
-                       "l2": f"inputs {io / 1e6:.0f} MB > L2 {L2_BYTES / 1e6:.0f} MB, no flush"},
+                       "l2": f"inputs {io / 1e6:.0f} MB > L2 {L2_BYTES / 1e6:.0f} MB, no flush",
+                       **({"modifiers": ", ".join(mods)} if mods else {})},
             "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": pk["bf16"],
                          "unit": "TFLOP/s", "frac": round(tf / pk["bf16"], 4),
-                         "traffic": profiled_traffic(f"prefill_kernel<{w.d},{str(w.causal).lower()}>",
-                                                     PREFILL_SRC, w.name),
+                         "traffic": profiled_traffic(kernel, PREFILL_SRC, w.name),
                          "peak_basis": f"{pk['basis']} bf16 dense (burst)",
-                         "kernel": f"prefill_kernel<{w.d},{str(w.causal).lower()}> "
-                                   "(one launch per step)"},
+                         "kernel": f"{kernel} (one launch per step)"},
         }
 
     def e2e_value(self, ms, world):
@@ -502,7 +518,7 @@ def run_ours(args, rank, world, dist):
     if w.kind == "kvcache":
         case = DecodeCase(w, dev, e4m3=args.kv_e4m3)
     else:
-        case = BwdCase(w, dev) if args.backward else DenseCase(w, dev)
+        case = BwdCase(w, dev) if args.backward else DenseCase(w, dev, args.softcap, args.alibi)
     fa.set_cta_pairs(args.cta_pairs)
     stream = torch.cuda.current_stream()
 
@@ -993,6 +1009,10 @@ def main():
     ap.add_argument("--shard", action="store_true",
                     help="N > 1: split the one workload's kv heads over the ranks (strong "
                          "scaling) instead of running it whole on every rank (weak scaling)")
+    ap.add_argument("--softcap", type=float, default=0.0,
+                    help="dense forward workloads: softcap the scores (tanh, this cap)")
+    ap.add_argument("--alibi", action="store_true",
+                    help="dense forward workloads: ALiBi bias, slopes 2^(-8 (h + 1) / H)")
     ap.add_argument("--cta-pairs", action="store_true",
                     help="dense forward workloads: run the forward on CTA pairs (cta_group::2)")
     args = ap.parse_args()

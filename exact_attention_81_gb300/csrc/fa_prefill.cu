@@ -695,6 +695,7 @@ __device__ void mma_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, uint32
       };
       if (!s_half(0)) goto out;
       if (n > 1 && !s_half(1)) goto out;
+      if (n <= 2) mma_commit_w(&bars->q_empty);  // Q released after the last S, as below
       // p_ready phases as bits (indexed by the runtime buffer number without local memory).
       uint32_t pb = p_phase[0] | (p_phase[1] << 1);
       for (int j = 0; j < n; ++j) {
@@ -720,10 +721,10 @@ __device__ void mma_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, uint32
           mma_commit_w(&bars->pv_done);
         }
         if (j + 2 < n && !s_half(buf)) goto out;
+        if (j + 3 == n) mma_commit_w(&bars->q_empty);
       }
       p_phase[0] = pb & 1u;
       p_phase[1] = (pb >> 1) & 1u;
-      mma_commit_w(&bars->q_empty);
       continue;
     }
     {
@@ -743,6 +744,10 @@ __device__ void mma_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, uint32
         }
       }
       mma_commit_w(&bars->kv_empty[slot_k]);
+      // Q is read by the S products alone: it is released once the tile's last S is issued
+      // (the commit fires when that S completes), so that the next tile's Q loads while
+      // this tile's last step runs.
+      if (n == 1) mma_commit_w(&bars->q_empty);
       for (int j = 0; j < n; ++j) {
         const int slot_v = static_cast<int>(kv_iter % C::NSLOTS);
         if (!warp_wait(&bars->kv_full[slot_v], (kv_iter / C::NSLOTS) & 1u, wc)) goto out;
@@ -788,9 +793,9 @@ __device__ void mma_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, uint32
           }
         }
         if (slot_k >= 0) mma_commit_w(&bars->kv_empty[slot_k]);
+        if (j == n - 2) mma_commit_w(&bars->q_empty);  // the last S was issued in this step
       }
     }
-    mma_commit_w(&bars->q_empty);
   }
 out:
   // Teardown: every MMA issued so far must finish before TMEM is released.
