@@ -769,6 +769,24 @@ def extra_workloads(args, dev, pk, world, dist):
         res[name] = {"ms": round(ms, 4), "TFLOPS": round(tf, 2),
                      "frac_of_bf16_peak": round(tf / pk["bf16"], 4)}
     del q, k, v, do, o, l, dq, dk, dv, bws
+    # backward at head dimension 256 (the wide kernel: units per d half, 64-query steps;
+    # FLOPs as above: the algorithmic five matmuls, not the recomputed S and dP of the
+    # second d half)
+    w = WORKLOADS["causal8k_d256"]
+    q, k, v = workload_inputs(w, device=dev)
+    do = torch.randn(q.shape, device=dev, generator=torch.Generator(device=dev).manual_seed(9))
+    do = do.to(torch.bfloat16)
+    o, l = fa.fa_fwd(q, k, v, causal=True)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    bws = torch.empty(fa.fa_bwd_workspace_size(w.B, w.Nq, w.Hq, w.d), dtype=torch.uint8,
+                      device=dev)
+    ms = time_calls(lambda: fa.fa_bwd(q, k, v, o, l, do, causal=True, dq=dq, dk=dk, dv=dv,
+                                      workspace=bws), max(10, args.steps // 4), stream)
+    tf = 2.5 * flops(w) / (ms * 1e-3) / 1e12
+    res["causal8k_d256_backward"] = {"ms": round(ms, 4), "TFLOPS": round(tf, 2),
+                                     "frac_of_bf16_peak": round(tf / pk["bf16"], 4),
+                                     "gpu_launches_per_call": 3}
+    del q, k, v, do, o, l, dq, dk, dv, bws
     w = WORKLOADS["decode"]
     q, kc, vc, lens = kvcache_workload_inputs(w, device=dev)
     ws = torch.empty(fa.fa_fwd_kvcache_workspace_size(w.B, w.Hq, w.Nk, w.d, 0), dtype=torch.uint8,

@@ -181,6 +181,40 @@ fa_status make_map_f32(CUtensorMap *map, void *base, int d, int64_t n, int64_t h
   return FA_OK;
 }
 
+// The transposed fp32 dQ accumulator [b, h, d, nq_pad] of the wide backward kernel: box =
+// 32 queries (128 bytes) x 128 d rows, 128-byte swizzle (the staging layout).
+fa_status make_map_dqt(CUtensorMap *map, void *base, int d, int64_t nq_pad, int64_t h,
+                       int64_t b) {
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(nq_pad), static_cast<cuuint64_t>(d),
+                        static_cast<cuuint64_t>(h), static_cast<cuuint64_t>(b)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(nq_pad) * 4,
+                           static_cast<cuuint64_t>(d * nq_pad) * 4,
+                           static_cast<cuuint64_t>(h * d * nq_pad) * 4};
+  cuuint32_t box[4] = {32, 128, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(g_cuda_msg, sizeof g_cuda_msg, "cuTensorMapEncodeTiled (fp32) failed (CUresult %d)",
+             static_cast<int>(r));
+    return FA_ERR_CUDA;
+  }
+  return FA_OK;
+}
+
+// Backward workspace parts: the fp32 dQ accumulator ([B, Nq, Hq, d]; kernel width 256: the
+// transposed [B, Hq, d, Nq rounded up to 4]) and the deterministic-order counters (per
+// (b, h, 128-query block); width 256: per (b, h, 64-query block, d half)), in elements.
+int64_t bwd_acc_elems(int B, int Nq, int Hq, int d) {
+  return fa::kernel_d(d) == 256 ? static_cast<int64_t>(B) * Hq * d * fa::dq_acc_nq(Nq)
+                                : static_cast<int64_t>(B) * Nq * Hq * d;
+}
+int64_t bwd_sem_elems(int B, int Nq, int Hq, int d) {
+  return fa::kernel_d(d) == 256 ? static_cast<int64_t>(B) * Hq * ((Nq + 63) / 64) * 2
+                                : static_cast<int64_t>(B) * Hq * ((Nq + 127) / 128);
+}
+
 bool stride_ok(int64_t s, int64_t extent) {
   if (extent <= 1) return s >= 0;
   return s > 0 && (s % 8) == 0 && s < (int64_t(1) << 38);
@@ -990,13 +1024,13 @@ fa_status fa_fwd_kvcache_fp8(const void *q, const void *k_cache, const void *v_c
 
 size_t fa_bwd_params_size(void) { return sizeof(fa_bwd_params); }
 
-// Workspace of fa_bwd: fp32 dQ accumulator [B, Nq, Hq, d], D [B, Hq, Nq], and one counter
-// per (batch, query head, 128-row query block), each part 256-byte aligned.
+// Workspace of fa_bwd: the fp32 dQ accumulator, D [B, Hq, Nq], and the counters of the
+// deterministic order (bwd_acc_elems, bwd_sem_elems), each part 256-byte aligned.
 size_t fa_bwd_workspace_size(int B, int Nq, int Hq, int d) {
   if (B <= 0 || Nq <= 0 || Hq <= 0 || d <= 0) return 0;
-  const int64_t acc = static_cast<int64_t>(B) * Nq * Hq * d * 4;
+  const int64_t acc = bwd_acc_elems(B, Nq, Hq, d) * 4;
   const int64_t vec = static_cast<int64_t>(B) * Hq * Nq * 4;
-  const int64_t sem = static_cast<int64_t>(B) * Hq * ((Nq + 127) / 128) * 4;
+  const int64_t sem = bwd_sem_elems(B, Nq, Hq, d) * 4;
   return static_cast<size_t>((acc + 255) / 256 * 256 + (vec + 255) / 256 * 256 +
                              (sem + 255) / 256 * 256);
 }
@@ -1006,7 +1040,7 @@ fa_status fa_bwd(const fa_bwd_params *p, cudaStream_t stream) {
   const fa_bwd_params &a = *p;
   if (a.B < 0 || a.Nq < 0 || a.Nk < 0 || a.Hq <= 0 || a.Hkv <= 0 || a.Hq % a.Hkv != 0)
     return FA_ERR_INVALID_ARG;
-  if (!head_dim_ok(a.d)) return FA_ERR_UNSUPPORTED;
+  if (!head_dim_ok(a.d, kMaxPrefillD)) return FA_ERR_UNSUPPORTED;
   if (!dtype_ok(a.dtype)) return FA_ERR_UNSUPPORTED;
   if (!scale_ok(a.scale)) return FA_ERR_INVALID_ARG;
   if (a.Nq > (1 << 30) || a.Nk > (1 << 30)) return FA_ERR_INVALID_ARG;
@@ -1039,8 +1073,9 @@ fa_status fa_bwd(const fa_bwd_params *p, cudaStream_t stream) {
   ModPlan mod;
   fa_status mst = plan_mod(&a.mod, a.causal, &mod);
   if (mst != FA_OK) return mst;
+  const bool wide = fa::kernel_d(a.d) == 256;  // units per d half, 64-query steps
   const int kblocks = ceil_div(a.Nk, 128);
-  const int64_t units = static_cast<int64_t>(kblocks) * a.B * a.Hkv;
+  const int64_t units = static_cast<int64_t>(kblocks) * a.B * a.Hkv * (wide ? 2 : 1);
   if (units > INT32_MAX) return FA_ERR_INVALID_ARG;
 
   DeviceInfo *dev = nullptr;
@@ -1057,25 +1092,29 @@ fa_status fa_bwd(const fa_bwd_params *p, cudaStream_t stream) {
     return e == cudaSuccess ? FA_OK : cuda_fail("zero kernel launch", e);
   }
   float *dq_acc = static_cast<float *>(a.workspace);
-  const int64_t acc_bytes = (static_cast<int64_t>(a.B) * a.Nq * a.Hq * a.d * 4 + 255) / 256 * 256;
+  const int64_t acc_n = bwd_acc_elems(a.B, a.Nq, a.Hq, a.d);
+  const int64_t acc_bytes = (acc_n * 4 + 255) / 256 * 256;
   float *dvec = reinterpret_cast<float *>(static_cast<char *>(a.workspace) + acc_bytes);
   const int64_t vec_bytes = (static_cast<int64_t>(a.B) * a.Hq * a.Nq * 4 + 255) / 256 * 256;
   int *sem = reinterpret_cast<int *>(static_cast<char *>(a.workspace) + acc_bytes + vec_bytes);
-  const int nsem = a.deterministic ? a.B * a.Hq * ceil_div(a.Nq, 128) : 0;
+  const int nsem = a.deterministic ? static_cast<int>(bwd_sem_elems(a.B, a.Nq, a.Hq, a.d)) : 0;
+  const int nq_pad = fa::dq_acc_nq(a.Nq);
+  const int qrows = wide ? 64 : 128;  // Q / dO box rows: the kernel's query step
   CUtensorMap tq, tk, tv, tdo, tdq;
   if ((st = make_map(&tq, a.q, a.d, a.Nq, a.Hq, a.B, a.q_strides[1], a.q_strides[2],
-                     a.q_strides[0], a.dtype)) != FA_OK ||
+                     a.q_strides[0], a.dtype, qrows)) != FA_OK ||
       (st = make_map(&tdo, a.dout, a.d, a.Nq, a.Hq, a.B, a.do_strides[1], a.do_strides[2],
-                     a.do_strides[0], a.dtype)) != FA_OK ||
+                     a.do_strides[0], a.dtype, qrows)) != FA_OK ||
       (st = make_map(&tk, a.k, a.d, a.Nk, a.Hkv, a.B, a.k_strides[1], a.k_strides[2],
                      a.k_strides[0], a.dtype)) != FA_OK ||
       (st = make_map(&tv, a.v, a.d, a.Nk, a.Hkv, a.B, a.v_strides[1], a.v_strides[2],
                      a.v_strides[0], a.dtype)) != FA_OK ||
-      (st = make_map_f32(&tdq, dq_acc, a.d, a.Nq, a.Hq, a.B)) != FA_OK)
+      (st = wide ? make_map_dqt(&tdq, dq_acc, a.d, nq_pad, a.Hq, a.B)
+                 : make_map_f32(&tdq, dq_acc, a.d, a.Nq, a.Hq, a.B)) != FA_OK)
     return st;
   const bool f16 = a.dtype == FA_FP16;
   e = fa::launch_bwd_pre(a.d, f16, a.o, a.dout, a.B, a.Nq, a.Hq, a.o_strides, a.do_strides, dvec,
-                         dq_acc, sem, nsem, stream);
+                         dq_acc, acc_n, sem, nsem, stream);
   if (e != cudaSuccess) return cuda_fail("backward preprocessing launch", e);
   fa::BwdArgs ba{};
   ba.lse = a.lse;
@@ -1083,7 +1122,7 @@ fa_status fa_bwd(const fa_bwd_params *p, cudaStream_t stream) {
   ba.lse_sb = static_cast<int64_t>(a.Hq) * a.Nq;
   ba.lse_sh = a.Nq;
   ba.varlen = 0;
-  ba.qblocks = ceil_div(a.Nq, 128);
+  ba.qblocks = ceil_div(a.Nq, wide ? 64 : 128);
   ba.dk = a.dk;
   ba.dv = a.dv;
   ba.dk_sb = a.dk_strides[0];
@@ -1111,7 +1150,10 @@ fa_status fa_bwd(const fa_bwd_params *p, cudaStream_t stream) {
   const int grid = static_cast<int>(units < dev->sm_count ? units : dev->sm_count);
   e = fa::launch_bwd(fa::kernel_d(a.d), mod.mask, f16, tq, tk, tv, tdo, tdq, ba, grid, stream);
   if (e != cudaSuccess) return cuda_fail("backward kernel launch", e);
-  e = fa::launch_bwd_post(a.d, f16, dq_acc, a.scale, a.dq, a.B, a.Nq, a.Hq, a.dq_strides, stream);
+  e = wide ? fa::launch_bwd_post_t(a.d, f16, dq_acc, a.scale, a.dq, a.B, a.Nq, nq_pad, a.Hq,
+                                   a.dq_strides, nullptr, 0, stream)
+           : fa::launch_bwd_post(a.d, f16, dq_acc, a.scale, a.dq, a.B, a.Nq, a.Hq, a.dq_strides,
+                                 stream);
   return e == cudaSuccess ? FA_OK : cuda_fail("backward postprocessing launch", e);
 }
 
@@ -1125,7 +1167,7 @@ fa_status fa_bwd_varlen(const void *q, const void *k, const void *v, const void 
   if (B < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || total_q < 0 || total_k < 0 || Hq <= 0 ||
       Hkv <= 0 || Hq % Hkv != 0)
     return FA_ERR_INVALID_ARG;
-  if (!head_dim_ok(d)) return FA_ERR_UNSUPPORTED;
+  if (!head_dim_ok(d, kMaxPrefillD)) return FA_ERR_UNSUPPORTED;
   if (!dtype_ok(dtype)) return FA_ERR_UNSUPPORTED;
   if (!scale_ok(scale)) return FA_ERR_INVALID_ARG;
   if (max_seqlen_q > (1 << 30) || max_seqlen_k > (1 << 30) || total_q > (1 << 30) ||
@@ -1148,8 +1190,9 @@ fa_status fa_bwd_varlen(const void *q, const void *k, const void *v, const void 
   if (q_side && k_side &&
       (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256)))
     return FA_ERR_WORKSPACE;
+  const bool wide = fa::kernel_d(d) == 256;  // units per d half, 64-query steps
   const int kblocks = ceil_div(max_seqlen_k, 128);
-  const int64_t units = static_cast<int64_t>(kblocks) * B * Hkv;
+  const int64_t units = static_cast<int64_t>(kblocks) * B * Hkv * (wide ? 2 : 1);
   if (units > INT32_MAX) return FA_ERR_INVALID_ARG;
   ModPlan mod;
   fa_status st = plan_mod(mod_in, causal, &mod);
@@ -1170,23 +1213,30 @@ fa_status fa_bwd_varlen(const void *q, const void *k, const void *v, const void 
     if (e == cudaSuccess) e = fa::launch_zero16(dv, 1, total_k, Hkv, d, kst, stream);
     return e == cudaSuccess ? FA_OK : cuda_fail("zero kernel launch", e);
   }
+  // dQ accumulator: packed [total_q, Hq, d]; kernel width 256: per sequence, transposed
+  // [B, Hq, d, max_seqlen_q rounded up to 4]
   float *dq_acc = static_cast<float *>(workspace);
-  const int64_t acc_bytes = (static_cast<int64_t>(total_q) * Hq * d * 4 + 255) / 256 * 256;
+  const int nq_pad = fa::dq_acc_nq(max_seqlen_q);
+  const int64_t acc_n = wide ? static_cast<int64_t>(B) * Hq * d * nq_pad
+                             : static_cast<int64_t>(total_q) * Hq * d;
+  const int64_t acc_bytes = (acc_n * 4 + 255) / 256 * 256;
   float *dvec = reinterpret_cast<float *>(static_cast<char *>(workspace) + acc_bytes);
   const int64_t vec_bytes = (static_cast<int64_t>(Hq) * total_q * 4 + 255) / 256 * 256;
   int *sem = reinterpret_cast<int *>(static_cast<char *>(workspace) + acc_bytes + vec_bytes);
-  const int qblocks = ceil_div(max_seqlen_q, 128);
-  const int nsem = deterministic ? B * Hq * qblocks : 0;
+  const int qblocks = ceil_div(max_seqlen_q, wide ? 64 : 128);
+  const int nsem = deterministic ? B * Hq * qblocks * (wide ? 2 : 1) : 0;
+  const int qrows = wide ? 64 : 128;  // Q / dO box rows: the kernel's query step
   CUtensorMap tq, tk, tv, tdo, tdq;
-  if ((st = make_map(&tq, q, d, total_q, Hq, 1, qst[1], d, 0, dtype)) != FA_OK ||
-      (st = make_map(&tdo, dout, d, total_q, Hq, 1, qst[1], d, 0, dtype)) != FA_OK ||
+  if ((st = make_map(&tq, q, d, total_q, Hq, 1, qst[1], d, 0, dtype, qrows)) != FA_OK ||
+      (st = make_map(&tdo, dout, d, total_q, Hq, 1, qst[1], d, 0, dtype, qrows)) != FA_OK ||
       (st = make_map(&tk, k, d, total_k, Hkv, 1, kst[1], d, 0, dtype)) != FA_OK ||
       (st = make_map(&tv, v, d, total_k, Hkv, 1, kst[1], d, 0, dtype)) != FA_OK ||
-      (st = make_map_f32(&tdq, dq_acc, d, total_q, Hq, 1)) != FA_OK)
+      (st = wide ? make_map_dqt(&tdq, dq_acc, d, nq_pad, Hq, B)
+                 : make_map_f32(&tdq, dq_acc, d, total_q, Hq, 1)) != FA_OK)
     return st;
   const bool f16 = dtype == FA_FP16;
-  e = fa::launch_bwd_pre(d, f16, o, dout, 1, total_q, Hq, qst, qst, dvec, dq_acc, sem, nsem,
-                         stream);
+  e = fa::launch_bwd_pre(d, f16, o, dout, 1, total_q, Hq, qst, qst, dvec, dq_acc, acc_n, sem,
+                         nsem, stream);
   if (e != cudaSuccess) return cuda_fail("backward preprocessing launch", e);
   fa::BwdArgs ba{};
   ba.lse = lse;
@@ -1223,7 +1273,9 @@ fa_status fa_bwd_varlen(const void *q, const void *k, const void *v, const void 
   const int grid = static_cast<int>(units < dev->sm_count ? units : dev->sm_count);
   e = fa::launch_bwd(fa::kernel_d(d), mod.mask, f16, tq, tk, tv, tdo, tdq, ba, grid, stream);
   if (e != cudaSuccess) return cuda_fail("backward kernel launch", e);
-  e = fa::launch_bwd_post(d, f16, dq_acc, scale, dq, 1, total_q, Hq, qst, stream);
+  e = wide ? fa::launch_bwd_post_t(d, f16, dq_acc, scale, dq, B, max_seqlen_q, nq_pad, Hq, qst,
+                                   cu_seqlens_q, total_q, stream)
+           : fa::launch_bwd_post(d, f16, dq_acc, scale, dq, 1, total_q, Hq, qst, stream);
   return e == cudaSuccess ? FA_OK : cuda_fail("backward postprocessing launch", e);
 }
 

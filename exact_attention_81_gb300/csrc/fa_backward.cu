@@ -85,9 +85,11 @@ struct BBars {
   uint64_t kv_full, kv_empty, q_full, q_empty, do_full, do_empty, vec_full, vec_empty;
   uint64_t st_full, dp_full, p_ready, dq_full, dq_empty, acc_full, acc_empty, mma_done;
   uint64_t dq_staged, dq_free;  // dQ staging tile written (compute) / read by the TMA (issuer)
+  uint64_t dq_free_r1;          // wide kernel: dq_free for the second staging round of a step
   uint32_t tmem_base;
   int abort;
 };
+static_assert(sizeof(BBars) <= 256, "backward barriers exceed their shared-memory region");
 
 struct BUnit {
   int b, g, j;
@@ -101,7 +103,7 @@ struct BUnit {
   int nit;             // steps: group * (ihi - ilo)
 };
 
-template <int MASK>
+template <int MASK, int QB = BQ>
 __device__ __forceinline__ BUnit bunit_of(const BwdArgs &a, int u) {
   BUnit w;
   // Units run in groups of HEAD_GROUP (batch, kv head) pairs, key-block-major inside a
@@ -138,7 +140,7 @@ __device__ __forceinline__ BUnit bunit_of(const BwdArgs &a, int u) {
     w.tma_b = w.b;
   }
   w.skip = w.j * BKEY >= w.nk;
-  w.nqb = (w.nq + BQ - 1) / BQ;
+  w.nqb = (w.nq + QB - 1) / QB;
   w.ilo = 0;
   w.ihi = w.nqb;
   const long long off = static_cast<long long>(w.nk) - w.nq;
@@ -147,15 +149,15 @@ __device__ __forceinline__ BUnit bunit_of(const BwdArgs &a, int u) {
   const int wl = WIN ? a.wl : -1;
   if (wr >= 0) {
     // first query block holding a row that sees a key of the block:
-    // i*128 + 127 + off + wr >= j*128
-    const long long t = static_cast<long long>(w.j) * BKEY - off - wr - (BQ - 1);
-    w.ilo = t <= 0 ? 0 : static_cast<int>(min((t + BQ - 1) / BQ, static_cast<long long>(w.nqb)));
+    // i*QB + QB-1 + off + wr >= j*128
+    const long long t = static_cast<long long>(w.j) * BKEY - off - wr - (QB - 1);
+    w.ilo = t <= 0 ? 0 : static_cast<int>(min((t + QB - 1) / QB, static_cast<long long>(w.nqb)));
   }
   if (wl >= 0) {
-    // last query block holding a row that sees a key of the block: i*128 + off - wl <= kmax
+    // last query block holding a row that sees a key of the block: i*QB + off - wl <= kmax
     const long long kmax = min(static_cast<long long>(w.j) * BKEY + BKEY - 1, w.nk - 1ll);
     const long long t = kmax - off + wl;
-    w.ihi = t < 0 ? 0 : static_cast<int>(min(t / BQ + 1, static_cast<long long>(w.nqb)));
+    w.ihi = t < 0 ? 0 : static_cast<int>(min(t / QB + 1, static_cast<long long>(w.nqb)));
   }
   if (w.ihi < w.ilo) w.ihi = w.ilo;
   w.nit = w.skip ? 0 : a.group * (w.ihi - w.ilo);
@@ -741,16 +743,605 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 }
 
 // ------------------------------------------------------------------------------------
-// Preprocessing: D = rowsum(dO * O) (one warp per row) and a zeroed dQ accumulator.
+// Head dimensions 136..256: bwd_wide_kernel<MASK, F16> (kernel width 256).
+//
+// dK and dV of 128 keys at d = 256 alone would fill TMEM, and 128-query Q / dO tiles would
+// not fit shared memory next to K and V, so a unit of this kernel is (batch, kv head,
+// 128-key block, d half h) and a step is 64 queries.  Each unit recomputes S^T and dP^T over
+// the full d and accumulates only its half of dK and dV, and adds its half of the d columns
+// of dQ (the two halves of a key block run as adjacent units, so the second reads K, V, Q
+// and dO mostly from L2).  Per step:
+//     S^T  = K Q^T,  dP^T = V dO^T          [128 keys x 64 queries], K-dim 256
+//     dK_h += dS^T Q_h,  dV_h += P^T dO_h    [128 keys x 128], K-dim 64 queries, A from TMEM
+//     dQ^T_h = K_h^T dS^T                    [128 d rows x 64 queries], K-dim 128 keys
+// TMEM: S^T [0,64), dP^T [64,128) (then dS^T, then dQ^T_h), dV_h [128,256), dK_h [256,384).
+// Warpgroup x takes queries [32x, 32x+32) of a step for P^T / dS^T (thread = key row, the
+// packed 16-bit results over the first 16 of the chunk's 32 source columns), and the same
+// 32 query columns of dQ^T_h (thread = d row), which go through one 16 KB staging box
+// (warpgroup 0's round, then warpgroup 1's) to a TMA reduce-add into the transposed fp32
+// accumulator [B, Hq, d, Nq rounded up to 4] at d rows [128h, 128h + 128).
+// Shared memory: K, V 64 KB each (four 128 x 64 boxes), Q, dO 32 KB each (four 64 x 64
+// boxes), dS 16 KB, dQ^T staging 16 KB, vectors and barriers: 226 KB.
+
+constexpr int WQ = 64;                // queries per step of the wide kernel
+constexpr int QBOX = WQ * 128;        // one 64-row box of Q or dO
+constexpr uint32_t W_ST = 0, W_DP = 64, W_DV = 128, W_DK = 256;
+
+struct WCfg {
+  static constexpr int K_OFF = 0;
+  static constexpr int V_OFF = 4 * BOX;
+  static constexpr int Q_OFF = 8 * BOX;
+  static constexpr int DO_OFF = Q_OFF + 4 * QBOX;
+  static constexpr int DS_OFF = DO_OFF + 4 * QBOX;  // dS [128 keys x 64 queries]: one box
+  static constexpr int DQ_OFF = DS_OFF + BOX;       // dQ^T staging: 128 d rows x 32 queries
+  static constexpr int VEC_OFF = DQ_OFF + BOX;      // LSE (log2) [64], D [64]
+  static constexpr int BAR_OFF = VEC_OFF + 2 * WQ * 4;
+  static constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;
+};
+static_assert(WCfg::SMEM_BYTES <= 232448, "wide backward kernel shared memory");
+
+template <bool F16>
+struct WDesc {
+  static constexpr uint32_t S = idesc_bf16_f32(128, WQ, false, false, F16);
+  static constexpr uint32_t ACC = idesc_bf16_f32(128, 128, false, true, F16);
+  static constexpr uint32_t DQT = idesc_bf16_f32(128, WQ, true, true, F16);
+};
+
+// S^T or dP^T [128 keys x 64 queries] = A [128 x 256] B [64 x 256]^T, both K-major: 16 MMAs
+// of 128 x 64 x 16; A's boxes are 16 KB apart, B's 8 KB.
+template <bool F16>
+__device__ __forceinline__ void wide_issue_s(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem) {
+#pragma unroll
+  for (int kk = 0; kk < 16; ++kk) {
+    const uint32_t in_row = static_cast<uint32_t>((kk & 3) * 32);
+    mma_bf16_ss_w(d_tmem, sw128_desc(a_smem + static_cast<uint32_t>((kk >> 2) * BOX) + in_row, 16, 1024),
+                  sw128_desc(b_smem + static_cast<uint32_t>((kk >> 2) * QBOX) + in_row, 16, 1024),
+                  WDesc<F16>::S, kk > 0 ? 1u : 0u);
+  }
+}
+
+// dK_h or dV_h [128 keys x 128] (+)= A [128 keys x 64 queries] (TMEM, packed pairs: queries
+// 0-31 at +0, 32-63 at +32) * B [64 queries x 128] (the d half of Q or dO, MN-major: two
+// 64-column boxes 8 KB apart); 4 MMAs of 128 x 128 x 16.
+template <bool F16>
+__device__ __forceinline__ void wide_issue_acc(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem,
+                                               bool accumulate) {
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk)
+    mma_bf16_ts_w(d_tmem, a_tmem + static_cast<uint32_t>(kk < 2 ? 8 * kk : 32 + 8 * (kk - 2)),
+                  sw128_desc(b_smem + static_cast<uint32_t>(kk * 16 * 128), QBOX, 1024),
+                  WDesc<F16>::ACC, (accumulate || kk > 0) ? 1u : 0u);
+}
+
+// dQ^T_h [128 d rows x 64 queries] = K_h^T [128 x 128 keys] dS^T: A = the d half of K as an
+// MN-major operand (two 64-d boxes 16 KB apart), B = dS (rows = keys, queries contiguous);
+// 8 MMAs of 128 x 64 x 16.
+template <bool F16>
+__device__ __forceinline__ void wide_issue_dqt(uint32_t d_tmem, uint32_t k_smem, uint32_t ds_smem) {
+#pragma unroll
+  for (int kk = 0; kk < BKEY / 16; ++kk) {
+    const uint32_t off = static_cast<uint32_t>(kk * 16 * 128);
+    mma_bf16_ss_w(d_tmem, sw128_desc(k_smem + off, BOX, 1024), sw128_desc(ds_smem + off, BOX, 1024),
+                  WDesc<F16>::DQT, kk > 0 ? 1u : 0u);
+  }
+}
+
+// One 32-query round of dQ^T (fp32 bits) into row r of the staging box, 128-byte swizzled.
+__device__ __forceinline__ void wide_stage_dqt(uint8_t *box, int r, const uint32_t (&v)[32]) {
+  uint8_t *row = box + r * 128;
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    *reinterpret_cast<uint4 *>(row + ((c ^ (r & 7)) << 4)) =
+        make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+}
+
+template <int MASK, bool F16>
+__device__ void wide_producer(const BwdArgs &a, const CUtensorMap *tq, const CUtensorMap *tk,
+                              const CUtensorMap *tv, const CUtensorMap *tdo, uint8_t *smem,
+                              BBars *bars, const WaitCtl &wc, int lane) {
+  using C = WCfg;
+  float *lse2 = reinterpret_cast<float *>(smem + C::VEC_OFF);
+  float *dvec = lse2 + WQ;
+  uint32_t kv_n = 0, q_n = 0, do_n = 0, vec_n = 0;
+  if (a.inject) goto out;  // failure injection: load nothing, the consumers' waits run out
+  for (int u = blockIdx.x; u < a.num_units; u += gridDim.x) {
+    const BUnit w = bunit_of<MASK, WQ>(a, u >> 1);
+    if (w.bad && w.j == 0 && w.g == 0 && (u & 1) == 0 && lane == 0)
+      atomicOr(a.err, DEVERR_BAD_CU_SEQLENS);
+    if (w.nit == 0) continue;
+    if (kv_n > 0 && !warp_wait(&bars->kv_empty, (kv_n - 1) & 1u, wc)) goto out;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&bars->kv_full, 8 * BOX);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        tma_load_4d(smem + C::K_OFF + c * BOX, tk, &bars->kv_full, c * 64, w.g,
+                    w.k_tok + w.j * BKEY, w.tma_b);
+        tma_load_4d(smem + C::V_OFF + c * BOX, tv, &bars->kv_full, c * 64, w.g,
+                    w.k_tok + w.j * BKEY, w.tma_b);
+      }
+    }
+    ++kv_n;
+    for (int t = 0; t < w.nit; ++t) {
+      int h, i;
+      bstep(a, w, t, h, i);
+      if (q_n > 0 && !warp_wait(&bars->q_empty, (q_n - 1) & 1u, wc)) goto out;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars->q_full, 4 * QBOX);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          tma_load_4d(smem + C::Q_OFF + c * QBOX, tq, &bars->q_full, c * 64, h,
+                      w.q_tok + i * WQ, w.tma_b);
+      }
+      ++q_n;
+      if (do_n > 0 && !warp_wait(&bars->do_empty, (do_n - 1) & 1u, wc)) goto out;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars->do_full, 4 * QBOX);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          tma_load_4d(smem + C::DO_OFF + c * QBOX, tdo, &bars->do_full, c * 64, h,
+                      w.q_tok + i * WQ, w.tma_b);
+      }
+      ++do_n;
+      // LSE (log2 domain; rows past the sequence or with no visible key give P = 0) and D.
+      if (vec_n > 0 && !warp_wait(&bars->vec_empty, (vec_n - 1) & 1u, wc)) goto out;
+      const int64_t base = w.b * a.lse_sb + h * a.lse_sh + w.q_tok;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int qi = lane * 2 + e, q = i * WQ + qi;
+        float l2 = INFINITY, dd = 0.f;
+        if (q < w.nq) {
+          const float l = a.lse[base + q];
+          l2 = l == -INFINITY ? INFINITY : l * LOG2E;
+          dd = a.dvec[base + q];
+        }
+        lse2[qi] = l2;
+        dvec[qi] = dd;
+      }
+      __syncwarp();
+      mbar_arrive(&bars->vec_full);
+      ++vec_n;
+    }
+  }
+out:
+  // Teardown: the last bulk copies issued must land before the CTA may exit.
+  if (lane == 0) {
+    if (kv_n > 0) mbar_wait_teardown(&bars->kv_full, (kv_n - 1) & 1u, 1000000000ull);
+    if (q_n > 0) mbar_wait_teardown(&bars->q_full, (q_n - 1) & 1u, 1000000000ull);
+    if (do_n > 0) mbar_wait_teardown(&bars->do_full, (do_n - 1) & 1u, 1000000000ull);
+  }
+}
+
+// dQ issuer of the wide kernel: per step two rounds (warpgroup 0's 32 queries, then
+// warpgroup 1's), each one TMA reduce-add of the staging box (32 queries x 128 d rows).
+// Deterministic order: counters per (batch, head, 64-query block, d half).
+template <int MASK, bool F16>
+__device__ void wide_dq_issuer(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *smem,
+                               BBars *bars, const WaitCtl &wc, int lane) {
+  using C = WCfg;
+  for (int u = blockIdx.x; u < a.num_units; u += gridDim.x) {
+    const BUnit w = bunit_of<MASK, WQ>(a, u >> 1);
+    const int dh = u & 1;
+    if (w.skip || w.nit == 0) continue;
+    const int off = w.nk - w.nq;
+    for (int t = 0; t < w.nit; ++t) {
+      int h, i;
+      bstep(a, w, t, h, i);
+      const int q0 = i * WQ;
+      int *sem = a.sem ? a.sem + ((static_cast<int64_t>(w.b) * a.Hq + h) * a.qblocks + i) * 2 + dh
+                       : nullptr;
+      for (int x = 0; x < 2; ++x) {
+        if (!warp_wait(&bars->dq_staged, static_cast<uint32_t>(x), wc)) return;
+        bool ok = true;
+        if (lane == 0) {
+          if (sem != nullptr && x == 0) {
+            int jmin = 0;
+            if (mask_has_window(MASK) && a.wl >= 0) jmin = max(q0 + off - a.wl, 0) / BKEY;
+            ok = wait_counter(sem, w.j - jmin, wc);
+          }
+          if (ok) {
+            // a round wholly past the sequence's queries adds zeros: skipped
+            if (q0 + 32 * x < w.nq) {
+              tma_reduce_add_4d(tdq, smem + C::DQ_OFF, q0 + 32 * x, 128 * dh, h, w.b);
+              bulk_commit_group();
+            }
+            if (sem != nullptr && x == 1) {
+              bulk_wait_all();             // the step's additions have been performed
+              fence_proxy_async_global();
+              __threadfence();
+              atomicAdd(sem, 1);
+            }
+            bulk_wait_read();              // the staging box may be written again
+            mbar_arrive(x == 0 ? &bars->dq_free : &bars->dq_free_r1);
+          }
+        }
+        if (!__all_sync(0xffffffffu, ok)) return;
+      }
+    }
+  }
+}
+
+template <int MASK, bool F16>
+__device__ void wide_mma(const BwdArgs &a, uint8_t *smem, BBars *bars, uint32_t tmem,
+                         const WaitCtl &wc) {
+  using C = WCfg;
+  const uint32_t sK = smem_u32(smem + C::K_OFF), sV = smem_u32(smem + C::V_OFF);
+  const uint32_t sQ = smem_u32(smem + C::Q_OFF), sDO = smem_u32(smem + C::DO_OFF);
+  const uint32_t sDS = smem_u32(smem + C::DS_OFF);
+  uint32_t kv_n = 0, it = 0, acc_n = 0;
+  for (int u = blockIdx.x; u < a.num_units; u += gridDim.x) {
+    const BUnit w = bunit_of<MASK, WQ>(a, u >> 1);
+    const uint32_t dh = static_cast<uint32_t>(u & 1);
+    if (w.nit == 0) continue;
+    if (!warp_wait(&bars->kv_full, kv_n & 1u, wc)) goto out;
+    ++kv_n;
+    if (acc_n > 0 && !warp_wait(&bars->acc_empty, (acc_n - 1) & 1u, wc)) goto out;
+    for (int t = 0; t < w.nit; ++t) {
+      if (!warp_wait(&bars->q_full, it & 1u, wc)) goto out;
+      tc_fence_after();
+      wide_issue_s<F16>(tmem + W_ST, sK, sQ);                       // S^T = K Q^T
+      mma_commit_w(&bars->st_full);
+      if (!warp_wait(&bars->do_full, it & 1u, wc)) goto out;
+      // dP^T overwrites the previous step's dQ^T: wait until the epilogue has read it.
+      if (it > 0 && !warp_wait(&bars->dq_empty, (it - 1) & 1u, wc)) goto out;
+      tc_fence_after();
+      wide_issue_s<F16>(tmem + W_DP, sV, sDO);                      // dP^T = V dO^T
+      mma_commit_w(&bars->dp_full);
+      if (!warp_wait(&bars->p_ready, it & 1u, wc)) goto out;
+      tc_fence_after();
+      wide_issue_acc<F16>(tmem + W_DK, tmem + W_DP, sQ + 2 * dh * QBOX, t > 0);   // dK_h
+      mma_commit_w(&bars->q_empty);
+      wide_issue_acc<F16>(tmem + W_DV, tmem + W_ST, sDO + 2 * dh * QBOX, t > 0);  // dV_h
+      mma_commit_w(&bars->do_empty);
+      wide_issue_dqt<F16>(tmem + W_DP, sK + 2 * dh * BOX, sDS);                   // dQ^T_h
+      mma_commit_w(&bars->dq_full);
+      ++it;
+    }
+    mma_commit_w(&bars->kv_empty);
+    mma_commit_w(&bars->acc_full);
+    ++acc_n;
+  }
+out:
+  mma_commit_w(&bars->mma_done);
+  mbar_wait_teardown(&bars->mma_done, 0u, 1000000000ull);
+}
+
+// Compute warps of the wide kernel: warpgroup x = warp / 4 takes queries [32x, 32x+32) of
+// every step (P^T, dS^T, and those columns of dQ^T_h) and d columns [64x, 64x+64) of the
+// unit's half of dK / dV; warp w handles TMEM lanes 32 (w % 4) .. +31.
+template <int MASK, bool F16>
+__device__ void wide_compute(const BwdArgs &a, uint8_t *smem, BBars *bars, uint32_t tmem,
+                             const WaitCtl &wc, int tid) {
+  using C = WCfg;
+  const int warp = tid >> 5;
+  const int half = warp >> 2;
+  const int r = (warp & 3) * 32 + (tid & 31);  // TMEM lane: key row, or d row of dQ^T_h
+  const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+  const float *lse2 = reinterpret_cast<const float *>(smem + C::VEC_OFF);
+  const float *dvec = lse2 + WQ;
+  uint8_t *ds_s = smem + C::DS_OFF;
+  uint8_t *stage = smem + C::DQ_OFF;
+  uint32_t it = 0, acc_n = 0;
+  for (int u = blockIdx.x; u < a.num_units; u += gridDim.x) {
+    const BUnit w = bunit_of<MASK, WQ>(a, u >> 1);
+    const int dh = u & 1;
+    if (w.skip) continue;
+    const int off = w.nk - w.nq;  // bottom-right alignment: query q sits at key position q + off
+    const int key = w.j * BKEY + r;
+    const int col0 = 128 * dh + 64 * half;  // this warp's first d column of dK / dV
+    uint16_t *dkrow = reinterpret_cast<uint16_t *>(a.dk) + w.b * a.dk_sb +
+                      (w.k_tok + key) * a.dk_sn + w.g * a.dk_sh + col0;
+    uint16_t *dvrow = reinterpret_cast<uint16_t *>(a.dv) + w.b * a.dv_sb +
+                      (w.k_tok + key) * a.dv_sn + w.g * a.dv_sh + col0;
+    if (w.nit == 0) {  // no query sees these keys: zero gradients
+      if (key < w.nk) {
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          if (col0 + 8 * v >= a.d) break;
+          reinterpret_cast<uint4 *>(dkrow)[v] = make_uint4(0u, 0u, 0u, 0u);
+          reinterpret_cast<uint4 *>(dvrow)[v] = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      continue;
+    }
+    for (int t = 0; t < w.nit; ++t) {
+      int h, i;
+      bstep(a, w, t, h, i);
+      const int q0 = i * WQ;
+      const int qh0 = q0 + 32 * half;  // first query of this warpgroup's chunk
+      const int kb = w.j * BKEY;
+      bool full;  // no pair of the 128 keys x 32 queries masked
+      if constexpr (MASK == MASK_NONE) {
+        full = kb + BKEY <= w.nk;
+      } else if constexpr (MASK == MASK_CAUSAL) {
+        full = kb + BKEY <= w.nk && kb + BKEY - 1 <= qh0 + off;
+      } else {
+        full = kb + BKEY <= w.nk && (a.wr < 0 || kb + BKEY - 1 <= qh0 + off + a.wr) &&
+               (a.wl < 0 || kb >= qh0 + 31 + off - a.wl);
+      }
+      // this key row's visible query positions (modifiers): key - wr - off <= q <= key + wl - off
+      constexpr bool WIN = mask_has_window(MASK);
+      constexpr bool SCORE_MOD = MASK == MASK_MOD || MASK == MASK_ALIBI;
+      const int qv_lo = WIN && a.wr >= 0 ? key - a.wr - off : INT_MIN;
+      const int qv_hi = WIN && a.wl >= 0 ? key + a.wl - off : INT_MAX;
+      const bool softcap = MASK == MASK_MOD && a.sc_out != 0.f;
+      const bool alibi = SCORE_MOD && a.alibi != nullptr;
+      // ALiBi without a softcap on a chunk with no masked pair whose queries all sit at or
+      // after its keys: the bias -slope2 (q + off - key) is linear in the query.
+      const bool alibi_lin = MASK == MASK_ALIBI && full && kb + BKEY - 1 <= qh0 + off;
+      const float slope2 = alibi ? a.alibi[w.b * a.alibi_sb + h] * LOG2E : 0.f;
+      if (!warp_wait(&bars->vec_full, it & 1u, wc)) return;
+      if (!warp_wait(&bars->st_full, it & 1u, wc)) return;
+      if (!warp_wait(&bars->dp_full, it & 1u, wc)) return;
+      tc_fence_after();
+      {
+        const int c2 = half;      // the warpgroup's 32-query chunk of the step
+        const int qc = 32 * half;  // its first query
+        uint32_t sr[32], dr[32];
+        tmem_ld_2x32(tmem + lane_off + W_ST + qc, tmem + lane_off + W_DP + qc, sr, dr);
+        uint32_t pp[16], dd[16];
+        if (MASK == MASK_ALIBI && alibi_lin) {
+          // P = 2^(S c - slope2 (q + off - key) - LSE2): the bias pairs of queries (e, e+1)
+          // and (e+2, e+3) step by -4 slope2 along two chains that start from exact
+          // products; then dS = P (dP - D), all on packed fp32 pairs.
+          const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
+          const float base = -slope2 * static_cast<float>(q0 + qc + off - key);
+          uint64_t w01 = f2_pack(base, base - slope2);
+          uint64_t w23 = f2_pack(base - 2.f * slope2, base - 3.f * slope2);
+          const uint64_t step = f2_pack(-4.f * slope2, -4.f * slope2);
+#pragma unroll
+          for (int e4 = 0; e4 < 32; e4 += 4) {
+            const float4 l4 = *reinterpret_cast<const float4 *>(lse2 + qc + e4);
+            const float4 d4 = *reinterpret_cast<const float4 *>(dvec + qc + e4);
+            float z0, z1, z2, z3, e0, e1, e2, e3;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e4]), __uint_as_float(sr[e4 + 1])), sc2,
+                             f2_add(w01, f2_pack(-l4.x, -l4.y))), z0, z1);
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e4 + 2]), __uint_as_float(sr[e4 + 3])),
+                             sc2, f2_add(w23, f2_pack(-l4.z, -l4.w))), z2, z3);
+            w01 = f2_add(w01, step);
+            w23 = f2_add(w23, step);
+            const float p0 = ex2_approx(z0), p1 = ex2_approx(z1);
+            const float p2 = ex2_approx(z2), p3 = ex2_approx(z3);
+            f2_unpack(f2_mul(f2_pack(p0, p1),
+                             f2_add(f2_pack(__uint_as_float(dr[e4]), __uint_as_float(dr[e4 + 1])),
+                                    f2_pack(-d4.x, -d4.y))), e0, e1);
+            f2_unpack(f2_mul(f2_pack(p2, p3),
+                             f2_add(f2_pack(__uint_as_float(dr[e4 + 2]),
+                                            __uint_as_float(dr[e4 + 3])),
+                                    f2_pack(-d4.z, -d4.w))), e2, e3);
+            pp[e4 / 2] = pack2<F16>(p0, p1);
+            pp[e4 / 2 + 1] = pack2<F16>(p2, p3);
+            dd[e4 / 2] = pack2<F16>(e0, e1);
+            dd[e4 / 2 + 1] = pack2<F16>(e2, e3);
+          }
+        } else if (!SCORE_MOD && full) {
+          // No masked pair and no modifier: P = 2^(S c - LSE2), dS = P (dP - D) on packed
+          // fp32 pairs.
+          const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
+#pragma unroll
+          for (int e4 = 0; e4 < 32; e4 += 4) {
+            const float4 l4 = *reinterpret_cast<const float4 *>(lse2 + qc + e4);
+            const float4 d4 = *reinterpret_cast<const float4 *>(dvec + qc + e4);
+            float z0, z1, z2, z3, e0, e1, e2, e3;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e4]), __uint_as_float(sr[e4 + 1])), sc2,
+                             f2_pack(-l4.x, -l4.y)), z0, z1);
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e4 + 2]), __uint_as_float(sr[e4 + 3])),
+                             sc2, f2_pack(-l4.z, -l4.w)), z2, z3);
+            const float p0 = ex2_approx(z0), p1 = ex2_approx(z1);
+            const float p2 = ex2_approx(z2), p3 = ex2_approx(z3);
+            f2_unpack(f2_mul(f2_pack(p0, p1),
+                             f2_add(f2_pack(__uint_as_float(dr[e4]), __uint_as_float(dr[e4 + 1])),
+                                    f2_pack(-d4.x, -d4.y))), e0, e1);
+            f2_unpack(f2_mul(f2_pack(p2, p3),
+                             f2_add(f2_pack(__uint_as_float(dr[e4 + 2]),
+                                            __uint_as_float(dr[e4 + 3])),
+                                    f2_pack(-d4.z, -d4.w))), e2, e3);
+            pp[e4 / 2] = pack2<F16>(p0, p1);
+            pp[e4 / 2 + 1] = pack2<F16>(p2, p3);
+            dd[e4 / 2] = pack2<F16>(e0, e1);
+            dd[e4 / 2 + 1] = pack2<F16>(e2, e3);
+          }
+        } else {
+#pragma unroll
+        for (int e4 = 0; e4 < 32; e4 += 4) {
+          const float4 l4 = *reinterpret_cast<const float4 *>(lse2 + qc + e4);
+          const float4 d4 = *reinterpret_cast<const float4 *>(dvec + qc + e4);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
+          float p[4], ds[4];
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            const int qi = qc + e4 + x;
+            const float sv = __uint_as_float(sr[e4 + x]);
+            float z2, dz = 1.f;  // score in log2 units and dz/ds
+            if constexpr (SCORE_MOD) {
+              if (softcap) {
+                const float t = tanh_ex2(sv * a.sc_in);
+                z2 = t * a.sc_out;
+                dz = 1.f - t * t;
+              } else {
+                z2 = sv * a.scale_log2;
+              }
+              if (alibi) z2 = fmaf(-slope2, fabsf(static_cast<float>(q0 + qi + off - key)), z2);
+            } else {
+              z2 = sv * a.scale_log2;
+            }
+            bool vis;
+            if constexpr (WIN)
+              vis = full || (key < w.nk && q0 + qi >= qv_lo && q0 + qi <= qv_hi);
+            else
+              vis = full || (key < w.nk && (MASK == MASK_NONE || key <= q0 + qi + off));
+            const float pv = ex2_approx(z2 - lv[x]);
+            p[x] = vis ? pv : 0.f;
+            ds[x] = p[x] * (__uint_as_float(dr[e4 + x]) - dv[x]) * dz;
+          }
+          pp[e4 / 2] = pack2<F16>(p[0], p[1]);
+          pp[e4 / 2 + 1] = pack2<F16>(p[2], p[3]);
+          dd[e4 / 2] = pack2<F16>(ds[0], ds[1]);
+          dd[e4 / 2 + 1] = pack2<F16>(ds[2], ds[3]);
+        }
+        }
+        // packed over the first 16 of the chunk's own 32 fp32 columns
+        tmem_st_x16(tmem + lane_off + W_ST + qc, pp);
+        tmem_st_x16(tmem + lane_off + W_DP + qc, dd);
+        uint8_t *box = ds_s + r * 128;  // [128 keys x 64 queries]: this chunk's 64 bytes
+#pragma unroll
+        for (int gi = 0; gi < 4; ++gi) {
+          const int gran = c2 * 4 + gi;
+          *reinterpret_cast<uint4 *>(box + ((gran ^ (r & 7)) << 4)) =
+              make_uint4(dd[4 * gi], dd[4 * gi + 1], dd[4 * gi + 2], dd[4 * gi + 3]);
+        }
+      }
+      mbar_arrive(&bars->vec_empty);
+      tmem_wait_st();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bars->p_ready);
+      // dQ^T_h epilogue: this warpgroup's 32 query columns (thread = d row) through the
+      // staging box, warpgroup 0 first; the reduce-add is the dQ issuer's.
+      if (!warp_wait(&bars->dq_full, it & 1u, wc)) return;
+      tc_fence_after();
+      uint32_t qv[32];
+      tmem_ld_x32(tmem + lane_off + W_DP + 32 * half, qv);
+      tc_fence_before();
+      mbar_arrive(&bars->dq_empty);
+      // The box is free once the issuer has read the round before this one: warpgroup 0's
+      // round follows the previous step's second round (dq_free_r1, one completion per
+      // step), warpgroup 1's this step's first (dq_free, one per step).  One barrier per
+      // round keeps every wait within one phase of its barrier: warpgroup 1 can reach its
+      // next round before the issuer has read its last one.
+      if (half == 0 ? it > 0 && !warp_wait(&bars->dq_free_r1, (it - 1) & 1u, wc)
+                    : !warp_wait(&bars->dq_free, it & 1u, wc))
+        return;
+      wide_stage_dqt(stage, r, qv);
+      fence_proxy_async_smem();
+      mbar_arrive(&bars->dq_staged);
+      ++it;
+    }
+    // Unit end: dV_h and scale * dK_h of this key row (this warp's 64 d columns) -> global.
+    if (!warp_wait(&bars->acc_full, acc_n & 1u, wc)) return;
+    tc_fence_after();
+#pragma unroll
+    for (int c2 = 0; c2 < 2; ++c2) {
+      const uint32_t cc = static_cast<uint32_t>(64 * half + 32 * c2);
+      uint32_t vr[32], kr[32];
+      tmem_ld_x32(tmem + lane_off + W_DV + cc, vr);
+      tmem_ld_x32(tmem + lane_off + W_DK + cc, kr);
+      if (key < w.nk) {
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          if (col0 + 32 * c2 + 8 * v >= a.d) break;  // columns past d are padding
+          uint4 wv, wk;
+          wv.x = pack2<F16>(__uint_as_float(vr[8 * v + 0]), __uint_as_float(vr[8 * v + 1]));
+          wv.y = pack2<F16>(__uint_as_float(vr[8 * v + 2]), __uint_as_float(vr[8 * v + 3]));
+          wv.z = pack2<F16>(__uint_as_float(vr[8 * v + 4]), __uint_as_float(vr[8 * v + 5]));
+          wv.w = pack2<F16>(__uint_as_float(vr[8 * v + 6]), __uint_as_float(vr[8 * v + 7]));
+          wk.x = pack2<F16>(__uint_as_float(kr[8 * v + 0]) * a.scale, __uint_as_float(kr[8 * v + 1]) * a.scale);
+          wk.y = pack2<F16>(__uint_as_float(kr[8 * v + 2]) * a.scale, __uint_as_float(kr[8 * v + 3]) * a.scale);
+          wk.z = pack2<F16>(__uint_as_float(kr[8 * v + 4]) * a.scale, __uint_as_float(kr[8 * v + 5]) * a.scale);
+          wk.w = pack2<F16>(__uint_as_float(kr[8 * v + 6]) * a.scale, __uint_as_float(kr[8 * v + 7]) * a.scale);
+          reinterpret_cast<uint4 *>(dvrow + 32 * c2)[v] = wv;
+          reinterpret_cast<uint4 *>(dkrow + 32 * c2)[v] = wk;
+        }
+      }
+    }
+    tc_fence_before();
+    mbar_arrive(&bars->acc_empty);
+    ++acc_n;
+  }
+}
+
+template <int MASK, bool F16>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    bwd_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                    const __grid_constant__ CUtensorMap tdq, const BwdArgs a) {
+  using C = WCfg;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  BBars *bars = reinterpret_cast<BBars *>(smem + C::BAR_OFF);
+  const int tid = static_cast<int>(threadIdx.x);
+  const int warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    mbar_init(&bars->kv_full, 1);
+    mbar_init(&bars->kv_empty, 1);
+    mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 1);
+    mbar_init(&bars->do_full, 1);
+    mbar_init(&bars->do_empty, 1);
+    mbar_init(&bars->vec_full, 32);
+    mbar_init(&bars->vec_empty, NCOMPUTE);
+    mbar_init(&bars->st_full, 1);
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->p_ready, NCOMPUTE);
+    mbar_init(&bars->dq_full, 1);
+    mbar_init(&bars->dq_empty, NCOMPUTE);
+    mbar_init(&bars->acc_full, 1);
+    mbar_init(&bars->acc_empty, NCOMPUTE);
+    mbar_init(&bars->mma_done, 1);
+    mbar_init(&bars->dq_staged, NCOMPUTE / 2);
+    mbar_init(&bars->dq_free, 1);
+    mbar_init(&bars->dq_free_r1, 1);
+    bars->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == PRODUCER_WARP && lane == 0) {
+    tma_prefetch_desc(&tq);
+    tma_prefetch_desc(&tk);
+    tma_prefetch_desc(&tv);
+    tma_prefetch_desc(&tdo);
+    tma_prefetch_desc(&tdq);
+  }
+  if (warp == MMA_WARP) {
+    tmem_alloc(&bars->tmem_base, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const WaitCtl wc{&bars->abort, a.err, a.timeout_ns, DEVERR_BWD_TIMEOUT};
+  if (warp < PRODUCER_WARP) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(COMPUTE_REGS));
+    wide_compute<MASK, F16>(a, smem, bars, tmem, wc, tid);
+    __syncwarp();
+    tc_fence_before();
+    named_barrier(1, NTHREADS);
+  } else {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(OTHER_REGS));
+    if (warp == PRODUCER_WARP) {
+      wide_producer<MASK, F16>(a, &tq, &tk, &tv, &tdo, smem, bars, wc, lane);
+    } else if (warp == MMA_WARP) {
+      wide_mma<MASK, F16>(a, smem, bars, tmem, wc);
+    } else if (warp == DQ_WARP) {
+      wide_dq_issuer<MASK, F16>(a, &tdq, smem, bars, wc, lane);
+      if (lane == 0) bulk_wait_all();  // every dQ reduction has landed
+    }
+    __syncwarp();
+    tc_fence_before();
+    named_barrier(1, NTHREADS);
+    if (warp == MMA_WARP) {
+      tc_fence_after();
+      tmem_dealloc(tmem, TMEM_COLS);
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------
+// Preprocessing: D = rowsum(dO * O) (one warp per row), a zeroed dQ accumulator (acc_n
+// floats, a multiple of 4) and zeroed counters.
 
 template <bool F16>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t *o, const uint16_t *dout,
                                                       int B, int Nq, int Hq, int d, int64_t os0,
                                                       int64_t os1, int64_t os2, int64_t ds0,
                                                       int64_t ds1, int64_t ds2, float *dvec,
-                                                      float *dq_acc, int *sem, int nsem) {
+                                                      float *dq_acc, int64_t acc_n, int *sem,
+                                                      int nsem) {
   for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < nsem; t += gridDim.x * blockDim.x)
     sem[t] = 0;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < acc_n / 4;
+       t += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    reinterpret_cast<float4 *>(dq_acc)[t] = make_float4(0.f, 0.f, 0.f, 0.f);
   const int lane = threadIdx.x & 31;
   const int64_t rows = static_cast<int64_t>(B) * Nq * Hq;
   for (int64_t rw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / 32; rw < rows;
@@ -771,9 +1362,6 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t *o, const u
 #pragma unroll
     for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
     if (lane == 0) dvec[(static_cast<int64_t>(b) * Hq + h) * Nq + n] = acc;
-    float *qrow = dq_acc + (bn * Hq + h) * d;
-    for (int c = lane * 4; c < d; c += 128)
-      *reinterpret_cast<float4 *>(qrow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 }
 
@@ -799,6 +1387,42 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const float *acc, float s
     w.z = pack2<F16>(v1.x * scale, v1.y * scale);
     w.w = pack2<F16>(v1.z * scale, v1.w * scale);
     *reinterpret_cast<uint4 *>(dq + b * s0 + n * s1 + h * s2 + c8 * 8) = w;
+  }
+}
+
+// Wide kernel: dQ = scale * the transposed accumulator [B, Hq, d, nq_pad], 8 d columns of
+// one query row per thread (queries fastest across threads: coalesced reads).  Varlen
+// (cu_q non-null): B sequences of at most Nq queries, row n of sequence b is token
+// cu_q[b] + n of the packed dq.
+template <bool F16>
+__global__ void __launch_bounds__(256) bwd_post_t_kernel(const float *acc, float scale,
+                                                         uint16_t *dq, int B, int Nq, int nq_pad,
+                                                         int Hq, int d, int64_t s0, int64_t s1,
+                                                         int64_t s2, const int *cu_q,
+                                                         int total_q) {
+  const int64_t total = static_cast<int64_t>(B) * Hq * (d / 8) * Nq;
+  for (int64_t x = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; x < total;
+       x += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int n = static_cast<int>(x % Nq);
+    int64_t rest = x / Nq;
+    const int c8 = static_cast<int>(rest % (d / 8));
+    rest /= d / 8;
+    const int h = static_cast<int>(rest % Hq);
+    const int b = static_cast<int>(rest / Hq);
+    int64_t row = n, bo = b;
+    if (cu_q != nullptr) {
+      const int q0 = cu_q[b], q1 = cu_q[b + 1];
+      if (q0 < 0 || q1 < q0 || q1 > total_q || n >= q1 - q0) continue;
+      row = q0 + n;
+      bo = 0;
+    }
+    const float *src = acc + ((static_cast<int64_t>(b) * Hq + h) * d + 8 * c8) * nq_pad + n;
+    uint4 w;
+    w.x = pack2<F16>(src[0] * scale, src[nq_pad] * scale);
+    w.y = pack2<F16>(src[2 * nq_pad] * scale, src[3 * nq_pad] * scale);
+    w.z = pack2<F16>(src[4 * nq_pad] * scale, src[5 * nq_pad] * scale);
+    w.w = pack2<F16>(src[6 * nq_pad] * scale, src[7 * nq_pad] * scale);
+    *reinterpret_cast<uint4 *>(dq + bo * s0 + row * s1 + h * s2 + c8 * 8) = w;
   }
 }
 
@@ -835,6 +1459,34 @@ cudaError_t launch_bwd_impl(const CUtensorMap &tq, const CUtensorMap &tk, const 
   return cudaGetLastError();
 }
 
+template <int MASK, bool F16>
+cudaError_t launch_wide_impl(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                             const CUtensorMap &tdo, const CUtensorMap &tdq, const BwdArgs &a,
+                             int grid, cudaStream_t stream) {
+  constexpr int smem = WCfg::SMEM_BYTES;
+  cudaError_t e = cudaFuncSetAttribute(bwd_wide_kernel<MASK, F16>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  bwd_wide_kernel<MASK, F16><<<grid, NTHREADS, smem, stream>>>(tq, tk, tv, tdo, tdq, a);
+  return cudaGetLastError();
+}
+
+template <bool F16>
+cudaError_t launch_wide(int mask, const CUtensorMap &tq, const CUtensorMap &tk,
+                        const CUtensorMap &tv, const CUtensorMap &tdo, const CUtensorMap &tdq,
+                        const BwdArgs &a, int grid, cudaStream_t stream) {
+  switch (mask) {
+    case MASK_NONE: return launch_wide_impl<MASK_NONE, F16>(tq, tk, tv, tdo, tdq, a, grid, stream);
+    case MASK_CAUSAL:
+      return launch_wide_impl<MASK_CAUSAL, F16>(tq, tk, tv, tdo, tdq, a, grid, stream);
+    case MASK_WINDOW:
+      return launch_wide_impl<MASK_WINDOW, F16>(tq, tk, tv, tdo, tdq, a, grid, stream);
+    case MASK_ALIBI:
+      return launch_wide_impl<MASK_ALIBI, F16>(tq, tk, tv, tdo, tdq, a, grid, stream);
+    default: return launch_wide_impl<MASK_MOD, F16>(tq, tk, tv, tdo, tdq, a, grid, stream);
+  }
+}
+
 template <int D, bool F16>
 cudaError_t launch_bwd_d(int mask, const CUtensorMap &tq, const CUtensorMap &tk,
                          const CUtensorMap &tv, const CUtensorMap &tdo, const CUtensorMap &tdq,
@@ -856,6 +1508,9 @@ cudaError_t launch_bwd_d(int mask, const CUtensorMap &tq, const CUtensorMap &tk,
 cudaError_t launch_bwd(int d, int mask, bool f16, const CUtensorMap &tq, const CUtensorMap &tk,
                        const CUtensorMap &tv, const CUtensorMap &tdo, const CUtensorMap &tdq,
                        const BwdArgs &a, int grid, cudaStream_t stream) {
+  if (d == 256)
+    return f16 ? launch_wide<true>(mask, tq, tk, tv, tdo, tdq, a, grid, stream)
+               : launch_wide<false>(mask, tq, tk, tv, tdo, tdq, a, grid, stream);
   if (d == 64)
     return f16 ? launch_bwd_d<64, true>(mask, tq, tk, tv, tdo, tdq, a, grid, stream)
                : launch_bwd_d<64, false>(mask, tq, tk, tv, tdo, tdq, a, grid, stream);
@@ -865,15 +1520,16 @@ cudaError_t launch_bwd(int d, int mask, bool f16, const CUtensorMap &tq, const C
 
 cudaError_t launch_bwd_pre(int d, bool f16, const void *o, const void *dout, int B, int Nq,
                            int Hq, const int64_t o_st[3], const int64_t do_st[3], float *dvec,
-                           float *dq_acc, int *sem, int nsem, cudaStream_t stream) {
+                           float *dq_acc, int64_t acc_n, int *sem, int nsem, cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(B) * Nq * Hq;
-  if (rows == 0) return cudaSuccess;
-  const int grid = grid_for(rows * 32, 256);
+  if (rows == 0 && acc_n == 0) return cudaSuccess;
+  const int64_t items = rows * 32 > acc_n / 4 ? rows * 32 : acc_n / 4;
+  const int grid = grid_for(items > nsem ? items : nsem, 256);
   const uint16_t *op = reinterpret_cast<const uint16_t *>(o);
   const uint16_t *dp = reinterpret_cast<const uint16_t *>(dout);
   auto kern = f16 ? bwd_pre_kernel<true> : bwd_pre_kernel<false>;
   kern<<<grid, 256, 0, stream>>>(op, dp, B, Nq, Hq, d, o_st[0], o_st[1], o_st[2], do_st[0],
-                                 do_st[1], do_st[2], dvec, dq_acc, sem, nsem);
+                                 do_st[1], do_st[2], dvec, dq_acc, acc_n, sem, nsem);
   return cudaGetLastError();
 }
 
@@ -890,6 +1546,21 @@ cudaError_t launch_bwd_post(int d, bool f16, const float *dq_acc, float scale, v
     bwd_post_kernel<false><<<grid_for(items, 256), 256, 0, stream>>>(dq_acc, scale, out, B, Nq,
                                                                      Hq, d, dq_st[0], dq_st[1],
                                                                      dq_st[2]);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_post_t(int d, bool f16, const float *dq_acc, float scale, void *dq, int B,
+                              int Nq, int nq_pad, int Hq, const int64_t dq_st[3],
+                              const int *cu_q, int total_q, cudaStream_t stream) {
+  const int64_t items = static_cast<int64_t>(B) * Nq * Hq * (d / 8);
+  if (items == 0) return cudaSuccess;
+  uint16_t *out = reinterpret_cast<uint16_t *>(dq);
+  if (f16)
+    bwd_post_t_kernel<true><<<grid_for(items, 256), 256, 0, stream>>>(
+        dq_acc, scale, out, B, Nq, nq_pad, Hq, d, dq_st[0], dq_st[1], dq_st[2], cu_q, total_q);
+  else
+    bwd_post_t_kernel<false><<<grid_for(items, 256), 256, 0, stream>>>(
+        dq_acc, scale, out, B, Nq, nq_pad, Hq, d, dq_st[0], dq_st[1], dq_st[2], cu_q, total_q);
   return cudaGetLastError();
 }
 

@@ -219,13 +219,18 @@ struct BwdArgs {
   int inject;                 // failure injection: the producer issues no load at all
 };
 
-// D = rowsum(dO * O) per query row and a zeroed fp32 dQ accumulator [B, Nq, Hq, d].
+// D = rowsum(dO * O) per query row, a zeroed fp32 dQ accumulator of acc_n floats (a
+// multiple of 4) and nsem zeroed counters.
 cudaError_t launch_bwd_pre(int d, bool f16, const void *o, const void *dout, int B, int Nq,
                            int Hq, const int64_t o_st[3], const int64_t do_st[3], float *dvec,
-                           float *dq_acc, int *sem, int nsem, cudaStream_t stream);
+                           float *dq_acc, int64_t acc_n, int *sem, int nsem, cudaStream_t stream);
 
 // tq, tk, tv, tdo: 16-bit maps like the forward's; tdq: fp32 map of the dQ accumulator
-// (box 32 x 128 rows, 128-byte swizzle).
+// (box 32 x 128 rows, 128-byte swizzle).  Kernel width d = 256 (head dimensions 136..256):
+// the wide kernel, whose units are (batch, kv head, key block, d half) and steps 64 queries
+// (num_units = 2 x kblocks x B x Hkv, qblocks = ceil(Nq / 64), counters per (b, h, 64-query
+// block, d half)); tq and tdo with 64-row boxes, tdq the transposed accumulator
+// [B, Hq, d, nq_pad] (box 32 queries x 128 d rows).
 cudaError_t launch_bwd(int d, int mask, bool f16, const CUtensorMap &tq, const CUtensorMap &tk,
                        const CUtensorMap &tv, const CUtensorMap &tdo, const CUtensorMap &tdq,
                        const BwdArgs &a, int grid, cudaStream_t stream);
@@ -233,6 +238,17 @@ cudaError_t launch_bwd(int d, int mask, bool f16, const CUtensorMap &tq, const C
 // dQ = scale * accumulator, rounded to the element type, into a strided [B, Nq, Hq, d].
 cudaError_t launch_bwd_post(int d, bool f16, const float *dq_acc, float scale, void *dq, int B,
                             int Nq, int Hq, const int64_t dq_st[3], cudaStream_t stream);
+
+// The wide kernel's dQ: scale * the transposed accumulator [B, Hq, d, nq_pad] into a strided
+// [B, Nq, Hq, d]; varlen (cu_q non-null): B sequences of at most Nq queries into the packed
+// [total_q, Hq, d] (strides dq_st[1], dq_st[2]).
+cudaError_t launch_bwd_post_t(int d, bool f16, const float *dq_acc, float scale, void *dq, int B,
+                              int Nq, int nq_pad, int Hq, const int64_t dq_st[3],
+                              const int *cu_q, int total_q, cudaStream_t stream);
+
+// Query extent of the wide kernel's transposed dQ accumulator: Nq rounded up to 4 (16-byte
+// rows).
+inline int dq_acc_nq(int nq) { return (nq + 3) / 4 * 4; }
 
 // Zeroes a strided 16-bit [B, N, H, d] tensor.
 cudaError_t launch_zero16(void *x, int B, int N, int H, int d, const int64_t st[3],

@@ -332,6 +332,9 @@ fa_status fa_fwd_kvcache_noalloc(const void *q, const void *k_cache, const void 
  * (GQA: dK and dV of a key/value head sum over the query heads that read it).
  *   q, o, dout, dq : [B, Nq, Hq, d] (strides as in fa_fwd_params)
  *   k, v, dk, dv   : [B, Nk, Hkv, d]
+ *   d              : a multiple of 8 from 8 to 256 (above 128 the work of a key block runs
+ *                    as two units, one per half of d, over 64-query steps, with the dQ
+ *                    accumulator stored transposed; fa_bwd_workspace_size accounts for it)
  *   lse            : [B, Hq, Nq] fp32, the LSE fa_fwd wrote for the same q, k, v
  *   workspace      : DEVICE, fa_bwd_workspace_size(B, Nq, Hq, d) bytes, 256-byte aligned,
  *                    owned by the caller (the fp32 dQ accumulator, the D vector and the

@@ -54,7 +54,7 @@ def _bwd_params(**kw):
 
 
 @pytest.mark.parametrize("change,status", [
-    ({"d": 100}, 2), ({"d": 136}, 2), ({"dtype": 3}, 2), ({"Hkv": 3}, 1), ({"scale": 0.0}, 1),
+    ({"d": 100}, 2), ({"d": 264}, 2), ({"dtype": 3}, 2), ({"Hkv": 3}, 1), ({"scale": 0.0}, 1),
     ({"dout": None}, 1),
     ({"lse": None}, 1), ({"dk": 4100}, 1), ({"workspace": None}, 4), ({"workspace_bytes": 16}, 4),
     ({"workspace": 4096 + 64}, 4), ({"B": 0}, 0),
@@ -67,6 +67,10 @@ def test_bwd_workspace_size(lib):
     ws = lib.fa_bwd_workspace_size
     assert ws(2, 1000, 4, 128) == (2 * 1000 * 4 * 128 * 4 + ((2 * 4 * 1000 * 4 + 255) // 256) * 256
                                    + 256)  # 2 x 4 x 8 block counters
+    # width 256 (d 136..256): the transposed accumulator [B, Hq, d, Nq rounded up to 4] and
+    # counters per (b, h, 64-query block, d half)
+    assert ws(2, 1001, 4, 256) == (2 * 4 * 256 * 1004 * 4 + ((2 * 4 * 1001 * 4 + 255) // 256) * 256
+                                   + 1024)  # 2 x 4 x 16 x 2 counters
     assert ws(0, 10, 4, 128) == 0
 
 

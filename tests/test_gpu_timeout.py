@@ -62,10 +62,11 @@ def test_decode_wait_timeout_reports_and_recovers():
     assert torch.equal(o2, o_ok) and torch.equal(l2, l_ok)
 
 
+@pytest.mark.parametrize("d", [128, 256])  # 256: the wide kernel (units per d half)
 @pytest.mark.parametrize("causal", [False, True])
-def test_backward_wait_timeout_reports_and_recovers(causal):
-    q, k, v = dense_inputs(2, 700, 700, 4, 2, 128, seed=73, device=DEV)
-    do = bf16_normal((2, 700, 4, 128), seed=74, device=DEV)
+def test_backward_wait_timeout_reports_and_recovers(causal, d):
+    q, k, v = dense_inputs(2, 700, 700, 4, 2, d, seed=73, device=DEV)
+    do = bf16_normal((2, 700, 4, d), seed=74, device=DEV)
     o, lse = fa_fwd(q, k, v, causal=causal)
     g_ok = fa_bwd(q, k, v, o, lse, do, causal=causal)
     assert get_last_device_error() == FA_OK
