@@ -58,6 +58,12 @@ constexpr int PRODUCER_WARP = 8;
 constexpr int DQ_WARP = 10;       // issues the dQ reduce-adds
 constexpr int MMA_WARP = 9;
 constexpr int HEAD_GROUP = 8;     // (batch, kv head) pairs per unit group
+// The d <= 128 kernel (bwd_kernel): 16 compute warps, four per TMEM lane quarter (warp w:
+// lanes 32 (w % 4) .. +31, queries 32 (w / 4) .. +31 of a step), 640 threads, no register
+// split; warp 16 is the producer, 17 the MMA issuer, 18 the dQ issuer, 19 idle.
+constexpr int NB_THREADS = 640;
+constexpr int NB_COMPUTE = 512;
+constexpr int NB_PRODUCER = 16, NB_MMA = 17, NB_DQ = 18;
 constexpr int BOX = 128 * 128;    // one 128-byte-swizzled box: 128 rows x 128 bytes
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t T_ST = 0, T_DP = 128, T_DV = 256, T_DK = 384;
@@ -207,10 +213,32 @@ __device__ __forceinline__ void issue_kmajor(uint32_t d_tmem, uint32_t a_smem, u
   }
 }
 
-// TMEM column of the packed pair holding queries (2c, 2c+1): each 64-query half sits at the
-// start of its own 64 fp32 source columns.
+// TMEM column of the packed pair holding queries (2c, 2c+1): each 32-query quarter of a step
+// sits at the start of its own 32 fp32 source columns.
 __host__ __device__ constexpr uint32_t packed_col(int query) {
-  return static_cast<uint32_t>((query < 64 ? 0 : 64) + (query & 63) / 2);
+  return static_cast<uint32_t>(32 * (query >> 5) + (query & 31) / 2);
+}
+
+// Two 32 lanes x 16-column TMEM loads completed by a single wait.
+__device__ __forceinline__ void tmem_ld_2x16(uint32_t taddr0, uint32_t taddr1, uint32_t (&r0)[16],
+                                             uint32_t (&r1)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%32];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%33];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r0[0]), "=r"(r0[1]), "=r"(r0[2]), "=r"(r0[3]), "=r"(r0[4]), "=r"(r0[5]), "=r"(r0[6]), "=r"(r0[7]), "=r"(r0[8]), "=r"(r0[9]), "=r"(r0[10]), "=r"(r0[11]), "=r"(r0[12]), "=r"(r0[13]), "=r"(r0[14]), "=r"(r0[15]),
+        "=r"(r1[0]), "=r"(r1[1]), "=r"(r1[2]), "=r"(r1[3]), "=r"(r1[4]), "=r"(r1[5]), "=r"(r1[6]), "=r"(r1[7]), "=r"(r1[8]), "=r"(r1[9]), "=r"(r1[10]), "=r"(r1[11]), "=r"(r1[12]), "=r"(r1[13]), "=r"(r1[14]), "=r"(r1[15])
+      : "r"(taddr0), "r"(taddr1)
+      : "memory");
+}
+
+// Stores 8 consecutive 32-bit TMEM columns of the thread's lane (no wait).
+__device__ __forceinline__ void tmem_st_x8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};\n"
+      :
+      : "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+      : "memory");
 }
 
 // D[128 keys x D] (+)= A[128 keys x 128 queries] (TMEM, packed pairs) * B[128 queries x D]
@@ -419,15 +447,17 @@ out:
 }
 
 // ------------------------------------------------------------------------------------
-// Compute warps: warp w handles TMEM lanes 32 (w % 4) .. +31 and column half w / 4.
+// Compute warps: warp w handles TMEM lanes 32 (w % 4) .. +31, queries 32 (w / 4) .. +31 of a
+// step for P^T / dS^T, and d columns (w / 4) D/4 .. +D/4 in the dQ, dK and dV epilogues.
 
 template <int D, int MASK, bool F16>
 __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *smem, BBars *bars,
                             uint32_t tmem, const WaitCtl &wc, int tid) {
   using C = BCfg<D, F16>;
   const int warp = tid >> 5;
-  const int half = warp >> 2;                 // query half (P, dS) / d half (dQ, dK, dV)
+  const int qd = warp >> 2;                   // query quarter (P, dS) / d quarter (dQ, dK, dV)
   const int r = (warp & 3) * 32 + (tid & 31); // TMEM lane: key row, or query row for dQ
+  constexpr int DW = D / 4;                   // d columns of a warp in the dQ, dK, dV epilogues
   const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
   const float *lse2 = reinterpret_cast<const float *>(smem + C::VEC_OFF);
   const float *dvec = lse2 + BQ;
@@ -446,7 +476,7 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
     if (w.nit == 0) {  // no query sees these keys: zero gradients
       if (key < w.nk) {
 #pragma unroll
-        for (int v = half * (D / 16); v < (half + 1) * (D / 16); ++v) {
+        for (int v = qd * (DW / 8); v < (qd + 1) * (DW / 8); ++v) {
           if (8 * v >= a.d) break;
           reinterpret_cast<uint4 *>(dkrow)[v] = make_uint4(0u, 0u, 0u, 0u);
           reinterpret_cast<uint4 *>(dvrow)[v] = make_uint4(0u, 0u, 0u, 0u);
@@ -479,8 +509,8 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
       // after its keys: the bias -slope2 (q + off - key) is linear in the query.
       const bool alibi_lin = MASK == MASK_ALIBI && full && kb + BKEY - 1 <= q0 + off;
       const float slope2 = alibi ? a.alibi[w.b * a.alibi_sb + h] * LOG2E : 0.f;
-      // P^T and dS^T = P^T (dP^T - D) of this key row for the 64 queries of this half,
-      // 32 at a time: P^T and dS^T to TMEM (dV, dK), dS to shared memory with queries
+      // P^T and dS^T = P^T (dP^T - D) of this key row for the 32 queries of this quarter,
+      // 16 at a time: P^T and dS^T to TMEM (dV, dK), dS to shared memory with queries
       // contiguous (dQ).
       if (!warp_wait(&bars->vec_full, it & 1u, wc)) return;
       if (!warp_wait(&bars->st_full, it & 1u, wc)) return;
@@ -488,10 +518,10 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
       tc_fence_after();
 #pragma unroll 1
       for (int c2 = 0; c2 < 2; ++c2) {
-        const int qc = half * 64 + c2 * 32;  // first query of the chunk
-        uint32_t sr[32], dr[32];
-        tmem_ld_2x32(tmem + lane_off + T_ST + qc, tmem + lane_off + T_DP + qc, sr, dr);
-        uint32_t pp[16], dd[16];
+        const int qc = qd * 32 + c2 * 16;  // first query of the chunk
+        uint32_t sr[16], dr[16];
+        tmem_ld_2x16(tmem + lane_off + T_ST + qc, tmem + lane_off + T_DP + qc, sr, dr);
+        uint32_t pp[8], dd[8];
         if (MASK == MASK_ALIBI && alibi_lin) {
           // P = 2^(S c - slope2 (q + off - key) - LSE2): the bias pairs of queries (e, e+1)
           // and (e+2, e+3) step by -4 slope2 along two chains that start from exact
@@ -502,7 +532,7 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
           uint64_t w23 = f2_pack(base - 2.f * slope2, base - 3.f * slope2);
           const uint64_t step = f2_pack(-4.f * slope2, -4.f * slope2);
 #pragma unroll
-          for (int e4 = 0; e4 < 32; e4 += 4) {
+          for (int e4 = 0; e4 < 16; e4 += 4) {
             const float4 l4 = *reinterpret_cast<const float4 *>(lse2 + qc + e4);
             const float4 d4 = *reinterpret_cast<const float4 *>(dvec + qc + e4);
             float z0, z1, z2, z3, e0, e1, e2, e3;
@@ -531,7 +561,7 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
           // fp32 pairs.
           const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
 #pragma unroll
-          for (int e4 = 0; e4 < 32; e4 += 4) {
+          for (int e4 = 0; e4 < 16; e4 += 4) {
             const float4 l4 = *reinterpret_cast<const float4 *>(lse2 + qc + e4);
             const float4 d4 = *reinterpret_cast<const float4 *>(dvec + qc + e4);
             float z0, z1, z2, z3, e0, e1, e2, e3;
@@ -555,7 +585,7 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
           }
         } else {
 #pragma unroll
-        for (int e4 = 0; e4 < 32; e4 += 4) {
+        for (int e4 = 0; e4 < 16; e4 += 4) {
           const float4 l4 = *reinterpret_cast<const float4 *>(lse2 + qc + e4);
           const float4 d4 = *reinterpret_cast<const float4 *>(dvec + qc + e4);
           const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
@@ -592,12 +622,12 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
           dd[e4 / 2 + 1] = pack2<F16>(ds[2], ds[3]);
         }
         }
-        tmem_st_x16(tmem + lane_off + T_ST + packed_col(qc), pp);
-        tmem_st_x16(tmem + lane_off + T_DP + packed_col(qc), dd);
-        uint8_t *box = ds_s + half * BOX + r * 128;  // box = query half
+        tmem_st_x8(tmem + lane_off + T_ST + packed_col(qc), pp);
+        tmem_st_x8(tmem + lane_off + T_DP + packed_col(qc), dd);
+        uint8_t *box = ds_s + (qc >> 6) * BOX + r * 128;  // box = query half
 #pragma unroll
-        for (int gi = 0; gi < 4; ++gi) {
-          const int gran = c2 * 4 + gi;
+        for (int gi = 0; gi < 2; ++gi) {
+          const int gran = ((qc & 63) >> 3) + gi;
           *reinterpret_cast<uint4 *>(box + ((gran ^ (r & 7)) << 4)) =
               make_uint4(dd[4 * gi], dd[4 * gi + 1], dd[4 * gi + 2], dd[4 * gi + 3]);
         }
@@ -613,16 +643,21 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
       tc_fence_after();
       // The issuer's previous reduction has read the staging tile.
       if (it > 0 && !warp_wait(&bars->dq_free, (it - 1) & 1u, wc)) return;
+      {
+        // this warp's DW columns of dQ: one 32-column box (D = 128) or half of one (D = 64)
+        uint32_t qr[DW];
+        if constexpr (DW == 32)
+          tmem_ld_x32(tmem + lane_off + T_DP + qd * DW, qr);
+        else
+          tmem_ld_x16(tmem + lane_off + T_DP + qd * DW, qr);
+        const int c0 = qd * DW;  // first dQ column
+        uint8_t *box = dq_s + (c0 >> 5) * BOX + r * 128;
 #pragma unroll
-      for (int c2 = 0; c2 < D / 64; ++c2) {
-        const int cc = half * (D / 64) + c2;  // 32-column box of dQ
-        uint32_t qr[32];
-        tmem_ld_x32(tmem + lane_off + T_DP + cc * 32, qr);
-        uint8_t *box = dq_s + cc * BOX + r * 128;
-#pragma unroll
-        for (int gran = 0; gran < 8; ++gran)
+        for (int gi = 0; gi < DW / 4; ++gi) {
+          const int gran = ((c0 & 31) >> 2) + gi;
           *reinterpret_cast<uint4 *>(box + ((gran ^ (r & 7)) << 4)) =
-              make_uint4(qr[4 * gran], qr[4 * gran + 1], qr[4 * gran + 2], qr[4 * gran + 3]);
+              make_uint4(qr[4 * gi], qr[4 * gi + 1], qr[4 * gi + 2], qr[4 * gi + 3]);
+        }
       }
       tc_fence_before();
       mbar_arrive(&bars->dq_empty);
@@ -630,19 +665,23 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
       mbar_arrive(&bars->dq_staged);
       ++it;
     }
-    // Unit end: dV and scale * dK of this key row (this warp's half of d) -> global memory.
+    // Unit end: dV and scale * dK of this key row (this warp's DW columns of d) -> global.
     if (!warp_wait(&bars->acc_full, acc_n & 1u, wc)) return;
     tc_fence_after();
-#pragma unroll
-    for (int c2 = 0; c2 < D / 64; ++c2) {
-      const int cc = half * (D / 64) + c2;
-      uint32_t vr[32], kr[32];
-      tmem_ld_x32(tmem + lane_off + T_DV + cc * 32, vr);
-      tmem_ld_x32(tmem + lane_off + T_DK + cc * 32, kr);
+    {
+      const int cc = qd * DW;  // first d column
+      uint32_t vr[DW], kr[DW];
+      if constexpr (DW == 32) {
+        tmem_ld_x32(tmem + lane_off + T_DV + cc, vr);
+        tmem_ld_x32(tmem + lane_off + T_DK + cc, kr);
+      } else {
+        tmem_ld_x16(tmem + lane_off + T_DV + cc, vr);
+        tmem_ld_x16(tmem + lane_off + T_DK + cc, kr);
+      }
       if (key < w.nk) {
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          if (cc * 32 + 8 * v >= a.d) break;  // columns past d are padding
+        for (int v = 0; v < DW / 8; ++v) {
+          if (cc + 8 * v >= a.d) break;  // columns past d are padding
           uint4 wv, wk;
           wv.x = pack2<F16>(__uint_as_float(vr[8 * v + 0]), __uint_as_float(vr[8 * v + 1]));
           wv.y = pack2<F16>(__uint_as_float(vr[8 * v + 2]), __uint_as_float(vr[8 * v + 3]));
@@ -652,8 +691,8 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
           wk.y = pack2<F16>(__uint_as_float(kr[8 * v + 2]) * a.scale, __uint_as_float(kr[8 * v + 3]) * a.scale);
           wk.z = pack2<F16>(__uint_as_float(kr[8 * v + 4]) * a.scale, __uint_as_float(kr[8 * v + 5]) * a.scale);
           wk.w = pack2<F16>(__uint_as_float(kr[8 * v + 6]) * a.scale, __uint_as_float(kr[8 * v + 7]) * a.scale);
-          reinterpret_cast<uint4 *>(dvrow + cc * 32)[v] = wv;
-          reinterpret_cast<uint4 *>(dkrow + cc * 32)[v] = wk;
+          reinterpret_cast<uint4 *>(dvrow + cc)[v] = wv;
+          reinterpret_cast<uint4 *>(dkrow + cc)[v] = wk;
         }
       }
     }
@@ -664,7 +703,7 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
 }
 
 template <int D, int MASK, bool F16>
-__global__ void __launch_bounds__(NTHREADS, 1)
+__global__ void __launch_bounds__(NB_THREADS, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                const __grid_constant__ CUtensorMap tdq, const BwdArgs a) {
@@ -683,28 +722,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     mbar_init(&bars->do_full, 1);
     mbar_init(&bars->do_empty, 1);
     mbar_init(&bars->vec_full, 32);
-    mbar_init(&bars->vec_empty, NCOMPUTE);
+    mbar_init(&bars->vec_empty, NB_COMPUTE);
     mbar_init(&bars->st_full, 1);
     mbar_init(&bars->dp_full, 1);
-    mbar_init(&bars->p_ready, NCOMPUTE);
+    mbar_init(&bars->p_ready, NB_COMPUTE);
     mbar_init(&bars->dq_full, 1);
-    mbar_init(&bars->dq_empty, NCOMPUTE);
+    mbar_init(&bars->dq_empty, NB_COMPUTE);
     mbar_init(&bars->acc_full, 1);
-    mbar_init(&bars->acc_empty, NCOMPUTE);
+    mbar_init(&bars->acc_empty, NB_COMPUTE);
     mbar_init(&bars->mma_done, 1);
-    mbar_init(&bars->dq_staged, NCOMPUTE);
+    mbar_init(&bars->dq_staged, NB_COMPUTE);
     mbar_init(&bars->dq_free, 1);
     bars->abort = 0;
     fence_barrier_init();
   }
-  if (warp == PRODUCER_WARP && lane == 0) {
+  if (warp == NB_PRODUCER && lane == 0) {
     tma_prefetch_desc(&tq);
     tma_prefetch_desc(&tk);
     tma_prefetch_desc(&tv);
     tma_prefetch_desc(&tdo);
     tma_prefetch_desc(&tdq);
   }
-  if (warp == MMA_WARP) {
+  if (warp == NB_MMA) {
     tmem_alloc(&bars->tmem_base, TMEM_COLS);
     tmem_relinquish();
   }
@@ -713,32 +752,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
   const WaitCtl wc{&bars->abort, a.err, a.timeout_ns, DEVERR_BWD_TIMEOUT};
-  // Each register-split branch ends on its own; the two meet at a named barrier before
-  // TMEM is released.
-  if (warp < PRODUCER_WARP) {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(COMPUTE_REGS));
+  // Every role ends on its own; all meet at a named barrier before TMEM is released.
+  if (warp < NB_PRODUCER) {
     bwd_compute<D, MASK, F16>(a, &tdq, smem, bars, tmem, wc, tid);
-
-    __syncwarp();
-    tc_fence_before();
-    named_barrier(1, NTHREADS);
-  } else {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(OTHER_REGS));
-    if (warp == PRODUCER_WARP) {
-      bwd_producer<D, MASK, F16>(a, &tq, &tk, &tv, &tdo, smem, bars, wc, lane);
-    } else if (warp == MMA_WARP) {
-      bwd_mma<D, MASK, F16>(a, smem, bars, tmem, wc);
-    } else if (warp == DQ_WARP) {
-      bwd_dq_issuer<D, MASK, F16>(a, &tdq, smem, bars, wc, lane);
-      if (lane == 0) bulk_wait_all();  // every dQ reduction has landed
-    }
-    __syncwarp();
-    tc_fence_before();
-    named_barrier(1, NTHREADS);
-    if (warp == MMA_WARP) {
-      tc_fence_after();
-      tmem_dealloc(tmem, TMEM_COLS);
-    }
+  } else if (warp == NB_PRODUCER) {
+    bwd_producer<D, MASK, F16>(a, &tq, &tk, &tv, &tdo, smem, bars, wc, lane);
+  } else if (warp == NB_MMA) {
+    bwd_mma<D, MASK, F16>(a, smem, bars, tmem, wc);
+  } else if (warp == NB_DQ) {
+    bwd_dq_issuer<D, MASK, F16>(a, &tdq, smem, bars, wc, lane);
+    if (lane == 0) bulk_wait_all();  // every dQ reduction has landed
+  }
+  __syncwarp();
+  tc_fence_before();
+  named_barrier(1, NB_THREADS);
+  if (warp == NB_MMA) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
   }
 }
 
@@ -1455,7 +1485,7 @@ cudaError_t launch_bwd_impl(const CUtensorMap &tq, const CUtensorMap &tk, const 
   cudaError_t e = cudaFuncSetAttribute(bwd_kernel<D, MASK, F16>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  bwd_kernel<D, MASK, F16><<<grid, NTHREADS, smem, stream>>>(tq, tk, tv, tdo, tdq, a);
+  bwd_kernel<D, MASK, F16><<<grid, NB_THREADS, smem, stream>>>(tq, tk, tv, tdo, tdq, a);
   return cudaGetLastError();
 }
 
