@@ -187,13 +187,15 @@ def test_varlen_wide_head_dims(causal):
     compare(*varlen_rows(o, lse), *varlen_rows(o_ref, lse_ref), f"varlen wide causal={causal}")
 
 
-def test_wide_head_dims_not_served_by_backward():
+def test_head_dims_past_256_not_served_by_backward():
+    """The backward serves d up to 256 (above 128 the wide kernel, tested in
+    test_gpu_backward_wide.py); a larger d is refused before any launch."""
     from exact_attention_81_gb300 import FAError
-    d = 256
+    d = 264
     q, k, v = dense_inputs(1, 128, 128, 2, 2, d, seed=894, device=DEV)
-    o, lse = fa_fwd(q, k, v)
+    lse = torch.zeros((1, 2, 128), dtype=torch.float32, device=DEV)
     with pytest.raises(FAError):
-        fa_bwd(q, k, v, o, lse, torch.ones_like(q))
+        fa_bwd(q, k, v, torch.zeros_like(q), lse, torch.ones_like(q))
 
 
 @pytest.mark.parametrize("d,group,dtype", [
