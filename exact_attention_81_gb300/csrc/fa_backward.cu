@@ -219,19 +219,6 @@ __host__ __device__ constexpr uint32_t packed_col(int query) {
   return static_cast<uint32_t>(32 * (query >> 5) + (query & 31) / 2);
 }
 
-// Two 32 lanes x 16-column TMEM loads completed by a single wait.
-__device__ __forceinline__ void tmem_ld_2x16(uint32_t taddr0, uint32_t taddr1, uint32_t (&r0)[16],
-                                             uint32_t (&r1)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%32];\n"
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%33];\n"
-      "tcgen05.wait::ld.sync.aligned;\n"
-      : "=r"(r0[0]), "=r"(r0[1]), "=r"(r0[2]), "=r"(r0[3]), "=r"(r0[4]), "=r"(r0[5]), "=r"(r0[6]), "=r"(r0[7]), "=r"(r0[8]), "=r"(r0[9]), "=r"(r0[10]), "=r"(r0[11]), "=r"(r0[12]), "=r"(r0[13]), "=r"(r0[14]), "=r"(r0[15]),
-        "=r"(r1[0]), "=r"(r1[1]), "=r"(r1[2]), "=r"(r1[3]), "=r"(r1[4]), "=r"(r1[5]), "=r"(r1[6]), "=r"(r1[7]), "=r"(r1[8]), "=r"(r1[9]), "=r"(r1[10]), "=r"(r1[11]), "=r"(r1[12]), "=r"(r1[13]), "=r"(r1[14]), "=r"(r1[15])
-      : "r"(taddr0), "r"(taddr1)
-      : "memory");
-}
-
 // Stores 8 consecutive 32-bit TMEM columns of the thread's lane (no wait).
 __device__ __forceinline__ void tmem_st_x8(uint32_t taddr, const uint32_t (&r)[8]) {
   asm volatile(
@@ -296,6 +283,16 @@ __device__ void bwd_producer(const BwdArgs &a, const CUtensorMap *tq, const CUte
     for (int t = 0; t < w.nit; ++t) {
       int h, i;
       bstep(a, w, t, h, i);
+      // LSE and D of the step's rows, loaded before the waits below so that their latency
+      // overlaps them (rows past the sequence, the next one's for varlen, are not read).
+      const int64_t base = w.b * a.lse_sb + h * a.lse_sh + w.q_tok;
+      float lv[4], dv[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int q = i * BQ + lane * 4 + e;
+        lv[e] = q < w.nq ? a.lse[base + q] : -INFINITY;
+        dv[e] = q < w.nq ? a.dvec[base + q] : 0.f;
+      }
       if (q_n > 0 && !warp_wait(&bars->q_empty, (q_n - 1) & 1u, wc)) goto out;
       if (lane == 0) {
         mbar_arrive_expect_tx(&bars->q_full, C::TILE);
@@ -312,20 +309,13 @@ __device__ void bwd_producer(const BwdArgs &a, const CUtensorMap *tq, const CUte
           tma_load_4d(smem + C::DO_OFF + c * BOX, tdo, &bars->do_full, c * 64, h,
                       w.q_tok + i * BQ, w.tma_b);
       }
-      // LSE (log2 domain; rows past Nq or with no visible key give P = 0) and D.
+      // LSE in the log2 domain (rows past the sequence or with no visible key: +inf, so
+      // that P = 0) and D.
       if (q_n > 0 && !warp_wait(&bars->vec_empty, (q_n - 1) & 1u, wc)) goto out;
-      const int64_t base = w.b * a.lse_sb + h * a.lse_sh + w.q_tok;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int qi = lane * 4 + e, q = i * BQ + qi;
-        float l2 = INFINITY, dd = 0.f;
-        if (q < w.nq) {  // rows past the sequence (the next one's, for varlen) get P = 0
-          const float l = a.lse[base + q];
-          l2 = l == -INFINITY ? INFINITY : l * LOG2E;
-          dd = a.dvec[base + q];
-        }
-        lse2[qi] = l2;
-        dvec[qi] = dd;
+        lse2[lane * 4 + e] = lv[e] == -INFINITY ? INFINITY : lv[e] * LOG2E;
+        dvec[lane * 4 + e] = dv[e];
       }
       __syncwarp();
       mbar_arrive(&bars->vec_full);
@@ -509,120 +499,120 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
       // after its keys: the bias -slope2 (q + off - key) is linear in the query.
       const bool alibi_lin = MASK == MASK_ALIBI && full && kb + BKEY - 1 <= q0 + off;
       const float slope2 = alibi ? a.alibi[w.b * a.alibi_sb + h] * LOG2E : 0.f;
-      // P^T and dS^T = P^T (dP^T - D) of this key row for the 32 queries of this quarter,
-      // 16 at a time: P^T and dS^T to TMEM (dV, dK), dS to shared memory with queries
-      // contiguous (dQ).
+      // Phase 1, as soon as S^T has landed (the MMA of dP^T may still run): P^T of this key
+      // row for the 32 queries of this quarter, to TMEM as packed 16-bit pairs over the
+      // quarter's first 16 source columns (dV).  P, times dz/ds under a softcap, stays in
+      // registers for phase 2.
       if (!warp_wait(&bars->vec_full, it & 1u, wc)) return;
       if (!warp_wait(&bars->st_full, it & 1u, wc)) return;
-      if (!warp_wait(&bars->dp_full, it & 1u, wc)) return;
       tc_fence_after();
-#pragma unroll 1
-      for (int c2 = 0; c2 < 2; ++c2) {
-        const int qc = qd * 32 + c2 * 16;  // first query of the chunk
-        uint32_t sr[16], dr[16];
-        tmem_ld_2x16(tmem + lane_off + T_ST + qc, tmem + lane_off + T_DP + qc, sr, dr);
-        uint32_t pp[8], dd[8];
+      const int qq = qd * 32;  // first query of the quarter
+      float pd[32];
+      {
+        uint32_t sr[32], pp[16];
+        tmem_ld_x32(tmem + lane_off + T_ST + qq, sr);
         if (MASK == MASK_ALIBI && alibi_lin) {
           // P = 2^(S c - slope2 (q + off - key) - LSE2): the bias pairs of queries (e, e+1)
           // and (e+2, e+3) step by -4 slope2 along two chains that start from exact
-          // products; then dS = P (dP - D), all on packed fp32 pairs.
+          // products, on packed fp32 pairs.
           const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
-          const float base = -slope2 * static_cast<float>(q0 + qc + off - key);
+          const float base = -slope2 * static_cast<float>(q0 + qq + off - key);
           uint64_t w01 = f2_pack(base, base - slope2);
           uint64_t w23 = f2_pack(base - 2.f * slope2, base - 3.f * slope2);
           const uint64_t step = f2_pack(-4.f * slope2, -4.f * slope2);
 #pragma unroll
-          for (int e4 = 0; e4 < 16; e4 += 4) {
-            const float4 l4 = *reinterpret_cast<const float4 *>(lse2 + qc + e4);
-            const float4 d4 = *reinterpret_cast<const float4 *>(dvec + qc + e4);
-            float z0, z1, z2, z3, e0, e1, e2, e3;
+          for (int e4 = 0; e4 < 32; e4 += 4) {
+            const float4 l4 = *reinterpret_cast<const float4 *>(lse2 + qq + e4);
+            float z0, z1, z2, z3;
             f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e4]), __uint_as_float(sr[e4 + 1])), sc2,
                              f2_add(w01, f2_pack(-l4.x, -l4.y))), z0, z1);
             f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e4 + 2]), __uint_as_float(sr[e4 + 3])),
                              sc2, f2_add(w23, f2_pack(-l4.z, -l4.w))), z2, z3);
             w01 = f2_add(w01, step);
             w23 = f2_add(w23, step);
-            const float p0 = ex2_approx(z0), p1 = ex2_approx(z1);
-            const float p2 = ex2_approx(z2), p3 = ex2_approx(z3);
-            f2_unpack(f2_mul(f2_pack(p0, p1),
-                             f2_add(f2_pack(__uint_as_float(dr[e4]), __uint_as_float(dr[e4 + 1])),
-                                    f2_pack(-d4.x, -d4.y))), e0, e1);
-            f2_unpack(f2_mul(f2_pack(p2, p3),
-                             f2_add(f2_pack(__uint_as_float(dr[e4 + 2]),
-                                            __uint_as_float(dr[e4 + 3])),
-                                    f2_pack(-d4.z, -d4.w))), e2, e3);
-            pp[e4 / 2] = pack2<F16>(p0, p1);
-            pp[e4 / 2 + 1] = pack2<F16>(p2, p3);
-            dd[e4 / 2] = pack2<F16>(e0, e1);
-            dd[e4 / 2 + 1] = pack2<F16>(e2, e3);
+            pd[e4] = ex2_approx(z0);
+            pd[e4 + 1] = ex2_approx(z1);
+            pd[e4 + 2] = ex2_approx(z2);
+            pd[e4 + 3] = ex2_approx(z3);
+            pp[e4 / 2] = pack2<F16>(pd[e4], pd[e4 + 1]);
+            pp[e4 / 2 + 1] = pack2<F16>(pd[e4 + 2], pd[e4 + 3]);
           }
         } else if (!SCORE_MOD && full) {
-          // No masked pair and no modifier: P = 2^(S c - LSE2), dS = P (dP - D) on packed
-          // fp32 pairs.
+          // No masked pair and no modifier: P = 2^(S c - LSE2) on packed fp32 pairs.
           const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
 #pragma unroll
-          for (int e4 = 0; e4 < 16; e4 += 4) {
-            const float4 l4 = *reinterpret_cast<const float4 *>(lse2 + qc + e4);
-            const float4 d4 = *reinterpret_cast<const float4 *>(dvec + qc + e4);
-            float z0, z1, z2, z3, e0, e1, e2, e3;
+          for (int e4 = 0; e4 < 32; e4 += 4) {
+            const float4 l4 = *reinterpret_cast<const float4 *>(lse2 + qq + e4);
+            float z0, z1, z2, z3;
             f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e4]), __uint_as_float(sr[e4 + 1])), sc2,
                              f2_pack(-l4.x, -l4.y)), z0, z1);
             f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e4 + 2]), __uint_as_float(sr[e4 + 3])),
                              sc2, f2_pack(-l4.z, -l4.w)), z2, z3);
-            const float p0 = ex2_approx(z0), p1 = ex2_approx(z1);
-            const float p2 = ex2_approx(z2), p3 = ex2_approx(z3);
-            f2_unpack(f2_mul(f2_pack(p0, p1),
-                             f2_add(f2_pack(__uint_as_float(dr[e4]), __uint_as_float(dr[e4 + 1])),
-                                    f2_pack(-d4.x, -d4.y))), e0, e1);
-            f2_unpack(f2_mul(f2_pack(p2, p3),
-                             f2_add(f2_pack(__uint_as_float(dr[e4 + 2]),
-                                            __uint_as_float(dr[e4 + 3])),
-                                    f2_pack(-d4.z, -d4.w))), e2, e3);
-            pp[e4 / 2] = pack2<F16>(p0, p1);
-            pp[e4 / 2 + 1] = pack2<F16>(p2, p3);
-            dd[e4 / 2] = pack2<F16>(e0, e1);
-            dd[e4 / 2 + 1] = pack2<F16>(e2, e3);
+            pd[e4] = ex2_approx(z0);
+            pd[e4 + 1] = ex2_approx(z1);
+            pd[e4 + 2] = ex2_approx(z2);
+            pd[e4 + 3] = ex2_approx(z3);
+            pp[e4 / 2] = pack2<F16>(pd[e4], pd[e4 + 1]);
+            pp[e4 / 2 + 1] = pack2<F16>(pd[e4 + 2], pd[e4 + 3]);
           }
         } else {
 #pragma unroll
-        for (int e4 = 0; e4 < 16; e4 += 4) {
-          const float4 l4 = *reinterpret_cast<const float4 *>(lse2 + qc + e4);
-          const float4 d4 = *reinterpret_cast<const float4 *>(dvec + qc + e4);
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
-          float p[4], ds[4];
+          for (int e2 = 0; e2 < 32; e2 += 2) {
+            float p[2];
 #pragma unroll
-          for (int x = 0; x < 4; ++x) {
-            const int qi = qc + e4 + x;
-            const float sv = __uint_as_float(sr[e4 + x]);
-            float z2, dz = 1.f;  // score in log2 units and dz/ds
-            if constexpr (SCORE_MOD) {
-              if (softcap) {
-                const float t = tanh_ex2(sv * a.sc_in);
-                z2 = t * a.sc_out;
-                dz = 1.f - t * t;
+            for (int x = 0; x < 2; ++x) {
+              const int qi = qq + e2 + x;
+              const float sv = __uint_as_float(sr[e2 + x]);
+              float z2, dz = 1.f;  // score in log2 units and dz/ds
+              if constexpr (SCORE_MOD) {
+                if (softcap) {
+                  const float t = tanh_ex2(sv * a.sc_in);
+                  z2 = t * a.sc_out;
+                  dz = 1.f - t * t;
+                } else {
+                  z2 = sv * a.scale_log2;
+                }
+                if (alibi) z2 = fmaf(-slope2, fabsf(static_cast<float>(q0 + qi + off - key)), z2);
               } else {
                 z2 = sv * a.scale_log2;
               }
-              if (alibi) z2 = fmaf(-slope2, fabsf(static_cast<float>(q0 + qi + off - key)), z2);
-            } else {
-              z2 = sv * a.scale_log2;
+              bool vis;
+              if constexpr (WIN)
+                vis = full || (key < w.nk && q0 + qi >= qv_lo && q0 + qi <= qv_hi);
+              else
+                vis = full || (key < w.nk && (MASK == MASK_NONE || key <= q0 + qi + off));
+              const float pv = ex2_approx(z2 - lse2[qi]);
+              p[x] = vis ? pv : 0.f;
+              pd[e2 + x] = p[x] * dz;
             }
-            bool vis;
-            if constexpr (WIN)
-              vis = full || (key < w.nk && q0 + qi >= qv_lo && q0 + qi <= qv_hi);
-            else
-              vis = full || (key < w.nk && (MASK == MASK_NONE || key <= q0 + qi + off));
-            const float pv = ex2_approx(z2 - lv[x]);
-            p[x] = vis ? pv : 0.f;
-            ds[x] = p[x] * (__uint_as_float(dr[e4 + x]) - dv[x]) * dz;
+            pp[e2 / 2] = pack2<F16>(p[0], p[1]);
           }
-          pp[e4 / 2] = pack2<F16>(p[0], p[1]);
-          pp[e4 / 2 + 1] = pack2<F16>(p[2], p[3]);
-          dd[e4 / 2] = pack2<F16>(ds[0], ds[1]);
-          dd[e4 / 2 + 1] = pack2<F16>(ds[2], ds[3]);
         }
+        tmem_st_x16(tmem + lane_off + T_ST + packed_col(qq), pp);
+      }
+      // Phase 2, once dP^T has landed: dS^T = P^T (dP^T - D) of the same 32 queries, 16 at a
+      // time, to TMEM as packed pairs (dK) and to shared memory with queries contiguous (dQ).
+      if (!warp_wait(&bars->dp_full, it & 1u, wc)) return;
+      tc_fence_after();
+#pragma unroll
+      for (int c2 = 0; c2 < 2; ++c2) {
+        const int qc = qq + c2 * 16;  // first query of the chunk
+        uint32_t dr[16], dd[8];
+        tmem_ld_x16(tmem + lane_off + T_DP + qc, dr);
+#pragma unroll
+        for (int e4 = 0; e4 < 16; e4 += 4) {
+          const float4 d4 = *reinterpret_cast<const float4 *>(dvec + qc + e4);
+          const float *pe = pd + c2 * 16 + e4;
+          float e0, e1, e2, e3;
+          f2_unpack(f2_mul(f2_pack(pe[0], pe[1]),
+                           f2_add(f2_pack(__uint_as_float(dr[e4]), __uint_as_float(dr[e4 + 1])),
+                                  f2_pack(-d4.x, -d4.y))), e0, e1);
+          f2_unpack(f2_mul(f2_pack(pe[2], pe[3]),
+                           f2_add(f2_pack(__uint_as_float(dr[e4 + 2]), __uint_as_float(dr[e4 + 3])),
+                                  f2_pack(-d4.z, -d4.w))), e2, e3);
+          dd[e4 / 2] = pack2<F16>(e0, e1);
+          dd[e4 / 2 + 1] = pack2<F16>(e2, e3);
         }
-        tmem_st_x8(tmem + lane_off + T_ST + packed_col(qc), pp);
         tmem_st_x8(tmem + lane_off + T_DP + packed_col(qc), dd);
         uint8_t *box = ds_s + (qc >> 6) * BOX + r * 128;  // box = query half
 #pragma unroll
@@ -641,8 +631,6 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
       // the accumulator is issued by the dQ issuer warp, off this critical path.
       if (!warp_wait(&bars->dq_full, it & 1u, wc)) return;
       tc_fence_after();
-      // The issuer's previous reduction has read the staging tile.
-      if (it > 0 && !warp_wait(&bars->dq_free, (it - 1) & 1u, wc)) return;
       {
         // this warp's DW columns of dQ: one 32-column box (D = 128) or half of one (D = 64)
         uint32_t qr[DW];
@@ -650,6 +638,11 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
           tmem_ld_x32(tmem + lane_off + T_DP + qd * DW, qr);
         else
           tmem_ld_x16(tmem + lane_off + T_DP + qd * DW, qr);
+        // The columns are in registers: the MMA of the next dP^T may overwrite them.
+        tc_fence_before();
+        mbar_arrive(&bars->dq_empty);
+        // The issuer's previous reduction has read the staging tile.
+        if (it > 0 && !warp_wait(&bars->dq_free, (it - 1) & 1u, wc)) return;
         const int c0 = qd * DW;  // first dQ column
         uint8_t *box = dq_s + (c0 >> 5) * BOX + r * 128;
 #pragma unroll
@@ -659,8 +652,6 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
               make_uint4(qr[4 * gi], qr[4 * gi + 1], qr[4 * gi + 2], qr[4 * gi + 3]);
         }
       }
-      tc_fence_before();
-      mbar_arrive(&bars->dq_empty);
       fence_proxy_async_smem();
       mbar_arrive(&bars->dq_staged);
       ++it;
