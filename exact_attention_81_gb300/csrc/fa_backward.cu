@@ -440,7 +440,7 @@ out:
 // Compute warps: warp w handles TMEM lanes 32 (w % 4) .. +31, queries 32 (w / 4) .. +31 of a
 // step for P^T / dS^T, and d columns (w / 4) D/4 .. +D/4 in the dQ, dK and dV epilogues.
 
-template <int D, int MASK, bool F16>
+template <int D, int MASK, bool F16, bool DET>
 __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *smem, BBars *bars,
                             uint32_t tmem, const WaitCtl &wc, int tid) {
   using C = BCfg<D, F16>;
@@ -454,6 +454,7 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
   uint8_t *ds_s = smem + C::DS_OFF;
   uint8_t *dq_s = smem + C::DQ_OFF;
   uint32_t it = 0, acc_n = 0;
+  bool vec_ready = false;  // the current step's LSE / D already waited for
   for (int u = blockIdx.x; u < a.num_units; u += gridDim.x) {
     const BUnit w = bunit_of<MASK>(a, u);
     if (w.skip) continue;
@@ -503,7 +504,8 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
       // row for the 32 queries of this quarter, to TMEM as packed 16-bit pairs over the
       // quarter's first 16 source columns (dV).  P, times dz/ds under a softcap, stays in
       // registers for phase 2.
-      if (!warp_wait(&bars->vec_full, it & 1u, wc)) return;
+      if (!vec_ready && !warp_wait(&bars->vec_full, it & 1u, wc)) return;
+      vec_ready = false;
       if (!warp_wait(&bars->st_full, it & 1u, wc)) return;
       tc_fence_after();
       const int qq = qd * 32;  // first query of the quarter
@@ -629,6 +631,16 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
       mbar_arrive(&bars->p_ready);
       // dQ epilogue: TMEM -> shared memory (fp32, 128-byte swizzle); the reduce-add into
       // the accumulator is issued by the dQ issuer warp, off this critical path.
+      // Barriers that complete early are polled before the staging stores below, which
+      // queue ahead of any later poll in the shared-memory pipe: the issuer's previous
+      // reduction has read the staging tile (unordered dQ only: in deterministic order that
+      // reduction waits for other CTAs, and the TMEM handoff must not wait behind it), and
+      // (within a unit) the next step's LSE / D.
+      if (!DET && it > 0 && !warp_wait(&bars->dq_free, (it - 1) & 1u, wc)) return;
+      if (t + 1 < w.nit) {
+        if (!warp_wait(&bars->vec_full, (it + 1) & 1u, wc)) return;
+        vec_ready = true;
+      }
       if (!warp_wait(&bars->dq_full, it & 1u, wc)) return;
       tc_fence_after();
       {
@@ -641,8 +653,7 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
         // The columns are in registers: the MMA of the next dP^T may overwrite them.
         tc_fence_before();
         mbar_arrive(&bars->dq_empty);
-        // The issuer's previous reduction has read the staging tile.
-        if (it > 0 && !warp_wait(&bars->dq_free, (it - 1) & 1u, wc)) return;
+        if (DET && it > 0 && !warp_wait(&bars->dq_free, (it - 1) & 1u, wc)) return;
         const int c0 = qd * DW;  // first dQ column
         uint8_t *box = dq_s + (c0 >> 5) * BOX + r * 128;
 #pragma unroll
@@ -693,7 +704,9 @@ __device__ void bwd_compute(const BwdArgs &a, const CUtensorMap *tdq, uint8_t *s
   }
 }
 
-template <int D, int MASK, bool F16>
+// DET: deterministic dQ order (a.sem != nullptr), a separate instance so that each order's
+// compute loop is scheduled on its own.
+template <int D, int MASK, bool F16, bool DET>
 __global__ void __launch_bounds__(NB_THREADS, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -745,7 +758,7 @@ __global__ void __launch_bounds__(NB_THREADS, 1)
   const WaitCtl wc{&bars->abort, a.err, a.timeout_ns, DEVERR_BWD_TIMEOUT};
   // Every role ends on its own; all meet at a named barrier before TMEM is released.
   if (warp < NB_PRODUCER) {
-    bwd_compute<D, MASK, F16>(a, &tdq, smem, bars, tmem, wc, tid);
+    bwd_compute<D, MASK, F16, DET>(a, &tdq, smem, bars, tmem, wc, tid);
   } else if (warp == NB_PRODUCER) {
     bwd_producer<D, MASK, F16>(a, &tq, &tk, &tv, &tdo, smem, bars, wc, lane);
   } else if (warp == NB_MMA) {
@@ -1473,10 +1486,17 @@ cudaError_t launch_bwd_impl(const CUtensorMap &tq, const CUtensorMap &tk, const 
                             int grid, cudaStream_t stream) {
   constexpr int smem = BCfg<D, F16>::SMEM_BYTES;
   static_assert(smem <= 232448, "backward kernel shared memory");
-  cudaError_t e = cudaFuncSetAttribute(bwd_kernel<D, MASK, F16>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  bwd_kernel<D, MASK, F16><<<grid, NB_THREADS, smem, stream>>>(tq, tk, tv, tdo, tdq, a);
+  if (a.sem != nullptr) {
+    cudaError_t e = cudaFuncSetAttribute(bwd_kernel<D, MASK, F16, true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    bwd_kernel<D, MASK, F16, true><<<grid, NB_THREADS, smem, stream>>>(tq, tk, tv, tdo, tdq, a);
+  } else {
+    cudaError_t e = cudaFuncSetAttribute(bwd_kernel<D, MASK, F16, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    bwd_kernel<D, MASK, F16, false><<<grid, NB_THREADS, smem, stream>>>(tq, tk, tv, tdo, tdq, a);
+  }
   return cudaGetLastError();
 }
 
