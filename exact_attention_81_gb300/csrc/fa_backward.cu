@@ -372,14 +372,14 @@ __device__ void bwd_dq_issuer(const BwdArgs &a, const CUtensorMap *tdq, uint8_t 
               tma_reduce_add_4d(tdq, dq_s + cc * BOX + rq * 32 * 128, cc * 32, h,
                                 w.q_tok + q0 + rq * 32, w.tma_b);
           bulk_commit_group();
+          bulk_wait_read();              // the staging tile may be written again
+          mbar_arrive(&bars->dq_free);
           if (sem != nullptr) {
             bulk_wait_all();             // the additions have been performed
             fence_proxy_async_global();
             __threadfence();
             atomicAdd(sem, 1);
           }
-          bulk_wait_read();              // the staging tile may be written again
-          mbar_arrive(&bars->dq_free);
         }
       }
       if (!__all_sync(0xffffffffu, ok)) return;
@@ -978,14 +978,14 @@ __device__ void wide_dq_issuer(const BwdArgs &a, const CUtensorMap *tdq, uint8_t
               tma_reduce_add_4d(tdq, smem + C::DQ_OFF, q0 + 32 * x, 128 * dh, h, w.b);
               bulk_commit_group();
             }
+            bulk_wait_read();              // the staging box may be written again
+            mbar_arrive(x == 0 ? &bars->dq_free : &bars->dq_free_r1);
             if (sem != nullptr && x == 1) {
               bulk_wait_all();             // the step's additions have been performed
               fence_proxy_async_global();
               __threadfence();
               atomicAdd(sem, 1);
             }
-            bulk_wait_read();              // the staging box may be written again
-            mbar_arrive(x == 0 ? &bars->dq_free : &bars->dq_free_r1);
           }
         }
         if (!__all_sync(0xffffffffu, ok)) return;
