@@ -1105,116 +1105,115 @@ __device__ void wide_compute(const BwdArgs &a, uint8_t *smem, BBars *bars, uint3
       const float slope2 = alibi ? a.alibi[w.b * a.alibi_sb + h] * LOG2E : 0.f;
       if (!warp_wait(&bars->vec_full, it & 1u, wc)) return;
       if (!warp_wait(&bars->st_full, it & 1u, wc)) return;
-      if (!warp_wait(&bars->dp_full, it & 1u, wc)) return;
       tc_fence_after();
       {
         const int c2 = half;      // the warpgroup's 32-query chunk of the step
         const int qc = 32 * half;  // its first query
-        uint32_t sr[32], dr[32];
-        tmem_ld_2x32(tmem + lane_off + W_ST + qc, tmem + lane_off + W_DP + qc, sr, dr);
-        uint32_t pp[16], dd[16];
-        if (MASK == MASK_ALIBI && alibi_lin) {
-          // P = 2^(S c - slope2 (q + off - key) - LSE2): the bias pairs of queries (e, e+1)
-          // and (e+2, e+3) step by -4 slope2 along two chains that start from exact
-          // products; then dS = P (dP - D), all on packed fp32 pairs.
-          const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
-          const float base = -slope2 * static_cast<float>(q0 + qc + off - key);
-          uint64_t w01 = f2_pack(base, base - slope2);
-          uint64_t w23 = f2_pack(base - 2.f * slope2, base - 3.f * slope2);
-          const uint64_t step = f2_pack(-4.f * slope2, -4.f * slope2);
+        // Phase 1, as soon as S^T has landed (dP^T may still be in the tensor core): P^T of
+        // the chunk -> TMEM, packed over the first 16 of its own 32 fp32 columns (dV); P,
+        // times dz/ds under a softcap, stays in registers for phase 2.
+        float pd[32];
+        {
+          uint32_t sr[32], pp[16];
+          tmem_ld_x32(tmem + lane_off + W_ST + qc, sr);
+          if (MASK == MASK_ALIBI && alibi_lin) {
+            // P = 2^(S c - slope2 (q + off - key) - LSE2): the bias pairs of queries (e, e+1)
+            // and (e+2, e+3) step by -4 slope2 along two chains that start from exact
+            // products, on packed fp32 pairs.
+            const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
+            const float base = -slope2 * static_cast<float>(q0 + qc + off - key);
+            uint64_t w01 = f2_pack(base, base - slope2);
+            uint64_t w23 = f2_pack(base - 2.f * slope2, base - 3.f * slope2);
+            const uint64_t step = f2_pack(-4.f * slope2, -4.f * slope2);
 #pragma unroll
-          for (int e4 = 0; e4 < 32; e4 += 4) {
-            const float4 l4 = *reinterpret_cast<const float4 *>(lse2 + qc + e4);
-            const float4 d4 = *reinterpret_cast<const float4 *>(dvec + qc + e4);
-            float z0, z1, z2, z3, e0, e1, e2, e3;
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e4]), __uint_as_float(sr[e4 + 1])), sc2,
-                             f2_add(w01, f2_pack(-l4.x, -l4.y))), z0, z1);
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e4 + 2]), __uint_as_float(sr[e4 + 3])),
-                             sc2, f2_add(w23, f2_pack(-l4.z, -l4.w))), z2, z3);
-            w01 = f2_add(w01, step);
-            w23 = f2_add(w23, step);
-            const float p0 = ex2_approx(z0), p1 = ex2_approx(z1);
-            const float p2 = ex2_approx(z2), p3 = ex2_approx(z3);
-            f2_unpack(f2_mul(f2_pack(p0, p1),
-                             f2_add(f2_pack(__uint_as_float(dr[e4]), __uint_as_float(dr[e4 + 1])),
-                                    f2_pack(-d4.x, -d4.y))), e0, e1);
-            f2_unpack(f2_mul(f2_pack(p2, p3),
-                             f2_add(f2_pack(__uint_as_float(dr[e4 + 2]),
-                                            __uint_as_float(dr[e4 + 3])),
-                                    f2_pack(-d4.z, -d4.w))), e2, e3);
-            pp[e4 / 2] = pack2<F16>(p0, p1);
-            pp[e4 / 2 + 1] = pack2<F16>(p2, p3);
-            dd[e4 / 2] = pack2<F16>(e0, e1);
-            dd[e4 / 2 + 1] = pack2<F16>(e2, e3);
-          }
-        } else if (!SCORE_MOD && full) {
-          // No masked pair and no modifier: P = 2^(S c - LSE2), dS = P (dP - D) on packed
-          // fp32 pairs.
-          const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
+            for (int e4 = 0; e4 < 32; e4 += 4) {
+              const float4 l4 = *reinterpret_cast<const float4 *>(lse2 + qc + e4);
+              float z0, z1, z2, z3;
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e4]), __uint_as_float(sr[e4 + 1])),
+                               sc2, f2_add(w01, f2_pack(-l4.x, -l4.y))), z0, z1);
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e4 + 2]), __uint_as_float(sr[e4 + 3])),
+                               sc2, f2_add(w23, f2_pack(-l4.z, -l4.w))), z2, z3);
+              w01 = f2_add(w01, step);
+              w23 = f2_add(w23, step);
+              pd[e4] = ex2_approx(z0);
+              pd[e4 + 1] = ex2_approx(z1);
+              pd[e4 + 2] = ex2_approx(z2);
+              pd[e4 + 3] = ex2_approx(z3);
+              pp[e4 / 2] = pack2<F16>(pd[e4], pd[e4 + 1]);
+              pp[e4 / 2 + 1] = pack2<F16>(pd[e4 + 2], pd[e4 + 3]);
+            }
+          } else if (!SCORE_MOD && full) {
+            // No masked pair and no modifier: P = 2^(S c - LSE2) on packed fp32 pairs.
+            const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
 #pragma unroll
-          for (int e4 = 0; e4 < 32; e4 += 4) {
-            const float4 l4 = *reinterpret_cast<const float4 *>(lse2 + qc + e4);
-            const float4 d4 = *reinterpret_cast<const float4 *>(dvec + qc + e4);
-            float z0, z1, z2, z3, e0, e1, e2, e3;
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e4]), __uint_as_float(sr[e4 + 1])), sc2,
-                             f2_pack(-l4.x, -l4.y)), z0, z1);
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e4 + 2]), __uint_as_float(sr[e4 + 3])),
-                             sc2, f2_pack(-l4.z, -l4.w)), z2, z3);
-            const float p0 = ex2_approx(z0), p1 = ex2_approx(z1);
-            const float p2 = ex2_approx(z2), p3 = ex2_approx(z3);
-            f2_unpack(f2_mul(f2_pack(p0, p1),
-                             f2_add(f2_pack(__uint_as_float(dr[e4]), __uint_as_float(dr[e4 + 1])),
-                                    f2_pack(-d4.x, -d4.y))), e0, e1);
-            f2_unpack(f2_mul(f2_pack(p2, p3),
-                             f2_add(f2_pack(__uint_as_float(dr[e4 + 2]),
-                                            __uint_as_float(dr[e4 + 3])),
-                                    f2_pack(-d4.z, -d4.w))), e2, e3);
-            pp[e4 / 2] = pack2<F16>(p0, p1);
-            pp[e4 / 2 + 1] = pack2<F16>(p2, p3);
-            dd[e4 / 2] = pack2<F16>(e0, e1);
-            dd[e4 / 2 + 1] = pack2<F16>(e2, e3);
+            for (int e4 = 0; e4 < 32; e4 += 4) {
+              const float4 l4 = *reinterpret_cast<const float4 *>(lse2 + qc + e4);
+              float z0, z1, z2, z3;
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e4]), __uint_as_float(sr[e4 + 1])),
+                               sc2, f2_pack(-l4.x, -l4.y)), z0, z1);
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e4 + 2]), __uint_as_float(sr[e4 + 3])),
+                               sc2, f2_pack(-l4.z, -l4.w)), z2, z3);
+              pd[e4] = ex2_approx(z0);
+              pd[e4 + 1] = ex2_approx(z1);
+              pd[e4 + 2] = ex2_approx(z2);
+              pd[e4 + 3] = ex2_approx(z3);
+              pp[e4 / 2] = pack2<F16>(pd[e4], pd[e4 + 1]);
+              pp[e4 / 2 + 1] = pack2<F16>(pd[e4 + 2], pd[e4 + 3]);
+            }
+          } else {
+#pragma unroll
+            for (int e2 = 0; e2 < 32; e2 += 2) {
+              float p[2];
+#pragma unroll
+              for (int x = 0; x < 2; ++x) {
+                const int qi = qc + e2 + x;
+                const float sv = __uint_as_float(sr[e2 + x]);
+                float z2, dz = 1.f;  // score in log2 units and dz/ds
+                if constexpr (SCORE_MOD) {
+                  if (softcap) {
+                    const float t = tanh_ex2(sv * a.sc_in);
+                    z2 = t * a.sc_out;
+                    dz = 1.f - t * t;
+                  } else {
+                    z2 = sv * a.scale_log2;
+                  }
+                  if (alibi) z2 = fmaf(-slope2, fabsf(static_cast<float>(q0 + qi + off - key)), z2);
+                } else {
+                  z2 = sv * a.scale_log2;
+                }
+                bool vis;
+                if constexpr (WIN)
+                  vis = full || (key < w.nk && q0 + qi >= qv_lo && q0 + qi <= qv_hi);
+                else
+                  vis = full || (key < w.nk && (MASK == MASK_NONE || key <= q0 + qi + off));
+                const float pv = ex2_approx(z2 - lse2[qi]);
+                p[x] = vis ? pv : 0.f;
+                pd[e2 + x] = p[x] * dz;
+              }
+              pp[e2 / 2] = pack2<F16>(p[0], p[1]);
+            }
           }
-        } else {
+          tmem_st_x16(tmem + lane_off + W_ST + qc, pp);
+        }
+        // Phase 2, once dP^T has landed: dS^T = P^T (dP^T - D) -> TMEM, packed over the first
+        // 16 of the chunk's dP^T columns (dK), and dS -> shared memory, queries contiguous.
+        if (!warp_wait(&bars->dp_full, it & 1u, wc)) return;
+        tc_fence_after();
+        uint32_t dr[32], dd[16];
+        tmem_ld_x32(tmem + lane_off + W_DP + qc, dr);
 #pragma unroll
         for (int e4 = 0; e4 < 32; e4 += 4) {
-          const float4 l4 = *reinterpret_cast<const float4 *>(lse2 + qc + e4);
           const float4 d4 = *reinterpret_cast<const float4 *>(dvec + qc + e4);
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
-          float p[4], ds[4];
-#pragma unroll
-          for (int x = 0; x < 4; ++x) {
-            const int qi = qc + e4 + x;
-            const float sv = __uint_as_float(sr[e4 + x]);
-            float z2, dz = 1.f;  // score in log2 units and dz/ds
-            if constexpr (SCORE_MOD) {
-              if (softcap) {
-                const float t = tanh_ex2(sv * a.sc_in);
-                z2 = t * a.sc_out;
-                dz = 1.f - t * t;
-              } else {
-                z2 = sv * a.scale_log2;
-              }
-              if (alibi) z2 = fmaf(-slope2, fabsf(static_cast<float>(q0 + qi + off - key)), z2);
-            } else {
-              z2 = sv * a.scale_log2;
-            }
-            bool vis;
-            if constexpr (WIN)
-              vis = full || (key < w.nk && q0 + qi >= qv_lo && q0 + qi <= qv_hi);
-            else
-              vis = full || (key < w.nk && (MASK == MASK_NONE || key <= q0 + qi + off));
-            const float pv = ex2_approx(z2 - lv[x]);
-            p[x] = vis ? pv : 0.f;
-            ds[x] = p[x] * (__uint_as_float(dr[e4 + x]) - dv[x]) * dz;
-          }
-          pp[e4 / 2] = pack2<F16>(p[0], p[1]);
-          pp[e4 / 2 + 1] = pack2<F16>(p[2], p[3]);
-          dd[e4 / 2] = pack2<F16>(ds[0], ds[1]);
-          dd[e4 / 2 + 1] = pack2<F16>(ds[2], ds[3]);
+          float e0, e1, e2, e3;
+          f2_unpack(f2_mul(f2_pack(pd[e4], pd[e4 + 1]),
+                           f2_add(f2_pack(__uint_as_float(dr[e4]), __uint_as_float(dr[e4 + 1])),
+                                  f2_pack(-d4.x, -d4.y))), e0, e1);
+          f2_unpack(f2_mul(f2_pack(pd[e4 + 2], pd[e4 + 3]),
+                           f2_add(f2_pack(__uint_as_float(dr[e4 + 2]), __uint_as_float(dr[e4 + 3])),
+                                  f2_pack(-d4.z, -d4.w))), e2, e3);
+          dd[e4 / 2] = pack2<F16>(e0, e1);
+          dd[e4 / 2 + 1] = pack2<F16>(e2, e3);
         }
-        }
-        // packed over the first 16 of the chunk's own 32 fp32 columns
-        tmem_st_x16(tmem + lane_off + W_ST + qc, pp);
         tmem_st_x16(tmem + lane_off + W_DP + qc, dd);
         uint8_t *box = ds_s + r * 128;  // [128 keys x 64 queries]: this chunk's 64 bytes
 #pragma unroll
