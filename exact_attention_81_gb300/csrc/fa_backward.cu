@@ -1229,7 +1229,11 @@ __device__ void wide_compute(const BwdArgs &a, uint8_t *smem, BBars *bars, uint3
       tc_fence_before();
       mbar_arrive(&bars->p_ready);
       // dQ^T_h epilogue: this warpgroup's 32 query columns (thread = d row) through the
-      // staging box, warpgroup 0 first; the reduce-add is the dQ issuer's.
+      // staging box, warpgroup 0 first; the reduce-add is the dQ issuer's.  Unordered dQ:
+      // warpgroup 0's wait for the previous round's read (complete by now) is polled here,
+      // ahead of the staging stores that would queue before it in the shared-memory pipe.
+      const bool early = half == 0 && a.sem == nullptr && it > 0;
+      if (early && !warp_wait(&bars->dq_free_r1, (it - 1) & 1u, wc)) return;
       if (!warp_wait(&bars->dq_full, it & 1u, wc)) return;
       tc_fence_after();
       uint32_t qv[32];
@@ -1241,7 +1245,7 @@ __device__ void wide_compute(const BwdArgs &a, uint8_t *smem, BBars *bars, uint3
       // step), warpgroup 1's this step's first (dq_free, one per step).  One barrier per
       // round keeps every wait within one phase of its barrier: warpgroup 1 can reach its
       // next round before the issuer has read its last one.
-      if (half == 0 ? it > 0 && !warp_wait(&bars->dq_free_r1, (it - 1) & 1u, wc)
+      if (half == 0 ? !early && it > 0 && !warp_wait(&bars->dq_free_r1, (it - 1) & 1u, wc)
                     : !warp_wait(&bars->dq_free, it & 1u, wc))
         return;
       wide_stage_dqt(stage, r, qv);
