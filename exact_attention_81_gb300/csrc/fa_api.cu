@@ -168,7 +168,7 @@ fa_status make_map_f32(CUtensorMap *map, void *base, int d, int64_t n, int64_t h
                         static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(b)};
   cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(h * d) * 4,
                            static_cast<cuuint64_t>(n * h * d) * 4};
-  cuuint32_t box[4] = {32, 1, 32, 1};  // 32 columns x the 32 rows of one compute warp
+  cuuint32_t box[4] = {32, 1, 128, 1};  // 32 columns x the 128 rows of a backward step
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

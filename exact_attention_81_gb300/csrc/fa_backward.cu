@@ -333,8 +333,8 @@ out:
 
 // ------------------------------------------------------------------------------------
 // dQ issuer: once the compute warps have staged a step's dQ tile, adds it into the fp32
-// accumulator with TMA reduce-adds (32 x 32 boxes), then frees the staging tile as soon as
-// the TMA has read it.  The whole warp runs the loop, lane 0 issues.  Deterministic
+// accumulator with TMA reduce-adds (one box of 32 columns x 128 rows per 32 columns), then
+// frees the staging tile as soon as the TMA has read it.  The whole warp runs the loop, lane 0 issues.  Deterministic
 // order: before adding, lane 0 waits until the (batch, head, query block) counter shows
 // that the key blocks before this one have added, and after its own addition has landed
 // it increments the counter.
@@ -367,10 +367,7 @@ __device__ void bwd_dq_issuer(const BwdArgs &a, const CUtensorMap *tdq, uint8_t 
         if (ok) {
 #pragma unroll
           for (int cc = 0; cc < D / 32; ++cc)
-#pragma unroll
-            for (int rq = 0; rq < 4; ++rq)
-              tma_reduce_add_4d(tdq, dq_s + cc * BOX + rq * 32 * 128, cc * 32, h,
-                                w.q_tok + q0 + rq * 32, w.tma_b);
+            tma_reduce_add_4d(tdq, dq_s + cc * BOX, cc * 32, h, w.q_tok + q0, w.tma_b);
           bulk_commit_group();
           bulk_wait_read();              // the staging tile may be written again
           mbar_arrive(&bars->dq_free);
