@@ -20,25 +20,28 @@
 // Keys are the MMA rows (TMEM lanes) of S^T, dP^T, dV and dK, so the dK and dV
 // accumulators stay in TMEM across the unit.
 //
-// Roles (384 threads, three warpgroups):
-//   warps 0-7  P^T and dS^T (thread = key row; warps 0-3 take queries 0-63 of the step,
-//              warps 4-7 queries 64-127), the dQ epilogue (thread = query row, half of the
-//              d columns each) and the dK / dV epilogue at the end of a unit
-//   warp  8    producer: K, V (once per unit), Q, dO (per step) by TMA; LSE and D vectors
-//   warp  9    TMEM allocator and MMA issuer (the whole warp, one elected lane issues)
-//   warp  10   dQ issuer: TMA reduce-adds of the staged dQ tiles (and the deterministic
+// Head dimensions up to 128 (bwd_kernel): 640 threads, no register split.
+//   warps 0-15 compute: warp w takes TMEM lanes 32 (w % 4) .. +31 and, for P^T and dS^T
+//              (thread = key row), queries 32 (w / 4) .. +31 of a step; for the dQ epilogue
+//              (thread = query row) and the dK / dV epilogue at the end of a unit (thread =
+//              key row), d columns (w / 4) D/4 .. +D/4
+//   warp 16    producer: K, V (once per unit), Q, dO (per step) by TMA; LSE and D vectors
+//   warp 17    TMEM allocator and MMA issuer (the whole warp, one elected lane issues)
+//   warp 18    dQ issuer: TMA reduce-adds of the staged dQ tiles (and the deterministic
 //              order), off the compute warps' critical path
-//   warp  11   idle; the third warpgroup gives registers back (setmaxnreg) so that the
-//              compute warps hold a 64-query row of P and its dS without spilling
-// TMEM: S^T [0,128), dP^T [128,256) (then dS^T, then dQ), dV [256,256+d), dK [384,384+d).
-// P^T and dS^T are written back as packed 16-bit pairs, each query half over the first
-// columns of its own fp32 source (queries 0-63 at +0, 64-127 at +64), and feed the dV and
-// dK MMAs from TMEM; dS is also written to shared memory (queries contiguous, the MN-major
-// A operand of the dQ MMA).  Each step's dQ tile goes through shared memory to a TMA bulk
-// reduce-add into an fp32 accumulator.
-// Per step the MMA issuer runs S^T (as soon as Q has landed), dP^T (once dO has landed
-// and the previous dQ has been read), then dK, dV and dQ: dK and dV release Q and dO so
-// that the next step's loads overlap the dQ product and its epilogue.
+//   warp 19    idle
+// TMEM: S^T [0,128) (then P^T), dP^T [128,256) (then dS^T, then dQ), dV [256,256+d),
+// dK [384,384+d).  P^T and dS^T are written back as packed 16-bit pairs, each 32-query
+// quarter over the first 16 of its own 32 fp32 source columns, and feed the dV and dK MMAs
+// from TMEM; dS is also written to shared memory (queries contiguous, the MN-major A
+// operand of the dQ MMA).  Each step's dQ tile goes through shared memory to TMA bulk
+// reduce-adds into an fp32 accumulator; the deterministic order (counters per query block)
+// is a separate kernel instance.
+// Per step the compute warps compute P^T as soon as S^T lands and dS^T once dP^T lands; the
+// MMA issuer runs S^T (as soon as Q has landed), dP^T (once dO has landed and the previous
+// dQ has been read), then dK, dV and dQ: dK and dV release Q and dO so that the next step's
+// loads overlap the dQ product and its epilogue.
+// Head dimensions 136..256: bwd_wide_kernel, described before its code below.
 #include <climits>
 #include <cmath>
 
@@ -50,6 +53,8 @@ namespace {
 
 constexpr int BKEY = 128;         // keys per unit
 constexpr int BQ = 128;           // queries per step
+// The d 136..256 kernel (bwd_wide_kernel): 384 threads, two compute warpgroups with a
+// register split, warp 8 the producer, 9 the MMA issuer, 10 the dQ issuer, 11 idle.
 constexpr int NTHREADS = 384;
 constexpr int NCOMPUTE = 256;
 constexpr int COMPUTE_REGS = 200;  // 2 x 128 threads x 200
