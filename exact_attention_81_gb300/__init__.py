@@ -26,6 +26,8 @@ from ._binding import (  # noqa: F401
     fa_fwd,
     fa_fwd_fp8,
     fa_fwd_fp8_workspace_size,
+    fa_fwd_varlen_fp8,
+    fa_fwd_varlen_fp8_workspace_size,
     fa_fwd_kvcache_fp8,
     fa_fwd_host,
     fa_fwd_kvcache,

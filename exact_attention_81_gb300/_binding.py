@@ -172,6 +172,11 @@ def load_library(path: str | None = None):
         lib.fa_fwd_fp8_workspace_size.restype = sz
         lib.fa_fwd_fp8.argtypes = [ctypes.POINTER(FwdParams), vp, vp, vp, vp, sz, vp]
         lib.fa_fwd_fp8.restype = i
+        lib.fa_fwd_varlen_fp8_workspace_size.argtypes = [i, i, i, i]
+        lib.fa_fwd_varlen_fp8_workspace_size.restype = sz
+        lib.fa_fwd_varlen_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f,
+                                          i, pmod, vp, vp, vp, vp, sz, vp]
+        lib.fa_fwd_varlen_fp8.restype = i
         lib.fa_fwd_params_size.argtypes = []
         lib.fa_fwd_params_size.restype = sz
         lib.fa_bwd.argtypes = [ctypes.POINTER(BwdParams), vp]
@@ -389,6 +394,66 @@ def fa_fwd_fp8(q, k, v, causal: bool = False, scale: float | None = None, q_desc
     st = load_library().fa_fwd_fp8(ctypes.byref(p), *ptrs, _ptr(workspace), workspace.numel(),
                                    _stream_handle(stream))
     _check(st, "fa_fwd_fp8")
+    return out, lse
+
+
+def fa_fwd_varlen_fp8_workspace_size(B: int, total_k: int, Hkv: int, d: int) -> int:
+    return int(load_library().fa_fwd_varlen_fp8_workspace_size(B, total_k, Hkv, d))
+
+
+def fa_fwd_varlen_fp8(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
+                      max_seqlen_k: int, causal: bool = False, scale: float | None = None,
+                      q_descale=None, k_descale=None, v_descale=None, out=None, lse=None,
+                      workspace=None, stream=None, window_size=None, softcap: float = 0.0,
+                      alibi_slopes=None):
+    """FP8 attention over packed sequences.  q [total_q,Hq,d], k/v [total_k,Hkv,d]
+    torch.float8_e4m3fn (CUDA, contiguous), cu_seqlens int32 [B+1], d a multiple of 16 up
+    to 128; q/k/v_descale fp32 [B, Hkv] CUDA tensors or None (= 1).
+    Returns (out [total_q,Hq,d] bf16, lse [Hq,total_q] fp32)."""
+    f8 = torch.float8_e4m3fn
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != f8 or not t.is_cuda or t.dim() != 3 or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous 3-D torch.float8_e4m3fn CUDA tensor")
+    for name, t in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous int32 CUDA tensor")
+    total_q, Hq, d = q.shape
+    total_k, Hkv = k.shape[0], k.shape[1]
+    if tuple(k.shape) != (total_k, Hkv, d) or tuple(v.shape) != (total_k, Hkv, d):
+        raise ValueError("k and v must be [total_k, Hkv, d] matching q")
+    B = cu_seqlens_q.numel() - 1
+    if cu_seqlens_k.numel() != B + 1:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must have the same length")
+    keep = []
+    ptrs = []
+    for name, t in (("q_descale", q_descale), ("k_descale", k_descale), ("v_descale", v_descale)):
+        if t is None:
+            ptrs.append(None)
+            continue
+        if t.dtype != torch.float32 or not t.is_cuda or t.numel() != B * Hkv:
+            raise TypeError(f"{name} must be an fp32 CUDA tensor of B * Hkv elements")
+        t = t.contiguous()
+        keep.append(t)
+        ptrs.append(_ptr(t))
+    if out is None:
+        out = torch.empty((total_q, Hq, d), dtype=torch.bfloat16, device=q.device)
+    elif out.dtype != torch.bfloat16 or tuple(out.shape) != (total_q, Hq, d) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 [total_q, Hq, d] tensor")
+    if lse is None:
+        lse = torch.empty((Hq, total_q), dtype=torch.float32, device=q.device)
+    elif lse.dtype != torch.float32 or tuple(lse.shape) != (Hq, total_q) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [Hq, total_q] tensor")
+    need = fa_fwd_varlen_fp8_workspace_size(B, total_k, Hkv, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    sc = default_scale(d) if scale is None else float(scale)
+    mod = _score_mod(B, Hq, q.device, window_size, softcap, alibi_slopes)
+    st = load_library().fa_fwd_varlen_fp8(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+        B, int(max_seqlen_q), int(max_seqlen_k), total_q, total_k, Hq, Hkv, d, sc,
+        int(bool(causal)), ctypes.byref(mod), *ptrs, _ptr(workspace), workspace.numel(),
+        _stream_handle(stream))
+    _check(st, "fa_fwd_varlen_fp8")
     return out, lse
 
 

@@ -375,6 +375,44 @@ bool stride_ok_16b(int64_t s, int64_t extent) {
 fa_status launch_dense(const fa_fwd_params &a, DeviceInfo *dev, const ModPlan &mod,
                        int64_t lse_sb, int64_t lse_sh, cudaStream_t stream);
 
+// Prefill arguments of packed sequences (o [total_q, Hq, d], lse [Hq, total_q]).
+fa::PrefillArgs varlen_args(void *o, float *lse, const int *cu_q, const int *cu_k, int B,
+                            int max_seqlen_q, int max_seqlen_k, int total_q, int total_k, int Hq,
+                            int Hkv, int d, float scale, int mblocks, int64_t tiles,
+                            DeviceInfo *dev, const ModPlan &mod) {
+  fa::PrefillArgs pa{};
+  pa.o = o;
+  pa.lse = lse;
+  pa.o_sb = 0;
+  pa.o_sn = static_cast<int64_t>(Hq) * d;
+  pa.o_sh = d;
+  pa.lse_sb = 0;
+  pa.lse_sh = total_q;
+  pa.B = B;
+  pa.Hq = Hq;
+  pa.Hkv = Hkv;
+  pa.group = Hq / Hkv;
+  pa.Nq = max_seqlen_q;
+  pa.Nk = max_seqlen_k;
+  pa.varlen = 1;
+  pa.cu_q = cu_q;
+  pa.cu_k = cu_k;
+  pa.total_q = total_q;
+  pa.total_k = total_k;
+  pa.mblocks = mblocks;
+  pa.num_tiles = static_cast<int>(tiles);
+  pa.half_from = pa.num_tiles;
+  pa.num_tickets = pa.num_tiles;
+  pa.scale_log2 = scale_log2(scale);
+  pa.err = dev->err;
+  pa.timeout_ns = g_timeout_ns;
+  pa.inject = g_inject;
+  pa.sched_slot = fa::next_prefill_sched_slot();
+  pa.d = d;
+  apply_mod(mod, scale, &pa);
+  return pa;
+}
+
 // Prefill arguments of a dense call (fa_fwd, fa_fwd_fp8).
 fa::PrefillArgs dense_args(const fa_fwd_params &a, int mblocks, int64_t tiles,
                            const DeviceInfo *dev, const ModPlan &mod, int64_t lse_sb,
@@ -556,6 +594,83 @@ fa_status fa_fwd_fp8(const fa_fwd_params *p, const float *q_descale, const float
   if (e != cudaSuccess) return cuda_fail("V transpose launch", e);
   fa::PrefillArgs pa = dense_args(a, mblocks, tiles, dev, mod, static_cast<int64_t>(a.Hq) * a.Nq,
                                   a.Nq);
+  pa.q_descale = q_descale;
+  pa.k_descale = k_descale;
+  pa.v_descale = v_descale;
+  const int grid = static_cast<int>(tiles < dev->sm_count ? tiles : dev->sm_count);
+  e = fa::launch_prefill_fp8(mod.mask, tq, tk, tvt, pa, grid, stream);
+  return e == cudaSuccess ? FA_OK : cuda_fail("prefill kernel launch", e);
+}
+
+// Columns of the varlen transposed V: sequence b's keys start at roundup16(cu_k[b]) + 16 b.
+int64_t vt_cols_varlen(int B, int64_t total_k) { return nk_pad16(total_k) + 16 * (B + 1ll); }
+
+size_t fa_fwd_varlen_fp8_workspace_size(int B, int total_k, int Hkv, int d) {
+  if (B <= 0 || total_k <= 0 || Hkv <= 0 || d <= 0) return 0;
+  const int64_t bytes = static_cast<int64_t>(Hkv) * d * vt_cols_varlen(B, total_k);
+  return static_cast<size_t>((bytes + 255) / 256 * 256);
+}
+
+fa_status fa_fwd_varlen_fp8(const void *q, const void *k, const void *v, void *o, float *lse,
+                            const int *cu_seqlens_q, const int *cu_seqlens_k, int B,
+                            int max_seqlen_q, int max_seqlen_k, int total_q, int total_k, int Hq,
+                            int Hkv, int d, float scale, int causal, const fa_score_mod *mod_in,
+                            const float *q_descale, const float *k_descale,
+                            const float *v_descale, void *workspace, size_t workspace_bytes,
+                            cudaStream_t stream) {
+  if (B < 0 || B > 65535 || max_seqlen_q < 0 || max_seqlen_k < 0 || total_q < 0 ||
+      total_k < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0)
+    return FA_ERR_INVALID_ARG;
+  if (d < 16 || d > 128 || d % 16 != 0) return FA_ERR_UNSUPPORTED;
+  if (!scale_ok(scale)) return FA_ERR_INVALID_ARG;
+  if (max_seqlen_q > (1 << 30) || total_q > (1 << 30) || total_k > (1 << 30))
+    return FA_ERR_INVALID_ARG;
+  if (B == 0 || total_q == 0 || max_seqlen_q == 0) return FA_OK;
+  if (q == nullptr || o == nullptr || lse == nullptr || cu_seqlens_q == nullptr ||
+      cu_seqlens_k == nullptr)
+    return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(o, 16) || !aligned(lse, 4) || !aligned(cu_seqlens_q, 4) ||
+      !aligned(cu_seqlens_k, 4))
+    return FA_ERR_INVALID_ARG;
+  for (const float *ds : {q_descale, k_descale, v_descale})
+    if (ds != nullptr && !aligned(ds, 4)) return FA_ERR_INVALID_ARG;
+  if (total_k > 0) {
+    if (k == nullptr || v == nullptr || !aligned(k, 16) || !aligned(v, 16))
+      return FA_ERR_INVALID_ARG;
+    const size_t need = fa_fwd_varlen_fp8_workspace_size(B, total_k, Hkv, d);
+    if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256))
+      return FA_ERR_WORKSPACE;
+  }
+  const int mblocks = ceil_div(max_seqlen_q, fa::prefill_tile_rows(128));
+  const int64_t tiles = static_cast<int64_t>(B) * Hq * mblocks;
+  if (tiles > INT32_MAX) return FA_ERR_INVALID_ARG;
+  ModPlan mod;
+  fa_status st = plan_mod(mod_in, causal, &mod);
+  if (st != FA_OK) return st;
+
+  DeviceInfo *dev = nullptr;
+  st = current_device(&dev);
+  if (st != FA_OK) return st;
+  if (total_k == 0) {
+    cudaError_t e = fa::launch_fill_empty(o, lse, 1, total_q, Hq, d, 0,
+                                          static_cast<int64_t>(Hq) * d, d, 0, total_q, stream);
+    return e == cudaSuccess ? FA_OK : cuda_fail("fill kernel launch", e);
+  }
+  const int64_t nt = vt_cols_varlen(B, total_k);
+  if (nt > INT32_MAX) return FA_ERR_INVALID_ARG;
+  CUtensorMap tq, tk, tvt;
+  if ((st = make_map(&tq, q, d, total_q, Hq, 1, static_cast<int64_t>(Hq) * d, d, 0,
+                     FA_E4M3)) != FA_OK ||
+      (st = make_map(&tk, k, d, total_k, Hkv, 1, static_cast<int64_t>(Hkv) * d, d, 0,
+                     FA_E4M3)) != FA_OK ||
+      (st = make_map_vt(&tvt, workspace, static_cast<int>(nt), d, Hkv, 1)) != FA_OK)
+    return st;
+  cudaError_t e = fa::launch_transpose_v_varlen(v, workspace, cu_seqlens_k, B, max_seqlen_k,
+                                                total_k, Hkv, d, static_cast<int>(nt), stream);
+  if (e != cudaSuccess) return cuda_fail("V transpose launch", e);
+  fa::PrefillArgs pa = varlen_args(o, lse, cu_seqlens_q, cu_seqlens_k, B, max_seqlen_q,
+                                   max_seqlen_k, total_q, total_k, Hq, Hkv, d, scale, mblocks,
+                                   tiles, dev, mod);
   pa.q_descale = q_descale;
   pa.k_descale = k_descale;
   pa.v_descale = v_descale;
@@ -759,36 +874,9 @@ fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, fl
   if ((st = make_map(&tv, v, d, total_k, Hkv, 1, static_cast<int64_t>(Hkv) * d, d, 0, dtype)) !=
       FA_OK)
     return st;
-  fa::PrefillArgs pa{};
-  pa.o = o;
-  pa.lse = lse;
-  pa.o_sb = 0;
-  pa.o_sn = o_sn;
-  pa.o_sh = o_sh;
-  pa.lse_sb = 0;
-  pa.lse_sh = total_q;
-  pa.B = B;
-  pa.Hq = Hq;
-  pa.Hkv = Hkv;
-  pa.group = Hq / Hkv;
-  pa.Nq = max_seqlen_q;
-  pa.Nk = max_seqlen_k;
-  pa.varlen = 1;
-  pa.cu_q = cu_seqlens_q;
-  pa.cu_k = cu_seqlens_k;
-  pa.total_q = total_q;
-  pa.total_k = total_k;
-  pa.mblocks = mblocks;
-  pa.num_tiles = static_cast<int>(tiles);
-  pa.half_from = pa.num_tiles;
-  pa.num_tickets = pa.num_tiles;
-  pa.scale_log2 = scale_log2(scale);
-  pa.err = dev->err;
-  pa.timeout_ns = g_timeout_ns;
-  pa.inject = g_inject;
-  pa.sched_slot = fa::next_prefill_sched_slot();
-  pa.d = d;
-  apply_mod(mod, scale, &pa);
+  fa::PrefillArgs pa = varlen_args(o, lse, cu_seqlens_q, cu_seqlens_k, B, max_seqlen_q,
+                                   max_seqlen_k, total_q, total_k, Hq, Hkv, d, scale, mblocks,
+                                   tiles, dev, mod);
   cudaError_t e;
   if (pairs) {
     e = fa::launch_prefill_pair(mod.mask, dtype == FA_FP16, tq, tk, tv, pa,

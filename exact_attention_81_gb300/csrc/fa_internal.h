@@ -90,7 +90,8 @@ cudaError_t launch_prefill_pair(int mask, bool f16, const CUtensorMap &tq, const
                                 cudaStream_t stream);
 
 // FP8 (E4M3) prefill, d <= 128 at kernel width 128: tq, tk over E4M3 Q and K, tvt over the
-// transposed V written by launch_transpose_v (dims {keys, d, kv head, batch}).
+// transposed V written by launch_transpose_v (dims {keys, d, kv head, batch}) or, packed
+// sequences (a.varlen), by launch_transpose_v_varlen (dims {nt, d, kv head, 1}).
 cudaError_t launch_prefill_fp8(int mask, const CUtensorMap &tq, const CUtensorMap &tk,
                                const CUtensorMap &tvt, const PrefillArgs &a, int grid,
                                cudaStream_t stream);
@@ -99,6 +100,13 @@ cudaError_t launch_prefill_fp8(int mask, const CUtensorMap &tq, const CUtensorMa
 // contiguous, zeros in the columns [Nk, nk_pad).
 cudaError_t launch_transpose_v(const void *v, int64_t v_sb, int64_t v_sn, int64_t v_sh, void *vt,
                                int B, int Nk, int Hkv, int d, int nk_pad, cudaStream_t stream);
+
+// Packed sequences: V [total_k, Hkv, d] E4M3 (contiguous) -> V^T [Hkv, d, nt] after zeroing
+// it, sequence b's keys at columns roundup16(cu_k[b]) + 16 b onwards; nt >= roundup16(total_k)
+// + 16 (B + 1), a multiple of 16.
+cudaError_t launch_transpose_v_varlen(const void *v, void *vt, const int *cu_k, int B,
+                                      int max_seqlen_k, int total_k, int Hkv, int d, int nt,
+                                      cudaStream_t stream);
 
 // O = 0 and LSE = -inf for every row (no visible keys anywhere).
 cudaError_t launch_fill_empty(void *o, float *lse, int B, int N, int H, int d, int64_t o_sb,

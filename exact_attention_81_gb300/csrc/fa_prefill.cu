@@ -458,10 +458,13 @@ __device__ void producer_role(const PrefillArgs &a, const CUtensorMap *tmq,
            load_slot(tmv, 2, 2, ti.hk, krow + (n - 1) * kst, ti.tma_b);
       if (!ok) goto out;
     } else if constexpr (F8) {
-      // V^T rows start at the sequence's first key (dense only: k_tok = 0).
+      // V^T columns of the sequence's keys: from column 0 per batch entry (dense), or, packed
+      // sequences, from the 16-aligned column roundup16(first token) + 16 b that the varlen
+      // transpose gives sequence b (a TMA box must start on a 16-byte boundary).
+      const int vrow = (a.varlen ? ((ti.k_tok + 15) & ~15) + 16 * ti.b : 0) + ti.kt_first * BC;
       for (int j = 0; j < n; ++j)
         if (!load_slot(tmk, 0, C::KCH, ti.hk, krow + j * kst, ti.tma_b) ||
-            !load_vt(ti.hk, krow + j * kst, ti.tma_b))
+            !load_vt(ti.hk, vrow + j * kst, ti.tma_b))
           goto out;
     } else {
       for (int j = 0; j < n; ++j)
@@ -1629,6 +1632,63 @@ cudaError_t launch_transpose_v(const void *v, int64_t v_sb, int64_t v_sn, int64_
   const dim3 grid((nk_pad + 63) / 64, Hkv, B);
   transpose_v_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint8_t *>(v), v_sb, v_sn, v_sh,
                                               static_cast<uint8_t *>(vt), Nk, Hkv, d, nk_pad);
+  return cudaGetLastError();
+}
+
+// Packed sequences: V [total_k, Hkv, d] E4M3 (contiguous) -> V^T [Hkv, d, nt], sequence b's
+// keys at columns vt0(b) = roundup16(cu_k[b]) + 16 b onwards (16-aligned for the TMA), up to
+// roundup16 of its length; the caller zeroes the buffer first, so the columns between
+// sequences read as 0.  One block per (64-key tile of a sequence, kv head, sequence);
+// sequences with inconsistent prefix sums are skipped (the prefill kernel reports them).
+__global__ void transpose_v_varlen_kernel(const uint8_t *v, uint8_t *vt, const int *cu_k,
+                                          int total_k, int Hkv, int d, int nt) {
+  __shared__ uint8_t tile[64][128 + 4];
+  const int k0 = blockIdx.x * 64, hk = blockIdx.y, b = blockIdx.z;
+  const int s0 = cu_k[b], s1 = cu_k[b + 1];
+  if (s0 < 0 || s1 < s0 || s1 > total_k) return;
+  const int len = s1 - s0;
+  if (k0 >= len) return;
+  const int chunks = d / 16;  // 16-byte chunks per key row
+  const int64_t v_sn = static_cast<int64_t>(Hkv) * d;
+  for (int i = threadIdx.x; i < 64 * chunks; i += blockDim.x) {
+    const int key = i / chunks, c = i - key * chunks;
+    uint4 w = make_uint4(0u, 0u, 0u, 0u);
+    if (k0 + key < len)
+      w = *reinterpret_cast<const uint4 *>(v + static_cast<int64_t>(s0 + k0 + key) * v_sn +
+                                           hk * d + c * 16);
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) tile[key][c * 16 + q * 4 + e] = static_cast<uint8_t>(ws[q] >> (8 * e));
+  }
+  __syncthreads();
+  const int vt0 = ((s0 + 15) & ~15) + 16 * b;
+  uint8_t *out = vt + static_cast<int64_t>(hk) * d * nt + vt0;
+  const int kcols = min(64, ((len + 15) & ~15) - k0);  // multiple of 16
+  for (int i = threadIdx.x; i < d * (kcols / 16); i += blockDim.x) {
+    const int row = i / (kcols / 16), c = i - row * (kcols / 16);
+    uint32_t ws[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      ws[q] = static_cast<uint32_t>(tile[c * 16 + q * 4][row]) |
+              (static_cast<uint32_t>(tile[c * 16 + q * 4 + 1][row]) << 8) |
+              (static_cast<uint32_t>(tile[c * 16 + q * 4 + 2][row]) << 16) |
+              (static_cast<uint32_t>(tile[c * 16 + q * 4 + 3][row]) << 24);
+    *reinterpret_cast<uint4 *>(out + static_cast<int64_t>(row) * nt + k0 + c * 16) =
+        make_uint4(ws[0], ws[1], ws[2], ws[3]);
+  }
+}
+
+cudaError_t launch_transpose_v_varlen(const void *v, void *vt, const int *cu_k, int B,
+                                      int max_seqlen_k, int total_k, int Hkv, int d, int nt,
+                                      cudaStream_t stream) {
+  cudaError_t e = cudaMemsetAsync(vt, 0, static_cast<size_t>(Hkv) * d * nt, stream);
+  if (e != cudaSuccess || B == 0 || max_seqlen_k == 0) return e;
+  const dim3 grid((max_seqlen_k + 63) / 64, Hkv, B);
+  transpose_v_varlen_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint8_t *>(v),
+                                                      static_cast<uint8_t *>(vt), cu_k, total_k,
+                                                      Hkv, d, nt);
   return cudaGetLastError();
 }
 

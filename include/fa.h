@@ -410,7 +410,8 @@ size_t fa_fwd_params_size(void);
  * fp32 device arrays [B, Hkv] (contiguous), each may be NULL (= 1).  So S = scale *
  * (dq dk) Q K^T and O = dv softmax(S) V.  P is rounded to E4M3 for the P V product; the
  * row sums and the LSE use the unrounded fp32 P.  The score modifiers (p->mod) and causal
- * apply as in fa_fwd.  d: a multiple of 16 up to 128.  Dense inputs only.
+ * apply as in fa_fwd.  d: a multiple of 16 up to 128.  Dense inputs (packed sequences:
+ * fa_fwd_varlen_fp8).
  * workspace: device memory of at least fa_fwd_fp8_workspace_size(B, Nk, Hkv, d) bytes,
  * 256-byte aligned, for the transposed V (written by the call, no content needed).
  * Errors as fa_fwd; FA_ERR_WORKSPACE when the workspace is missing or too small.
@@ -419,6 +420,28 @@ size_t fa_fwd_fp8_workspace_size(int B, int Nk, int Hkv, int d);
 fa_status fa_fwd_fp8(const fa_fwd_params *p, const float *q_descale, const float *k_descale,
                      const float *v_descale, void *workspace, size_t workspace_bytes,
                      cudaStream_t stream);
+
+/*
+ * FP8 forward over packed sequences: the computation of fa_fwd_fp8 with the layout and the
+ * sequence handling of fa_fwd_varlen.  q [total_q, Hq, d], k, v [total_k, Hkv, d], E4M3,
+ * contiguous; o [total_q, Hq, d] bf16 and lse [Hq, total_q] fp32 as in fa_fwd_varlen;
+ * cu_seqlens_q / cu_seqlens_k, B, max_seqlen_q / max_seqlen_k, causal (bottom-right aligned
+ * per sequence) and mod as in fa_fwd_varlen.  q/k/v_descale: fp32 device arrays [B, Hkv],
+ * one factor per (sequence, kv head), each may be NULL (= 1).  d: a multiple of 16 up to
+ * 128; B <= 65535.
+ * workspace: device memory of at least fa_fwd_varlen_fp8_workspace_size(B, total_k, Hkv, d)
+ * bytes, 256-byte aligned, for the transposed V (each sequence's keys from a 16-aligned
+ * column; written by the call, no content needed).
+ * Errors as fa_fwd_varlen; FA_ERR_WORKSPACE when the workspace is missing or too small.
+ */
+size_t fa_fwd_varlen_fp8_workspace_size(int B, int total_k, int Hkv, int d);
+fa_status fa_fwd_varlen_fp8(const void *q, const void *k, const void *v, void *o, float *lse,
+                            const int *cu_seqlens_q, const int *cu_seqlens_k, int B,
+                            int max_seqlen_q, int max_seqlen_k, int total_q, int total_k, int Hq,
+                            int Hkv, int d, float scale, int causal, const fa_score_mod *mod,
+                            const float *q_descale, const float *k_descale,
+                            const float *v_descale, void *workspace, size_t workspace_bytes,
+                            cudaStream_t stream);
 
 /* Static text for a status code. */
 const char *fa_status_string(fa_status s);

@@ -1,5 +1,5 @@
-"""GPU parity of the FP8 forward (fa_fwd_fp8: E4M3 Q, K, V with per-(batch, kv head)
-descale factors, bf16 O) and of the decode call over E4M3 caches (fa_fwd_kvcache_fp8)
+"""GPU parity of the FP8 forward (fa_fwd_fp8 and, over packed sequences, fa_fwd_varlen_fp8:
+E4M3 Q, K, V with per-(batch, kv head) descale factors, bf16 O) and of the decode call over E4M3 caches (fa_fwd_kvcache_fp8)
 against the fp64 oracle.
 
 The pages fix no tolerance for FP8.  The bar is their own test criterion ("flash-attention",
@@ -16,7 +16,7 @@ import pytest
 import torch
 
 import oracle.oracle as ORACLE
-from exact_attention_81_gb300 import FA_OK, fa_fwd_fp8, get_last_device_error
+from exact_attention_81_gb300 import FA_OK, fa_fwd_fp8, fa_fwd_varlen_fp8, get_last_device_error
 from exact_attention_81_gb300.inputs import fp8_inputs
 
 pytestmark = pytest.mark.gpu
@@ -102,6 +102,79 @@ def test_fp8_no_descales():
                                  dict(window_size=(100, 30), softcap=5.0)])
 def test_fp8_modifiers(mod):
     _check(2, 600, 600, 4, 2, 128, False, seed=23, what=f"fp8 {mod}", **mod)
+
+
+def _varlen_fp8(sq, sk, Hq, Hkv, d, causal, seed, **mod):
+    """Packed sequences through fa_fwd_varlen_fp8, each sequence checked under the bar of
+    _check against the dense FP8 oracle of that sequence alone.  Returns the per-sequence
+    inputs and outputs."""
+    per = [fp8_inputs(1, nq, nk, Hq, Hkv, d, seed + b, device=DEV) for b, (nq, nk) in
+           enumerate(zip(sq, sk))]
+    q = torch.cat([t[0][0] for t in per]).contiguous()
+    k = torch.cat([t[1][0] for t in per]).contiguous()
+    v = torch.cat([t[2][0] for t in per]).contiguous()
+    dq, dk, dv = (torch.cat([t[i] for t in per]).contiguous() for i in (3, 4, 5))
+    cu_q = torch.tensor([0] + list(np.cumsum(sq)), dtype=torch.int32, device=DEV)
+    cu_k = torch.tensor([0] + list(np.cumsum(sk)), dtype=torch.int32, device=DEV)
+    scale = float(np.float32(1 / math.sqrt(d)))
+    o, lse = fa_fwd_varlen_fp8(q, k, v, cu_q, cu_k, max(sq), max(sk), causal=causal,
+                               scale=scale, q_descale=dq, k_descale=dk, v_descale=dv, **mod)
+    assert get_last_device_error() == FA_OK
+    window = mod.get("window_size", (-1, -1))
+    softcap = mod.get("softcap", 0.0)
+    for b, (nq, nk) in enumerate(zip(sq, sk)):
+        qb, kb, vb, dqb, dkb, dvb = per[b]
+        ob = o[int(cu_q[b]):int(cu_q[b + 1])].double().cpu().numpy()[None]
+        lb = lse[:, int(cu_q[b]):int(cu_q[b + 1])].double().cpu().numpy()[None]
+        if nq == 0:
+            continue
+        if nk == 0:
+            assert np.all(ob == 0) and np.all(lb == -np.inf), f"sequence {b}: empty keys"
+            continue
+        o_ref, lse_ref = ORACLE.attention_fp8(qb.cpu(), kb.cpu(), vb.cpu(), scale, causal,
+                                              dqb.cpu(), dkb.cpu(), dvb.cpu(), window=window,
+                                              softcap=softcap)
+        base = _baseline(qb, kb, vb, dqb, dkb, dvb, scale, causal, window, softcap)
+        what = f"varlen fp8 sequence {b} ({nq} x {nk})"
+        assert np.all(np.isfinite(ob)), f"{what}: non-finite O"
+        e_gpu, e_base = np.abs(ob - o_ref), np.abs(base - o_ref)
+        assert e_gpu.max() <= 2 * e_base.max() + 1e-4, \
+            f"{what}: max |dO| {e_gpu.max():.3e} > 2 x baseline {e_base.max():.3e}"
+        assert e_gpu.mean() <= 2 * e_base.mean() + 1e-4, \
+            f"{what}: mean |dO| {e_gpu.mean():.3e} > 2 x baseline {e_base.mean():.3e}"
+        fin = np.isfinite(lse_ref)
+        assert np.array_equal(np.isfinite(lb), fin), f"{what}: LSE finiteness"
+        assert np.abs(lb[fin] - lse_ref[fin]).max(initial=0.0) <= 1e-3, f"{what}: LSE"
+    return per, o, lse
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_varlen(causal):
+    # sequence starts that are not multiples of 16 (the transposed V gives each its own
+    # 16-aligned column), an empty key range, Nq != Nk within a sequence, GQA
+    _varlen_fp8([37, 1, 300, 129, 64, 200], [37, 0, 333, 129, 17, 450], 4, 2, 128, causal,
+                seed=1900)
+
+
+@pytest.mark.parametrize("d", [64, 96])
+def test_fp8_varlen_head_dims(d):
+    _varlen_fp8([100, 257, 3], [150, 257, 40], 2, 1, d, True, seed=1910 + d)
+
+
+def test_fp8_varlen_window():
+    _varlen_fp8([300, 45, 512], [300, 90, 700], 4, 4, 128, False, seed=1920,
+                window_size=(100, 20))
+
+
+def test_fp8_varlen_one_sequence_equals_dense():
+    """One sequence: the same kernel over the same K / V tiles as fa_fwd_fp8, bit for bit."""
+    per, o, lse = _varlen_fp8([333], [517], 4, 2, 128, True, seed=1930)
+    q, k, v, dq, dk, dv = per[0]
+    scale = float(np.float32(1 / math.sqrt(128)))
+    o_d, lse_d = fa_fwd_fp8(q, k, v, causal=True, scale=scale, q_descale=dq, k_descale=dk,
+                            v_descale=dv)
+    assert torch.equal(o, o_d[0]), "varlen O differs from the dense call"
+    assert torch.equal(lse, lse_d[0]), "varlen LSE differs from the dense call"
 
 
 def test_fp8_empty_keys_and_rows_without_keys():
