@@ -281,6 +281,34 @@ def test_fp8_rejects_bad_arguments(lib):
     assert lib.fa_fwd_fp8_workspace_size(0, 10, 2, 128) == 0
 
 
+def test_varlen_fp8_rejects_bad_arguments(lib):
+    """fa_fwd_varlen_fp8 validates before any CUDA call: d a multiple of 16 up to 128, at
+    most 65535 sequences, aligned pointers, a large enough 256-byte-aligned workspace (the
+    transposed V with every sequence from a 16-aligned column)."""
+    B, total_q, total_k, Hq, Hkv, d = 3, 500, 700, 4, 2, 128
+
+    def call(ws=4096, wsb=1 << 30, **kw):
+        a = dict(q=4096, k=4096, v=4096, o=4096, lse=4096, cu_q=4096, cu_k=4096, B=B,
+                 max_q=300, max_k=400, total_q=total_q, total_k=total_k, Hq=Hq, Hkv=Hkv, d=d)
+        a.update(kw)
+        return lib.fa_fwd_varlen_fp8(a["q"], a["k"], a["v"], a["o"], a["lse"], a["cu_q"],
+                                     a["cu_k"], a["B"], a["max_q"], a["max_k"], a["total_q"],
+                                     a["total_k"], a["Hq"], a["Hkv"], a["d"], 0.088, 1, None,
+                                     None, None, None, ws, wsb, None)
+
+    assert call(d=120) == 2 and call(d=144) == 2 and call(d=8) == 2
+    assert call(B=70000) == 1                      # more sequences than a grid dimension
+    assert call(Hq=3) == 1                         # Hq not a multiple of Hkv
+    assert call(k=4104) == 1 and call(cu_k=4098) == 1   # misaligned pointers
+    assert call(ws=None) == 4
+    need = lib.fa_fwd_varlen_fp8_workspace_size(B, total_k, Hkv, d)
+    assert need == ((Hkv * d * (704 + 16 * (B + 1)) + 255) // 256) * 256
+    assert call(wsb=need - 1) == 4
+    assert call(ws=4096 + 128) == 4                # workspace not 256-byte aligned
+    assert call(B=0) == 0 and call(total_q=0) == 0     # nothing to do
+    assert lib.fa_fwd_varlen_fp8_workspace_size(0, 10, 2, 128) == 0
+
+
 def test_host_call_rejects_bad_arguments(lib):
     """fa_fwd_host validates before any CUDA call: 1..64 ranges, contiguous layouts, device
     buffers present and aligned."""
