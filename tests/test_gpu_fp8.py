@@ -166,6 +166,10 @@ def test_fp8_varlen_window():
                 window_size=(100, 20))
 
 
+def test_fp8_varlen_softcap():
+    _varlen_fp8([130, 7, 400], [260, 7, 400], 4, 2, 128, True, seed=1925, softcap=10.0)
+
+
 def test_fp8_varlen_one_sequence_equals_dense():
     """One sequence: the same kernel over the same K / V tiles as fa_fwd_fp8, bit for bit."""
     per, o, lse = _varlen_fp8([333], [517], 4, 2, 128, True, seed=1930)
