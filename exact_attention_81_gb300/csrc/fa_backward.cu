@@ -62,7 +62,6 @@ constexpr int OTHER_REGS = 96;     //   + 128 threads x 96 <= 384 threads x 168 
 constexpr int PRODUCER_WARP = 8;
 constexpr int DQ_WARP = 10;       // issues the dQ reduce-adds
 constexpr int MMA_WARP = 9;
-constexpr int HEAD_GROUP = 8;     // (batch, kv head) pairs per unit group
 // The d <= 128 kernel (bwd_kernel): 16 compute warps, four per TMEM lane quarter (warp w:
 // lanes 32 (w % 4) .. +31, queries 32 (w / 4) .. +31 of a step), 640 threads, no register
 // split; warp 16 is the producer, 17 the MMA issuer, 18 the dQ issuer, 19 idle.
@@ -117,12 +116,12 @@ struct BUnit {
 template <int MASK, int QB = BQ>
 __device__ __forceinline__ BUnit bunit_of(const BwdArgs &a, int u) {
   BUnit w;
-  // Units run in groups of HEAD_GROUP (batch, kv head) pairs, key-block-major inside a
+  // Units run in groups of a.head_group (batch, kv head) pairs, key-block-major inside a
   // group: the CTAs running together then add dQ into a few heads' accumulators (4 MB
   // each at N = 8192, d = 128), which stay in L2, and causal work still mixes short and
-  // long key blocks (measured: 737 against 706 TFLOPS with all heads key-block-major).
+  // long key blocks.
   const int bg = a.B * a.Hkv;
-  const int S = HEAD_GROUP < bg ? HEAD_GROUP : bg;
+  const int S = a.head_group < bg ? a.head_group : bg;
   const int per = a.kblocks * S;
   const int grp = u / per;
   const int rem = u - grp * per;

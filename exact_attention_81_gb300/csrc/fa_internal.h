@@ -221,6 +221,7 @@ struct BwdArgs {
   const float *alibi;
   int64_t alibi_sb;
   int num_units;              // kblocks * B * Hkv
+  int head_group;             // (batch, kv head) pairs per unit group, >= 1
   float scale, scale_log2;
   unsigned int *err;
   unsigned long long timeout_ns;
