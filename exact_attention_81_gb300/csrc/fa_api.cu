@@ -521,8 +521,11 @@ fa_status launch_dense(const fa_fwd_params &a, DeviceInfo *dev, const ModPlan &m
       pa.half_from = static_cast<int>(tiles - tiles % grid);
       pa.num_tickets = pa.half_from + 2 * static_cast<int>(tiles % grid);
     }
-    e = fa::launch_prefill(fa::kernel_d(a.d), mod.mask, a.dtype == FA_FP16, tq, tk, tv, pa, grid,
-                           stream);
+    CUtensorMap to;
+    pa.o_tma = make_map(&to, a.o, a.d, a.Nq, a.Hq, a.B, a.o_strides[1], a.o_strides[2],
+                        a.o_strides[0], a.dtype, 32) == FA_OK;
+    e = fa::launch_prefill(fa::kernel_d(a.d), mod.mask, a.dtype == FA_FP16, tq, tk, tv,
+                           pa.o_tma ? &to : nullptr, pa, grid, stream);
   }
   return e == cudaSuccess ? FA_OK : cuda_fail("prefill kernel launch", e);
 }
@@ -598,7 +601,10 @@ fa_status fa_fwd_fp8(const fa_fwd_params *p, const float *q_descale, const float
   pa.k_descale = k_descale;
   pa.v_descale = v_descale;
   const int grid = static_cast<int>(tiles < dev->sm_count ? tiles : dev->sm_count);
-  e = fa::launch_prefill_fp8(mod.mask, tq, tk, tvt, pa, grid, stream);
+  CUtensorMap to;
+  pa.o_tma = make_map(&to, a.o, a.d, a.Nq, a.Hq, a.B, a.o_strides[1], a.o_strides[2],
+                      a.o_strides[0], FA_BF16, 32) == FA_OK;
+  e = fa::launch_prefill_fp8(mod.mask, tq, tk, tvt, pa.o_tma ? &to : nullptr, pa, grid, stream);
   return e == cudaSuccess ? FA_OK : cuda_fail("prefill kernel launch", e);
 }
 
@@ -675,7 +681,10 @@ fa_status fa_fwd_varlen_fp8(const void *q, const void *k, const void *v, void *o
   pa.k_descale = k_descale;
   pa.v_descale = v_descale;
   const int grid = static_cast<int>(tiles < dev->sm_count ? tiles : dev->sm_count);
-  e = fa::launch_prefill_fp8(mod.mask, tq, tk, tvt, pa, grid, stream);
+  CUtensorMap to;
+  pa.o_tma = make_map(&to, o, d, total_q, Hq, 1, static_cast<int64_t>(Hq) * d, d, 0, FA_BF16,
+                      32) == FA_OK;
+  e = fa::launch_prefill_fp8(mod.mask, tq, tk, tvt, pa.o_tma ? &to : nullptr, pa, grid, stream);
   return e == cudaSuccess ? FA_OK : cuda_fail("prefill kernel launch", e);
 }
 
@@ -883,8 +892,10 @@ fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, fl
                                 static_cast<int>(tiles), stream);
   } else {
     const int grid = static_cast<int>(tiles < dev->sm_count ? tiles : dev->sm_count);
-    e = fa::launch_prefill(fa::kernel_d(d), mod.mask, dtype == FA_FP16, tq, tk, tv, pa, grid,
-                           stream);
+    CUtensorMap to;
+    pa.o_tma = make_map(&to, o, d, total_q, Hq, 1, o_sn, o_sh, 0, dtype, 32) == FA_OK;
+    e = fa::launch_prefill(fa::kernel_d(d), mod.mask, dtype == FA_FP16, tq, tk, tv,
+                           pa.o_tma ? &to : nullptr, pa, grid, stream);
   }
   return e == cudaSuccess ? FA_OK : cuda_fail("prefill kernel launch", e);
 }

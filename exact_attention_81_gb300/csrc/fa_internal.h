@@ -54,6 +54,10 @@ struct PrefillArgs {
   int kv_rev;                 // stream each block's K/V tiles last-first (ALiBi, right-bounded)
   // FP8 launches: descale factors per (batch, kv head) at [b * Hkv + hk], or null (= 1).
   const float *q_descale, *k_descale, *v_descale;
+  // The launch's O map (32-row boxes) is valid: a softmax warp whose 32 rows all lie in the
+  // sub-tile stages its O rows in shared memory and writes them with TMA stores (kernels of
+  // width <= 128 without ALiBi, single CTAs); other warps store rows directly.
+  int o_tma;
 };
 
 // Masking mode of a prefill launch.
@@ -77,10 +81,11 @@ int next_prefill_sched_slot();
 // Unit-ticket counter slot for the next decode launch (round robin over the slots).
 int next_decode_sched_slot();
 
-// f16: inputs and output are fp16 instead of bf16.
+// f16: inputs and output are fp16 instead of bf16.  tmo: map over O with 32-row boxes
+// (make_map), read when a.o_tma is set; null otherwise.
 cudaError_t launch_prefill(int d, int mask, bool f16, const CUtensorMap &tq,
-                           const CUtensorMap &tk, const CUtensorMap &tv, const PrefillArgs &a,
-                           int grid, cudaStream_t stream);
+                           const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap *tmo,
+                           const PrefillArgs &a, int grid, cudaStream_t stream);
 
 // The width-128 16-bit prefill on CTA pairs (clusters of two computing each 256-row sub-tile
 // as one cta_group::2 product; work tiles of 512 query rows): tk is a K map with 64-row boxes,
@@ -93,8 +98,8 @@ cudaError_t launch_prefill_pair(int mask, bool f16, const CUtensorMap &tq, const
 // transposed V written by launch_transpose_v (dims {keys, d, kv head, batch}) or, packed
 // sequences (a.varlen), by launch_transpose_v_varlen (dims {nt, d, kv head, 1}).
 cudaError_t launch_prefill_fp8(int mask, const CUtensorMap &tq, const CUtensorMap &tk,
-                               const CUtensorMap &tvt, const PrefillArgs &a, int grid,
-                               cudaStream_t stream);
+                               const CUtensorMap &tvt, const CUtensorMap *tmo,
+                               const PrefillArgs &a, int grid, cudaStream_t stream);
 
 // V [B, Nk, Hkv, d] E4M3 (byte strides v_sb, v_sn, v_sh) -> V^T [B, Hkv, d, nk_pad], keys
 // contiguous, zeros in the columns [Nk, nk_pad).

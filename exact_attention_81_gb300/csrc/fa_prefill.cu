@@ -124,11 +124,25 @@ __host__ __device__ constexpr bool abias() {
   return MASK == MASK_ALIBI && !F8 && !PAIR && D <= 128;
 }
 constexpr int ABIAS_BYTES = 2 * BR * 128;
+// Staged O stores (PrefillArgs::o_tma): one 32-row x 64-column box (4 KB, 128-byte swizzled)
+// per softmax warp at STG_OFF, the place of the ALiBi operands, which leave no room for it.
+template <int D, int MASK, bool F8, bool PAIR>
+__host__ __device__ constexpr bool stg_ok() {
+  return !PAIR && D <= 128 && MASK != MASK_ALIBI;
+}
+constexpr int STG_WARP_BYTES = 32 * 128;
+constexpr int STG_BYTES = 8 * STG_WARP_BYTES;
 template <int D, int MASK, bool F16, bool F8, bool PAIR>
 __host__ __device__ constexpr int prefill_smem() {
   using C = Cfg<D, F16, F8, PAIR>;
-  return abias<D, MASK, F8, PAIR>() ? C::BAR_OFF + 1024 + ABIAS_BYTES + 1024 : C::SMEM_BYTES;
+  return abias<D, MASK, F8, PAIR>()    ? C::BAR_OFF + 1024 + ABIAS_BYTES + 1024
+         : stg_ok<D, MASK, F8, PAIR>() ? C::BAR_OFF + 1024 + STG_BYTES + 1024
+                                       : C::SMEM_BYTES;
 }
+static_assert(prefill_smem<128, MASK_CAUSAL, false, false, false>() <= 227 * 1024,
+              "prefill with O staging exceeds shared memory");
+static_assert(prefill_smem<128, MASK_CAUSAL, false, true, false>() <= 227 * 1024,
+              "fp8 prefill with O staging exceeds shared memory");
 static_assert(prefill_smem<128, MASK_ALIBI, false, false, false>() <= 227 * 1024,
               "ALiBi prefill exceeds shared memory");
 
@@ -422,7 +436,24 @@ __device__ void producer_role(const PrefillArgs &a, const CUtensorMap *tmq,
     if (a.varlen && (ti.q_row0 == 0) && varlen_bad(a, ti.b)) atomicOr(a.err, DEVERR_BAD_CU_SEQLENS);
     const int n = max(ti.je[0], ti.je[1]);
     if (n == 0) continue;
-    if (q_iter > 0 && !mbar_wait(&bars->q_empty, (q_iter - 1) & 1u, wc)) goto out;
+    const int krow = ti.k_tok + ti.kt_first * BC;  // K/V row of stream step j: krow + j kst
+    const int kst = ti.kdir * BC;
+    if (q_iter > 0) {
+      // The ticket is taken while the previous tile still has about two steps to run, and
+      // the Q buffer is free only after its last S: pull this tile's Q and first K / V
+      // tiles into L2 now, so that the loads below hit L2 instead of waiting on HBM (where
+      // CTAs with equal-length tiles all fetch their next Q at the same time).
+      for (int t = 0; t < (ti.half ? 1 : C::NSUB); ++t)
+#pragma unroll
+        for (int c = 0; c < C::KCH; ++c)
+          tma_prefetch_4d(tmq, c * C::BOX_ELEMS, ti.h, ti.q_tok + ti.q_row0 + t * BR, ti.tma_b);
+#pragma unroll
+      for (int c = 0; c < C::KCH; ++c) {
+        tma_prefetch_4d(tmk, c * C::BOX_ELEMS, ti.hk, krow, ti.tma_b);
+        if (!F8) tma_prefetch_4d(tmv, c * C::BOX_ELEMS, ti.hk, krow, ti.tma_b);
+      }
+      if (!mbar_wait(&bars->q_empty, (q_iter - 1) & 1u, wc)) goto out;
+    }
     {
       const int nsub = ti.half ? 1 : C::NSUB;
       mbar_arrive_expect_tx(&bars->q_full, nsub * C::TILE_BYTES);
@@ -433,8 +464,6 @@ __device__ void producer_role(const PrefillArgs &a, const CUtensorMap *tmq,
                       c * C::BOX_ELEMS, ti.h, ti.q_tok + ti.q_row0 + t * BR, ti.tma_b);
     }
     ++q_iter;
-    const int krow = ti.k_tok + ti.kt_first * BC;  // K/V row of stream step j: krow + j kst
-    const int kst = ti.kdir * BC;
     if (!C::WIDE && !F8 && ti.half) {
       // half tile: S is double-buffered, so K(j + 1) is needed before V(j): ring order
       // K_0, K_1, V_0, K_2, V_1, ..., V_{n-1}
@@ -998,7 +1027,7 @@ out:
 // scheduler ring are the even CTA's: one arrival per warp, with cluster-scope release.
 template <int D, int MASK, bool F16, bool F8 = false, bool PAIR = false>
 __device__ void softmax_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, uint32_t tmem,
-                             const WaitCtl &wc, int warp, int lane) {
+                             const WaitCtl &wc, int warp, int lane, const CUtensorMap *tmo) {
   using C = Cfg<D, F16, F8, PAIR>;
   const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
   // Arrival on a barrier of the even CTA (after this thread's tcgen05 fences): one per warp
@@ -1316,6 +1345,41 @@ __device__ void softmax_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, ui
       o_phase ^= 1u;
       tc_fence_after();
       const float inv_l = l > 0.f ? vds / (l + lq) : 0.f;  // vds: FP8 V descale, else 1
+      if (stg_ok<D, MASK, F8, PAIR>() && a.o_tma && (wq + 1) * 32 <= nrows) {
+        // The warp's 32 rows go through its staging box, 64 columns at a time, each half
+        // written by one TMA store: rows of 16-byte pieces per thread would cost the
+        // load/store unit 8 x the wavefronts of whole 128-byte lines.  Chunk q (8 columns)
+        // of row r sits at 16-byte position q ^ (r mod 8) (the map's 128-byte swizzle).
+        uint8_t *stg = smem + C::BAR_OFF + 1024 + warp * STG_WARP_BYTES;
+        uint8_t *srow = stg + lane * 128;
+#pragma unroll
+        for (int h = 0; h < D / 64; ++h) {
+          uint32_t r0[32], r1[32];
+          tmem_ld_x32(tO + h * 64, r0);
+          tmem_ld_x32(tO + h * 64 + 32, r1);
+          // The previous store from this box (the last half, or the previous tile's) has
+          // read it.
+          if (lane == 0) bulk_wait_read();
+          __syncwarp();
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const uint32_t *rv = q < 4 ? &r0[8 * q] : &r1[8 * (q - 4)];
+            uint4 w;
+            w.x = pack2<F16>(__uint_as_float(rv[0]) * inv_l, __uint_as_float(rv[1]) * inv_l);
+            w.y = pack2<F16>(__uint_as_float(rv[2]) * inv_l, __uint_as_float(rv[3]) * inv_l);
+            w.z = pack2<F16>(__uint_as_float(rv[4]) * inv_l, __uint_as_float(rv[5]) * inv_l);
+            w.w = pack2<F16>(__uint_as_float(rv[6]) * inv_l, __uint_as_float(rv[7]) * inv_l);
+            *reinterpret_cast<uint4 *>(srow + ((q ^ (lane & 7)) << 4)) = w;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_4d(tmo, stg, h * 64, ti.h, static_cast<int>(ti.q_tok) + first_row + wq * 32,
+                         ti.tma_b);
+            bulk_commit_group();
+          }
+        }
+      } else {
 #pragma unroll
       for (int cc = 0; cc < D; cc += 32) {
         uint32_t r[32];
@@ -1333,6 +1397,7 @@ __device__ void softmax_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, ui
             dst[v] = w;
           }
         }
+      }
       }
       tc_fence_before();
       arrive_leader(&bars->o_empty[t], true);
@@ -1352,7 +1417,8 @@ __device__ void softmax_role(const PrefillArgs &a, uint8_t *smem, Bars *bars, ui
 template <int D, int MASK, bool F16, bool F8 = false, bool PAIR = false>
 __global__ void __launch_bounds__(NTHREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                   const __grid_constant__ CUtensorMap tmv, const PrefillArgs a) {
+                   const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo,
+                   const PrefillArgs a) {
   using C = Cfg<D, F16, F8, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -1438,7 +1504,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(IDLE_REGS));
     } else {
       asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(SOFTMAX_REGS));
-      softmax_role<D, MASK, F16, F8, PAIR>(a, smem, bars, tmem, wc, warp, lane);
+      softmax_role<D, MASK, F16, F8, PAIR>(a, smem, bars, tmem, wc, warp, lane, &tmo);
+      // The staged O stores of this warp have read shared memory and written O.
+      if (stg_ok<D, MASK, F8, PAIR>() && lane == 0) bulk_wait_all();
     }
     __syncwarp();
     tc_fence_before();
@@ -1492,12 +1560,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
 template <int D, int MASK, bool F16, bool F8 = false>
 cudaError_t launch_impl(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                        const PrefillArgs &a, int grid, cudaStream_t stream) {
+                        const CUtensorMap &tmo, const PrefillArgs &a, int grid,
+                        cudaStream_t stream) {
   constexpr int smem = prefill_smem<D, MASK, F16, F8, false>();
   cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, MASK, F16, F8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  prefill_kernel<D, MASK, F16, F8><<<grid, NTHREADS, smem, stream>>>(tq, tk, tv, a);
+  prefill_kernel<D, MASK, F16, F8><<<grid, NTHREADS, smem, stream>>>(tq, tk, tv, tmo, a);
   return cudaGetLastError();
 }
 
@@ -1538,7 +1607,8 @@ cudaError_t launch_pair_impl(const CUtensorMap &tq, const CUtensorMap &tk, const
   }
   const int clusters = tiles < max_clusters[dev] ? tiles : max_clusters[dev];
   cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
-  e = cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, a);
+  const CUtensorMap no_map{};  // pairs store O rows directly
+  e = cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, no_map, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -1573,21 +1643,26 @@ int prefill_smem_bytes(int d) {
 
 template <int D, bool F16, bool F8 = false>
 cudaError_t launch_mask(int mask, const CUtensorMap &tq, const CUtensorMap &tk,
-                        const CUtensorMap &tv, const PrefillArgs &a, int grid,
-                        cudaStream_t stream) {
+                        const CUtensorMap &tv, const CUtensorMap *tmo_in, PrefillArgs a,
+                        int grid, cudaStream_t stream) {
+  const CUtensorMap no_map{};
+  if (tmo_in == nullptr) a.o_tma = 0;
+  const CUtensorMap &tmo = tmo_in != nullptr ? *tmo_in : no_map;
   switch (mask) {
-    case MASK_NONE: return launch_impl<D, MASK_NONE, F16, F8>(tq, tk, tv, a, grid, stream);
-    case MASK_CAUSAL: return launch_impl<D, MASK_CAUSAL, F16, F8>(tq, tk, tv, a, grid, stream);
-    case MASK_WINDOW: return launch_impl<D, MASK_WINDOW, F16, F8>(tq, tk, tv, a, grid, stream);
-    case MASK_ALIBI: return launch_impl<D, MASK_ALIBI, F16, F8>(tq, tk, tv, a, grid, stream);
-    default: return launch_impl<D, MASK_MOD, F16, F8>(tq, tk, tv, a, grid, stream);
+    case MASK_NONE: return launch_impl<D, MASK_NONE, F16, F8>(tq, tk, tv, tmo, a, grid, stream);
+    case MASK_CAUSAL:
+      return launch_impl<D, MASK_CAUSAL, F16, F8>(tq, tk, tv, tmo, a, grid, stream);
+    case MASK_WINDOW:
+      return launch_impl<D, MASK_WINDOW, F16, F8>(tq, tk, tv, tmo, a, grid, stream);
+    case MASK_ALIBI: return launch_impl<D, MASK_ALIBI, F16, F8>(tq, tk, tv, tmo, a, grid, stream);
+    default: return launch_impl<D, MASK_MOD, F16, F8>(tq, tk, tv, tmo, a, grid, stream);
   }
 }
 
 cudaError_t launch_prefill_fp8(int mask, const CUtensorMap &tq, const CUtensorMap &tk,
-                               const CUtensorMap &tvt, const PrefillArgs &a, int grid,
-                               cudaStream_t stream) {
-  return launch_mask<128, false, true>(mask, tq, tk, tvt, a, grid, stream);
+                               const CUtensorMap &tvt, const CUtensorMap *tmo,
+                               const PrefillArgs &a, int grid, cudaStream_t stream) {
+  return launch_mask<128, false, true>(mask, tq, tk, tvt, tmo, a, grid, stream);
 }
 
 // V [B, Nk, Hkv, d] E4M3 -> V^T [B, Hkv, d, nk_pad] (keys contiguous, zero past Nk), the
@@ -1713,16 +1788,16 @@ cudaError_t launch_prefill_pair(int mask, bool f16, const CUtensorMap &tq, const
 }
 
 cudaError_t launch_prefill(int d, int mask, bool f16, const CUtensorMap &tq,
-                           const CUtensorMap &tk, const CUtensorMap &tv, const PrefillArgs &a,
-                           int grid, cudaStream_t stream) {
+                           const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap *tmo,
+                           const PrefillArgs &a, int grid, cudaStream_t stream) {
   if (d == 64)
-    return f16 ? launch_mask<64, true>(mask, tq, tk, tv, a, grid, stream)
-               : launch_mask<64, false>(mask, tq, tk, tv, a, grid, stream);
+    return f16 ? launch_mask<64, true>(mask, tq, tk, tv, tmo, a, grid, stream)
+               : launch_mask<64, false>(mask, tq, tk, tv, tmo, a, grid, stream);
   if (d == 256)
-    return f16 ? launch_mask<256, true>(mask, tq, tk, tv, a, grid, stream)
-               : launch_mask<256, false>(mask, tq, tk, tv, a, grid, stream);
-  return f16 ? launch_mask<128, true>(mask, tq, tk, tv, a, grid, stream)
-             : launch_mask<128, false>(mask, tq, tk, tv, a, grid, stream);
+    return f16 ? launch_mask<256, true>(mask, tq, tk, tv, tmo, a, grid, stream)
+               : launch_mask<256, false>(mask, tq, tk, tv, tmo, a, grid, stream);
+  return f16 ? launch_mask<128, true>(mask, tq, tk, tv, tmo, a, grid, stream)
+             : launch_mask<128, false>(mask, tq, tk, tv, tmo, a, grid, stream);
 }
 
 cudaError_t launch_fill_empty(void *o, float *lse, int B, int N, int H, int d, int64_t o_sb,
