@@ -143,6 +143,46 @@ def test_varlen(case, causal):
     assert torch.all(o_buf[:4] == 3.0) and torch.all(o_buf[total_q + 4:] == 3.0)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_varlen_staged_and_direct_row_stores(d):
+    """Sequences of 31..223 rows: a softmax warp whose 32 rows all lie in its sequence
+    stages O in shared memory and writes it with TMA stores, the others store their rows
+    one by one.  Each sequence matches the oracle, and the rows around the output (and of
+    the neighbouring sequences) are untouched."""
+    sq = [31, 32, 33, 95, 96, 97, 160, 223]
+    Hq, Hkv = 4, 2
+    q, k, v, cu_q, cu_k = varlen_inputs(sq, sq, Hq, Hkv, d, seed=57 + d, device=DEV)
+    total_q = q.shape[0]
+    o_buf = torch.full((total_q + 8, Hq, d), 5.0, dtype=torch.bfloat16, device=DEV)
+    out = o_buf[4:total_q + 4]
+    o, lse = fa_fwd_varlen(q, k, v, cu_q, cu_k, max(sq), max(sq), causal=True, out=out)
+    assert get_last_device_error() == FA_OK
+    o_ref, lse_ref = ORACLE.attention_varlen(q.cpu(), k.cpu(), v.cpu(), cu_q.cpu(), cu_k.cpu(),
+                                             float(np.float32(1 / math.sqrt(d))), True)
+    compare(*varlen_rows(o, lse), *varlen_rows(o_ref, lse_ref), f"varlen staged d={d}")
+    assert torch.all(o_buf[:4] == 5.0) and torch.all(o_buf[total_q + 4:] == 5.0)
+
+
+@pytest.mark.parametrize("d", [40, 96])
+@pytest.mark.parametrize("causal", [False, True])
+def test_staged_stores_into_padded_view(d, causal):
+    """O as a view of a wider buffer (an extra head before it, columns past d, rows around
+    it): the staged TMA stores write d columns of the view's rows and heads only, for a
+    sub-tile whose last warp holds a partial row block (223 = 128 + 64 + 31 rows)."""
+    B, N, H = 2, 223, 3
+    q, k, v = dense_inputs(B, N, N, H, H, d, seed=61 + d, device=DEV)
+    dw = 64 if d <= 56 else 128
+    buf = torch.full((B, N + 16, H + 1, dw), 7.0, dtype=torch.bfloat16, device=DEV)
+    out = buf[:, 8:N + 8, 1:, :d]
+    o, lse = fa_fwd(q, k, v, causal=causal, out=out)
+    assert get_last_device_error() == FA_OK
+    o_ref, lse_ref = _oracle_dense(q, k, v, causal, float(np.float32(1 / math.sqrt(d))))
+    compare(*dense_rows(o, lse), *dense_rows(o_ref, lse_ref), f"padded view d={d}")
+    mask = torch.ones_like(buf, dtype=torch.bool)
+    mask[:, 8:N + 8, 1:, :d] = False
+    assert torch.all(buf[mask] == 7.0), "write outside the output view"
+
+
 def test_varlen_matches_dense():
     """A one-sequence varlen call equals the dense call bit for bit."""
     q, k, v = dense_inputs(1, 500, 500, 4, 2, 128, seed=41, device=DEV)
