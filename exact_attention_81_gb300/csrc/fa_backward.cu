@@ -1403,6 +1403,57 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t *o, const u
   }
 }
 
+// The same with 16-byte loads (O and dO rows 16-byte aligned): 2^lpr_log2 lanes per row,
+// 8 elements per lane and load, 32 >> lpr_log2 rows per warp at a time, the row's partial
+// sums reduced within its lane group.  Four bytes per lane and load left too few loads in
+// flight to stream O and dO at the copy rate.
+template <bool F16>
+__global__ void __launch_bounds__(256) bwd_pre_vec_kernel(const uint16_t *o, const uint16_t *dout,
+                                                          int B, int Nq, int Hq, int d,
+                                                          int64_t os0, int64_t os1, int64_t os2,
+                                                          int64_t ds0, int64_t ds1, int64_t ds2,
+                                                          float *dvec, float *dq_acc,
+                                                          int64_t acc_n, int *sem, int nsem,
+                                                          int lpr_log2) {
+  for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < nsem; t += gridDim.x * blockDim.x)
+    sem[t] = 0;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < acc_n / 4;
+       t += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    reinterpret_cast<float4 *>(dq_acc)[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int lane = threadIdx.x & 31;
+  const int lpr = 1 << lpr_log2;
+  const int sub = lane & (lpr - 1);
+  const int rpw = 32 >> lpr_log2;
+  const int64_t rows = static_cast<int64_t>(B) * Nq * Hq;
+  const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * blockDim.x / 32;
+  for (int64_t base = warp0 * rpw; base < rows; base += nwarps * rpw) {
+    const int64_t rw = base + (lane >> lpr_log2);
+    float acc = 0.f;
+    int b = 0, n = 0, h = 0;
+    if (rw < rows) {
+      h = static_cast<int>(rw % Hq);
+      const int64_t bn = rw / Hq;
+      n = static_cast<int>(bn % Nq);
+      b = static_cast<int>(bn / Nq);
+      const uint16_t *orow = o + b * os0 + n * os1 + h * os2;
+      const uint16_t *drow = dout + b * ds0 + n * ds1 + h * ds2;
+      for (int c = sub * 8; c < d; c += lpr * 8) {
+        const uint4 ov = *reinterpret_cast<const uint4 *>(orow + c);
+        const uint4 dv = *reinterpret_cast<const uint4 *>(drow + c);
+        const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w}, dw[4] = {dv.x, dv.y, dv.z, dv.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc = fmaf(lo_to_f32<F16>(ow[i]), lo_to_f32<F16>(dw[i]), acc);
+          acc = fmaf(hi_to_f32<F16>(ow[i]), hi_to_f32<F16>(dw[i]), acc);
+        }
+      }
+    }
+    for (int s2 = lpr >> 1; s2 > 0; s2 >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s2);
+    if (rw < rows && sub == 0) dvec[(static_cast<int64_t>(b) * Hq + h) * Nq + n] = acc;
+  }
+}
+
 // dQ = scale * accumulator, 8 elements per thread.
 template <bool F16>
 __global__ void __launch_bounds__(256) bwd_post_kernel(const float *acc, float scale, uint16_t *dq,
@@ -1572,6 +1623,18 @@ cudaError_t launch_bwd_pre(int d, bool f16, const void *o, const void *dout, int
   const int grid = grid_for(items > nsem ? items : nsem, 256);
   const uint16_t *op = reinterpret_cast<const uint16_t *>(o);
   const uint16_t *dp = reinterpret_cast<const uint16_t *>(dout);
+  const bool vec = reinterpret_cast<uintptr_t>(o) % 16 == 0 &&
+                   reinterpret_cast<uintptr_t>(dout) % 16 == 0 && d % 8 == 0 && d <= 256 &&
+                   o_st[0] % 8 == 0 && o_st[1] % 8 == 0 && o_st[2] % 8 == 0 &&
+                   do_st[0] % 8 == 0 && do_st[1] % 8 == 0 && do_st[2] % 8 == 0;
+  if (vec) {
+    int lpr_log2 = 0;
+    while ((8 << lpr_log2) < d) ++lpr_log2;  // lanes per row: d / 8 rounded up to a power of 2
+    auto vk = f16 ? bwd_pre_vec_kernel<true> : bwd_pre_vec_kernel<false>;
+    vk<<<grid, 256, 0, stream>>>(op, dp, B, Nq, Hq, d, o_st[0], o_st[1], o_st[2], do_st[0],
+                                 do_st[1], do_st[2], dvec, dq_acc, acc_n, sem, nsem, lpr_log2);
+    return cudaGetLastError();
+  }
   auto kern = f16 ? bwd_pre_kernel<true> : bwd_pre_kernel<false>;
   kern<<<grid, 256, 0, stream>>>(op, dp, B, Nq, Hq, d, o_st[0], o_st[1], o_st[2], do_st[0],
                                  do_st[1], do_st[2], dvec, dq_acc, acc_n, sem, nsem);
