@@ -17,7 +17,8 @@
 // reference max P and l share), and
 // the division by l deferred to the epilogue ("FlashAttention 1-4 详解", FlashAttention 2,
 // normalise once after the inner loop).  The epilogue writes O (bf16) and the natural-log
-// LSE = ln2 * (m + log2 l).  S and P never leave the SM.
+// LSE = ln2 * (m + log2 l); O goes through a per-warp shared-memory box and TMA stores where
+// shared memory allows (width <= 128, no ALiBi, single CTAs).  S and P never leave the SM.
 //
 // Warp roles (384 threads, three warpgroups):
 //   warps 0-3  softmax + correction + epilogue for sub-tile 0 (thread = query row)
@@ -45,7 +46,9 @@
 // dynamically: the producer lane of each CTA takes the next ticket from a per-launch
 // atomic counter and passes the tile to the other roles through a small shared-memory
 // ring.  CTAs that run at the same time therefore share a few heads' K/V in L2, long tiles
-// start early, and no CTA idles while another still holds several tiles.
+// start early, and no CTA idles while another still holds several tiles.  On taking a
+// ticket the producer prefetches the tile's Q and first K/V boxes into L2, about two steps
+// before the Q buffer is free for them.
 #include <atomic>
 #include <cmath>
 
