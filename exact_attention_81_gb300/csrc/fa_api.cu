@@ -308,9 +308,14 @@ void set_mod_fields(const ModPlan &m, float scale, Args *a) {
   a->alibi_sb = m.alibi_sb;
 }
 
+// (batch, head) pairs per group of the longest-first tile order (causal and right-bounded
+// windows).
+static int prefill_head_group() { return 8; }
+
 void apply_mod(const ModPlan &m, float scale, fa::PrefillArgs *pa) {
   set_mod_fields(m, scale, pa);
   pa->desc = m.wr >= 0;
+  pa->head_group = prefill_head_group();
   // ALiBi with a right-bounded window: the bias grows toward the last visible key, so the
   // K/V tiles run last-first and the row max is met on the first tile instead of moving
   // (and rescaling O) on every one.  Not with a softcap: there the reversed order measured

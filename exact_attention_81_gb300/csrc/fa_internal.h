@@ -51,6 +51,7 @@ struct PrefillArgs {
   const float *alibi;         // slopes of (b, h) at alibi[b * alibi_sb + h], or null
   int64_t alibi_sb;
   int desc;                   // hand out query blocks last-first (right-bounded windows)
+  int head_group;             // last-first order: (batch, head) pairs per group (<= 1: one)
   int kv_rev;                 // stream each block's K/V tiles last-first (ALiBi, right-bounded)
   // FP8 launches: descale factors per (batch, kv head) at [b * Hkv + hk], or null (= 1).
   const float *q_descale, *k_descale, *v_descale;

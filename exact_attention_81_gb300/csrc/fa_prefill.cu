@@ -42,11 +42,12 @@
 // tiles between its first row's window start and its last row's window end, each
 // sub-tile joins the stream steps its rows can see, and the scores are softcapped and
 // biased in the log2 domain before the row max.
-// Tiles are ordered head-major with the largest causal query blocks first and handed out
-// dynamically: the producer lane of each CTA takes the next ticket from a per-launch
-// atomic counter and passes the tile to the other roles through a small shared-memory
-// ring.  CTAs that run at the same time therefore share a few heads' K/V in L2, long tiles
-// start early, and no CTA idles while another still holds several tiles.  On taking a
+// Tiles are handed out dynamically: the producer lane of each CTA takes the next ticket
+// from a per-launch atomic counter and passes the tile to the other roles through a small
+// shared-memory ring.  Causal (and right-bounded window) tiles go out longest first within
+// groups of a few (batch, head) pairs, one query-block level at a time over the group, so
+// that CTAs running at the same time share a few heads' K/V in L2, long tiles start early,
+// and the launch ends on short tiles instead of one head's longest ones.  On taking a
 // ticket the producer prefetches the tile's Q and first K/V boxes into L2, about two steps
 // before the Q buffer is free for them.
 #include <atomic>
@@ -197,9 +198,24 @@ __device__ __forceinline__ TileInfo tile_info(const PrefillArgs &a, int ticket) 
     tile = a.half_from + (hh >> 1);
   }
   ti.half = half >= 0;
-  const int bh = tile / a.mblocks;
-  const int r = tile - bh * a.mblocks;
   const bool desc = MASK == MASK_CAUSAL || (mask_has_window(MASK) && a.desc);
+  int bh, r;
+  if (desc && a.head_group > 1) {
+    // Longest first across groups of head_group (batch, head) pairs: a group's tiles go
+    // out one query-block level at a time over all its pairs, so that the last tickets of
+    // the launch are short blocks of many heads (head by head, the last head's longest
+    // blocks started when little other work was left), while the CTAs running together
+    // still share a few heads' K/V in L2.
+    const int per = a.head_group * a.mblocks;
+    const int g = tile / per;
+    const int r2 = tile - g * per;
+    const int gs = min(a.head_group, a.num_tiles / a.mblocks - g * a.head_group);
+    r = r2 / gs;
+    bh = g * a.head_group + (r2 - r * gs);
+  } else {
+    bh = tile / a.mblocks;
+    r = tile - bh * a.mblocks;
+  }
   const int mb = desc ? (a.mblocks - 1 - r) : r;
   ti.b = bh / a.Hq;
   ti.h = bh - ti.b * a.Hq;
