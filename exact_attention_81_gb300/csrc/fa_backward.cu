@@ -12,10 +12,12 @@
 // and finally dK *= scale, dQ *= scale (a postprocessing kernel converts dQ).
 //
 // Work unit = (batch b, kv head g, 128-key block j), persistent CTAs taking units in order:
-// groups of 8 (b, g) pairs one after the other, key-block-major inside a group (with
-// causal masking the first key blocks see the most queries, so the longest units of a
-// group come first, and the group's dQ accumulators stay in L2; all heads key-block-major:
-// 706 TFLOPS, head-major: 663, groups of 8: 737).  A unit visits every
+// groups of BwdArgs::head_group (b, g) pairs one after the other (8; 16 for the
+// deterministic dQ order, whose CTAs wait on one another per pair; 4 at d > 128),
+// key-block-major inside a group (with causal masking the first key blocks see the most
+// queries, so the longest units of a group come first, and the group's dQ accumulators
+// stay in L2; all heads key-block-major: 706 TFLOPS, head-major: 663, groups of 8: 737,
+// measured on an earlier version of the kernel).  A unit visits every
 // 128-query block i of every query head of group g whose rows can see a key of block j.
 // Keys are the MMA rows (TMEM lanes) of S^T, dP^T, dV and dK, so the dK and dV
 // accumulators stay in TMEM across the unit.
